@@ -1,0 +1,435 @@
+"""Benchmark of the GB300 pre-norm SwiGLU FFN block.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = one ffn_block_forward of the prefill workload: 4096 tokens, d=4096,
+ffn=11008, bf16 storage with fp32 accumulation (RMSNorm -> tcgen05 gate/up
+GEMM with the SwiGLU epilogue -> tcgen05 down GEMM), on seeded synthetic
+inputs.  Rank 0 prints one JSON line.  The standalone RMSNorm and SwiGLU
+workloads, the bf16 decode block and the Q4 decode block are timed after it
+and reported under "sub".
+
+--impl reference times the float64 CPU oracle on the host cores on a bounded
+sample of the same workload (a few token rows per step).
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "FFN-block tokens/sec at 1 GB300; achieved HBM GB/s and tensor-pipe % of peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-sub", action="store_true", help="skip the secondary workloads")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU baseline")
+    return ap.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_uuid: str | None):
+        self.uuid = device_uuid
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                   "-lms", "50"]
+            if self.uuid:
+                cmd += ["-i", self.uuid]
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(cmd, stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+        return False
+
+    def summary(self, t0: float, t1: float):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                rows.append(parts)
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        reasons = set()
+        for r in rows:
+            for n, v in zip(names, r[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        # keep only the samples taken while the GPU was busy (the middle of the list)
+        busy = sm[2:-2] if len(sm) > 6 else sm
+        return {"sm_mhz": statistics.median(busy) if busy else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(busy)}
+
+
+# ------------------------------------------------------------- utilities
+def to_dev(a, dtype, torch, device):
+    if dtype == "bf16":
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(device).view(torch.bfloat16)
+    return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+
+
+def timed_loop(torch, fn, steps, warmup, stream):
+    for i in range(warmup):
+        fn(i)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(steps):
+        fn(i)
+    e1.record(stream)
+    e1.synchronize()
+    return e0.elapsed_time(e1)
+
+
+def kernel_table(res):
+    return {k: {"launches": n, "avg_us": round(1000.0 * ms / n, 3)} for k, (n, ms) in res.items()}
+
+
+# --------------------------------------------------------- secondary workloads
+def sub_benchmarks(torch, ffn, device, peaks, peak_src, stream):
+    out = []
+    hbm = peaks["hbm_gbs"]
+    iters, warm = 50, 5
+
+    # RMSNorm 16384 x 4096 fp16
+    inp = synth.make_norm_inputs(synth.C2A_RMSNORM_F16, seed=0)
+    x = [to_dev(inp["x"], "f16", torch, device) for _ in range(2)]
+    g = to_dev(inp["g"], "f16", torch, device)
+    n = [torch.empty_like(x[0]) for _ in range(2)]
+    with ffn.KernelTimer() as kt:
+        ms = timed_loop(torch, lambda i: ffn.ffn_rmsnorm(x[i % 2], g, 1e-5, out=n[i % 2]), iters, warm, stream)
+        res = kt.read()
+    byts = 2 * 16384 * 4096 * 2 + 4096 * 2
+    cnt, tot = res["rmsnorm"]
+    kus = 1000.0 * tot / cnt
+    out.append({"workload": synth.C2A_RMSNORM_F16.name, "us_per_call": round(1000 * ms / iters, 3),
+                "kernel": "rmsnorm", "kernel_avg_us": round(kus, 3),
+                "roofline": {"bound": "hbm", "achieved": round(byts / kus / 1e3, 1), "peak": hbm,
+                             "unit": "GB/s", "frac": round(byts / kus / 1e3 / hbm, 4),
+                             "peak_source": peak_src + " hbm_gbs (copy, burst)", "algorithmic_bytes": byts}})
+    del x, n
+
+    # SwiGLU two 16384 x 11008 fp16
+    inp = synth.make_swiglu_inputs(synth.C2B_SWIGLU_F16, seed=0)
+    ga = to_dev(inp["gate"], "f16", torch, device)
+    up = to_dev(inp["up"], "f16", torch, device)
+    h = torch.empty_like(ga)
+    with ffn.KernelTimer() as kt:
+        ms = timed_loop(torch, lambda i: ffn.ffn_swiglu(ga, up, out=h), iters, warm, stream)
+        res = kt.read()
+    byts = 3 * 16384 * 11008 * 2
+    cnt, tot = res["swiglu"]
+    kus = 1000.0 * tot / cnt
+    out.append({"workload": synth.C2B_SWIGLU_F16.name, "us_per_call": round(1000 * ms / iters, 3),
+                "kernel": "swiglu", "kernel_avg_us": round(kus, 3),
+                "roofline": {"bound": "hbm", "achieved": round(byts / kus / 1e3, 1), "peak": hbm,
+                             "unit": "GB/s", "frac": round(byts / kus / 1e3 / hbm, 4),
+                             "peak_source": peak_src + " hbm_gbs (copy, burst)", "algorithmic_bytes": byts}})
+    del ga, up, h
+
+    # decode bf16 8 x 4096 x 14336
+    cfg = synth.C3_DECODE_BF16
+    inp = synth.make_block_inputs(cfg, seed=0)
+    args = [to_dev(inp[k], "bf16", torch, device) for k in ("x", "g", "w_gate", "w_up", "w_down")]
+    y = torch.empty_like(args[0])
+    ws = ffn.workspace(ffn.ffn_block_workspace_bytes(cfg.rows, cfg.d, cfg.ffn, torch.bfloat16), device)
+    with ffn.KernelTimer() as kt:
+        ms = timed_loop(torch, lambda i: ffn.ffn_block_forward(*args, eps=cfg.eps, out=y, ws=ws), iters, warm, stream)
+        res = kt.read()
+    wbytes = 3 * cfg.ffn * cfg.d * 2
+    gu = res["gemv_gateup"]
+    gu_us = 1000.0 * gu[1] / gu[0]
+    gu_bytes = 2 * cfg.ffn * cfg.d * 2
+    us = 1000 * ms / iters
+    out.append({"workload": cfg.name, "us_per_call": round(us, 3), "tokens_per_s": round(cfg.rows / us * 1e6, 1),
+                "block_weight_GBps": round(wbytes / us / 1e3, 1), "kernels": kernel_table(res),
+                "roofline": {"bound": "hbm", "kernel": "gemv_gateup", "achieved": round(gu_bytes / gu_us / 1e3, 1),
+                             "peak": hbm, "unit": "GB/s", "frac": round(gu_bytes / gu_us / 1e3 / hbm, 4),
+                             "peak_source": peak_src + " hbm_gbs (copy, burst)", "algorithmic_bytes": gu_bytes}})
+    del args, y, ws
+
+    # Q4 decode 8 x 5120 x 17408, two weight copies rotated (2 x 150 MB > L2)
+    cfg = synth.C5_DECODE_Q4
+    inp = synth.make_q4_inputs(cfg, seed=0)
+    xq = to_dev(inp["x"], "bf16", torch, device)
+    gq = to_dev(inp["g"], "bf16", torch, device)
+    wsets = []
+    for _ in range(2):
+        wsets.append([(torch.from_numpy(inp["qs_" + n]).to(device),
+                       torch.from_numpy(inp["sc_" + n].view(np.int16)).to(device)) for n in ("gate", "up", "down")])
+    yq = torch.empty_like(xq)
+    ws = ffn.workspace(ffn.ffn_block_q4_workspace_bytes(cfg.rows, cfg.d, cfg.ffn), device)
+    with ffn.KernelTimer() as kt:
+        ms = timed_loop(torch, lambda i: ffn.ffn_block_forward_q4(xq, gq, *wsets[i % 2], ffn=cfg.ffn, eps=cfg.eps,
+                                                                  out=yq, ws=ws), iters, warm, stream)
+        res = kt.read()
+    wbytes = 3 * cfg.ffn * cfg.d * 18 // 32
+    gu = res["gemv_gateup"]
+    gu_us = 1000.0 * gu[1] / gu[0]
+    gu_bytes = 2 * cfg.ffn * cfg.d * 18 // 32
+    us = 1000 * ms / iters
+    out.append({"workload": cfg.name, "us_per_call": round(us, 3), "tokens_per_s": round(cfg.rows / us * 1e6, 1),
+                "block_weight_GBps": round(wbytes / us / 1e3, 1), "kernels": kernel_table(res),
+                "l2": "two weight copies rotated",
+                "roofline": {"bound": "hbm", "kernel": "gemv_gateup", "achieved": round(gu_bytes / gu_us / 1e3, 1),
+                             "peak": hbm, "unit": "GB/s", "frac": round(gu_bytes / gu_us / 1e3 / hbm, 4),
+                             "peak_source": peak_src + " hbm_gbs (copy, burst)", "algorithmic_bytes": gu_bytes}})
+    return out
+
+
+# ----------------------------------------------------------- CPU baseline
+def cpu_oracle_rate(inp, rows_per_step: int, steps: int, warmup: int = 0, seed: int = 0):
+    """tokens/s of the float64 oracle on `rows_per_step` sampled token rows per step."""
+    import oracle
+    o = oracle.get()
+    dt = inp["cfg"].dtype
+    g = oracle.widen(inp["g"], dt)
+    wg, wu, wd = (oracle.widen(inp[k], dt) for k in ("w_gate", "w_up", "w_down"))
+    rng = np.random.default_rng(seed)
+    M = inp["cfg"].rows
+    threads = oracle.default_threads()
+    for _ in range(warmup):
+        r = rng.integers(0, M, rows_per_step)
+        o.ffn_block(oracle.widen(inp["x"][r], dt), g, wg, wu, wd, inp["cfg"].eps, threads)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        r = rng.integers(0, M, rows_per_step)
+        o.ffn_block(oracle.widen(inp["x"][r], dt), g, wg, wu, wd, inp["cfg"].eps, threads)
+    dt_s = time.perf_counter() - t0
+    return rows_per_step * steps / dt_s, dt_s, threads
+
+
+# ------------------------------------------------------------------- main
+def dist_init():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_reference(args):
+    world, rank, _ = dist_init()
+    if rank != 0:
+        return
+    cfg = synth.C4_PREFILL_BF16
+    inp = synth.make_block_inputs(cfg, seed=0)
+    rows_per_step = 4
+    rate, secs, threads = cpu_oracle_rate(inp, rows_per_step, args.steps, args.warmup)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(rate, 3), "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1000 * secs / max(1, args.steps), 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic, seeded (numpy PCG64, seed 0)",
+        "config": {"workload": cfg.name, "rows": cfg.rows, "d": cfg.d, "ffn": cfg.ffn, "eps": cfg.eps,
+                   "storage": "bf16", "parallelism": "replicas"},
+        "cpu_baseline": {"value": round(rate, 3), "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{rows_per_step} random token rows of the {cfg.rows}-row batch per step"},
+        "e2e": {"value": round(rate, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    import torch
+    world, rank, local = dist_init()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    from transformer_ffn_rmsnorm_gb300 import ffn
+
+    peaks, peak_src = load_peaks()
+    cfg = synth.C4_PREFILL_BF16
+    inp = synth.make_block_inputs(cfg, seed=rank)
+    x, g, wg, wu, wd = (to_dev(inp[k], "bf16", torch, device) for k in ("x", "g", "w_gate", "w_up", "w_down"))
+    y = torch.empty_like(x)
+    ws = ffn.workspace(ffn.ffn_block_workspace_bytes(cfg.rows, cfg.d, cfg.ffn, torch.bfloat16), device)
+    stream = torch.cuda.current_stream()
+
+    def step(_i):
+        ffn.ffn_block_forward(x, g, wg, wu, wd, eps=cfg.eps, out=y, ws=ws)
+
+    for _ in range(args.warmup):
+        step(0)
+    torch.cuda.synchronize()
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
+    except Exception:
+        pass
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    launches0 = ffn.ffn_launch_count()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(uuid) as clk, ffn.KernelTimer() as kt:
+        barrier()
+        torch.cuda.synchronize()
+        t0 = time.time()
+        e0.record(stream)
+        for i in range(args.steps):
+            step(i)
+        e1.record(stream)
+        e1.synchronize()
+        barrier()
+        torch.cuda.synchronize()
+        t1 = time.time()
+        res = kt.read()
+    launches = ffn.ffn_launch_count() - launches0
+    ms = e0.elapsed_time(e1)
+    clocks = clk.summary(t0, t1)
+    if world > 1:
+        t = torch.tensor([ms], device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+
+    tokens = cfg.rows * args.steps * world
+    value = tokens / (ms / 1000.0)
+    flops_gu = 2.0 * cfg.rows * cfg.d * (2 * cfg.ffn)
+    n_gu, ms_gu = res["gemm_gateup"]
+    gu_avg_s = ms_gu / n_gu / 1000.0
+    peak_t = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    achieved_t = flops_gu / gu_avg_s / 1e12
+    roof = {"bound": "tensor", "kernel": "gemm_gateup", "achieved": round(achieved_t, 1), "peak": peak_t,
+            "unit": "TFLOP/s", "frac": round(achieved_t / peak_t, 4),
+            "peak_source": f"{peak_src} bf16_tflops_sustained (cuBLAS, seconds-long loop)",
+            "algorithmic_flops_per_launch": flops_gu, "traffic": None}
+    n_dn, ms_dn = res["gemm_down"]
+    flops_dn = 2.0 * cfg.rows * cfg.ffn * cfg.d
+    extra = {"gemm_down_TFLOPs": round(flops_dn / (ms_dn / n_dn / 1000.0) / 1e12, 1),
+             "block_TFLOPs": round((flops_gu + flops_dn) / (ms / args.steps / 1000.0) / 1e12, 1)}
+
+    # end to end: pinned host x -> device -> block -> pinned host y, per step
+    xh = x.cpu().pin_memory()
+    yh = torch.empty_like(xh).pin_memory()
+
+    def e2e_step(_i):
+        x.copy_(xh, non_blocking=True)
+        ffn.ffn_block_forward(x, g, wg, wu, wd, eps=cfg.eps, out=y, ws=ws)
+        yh.copy_(y, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 200))
+    e2e_ms = timed_loop(torch, e2e_step, e2e_steps, 3, stream)
+    e2e_val = cfg.rows * e2e_steps * world / (e2e_ms / 1000.0)
+
+    sub = []
+    if not args.no_sub and rank == 0:
+        del xh, yh
+        sub = sub_benchmarks(torch, ffn, device, peaks, peak_src, stream)
+
+    cpu = None
+    if not args.no_cpu and rank == 0:
+        rows_sample = 32
+        rate, secs, threads = cpu_oracle_rate(inp, rows_sample, 2, 0)
+        cpu = {"value": round(rate, 3), "unit": "tokens/s", "cores": threads, "kind": "oracle",
+               "sample": f"2 x {rows_sample} random token rows of the {cfg.rows}-row batch ({secs:.1f} s wall)"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic, seeded (numpy PCG64, seed = rank): x~N(0,1), g=1+0.1N(0,1), W~N(0,1/fan_in)",
+            "config": {"workload": cfg.name, "rows": cfg.rows, "d": cfg.d, "ffn": cfg.ffn, "eps": cfg.eps,
+                       "storage": "bf16", "accumulate": "fp32", "gateup_epilogue": "fused",
+                       "parallelism": "replicas" if world > 1 else "single",
+                       "l2": "inputs larger than L2 (weights 270.5 MB + x 33.5 MB + n/h 124 MB per step)"},
+            "roofline": roof, "extra": extra,
+            "kernels": kernel_table(res), "gpu_launches": launches,
+            "clocks": clocks,
+            "e2e": {"value": round(e2e_val, 1), "unit": "tokens/s",
+                    "h2d_bytes_per_step": cfg.rows * cfg.d * 2, "d2h_bytes_per_step": cfg.rows * cfg.d * 2},
+            "cpu_baseline": cpu, "sub": sub,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.steps < 1 or args.warmup < 0:
+        raise SystemExit("--steps must be >= 1 and --warmup >= 0")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,185 @@
+/*
+ * ffn.h -- C ABI of the GB300 (sm_103a) pre-norm SwiGLU feed-forward block.
+ *
+ *   n = RMSNorm(x) = x * rsqrt(mean(x^2) + eps) * g
+ *   y = W_down * ( silu(W_gate * n) (*) (W_up * n) ),   silu(z) = z / (1 + e^-z)
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Tensor pointers are DEVICE pointers owned by the caller.  The library never
+ *   allocates, frees or synchronises device memory (ffn_device_status and
+ *   ffn_timing_collect are the only calls that synchronise).
+ * - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *   stream).  Every buffer must stay alive and unmodified until the stream has
+ *   passed the call: the library does not track buffer lifetimes ("How
+ *   Megakernels Work", section "Dependencies and synchronization": buffers may
+ *   not be released while submitted work can still read them).
+ * - Row-major layouts.  Activations are [rows x d]; weights are [out x in] with
+ *   the input (reduction) dimension contiguous.
+ * - All arithmetic is fp32 on fp32/fp16/bf16 storage; every stored output is
+ *   rounded once, round-to-nearest-even, to the storage type.
+ * - Arguments are validated on the host before any launch.  A violation
+ *   returns an error status and launches nothing.  rows == 0 (an empty batch)
+ *   is valid and launches nothing.  Pointers must be 16-byte aligned.
+ * - After launching, a failed launch is reported as FFN_ERR_CUDA.  A kernel
+ *   that gives up a bounded wait records FFN_ERR_TIMEOUT in a device status
+ *   word that ffn_device_status() reads; no C++ exception crosses this ABI.
+ * - A workspace must not be shared by calls that may run concurrently.
+ */
+#ifndef FFN_GB300_H
+#define FFN_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FFN_OK = 0,
+    FFN_ERR_NULL = 1,       /* a required pointer is NULL                          */
+    FFN_ERR_SHAPE = 2,      /* a size is out of range or breaks a divisibility rule */
+    FFN_ERR_DTYPE = 3,      /* unknown or unsupported storage type                 */
+    FFN_ERR_ALIGN = 4,      /* a pointer is not 16-byte aligned                    */
+    FFN_ERR_WORKSPACE = 5,  /* workspace NULL or smaller than the query returned   */
+    FFN_ERR_ALIAS = 6,      /* an output overlaps an input it may not overlap      */
+    FFN_ERR_CUDA = 7,       /* a CUDA runtime call failed                          */
+    FFN_ERR_TIMEOUT = 8,    /* a kernel abandoned a bounded wait                   */
+    FFN_ERR_FLAGS = 9       /* contradictory or unknown flag bits                  */
+} ffn_status;
+
+typedef enum { FFN_F32 = 0, FFN_F16 = 1, FFN_BF16 = 2 } ffn_dtype;
+
+/* flags for ffn_block_forward / ffn_block_forward_q4 */
+#define FFN_AUTO 0u
+/* tensor-core path: silu(G)*U computed in the gate/up GEMM epilogue (default) */
+#define FFN_GATEUP_FUSED 1u
+/* tensor-core path: the gate/up GEMM stores G and U; a separate SwiGLU pass
+ * reads them back ("Unfusing a Kernel Made It 1.63x Faster", Finding 1)     */
+#define FFN_GATEUP_UNFUSED 2u
+/* force the tcgen05 tensor-core GEMM path (16-bit dtypes, any rows)          */
+#define FFN_PATH_GEMM 4u
+/* force the weight-streaming decode path (16-bit dtypes, rows <= 16)         */
+#define FFN_PATH_GEMV 8u
+
+/* ------------------------------------------------------------------------
+ * ffn_rmsnorm -- n[r,c] = x[r,c] * rsqrt(ms_r + eps) * g[c],
+ *                ms_r = (1/d) sum_c x[r,c]^2 accumulated in fp32.
+ * "When to hand-write a GPU kernel on Apple Silicon", Rung 2 (row reduction,
+ * then the reciprocal root of mean + eps) and Rung 4 (wide loads, a warp
+ * reduction, then a small cross-warp combine).
+ *   x [rows x d], g [d], n [rows x d], all of `dtype`.  n may equal x (in
+ *   place); any other overlap is FFN_ERR_ALIAS.  rows >= 0, d >= 1.
+ * ---------------------------------------------------------------------- */
+ffn_status ffn_rmsnorm(const void *x, const void *g, void *n, int64_t rows, int64_t d,
+                       float eps, ffn_dtype dtype, void *stream);
+
+/* ------------------------------------------------------------------------
+ * ffn_swiglu -- h[i] = silu(gate[i]) * up[i], silu in fp32.
+ * "When to hand-write a GPU kernel on Apple Silicon", Rung 1 (one pass,
+ * activation upcast to fp32).
+ *   gate, up, h: `count` elements of `dtype`.  h may equal gate or up (in
+ *   place); any other overlap is FFN_ERR_ALIAS.  count >= 0.
+ * ---------------------------------------------------------------------- */
+ffn_status ffn_swiglu(const void *gate, const void *up, void *h, int64_t count,
+                      ffn_dtype dtype, void *stream);
+
+/* ------------------------------------------------------------------------
+ * ffn_block_workspace_bytes -- device scratch bytes ffn_block_forward needs
+ * for these sizes, dtype and flags (the same path choice the forward call
+ * makes).  Host-only; writes *bytes.  Shape errors as in ffn_block_forward.
+ * ---------------------------------------------------------------------- */
+ffn_status ffn_block_workspace_bytes(int64_t rows, int64_t d, int64_t ffn, ffn_dtype dtype,
+                                     uint32_t flags, size_t *bytes);
+
+/* ------------------------------------------------------------------------
+ * ffn_block_forward -- y = W_down (silu(W_gate n) * (W_up n)), n = RMSNorm(x).
+ * "Unfusing a Kernel Made It 1.63x Faster", Finding 1 (gate and up
+ * projections, then the activation, then the down projection) with the norm
+ * of "When to hand-write a GPU kernel on Apple Silicon", Rung 2.
+ *   x [rows x d], g [d], w_gate and w_up [ffn x d], w_down [d x ffn],
+ *   y [rows x d]; all of `dtype`.  y must not overlap any input.
+ *   Paths: FFN_F32 -> fp32 SIMT FFMA kernels (any rows).  FFN_F16/FFN_BF16 ->
+ *   rows <= 16: weight-streaming decode kernels; otherwise tcgen05/TMEM GEMMs
+ *   fed by TMA.  Rules: d, ffn >= 1; 16-bit dtypes need d % 8 == 0 and
+ *   ffn % 8 == 0; fp32 needs d % 4 == 0 and ffn % 4 == 0.
+ *   workspace: at least ffn_block_workspace_bytes(...) bytes, 16-byte aligned.
+ *   Intermediates (n, h, split-K partials) round to `dtype` where they feed
+ *   a tensor-core operand and stay fp32 otherwise.
+ * ---------------------------------------------------------------------- */
+ffn_status ffn_block_forward(const void *x, const void *g, const void *w_gate, const void *w_up,
+                             const void *w_down, void *y, int64_t rows, int64_t d, int64_t ffn,
+                             float eps, ffn_dtype dtype, uint32_t flags, void *workspace,
+                             size_t workspace_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Q4 weights ("Unfusing a Kernel Made It 1.63x Faster", section "The finding
+ * that keeps us honest about microbenchmarks": 18-byte blocks of 32 weights,
+ * 16 bytes of nibbles plus a half-precision scale, repacked so each block is
+ * read once and coalesced).
+ *   Canonical block: weight j (0..31) is q_j in [-8, 7] stored offset-binary
+ *   u_j = q_j + 8; canonical byte i (0..15) holds u_i in the low nibble and
+ *   u_(i+16) in the high nibble; the weight is w_j = (u_j - 8) * s.
+ *   Device layout of qs: each weight row holds in/2 bytes; blocks go four at a
+ *   time along the input dimension (128 weights, 64 bytes per group); byte
+ *   16*t + 4*b + e of a group is canonical byte 4*t + e of block b of the group
+ *   (t, b, e in 0..3).  scales: [out][in/32] IEEE fp16 bit patterns.
+ *   Both arrays are device pointers (16-byte aligned) owned by the caller.
+ * ---------------------------------------------------------------------- */
+typedef struct {
+    const uint8_t *qs;
+    const uint16_t *scales;
+} ffn_q4_weight;
+
+ffn_status ffn_block_q4_workspace_bytes(int64_t rows, int64_t d, int64_t ffn, size_t *bytes);
+
+/* ------------------------------------------------------------------------
+ * ffn_block_forward_q4 -- the block with Q4 weights, dequantised in registers.
+ * "How Megakernels Work", section "Threadgroup staging" (stream Q4 weights
+ * to registers; staging through shared memory lost).
+ *   x [rows x d] bf16, g [d] bf16, y [rows x d] bf16; w_gate/w_up are Q4
+ *   [ffn x d], w_down is Q4 [d x ffn].  Needs d % 128 == 0, ffn % 128 == 0,
+ *   d <= 12288.  Rows are processed in groups of up to 16; each group streams
+ *   the weights once.  flags must be FFN_AUTO.
+ * ---------------------------------------------------------------------- */
+ffn_status ffn_block_forward_q4(const void *x, const void *g, ffn_q4_weight w_gate,
+                                ffn_q4_weight w_up, ffn_q4_weight w_down, void *y, int64_t rows,
+                                int64_t d, int64_t ffn, float eps, uint32_t flags, void *workspace,
+                                size_t workspace_bytes, void *stream);
+
+/* Host helper (not on the hot path): pack int8 q [out x in] (values -8..7) and
+ * fp16 scale bits [out x in/32] into the device layout above.  Host pointers;
+ * qs_out holds out*in/2 bytes, scales_out out*in/32 entries.  in % 128 == 0. */
+ffn_status ffn_q4_pack_host(const int8_t *q, const uint16_t *scales, int64_t out, int64_t in,
+                            uint8_t *qs_out, uint16_t *scales_out);
+
+/* Text for a status code (static storage). */
+const char *ffn_status_string(ffn_status status);
+
+/* Synchronises the current device, then returns and clears the device status
+ * word: FFN_OK, or FFN_ERR_TIMEOUT if a kernel abandoned a bounded wait since
+ * the last call, or FFN_ERR_CUDA if the synchronisation itself failed. */
+ffn_status ffn_device_status(void);
+
+/* Number of kernels this library has launched since it was loaded (host count). */
+uint64_t ffn_launch_count(void);
+
+/* ------------------------------------------------------------------------
+ * Measurement hooks.  With timing on, every launch is bracketed by CUDA events
+ * recorded on its own stream.  ffn_timing_collect() synchronises the pending
+ * events and adds their durations to per-kernel totals; ffn_timing_read()
+ * returns the totals for kernel kind `kind` (0 <= kind < ffn_kernel_kinds()).
+ * ---------------------------------------------------------------------- */
+ffn_status ffn_timing_enable(int on);
+ffn_status ffn_timing_collect(void);
+ffn_status ffn_timing_reset(void);
+int ffn_kernel_kinds(void);
+const char *ffn_kernel_name(int kind);
+ffn_status ffn_timing_read(int kind, uint64_t *launches, double *total_ms);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FFN_GB300_H */

@@ -1,0 +1,132 @@
+"""The C ABI on the host (CPU only): the library loads, exports every symbol
+include/ffn.h declares, and rejects bad arguments before touching CUDA."""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import synth
+from transformer_ffn_rmsnorm_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ffn.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = set(re.findall(r"\b(ffn_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return _lib.load()
+
+
+def test_header_declares_the_four_entry_points():
+    names = declared_functions()
+    for n in ("ffn_rmsnorm", "ffn_swiglu", "ffn_block_forward", "ffn_block_forward_q4"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert name in _lib.SIGNATURES, f"binding lacks a signature for {name}"
+
+
+def test_status_strings(lib):
+    for code in range(10):
+        s = lib.ffn_status_string(code).decode()
+        assert s and s != "unknown status"
+    assert lib.ffn_status_string(99).decode() == "unknown status"
+
+
+def test_null_and_shape_errors_without_gpu(lib):
+    p = ctypes.c_void_p(4096)  # never dereferenced: validation fails first
+    assert lib.ffn_rmsnorm(None, p, p, 1, 8, 1e-5, _lib.FFN_BF16, None) == _lib.FFN_ERR_NULL
+    assert lib.ffn_rmsnorm(p, p, ctypes.c_void_p(8192), -1, 8, 1e-5, _lib.FFN_BF16, None) == _lib.FFN_ERR_SHAPE
+    assert lib.ffn_rmsnorm(p, p, ctypes.c_void_p(8192), 1, 0, 1e-5, _lib.FFN_BF16, None) == _lib.FFN_ERR_SHAPE
+    assert lib.ffn_rmsnorm(p, p, ctypes.c_void_p(8192), 1, 8, 1e-5, 7, None) == _lib.FFN_ERR_DTYPE
+    assert lib.ffn_rmsnorm(ctypes.c_void_p(4098), p, ctypes.c_void_p(8192), 1, 8, 1e-5, _lib.FFN_BF16,
+                           None) == _lib.FFN_ERR_ALIGN
+    assert lib.ffn_swiglu(p, None, p, 4, _lib.FFN_F16, None) == _lib.FFN_ERR_NULL
+    assert lib.ffn_swiglu(p, p, p, -4, _lib.FFN_F16, None) == _lib.FFN_ERR_SHAPE
+    # h overlapping gate at an offset (not in place) is rejected
+    assert lib.ffn_swiglu(ctypes.c_void_p(4096), ctypes.c_void_p(1 << 20), ctypes.c_void_p(4096 + 16),
+                          64, _lib.FFN_F16, None) == _lib.FFN_ERR_ALIAS
+    # empty inputs are valid and launch nothing
+    assert lib.ffn_rmsnorm(p, ctypes.c_void_p(1 << 20), ctypes.c_void_p(1 << 21), 0, 8, 1e-5,
+                           _lib.FFN_BF16, None) == _lib.FFN_OK
+    assert lib.ffn_swiglu(p, ctypes.c_void_p(1 << 20), ctypes.c_void_p(1 << 21), 0, _lib.FFN_F16,
+                          None) == _lib.FFN_OK
+
+
+def _ws(lib, rows, d, ffn, dt, flags=0):
+    out = ctypes.c_size_t(0)
+    st = lib.ffn_block_workspace_bytes(rows, d, ffn, dt, flags, ctypes.byref(out))
+    return st, out.value
+
+
+def test_workspace_query(lib):
+    st, n = _ws(lib, 8, 4096, 14336, _lib.FFN_BF16)
+    assert st == 0 and n > 0
+    st, n2 = _ws(lib, 4096, 4096, 11008, _lib.FFN_BF16)
+    assert st == 0 and n2 >= 4096 * (4096 + 11008) * 2
+    st, n3 = _ws(lib, 4096, 4096, 11008, _lib.FFN_BF16, _lib.FFN_GATEUP_UNFUSED)
+    assert st == 0 and n3 >= n2 + 2 * 4096 * 11008 * 2
+    assert _ws(lib, 0, 4096, 11008, _lib.FFN_BF16) == (0, 0)
+    assert _ws(lib, 4, 4100, 11008, _lib.FFN_BF16)[0] == _lib.FFN_ERR_SHAPE       # d % 8
+    assert _ws(lib, 4, 4096, 11008, _lib.FFN_F32, _lib.FFN_PATH_GEMM)[0] == _lib.FFN_ERR_FLAGS
+    assert _ws(lib, 4, 4096, 11008, _lib.FFN_BF16, 3)[0] == _lib.FFN_ERR_FLAGS      # fused+unfused
+    assert _ws(lib, 4, 4096, 11008, _lib.FFN_BF16, 1 << 20)[0] == _lib.FFN_ERR_FLAGS
+    assert _ws(lib, 17, 4096, 11008, _lib.FFN_BF16, _lib.FFN_PATH_GEMV)[0] == _lib.FFN_ERR_SHAPE
+    out = ctypes.c_size_t(0)
+    assert lib.ffn_block_q4_workspace_bytes(8, 5120, 17408, ctypes.byref(out)) == 0 and out.value > 0
+    assert lib.ffn_block_q4_workspace_bytes(8, 5000, 17408, ctypes.byref(out)) == _lib.FFN_ERR_SHAPE
+
+
+def test_block_forward_rejects_before_launch(lib):
+    p = [ctypes.c_void_p((i + 1) << 24) for i in range(8)]
+    # workspace too small
+    assert lib.ffn_block_forward(*p[:6], 8, 4096, 14336, 1e-5, _lib.FFN_BF16, 0, p[6], 16,
+                                 None) == _lib.FFN_ERR_WORKSPACE
+    # y aliases x
+    st, need = _ws(lib, 8, 64, 128, _lib.FFN_BF16)
+    assert lib.ffn_block_forward(p[0], p[1], p[2], p[3], p[4], p[0], 8, 64, 128, 1e-5, _lib.FFN_BF16,
+                                 0, p[6], need, None) == _lib.FFN_ERR_ALIAS
+    # misaligned weight
+    assert lib.ffn_block_forward(p[0], p[1], ctypes.c_void_p((3 << 24) + 8), p[3], p[4], p[5], 8, 64,
+                                 128, 1e-5, _lib.FFN_BF16, 0, p[6], need, None) == _lib.FFN_ERR_ALIGN
+    q = _lib.Q4Weight(p[2].value, p[3].value)
+    assert lib.ffn_block_forward_q4(p[0], p[1], q, q, q, p[5], 8, 512, 1024, 1e-6, 1, p[6], 1 << 30,
+                                    None) == _lib.FFN_ERR_FLAGS
+
+
+def test_q4_pack_host_matches_layout(lib):
+    from transformer_ffn_rmsnorm_gb300 import ffn
+    inp = synth.make_q4_inputs(synth.C5_DECODE_Q4, seed=4, rows=1, d=256, ffn=384)
+    qs, sc = ffn.ffn_q4_pack_host(inp["q_gate"], inp["s_gate"].view(np.uint16))
+    assert np.array_equal(qs, inp["qs_gate"])
+    assert np.array_equal(sc, inp["sc_gate"])
+    bad = inp["q_gate"].copy()
+    bad[0, 0] = 8
+    with pytest.raises(Exception):
+        ffn.ffn_q4_pack_host(bad, inp["s_gate"].view(np.uint16))
+
+
+def test_launch_counter_starts_quiet(lib):
+    before = lib.ffn_launch_count()
+    p = ctypes.c_void_p(4096)
+    lib.ffn_rmsnorm(None, p, p, 1, 8, 1e-5, _lib.FFN_BF16, None)
+    assert lib.ffn_launch_count() == before   # rejected calls launch nothing
+
+
+def test_kernel_names(lib):
+    n = lib.ffn_kernel_kinds()
+    names = [lib.ffn_kernel_name(k).decode() for k in range(n)]
+    assert "gemm_gateup" in names and "rmsnorm" in names and len(set(names)) == n

@@ -1,0 +1,145 @@
+"""ffn_block_forward on the GPU against the float64 oracle: the fp32 SIMT path,
+the weight-streaming decode path and the tcgen05 prefill path."""
+
+import hashlib
+
+import numpy as np
+import pytest
+
+import synth
+from gpu_util import assert_dtype, assert_f32, assert_lowp, to_dev, to_host64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ffn():
+    from transformer_ffn_rmsnorm_gb300 import ffn as m
+    return m
+
+
+def run_block(ffn, inp, flags=0):
+    dt = inp["cfg"].dtype
+    args = [to_dev(inp[k], dt) for k in ("x", "g", "w_gate", "w_up", "w_down")]
+    y = ffn.ffn_block_forward(*args, eps=inp["cfg"].eps, flags=flags)
+    return y
+
+
+def test_tiny_fp32_block(ffn, oracle_lib):
+    """64 rows, d=256, ffn=704, fp32: within 1e-4 * rms of the oracle."""
+    inp = synth.make_block_inputs(synth.C1_TINY_F32, seed=0)
+    y = run_block(ffn, inp)
+    assert_f32(to_host64(y), oracle_lib.block_from_inputs(inp))
+
+
+@pytest.mark.parametrize("rows,d,ffn_", [(1, 4, 4), (3, 36, 20), (70, 260, 132), (129, 512, 300)])
+def test_fp32_block_ragged(ffn, oracle_lib, rows, d, ffn_):
+    inp = synth.make_block_inputs(synth.C1_TINY_F32, seed=rows, rows=rows, d=d, ffn=ffn_)
+    assert_f32(to_host64(run_block(ffn, inp)), oracle_lib.block_from_inputs(inp))
+
+
+def test_decode_bf16_full_size(ffn, oracle_lib):
+    """8 rows, d=4096, ffn=14336, bf16: the decode workload at full size."""
+    inp = synth.make_block_inputs(synth.C3_DECODE_BF16, seed=0)
+    y = run_block(ffn, inp)
+    assert_lowp(to_host64(y), oracle_lib.block_from_inputs(inp))
+
+
+@pytest.mark.parametrize("rows", [1, 2, 5, 8, 9, 12, 16])
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_decode_rows(ffn, oracle_lib, rows, dtype):
+    cfg = synth.BlockConfig("t", rows, 1024, 2816, 1e-5, dtype)
+    inp = synth.make_block_inputs(cfg, seed=100 + rows)
+    y = run_block(ffn, inp)
+    assert_lowp(to_host64(y), oracle_lib.block_from_inputs(inp))
+
+
+@pytest.mark.parametrize("d,ffn_", [(264, 200), (8, 8), (520, 4104), (2048, 2056)])
+def test_decode_ragged_k(ffn, oracle_lib, d, ffn_):
+    """Reduction lengths that are not multiples of 32, feature counts that are
+    not multiples of 16 or 64."""
+    cfg = synth.BlockConfig("t", 5, d, ffn_, 1e-5, "bf16")
+    inp = synth.make_block_inputs(cfg, seed=d + ffn_)
+    assert_lowp(to_host64(run_block(ffn, inp)), oracle_lib.block_from_inputs(inp))
+
+
+@pytest.mark.parametrize("flags", [0, 1, 2])
+@pytest.mark.parametrize("rows,d,ffn_", [(300, 512, 704), (128, 256, 128), (17, 1024, 2816),
+                                         (513, 456, 392)])
+def test_prefill_gemm(ffn, oracle_lib, flags, rows, d, ffn_):
+    """tcgen05 path: ragged M (rows % 128), K % 64 != 0, ffn % 128 != 0; fused
+    and unfused gate/up epilogues."""
+    cfg = synth.BlockConfig("t", rows, d, ffn_, 1e-6, "bf16")
+    inp = synth.make_block_inputs(cfg, seed=rows + d)
+    y = run_block(ffn, inp, flags)
+    assert_lowp(to_host64(y), oracle_lib.block_from_inputs(inp))
+
+
+def test_prefill_gemm_fp16(ffn, oracle_lib):
+    cfg = synth.BlockConfig("t", 256, 512, 1024, 1e-6, "f16")
+    inp = synth.make_block_inputs(cfg, seed=3)
+    assert_lowp(to_host64(run_block(ffn, inp)), oracle_lib.block_from_inputs(inp))
+
+
+@pytest.mark.parametrize("rows", [1, 8, 16])
+def test_forced_gemm_path_for_few_rows(ffn, oracle_lib, rows):
+    cfg = synth.BlockConfig("t", rows, 1024, 2816, 1e-5, "bf16")
+    inp = synth.make_block_inputs(cfg, seed=200 + rows)
+    y = run_block(ffn, inp, ffn.FFN_PATH_GEMM)
+    assert_lowp(to_host64(y), oracle_lib.block_from_inputs(inp))
+
+
+def test_prefill_full_size_sampled(ffn, oracle_lib):
+    """4096 tokens x d=4096, ffn=11008 bf16 (the launch configuration the
+    benchmark times): sampled token rows against the oracle."""
+    inp = synth.make_block_inputs(synth.C4_PREFILL_BF16, seed=0)
+    y = to_host64(run_block(ffn, inp))
+    rows = np.unique(np.concatenate([[0, 127, 128, 4095], np.random.default_rng(2).integers(0, 4096, 8)]))
+    ref = oracle_lib.block_from_inputs(inp, rows=rows)
+    assert_lowp(y[rows], ref)
+
+
+def test_prefill_fused_equals_unfused_closely(ffn):
+    cfg = synth.BlockConfig("t", 384, 1024, 1536, 1e-6, "bf16")
+    inp = synth.make_block_inputs(cfg, seed=9)
+    a = to_host64(run_block(ffn, inp, 1))
+    b = to_host64(run_block(ffn, inp, 2))
+    # the arms round h identically (bf16 of fp32 silu(G)*U vs bf16 of silu(bf16 G)*bf16 U)
+    rms = np.sqrt(np.mean(a * a))
+    assert np.abs(a - b).max() <= 2e-2 * rms
+
+
+@pytest.mark.parametrize("rows", [8, 300])
+def test_deterministic(ffn, rows):
+    cfg = synth.BlockConfig("t", rows, 1024, 2816, 1e-5, "bf16")
+    inp = synth.make_block_inputs(cfg, seed=11)
+    h = [hashlib.sha256(run_block(ffn, inp).view(-1).cpu().numpy().tobytes()).hexdigest() for _ in range(3)]
+    assert h[0] == h[1] == h[2]
+
+
+def test_empty_batch(ffn):
+    import torch
+    x = torch.empty((0, 256), dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros((512, 256), dtype=torch.bfloat16, device="cuda")
+    wd = torch.zeros((256, 512), dtype=torch.bfloat16, device="cuda")
+    g = torch.ones(256, dtype=torch.bfloat16, device="cuda")
+    assert ffn.ffn_block_forward(x, g, w, w, wd, eps=1e-5).shape == (0, 256)
+
+
+def test_device_status_clean(ffn):
+    import torch
+    torch.cuda.synchronize()
+    ffn.ffn_device_status()
+
+
+def test_launch_counter_and_timing(ffn):
+    cfg = synth.BlockConfig("t", 256, 512, 1024, 1e-6, "bf16")
+    inp = synth.make_block_inputs(cfg, seed=12)
+    args = [to_dev(inp[k], "bf16") for k in ("x", "g", "w_gate", "w_up", "w_down")]
+    before = ffn.ffn_launch_count()
+    with ffn.KernelTimer() as t:
+        ffn.ffn_block_forward(*args, eps=1e-6)
+        res = t.read()
+    assert ffn.ffn_launch_count() - before == 3
+    assert set(res) == {"rmsnorm", "gemm_gateup", "gemm_down"}
+    assert all(n == 1 and ms > 0 for n, ms in res.values())

@@ -1,0 +1,303 @@
+// ffn_internal.cuh -- shared declarations of the sm_103a kernels behind include/ffn.h.
+//
+// Everything here is internal: launchers return cudaError_t and assume the
+// C-ABI layer (api.cu) has validated their arguments.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace ffn {
+
+enum DType : int { DT_F32 = 0, DT_F16 = 1, DT_BF16 = 2 };
+
+// Kernel kinds, for launch counting and event timing.
+enum KernelKind : int {
+    K_RMSNORM = 0,
+    K_SWIGLU,
+    K_SIMT_GATEUP,
+    K_SIMT_DOWN,
+    K_GEMV_NORM,
+    K_GEMV_GATEUP,
+    K_GEMV_DOWN,
+    K_GEMM_GATEUP,
+    K_GEMM_DOWN,
+    K_NUM_KINDS
+};
+const char *kernel_name(int kind);
+
+// Brackets one launch: counts it and, when timing is on, records events on
+// the launch stream around it.
+struct LaunchScope {
+    int kind;
+    cudaStream_t stream;
+    void *ev0;
+    LaunchScope(int kind, cudaStream_t s);
+    ~LaunchScope();
+};
+
+// Device status word bits (written by kernels with bounded waits).
+enum : unsigned { DEVERR_TIMEOUT = 1u };
+unsigned *device_status_word();   // device address, for the current device
+int sm_count();                   // multiprocessors on the current device
+
+// ---------------------------------------------------------------- launchers
+cudaError_t launch_rmsnorm(const void *x, const void *g, void *n, int64_t rows, int64_t d,
+                           float eps, int dt, cudaStream_t s);
+cudaError_t launch_swiglu(const void *gate, const void *up, void *h, int64_t count, int dt,
+                          cudaStream_t s);
+
+// fp32 SIMT block: n (rows x d) and h (rows x ffn) are fp32 scratch.
+cudaError_t launch_simt_block(const float *x, const float *g, const float *wg, const float *wu,
+                              const float *wd, float *y, int64_t rows, int64_t d, int64_t ffn,
+                              float eps, float *n, float *h, cudaStream_t s);
+
+// Decode (weight-streaming) block for rows <= 16.
+struct GemvWorkspace {
+    void *nfrag;        // normalised activations in mma B-fragment order
+    void *hfrag;        // hidden activations in mma B-fragment order
+    float *partials;    // [splits][rows][d] fp32
+    unsigned *counters; // [d / 64] arrival counters
+};
+size_t gemv_workspace_bytes(int64_t rows, int64_t d, int64_t ffn);
+void gemv_carve(void *base, int64_t rows, int64_t d, int64_t ffn, GemvWorkspace *ws);
+// wfmt: 0 f16, 1 bf16, 2 q4 (then activations are bf16)
+struct GemvWeights {
+    const void *w;          // f16/bf16 [out x in]
+    const uint8_t *qs;      // q4 device layout
+    const uint16_t *sc;     // q4 scales
+};
+cudaError_t launch_gemv_block(int wfmt, const void *x, const void *g, GemvWeights wg,
+                              GemvWeights wu, GemvWeights wd, void *y, int64_t rows, int64_t d,
+                              int64_t ffn, float eps, const GemvWorkspace &ws, cudaStream_t s);
+
+// Prefill tensor-core GEMMs (tcgen05 + TMEM + TMA).
+//   gate/up: A = n [M x K], B = W_gate, W_up [F x K]; fused -> h [M x F]
+//            unfused -> G, U [M x F] each
+//   down:    A = h [M x F], B = W_down [N x F] -> C [M x N]
+cudaError_t launch_gemm_gateup(int dt, const void *A, const void *Wg, const void *Wu, void *H,
+                               void *G, void *U, int64_t M, int64_t K, int64_t F, bool fused,
+                               cudaStream_t s);
+cudaError_t launch_gemm_plain(int dt, const void *A, const void *B, void *C, int64_t M,
+                              int64_t K, int64_t N, cudaStream_t s);
+
+}  // namespace ffn
+
+// ====================================================================== PTX
+// Thin wrappers over inline PTX used by the kernels.
+namespace ffn {
+namespace ptx {
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// ---- mbarrier
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Wait for the phase of parity `parity` to complete.  Gives up (returns
+// false) after `limit_ns` of wall time or as soon as *abort is non-zero.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort,
+                                          uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort) return false;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
+    }
+}
+
+// ---- TMA
+__device__ __forceinline__ void tma_prefetch_map(const void *map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *map, uint32_t bar, int x,
+                                            int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+        : "memory");
+}
+
+// ---- tcgen05 (cta_group::1)
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     dst_smem),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// Arrive once on `bar` when every tcgen05 op issued so far by this thread completes.
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+}
+// D[tmem] (+)= A[smem] * B[smem]^T, kind::f16 (bf16 or fp16 inputs, fp32 accumulate)
+__device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                           uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// 32 lanes x 32 consecutive 32-bit columns: thread t gets lane (base lane + t)
+__device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_ld_wait() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor for a K-major tile written by TMA with
+// 128-byte swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t sdesc_k_sw128(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);   // start address
+    d |= static_cast<uint64_t>(1) << 16;                    // leading byte offset (unused)
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;            // stride byte offset
+    d |= static_cast<uint64_t>(1) << 46;                    // descriptor version
+    d |= static_cast<uint64_t>(2) << 61;                    // 128-byte swizzle
+    return d;
+}
+// Instruction descriptor, kind::f16: fp32 accumulate, both operands K-major.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool bf16) {
+    return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
+           (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// ---- warp-level mma (m16n8k16, fp32 accumulate)
+template <bool BF16>
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1) {
+    if constexpr (BF16) {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+            "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+    } else {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
+            "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+    }
+}
+
+// ---- streaming global loads
+__device__ __forceinline__ uint4 ld_stream_v4(const void *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+__device__ __forceinline__ uint2 ld_stream_v2(const void *p) {
+    uint2 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];"
+                 : "=r"(v.x), "=r"(v.y)
+                 : "l"(p));
+    return v;
+}
+
+}  // namespace ptx
+
+// ------------------------------------------------------------ conversions
+template <int DT> struct Storage;
+template <> struct Storage<DT_F32> { using T = float; };
+template <> struct Storage<DT_F16> { using T = __half; };
+template <> struct Storage<DT_BF16> { using T = __nv_bfloat16; };
+
+__device__ __forceinline__ float to_f32(float v) { return v; }
+__device__ __forceinline__ float to_f32(__half v) { return __half2float(v); }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float v);
+template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ __half from_f32<__half>(float v) { return __float2half_rn(v); }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) {
+    return __float2bfloat16_rn(v);
+}
+
+// 16 bytes <-> floats
+template <typename T> struct Vec16 {
+    static constexpr int N = 16 / sizeof(T);
+    __device__ static __forceinline__ void unpack(const uint4 &v, float (&f)[16 / sizeof(T)]) {
+        const T *e = reinterpret_cast<const T *>(&v);
+#pragma unroll
+        for (int i = 0; i < N; ++i) f[i] = to_f32(e[i]);
+    }
+    __device__ static __forceinline__ uint4 pack(const float (&f)[16 / sizeof(T)]) {
+        uint4 v;
+        T *e = reinterpret_cast<T *>(&v);
+#pragma unroll
+        for (int i = 0; i < N; ++i) e[i] = from_f32<T>(f[i]);
+        return v;
+    }
+};
+
+// silu(z) = z / (1 + exp(-z)) in fp32 (the limit 0 for very negative z comes
+// out of exp overflowing to +inf).
+__device__ __forceinline__ float silu_f32(float z) { return z / (1.0f + __expf(-z)); }
+
+}  // namespace ffn

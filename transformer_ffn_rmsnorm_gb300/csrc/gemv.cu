@@ -1,0 +1,520 @@
+// gemv.cu -- the FFN block for few token rows (decode): weight streaming.
+//
+// With at most 16 token rows every weight byte is used for at most 16
+// multiply-adds, far below the GB300's ridge point, so the time is the HBM
+// stream of W_gate, W_up and W_down ("How Megakernels Work", section
+// "Projection shape changes the achieved rate": eight-row projections, and
+// a deeper K split for the long-K down projection).  Design:
+//
+// * The weights are the M side of a warp-level m16n8k16 tensor-core MMA and
+//   the (<= 8 per n-tile) token rows are the N side, so no MMA lane is wasted
+//   on padding.  Each lane loads 16 contiguous weight bytes per row straight
+//   from HBM into the A fragment.  Because K is only summed over, the k
+//   index inside one MMA can be permuted freely as long as A and B agree;
+//   the activations are therefore pre-arranged once per call ("fragment
+//   order") so that each lane's B operand is one 16-byte load.  fp32 FFMA
+//   would need 8-16 issue slots per weight pair at these row counts, about
+//   as long as the weight stream itself; the MMA needs one per 256 weights.
+// * Q4 weights ("Unfusing a Kernel Made It 1.63x Faster", section "The
+//   finding that keeps us honest about microbenchmarks": repacked so every
+//   block is read once, coalesced; "How Megakernels Work", section
+//   "Threadgroup staging": no shared-memory staging) are dequantised in
+//   registers: nibbles become (u - 8) exactly in bf16, one block's two MMAs
+//   accumulate into a fresh fp32 fragment, and the block scale multiplies
+//   that fragment (w = (u - 8) * s applied exactly in fp32).
+// * gate/up: 4 warps split K for each 16-feature tile and combine their
+//   partial fragments in shared memory in a fixed order; the epilogue applies
+//   silu(G)*U and writes h already in the down projection's fragment order.
+// * down: K (= ffn) is split across CTAs; each CTA writes fp32 partials and
+//   the last CTA to arrive for a feature group sums the partials in split
+//   order and writes y.  No CTA ever waits for another, and the sum order is
+//   fixed, so results are bitwise reproducible.
+#include "ffn_internal.cuh"
+
+namespace ffn {
+namespace {
+
+constexpr int kChunk = 32;              // k values per MMA pair
+constexpr int kSplitK = 2048;           // down projection: k values per CTA split
+constexpr int kGuKS = 4;                // gate/up: warps along K per tile
+constexpr int kGuTPC = 2;               // gate/up: 16-feature tiles per CTA
+constexpr int kDnTPC = 4;               // down: 16-feature tiles per CTA (one per warp)
+constexpr int kDnFeat = 16 * kDnTPC;    // features per down CTA
+
+enum { WF_F16 = 0, WF_BF16 = 1, WF_Q4 = 2 };
+
+__host__ __device__ inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Fragment order of an activation vector of length K for one token:
+//   16-bit element index = ((nt * nch + c) * 32 + lane) * 8 + slot
+//   lane = 4 * (token % 8) + tid, nt = token / 8, c = k / 32.
+// Natural order (f16/bf16 weights): k % 32 = 8 * tid + slot.
+// Q4 order: position p = k % 32, hi = p / 16, q = p % 16, tid = q / 4,
+//   slot = 4 * hi + perm[q % 4] with perm = {0, 2, 1, 3}; this matches the
+//   nibble unpacking in dequant_word below.
+__device__ __forceinline__ int64_t frag_elem(bool q4, int64_t nch, int token, int64_t k) {
+    const int64_t c = k / kChunk;
+    const int p = static_cast<int>(k % kChunk);
+    int tid, slot;
+    if (q4) {
+        const int hi = p >> 4, q = p & 15;
+        tid = q >> 2;
+        const int e = q & 3;
+        slot = 4 * hi + ((e == 1) ? 2 : (e == 2) ? 1 : e);
+    } else {
+        tid = p >> 3;
+        slot = p & 7;
+    }
+    const int lane = 4 * (token & 7) + tid;
+    return (((token >> 3) * nch + c) * 32 + lane) * 8 + slot;
+}
+
+template <int WF> struct Act;
+template <> struct Act<WF_F16> { using T = __half; static constexpr bool bf16 = false; };
+template <> struct Act<WF_BF16> { using T = __nv_bfloat16; static constexpr bool bf16 = true; };
+template <> struct Act<WF_Q4> { using T = __nv_bfloat16; static constexpr bool bf16 = true; };
+
+// ---------------------------------------------------------------------------
+// 1. RMSNorm of <= 16 token rows, written in fragment order.
+//    One CTA per token slot; slots >= rows (and k >= K) are written as zeros.
+template <int WF>
+__global__ void __launch_bounds__(256) gemv_norm_frag_kernel(const void *x_, const void *g_,
+                                                             uint16_t *nfrag, int rows, int64_t K,
+                                                             int64_t nch, float eps) {
+    using T = typename Act<WF>::T;
+    constexpr bool q4 = WF == WF_Q4;
+    __shared__ float partial[8];
+    const int token = blockIdx.x;
+    const T *x = static_cast<const T *>(x_) + static_cast<int64_t>(token) * K;
+    const T *g = static_cast<const T *>(g_);
+    const int64_t ngroups = nch * 4;  // 8-element groups incl. the zero tail
+    if (token >= rows) {
+        for (int64_t v = threadIdx.x; v < ngroups; v += blockDim.x) {
+            const int64_t k = 8 * v;
+            if (q4) {
+                *reinterpret_cast<uint2 *>(nfrag + frag_elem(true, nch, token, k)) = make_uint2(0, 0);
+                *reinterpret_cast<uint2 *>(nfrag + frag_elem(true, nch, token, k + 4)) = make_uint2(0, 0);
+            } else {
+                *reinterpret_cast<uint4 *>(nfrag + frag_elem(false, nch, token, k)) = make_uint4(0, 0, 0, 0);
+            }
+        }
+        return;
+    }
+    const int64_t nv = K / 8;
+    float ss = 0.f;
+    for (int64_t v = threadIdx.x; v < nv; v += blockDim.x) {
+        float f[8];
+        Vec16<T>::unpack(reinterpret_cast<const uint4 *>(x)[v], f);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if ((threadIdx.x & 31) == 0) partial[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    ss = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) ss += partial[w];
+    const float inv = rsqrtf(ss / static_cast<float>(K) + eps);
+
+    for (int64_t v = threadIdx.x; v < ngroups; v += blockDim.x) {
+        const int64_t k = 8 * v;
+        float f[8];
+        if (v < nv) {
+            float gf[8];
+            Vec16<T>::unpack(reinterpret_cast<const uint4 *>(x)[v], f);
+            Vec16<T>::unpack(reinterpret_cast<const uint4 *>(g)[v], gf);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) f[e] = f[e] * inv * gf[e];
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) f[e] = 0.f;
+        }
+        if (q4) {
+            // two runs of 4 consecutive k; each lands in one 8-byte half of a
+            // lane's fragment with its elements in order {0, 2, 1, 3}
+#pragma unroll
+            for (int run = 0; run < 2; ++run) {
+                T o[4];
+                o[0] = from_f32<T>(f[4 * run + 0]);
+                o[1] = from_f32<T>(f[4 * run + 2]);
+                o[2] = from_f32<T>(f[4 * run + 1]);
+                o[3] = from_f32<T>(f[4 * run + 3]);
+                const int64_t base = frag_elem(true, nch, token, k + 4 * run);
+                *reinterpret_cast<uint2 *>(nfrag + base) = *reinterpret_cast<const uint2 *>(o);
+            }
+        } else {
+            *reinterpret_cast<uint4 *>(nfrag + frag_elem(false, nch, token, k)) = Vec16<T>::pack(f);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Q4: one 32-bit word = canonical bytes 4*tid .. 4*tid+3 of a block.
+// Returns (u - 8) as bf16 pairs:
+//   r[0] = (e0, e2), r[1] = (e16, e18), r[2] = (e1, e3), r[3] = (e17, e19)
+// relative to element 4*tid of the block.  0x4300 is bf16 128.0, so
+// 0x4300 | u is exactly 128 + u, and subtracting 136 gives u - 8 exactly.
+__device__ __forceinline__ void dequant_word(uint32_t w, uint32_t (&r)[4]) {
+    const __nv_bfloat162 k136 = __floats2bfloat162_rn(136.f, 136.f);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t sh = (i == 0) ? 0 : (i == 1) ? 4 : (i == 2) ? 8 : 12;
+        uint32_t v = ((w >> sh) & 0x000F000Fu) | 0x43004300u;
+        __nv_bfloat162 b = *reinterpret_cast<__nv_bfloat162 *>(&v);
+        b = __hsub2(b, k136);
+        r[i] = *reinterpret_cast<uint32_t *>(&b);
+    }
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4 &v, int b) {
+    return b == 0 ? v.x : b == 1 ? v.y : b == 2 ? v.z : v.w;
+}
+
+// Accumulate RT row tiles (16 weight rows each) x NT token tiles over a
+// range of K for one warp.  For f16/bf16, [c0, c1) are 32-wide chunks; for
+// Q4, [c0, c1) are 128-wide groups (four blocks).
+template <int WF, int RT, int NT, int U>
+__device__ __forceinline__ void warp_accumulate(const void *const (&w)[RT],
+                                                const uint16_t *const (&sc)[RT],
+                                                const int64_t (&row)[RT][2],
+                                                const bool (&rowok)[RT][2], int64_t K,
+                                                const uint4 *__restrict__ bfrag, int64_t nch,
+                                                int64_t c0, int64_t c1, float (&acc)[RT][NT][4]) {
+    constexpr bool bf = Act<WF>::bf16;
+    const int lane = threadIdx.x & 31, tid = lane & 3;
+    if constexpr (WF != WF_Q4) {
+        const uint16_t *W[RT];
+#pragma unroll
+        for (int r = 0; r < RT; ++r) W[r] = static_cast<const uint16_t *>(w[r]);
+        for (int64_t c = c0; c < c1; c += U) {
+            uint4 a[U][RT][2], b[U][NT];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t cc = c + u;
+                const int64_t k = cc * kChunk + 8 * tid;
+                const bool ok = cc < c1 && k < K;
+#pragma unroll
+                for (int r = 0; r < RT; ++r)
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+                        a[u][r][h] = (ok && rowok[r][h]) ? ptx::ld_stream_v4(W[r] + row[r][h] * K + k)
+                                                         : make_uint4(0, 0, 0, 0);
+#pragma unroll
+                for (int n = 0; n < NT; ++n)
+                    b[u][n] = (cc < c1) ? __ldg(bfrag + (n * nch + cc) * 32 + lane) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+#pragma unroll
+                for (int r = 0; r < RT; ++r)
+#pragma unroll
+                    for (int n = 0; n < NT; ++n) {
+                        ptx::mma_16816<bf>(acc[r][n], a[u][r][0].x, a[u][r][1].x, a[u][r][0].y,
+                                           a[u][r][1].y, b[u][n].x, b[u][n].y);
+                        ptx::mma_16816<bf>(acc[r][n], a[u][r][0].z, a[u][r][1].z, a[u][r][0].w,
+                                           a[u][r][1].w, b[u][n].z, b[u][n].w);
+                    }
+        }
+    } else {
+        const int64_t qrow = K / 2;    // bytes per weight row
+        const int64_t srow = K / 32;   // scales per weight row
+        for (int64_t gi = c0; gi < c1; gi += U) {
+            uint4 q[U][RT][2];
+            uint2 s[U][RT][2];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t gg = gi + u;
+                const bool ok = gg < c1;
+#pragma unroll
+                for (int r = 0; r < RT; ++r)
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const bool live = ok && rowok[r][h];
+                        const uint8_t *qp = static_cast<const uint8_t *>(w[r]) + row[r][h] * qrow + gg * 64 + 16 * tid;
+                        q[u][r][h] = live ? ptx::ld_stream_v4(qp) : make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);
+                        s[u][r][h] = live ? ptx::ld_stream_v2(sc[r] + row[r][h] * srow + gg * 4) : make_uint2(0, 0);
+                    }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t gg = gi + u;
+                if (gg >= c1) break;
+#pragma unroll
+                for (int blk = 0; blk < 4; ++blk) {
+                    uint4 b[NT];
+#pragma unroll
+                    for (int n = 0; n < NT; ++n) b[n] = __ldg(bfrag + (n * nch + gg * 4 + blk) * 32 + lane);
+#pragma unroll
+                    for (int r = 0; r < RT; ++r) {
+                        uint32_t lo[4], hi[4];
+                        dequant_word(word_of(q[u][r][0], blk), lo);
+                        dequant_word(word_of(q[u][r][1], blk), hi);
+                        const uint32_t s0 = (blk < 2 ? s[u][r][0].x : s[u][r][0].y) >> (16 * (blk & 1));
+                        const uint32_t s1 = (blk < 2 ? s[u][r][1].x : s[u][r][1].y) >> (16 * (blk & 1));
+                        const float f0 = __half2float(__ushort_as_half(static_cast<unsigned short>(s0 & 0xFFFFu)));
+                        const float f1 = __half2float(__ushort_as_half(static_cast<unsigned short>(s1 & 0xFFFFu)));
+#pragma unroll
+                        for (int n = 0; n < NT; ++n) {
+                            float t[4] = {0.f, 0.f, 0.f, 0.f};
+                            ptx::mma_16816<true>(t, lo[0], hi[0], lo[2], hi[2], b[n].x, b[n].y);
+                            ptx::mma_16816<true>(t, lo[1], hi[1], lo[3], hi[3], b[n].z, b[n].w);
+                            acc[r][n][0] = fmaf(f0, t[0], acc[r][n][0]);
+                            acc[r][n][1] = fmaf(f0, t[1], acc[r][n][1]);
+                            acc[r][n][2] = fmaf(f1, t[2], acc[r][n][2]);
+                            acc[r][n][3] = fmaf(f1, t[3], acc[r][n][3]);
+                        }
+                    }
+                }
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// 2. gate/up: h = silu(W_gate n) * (W_up n), written in fragment order for
+//    the down projection.  CTA = kGuTPC tiles x kGuKS warps along K.
+template <int WF, int NT>
+__global__ void __launch_bounds__(256) gemv_gateup_kernel(
+    const void *wg, const void *wu, const uint16_t *sg, const uint16_t *su,
+    const uint4 *__restrict__ nfrag, uint16_t *hfrag, int64_t K, int64_t F, int64_t nchK,
+    int64_t nchF, int64_t nunits, unsigned *counters, int ncounters) {
+    using T = typename Act<WF>::T;
+    constexpr bool q4 = WF == WF_Q4;
+    constexpr int U = q4 ? 2 : 4;
+    __shared__ float red[kGuTPC][kGuKS - 1][32][2 * NT * 4];
+    if (blockIdx.x == 0)
+        for (int i = threadIdx.x; i < ncounters; i += blockDim.x) counters[i] = 0u;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tl = warp / kGuKS, ks = warp % kGuKS;
+    const int64_t tile = static_cast<int64_t>(blockIdx.x) * kGuTPC + tl;
+    const int64_t f0 = tile * 16;
+    const int gq = lane >> 2, tid = lane & 3;
+    const int64_t c0 = nunits * ks / kGuKS, c1 = nunits * (ks + 1) / kGuKS;
+
+    const void *const w[2] = {wg, wu};
+    const uint16_t *const sc[2] = {sg, su};
+    int64_t row[2][2];
+    bool rowok[2][2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            row[r][h] = f0 + gq + 8 * h;
+            rowok[r][h] = row[r][h] < F;
+        }
+    float acc[2][NT][4];
+#pragma unroll
+    for (int r = 0; r < 2; ++r)
+#pragma unroll
+        for (int n = 0; n < NT; ++n)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[r][n][i] = 0.f;
+    warp_accumulate<WF, 2, NT, U>(w, sc, row, rowok, K, nfrag, nchK, c0, c1, acc);
+
+    if (ks > 0) {
+        float *dst = red[tl][ks - 1][lane];
+#pragma unroll
+        for (int r = 0; r < 2; ++r)
+#pragma unroll
+            for (int n = 0; n < NT; ++n)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) dst[(r * NT + n) * 4 + i] = acc[r][n][i];
+    }
+    __syncthreads();
+    if (ks != 0) return;
+#pragma unroll
+    for (int j = 0; j < kGuKS - 1; ++j) {
+        const float *src = red[tl][j][lane];
+#pragma unroll
+        for (int r = 0; r < 2; ++r)
+#pragma unroll
+            for (int n = 0; n < NT; ++n)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) acc[r][n][i] += src[(r * NT + n) * 4 + i];
+    }
+#pragma unroll
+    for (int n = 0; n < NT; ++n)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int64_t feat = f0 + gq + 8 * (i >> 1);
+            const int token = 8 * n + 2 * tid + (i & 1);
+            const float hv = silu_f32(acc[0][n][i]) * acc[1][n][i];
+            const T t = from_f32<T>(hv);
+            hfrag[frag_elem(q4, nchF, token, feat)] = *reinterpret_cast<const uint16_t *>(&t);
+        }
+}
+
+// ---------------------------------------------------------------------------
+// 3. down: y = W_down h.  grid = (feature groups of 64, K splits).
+template <int WF, int NT>
+__global__ void __launch_bounds__(128) gemv_down_kernel(
+    const void *wd, const uint16_t *sd, const uint4 *__restrict__ hfrag, void *y_, float *partials,
+    unsigned *counters, int rows, int64_t D, int64_t F, int64_t nchF, int64_t units_per_split) {
+    using T = typename Act<WF>::T;
+    constexpr bool q4 = WF == WF_Q4;
+    constexpr int U = q4 ? 2 : 8;
+    __shared__ int s_last;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gq = lane >> 2, tid = lane & 3;
+    const int64_t f0 = (static_cast<int64_t>(blockIdx.x) * kDnTPC + warp) * 16;
+    const int split = blockIdx.y, nsplit = gridDim.y;
+    const int64_t nunits = q4 ? (F / 128) : nchF;
+    const int64_t c0 = split * units_per_split;
+    const int64_t c1 = (c0 + units_per_split < nunits) ? c0 + units_per_split : nunits;
+
+    const void *const w[1] = {wd};
+    const uint16_t *const sc[1] = {sd};
+    int64_t row[1][2];
+    bool rowok[1][2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        row[0][h] = f0 + gq + 8 * h;
+        rowok[0][h] = row[0][h] < D;
+    }
+    float acc[1][NT][4];
+#pragma unroll
+    for (int n = 0; n < NT; ++n)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[0][n][i] = 0.f;
+    warp_accumulate<WF, 1, NT, U>(w, sc, row, rowok, F, hfrag, nchF, c0, c1, acc);
+
+#pragma unroll
+    for (int n = 0; n < NT; ++n)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int64_t feat = f0 + gq + 8 * (i >> 1);
+            const int token = 8 * n + 2 * tid + (i & 1);
+            if (token < rows && feat < D)
+                partials[(static_cast<int64_t>(split) * rows + token) * D + feat] = acc[0][n][i];
+        }
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = atomicAdd(&counters[blockIdx.x], 1u) == static_cast<unsigned>(nsplit - 1);
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    T *y = static_cast<T *>(y_);
+    const int64_t fbase = static_cast<int64_t>(blockIdx.x) * kDnFeat;
+    for (int i = threadIdx.x; i < rows * kDnFeat; i += blockDim.x) {
+        const int token = i / kDnFeat;
+        const int64_t feat = fbase + i % kDnFeat;
+        if (feat >= D) continue;
+        float sum = 0.f;
+        for (int sp = 0; sp < nsplit; ++sp)
+            sum += __ldcg(partials + (static_cast<int64_t>(sp) * rows + token) * D + feat);
+        y[static_cast<int64_t>(token) * D + feat] = from_f32<T>(sum);
+    }
+    if (threadIdx.x == 0) counters[blockIdx.x] = 0u;
+}
+
+// ---------------------------------------------------------------------------
+struct Geometry {
+    int nt;            // token tiles of 8
+    int64_t nchK;      // chunks of 32 along d (gate/up K)
+    int64_t nchF;      // chunks of 32 along ffn (down K)
+    int64_t splits;    // down-projection K splits
+    int64_t ups;       // units (chunks or Q4 groups) per split
+    int64_t groups;    // down feature groups of 64
+};
+
+Geometry geometry(int64_t rows, int64_t d, int64_t ffn, bool q4) {
+    Geometry g;
+    g.nt = rows > 8 ? 2 : 1;
+    g.nchK = cdiv(d, kChunk);
+    g.nchF = cdiv(ffn, kChunk);
+    g.ups = q4 ? kSplitK / 128 : kSplitK / kChunk;
+    const int64_t units = q4 ? ffn / 128 : g.nchF;
+    g.splits = cdiv(units, g.ups);
+    g.groups = cdiv(d, kDnFeat);
+    return g;
+}
+
+size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
+
+template <int WF, int NT>
+cudaError_t launch_typed(const void *x, const void *gain, GemvWeights wg, GemvWeights wu,
+                         GemvWeights wd, void *y, int rows, int64_t d, int64_t ffn, float eps,
+                         const GemvWorkspace &ws, const Geometry &geo, cudaStream_t s) {
+    constexpr bool q4 = WF == WF_Q4;
+    {
+        LaunchScope scope(K_GEMV_NORM, s);
+        gemv_norm_frag_kernel<WF><<<8 * NT, 256, 0, s>>>(x, gain, static_cast<uint16_t *>(ws.nfrag),
+                                                         rows, d, geo.nchK, eps);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    {
+        const int64_t tiles = 2 * geo.nchF;  // covers every fragment slot of h
+        const int64_t blocks = cdiv(tiles, kGuTPC);
+        const int64_t units = q4 ? d / 128 : geo.nchK;
+        LaunchScope scope(K_GEMV_GATEUP, s);
+        gemv_gateup_kernel<WF, NT><<<static_cast<unsigned>(blocks), 32 * kGuTPC * kGuKS, 0, s>>>(
+            q4 ? static_cast<const void *>(wg.qs) : wg.w, q4 ? static_cast<const void *>(wu.qs) : wu.w,
+            wg.sc, wu.sc, static_cast<const uint4 *>(ws.nfrag), static_cast<uint16_t *>(ws.hfrag), d,
+            ffn, geo.nchK, geo.nchF, units, ws.counters, static_cast<int>(geo.groups));
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    {
+        dim3 grid(static_cast<unsigned>(geo.groups), static_cast<unsigned>(geo.splits));
+        LaunchScope scope(K_GEMV_DOWN, s);
+        gemv_down_kernel<WF, NT><<<grid, 32 * kDnTPC, 0, s>>>(
+            q4 ? static_cast<const void *>(wd.qs) : wd.w, wd.sc, static_cast<const uint4 *>(ws.hfrag), y,
+            ws.partials, ws.counters, rows, d, ffn, geo.nchF, geo.ups);
+        return cudaGetLastError();
+    }
+}
+
+}  // namespace
+
+size_t gemv_workspace_bytes(int64_t rows, int64_t d, int64_t ffn) {
+    // sized for the Q4 or 16-bit geometry, whichever is larger
+    const Geometry a = geometry(rows, d, ffn, false);
+    const Geometry b = geometry(rows, d, ffn, (d % 128 == 0) && (ffn % 128 == 0));
+    const int64_t splits = a.splits > b.splits ? a.splits : b.splits;
+    const int nt = a.nt;
+    size_t bytes = 0;
+    bytes += align256(static_cast<size_t>(nt) * a.nchK * 32 * 16);
+    bytes += align256(static_cast<size_t>(nt) * a.nchF * 32 * 16);
+    bytes += align256(static_cast<size_t>(splits) * (rows > 16 ? 16 : rows) * d * 4);
+    bytes += align256(static_cast<size_t>(a.groups) * 4);
+    return bytes;
+}
+
+void gemv_carve(void *base, int64_t rows, int64_t d, int64_t ffn, GemvWorkspace *ws) {
+    const Geometry a = geometry(rows, d, ffn, false);
+    const Geometry b = geometry(rows, d, ffn, (d % 128 == 0) && (ffn % 128 == 0));
+    const int64_t splits = a.splits > b.splits ? a.splits : b.splits;
+    char *p = static_cast<char *>(base);
+    ws->nfrag = p;
+    p += align256(static_cast<size_t>(a.nt) * a.nchK * 32 * 16);
+    ws->hfrag = p;
+    p += align256(static_cast<size_t>(a.nt) * a.nchF * 32 * 16);
+    ws->partials = reinterpret_cast<float *>(p);
+    p += align256(static_cast<size_t>(splits) * (rows > 16 ? 16 : rows) * d * 4);
+    ws->counters = reinterpret_cast<unsigned *>(p);
+}
+
+cudaError_t launch_gemv_block(int wfmt, const void *x, const void *g, GemvWeights wg,
+                              GemvWeights wu, GemvWeights wd, void *y, int64_t rows, int64_t d,
+                              int64_t ffn, float eps, const GemvWorkspace &ws, cudaStream_t s) {
+    if (rows <= 0) return cudaSuccess;
+    const Geometry geo = geometry(rows, d, ffn, wfmt == WF_Q4);
+    const int r = static_cast<int>(rows);
+    if (geo.nt == 1) {
+        switch (wfmt) {
+            case WF_F16: return launch_typed<WF_F16, 1>(x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s);
+            case WF_BF16: return launch_typed<WF_BF16, 1>(x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s);
+            default: return launch_typed<WF_Q4, 1>(x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s);
+        }
+    }
+    switch (wfmt) {
+        case WF_F16: return launch_typed<WF_F16, 2>(x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s);
+        case WF_BF16: return launch_typed<WF_BF16, 2>(x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s);
+        default: return launch_typed<WF_Q4, 2>(x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s);
+    }
+}
+
+}  // namespace ffn
