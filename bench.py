@@ -43,6 +43,8 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-sub", action="store_true", help="skip the secondary workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU baseline")
+    ap.add_argument("--only-main", action="store_true",
+                    help="time the main step only (no arm comparison, e2e, sub-workloads or CPU baseline)")
     return ap.parse_args()
 
 
@@ -367,11 +369,41 @@ def run_ours(args):
     roof = {"bound": "tensor", "kernel": "gemm_gateup", "achieved": round(achieved_t, 1), "peak": peak_t,
             "unit": "TFLOP/s", "frac": round(achieved_t / peak_t, 4),
             "peak_source": f"{peak_src} bf16_tflops_sustained (cuBLAS, seconds-long loop)",
-            "algorithmic_flops_per_launch": flops_gu, "traffic": None}
+            "algorithmic_flops_per_launch": flops_gu,
+            "mma_flops_per_launch": 2 * flops_gu,
+            "note": "n enters as hi + lo bf16 terms, so the kernel issues twice the algorithmic MMA work",
+            "tensor_pipe_frac": round(2 * achieved_t / peak_t, 4), "traffic": None}
     n_dn, ms_dn = res["gemm_down"]
     flops_dn = 2.0 * cfg.rows * cfg.ffn * cfg.d
     extra = {"gemm_down_TFLOPs": round(flops_dn / (ms_dn / n_dn / 1000.0) / 1e12, 1),
              "block_TFLOPs": round((flops_gu + flops_dn) / (ms / args.steps / 1000.0) / 1e12, 1)}
+
+    # gate/up arms, timed interleaved call by call (each pair shares one
+    # thermal window): fused epilogue vs unfused (G, U stored + SwiGLU pass),
+    # each with n as hi + lo (default for bf16) and as one rounding
+    arms = {}
+    if rank == 0 and not args.only_main:
+        variants = {"fused_split": ffn.FFN_GATEUP_FUSED, "unfused_split": ffn.FFN_GATEUP_UNFUSED,
+                    "fused_single": ffn.FFN_GATEUP_FUSED | ffn.FFN_NORM_SINGLE,
+                    "unfused_single": ffn.FFN_GATEUP_UNFUSED | ffn.FFN_NORM_SINGLE}
+        wss = {k: ffn.workspace(ffn.ffn_block_workspace_bytes(cfg.rows, cfg.d, cfg.ffn, torch.bfloat16, f), device)
+               for k, f in variants.items()}
+        ev = {k: [] for k in variants}
+        for _ in range(3):
+            for k, f in variants.items():
+                ffn.ffn_block_forward(x, g, wg, wu, wd, eps=cfg.eps, flags=f, out=y, ws=wss[k])
+        for _ in range(12):
+            for k, f in variants.items():
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                ffn.ffn_block_forward(x, g, wg, wu, wd, eps=cfg.eps, flags=f, out=y, ws=wss[k])
+                b.record(stream)
+                ev[k].append((a, b))
+        torch.cuda.synchronize()
+        for k in variants:
+            t = sorted(a.elapsed_time(b) for a, b in ev[k])
+            arms[k] = {"median_ms": round(t[len(t) // 2], 4), "min_ms": round(t[0], 4)}
+        del wss
 
     # end to end: pinned host x -> device -> block -> pinned host y, per step
     xh = x.cpu().pin_memory()
@@ -382,17 +414,19 @@ def run_ours(args):
         ffn.ffn_block_forward(x, g, wg, wu, wd, eps=cfg.eps, out=y, ws=ws)
         yh.copy_(y, non_blocking=True)
 
-    e2e_steps = max(3, min(args.steps, 200))
-    e2e_ms = timed_loop(torch, e2e_step, e2e_steps, 3, stream)
-    e2e_val = cfg.rows * e2e_steps * world / (e2e_ms / 1000.0)
+    e2e_val = None
+    if not args.only_main:
+        e2e_steps = max(3, min(args.steps, 200))
+        e2e_ms = timed_loop(torch, e2e_step, e2e_steps, 3, stream)
+        e2e_val = round(cfg.rows * e2e_steps * world / (e2e_ms / 1000.0), 1)
 
     sub = []
-    if not args.no_sub and rank == 0:
+    if not args.no_sub and not args.only_main and rank == 0:
         del xh, yh
         sub = sub_benchmarks(torch, ffn, device, peaks, peak_src, stream)
 
     cpu = None
-    if not args.no_cpu and rank == 0:
+    if not args.no_cpu and not args.only_main and rank == 0:
         rows_sample = 32
         rate, secs, threads = cpu_oracle_rate(inp, rows_sample, 2, 0)
         cpu = {"value": round(rate, 3), "unit": "tokens/s", "cores": threads, "kind": "oracle",
@@ -406,12 +440,13 @@ def run_ours(args):
             "data": "synthetic, seeded (numpy PCG64, seed = rank): x~N(0,1), g=1+0.1N(0,1), W~N(0,1/fan_in)",
             "config": {"workload": cfg.name, "rows": cfg.rows, "d": cfg.d, "ffn": cfg.ffn, "eps": cfg.eps,
                        "storage": "bf16", "accumulate": "fp32", "gateup_epilogue": "fused",
+                       "norm_operand": "hi+lo bf16 terms",
                        "parallelism": "replicas" if world > 1 else "single",
                        "l2": "inputs larger than L2 (weights 270.5 MB + x 33.5 MB + n/h 124 MB per step)"},
-            "roofline": roof, "extra": extra,
+            "roofline": roof, "extra": extra, "gateup_arms_ms": arms,
             "kernels": kernel_table(res), "gpu_launches": launches,
             "clocks": clocks,
-            "e2e": {"value": round(e2e_val, 1), "unit": "tokens/s",
+            "e2e": {"value": e2e_val, "unit": "tokens/s",
                     "h2d_bytes_per_step": cfg.rows * cfg.d * 2, "d2h_bytes_per_step": cfg.rows * cfg.d * 2},
             "cpu_baseline": cpu, "sub": sub,
         }

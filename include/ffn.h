@@ -62,6 +62,14 @@ typedef enum { FFN_F32 = 0, FFN_F16 = 1, FFN_BF16 = 2 } ffn_dtype;
 #define FFN_PATH_GEMM 4u
 /* force the weight-streaming decode path (16-bit dtypes, rows <= 16)         */
 #define FFN_PATH_GEMV 8u
+/* tensor-core path: feed the gate/up GEMM one rounding of n (fastest).  With
+ * bf16 storage this leaves max|y - y_exact| near 2.2e-2 * rms(y) on the
+ * 4096 x 4096 -> 11008 workload, above the 2e-2 bound, so it is opt-in.     */
+#define FFN_NORM_SINGLE 16u
+/* tensor-core path: feed n as two terms hi + lo (hi = round(n),
+ * lo = round(n - hi)) that share each weight tile: ~16 significant bits for n
+ * at twice the gate/up MMA work.  Default for bf16; opt-in for fp16.         */
+#define FFN_NORM_SPLIT 32u
 
 /* ------------------------------------------------------------------------
  * ffn_rmsnorm -- n[r,c] = x[r,c] * rsqrt(ms_r + eps) * g[c],

@@ -75,10 +75,30 @@ def test_prefill_gemm(ffn, oracle_lib, flags, rows, d, ffn_):
     assert_lowp(to_host64(y), oracle_lib.block_from_inputs(inp))
 
 
-def test_prefill_gemm_fp16(ffn, oracle_lib):
+@pytest.mark.parametrize("flags", [0, 32])
+def test_prefill_gemm_fp16(ffn, oracle_lib, flags):
+    """fp16 storage: one rounding of n keeps 11 bits (default); FFN_NORM_SPLIT
+    also works for fp16."""
     cfg = synth.BlockConfig("t", 256, 512, 1024, 1e-6, "f16")
     inp = synth.make_block_inputs(cfg, seed=3)
-    assert_lowp(to_host64(run_block(ffn, inp)), oracle_lib.block_from_inputs(inp))
+    assert_lowp(to_host64(run_block(ffn, inp, flags)), oracle_lib.block_from_inputs(inp))
+
+
+def test_prefill_single_term_norm_is_opt_in(ffn, oracle_lib):
+    """FFN_NORM_SINGLE feeds one bf16 rounding of n to the gate/up GEMM.  Its
+    error is the plain three-rounding (n, h, y) error: the mean stays inside
+    the bound but the max sits near 2e-2 * rms, which is why it is not the
+    default.  Checked here against the mean bound and a 3e-2 max."""
+    from gpu_util import errors
+    cfg = synth.BlockConfig("t", 300, 512, 704, 1e-6, "bf16")
+    inp = synth.make_block_inputs(cfg, seed=812)
+    y = to_host64(run_block(ffn, inp, ffn.FFN_NORM_SINGLE))
+    ref = oracle_lib.block_from_inputs(inp)
+    _, mx, mean = errors(y, ref)
+    assert mean <= 4e-3 and mx <= 3e-2
+    ys = to_host64(run_block(ffn, inp))
+    _, mx2, mean2 = errors(ys, ref)
+    assert mx2 < mx and mean2 < mean
 
 
 @pytest.mark.parametrize("rows", [1, 8, 16])
@@ -94,7 +114,7 @@ def test_prefill_full_size_sampled(ffn, oracle_lib):
     benchmark times): sampled token rows against the oracle."""
     inp = synth.make_block_inputs(synth.C4_PREFILL_BF16, seed=0)
     y = to_host64(run_block(ffn, inp))
-    rows = np.unique(np.concatenate([[0, 127, 128, 4095], np.random.default_rng(2).integers(0, 4096, 8)]))
+    rows = np.unique(np.concatenate([[0, 127, 128, 4095], np.random.default_rng(2).integers(0, 4096, 28)]))
     ref = oracle_lib.block_from_inputs(inp, rows=rows)
     assert_lowp(y[rows], ref)
 

@@ -72,6 +72,7 @@ enum Path { PATH_SIMT, PATH_GEMV, PATH_GEMM };
 struct Plan {
     Path path;
     bool fused;
+    bool split_norm;   // tensor-core path: RMSNorm output as hi + lo terms
     size_t workspace;
 };
 
@@ -88,11 +89,16 @@ ffn_status plan_block(int64_t rows, int64_t d, int64_t ffn, ffn_dtype dt, uint32
                       Plan *plan) {
     ffn_status st = check_block_shape(rows, d, ffn, dt);
     if (st != FFN_OK) return st;
-    const uint32_t known = FFN_GATEUP_FUSED | FFN_GATEUP_UNFUSED | FFN_PATH_GEMM | FFN_PATH_GEMV;
+    const uint32_t known = FFN_GATEUP_FUSED | FFN_GATEUP_UNFUSED | FFN_PATH_GEMM | FFN_PATH_GEMV |
+                           FFN_NORM_SINGLE | FFN_NORM_SPLIT;
     if (flags & ~known) return FFN_ERR_FLAGS;
     if ((flags & FFN_GATEUP_FUSED) && (flags & FFN_GATEUP_UNFUSED)) return FFN_ERR_FLAGS;
     if ((flags & FFN_PATH_GEMM) && (flags & FFN_PATH_GEMV)) return FFN_ERR_FLAGS;
+    if ((flags & FFN_NORM_SINGLE) && (flags & FFN_NORM_SPLIT)) return FFN_ERR_FLAGS;
     plan->fused = !(flags & FFN_GATEUP_UNFUSED);
+    // bf16 keeps 8 significant bits: one rounding of n costs more than the
+    // block's error budget allows, so by default n goes in as hi + lo.
+    plan->split_norm = (flags & FFN_NORM_SPLIT) || (dt == FFN_BF16 && !(flags & FFN_NORM_SINGLE));
     if (dt == FFN_F32) {
         if (flags & (FFN_PATH_GEMM | FFN_PATH_GEMV)) return FFN_ERR_FLAGS;
         plan->path = PATH_SIMT;
@@ -115,6 +121,7 @@ ffn_status plan_block(int64_t rows, int64_t d, int64_t ffn, ffn_dtype dt, uint32
             break;
         case PATH_GEMM:
             plan->workspace = align256(r * d * es) + align256(r * ffn * es);
+            if (plan->split_norm) plan->workspace += align256(r * d * es);
             if (!plan->fused) plan->workspace += 2 * align256(r * ffn * es);
             break;
     }
@@ -281,16 +288,26 @@ ffn_status ffn_block_forward(const void *x, const void *g, const void *w_gate, c
         case PATH_GEMM: {
             const size_t nb = align256(static_cast<size_t>(rows) * d * es);
             const size_t hb = align256(static_cast<size_t>(rows) * ffn * es);
-            void *n = ws;
-            void *h = ws + nb;
-            cudaError_t e = launch_rmsnorm(x, g, n, rows, d, eps, dtype, s);
+            char *p = ws;
+            void *n = p;
+            p += nb;
+            void *n_lo = nullptr;
+            if (plan.split_norm) {
+                n_lo = p;
+                p += nb;
+            }
+            void *h = p;
+            p += hb;
+            cudaError_t e = plan.split_norm ? launch_rmsnorm_split(x, g, n, n_lo, rows, d, eps, dtype, s)
+                                            : launch_rmsnorm(x, g, n, rows, d, eps, dtype, s);
             if (e != cudaSuccess) return FFN_ERR_CUDA;
             if (plan.fused) {
-                e = launch_gemm_gateup(dtype, n, w_gate, w_up, h, nullptr, nullptr, rows, d, ffn, true, s);
+                e = launch_gemm_gateup(dtype, n, n_lo, w_gate, w_up, h, nullptr, nullptr, rows, d, ffn,
+                                       true, s);
             } else {
-                void *G = ws + nb + hb;
-                void *U = ws + nb + 2 * hb;
-                e = launch_gemm_gateup(dtype, n, w_gate, w_up, nullptr, G, U, rows, d, ffn, false, s);
+                void *G = p;
+                void *U = p + hb;
+                e = launch_gemm_gateup(dtype, n, n_lo, w_gate, w_up, nullptr, G, U, rows, d, ffn, false, s);
                 if (e == cudaSuccess) e = launch_swiglu(G, U, h, rows * ffn, dtype, s);
             }
             if (e != cudaSuccess) return FFN_ERR_CUDA;

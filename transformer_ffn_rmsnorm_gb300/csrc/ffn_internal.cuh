@@ -47,6 +47,10 @@ int sm_count();                   // multiprocessors on the current device
 // ---------------------------------------------------------------- launchers
 cudaError_t launch_rmsnorm(const void *x, const void *g, void *n, int64_t rows, int64_t d,
                            float eps, int dt, cudaStream_t s);
+// As launch_rmsnorm, for 16-bit storage, also writing the rounding residual:
+// n_hi = round(v), n_lo = round(v - n_hi), so n_hi + n_lo carries ~16 bits.
+cudaError_t launch_rmsnorm_split(const void *x, const void *g, void *n_hi, void *n_lo,
+                                 int64_t rows, int64_t d, float eps, int dt, cudaStream_t s);
 cudaError_t launch_swiglu(const void *gate, const void *up, void *h, int64_t count, int dt,
                           cudaStream_t s);
 
@@ -75,12 +79,12 @@ cudaError_t launch_gemv_block(int wfmt, const void *x, const void *g, GemvWeight
                               int64_t ffn, float eps, const GemvWorkspace &ws, cudaStream_t s);
 
 // Prefill tensor-core GEMMs (tcgen05 + TMEM + TMA).
-//   gate/up: A = n [M x K], B = W_gate, W_up [F x K]; fused -> h [M x F]
-//            unfused -> G, U [M x F] each
+//   gate/up: A = n [M x K] (plus its residual A_lo, or nullptr), B = W_gate,
+//            W_up [F x K]; fused -> h [M x F]; unfused -> G, U [M x F] each
 //   down:    A = h [M x F], B = W_down [N x F] -> C [M x N]
-cudaError_t launch_gemm_gateup(int dt, const void *A, const void *Wg, const void *Wu, void *H,
-                               void *G, void *U, int64_t M, int64_t K, int64_t F, bool fused,
-                               cudaStream_t s);
+cudaError_t launch_gemm_gateup(int dt, const void *A, const void *A_lo, const void *Wg,
+                               const void *Wu, void *H, void *G, void *U, int64_t M, int64_t K,
+                               int64_t F, bool fused, cudaStream_t s);
 cudaError_t launch_gemm_plain(int dt, const void *A, const void *B, void *C, int64_t M,
                               int64_t K, int64_t N, cudaStream_t s);
 

@@ -36,13 +36,20 @@
 namespace ffn {
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4, UMMA_K = 16;
+constexpr int BM = 128, BN = 256, BK = 64, UMMA_K = 16;
 constexpr uint32_t A_BYTES = BM * BK * 2;
 constexpr uint32_t B_BYTES = BN * BK * 2;
-constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int NUM_THREADS = 192;
-constexpr size_t SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
+
+// A_TERMS = 2: the A operand is given as two bf16 matrices whose sum is the
+// fp32 value (hi + lo); both are multiplied by the same B tile and accumulate
+// into the same TMEM accumulator, so A carries ~16 significant bits.
+template <int A_TERMS> struct Ring {
+    static constexpr int STAGES = A_TERMS == 1 ? 4 : 3;
+    static constexpr uint32_t STAGE_BYTES = A_TERMS * A_BYTES + B_BYTES;
+    static constexpr size_t SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
+};
 constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;
 
 enum Mode { MODE_PLAIN = 0, MODE_GATEUP_FUSED = 1, MODE_GATEUP_SPLIT = 2 };
@@ -70,12 +77,15 @@ __device__ __forceinline__ void store_row32(T *dst, int64_t col, int64_t ncols, 
     }
 }
 
-template <int MODE, bool BF16>
+template <int MODE, bool BF16, int A_TERMS>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a,
+                        const __grid_constant__ CUtensorMap map_a2,
                         const __grid_constant__ CUtensorMap map_b0,
                         const __grid_constant__ CUtensorMap map_b1, const GemmParams p) {
     using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
+    constexpr int STAGES = Ring<A_TERMS>::STAGES;
+    constexpr uint32_t STAGE_BYTES = Ring<A_TERMS>::STAGE_BYTES;
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bar_full[STAGES], bar_empty[STAGES];
     __shared__ __align__(8) uint64_t bar_tfull[2], bar_tempty[2], bar_drain;
@@ -84,7 +94,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t base = (ptx::smem_u32(smem_raw) + 1023u) & ~1023u;
-    const uint32_t sA = base, sB = base + STAGES * A_BYTES;
+    // stage s: A term 0 | A term 1 (if any) | B, each 1024-byte aligned
+    auto sA = [&](uint32_t s, int t) { return base + s * STAGE_BYTES + t * A_BYTES; };
+    auto sB = [&](uint32_t s) { return base + s * STAGE_BYTES + A_TERMS * A_BYTES; };
     auto full = [&](uint32_t s) { return ptx::smem_u32(&bar_full[s]); };
     auto empty = [&](uint32_t s) { return ptx::smem_u32(&bar_empty[s]); };
     auto tfull = [&](uint32_t a) { return ptx::smem_u32(&bar_tfull[a]); };
@@ -104,6 +116,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         s_never = 0;
         ptx::fence_mbar_init();
         ptx::tma_prefetch_map(&map_a);
+        if (A_TERMS == 2) ptx::tma_prefetch_map(&map_a2);
         ptx::tma_prefetch_map(&map_b0);
         if (MODE != MODE_PLAIN) ptx::tma_prefetch_map(&map_b1);
     }
@@ -135,13 +148,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 ptx::mbar_arrive_expect_tx(full(s), STAGE_BYTES);
                 const int k0 = kb * BK;
-                ptx::tma_load_2d(sA + s * A_BYTES, &map_a, full(s), k0, m0);
+                ptx::tma_load_2d(sA(s, 0), &map_a, full(s), k0, m0);
+                if (A_TERMS == 2) ptx::tma_load_2d(sA(s, 1), &map_a2, full(s), k0, m0);
                 if (MODE == MODE_PLAIN) {
-                    ptx::tma_load_2d(sB + s * B_BYTES, &map_b0, full(s), k0, static_cast<int>(n_blk * BN));
+                    ptx::tma_load_2d(sB(s), &map_b0, full(s), k0, static_cast<int>(n_blk * BN));
                 } else {
                     const int f0 = static_cast<int>(n_blk * (BN / 2));
-                    ptx::tma_load_2d(sB + s * B_BYTES, &map_b0, full(s), k0, f0);
-                    ptx::tma_load_2d(sB + s * B_BYTES + B_BYTES / 2, &map_b1, full(s), k0, f0);
+                    ptx::tma_load_2d(sB(s), &map_b0, full(s), k0, f0);
+                    ptx::tma_load_2d(sB(s) + B_BYTES / 2, &map_b1, full(s), k0, f0);
                 }
                 ++produced;
             }
@@ -171,12 +185,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     break;
                 }
                 ptx::tc_fence_after();
-                const uint32_t a0 = sA + s * A_BYTES, b0 = sB + s * B_BYTES;
+                const uint32_t b0 = sB(s);
 #pragma unroll
-                for (int k = 0; k < BK / UMMA_K; ++k)
-                    ptx::tc_mma_f16(d_tmem, ptx::sdesc_k_sw128(a0 + k * UMMA_K * 2),
-                                    ptx::sdesc_k_sw128(b0 + k * UMMA_K * 2), idesc,
-                                    (kb | k) != 0 ? 1u : 0u);
+                for (int t = 0; t < A_TERMS; ++t) {
+                    const uint32_t a0 = sA(s, t);
+#pragma unroll
+                    for (int k = 0; k < BK / UMMA_K; ++k)
+                        ptx::tc_mma_f16(d_tmem, ptx::sdesc_k_sw128(a0 + k * UMMA_K * 2),
+                                        ptx::sdesc_k_sw128(b0 + k * UMMA_K * 2), idesc,
+                                        (kb | k | t) != 0 ? 1u : 0u);
+                }
                 ptx::tc_commit(empty(s));
                 ++consumed;
             }
@@ -311,23 +329,26 @@ bool make_map(CUtensorMap *m, const void *ptr, bool bf16, int64_t inner, int64_t
     return r == CUDA_SUCCESS;
 }
 
-template <int MODE, bool BF16>
-cudaError_t launch_impl(const void *A, const void *B0, const void *B1, void *out0, void *out1,
-                        int64_t M, int64_t K, int64_t N, int kind, cudaStream_t s) {
+template <int MODE, bool BF16, int A_TERMS>
+cudaError_t launch_impl(const void *A, const void *A2, const void *B0, const void *B1, void *out0,
+                        void *out1, int64_t M, int64_t K, int64_t N, int kind, cudaStream_t s) {
     if (M <= 0) return cudaSuccess;
+    constexpr size_t SMEM_BYTES = Ring<A_TERMS>::SMEM_BYTES;
     static int configured_device = -1;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (configured_device != dev) {
-        e = cudaFuncSetAttribute(gemm_tcgen05_kernel<MODE, BF16>,
+        e = cudaFuncSetAttribute(gemm_tcgen05_kernel<MODE, BF16, A_TERMS>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(SMEM_BYTES));
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
-    CUtensorMap ma, mb0, mb1;
+    CUtensorMap ma, ma2, mb0, mb1;
     if (!make_map(&ma, A, BF16, K, M, BM)) return cudaErrorInvalidValue;
+    ma2 = ma;
+    if (A_TERMS == 2 && !make_map(&ma2, A2, BF16, K, M, BM)) return cudaErrorInvalidValue;
     if (MODE == MODE_PLAIN) {
         if (!make_map(&mb0, B0, BF16, K, N, BN)) return cudaErrorInvalidValue;
         mb1 = mb0;
@@ -353,28 +374,37 @@ cudaError_t launch_impl(const void *A, const void *B0, const void *B1, void *out
     int64_t grid = sm_count();
     if (grid > p.num_tiles) grid = p.num_tiles;
     LaunchScope scope(kind, s);
-    gemm_tcgen05_kernel<MODE, BF16>
-        <<<static_cast<unsigned>(grid), NUM_THREADS, SMEM_BYTES, s>>>(ma, mb0, mb1, p);
+    gemm_tcgen05_kernel<MODE, BF16, A_TERMS>
+        <<<static_cast<unsigned>(grid), NUM_THREADS, SMEM_BYTES, s>>>(ma, ma2, mb0, mb1, p);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_gemm_gateup(int dt, const void *A, const void *Wg, const void *Wu, void *H,
-                               void *G, void *U, int64_t M, int64_t K, int64_t F, bool fused,
-                               cudaStream_t s) {
+cudaError_t launch_gemm_gateup(int dt, const void *A, const void *A_lo, const void *Wg,
+                               const void *Wu, void *H, void *G, void *U, int64_t M, int64_t K,
+                               int64_t F, bool fused, cudaStream_t s) {
     const bool bf = dt == DT_BF16;
+    const int k = K_GEMM_GATEUP;
+    if (A_lo) {
+        if (fused)
+            return bf ? launch_impl<MODE_GATEUP_FUSED, true, 2>(A, A_lo, Wg, Wu, H, nullptr, M, K, F, k, s)
+                      : launch_impl<MODE_GATEUP_FUSED, false, 2>(A, A_lo, Wg, Wu, H, nullptr, M, K, F, k, s);
+        return bf ? launch_impl<MODE_GATEUP_SPLIT, true, 2>(A, A_lo, Wg, Wu, G, U, M, K, F, k, s)
+                  : launch_impl<MODE_GATEUP_SPLIT, false, 2>(A, A_lo, Wg, Wu, G, U, M, K, F, k, s);
+    }
     if (fused)
-        return bf ? launch_impl<MODE_GATEUP_FUSED, true>(A, Wg, Wu, H, nullptr, M, K, F, K_GEMM_GATEUP, s)
-                  : launch_impl<MODE_GATEUP_FUSED, false>(A, Wg, Wu, H, nullptr, M, K, F, K_GEMM_GATEUP, s);
-    return bf ? launch_impl<MODE_GATEUP_SPLIT, true>(A, Wg, Wu, G, U, M, K, F, K_GEMM_GATEUP, s)
-              : launch_impl<MODE_GATEUP_SPLIT, false>(A, Wg, Wu, G, U, M, K, F, K_GEMM_GATEUP, s);
+        return bf ? launch_impl<MODE_GATEUP_FUSED, true, 1>(A, nullptr, Wg, Wu, H, nullptr, M, K, F, k, s)
+                  : launch_impl<MODE_GATEUP_FUSED, false, 1>(A, nullptr, Wg, Wu, H, nullptr, M, K, F, k, s);
+    return bf ? launch_impl<MODE_GATEUP_SPLIT, true, 1>(A, nullptr, Wg, Wu, G, U, M, K, F, k, s)
+              : launch_impl<MODE_GATEUP_SPLIT, false, 1>(A, nullptr, Wg, Wu, G, U, M, K, F, k, s);
 }
 
 cudaError_t launch_gemm_plain(int dt, const void *A, const void *B, void *C, int64_t M, int64_t K,
                               int64_t N, cudaStream_t s) {
-    return dt == DT_BF16 ? launch_impl<MODE_PLAIN, true>(A, B, nullptr, C, nullptr, M, K, N, K_GEMM_DOWN, s)
-                         : launch_impl<MODE_PLAIN, false>(A, B, nullptr, C, nullptr, M, K, N, K_GEMM_DOWN, s);
+    return dt == DT_BF16
+               ? launch_impl<MODE_PLAIN, true, 1>(A, nullptr, B, nullptr, C, nullptr, M, K, N, K_GEMM_DOWN, s)
+               : launch_impl<MODE_PLAIN, false, 1>(A, nullptr, B, nullptr, C, nullptr, M, K, N, K_GEMM_DOWN, s);
 }
 
 }  // namespace ffn
