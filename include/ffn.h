@@ -55,8 +55,9 @@ typedef enum { FFN_F32 = 0, FFN_F16 = 1, FFN_BF16 = 2 } ffn_dtype;
 #define FFN_AUTO 0u
 /* tensor-core path: silu(G)*U computed in the gate/up GEMM epilogue (default) */
 #define FFN_GATEUP_FUSED 1u
-/* tensor-core path: the gate/up GEMM stores G and U; a separate SwiGLU pass
- * reads them back ("Unfusing a Kernel Made It 1.63x Faster", Finding 1)     */
+/* tensor-core path: the gate/up GEMM stores G and U (fp32, so h is still
+ * rounded once); a separate SwiGLU pass reads them back ("Unfusing a Kernel
+ * Made It 1.63x Faster", Finding 1)                                          */
 #define FFN_GATEUP_UNFUSED 2u
 /* force the tcgen05 tensor-core GEMM path (16-bit dtypes, any rows)          */
 #define FFN_PATH_GEMM 4u
@@ -155,6 +156,30 @@ ffn_status ffn_block_forward_q4(const void *x, const void *g, ffn_q4_weight w_ga
                                 ffn_q4_weight w_up, ffn_q4_weight w_down, void *y, int64_t rows,
                                 int64_t d, int64_t ffn, float eps, uint32_t flags, void *workspace,
                                 size_t workspace_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
+ * ffn_block_forward_decode_static -- the decode block (same kernels and
+ * results as ffn_block_forward on its weight-streaming path) for callers that
+ * cannot hand the library a workspace: runtimes that plan all device memory
+ * up front and allow no allocation while serving, plugins that receive only
+ * their input and output buffers, and decode loops that must not call
+ * cudaMalloc (it can synchronise the device).  The pages describe no such
+ * call; it has no counterpart there.
+ *   Scratch: one 10 MiB array in device memory owned by the library, present
+ *   on every GPU that loads the library until the process exits.  No
+ *   allocation, no free, no allocating library call is made.  Limits (checked,
+ *   FFN_ERR_SHAPE beyond them): rows <= 16, d <= 8192, ffn <= 32768, plus
+ *   d % 8 == 0 and ffn % 8 == 0; dtype FFN_F16 or FFN_BF16.
+ *   The first call on a device looks up the array's device address (with that
+ *   device current) -- make that first call before any stream capture.
+ *   Every call reuses the same array: calls that may run at the same time on
+ *   the GPU (other streams, other host threads) race and must be serialised
+ *   by the caller.  Other arguments, layouts and errors as ffn_block_forward.
+ * ---------------------------------------------------------------------- */
+ffn_status ffn_block_forward_decode_static(const void *x, const void *g, const void *w_gate,
+                                           const void *w_up, const void *w_down, void *y,
+                                           int64_t rows, int64_t d, int64_t ffn, float eps,
+                                           ffn_dtype dtype, void *stream);
 
 /* Host helper (not on the hot path): pack int8 q [out x in] (values -8..7) and
  * fp16 scale bits [out x in/32] into the device layout above.  Host pointers;

@@ -44,6 +44,9 @@ SIGNATURES = {
     "ffn_block_forward_q4": (c_int, [c_void_p, c_void_p, Q4Weight, Q4Weight, Q4Weight, c_void_p,
                                      c_int64, c_int64, c_int64, c_float, c_uint32, c_void_p,
                                      c_size_t, c_void_p]),
+    "ffn_block_forward_decode_static": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                                c_void_p, c_int64, c_int64, c_int64, c_float, c_int,
+                                                c_void_p]),
     "ffn_q4_pack_host": (c_int, [c_void_p, c_void_p, c_int64, c_int64, c_void_p, c_void_p]),
     "ffn_status_string": (ctypes.c_char_p, [c_int]),
     "ffn_device_status": (c_int, []),
