@@ -20,7 +20,8 @@
  *   rounded once, round-to-nearest-even, to the storage type.
  * - Arguments are validated on the host before any launch.  A violation
  *   returns an error status and launches nothing.  rows == 0 (an empty batch)
- *   is valid and launches nothing.  Pointers must be 16-byte aligned.
+ *   is valid and launches nothing (x, y and n may then be NULL).  Pointers
+ *   must be 16-byte aligned.
  * - After launching, a failed launch is reported as FFN_ERR_CUDA.  A kernel
  *   that gives up a bounded wait records FFN_ERR_TIMEOUT in a device status
  *   word that ffn_device_status() reads; no C++ exception crosses this ABI.
@@ -63,14 +64,16 @@ typedef enum { FFN_F32 = 0, FFN_F16 = 1, FFN_BF16 = 2 } ffn_dtype;
 #define FFN_PATH_GEMM 4u
 /* force the weight-streaming decode path (16-bit dtypes, rows <= 16)         */
 #define FFN_PATH_GEMV 8u
-/* tensor-core path: feed the gate/up GEMM one rounding of n (fastest).  With
- * bf16 storage this leaves max|y - y_exact| near 2.2e-2 * rms(y) on the
- * 4096 x 4096 -> 11008 workload, above the 2e-2 bound, so it is opt-in.     */
-#define FFN_NORM_SINGLE 16u
-/* tensor-core path: feed n as two terms hi + lo (hi = round(n),
- * lo = round(n - hi)) that share each weight tile: ~16 significant bits for n
- * at twice the gate/up MMA work.  Default for bf16; opt-in for fp16.         */
-#define FFN_NORM_SPLIT 32u
+/* 16-bit paths: n (RMSNorm output) and h (silu(G)*U) enter the tensor-core
+ * operations as one rounding to the storage type (fastest).  With bf16 this
+ * leaves max|y - y_exact| up to about 2.2e-2 * rms(y), above the 2e-2 bound,
+ * so it is opt-in.                                                          */
+#define FFN_ACT_SINGLE 16u
+/* 16-bit paths: n and h enter as two terms hi + lo (hi = round(v),
+ * lo = round(v - hi)), each multiplied by the same weight tile: ~16
+ * significant bits, at twice the MMA work.  Default for bf16 (and Q4);
+ * opt-in for fp16, whose 11 bits already fit the budget.                    */
+#define FFN_ACT_SPLIT 32u
 
 /* ------------------------------------------------------------------------
  * ffn_rmsnorm -- n[r,c] = x[r,c] * rsqrt(ms_r + eps) * g[c],
@@ -149,8 +152,9 @@ ffn_status ffn_block_q4_workspace_bytes(int64_t rows, int64_t d, int64_t ffn, si
  * to registers; staging through shared memory lost).
  *   x [rows x d] bf16, g [d] bf16, y [rows x d] bf16; w_gate/w_up are Q4
  *   [ffn x d], w_down is Q4 [d x ffn].  Needs d % 128 == 0, ffn % 128 == 0,
- *   d <= 12288.  Rows are processed in groups of up to 16; each group streams
- *   the weights once.  flags must be FFN_AUTO.
+ *   Rows are processed in groups of up to 16; each group streams the weights
+ *   once.  flags: FFN_AUTO (activations as hi + lo terms), FFN_ACT_SINGLE or
+ *   FFN_ACT_SPLIT.  The workspace query covers either.
  * ---------------------------------------------------------------------- */
 ffn_status ffn_block_forward_q4(const void *x, const void *g, ffn_q4_weight w_gate,
                                 ffn_q4_weight w_up, ffn_q4_weight w_down, void *y, int64_t rows,
@@ -165,7 +169,7 @@ ffn_status ffn_block_forward_q4(const void *x, const void *g, ffn_q4_weight w_ga
  * their input and output buffers, and decode loops that must not call
  * cudaMalloc (it can synchronise the device).  The pages describe no such
  * call; it has no counterpart there.
- *   Scratch: one 10 MiB array in device memory owned by the library, present
+ *   Scratch: one 12 MiB array in device memory owned by the library, present
  *   on every GPU that loads the library until the process exits.  No
  *   allocation, no free, no allocating library call is made.  Limits (checked,
  *   FFN_ERR_SHAPE beyond them): rows <= 16, d <= 8192, ffn <= 32768, plus

@@ -24,7 +24,7 @@ FFN_OK, FFN_ERR_NULL, FFN_ERR_SHAPE, FFN_ERR_DTYPE, FFN_ERR_ALIGN = 0, 1, 2, 3, 
 FFN_ERR_WORKSPACE, FFN_ERR_ALIAS, FFN_ERR_CUDA, FFN_ERR_TIMEOUT, FFN_ERR_FLAGS = 5, 6, 7, 8, 9
 FFN_F32, FFN_F16, FFN_BF16 = 0, 1, 2
 FFN_AUTO, FFN_GATEUP_FUSED, FFN_GATEUP_UNFUSED, FFN_PATH_GEMM, FFN_PATH_GEMV = 0, 1, 2, 4, 8
-FFN_NORM_SINGLE, FFN_NORM_SPLIT = 16, 32
+FFN_ACT_SINGLE, FFN_ACT_SPLIT = 16, 32
 
 
 class Q4Weight(ctypes.Structure):

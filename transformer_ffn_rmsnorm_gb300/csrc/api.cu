@@ -72,7 +72,7 @@ enum Path { PATH_SIMT, PATH_GEMV, PATH_GEMM };
 struct Plan {
     Path path;
     bool fused;
-    bool split_norm;   // tensor-core path: RMSNorm output as hi + lo terms
+    bool split_act;    // 16-bit paths: n and h enter the tensor ops as hi + lo terms
     size_t workspace;
 };
 
@@ -90,15 +90,16 @@ ffn_status plan_block(int64_t rows, int64_t d, int64_t ffn, ffn_dtype dt, uint32
     ffn_status st = check_block_shape(rows, d, ffn, dt);
     if (st != FFN_OK) return st;
     const uint32_t known = FFN_GATEUP_FUSED | FFN_GATEUP_UNFUSED | FFN_PATH_GEMM | FFN_PATH_GEMV |
-                           FFN_NORM_SINGLE | FFN_NORM_SPLIT;
+                           FFN_ACT_SINGLE | FFN_ACT_SPLIT;
     if (flags & ~known) return FFN_ERR_FLAGS;
     if ((flags & FFN_GATEUP_FUSED) && (flags & FFN_GATEUP_UNFUSED)) return FFN_ERR_FLAGS;
     if ((flags & FFN_PATH_GEMM) && (flags & FFN_PATH_GEMV)) return FFN_ERR_FLAGS;
-    if ((flags & FFN_NORM_SINGLE) && (flags & FFN_NORM_SPLIT)) return FFN_ERR_FLAGS;
+    if ((flags & FFN_ACT_SINGLE) && (flags & FFN_ACT_SPLIT)) return FFN_ERR_FLAGS;
     plan->fused = !(flags & FFN_GATEUP_UNFUSED);
-    // bf16 keeps 8 significant bits: one rounding of n costs more than the
-    // block's error budget allows, so by default n goes in as hi + lo.
-    plan->split_norm = (flags & FFN_NORM_SPLIT) || (dt == FFN_BF16 && !(flags & FFN_NORM_SINGLE));
+    // bf16 keeps 8 significant bits: rounding n and h once each costs more
+    // than the block's error budget allows, so by default they enter the
+    // tensor ops as hi + lo (about 16 bits).
+    plan->split_act = (flags & FFN_ACT_SPLIT) || (dt == FFN_BF16 && !(flags & FFN_ACT_SINGLE));
     if (dt == FFN_F32) {
         if (flags & (FFN_PATH_GEMM | FFN_PATH_GEMV)) return FFN_ERR_FLAGS;
         plan->path = PATH_SIMT;
@@ -117,12 +118,12 @@ ffn_status plan_block(int64_t rows, int64_t d, int64_t ffn, ffn_dtype dt, uint32
             plan->workspace = align256(r * d * 4) + align256(r * ffn * 4);
             break;
         case PATH_GEMV:
-            plan->workspace = rows == 0 ? 0 : gemv_workspace_bytes(rows, d, ffn);
+            plan->workspace = rows == 0 ? 0 : gemv_workspace_bytes(rows, d, ffn, plan->split_act);
             break;
         case PATH_GEMM:
             plan->workspace = align256(r * d * es) + align256(r * ffn * es);
-            if (plan->split_norm) plan->workspace += align256(r * d * es);
-            if (!plan->fused) plan->workspace += 2 * align256(r * ffn * es);
+            if (plan->split_act) plan->workspace += align256(r * d * es) + align256(r * ffn * es);
+            if (!plan->fused) plan->workspace += 2 * align256(r * ffn * 4);
             break;
     }
     return FFN_OK;
@@ -207,9 +208,10 @@ uint64_t ffn_launch_count(void) { return g_launch_count.load(); }
 
 ffn_status ffn_rmsnorm(const void *x, const void *g, void *n, int64_t rows, int64_t d, float eps,
                        ffn_dtype dtype, void *stream) {
-    if (!x || !g || !n) return FFN_ERR_NULL;
+    if (!g || (rows != 0 && (!x || !n))) return FFN_ERR_NULL;
     if (!valid_dtype(dtype)) return FFN_ERR_DTYPE;
     if (rows < 0 || d < 1 || rows > INT32_MAX || d > INT32_MAX) return FFN_ERR_SHAPE;
+    if (rows == 0) return FFN_OK;
     if (!aligned16(x) || !aligned16(g) || !aligned16(n)) return FFN_ERR_ALIGN;
     const size_t es = dtype_size(dtype);
     const Range rx{x, static_cast<size_t>(rows) * d * es}, rg{g, static_cast<size_t>(d) * es},
@@ -222,9 +224,10 @@ ffn_status ffn_rmsnorm(const void *x, const void *g, void *n, int64_t rows, int6
 
 ffn_status ffn_swiglu(const void *gate, const void *up, void *h, int64_t count, ffn_dtype dtype,
                       void *stream) {
-    if (!gate || !up || !h) return FFN_ERR_NULL;
+    if (count != 0 && (!gate || !up || !h)) return FFN_ERR_NULL;
     if (!valid_dtype(dtype)) return FFN_ERR_DTYPE;
     if (count < 0) return FFN_ERR_SHAPE;
+    if (count == 0) return FFN_OK;
     if (!aligned16(gate) || !aligned16(up) || !aligned16(h)) return FFN_ERR_ALIGN;
     const size_t bytes = static_cast<size_t>(count) * dtype_size(dtype);
     const Range rg{gate, bytes}, ru{up, bytes}, rh{h, bytes};
@@ -248,10 +251,11 @@ ffn_status ffn_block_forward(const void *x, const void *g, const void *w_gate, c
                              const void *w_down, void *y, int64_t rows, int64_t d, int64_t ffn,
                              float eps, ffn_dtype dtype, uint32_t flags, void *workspace,
                              size_t workspace_bytes, void *stream) {
-    if (!x || !g || !w_gate || !w_up || !w_down || !y) return FFN_ERR_NULL;
+    if (!g || !w_gate || !w_up || !w_down || (rows != 0 && (!x || !y))) return FFN_ERR_NULL;
     Plan plan;
     ffn_status st = plan_block(rows, d, ffn, dtype, flags, &plan);
     if (st != FFN_OK) return st;
+    if (rows == 0) return FFN_OK;
     if (plan.workspace > 0 && !workspace) return FFN_ERR_WORKSPACE;
     if (workspace_bytes < plan.workspace) return FFN_ERR_WORKSPACE;
     if (!aligned16(x) || !aligned16(g) || !aligned16(w_gate) || !aligned16(w_up) ||
@@ -280,7 +284,7 @@ ffn_status ffn_block_forward(const void *x, const void *g, const void *w_gate, c
         }
         case PATH_GEMV: {
             GemvWorkspace gw;
-            gemv_carve(workspace, rows, d, ffn, &gw);
+            gemv_carve(workspace, rows, d, ffn, plan.split_act, &gw);
             GemvWeights a{w_gate, nullptr, nullptr}, b{w_up, nullptr, nullptr}, c{w_down, nullptr, nullptr};
             return from_cuda(launch_gemv_block(dtype == FFN_BF16 ? 1 : 0, x, g, a, b, c, y, rows, d,
                                                ffn, eps, gw, s));
@@ -292,26 +296,33 @@ ffn_status ffn_block_forward(const void *x, const void *g, const void *w_gate, c
             void *n = p;
             p += nb;
             void *n_lo = nullptr;
-            if (plan.split_norm) {
+            void *h = nullptr;
+            void *h_lo = nullptr;
+            if (plan.split_act) {
                 n_lo = p;
                 p += nb;
             }
-            void *h = p;
+            h = p;
             p += hb;
-            cudaError_t e = plan.split_norm ? launch_rmsnorm_split(x, g, n, n_lo, rows, d, eps, dtype, s)
-                                            : launch_rmsnorm(x, g, n, rows, d, eps, dtype, s);
+            if (plan.split_act) {
+                h_lo = p;
+                p += hb;
+            }
+            cudaError_t e = plan.split_act ? launch_rmsnorm_split(x, g, n, n_lo, rows, d, eps, dtype, s)
+                                           : launch_rmsnorm(x, g, n, rows, d, eps, dtype, s);
             if (e != cudaSuccess) return FFN_ERR_CUDA;
             if (plan.fused) {
-                e = launch_gemm_gateup(dtype, n, n_lo, w_gate, w_up, h, nullptr, nullptr, rows, d, ffn,
-                                       true, s);
+                e = launch_gemm_gateup(dtype, n, n_lo, w_gate, w_up, h, h_lo, nullptr, nullptr, rows, d,
+                                       ffn, true, s);
             } else {
-                void *G = p;
-                void *U = p + hb;
-                e = launch_gemm_gateup(dtype, n, n_lo, w_gate, w_up, nullptr, G, U, rows, d, ffn, false, s);
-                if (e == cudaSuccess) e = launch_swiglu(G, U, h, rows * ffn, dtype, s);
+                float *G = reinterpret_cast<float *>(p);
+                float *U = reinterpret_cast<float *>(p + align256(static_cast<size_t>(rows) * ffn * 4));
+                e = launch_gemm_gateup(dtype, n, n_lo, w_gate, w_up, nullptr, nullptr, G, U, rows, d, ffn,
+                                       false, s);
+                if (e == cudaSuccess) e = launch_swiglu_f32in(G, U, h, h_lo, rows * ffn, dtype, s);
             }
             if (e != cudaSuccess) return FFN_ERR_CUDA;
-            return from_cuda(launch_gemm_plain(dtype, h, w_down, y, rows, ffn, d, s));
+            return from_cuda(launch_gemm_plain(dtype, h, h_lo, w_down, y, rows, ffn, d, s));
         }
     }
     return FFN_ERR_SHAPE;
@@ -321,7 +332,8 @@ ffn_status ffn_block_q4_workspace_bytes(int64_t rows, int64_t d, int64_t ffn, si
     if (!bytes) return FFN_ERR_NULL;
     if (rows < 0 || d < 128 || ffn < 128 || d % 128 || ffn % 128) return FFN_ERR_SHAPE;
     if (rows > INT32_MAX || d > INT32_MAX || ffn > INT32_MAX) return FFN_ERR_SHAPE;
-    *bytes = rows == 0 ? 0 : gemv_workspace_bytes(std::min<int64_t>(rows, kGemvMaxRows), d, ffn);
+    // sized for two-term activations (enough for either flag)
+    *bytes = rows == 0 ? 0 : gemv_workspace_bytes(std::min<int64_t>(rows, kGemvMaxRows), d, ffn, true);
     return FFN_OK;
 }
 
@@ -329,10 +341,12 @@ ffn_status ffn_block_forward_q4(const void *x, const void *g, ffn_q4_weight w_ga
                                 ffn_q4_weight w_up, ffn_q4_weight w_down, void *y, int64_t rows,
                                 int64_t d, int64_t ffn, float eps, uint32_t flags, void *workspace,
                                 size_t workspace_bytes, void *stream) {
-    if (!x || !g || !y || !w_gate.qs || !w_gate.scales || !w_up.qs || !w_up.scales || !w_down.qs ||
-        !w_down.scales)
+    if (!g || !w_gate.qs || !w_gate.scales || !w_up.qs || !w_up.scales || !w_down.qs ||
+        !w_down.scales || (rows != 0 && (!x || !y)))
         return FFN_ERR_NULL;
-    if (flags != FFN_AUTO) return FFN_ERR_FLAGS;
+    if ((flags & ~(FFN_ACT_SINGLE | FFN_ACT_SPLIT)) || (flags == (FFN_ACT_SINGLE | FFN_ACT_SPLIT)))
+        return FFN_ERR_FLAGS;
+    const bool two = !(flags & FFN_ACT_SINGLE);
     size_t need = 0;
     ffn_status st = ffn_block_q4_workspace_bytes(rows, d, ffn, &need);
     if (st != FFN_OK) return st;
@@ -356,7 +370,7 @@ ffn_status ffn_block_forward_q4(const void *x, const void *g, ffn_q4_weight w_ga
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int64_t grp = std::min<int64_t>(rows, kGemvMaxRows);
     GemvWorkspace gw;
-    gemv_carve(workspace, grp, d, ffn, &gw);
+    gemv_carve(workspace, grp, d, ffn, two, &gw);
     GemvWeights a{nullptr, w_gate.qs, w_gate.scales}, b{nullptr, w_up.qs, w_up.scales},
         c{nullptr, w_down.qs, w_down.scales};
     for (int64_t r0 = 0; r0 < rows; r0 += kGemvMaxRows) {

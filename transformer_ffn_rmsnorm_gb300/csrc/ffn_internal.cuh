@@ -54,6 +54,11 @@ cudaError_t launch_rmsnorm_split(const void *x, const void *g, void *n_hi, void 
 cudaError_t launch_swiglu(const void *gate, const void *up, void *h, int64_t count, int dt,
                           cudaStream_t s);
 
+// fp32 G, U -> 16-bit h, and its residual h_lo when non-null (unfused arm of
+// the tensor-core path)
+cudaError_t launch_swiglu_f32in(const float *gate, const float *up, void *h, void *h_lo,
+                                int64_t count, int dt, cudaStream_t s);
+
 // fp32 SIMT block: n (rows x d) and h (rows x ffn) are fp32 scratch.
 cudaError_t launch_simt_block(const float *x, const float *g, const float *wg, const float *wu,
                               const float *wd, float *y, int64_t rows, int64_t d, int64_t ffn,
@@ -63,11 +68,13 @@ cudaError_t launch_simt_block(const float *x, const float *g, const float *wg, c
 struct GemvWorkspace {
     void *nfrag;        // normalised activations in mma B-fragment order
     void *hfrag;        // hidden activations in mma B-fragment order
+    void *nfrag_lo;     // their rounding residuals (two-term operands), or null
+    void *hfrag_lo;
     float *partials;    // [splits][rows][d] fp32
     unsigned *counters; // [d / 64] arrival counters
 };
-size_t gemv_workspace_bytes(int64_t rows, int64_t d, int64_t ffn);
-void gemv_carve(void *base, int64_t rows, int64_t d, int64_t ffn, GemvWorkspace *ws);
+size_t gemv_workspace_bytes(int64_t rows, int64_t d, int64_t ffn, bool two_terms);
+void gemv_carve(void *base, int64_t rows, int64_t d, int64_t ffn, bool two_terms, GemvWorkspace *ws);
 // wfmt: 0 f16, 1 bf16, 2 q4 (then activations are bf16)
 struct GemvWeights {
     const void *w;          // f16/bf16 [out x in]
@@ -80,13 +87,15 @@ cudaError_t launch_gemv_block(int wfmt, const void *x, const void *g, GemvWeight
 
 // Prefill tensor-core GEMMs (tcgen05 + TMEM + TMA).
 //   gate/up: A = n [M x K] (plus its residual A_lo, or nullptr), B = W_gate,
-//            W_up [F x K]; fused -> h [M x F]; unfused -> G, U [M x F] each
-//   down:    A = h [M x F], B = W_down [N x F] -> C [M x N]
+//            W_up [F x K]; fused -> h [M x F] (plus residual H_lo if non-null);
+//            unfused -> G, U [M x F] fp32 each
+//   down:    A = h [M x F] (plus residual A_lo, or nullptr), B = W_down [N x F]
+//            -> C [M x N]
 cudaError_t launch_gemm_gateup(int dt, const void *A, const void *A_lo, const void *Wg,
-                               const void *Wu, void *H, void *G, void *U, int64_t M, int64_t K,
-                               int64_t F, bool fused, cudaStream_t s);
-cudaError_t launch_gemm_plain(int dt, const void *A, const void *B, void *C, int64_t M,
-                              int64_t K, int64_t N, cudaStream_t s);
+                               const void *Wu, void *H, void *H_lo, void *G, void *U, int64_t M,
+                               int64_t K, int64_t F, bool fused, cudaStream_t s);
+cudaError_t launch_gemm_plain(int dt, const void *A, const void *A_lo, const void *B, void *C,
+                              int64_t M, int64_t K, int64_t N, cudaStream_t s);
 
 }  // namespace ffn
 

@@ -2,7 +2,7 @@
 //
 //   gate/up:  [G | U] = n * [W_gate ; W_up]^T   (n [M x K], W [F x K])
 //             fused epilogue:   h = silu(G) * U            -> h [M x F]
-//             unfused epilogue: G and U stored separately  -> a SwiGLU pass
+//             unfused epilogue: G and U stored in fp32     -> a SwiGLU pass
 //   down:     y = h * W_down^T                  (h [M x F], W_down [d x F])
 //
 // "Unfusing a Kernel Made It 1.63x Faster", Finding 1: on the Apple part the
@@ -58,23 +58,43 @@ struct GemmParams {
     int64_t M, N, K;          // N: output columns (ffn for gate/up, d for down)
     int64_t num_m_blocks, num_tiles;
     int num_k_blocks;
-    void *out0, *out1;        // plain: C; fused: h; split: G, U
+    void *out0, *out1;        // plain: C; fused: h (and its residual, or null); split: G, U
     int64_t ldo;              // output row stride in elements
     unsigned *err;
     uint64_t wait_limit_ns;
 };
 
+// Stores 32 values rounded once; with `lo` also the rounding residual
+// v - round(v), rounded once, so that hi + lo carries ~16 significant bits.
 template <typename T>
-__device__ __forceinline__ void store_row32(T *dst, int64_t col, int64_t ncols, const float (&v)[32]) {
+__device__ __forceinline__ void store_row32(T *dst, T *lo, int64_t col, int64_t ncols,
+                                            const float (&v)[32]) {
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         if (col + 8 * j < ncols) {
             float f[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) f[e] = v[8 * j + e];
-            *reinterpret_cast<uint4 *>(dst + col + 8 * j) = Vec16<T>::pack(f);
+            const uint4 hv = Vec16<T>::pack(f);
+            *reinterpret_cast<uint4 *>(dst + col + 8 * j) = hv;
+            if (lo) {
+                float hf[8];
+                Vec16<T>::unpack(hv, hf);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) f[e] -= hf[e];
+                *reinterpret_cast<uint4 *>(lo + col + 8 * j) = Vec16<T>::pack(f);
+            }
         }
     }
+}
+
+__device__ __forceinline__ void store_row32_f32(float *dst, int64_t col, int64_t ncols,
+                                               const float (&v)[32]) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        if (col + 4 * j < ncols)
+            *reinterpret_cast<float4 *>(dst + col + 4 * j) =
+                make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
 }
 
 template <int MODE, bool BF16, int A_TERMS>
@@ -239,7 +259,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     float v[32];
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-                    if (live) store_row32<T>(out0 + row * p.ldo, n_blk * BN + c, p.N, v);
+                    if (live) store_row32<T>(out0 + row * p.ldo, nullptr, n_blk * BN + c, p.N, v);
                 }
             } else {
 #pragma unroll 1
@@ -254,7 +274,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                         for (int j = 0; j < 32; ++j)
                             h[j] = silu_f32(__uint_as_float(rg[j])) * __uint_as_float(ru[j]);
-                        if (live) store_row32<T>(out0 + row * p.ldo, col, p.N, h);
+                        if (live)
+                            store_row32<T>(out0 + row * p.ldo, out1 ? out1 + row * p.ldo : nullptr,
+                                           col, p.N, h);
                     } else {
                         float g[32], u[32];
 #pragma unroll
@@ -262,9 +284,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             g[j] = __uint_as_float(rg[j]);
                             u[j] = __uint_as_float(ru[j]);
                         }
+                        // G and U stay fp32 so that h is rounded exactly
+                        // once, as in the fused arm
                         if (live) {
-                            store_row32<T>(out0 + row * p.ldo, col, p.N, g);
-                            store_row32<T>(out1 + row * p.ldo, col, p.N, u);
+                            store_row32_f32(static_cast<float *>(p.out0) + row * p.ldo, col, p.N, g);
+                            store_row32_f32(static_cast<float *>(p.out1) + row * p.ldo, col, p.N, u);
                         }
                     }
                 }
@@ -382,29 +406,33 @@ cudaError_t launch_impl(const void *A, const void *A2, const void *B0, const voi
 }  // namespace
 
 cudaError_t launch_gemm_gateup(int dt, const void *A, const void *A_lo, const void *Wg,
-                               const void *Wu, void *H, void *G, void *U, int64_t M, int64_t K,
-                               int64_t F, bool fused, cudaStream_t s) {
+                               const void *Wu, void *H, void *H_lo, void *G, void *U, int64_t M,
+                               int64_t K, int64_t F, bool fused, cudaStream_t s) {
     const bool bf = dt == DT_BF16;
     const int k = K_GEMM_GATEUP;
     if (A_lo) {
         if (fused)
-            return bf ? launch_impl<MODE_GATEUP_FUSED, true, 2>(A, A_lo, Wg, Wu, H, nullptr, M, K, F, k, s)
-                      : launch_impl<MODE_GATEUP_FUSED, false, 2>(A, A_lo, Wg, Wu, H, nullptr, M, K, F, k, s);
+            return bf ? launch_impl<MODE_GATEUP_FUSED, true, 2>(A, A_lo, Wg, Wu, H, H_lo, M, K, F, k, s)
+                      : launch_impl<MODE_GATEUP_FUSED, false, 2>(A, A_lo, Wg, Wu, H, H_lo, M, K, F, k, s);
         return bf ? launch_impl<MODE_GATEUP_SPLIT, true, 2>(A, A_lo, Wg, Wu, G, U, M, K, F, k, s)
                   : launch_impl<MODE_GATEUP_SPLIT, false, 2>(A, A_lo, Wg, Wu, G, U, M, K, F, k, s);
     }
     if (fused)
-        return bf ? launch_impl<MODE_GATEUP_FUSED, true, 1>(A, nullptr, Wg, Wu, H, nullptr, M, K, F, k, s)
-                  : launch_impl<MODE_GATEUP_FUSED, false, 1>(A, nullptr, Wg, Wu, H, nullptr, M, K, F, k, s);
+        return bf ? launch_impl<MODE_GATEUP_FUSED, true, 1>(A, nullptr, Wg, Wu, H, H_lo, M, K, F, k, s)
+                  : launch_impl<MODE_GATEUP_FUSED, false, 1>(A, nullptr, Wg, Wu, H, H_lo, M, K, F, k, s);
     return bf ? launch_impl<MODE_GATEUP_SPLIT, true, 1>(A, nullptr, Wg, Wu, G, U, M, K, F, k, s)
               : launch_impl<MODE_GATEUP_SPLIT, false, 1>(A, nullptr, Wg, Wu, G, U, M, K, F, k, s);
 }
 
-cudaError_t launch_gemm_plain(int dt, const void *A, const void *B, void *C, int64_t M, int64_t K,
-                              int64_t N, cudaStream_t s) {
-    return dt == DT_BF16
-               ? launch_impl<MODE_PLAIN, true, 1>(A, nullptr, B, nullptr, C, nullptr, M, K, N, K_GEMM_DOWN, s)
-               : launch_impl<MODE_PLAIN, false, 1>(A, nullptr, B, nullptr, C, nullptr, M, K, N, K_GEMM_DOWN, s);
+cudaError_t launch_gemm_plain(int dt, const void *A, const void *A_lo, const void *B, void *C,
+                              int64_t M, int64_t K, int64_t N, cudaStream_t s) {
+    const bool bf = dt == DT_BF16;
+    const int k = K_GEMM_DOWN;
+    if (A_lo)
+        return bf ? launch_impl<MODE_PLAIN, true, 2>(A, A_lo, B, nullptr, C, nullptr, M, K, N, k, s)
+                  : launch_impl<MODE_PLAIN, false, 2>(A, A_lo, B, nullptr, C, nullptr, M, K, N, k, s);
+    return bf ? launch_impl<MODE_PLAIN, true, 1>(A, nullptr, B, nullptr, C, nullptr, M, K, N, k, s)
+              : launch_impl<MODE_PLAIN, false, 1>(A, nullptr, B, nullptr, C, nullptr, M, K, N, k, s);
 }
 
 }  // namespace ffn

@@ -77,10 +77,12 @@ template <> struct Act<WF_Q4> { using T = __nv_bfloat16; static constexpr bool b
 // ---------------------------------------------------------------------------
 // 1. RMSNorm of <= 16 token rows, written in fragment order.
 //    One CTA per token slot; slots >= rows (and k >= K) are written as zeros.
-template <int WF>
+//    With TWO, nlo receives the rounding residual of every value (same order).
+template <int WF, bool TWO>
 __global__ void __launch_bounds__(256) gemv_norm_frag_kernel(const void *x_, const void *g_,
-                                                             uint16_t *nfrag, int rows, int64_t K,
-                                                             int64_t nch, float eps) {
+                                                             uint16_t *nfrag, uint16_t *nlo,
+                                                             int rows, int64_t K, int64_t nch,
+                                                             float eps) {
     using T = typename Act<WF>::T;
     constexpr bool q4 = WF == WF_Q4;
     __shared__ float partial[8];
@@ -94,8 +96,14 @@ __global__ void __launch_bounds__(256) gemv_norm_frag_kernel(const void *x_, con
             if (q4) {
                 *reinterpret_cast<uint2 *>(nfrag + frag_elem(true, nch, token, k)) = make_uint2(0, 0);
                 *reinterpret_cast<uint2 *>(nfrag + frag_elem(true, nch, token, k + 4)) = make_uint2(0, 0);
+                if (TWO) {
+                    *reinterpret_cast<uint2 *>(nlo + frag_elem(true, nch, token, k)) = make_uint2(0, 0);
+                    *reinterpret_cast<uint2 *>(nlo + frag_elem(true, nch, token, k + 4)) = make_uint2(0, 0);
+                }
             } else {
                 *reinterpret_cast<uint4 *>(nfrag + frag_elem(false, nch, token, k)) = make_uint4(0, 0, 0, 0);
+                if (TWO)
+                    *reinterpret_cast<uint4 *>(nlo + frag_elem(false, nch, token, k)) = make_uint4(0, 0, 0, 0);
             }
         }
         return;
@@ -130,21 +138,29 @@ __global__ void __launch_bounds__(256) gemv_norm_frag_kernel(const void *x_, con
 #pragma unroll
             for (int e = 0; e < 8; ++e) f[e] = 0.f;
         }
+        float r[8];   // residuals v - round(v)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) r[e] = f[e] - to_f32(from_f32<T>(f[e]));
         if (q4) {
             // two runs of 4 consecutive k; each lands in one 8-byte half of a
             // lane's fragment with its elements in order {0, 2, 1, 3}
 #pragma unroll
             for (int run = 0; run < 2; ++run) {
-                T o[4];
-                o[0] = from_f32<T>(f[4 * run + 0]);
-                o[1] = from_f32<T>(f[4 * run + 2]);
-                o[2] = from_f32<T>(f[4 * run + 1]);
-                o[3] = from_f32<T>(f[4 * run + 3]);
+                T o[4], ol[4];
+                const int src[4] = {0, 2, 1, 3};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    o[e] = from_f32<T>(f[4 * run + src[e]]);
+                    ol[e] = from_f32<T>(r[4 * run + src[e]]);
+                }
                 const int64_t base = frag_elem(true, nch, token, k + 4 * run);
                 *reinterpret_cast<uint2 *>(nfrag + base) = *reinterpret_cast<const uint2 *>(o);
+                if (TWO) *reinterpret_cast<uint2 *>(nlo + base) = *reinterpret_cast<const uint2 *>(ol);
             }
         } else {
-            *reinterpret_cast<uint4 *>(nfrag + frag_elem(false, nch, token, k)) = Vec16<T>::pack(f);
+            const int64_t base = frag_elem(false, nch, token, k);
+            *reinterpret_cast<uint4 *>(nfrag + base) = Vec16<T>::pack(f);
+            if (TWO) *reinterpret_cast<uint4 *>(nlo + base) = Vec16<T>::pack(r);
         }
     }
 }
@@ -174,12 +190,15 @@ __device__ __forceinline__ uint32_t word_of(const uint4 &v, int b) {
 // Accumulate RT row tiles (16 weight rows each) x NT token tiles over a
 // range of K for one warp.  For f16/bf16, [c0, c1) are 32-wide chunks; for
 // Q4, [c0, c1) are 128-wide groups (four blocks).
-template <int WF, int RT, int NT, int U>
+// With TWO, the activation operand is given as two fragments (value and
+// rounding residual) and every weight fragment is multiplied by both.
+template <int WF, int RT, int NT, int U, bool TWO>
 __device__ __forceinline__ void warp_accumulate(const void *const (&w)[RT],
                                                 const uint16_t *const (&sc)[RT],
                                                 const int64_t (&row)[RT][2],
                                                 const bool (&rowok)[RT][2], int64_t K,
-                                                const uint4 *__restrict__ bfrag, int64_t nch,
+                                                const uint4 *__restrict__ bfrag,
+                                                const uint4 *__restrict__ bfrag_lo, int64_t nch,
                                                 int64_t c0, int64_t c1, float (&acc)[RT][NT][4]) {
     constexpr bool bf = Act<WF>::bf16;
     const int lane = threadIdx.x & 31, tid = lane & 3;
@@ -188,7 +207,7 @@ __device__ __forceinline__ void warp_accumulate(const void *const (&w)[RT],
 #pragma unroll
         for (int r = 0; r < RT; ++r) W[r] = static_cast<const uint16_t *>(w[r]);
         for (int64_t c = c0; c < c1; c += U) {
-            uint4 a[U][RT][2], b[U][NT];
+            uint4 a[U][RT][2], b[U][NT], bl[U][TWO ? NT : 1];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int64_t cc = c + u;
@@ -201,8 +220,12 @@ __device__ __forceinline__ void warp_accumulate(const void *const (&w)[RT],
                         a[u][r][h] = (ok && rowok[r][h]) ? ptx::ld_stream_v4(W[r] + row[r][h] * K + k)
                                                          : make_uint4(0, 0, 0, 0);
 #pragma unroll
-                for (int n = 0; n < NT; ++n)
+                for (int n = 0; n < NT; ++n) {
                     b[u][n] = (cc < c1) ? __ldg(bfrag + (n * nch + cc) * 32 + lane) : make_uint4(0, 0, 0, 0);
+                    if constexpr (TWO)
+                        bl[u][n] = (cc < c1) ? __ldg(bfrag_lo + (n * nch + cc) * 32 + lane)
+                                             : make_uint4(0, 0, 0, 0);
+                }
             }
 #pragma unroll
             for (int u = 0; u < U; ++u)
@@ -214,6 +237,12 @@ __device__ __forceinline__ void warp_accumulate(const void *const (&w)[RT],
                                            a[u][r][1].y, b[u][n].x, b[u][n].y);
                         ptx::mma_16816<bf>(acc[r][n], a[u][r][0].z, a[u][r][1].z, a[u][r][0].w,
                                            a[u][r][1].w, b[u][n].z, b[u][n].w);
+                        if constexpr (TWO) {
+                            ptx::mma_16816<bf>(acc[r][n], a[u][r][0].x, a[u][r][1].x, a[u][r][0].y,
+                                               a[u][r][1].y, bl[u][n].x, bl[u][n].y);
+                            ptx::mma_16816<bf>(acc[r][n], a[u][r][0].z, a[u][r][1].z, a[u][r][0].w,
+                                               a[u][r][1].w, bl[u][n].z, bl[u][n].w);
+                        }
                     }
         }
     } else {
@@ -242,9 +271,12 @@ __device__ __forceinline__ void warp_accumulate(const void *const (&w)[RT],
                 if (gg >= c1) break;
 #pragma unroll
                 for (int blk = 0; blk < 4; ++blk) {
-                    uint4 b[NT];
+                    uint4 b[NT], bl[TWO ? NT : 1];
 #pragma unroll
-                    for (int n = 0; n < NT; ++n) b[n] = __ldg(bfrag + (n * nch + gg * 4 + blk) * 32 + lane);
+                    for (int n = 0; n < NT; ++n) {
+                        b[n] = __ldg(bfrag + (n * nch + gg * 4 + blk) * 32 + lane);
+                        if constexpr (TWO) bl[n] = __ldg(bfrag_lo + (n * nch + gg * 4 + blk) * 32 + lane);
+                    }
 #pragma unroll
                     for (int r = 0; r < RT; ++r) {
                         uint32_t lo[4], hi[4];
@@ -259,6 +291,10 @@ __device__ __forceinline__ void warp_accumulate(const void *const (&w)[RT],
                             float t[4] = {0.f, 0.f, 0.f, 0.f};
                             ptx::mma_16816<true>(t, lo[0], hi[0], lo[2], hi[2], b[n].x, b[n].y);
                             ptx::mma_16816<true>(t, lo[1], hi[1], lo[3], hi[3], b[n].z, b[n].w);
+                            if constexpr (TWO) {
+                                ptx::mma_16816<true>(t, lo[0], hi[0], lo[2], hi[2], bl[n].x, bl[n].y);
+                                ptx::mma_16816<true>(t, lo[1], hi[1], lo[3], hi[3], bl[n].z, bl[n].w);
+                            }
                             acc[r][n][0] = fmaf(f0, t[0], acc[r][n][0]);
                             acc[r][n][1] = fmaf(f0, t[1], acc[r][n][1]);
                             acc[r][n][2] = fmaf(f1, t[2], acc[r][n][2]);
@@ -274,11 +310,12 @@ __device__ __forceinline__ void warp_accumulate(const void *const (&w)[RT],
 // ---------------------------------------------------------------------------
 // 2. gate/up: h = silu(W_gate n) * (W_up n), written in fragment order for
 //    the down projection.  CTA = kGuTPC tiles x kGuKS warps along K.
-template <int WF, int NT>
+template <int WF, int NT, bool TWO>
 __global__ void __launch_bounds__(256) gemv_gateup_kernel(
     const void *wg, const void *wu, const uint16_t *sg, const uint16_t *su,
-    const uint4 *__restrict__ nfrag, uint16_t *hfrag, int64_t K, int64_t F, int64_t nchK,
-    int64_t nchF, int64_t nunits, unsigned *counters, int ncounters) {
+    const uint4 *__restrict__ nfrag, const uint4 *__restrict__ nfrag_lo, uint16_t *hfrag,
+    uint16_t *hfrag_lo, int64_t K, int64_t F, int64_t nchK, int64_t nchF, int64_t nunits,
+    unsigned *counters, int ncounters) {
     using T = typename Act<WF>::T;
     constexpr bool q4 = WF == WF_Q4;
     constexpr int U = q4 ? 2 : 4;
@@ -311,7 +348,7 @@ __global__ void __launch_bounds__(256) gemv_gateup_kernel(
         for (int n = 0; n < NT; ++n)
 #pragma unroll
             for (int i = 0; i < 4; ++i) acc[r][n][i] = 0.f;
-    warp_accumulate<WF, 2, NT, U>(w, sc, row, rowok, K, nfrag, nchK, c0, c1, acc);
+    warp_accumulate<WF, 2, NT, U, TWO>(w, sc, row, rowok, K, nfrag, nfrag_lo, nchK, c0, c1, acc);
 
     if (ks > 0) {
         float *dst = red[tl][ks - 1][lane];
@@ -342,15 +379,21 @@ __global__ void __launch_bounds__(256) gemv_gateup_kernel(
             const int token = 8 * n + 2 * tid + (i & 1);
             const float hv = silu_f32(acc[0][n][i]) * acc[1][n][i];
             const T t = from_f32<T>(hv);
-            hfrag[frag_elem(q4, nchF, token, feat)] = *reinterpret_cast<const uint16_t *>(&t);
+            const int64_t at = frag_elem(q4, nchF, token, feat);
+            hfrag[at] = *reinterpret_cast<const uint16_t *>(&t);
+            if (TWO) {
+                const T tl = from_f32<T>(hv - to_f32(t));
+                hfrag_lo[at] = *reinterpret_cast<const uint16_t *>(&tl);
+            }
         }
 }
 
 // ---------------------------------------------------------------------------
 // 3. down: y = W_down h.  grid = (feature groups of 64, K splits).
-template <int WF, int NT>
+template <int WF, int NT, bool TWO>
 __global__ void __launch_bounds__(128) gemv_down_kernel(
-    const void *wd, const uint16_t *sd, const uint4 *__restrict__ hfrag, void *y_, float *partials,
+    const void *wd, const uint16_t *sd, const uint4 *__restrict__ hfrag,
+    const uint4 *__restrict__ hfrag_lo, void *y_, float *partials,
     unsigned *counters, int rows, int64_t D, int64_t F, int64_t nchF, int64_t units_per_split) {
     using T = typename Act<WF>::T;
     constexpr bool q4 = WF == WF_Q4;
@@ -378,7 +421,7 @@ __global__ void __launch_bounds__(128) gemv_down_kernel(
     for (int n = 0; n < NT; ++n)
 #pragma unroll
         for (int i = 0; i < 4; ++i) acc[0][n][i] = 0.f;
-    warp_accumulate<WF, 1, NT, U>(w, sc, row, rowok, F, hfrag, nchF, c0, c1, acc);
+    warp_accumulate<WF, 1, NT, U, TWO>(w, sc, row, rowok, F, hfrag, hfrag_lo, nchF, c0, c1, acc);
 
 #pragma unroll
     for (int n = 0; n < NT; ++n)
@@ -433,15 +476,16 @@ Geometry geometry(int64_t rows, int64_t d, int64_t ffn, bool q4) {
 
 size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 
-template <int WF, int NT>
+template <int WF, int NT, bool TWO>
 cudaError_t launch_typed(const void *x, const void *gain, GemvWeights wg, GemvWeights wu,
                          GemvWeights wd, void *y, int rows, int64_t d, int64_t ffn, float eps,
                          const GemvWorkspace &ws, const Geometry &geo, cudaStream_t s) {
     constexpr bool q4 = WF == WF_Q4;
     {
         LaunchScope scope(K_GEMV_NORM, s);
-        gemv_norm_frag_kernel<WF><<<8 * NT, 256, 0, s>>>(x, gain, static_cast<uint16_t *>(ws.nfrag),
-                                                         rows, d, geo.nchK, eps);
+        gemv_norm_frag_kernel<WF, TWO><<<8 * NT, 256, 0, s>>>(
+            x, gain, static_cast<uint16_t *>(ws.nfrag), static_cast<uint16_t *>(ws.nfrag_lo), rows, d,
+            geo.nchK, eps);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
@@ -450,50 +494,75 @@ cudaError_t launch_typed(const void *x, const void *gain, GemvWeights wg, GemvWe
         const int64_t blocks = cdiv(tiles, kGuTPC);
         const int64_t units = q4 ? d / 128 : geo.nchK;
         LaunchScope scope(K_GEMV_GATEUP, s);
-        gemv_gateup_kernel<WF, NT><<<static_cast<unsigned>(blocks), 32 * kGuTPC * kGuKS, 0, s>>>(
+        gemv_gateup_kernel<WF, NT, TWO><<<static_cast<unsigned>(blocks), 32 * kGuTPC * kGuKS, 0, s>>>(
             q4 ? static_cast<const void *>(wg.qs) : wg.w, q4 ? static_cast<const void *>(wu.qs) : wu.w,
-            wg.sc, wu.sc, static_cast<const uint4 *>(ws.nfrag), static_cast<uint16_t *>(ws.hfrag), d,
-            ffn, geo.nchK, geo.nchF, units, ws.counters, static_cast<int>(geo.groups));
+            wg.sc, wu.sc, static_cast<const uint4 *>(ws.nfrag), static_cast<const uint4 *>(ws.nfrag_lo),
+            static_cast<uint16_t *>(ws.hfrag), static_cast<uint16_t *>(ws.hfrag_lo), d, ffn, geo.nchK,
+            geo.nchF, units, ws.counters, static_cast<int>(geo.groups));
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     {
         dim3 grid(static_cast<unsigned>(geo.groups), static_cast<unsigned>(geo.splits));
         LaunchScope scope(K_GEMV_DOWN, s);
-        gemv_down_kernel<WF, NT><<<grid, 32 * kDnTPC, 0, s>>>(
-            q4 ? static_cast<const void *>(wd.qs) : wd.w, wd.sc, static_cast<const uint4 *>(ws.hfrag), y,
-            ws.partials, ws.counters, rows, d, ffn, geo.nchF, geo.ups);
+        gemv_down_kernel<WF, NT, TWO><<<grid, 32 * kDnTPC, 0, s>>>(
+            q4 ? static_cast<const void *>(wd.qs) : wd.w, wd.sc, static_cast<const uint4 *>(ws.hfrag),
+            static_cast<const uint4 *>(ws.hfrag_lo), y, ws.partials, ws.counters, rows, d, ffn, geo.nchF,
+            geo.ups);
         return cudaGetLastError();
     }
 }
 
-}  // namespace
+template <int WF, bool TWO>
+cudaError_t launch_nt(int nt, const void *x, const void *g, GemvWeights wg, GemvWeights wu,
+                      GemvWeights wd, void *y, int rows, int64_t d, int64_t ffn, float eps,
+                      const GemvWorkspace &ws, const Geometry &geo, cudaStream_t s) {
+    return nt == 1 ? launch_typed<WF, 1, TWO>(x, g, wg, wu, wd, y, rows, d, ffn, eps, ws, geo, s)
+                   : launch_typed<WF, 2, TWO>(x, g, wg, wu, wd, y, rows, d, ffn, eps, ws, geo, s);
+}
 
-size_t gemv_workspace_bytes(int64_t rows, int64_t d, int64_t ffn) {
+struct Layout {
+    size_t frag_n, frag_h, partials, counters;
+};
+
+Layout layout(int64_t rows, int64_t d, int64_t ffn) {
     // sized for the Q4 or 16-bit geometry, whichever is larger
     const Geometry a = geometry(rows, d, ffn, false);
     const Geometry b = geometry(rows, d, ffn, (d % 128 == 0) && (ffn % 128 == 0));
     const int64_t splits = a.splits > b.splits ? a.splits : b.splits;
-    const int nt = a.nt;
-    size_t bytes = 0;
-    bytes += align256(static_cast<size_t>(nt) * a.nchK * 32 * 16);
-    bytes += align256(static_cast<size_t>(nt) * a.nchF * 32 * 16);
-    bytes += align256(static_cast<size_t>(splits) * (rows > 16 ? 16 : rows) * d * 4);
-    bytes += align256(static_cast<size_t>(a.groups) * 4);
-    return bytes;
+    Layout l;
+    l.frag_n = align256(static_cast<size_t>(a.nt) * a.nchK * 32 * 16);
+    l.frag_h = align256(static_cast<size_t>(a.nt) * a.nchF * 32 * 16);
+    l.partials = align256(static_cast<size_t>(splits) * (rows > 16 ? 16 : rows) * d * 4);
+    l.counters = align256(static_cast<size_t>(a.groups) * 4);
+    return l;
 }
 
-void gemv_carve(void *base, int64_t rows, int64_t d, int64_t ffn, GemvWorkspace *ws) {
-    const Geometry a = geometry(rows, d, ffn, false);
-    const Geometry b = geometry(rows, d, ffn, (d % 128 == 0) && (ffn % 128 == 0));
-    const int64_t splits = a.splits > b.splits ? a.splits : b.splits;
+}  // namespace
+
+size_t gemv_workspace_bytes(int64_t rows, int64_t d, int64_t ffn, bool two_terms) {
+    const Layout l = layout(rows, d, ffn);
+    const size_t frags = l.frag_n + l.frag_h;
+    return (two_terms ? 2 * frags : frags) + l.partials + l.counters;
+}
+
+void gemv_carve(void *base, int64_t rows, int64_t d, int64_t ffn, bool two_terms, GemvWorkspace *ws) {
+    const Layout l = layout(rows, d, ffn);
     char *p = static_cast<char *>(base);
     ws->nfrag = p;
-    p += align256(static_cast<size_t>(a.nt) * a.nchK * 32 * 16);
+    p += l.frag_n;
     ws->hfrag = p;
-    p += align256(static_cast<size_t>(a.nt) * a.nchF * 32 * 16);
+    p += l.frag_h;
+    ws->nfrag_lo = nullptr;
+    ws->hfrag_lo = nullptr;
+    if (two_terms) {
+        ws->nfrag_lo = p;
+        p += l.frag_n;
+        ws->hfrag_lo = p;
+        p += l.frag_h;
+    }
     ws->partials = reinterpret_cast<float *>(p);
-    p += align256(static_cast<size_t>(splits) * (rows > 16 ? 16 : rows) * d * 4);
+    p += l.partials;
     ws->counters = reinterpret_cast<unsigned *>(p);
 }
 
@@ -503,17 +572,17 @@ cudaError_t launch_gemv_block(int wfmt, const void *x, const void *g, GemvWeight
     if (rows <= 0) return cudaSuccess;
     const Geometry geo = geometry(rows, d, ffn, wfmt == WF_Q4);
     const int r = static_cast<int>(rows);
-    if (geo.nt == 1) {
-        switch (wfmt) {
-            case WF_F16: return launch_typed<WF_F16, 1>(x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s);
-            case WF_BF16: return launch_typed<WF_BF16, 1>(x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s);
-            default: return launch_typed<WF_Q4, 1>(x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s);
-        }
-    }
+    const bool two = ws.nfrag_lo != nullptr;
     switch (wfmt) {
-        case WF_F16: return launch_typed<WF_F16, 2>(x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s);
-        case WF_BF16: return launch_typed<WF_BF16, 2>(x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s);
-        default: return launch_typed<WF_Q4, 2>(x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s);
+        case WF_F16:
+            return two ? launch_nt<WF_F16, true>(geo.nt, x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s)
+                       : launch_nt<WF_F16, false>(geo.nt, x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s);
+        case WF_BF16:
+            return two ? launch_nt<WF_BF16, true>(geo.nt, x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s)
+                       : launch_nt<WF_BF16, false>(geo.nt, x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s);
+        default:
+            return two ? launch_nt<WF_Q4, true>(geo.nt, x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s)
+                       : launch_nt<WF_Q4, false>(geo.nt, x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s);
     }
 }
 

@@ -23,7 +23,7 @@ namespace {
 constexpr int64_t kStaticMaxRows = 16;
 constexpr int64_t kStaticMaxD = 8192;
 constexpr int64_t kStaticMaxFfn = 32768;
-constexpr size_t kStaticScratchBytes = size_t(10) << 20;   // 10 MiB
+constexpr size_t kStaticScratchBytes = size_t(12) << 20;   // 12 MiB
 constexpr int kMaxDevices = 64;
 
 }  // namespace
@@ -69,12 +69,15 @@ extern "C" ffn_status ffn_block_forward_decode_static(const void *x, const void 
                                                       const void *w_down, void *y, int64_t rows,
                                                       int64_t d, int64_t ffn, float eps,
                                                       ffn_dtype dtype, void *stream) {
-    if (!x || !g || !w_gate || !w_up || !w_down || !y) return FFN_ERR_NULL;
+    if (!g || !w_gate || !w_up || !w_down || (rows != 0 && (!x || !y))) return FFN_ERR_NULL;
     if (dtype != FFN_F16 && dtype != FFN_BF16) return FFN_ERR_DTYPE;
     if (rows < 0 || d < 1 || ffn < 1 || d % 8 || ffn % 8) return FFN_ERR_SHAPE;
     if (rows > kStaticMaxRows || d > kStaticMaxD || ffn > kStaticMaxFfn) return FFN_ERR_SHAPE;
+    // same operand precision as ffn_block_forward's defaults: bf16 activations
+    // enter the tensor ops as hi + lo terms, fp16 as one rounding
+    const bool two = dtype == FFN_BF16;
     const int64_t grp = std::max<int64_t>(rows, 1);
-    if (ffn::gemv_workspace_bytes(grp, d, ffn) > kStaticScratchBytes) return FFN_ERR_SHAPE;
+    if (ffn::gemv_workspace_bytes(grp, d, ffn, two) > kStaticScratchBytes) return FFN_ERR_SHAPE;
     const void *ptrs[] = {x, g, w_gate, w_up, w_down, y};
     for (const void *p : ptrs)
         if (!aligned16(p)) return FFN_ERR_ALIGN;
@@ -88,7 +91,7 @@ extern "C" ffn_status ffn_block_forward_decode_static(const void *x, const void 
     void *scratch = static_scratch(&e);
     if (!scratch) return FFN_ERR_CUDA;
     ffn::GemvWorkspace ws;
-    ffn::gemv_carve(scratch, rows, d, ffn, &ws);
+    ffn::gemv_carve(scratch, rows, d, ffn, two, &ws);
     ffn::GemvWeights a{w_gate, nullptr, nullptr}, b{w_up, nullptr, nullptr}, c{w_down, nullptr, nullptr};
     e = ffn::launch_gemv_block(dtype == FFN_BF16 ? 1 : 0, x, g, a, b, c, y, rows, d, ffn, eps, ws,
                                static_cast<cudaStream_t>(stream));
