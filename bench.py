@@ -3,9 +3,11 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 One step = one ffn_block_forward of the prefill workload: 4096 tokens, d=4096,
-ffn=11008, bf16 storage with fp32 accumulation (RMSNorm -> tcgen05 gate/up
-GEMM with the SwiGLU epilogue -> tcgen05 down GEMM), on seeded synthetic
-inputs.  Rank 0 prints one JSON line.  The standalone RMSNorm and SwiGLU
+ffn=11008, bf16 x/g/y and bf16 weight values with fp32 accumulation (RMSNorm ->
+tcgen05 gate/up GEMM with the SwiGLU epilogue -> tcgen05 down GEMM), on seeded
+synthetic inputs.  The weights are re-encoded once, before timing, by
+ffn_prepare_weights (fp16 values of w * 2^8, exact), so the tensor operands are
+fp16; the unprepared bf16 path (hi + lo activation terms) is timed beside it.  Rank 0 prints one JSON line.  The standalone RMSNorm and SwiGLU
 workloads, the bf16 decode block and the Q4 decode block are timed after it
 and reported under "sub".
 
@@ -334,12 +336,17 @@ def run_ours(args):
     cfg = synth.C4_PREFILL_BF16
     inp = synth.make_block_inputs(cfg, seed=rank)
     x, g, wg, wu, wd = (to_dev(inp[k], "bf16", torch, device) for k in ("x", "g", "w_gate", "w_up", "w_down"))
+    # one-time weight preparation (model load), outside the timed region
+    wgp, wup, wdp = (ffn.ffn_prepare_weights(w) for w in (wg, wu, wd))
+    torch.cuda.synchronize()
+    ffn.ffn_device_status()
+    PREP = ffn.FFN_PREPARED_WEIGHTS
     y = torch.empty_like(x)
-    ws = ffn.workspace(ffn.ffn_block_workspace_bytes(cfg.rows, cfg.d, cfg.ffn, torch.bfloat16), device)
+    ws = ffn.workspace(ffn.ffn_block_workspace_bytes(cfg.rows, cfg.d, cfg.ffn, torch.bfloat16, PREP), device)
     stream = torch.cuda.current_stream()
 
     def step(_i):
-        ffn.ffn_block_forward(x, g, wg, wu, wd, eps=cfg.eps, out=y, ws=ws)
+        ffn.ffn_block_forward(x, g, wgp, wup, wdp, eps=cfg.eps, flags=PREP, out=y, ws=ws)
 
     for _ in range(args.warmup):
         step(0)
@@ -387,17 +394,14 @@ def run_ours(args):
     achieved_t = flops_gu / gu_avg_s / 1e12
     roof = {"bound": "tensor", "kernel": "gemm_gateup", "achieved": round(achieved_t, 1), "peak": peak_t,
             "unit": "TFLOP/s", "frac": round(achieved_t / peak_t, 4),
-            "peak_source": f"{peak_src} bf16_tflops_sustained (cuBLAS, seconds-long loop)",
+            "peak_source": f"{peak_src} bf16_tflops_sustained (cuBLAS, seconds-long loop; fp16 dense rate = bf16)",
             "algorithmic_flops_per_launch": flops_gu,
-            "mma_flops_per_launch": 2 * flops_gu,
-            "note": "n and h enter as hi + lo bf16 terms, so the GEMMs issue twice the algorithmic MMA work",
-            "tensor_pipe_frac": round(2 * achieved_t / peak_t, 4),
             "traffic": measured_traffic("gemm_gateup"),
             "traffic_note": "dram read+write bytes per launch from the committed ncu capture"}
     n_dn, ms_dn = res["gemm_down"]
     flops_dn = 2.0 * cfg.rows * cfg.ffn * cfg.d
     extra = {"gemm_down_TFLOPs": round(flops_dn / (ms_dn / n_dn / 1000.0) / 1e12, 1),
-             "gemm_down_tensor_pipe_frac": round(2 * flops_dn / (ms_dn / n_dn / 1000.0) / 1e12 / peak_t, 4),
+             "gemm_down_frac": round(flops_dn / (ms_dn / n_dn / 1000.0) / 1e12 / peak_t, 4),
              "block_TFLOPs": round((flops_gu + flops_dn) / (ms / args.steps / 1000.0) / 1e12, 1)}
 
     # gate/up arms, timed interleaved call by call (each pair shares one
@@ -405,20 +409,23 @@ def run_ours(args):
     # each with n as hi + lo (default for bf16) and as one rounding
     arms = {}
     if rank == 0 and not args.only_main:
-        variants = {"fused_split": ffn.FFN_GATEUP_FUSED, "unfused_split": ffn.FFN_GATEUP_UNFUSED,
-                    "fused_single": ffn.FFN_GATEUP_FUSED | ffn.FFN_ACT_SINGLE,
-                    "unfused_single": ffn.FFN_GATEUP_UNFUSED | ffn.FFN_ACT_SINGLE}
+        variants = {"prepared_fused": PREP | ffn.FFN_GATEUP_FUSED,
+                    "prepared_unfused": PREP | ffn.FFN_GATEUP_UNFUSED,
+                    "bf16_hi_lo_fused": ffn.FFN_GATEUP_FUSED,
+                    "bf16_hi_lo_unfused": ffn.FFN_GATEUP_UNFUSED,
+                    "bf16_single_fused": ffn.FFN_GATEUP_FUSED | ffn.FFN_ACT_SINGLE}
         wss = {k: ffn.workspace(ffn.ffn_block_workspace_bytes(cfg.rows, cfg.d, cfg.ffn, torch.bfloat16, f), device)
                for k, f in variants.items()}
+        wts = {k: ((wgp, wup, wdp) if f & PREP else (wg, wu, wd)) for k, f in variants.items()}
         ev = {k: [] for k in variants}
         for _ in range(3):
             for k, f in variants.items():
-                ffn.ffn_block_forward(x, g, wg, wu, wd, eps=cfg.eps, flags=f, out=y, ws=wss[k])
+                ffn.ffn_block_forward(x, g, *wts[k], eps=cfg.eps, flags=f, out=y, ws=wss[k])
         for _ in range(12):
             for k, f in variants.items():
                 a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 a.record(stream)
-                ffn.ffn_block_forward(x, g, wg, wu, wd, eps=cfg.eps, flags=f, out=y, ws=wss[k])
+                ffn.ffn_block_forward(x, g, *wts[k], eps=cfg.eps, flags=f, out=y, ws=wss[k])
                 b.record(stream)
                 ev[k].append((a, b))
         torch.cuda.synchronize()
@@ -433,7 +440,7 @@ def run_ours(args):
 
     def e2e_step(_i):
         x.copy_(xh, non_blocking=True)
-        ffn.ffn_block_forward(x, g, wg, wu, wd, eps=cfg.eps, out=y, ws=ws)
+        ffn.ffn_block_forward(x, g, wgp, wup, wdp, eps=cfg.eps, flags=PREP, out=y, ws=ws)
         yh.copy_(y, non_blocking=True)
 
     e2e_val = None
@@ -461,8 +468,10 @@ def run_ours(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic, seeded (numpy PCG64, seed = rank): x~N(0,1), g=1+0.1N(0,1), W~N(0,1/fan_in)",
             "config": {"workload": cfg.name, "rows": cfg.rows, "d": cfg.d, "ffn": cfg.ffn, "eps": cfg.eps,
-                       "storage": "bf16", "accumulate": "fp32", "gateup_epilogue": "fused",
-                       "activation_operands": "hi+lo bf16 terms (n and h)",
+                       "storage": "bf16 (x, g, y and the weights' values)", "accumulate": "fp32",
+                       "weights": "re-encoded once before timing by ffn_prepare_weights: fp16 of w*2^8, exact for 2^-25<=|w|<256",
+                       "tensor_operands": "fp16 (n and h one rounding each; h stored x2^-8)",
+                       "gateup_epilogue": "fused",
                        "parallelism": "replicas" if world > 1 else "single",
                        "l2": "inputs larger than L2 (weights 270.5 MB + x 33.5 MB + n/h 124 MB per step)"},
             "roofline": roof, "extra": extra, "gateup_arms_ms": arms,

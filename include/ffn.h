@@ -47,7 +47,8 @@ typedef enum {
     FFN_ERR_ALIAS = 6,      /* an output overlaps an input it may not overlap      */
     FFN_ERR_CUDA = 7,       /* a CUDA runtime call failed                          */
     FFN_ERR_TIMEOUT = 8,    /* a kernel abandoned a bounded wait                   */
-    FFN_ERR_FLAGS = 9       /* contradictory or unknown flag bits                  */
+    FFN_ERR_FLAGS = 9,      /* contradictory or unknown flag bits                  */
+    FFN_ERR_RANGE = 10      /* a weight does not fit the prepared (fp16) format    */
 } ffn_status;
 
 typedef enum { FFN_F32 = 0, FFN_F16 = 1, FFN_BF16 = 2 } ffn_dtype;
@@ -74,6 +75,12 @@ typedef enum { FFN_F32 = 0, FFN_F16 = 1, FFN_BF16 = 2 } ffn_dtype;
  * significant bits, at twice the MMA work.  Default for bf16 (and Q4);
  * opt-in for fp16, whose 11 bits already fit the budget.                    */
 #define FFN_ACT_SPLIT 32u
+/* 16-bit paths: w_gate, w_up and w_down hold ffn_prepare_weights output (fp16
+ * values of w * 2^8) while x, g and y keep `dtype`.  n and h enter every
+ * tensor op as one fp16 rounding (11 significant bits; h is stored times
+ * 2^-8, which keeps it clear of fp16 overflow up to |h| ~ 1.6e7), at single-
+ * term speed.  Not combinable with FFN_ACT_SPLIT or FFN_F32.               */
+#define FFN_PREPARED_WEIGHTS 64u
 
 /* ------------------------------------------------------------------------
  * ffn_rmsnorm -- n[r,c] = x[r,c] * rsqrt(ms_r + eps) * g[c],
@@ -153,8 +160,9 @@ ffn_status ffn_block_q4_workspace_bytes(int64_t rows, int64_t d, int64_t ffn, si
  *   x [rows x d] bf16, g [d] bf16, y [rows x d] bf16; w_gate/w_up are Q4
  *   [ffn x d], w_down is Q4 [d x ffn].  Needs d % 128 == 0, ffn % 128 == 0,
  *   Rows are processed in groups of up to 16; each group streams the weights
- *   once.  flags: FFN_AUTO (activations as hi + lo terms), FFN_ACT_SINGLE or
- *   FFN_ACT_SPLIT.  The workspace query covers either.
+ *   once.  The codes (u - 8) are exact in fp16, so the MMAs run on fp16:
+ *   activations enter as one fp16 rounding (h stored times 2^-8).  flags
+ *   must be FFN_AUTO.
  * ---------------------------------------------------------------------- */
 ffn_status ffn_block_forward_q4(const void *x, const void *g, ffn_q4_weight w_gate,
                                 ffn_q4_weight w_up, ffn_q4_weight w_down, void *y, int64_t rows,
@@ -185,6 +193,21 @@ ffn_status ffn_block_forward_decode_static(const void *x, const void *g, const v
                                            int64_t rows, int64_t d, int64_t ffn, float eps,
                                            ffn_dtype dtype, void *stream);
 
+/* ------------------------------------------------------------------------
+ * ffn_prepare_weights -- one-time re-encoding of a weight matrix for
+ * FFN_PREPARED_WEIGHTS: dst[i] = fp16(src[i] * 2^8), round to nearest even.
+ * No page describes this step; it exists because the tensor-core instruction
+ * needs both operands in one type and fp16 keeps 11 significant bits of the
+ * activations where bf16 keeps 8.  For bf16 src every value with
+ * 2^-25 <= |w| < 256 is represented exactly; smaller ones round by at most
+ * 2^-33 absolute; |w| >= 255.9375 becomes infinite and FFN_ERR_RANGE is
+ * recorded in the device status word (see ffn_device_status).
+ *   src: `count` device values of src_dtype (FFN_BF16 or FFN_F16);
+ *   dst: `count` device fp16 values (may equal src, then in place).
+ * ---------------------------------------------------------------------- */
+ffn_status ffn_prepare_weights(const void *src, void *dst, int64_t count, ffn_dtype src_dtype,
+                               void *stream);
+
 /* Host helper (not on the hot path): pack int8 q [out x in] (values -8..7) and
  * fp16 scale bits [out x in/32] into the device layout above.  Host pointers;
  * qs_out holds out*in/2 bytes, scales_out out*in/32 entries.  in % 128 == 0. */
@@ -195,8 +218,9 @@ ffn_status ffn_q4_pack_host(const int8_t *q, const uint16_t *scales, int64_t out
 const char *ffn_status_string(ffn_status status);
 
 /* Synchronises the current device, then returns and clears the device status
- * word: FFN_OK, or FFN_ERR_TIMEOUT if a kernel abandoned a bounded wait since
- * the last call, or FFN_ERR_CUDA if the synchronisation itself failed. */
+ * word: FFN_OK; FFN_ERR_TIMEOUT if a kernel abandoned a bounded wait since
+ * the last call; else FFN_ERR_RANGE if ffn_prepare_weights met a weight out
+ * of range; FFN_ERR_CUDA if the synchronisation itself failed. */
 ffn_status ffn_device_status(void);
 
 /* Number of kernels this library has launched since it was loaded (host count). */

@@ -40,7 +40,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings(lib):
-    for code in range(10):
+    for code in range(11):
         s = lib.ffn_status_string(code).decode()
         assert s and s != "unknown status"
     assert lib.ffn_status_string(99).decode() == "unknown status"
@@ -130,3 +130,19 @@ def test_kernel_names(lib):
     n = lib.ffn_kernel_kinds()
     names = [lib.ffn_kernel_name(k).decode() for k in range(n)]
     assert "gemm_gateup" in names and "rmsnorm" in names and len(set(names)) == n
+
+
+def test_prepare_weights_rejects_before_launch(lib):
+    p = ctypes.c_void_p(4096)
+    assert lib.ffn_prepare_weights(None, p, 8, _lib.FFN_BF16, None) == _lib.FFN_ERR_NULL
+    assert lib.ffn_prepare_weights(p, ctypes.c_void_p(1 << 20), 8, _lib.FFN_F32, None) == _lib.FFN_ERR_DTYPE
+    assert lib.ffn_prepare_weights(p, ctypes.c_void_p(1 << 20), -1, _lib.FFN_BF16, None) == _lib.FFN_ERR_SHAPE
+    assert lib.ffn_prepare_weights(p, ctypes.c_void_p(4096 + 16), 64, _lib.FFN_BF16, None) == _lib.FFN_ERR_ALIAS
+    assert lib.ffn_prepare_weights(None, None, 0, _lib.FFN_BF16, None) == _lib.FFN_OK
+    out = ctypes.c_size_t(0)
+    flags = _lib.FFN_PREPARED_WEIGHTS
+    assert lib.ffn_block_workspace_bytes(4096, 4096, 11008, _lib.FFN_BF16, flags, ctypes.byref(out)) == 0
+    assert out.value >= 4096 * (4096 + 11008) * 2
+    assert lib.ffn_block_workspace_bytes(8, 64, 64, _lib.FFN_F32, flags, ctypes.byref(out)) == _lib.FFN_ERR_FLAGS
+    assert lib.ffn_block_workspace_bytes(8, 64, 64, _lib.FFN_BF16, flags | _lib.FFN_ACT_SPLIT,
+                                         ctypes.byref(out)) == _lib.FFN_ERR_FLAGS

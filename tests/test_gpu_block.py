@@ -167,3 +167,68 @@ def test_launch_counter_and_timing(ffn):
     assert ffn.ffn_launch_count() - before == 3
     assert set(res) == {"rmsnorm", "gemm_gateup", "gemm_down"}
     assert all(n == 1 and ms > 0 for n, ms in res.values())
+
+
+# ---------------------------------------------------------------- prepared weights
+
+def prepared(ffn, inp):
+    dt = inp["cfg"].dtype
+    x, g = to_dev(inp["x"], dt), to_dev(inp["g"], dt)
+    ws = [ffn.ffn_prepare_weights(to_dev(inp[k], dt)) for k in ("w_gate", "w_up", "w_down")]
+    return x, g, ws
+
+
+def test_prepare_weights_exact_and_range(ffn):
+    import torch
+    rng = np.random.default_rng(7)
+    v = np.concatenate([rng.standard_normal(4093) * 0.02, [255.0, -255.9, 2.0 ** -25, 3e-9, 0.0, -0.0, 1.0]])
+    b = synth.round_to_storage(v, "bf16")
+    w64 = oracle_widen(b)
+    got = ffn.ffn_prepare_weights(to_dev(b, "bf16")).cpu().numpy().astype(np.float64)
+    ref = (w64 * 256.0).astype(np.float16).astype(np.float64)
+    assert np.array_equal(got, ref)
+    exact = np.abs(w64) >= 2.0 ** -25
+    assert np.array_equal(got[exact] / 256.0, w64[exact])
+    ffn.ffn_device_status()
+    big = to_dev(synth.round_to_storage(np.array([1.0, 300.0, 2.0, 3.0, 4.0, 5.0, 6.0, 7.0]), "bf16"), "bf16")
+    out = ffn.ffn_prepare_weights(big)
+    with pytest.raises(ffn.FFNError) as e:
+        ffn.ffn_device_status()
+    assert e.value.status == 10
+    assert torch.isinf(out[1]).item()
+
+
+def oracle_widen(b):
+    from oracle import widen
+    return widen(b, "bf16")
+
+
+@pytest.mark.parametrize("flags", [0, 2])
+@pytest.mark.parametrize("rows,d,ffn_", [(300, 512, 704), (128, 256, 128), (17, 1024, 2816),
+                                         (513, 456, 392), (1, 1024, 2816), (8, 520, 4104),
+                                         (16, 2048, 2056)])
+def test_prepared_weights(ffn, oracle_lib, flags, rows, d, ffn_):
+    """fp16 operands (weights prepared once): tcgen05 path for rows > 16, the
+    weight-streaming path for rows <= 16."""
+    cfg = synth.BlockConfig("t", rows, d, ffn_, 1e-6, "bf16")
+    inp = synth.make_block_inputs(cfg, seed=rows + d + 1)
+    x, g, (wg, wu, wd) = prepared(ffn, inp)
+    y = ffn.ffn_block_forward(x, g, wg, wu, wd, eps=cfg.eps, flags=ffn.FFN_PREPARED_WEIGHTS | flags)
+    assert y.dtype == x.dtype
+    assert_lowp(to_host64(y), oracle_lib.block_from_inputs(inp))
+
+
+def test_prepared_weights_full_size_sampled(ffn, oracle_lib):
+    """4096 x 4096 -> 11008 with prepared weights (the benchmark's timed path)."""
+    inp = synth.make_block_inputs(synth.C4_PREFILL_BF16, seed=0)
+    x, g, (wg, wu, wd) = prepared(ffn, inp)
+    y = to_host64(ffn.ffn_block_forward(x, g, wg, wu, wd, eps=inp["cfg"].eps, flags=ffn.FFN_PREPARED_WEIGHTS))
+    rows = np.unique(np.concatenate([[0, 127, 128, 4095], np.random.default_rng(3).integers(0, 4096, 28)]))
+    assert_lowp(y[rows], oracle_lib.block_from_inputs(inp, rows=rows))
+
+
+def test_prepared_decode_full_size(ffn, oracle_lib):
+    inp = synth.make_block_inputs(synth.C3_DECODE_BF16, seed=0)
+    x, g, (wg, wu, wd) = prepared(ffn, inp)
+    y = ffn.ffn_block_forward(x, g, wg, wu, wd, eps=inp["cfg"].eps, flags=ffn.FFN_PREPARED_WEIGHTS)
+    assert_lowp(to_host64(y), oracle_lib.block_from_inputs(inp))

@@ -18,13 +18,14 @@ c_void_p, c_int64, c_float, c_int, c_uint32, c_size_t = (
 STATUS = {
     0: "FFN_OK", 1: "FFN_ERR_NULL", 2: "FFN_ERR_SHAPE", 3: "FFN_ERR_DTYPE", 4: "FFN_ERR_ALIGN",
     5: "FFN_ERR_WORKSPACE", 6: "FFN_ERR_ALIAS", 7: "FFN_ERR_CUDA", 8: "FFN_ERR_TIMEOUT",
-    9: "FFN_ERR_FLAGS",
+    9: "FFN_ERR_FLAGS", 10: "FFN_ERR_RANGE",
 }
 FFN_OK, FFN_ERR_NULL, FFN_ERR_SHAPE, FFN_ERR_DTYPE, FFN_ERR_ALIGN = 0, 1, 2, 3, 4
 FFN_ERR_WORKSPACE, FFN_ERR_ALIAS, FFN_ERR_CUDA, FFN_ERR_TIMEOUT, FFN_ERR_FLAGS = 5, 6, 7, 8, 9
+FFN_ERR_RANGE = 10
 FFN_F32, FFN_F16, FFN_BF16 = 0, 1, 2
 FFN_AUTO, FFN_GATEUP_FUSED, FFN_GATEUP_UNFUSED, FFN_PATH_GEMM, FFN_PATH_GEMV = 0, 1, 2, 4, 8
-FFN_ACT_SINGLE, FFN_ACT_SPLIT = 16, 32
+FFN_ACT_SINGLE, FFN_ACT_SPLIT, FFN_PREPARED_WEIGHTS = 16, 32, 64
 
 
 class Q4Weight(ctypes.Structure):
@@ -47,6 +48,7 @@ SIGNATURES = {
     "ffn_block_forward_decode_static": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                                 c_void_p, c_int64, c_int64, c_int64, c_float, c_int,
                                                 c_void_p]),
+    "ffn_prepare_weights": (c_int, [c_void_p, c_void_p, c_int64, c_int, c_void_p]),
     "ffn_q4_pack_host": (c_int, [c_void_p, c_void_p, c_int64, c_int64, c_void_p, c_void_p]),
     "ffn_status_string": (ctypes.c_char_p, [c_int]),
     "ffn_device_status": (c_int, []),

@@ -5,6 +5,9 @@
 //   fp32                      -> SIMT FFMA kernels (TF32 cannot meet 1e-4*rms)
 //   fp16/bf16, rows <= 16     -> weight-streaming decode kernels (gemv.cu)
 //   fp16/bf16, rows >  16     -> RMSNorm + tcgen05 gate/up GEMM + tcgen05 down GEMM
+// Operands of the tensor ops: bf16 activations enter as hi + lo terms unless
+// FFN_ACT_SINGLE; with FFN_PREPARED_WEIGHTS everything runs on fp16 operands
+// (weights re-encoded once by ffn_prepare_weights).
 #include <algorithm>
 #include <atomic>
 #include <cstring>
@@ -73,6 +76,7 @@ struct Plan {
     Path path;
     bool fused;
     bool split_act;    // 16-bit paths: n and h enter the tensor ops as hi + lo terms
+    bool prepared;     // weights are fp16 * 2^8 (ffn_prepare_weights); fp16 operands
     size_t workspace;
 };
 
@@ -90,7 +94,7 @@ ffn_status plan_block(int64_t rows, int64_t d, int64_t ffn, ffn_dtype dt, uint32
     ffn_status st = check_block_shape(rows, d, ffn, dt);
     if (st != FFN_OK) return st;
     const uint32_t known = FFN_GATEUP_FUSED | FFN_GATEUP_UNFUSED | FFN_PATH_GEMM | FFN_PATH_GEMV |
-                           FFN_ACT_SINGLE | FFN_ACT_SPLIT;
+                           FFN_ACT_SINGLE | FFN_ACT_SPLIT | FFN_PREPARED_WEIGHTS;
     if (flags & ~known) return FFN_ERR_FLAGS;
     if ((flags & FFN_GATEUP_FUSED) && (flags & FFN_GATEUP_UNFUSED)) return FFN_ERR_FLAGS;
     if ((flags & FFN_PATH_GEMM) && (flags & FFN_PATH_GEMV)) return FFN_ERR_FLAGS;
@@ -99,7 +103,10 @@ ffn_status plan_block(int64_t rows, int64_t d, int64_t ffn, ffn_dtype dt, uint32
     // bf16 keeps 8 significant bits: rounding n and h once each costs more
     // than the block's error budget allows, so by default they enter the
     // tensor ops as hi + lo (about 16 bits).
-    plan->split_act = (flags & FFN_ACT_SPLIT) || (dt == FFN_BF16 && !(flags & FFN_ACT_SINGLE));
+    plan->prepared = (flags & FFN_PREPARED_WEIGHTS) != 0;
+    if (plan->prepared && (dt == FFN_F32 || (flags & FFN_ACT_SPLIT))) return FFN_ERR_FLAGS;
+    plan->split_act = !plan->prepared &&
+                      ((flags & FFN_ACT_SPLIT) || (dt == FFN_BF16 && !(flags & FFN_ACT_SINGLE)));
     if (dt == FFN_F32) {
         if (flags & (FFN_PATH_GEMM | FFN_PATH_GEMV)) return FFN_ERR_FLAGS;
         plan->path = PATH_SIMT;
@@ -120,7 +127,7 @@ ffn_status plan_block(int64_t rows, int64_t d, int64_t ffn, ffn_dtype dt, uint32
         case PATH_GEMV:
             plan->workspace = rows == 0 ? 0 : gemv_workspace_bytes(rows, d, ffn, plan->split_act);
             break;
-        case PATH_GEMM:
+        case PATH_GEMM:   // n and h (and their residuals); both 2 bytes when prepared
             plan->workspace = align256(r * d * es) + align256(r * ffn * es);
             if (plan->split_act) plan->workspace += align256(r * d * es) + align256(r * ffn * es);
             if (!plan->fused) plan->workspace += 2 * align256(r * ffn * 4);
@@ -136,7 +143,7 @@ ffn_status from_cuda(cudaError_t e) { return e == cudaSuccess ? FFN_OK : FFN_ERR
 // ------------------------------------------------------------ shared helpers
 const char *kernel_name(int kind) {
     static const char *names[K_NUM_KINDS] = {
-        "rmsnorm", "swiglu", "simt_gateup", "simt_down", "gemv_norm",
+        "prepare", "rmsnorm", "swiglu", "simt_gateup", "simt_down", "gemv_norm",
         "gemv_gateup", "gemv_down", "gemm_gateup", "gemm_down"};
     return (kind >= 0 && kind < K_NUM_KINDS) ? names[kind] : "unknown";
 }
@@ -200,6 +207,7 @@ const char *ffn_status_string(ffn_status s) {
         case FFN_ERR_CUDA: return "a CUDA runtime call failed";
         case FFN_ERR_TIMEOUT: return "a kernel abandoned a bounded wait";
         case FFN_ERR_FLAGS: return "contradictory or unknown flags";
+        case FFN_ERR_RANGE: return "a weight is outside the prepared format's range";
     }
     return "unknown status";
 }
@@ -286,8 +294,9 @@ ffn_status ffn_block_forward(const void *x, const void *g, const void *w_gate, c
             GemvWorkspace gw;
             gemv_carve(workspace, rows, d, ffn, plan.split_act, &gw);
             GemvWeights a{w_gate, nullptr, nullptr}, b{w_up, nullptr, nullptr}, c{w_down, nullptr, nullptr};
-            return from_cuda(launch_gemv_block(dtype == FFN_BF16 ? 1 : 0, x, g, a, b, c, y, rows, d,
-                                               ffn, eps, gw, s));
+            const int wf = plan.prepared ? (dtype == FFN_BF16 ? WF_F16P : WF_F16)
+                                         : (dtype == FFN_BF16 ? WF_BF16 : WF_F16);
+            return from_cuda(launch_gemv_block(wf, x, g, a, b, c, y, rows, d, ffn, eps, gw, s));
         }
         case PATH_GEMM: {
             const size_t nb = align256(static_cast<size_t>(rows) * d * es);
@@ -308,21 +317,32 @@ ffn_status ffn_block_forward(const void *x, const void *g, const void *w_gate, c
                 h_lo = p;
                 p += hb;
             }
-            cudaError_t e = plan.split_act ? launch_rmsnorm_split(x, g, n, n_lo, rows, d, eps, dtype, s)
-                                           : launch_rmsnorm(x, g, n, rows, d, eps, dtype, s);
+            // prepared weights: fp16 operands; the weights' 2^8 is undone on
+            // G and U, h is stored times 2^-8 and the two cancel in the down GEMM
+            const int op = plan.prepared ? DT_F16 : dtype;
+            const float w_unscale = plan.prepared ? 1.f / kPreparedScale : 1.f;
+            const float h_scale = plan.prepared ? 1.f / 256.f : 1.f;
+            cudaError_t e;
+            if (plan.prepared)
+                e = launch_rmsnorm_to_f16(x, g, n, rows, d, eps, dtype, s);
+            else if (plan.split_act)
+                e = launch_rmsnorm_split(x, g, n, n_lo, rows, d, eps, dtype, s);
+            else
+                e = launch_rmsnorm(x, g, n, rows, d, eps, dtype, s);
             if (e != cudaSuccess) return FFN_ERR_CUDA;
             if (plan.fused) {
-                e = launch_gemm_gateup(dtype, n, n_lo, w_gate, w_up, h, h_lo, nullptr, nullptr, rows, d,
-                                       ffn, true, s);
+                e = launch_gemm_gateup(op, n, n_lo, w_gate, w_up, h, h_lo, nullptr, nullptr, rows, d,
+                                       ffn, true, w_unscale, h_scale, s);
             } else {
                 float *G = reinterpret_cast<float *>(p);
                 float *U = reinterpret_cast<float *>(p + align256(static_cast<size_t>(rows) * ffn * 4));
-                e = launch_gemm_gateup(dtype, n, n_lo, w_gate, w_up, nullptr, nullptr, G, U, rows, d, ffn,
-                                       false, s);
-                if (e == cudaSuccess) e = launch_swiglu_f32in(G, U, h, h_lo, rows * ffn, dtype, s);
+                e = launch_gemm_gateup(op, n, n_lo, w_gate, w_up, nullptr, nullptr, G, U, rows, d, ffn,
+                                       false, w_unscale, 1.f, s);
+                if (e == cudaSuccess) e = launch_swiglu_f32in(G, U, h, h_lo, rows * ffn, op, h_scale, s);
             }
             if (e != cudaSuccess) return FFN_ERR_CUDA;
-            return from_cuda(launch_gemm_plain(dtype, h, h_lo, w_down, y, rows, ffn, d, s));
+            return from_cuda(launch_gemm_plain(op, dtype, h, h_lo, w_down, y, rows, ffn, d,
+                                               w_unscale / h_scale, s));
         }
     }
     return FFN_ERR_SHAPE;
@@ -332,8 +352,7 @@ ffn_status ffn_block_q4_workspace_bytes(int64_t rows, int64_t d, int64_t ffn, si
     if (!bytes) return FFN_ERR_NULL;
     if (rows < 0 || d < 128 || ffn < 128 || d % 128 || ffn % 128) return FFN_ERR_SHAPE;
     if (rows > INT32_MAX || d > INT32_MAX || ffn > INT32_MAX) return FFN_ERR_SHAPE;
-    // sized for two-term activations (enough for either flag)
-    *bytes = rows == 0 ? 0 : gemv_workspace_bytes(std::min<int64_t>(rows, kGemvMaxRows), d, ffn, true);
+    *bytes = rows == 0 ? 0 : gemv_workspace_bytes(std::min<int64_t>(rows, kGemvMaxRows), d, ffn, false);
     return FFN_OK;
 }
 
@@ -344,9 +363,7 @@ ffn_status ffn_block_forward_q4(const void *x, const void *g, ffn_q4_weight w_ga
     if (!g || !w_gate.qs || !w_gate.scales || !w_up.qs || !w_up.scales || !w_down.qs ||
         !w_down.scales || (rows != 0 && (!x || !y)))
         return FFN_ERR_NULL;
-    if ((flags & ~(FFN_ACT_SINGLE | FFN_ACT_SPLIT)) || (flags == (FFN_ACT_SINGLE | FFN_ACT_SPLIT)))
-        return FFN_ERR_FLAGS;
-    const bool two = !(flags & FFN_ACT_SINGLE);
+    if (flags != FFN_AUTO) return FFN_ERR_FLAGS;
     size_t need = 0;
     ffn_status st = ffn_block_q4_workspace_bytes(rows, d, ffn, &need);
     if (st != FFN_OK) return st;
@@ -370,14 +387,14 @@ ffn_status ffn_block_forward_q4(const void *x, const void *g, ffn_q4_weight w_ga
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int64_t grp = std::min<int64_t>(rows, kGemvMaxRows);
     GemvWorkspace gw;
-    gemv_carve(workspace, grp, d, ffn, two, &gw);
+    gemv_carve(workspace, grp, d, ffn, false, &gw);
     GemvWeights a{nullptr, w_gate.qs, w_gate.scales}, b{nullptr, w_up.qs, w_up.scales},
         c{nullptr, w_down.qs, w_down.scales};
     for (int64_t r0 = 0; r0 < rows; r0 += kGemvMaxRows) {
         const int64_t nr = std::min<int64_t>(kGemvMaxRows, rows - r0);
         const char *xr = static_cast<const char *>(x) + r0 * d * 2;
         char *yr = static_cast<char *>(y) + r0 * d * 2;
-        cudaError_t e = launch_gemv_block(2, xr, g, a, b, c, yr, nr, d, ffn, eps, gw, s);
+        cudaError_t e = launch_gemv_block(WF_Q4, xr, g, a, b, c, yr, nr, d, ffn, eps, gw, s);
         if (e != cudaSuccess) return FFN_ERR_CUDA;
     }
     return FFN_OK;
@@ -416,7 +433,20 @@ ffn_status ffn_device_status(void) {
         const unsigned zero = 0;
         if (cudaMemcpyToSymbol(g_ffn_status_word, &zero, sizeof(zero)) != cudaSuccess) return FFN_ERR_CUDA;
     }
-    return (word & DEVERR_TIMEOUT) ? FFN_ERR_TIMEOUT : FFN_OK;
+    if (word & DEVERR_TIMEOUT) return FFN_ERR_TIMEOUT;
+    return (word & DEVERR_RANGE) ? FFN_ERR_RANGE : FFN_OK;
+}
+
+ffn_status ffn_prepare_weights(const void *src, void *dst, int64_t count, ffn_dtype src_dtype,
+                               void *stream) {
+    if (count != 0 && (!src || !dst)) return FFN_ERR_NULL;
+    if (src_dtype != FFN_BF16 && src_dtype != FFN_F16) return FFN_ERR_DTYPE;
+    if (count < 0) return FFN_ERR_SHAPE;
+    if (count == 0) return FFN_OK;
+    if (!aligned16(src) || !aligned16(dst)) return FFN_ERR_ALIGN;
+    const size_t bytes = static_cast<size_t>(count) * 2;
+    if (overlaps({src, bytes}, {dst, bytes}) && src != dst) return FFN_ERR_ALIAS;
+    return from_cuda(launch_prepare_weights(src, dst, count, src_dtype, static_cast<cudaStream_t>(stream)));
 }
 
 ffn_status ffn_timing_enable(int on) {

@@ -16,7 +16,8 @@ enum DType : int { DT_F32 = 0, DT_F16 = 1, DT_BF16 = 2 };
 
 // Kernel kinds, for launch counting and event timing.
 enum KernelKind : int {
-    K_RMSNORM = 0,
+    K_PREPARE = 0,
+    K_RMSNORM,
     K_SWIGLU,
     K_SIMT_GATEUP,
     K_SIMT_DOWN,
@@ -39,8 +40,11 @@ struct LaunchScope {
     ~LaunchScope();
 };
 
-// Device status word bits (written by kernels with bounded waits).
-enum : unsigned { DEVERR_TIMEOUT = 1u };
+// Device status word bits (bounded waits that gave up; weights out of range).
+enum : unsigned { DEVERR_TIMEOUT = 1u, DEVERR_RANGE = 2u };
+
+// Prepared weights are fp16 values of w * 2^8 (exact for 2^-25 <= |w| < 256).
+constexpr float kPreparedScale = 256.0f;
 unsigned *device_status_word();   // device address, for the current device
 int sm_count();                   // multiprocessors on the current device
 
@@ -51,13 +55,19 @@ cudaError_t launch_rmsnorm(const void *x, const void *g, void *n, int64_t rows, 
 // n_hi = round(v), n_lo = round(v - n_hi), so n_hi + n_lo carries ~16 bits.
 cudaError_t launch_rmsnorm_split(const void *x, const void *g, void *n_hi, void *n_lo,
                                  int64_t rows, int64_t d, float eps, int dt, cudaStream_t s);
+// 16-bit x and g of type dt_in, n written as fp16 (operand of fp16 tensor ops).
+cudaError_t launch_rmsnorm_to_f16(const void *x, const void *g, void *n, int64_t rows, int64_t d,
+                                  float eps, int dt_in, cudaStream_t s);
+// dst[i] = fp16(src[i] * 2^8) for 16-bit src of type dt; out-of-range values
+// set DEVERR_RANGE in the device status word.
+cudaError_t launch_prepare_weights(const void *src, void *dst, int64_t count, int dt, cudaStream_t s);
 cudaError_t launch_swiglu(const void *gate, const void *up, void *h, int64_t count, int dt,
                           cudaStream_t s);
 
-// fp32 G, U -> 16-bit h, and its residual h_lo when non-null (unfused arm of
-// the tensor-core path)
+// fp32 G, U -> 16-bit h = silu(G) * U * out_scale, and its residual h_lo
+// when non-null (unfused arm of the tensor-core path)
 cudaError_t launch_swiglu_f32in(const float *gate, const float *up, void *h, void *h_lo,
-                                int64_t count, int dt, cudaStream_t s);
+                                int64_t count, int dt, float out_scale, cudaStream_t s);
 
 // fp32 SIMT block: n (rows x d) and h (rows x ffn) are fp32 scratch.
 cudaError_t launch_simt_block(const float *x, const float *g, const float *wg, const float *wu,
@@ -75,7 +85,9 @@ struct GemvWorkspace {
 };
 size_t gemv_workspace_bytes(int64_t rows, int64_t d, int64_t ffn, bool two_terms);
 void gemv_carve(void *base, int64_t rows, int64_t d, int64_t ffn, bool two_terms, GemvWorkspace *ws);
-// wfmt: 0 f16, 1 bf16, 2 q4 (then activations are bf16)
+// wfmt: 0 f16, 1 bf16, 2 q4 (bf16 x/y, fp16 operands), 3 prepared fp16 weights
+// (bf16 x/y, fp16 operands)
+enum { WF_F16 = 0, WF_BF16 = 1, WF_Q4 = 2, WF_F16P = 3 };
 struct GemvWeights {
     const void *w;          // f16/bf16 [out x in]
     const uint8_t *qs;      // q4 device layout
@@ -87,15 +99,19 @@ cudaError_t launch_gemv_block(int wfmt, const void *x, const void *g, GemvWeight
 
 // Prefill tensor-core GEMMs (tcgen05 + TMEM + TMA).
 //   gate/up: A = n [M x K] (plus its residual A_lo, or nullptr), B = W_gate,
-//            W_up [F x K]; fused -> h [M x F] (plus residual H_lo if non-null);
-//            unfused -> G, U [M x F] fp32 each
+//            W_up [F x K]; G, U = accumulator * acc_scale;
+//            fused -> h = silu(G) U out_scale [M x F] (plus residual H_lo if
+//            non-null); unfused -> G, U [M x F] fp32 each
 //   down:    A = h [M x F] (plus residual A_lo, or nullptr), B = W_down [N x F]
-//            -> C [M x N]
+//            -> C = accumulator * acc_scale [M x N] stored as dt_out
+// dt: the operand type (bf16 or fp16); h has the operand type.
 cudaError_t launch_gemm_gateup(int dt, const void *A, const void *A_lo, const void *Wg,
                                const void *Wu, void *H, void *H_lo, void *G, void *U, int64_t M,
-                               int64_t K, int64_t F, bool fused, cudaStream_t s);
-cudaError_t launch_gemm_plain(int dt, const void *A, const void *A_lo, const void *B, void *C,
-                              int64_t M, int64_t K, int64_t N, cudaStream_t s);
+                               int64_t K, int64_t F, bool fused, float acc_scale, float out_scale,
+                               cudaStream_t s);
+cudaError_t launch_gemm_plain(int dt, int dt_out, const void *A, const void *A_lo, const void *B,
+                              void *C, int64_t M, int64_t K, int64_t N, float acc_scale,
+                              cudaStream_t s);
 
 }  // namespace ffn
 

@@ -62,6 +62,8 @@ struct GemmParams {
     int64_t ldo;              // output row stride in elements
     unsigned *err;
     uint64_t wait_limit_ns;
+    float acc_scale;          // applied to every accumulator value (exact powers of two)
+    float out_scale;          // fused: applied to h before rounding
 };
 
 // Stores 32 values rounded once; with `lo` also the rounding residual
@@ -97,13 +99,16 @@ __device__ __forceinline__ void store_row32_f32(float *dst, int64_t col, int64_t
                 make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
 }
 
-template <int MODE, bool BF16, int A_TERMS>
+// BF16: operand type (bf16 or fp16); OUT_BF16: type of the stored output
+// (plain mode; the fused h has the operand type, it feeds the next GEMM).
+template <int MODE, bool BF16, int A_TERMS, bool OUT_BF16>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a,
                         const __grid_constant__ CUtensorMap map_a2,
                         const __grid_constant__ CUtensorMap map_b0,
                         const __grid_constant__ CUtensorMap map_b1, const GemmParams p) {
     using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
+    using TOut = typename std::conditional<OUT_BF16, __nv_bfloat16, __half>::type;
     constexpr int STAGES = Ring<A_TERMS>::STAGES;
     constexpr uint32_t STAGE_BYTES = Ring<A_TERMS>::STAGE_BYTES;
     extern __shared__ uint8_t smem_raw[];
@@ -258,8 +263,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     ptx::tmem_ld_wait();
                     float v[32];
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-                    if (live) store_row32<T>(out0 + row * p.ldo, nullptr, n_blk * BN + c, p.N, v);
+                    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]) * p.acc_scale;
+                    if (live)
+                        store_row32<TOut>(static_cast<TOut *>(p.out0) + row * p.ldo, nullptr,
+                                          n_blk * BN + c, p.N, v);
                 }
             } else {
 #pragma unroll 1
@@ -273,7 +280,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         float h[32];
 #pragma unroll
                         for (int j = 0; j < 32; ++j)
-                            h[j] = silu_f32(__uint_as_float(rg[j])) * __uint_as_float(ru[j]);
+                            h[j] = silu_f32(__uint_as_float(rg[j]) * p.acc_scale) *
+                                   (__uint_as_float(ru[j]) * p.acc_scale) * p.out_scale;
                         if (live)
                             store_row32<T>(out0 + row * p.ldo, out1 ? out1 + row * p.ldo : nullptr,
                                            col, p.N, h);
@@ -281,8 +289,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         float g[32], u[32];
 #pragma unroll
                         for (int j = 0; j < 32; ++j) {
-                            g[j] = __uint_as_float(rg[j]);
-                            u[j] = __uint_as_float(ru[j]);
+                            g[j] = __uint_as_float(rg[j]) * p.acc_scale;
+                            u[j] = __uint_as_float(ru[j]) * p.acc_scale;
                         }
                         // G and U stay fp32 so that h is rounded exactly
                         // once, as in the fused arm
@@ -353,9 +361,10 @@ bool make_map(CUtensorMap *m, const void *ptr, bool bf16, int64_t inner, int64_t
     return r == CUDA_SUCCESS;
 }
 
-template <int MODE, bool BF16, int A_TERMS>
+template <int MODE, bool BF16, int A_TERMS, bool OUT_BF16 = BF16>
 cudaError_t launch_impl(const void *A, const void *A2, const void *B0, const void *B1, void *out0,
-                        void *out1, int64_t M, int64_t K, int64_t N, int kind, cudaStream_t s) {
+                        void *out1, int64_t M, int64_t K, int64_t N, int kind, float acc_scale,
+                        float out_scale, cudaStream_t s) {
     if (M <= 0) return cudaSuccess;
     constexpr size_t SMEM_BYTES = Ring<A_TERMS>::SMEM_BYTES;
     static int configured_device = -1;
@@ -363,7 +372,7 @@ cudaError_t launch_impl(const void *A, const void *A2, const void *B0, const voi
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (configured_device != dev) {
-        e = cudaFuncSetAttribute(gemm_tcgen05_kernel<MODE, BF16, A_TERMS>,
+        e = cudaFuncSetAttribute(gemm_tcgen05_kernel<MODE, BF16, A_TERMS, OUT_BF16>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(SMEM_BYTES));
         if (e != cudaSuccess) return e;
@@ -394,11 +403,13 @@ cudaError_t launch_impl(const void *A, const void *A2, const void *B0, const voi
     p.ldo = N;
     p.err = device_status_word();
     p.wait_limit_ns = WAIT_LIMIT_NS;
+    p.acc_scale = acc_scale;
+    p.out_scale = out_scale;
     if (!p.err) return cudaErrorUnknown;
     int64_t grid = sm_count();
     if (grid > p.num_tiles) grid = p.num_tiles;
     LaunchScope scope(kind, s);
-    gemm_tcgen05_kernel<MODE, BF16, A_TERMS>
+    gemm_tcgen05_kernel<MODE, BF16, A_TERMS, OUT_BF16>
         <<<static_cast<unsigned>(grid), NUM_THREADS, SMEM_BYTES, s>>>(ma, ma2, mb0, mb1, p);
     return cudaGetLastError();
 }
@@ -407,32 +418,41 @@ cudaError_t launch_impl(const void *A, const void *A2, const void *B0, const voi
 
 cudaError_t launch_gemm_gateup(int dt, const void *A, const void *A_lo, const void *Wg,
                                const void *Wu, void *H, void *H_lo, void *G, void *U, int64_t M,
-                               int64_t K, int64_t F, bool fused, cudaStream_t s) {
+                               int64_t K, int64_t F, bool fused, float acc_scale, float out_scale,
+                               cudaStream_t s) {
     const bool bf = dt == DT_BF16;
     const int k = K_GEMM_GATEUP;
+    const float a = acc_scale, o = out_scale;
     if (A_lo) {
         if (fused)
-            return bf ? launch_impl<MODE_GATEUP_FUSED, true, 2>(A, A_lo, Wg, Wu, H, H_lo, M, K, F, k, s)
-                      : launch_impl<MODE_GATEUP_FUSED, false, 2>(A, A_lo, Wg, Wu, H, H_lo, M, K, F, k, s);
-        return bf ? launch_impl<MODE_GATEUP_SPLIT, true, 2>(A, A_lo, Wg, Wu, G, U, M, K, F, k, s)
-                  : launch_impl<MODE_GATEUP_SPLIT, false, 2>(A, A_lo, Wg, Wu, G, U, M, K, F, k, s);
+            return bf ? launch_impl<MODE_GATEUP_FUSED, true, 2>(A, A_lo, Wg, Wu, H, H_lo, M, K, F, k, a, o, s)
+                      : launch_impl<MODE_GATEUP_FUSED, false, 2>(A, A_lo, Wg, Wu, H, H_lo, M, K, F, k, a, o, s);
+        return bf ? launch_impl<MODE_GATEUP_SPLIT, true, 2>(A, A_lo, Wg, Wu, G, U, M, K, F, k, a, o, s)
+                  : launch_impl<MODE_GATEUP_SPLIT, false, 2>(A, A_lo, Wg, Wu, G, U, M, K, F, k, a, o, s);
     }
     if (fused)
-        return bf ? launch_impl<MODE_GATEUP_FUSED, true, 1>(A, nullptr, Wg, Wu, H, H_lo, M, K, F, k, s)
-                  : launch_impl<MODE_GATEUP_FUSED, false, 1>(A, nullptr, Wg, Wu, H, H_lo, M, K, F, k, s);
-    return bf ? launch_impl<MODE_GATEUP_SPLIT, true, 1>(A, nullptr, Wg, Wu, G, U, M, K, F, k, s)
-              : launch_impl<MODE_GATEUP_SPLIT, false, 1>(A, nullptr, Wg, Wu, G, U, M, K, F, k, s);
+        return bf ? launch_impl<MODE_GATEUP_FUSED, true, 1>(A, nullptr, Wg, Wu, H, H_lo, M, K, F, k, a, o, s)
+                  : launch_impl<MODE_GATEUP_FUSED, false, 1>(A, nullptr, Wg, Wu, H, H_lo, M, K, F, k, a, o, s);
+    return bf ? launch_impl<MODE_GATEUP_SPLIT, true, 1>(A, nullptr, Wg, Wu, G, U, M, K, F, k, a, o, s)
+              : launch_impl<MODE_GATEUP_SPLIT, false, 1>(A, nullptr, Wg, Wu, G, U, M, K, F, k, a, o, s);
 }
 
-cudaError_t launch_gemm_plain(int dt, const void *A, const void *A_lo, const void *B, void *C,
-                              int64_t M, int64_t K, int64_t N, cudaStream_t s) {
-    const bool bf = dt == DT_BF16;
+cudaError_t launch_gemm_plain(int dt, int dt_out, const void *A, const void *A_lo, const void *B,
+                              void *C, int64_t M, int64_t K, int64_t N, float acc_scale,
+                              cudaStream_t s) {
     const int k = K_GEMM_DOWN;
-    if (A_lo)
-        return bf ? launch_impl<MODE_PLAIN, true, 2>(A, A_lo, B, nullptr, C, nullptr, M, K, N, k, s)
-                  : launch_impl<MODE_PLAIN, false, 2>(A, A_lo, B, nullptr, C, nullptr, M, K, N, k, s);
-    return bf ? launch_impl<MODE_PLAIN, true, 1>(A, nullptr, B, nullptr, C, nullptr, M, K, N, k, s)
-              : launch_impl<MODE_PLAIN, false, 1>(A, nullptr, B, nullptr, C, nullptr, M, K, N, k, s);
+    const float a = acc_scale;
+    if (dt == DT_BF16) {
+        if (A_lo) return launch_impl<MODE_PLAIN, true, 2>(A, A_lo, B, nullptr, C, nullptr, M, K, N, k, a, 1.f, s);
+        return launch_impl<MODE_PLAIN, true, 1>(A, nullptr, B, nullptr, C, nullptr, M, K, N, k, a, 1.f, s);
+    }
+    if (dt_out == DT_BF16) {   // fp16 operands, bf16 output (prepared-weights path)
+        if (A_lo)
+            return launch_impl<MODE_PLAIN, false, 2, true>(A, A_lo, B, nullptr, C, nullptr, M, K, N, k, a, 1.f, s);
+        return launch_impl<MODE_PLAIN, false, 1, true>(A, nullptr, B, nullptr, C, nullptr, M, K, N, k, a, 1.f, s);
+    }
+    if (A_lo) return launch_impl<MODE_PLAIN, false, 2>(A, A_lo, B, nullptr, C, nullptr, M, K, N, k, a, 1.f, s);
+    return launch_impl<MODE_PLAIN, false, 1>(A, nullptr, B, nullptr, C, nullptr, M, K, N, k, a, 1.f, s);
 }
 
 }  // namespace ffn

@@ -41,8 +41,6 @@ constexpr int kGuTPC = 2;               // gate/up: 16-feature tiles per CTA
 constexpr int kDnTPC = 4;               // down: 16-feature tiles per CTA (one per warp)
 constexpr int kDnFeat = 16 * kDnTPC;    // features per down CTA
 
-enum { WF_F16 = 0, WF_BF16 = 1, WF_Q4 = 2 };
-
 __host__ __device__ inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // Fragment order of an activation vector of length K for one token:
@@ -69,10 +67,34 @@ __device__ __forceinline__ int64_t frag_elem(bool q4, int64_t nch, int token, in
     return (((token >> 3) * nch + c) * 32 + lane) * 8 + slot;
 }
 
-template <int WF> struct Act;
-template <> struct Act<WF_F16> { using T = __half; static constexpr bool bf16 = false; };
-template <> struct Act<WF_BF16> { using T = __nv_bfloat16; static constexpr bool bf16 = true; };
-template <> struct Act<WF_Q4> { using T = __nv_bfloat16; static constexpr bool bf16 = true; };
+// Per weight format: TIn stores x, g and y; TOp is the MMA operand type of the
+// activation fragments; the weights carry a factor w_scale (undone on the
+// fp32 accumulator) and h is stored times h_scale (undone after the down
+// projection).  All factors are powers of two, so they change no bits.
+template <int WF> struct Fmt;
+template <> struct Fmt<WF_F16> {
+    using TIn = __half; using TOp = __half;
+    static constexpr bool op_bf16 = false;
+    static constexpr float w_unscale = 1.f, h_scale = 1.f;
+};
+template <> struct Fmt<WF_BF16> {
+    using TIn = __nv_bfloat16; using TOp = __nv_bfloat16;
+    static constexpr bool op_bf16 = true;
+    static constexpr float w_unscale = 1.f, h_scale = 1.f;
+};
+// Q4 codes (u - 8) are exact in fp16; activations go in as fp16 (11 bits),
+// h scaled by 2^-8 to keep fp16 clear of overflow.
+template <> struct Fmt<WF_Q4> {
+    using TIn = __nv_bfloat16; using TOp = __half;
+    static constexpr bool op_bf16 = false;
+    static constexpr float w_unscale = 1.f, h_scale = 1.f / 256.f;
+};
+// Prepared weights: fp16 values of w * 2^8.
+template <> struct Fmt<WF_F16P> {
+    using TIn = __nv_bfloat16; using TOp = __half;
+    static constexpr bool op_bf16 = false;
+    static constexpr float w_unscale = 1.f / kPreparedScale, h_scale = 1.f / 256.f;
+};
 
 // ---------------------------------------------------------------------------
 // 1. RMSNorm of <= 16 token rows, written in fragment order.
@@ -83,7 +105,8 @@ __global__ void __launch_bounds__(256) gemv_norm_frag_kernel(const void *x_, con
                                                              uint16_t *nfrag, uint16_t *nlo,
                                                              int rows, int64_t K, int64_t nch,
                                                              float eps) {
-    using T = typename Act<WF>::T;
+    using T = typename Fmt<WF>::TIn;
+    using TO = typename Fmt<WF>::TOp;
     constexpr bool q4 = WF == WF_Q4;
     __shared__ float partial[8];
     const int token = blockIdx.x;
@@ -140,18 +163,18 @@ __global__ void __launch_bounds__(256) gemv_norm_frag_kernel(const void *x_, con
         }
         float r[8];   // residuals v - round(v)
 #pragma unroll
-        for (int e = 0; e < 8; ++e) r[e] = f[e] - to_f32(from_f32<T>(f[e]));
+        for (int e = 0; e < 8; ++e) r[e] = f[e] - to_f32(from_f32<TO>(f[e]));
         if (q4) {
             // two runs of 4 consecutive k; each lands in one 8-byte half of a
             // lane's fragment with its elements in order {0, 2, 1, 3}
 #pragma unroll
             for (int run = 0; run < 2; ++run) {
-                T o[4], ol[4];
+                TO o[4], ol[4];
                 const int src[4] = {0, 2, 1, 3};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    o[e] = from_f32<T>(f[4 * run + src[e]]);
-                    ol[e] = from_f32<T>(r[4 * run + src[e]]);
+                    o[e] = from_f32<TO>(f[4 * run + src[e]]);
+                    ol[e] = from_f32<TO>(r[4 * run + src[e]]);
                 }
                 const int64_t base = frag_elem(true, nch, token, k + 4 * run);
                 *reinterpret_cast<uint2 *>(nfrag + base) = *reinterpret_cast<const uint2 *>(o);
@@ -159,26 +182,27 @@ __global__ void __launch_bounds__(256) gemv_norm_frag_kernel(const void *x_, con
             }
         } else {
             const int64_t base = frag_elem(false, nch, token, k);
-            *reinterpret_cast<uint4 *>(nfrag + base) = Vec16<T>::pack(f);
-            if (TWO) *reinterpret_cast<uint4 *>(nlo + base) = Vec16<T>::pack(r);
+            *reinterpret_cast<uint4 *>(nfrag + base) = Vec16<TO>::pack(f);
+            if (TWO) *reinterpret_cast<uint4 *>(nlo + base) = Vec16<TO>::pack(r);
         }
     }
 }
 
 // ---------------------------------------------------------------------------
 // Q4: one 32-bit word = canonical bytes 4*tid .. 4*tid+3 of a block.
-// Returns (u - 8) as bf16 pairs:
+// Returns (u - 8) as fp16 pairs:
 //   r[0] = (e0, e2), r[1] = (e16, e18), r[2] = (e1, e3), r[3] = (e17, e19)
-// relative to element 4*tid of the block.  0x4300 is bf16 128.0, so
-// 0x4300 | u is exactly 128 + u, and subtracting 136 gives u - 8 exactly.
+// relative to element 4*tid of the block.  0x6400 is fp16 1024.0, whose ulp
+// is 1, so 0x6400 | u is exactly 1024 + u, and subtracting 1032 gives u - 8
+// exactly.
 __device__ __forceinline__ void dequant_word(uint32_t w, uint32_t (&r)[4]) {
-    const __nv_bfloat162 k136 = __floats2bfloat162_rn(136.f, 136.f);
+    const __half2 k1032 = __floats2half2_rn(1032.f, 1032.f);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const uint32_t sh = (i == 0) ? 0 : (i == 1) ? 4 : (i == 2) ? 8 : 12;
-        uint32_t v = ((w >> sh) & 0x000F000Fu) | 0x43004300u;
-        __nv_bfloat162 b = *reinterpret_cast<__nv_bfloat162 *>(&v);
-        b = __hsub2(b, k136);
+        uint32_t v = ((w >> sh) & 0x000F000Fu) | 0x64006400u;
+        __half2 b = *reinterpret_cast<__half2 *>(&v);
+        b = __hsub2(b, k1032);
         r[i] = *reinterpret_cast<uint32_t *>(&b);
     }
 }
@@ -200,7 +224,7 @@ __device__ __forceinline__ void warp_accumulate(const void *const (&w)[RT],
                                                 const uint4 *__restrict__ bfrag,
                                                 const uint4 *__restrict__ bfrag_lo, int64_t nch,
                                                 int64_t c0, int64_t c1, float (&acc)[RT][NT][4]) {
-    constexpr bool bf = Act<WF>::bf16;
+    constexpr bool bf = Fmt<WF>::op_bf16;
     const int lane = threadIdx.x & 31, tid = lane & 3;
     if constexpr (WF != WF_Q4) {
         const uint16_t *W[RT];
@@ -289,11 +313,11 @@ __device__ __forceinline__ void warp_accumulate(const void *const (&w)[RT],
 #pragma unroll
                         for (int n = 0; n < NT; ++n) {
                             float t[4] = {0.f, 0.f, 0.f, 0.f};
-                            ptx::mma_16816<true>(t, lo[0], hi[0], lo[2], hi[2], b[n].x, b[n].y);
-                            ptx::mma_16816<true>(t, lo[1], hi[1], lo[3], hi[3], b[n].z, b[n].w);
+                            ptx::mma_16816<bf>(t, lo[0], hi[0], lo[2], hi[2], b[n].x, b[n].y);
+                            ptx::mma_16816<bf>(t, lo[1], hi[1], lo[3], hi[3], b[n].z, b[n].w);
                             if constexpr (TWO) {
-                                ptx::mma_16816<true>(t, lo[0], hi[0], lo[2], hi[2], bl[n].x, bl[n].y);
-                                ptx::mma_16816<true>(t, lo[1], hi[1], lo[3], hi[3], bl[n].z, bl[n].w);
+                                ptx::mma_16816<bf>(t, lo[0], hi[0], lo[2], hi[2], bl[n].x, bl[n].y);
+                                ptx::mma_16816<bf>(t, lo[1], hi[1], lo[3], hi[3], bl[n].z, bl[n].w);
                             }
                             acc[r][n][0] = fmaf(f0, t[0], acc[r][n][0]);
                             acc[r][n][1] = fmaf(f0, t[1], acc[r][n][1]);
@@ -316,7 +340,7 @@ __global__ void __launch_bounds__(256) gemv_gateup_kernel(
     const uint4 *__restrict__ nfrag, const uint4 *__restrict__ nfrag_lo, uint16_t *hfrag,
     uint16_t *hfrag_lo, int64_t K, int64_t F, int64_t nchK, int64_t nchF, int64_t nunits,
     unsigned *counters, int ncounters) {
-    using T = typename Act<WF>::T;
+    using TO = typename Fmt<WF>::TOp;
     constexpr bool q4 = WF == WF_Q4;
     constexpr int U = q4 ? 2 : 4;
     __shared__ float red[kGuTPC][kGuKS - 1][32][2 * NT * 4];
@@ -377,12 +401,13 @@ __global__ void __launch_bounds__(256) gemv_gateup_kernel(
         for (int i = 0; i < 4; ++i) {
             const int64_t feat = f0 + gq + 8 * (i >> 1);
             const int token = 8 * n + 2 * tid + (i & 1);
-            const float hv = silu_f32(acc[0][n][i]) * acc[1][n][i];
-            const T t = from_f32<T>(hv);
+            constexpr float ws = Fmt<WF>::w_unscale;
+            const float hv = silu_f32(acc[0][n][i] * ws) * (acc[1][n][i] * ws) * Fmt<WF>::h_scale;
+            const TO t = from_f32<TO>(hv);
             const int64_t at = frag_elem(q4, nchF, token, feat);
             hfrag[at] = *reinterpret_cast<const uint16_t *>(&t);
             if (TWO) {
-                const T tl = from_f32<T>(hv - to_f32(t));
+                const TO tl = from_f32<TO>(hv - to_f32(t));
                 hfrag_lo[at] = *reinterpret_cast<const uint16_t *>(&tl);
             }
         }
@@ -395,9 +420,10 @@ __global__ void __launch_bounds__(128) gemv_down_kernel(
     const void *wd, const uint16_t *sd, const uint4 *__restrict__ hfrag,
     const uint4 *__restrict__ hfrag_lo, void *y_, float *partials,
     unsigned *counters, int rows, int64_t D, int64_t F, int64_t nchF, int64_t units_per_split) {
-    using T = typename Act<WF>::T;
+    using T = typename Fmt<WF>::TIn;
     constexpr bool q4 = WF == WF_Q4;
     constexpr int U = q4 ? 2 : 8;
+    constexpr float out_scale = Fmt<WF>::w_unscale / Fmt<WF>::h_scale;
     __shared__ int s_last;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int gq = lane >> 2, tid = lane & 3;
@@ -447,7 +473,7 @@ __global__ void __launch_bounds__(128) gemv_down_kernel(
         float sum = 0.f;
         for (int sp = 0; sp < nsplit; ++sp)
             sum += __ldcg(partials + (static_cast<int64_t>(sp) * rows + token) * D + feat);
-        y[static_cast<int64_t>(token) * D + feat] = from_f32<T>(sum);
+        y[static_cast<int64_t>(token) * D + feat] = from_f32<T>(sum * out_scale);
     }
     if (threadIdx.x == 0) counters[blockIdx.x] = 0u;
 }
@@ -580,9 +606,10 @@ cudaError_t launch_gemv_block(int wfmt, const void *x, const void *g, GemvWeight
         case WF_BF16:
             return two ? launch_nt<WF_BF16, true>(geo.nt, x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s)
                        : launch_nt<WF_BF16, false>(geo.nt, x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s);
-        default:
-            return two ? launch_nt<WF_Q4, true>(geo.nt, x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s)
-                       : launch_nt<WF_Q4, false>(geo.nt, x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s);
+        case WF_Q4:   // fp16 operands: one term is enough
+            return launch_nt<WF_Q4, false>(geo.nt, x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s);
+        default:      // prepared fp16 weights
+            return launch_nt<WF_F16P, false>(geo.nt, x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s);
     }
 }
 

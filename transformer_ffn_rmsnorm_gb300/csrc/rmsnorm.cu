@@ -33,11 +33,13 @@ __device__ __forceinline__ void store_vec(T *hi, T *lo, int64_t i, const float (
 }
 
 // One row per group of WPR warps; each thread holds VPT 16-byte vectors.
-template <typename T, int VPT, int WPR, bool SPLIT>
+// T: storage of x and g; TO: storage of n (same element size).
+template <typename T, typename TO, int VPT, int WPR, bool SPLIT>
 __global__ void __launch_bounds__(256) rmsnorm_reg_kernel(const T *x,
                                                           const T *__restrict__ g,
-                                                          T *n, T *nlo, int64_t rows,
+                                                          TO *n, TO *nlo, int64_t rows,
                                                           int d, float eps) {
+    static_assert(sizeof(T) == sizeof(TO), "input and output element sizes must match");
     constexpr int EPV = 16 / sizeof(T);
     __shared__ float partial[256 / 32];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -75,8 +77,8 @@ __global__ void __launch_bounds__(256) rmsnorm_reg_kernel(const T *x,
     if (!valid) return;
     const float inv = rsqrtf(ss / static_cast<float>(d) + eps);
     const uint4 *gv = reinterpret_cast<const uint4 *>(g);
-    T *nr = n + row * d;
-    T *lr = SPLIT ? nlo + row * d : nullptr;
+    TO *nr = n + row * d;
+    TO *lr = SPLIT ? nlo + row * d : nullptr;
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
         const int vi = (i * WPR + wr) * 32 + lane;
@@ -86,17 +88,17 @@ __global__ void __launch_bounds__(256) rmsnorm_reg_kernel(const T *x,
             Vec16<T>::unpack(gv[vi], gf);
 #pragma unroll
             for (int e = 0; e < EPV; ++e) f[e] = f[e] * inv * gf[e];
-            store_vec<T, EPV, SPLIT>(nr, lr, vi, f);
+            store_vec<TO, EPV, SPLIT>(nr, lr, vi, f);
         }
     }
 }
 
 // Any d (including rows whose length is not a whole number of 16-byte
 // vectors): one CTA per row, scalar loads, two passes over the row.
-template <typename T, bool SPLIT>
+template <typename T, typename TO, bool SPLIT>
 __global__ void __launch_bounds__(256) rmsnorm_generic_kernel(const T *x,
                                                               const T *__restrict__ g,
-                                                              T *n, T *nlo, int64_t rows,
+                                                              TO *n, TO *nlo, int64_t rows,
                                                               int64_t d, float eps) {
     __shared__ float partial[8];
     const int64_t row = blockIdx.x;
@@ -114,40 +116,40 @@ __global__ void __launch_bounds__(256) rmsnorm_generic_kernel(const T *x,
     ss = 0.f;
     for (int w = 0; w < (int)(blockDim.x >> 5); ++w) ss += partial[w];
     const float inv = rsqrtf(ss / static_cast<float>(d) + eps);
-    T *nr = n + row * d;
+    TO *nr = n + row * d;
     for (int64_t c = threadIdx.x; c < d; c += blockDim.x) {
         const float v = to_f32(xr[c]) * inv * to_f32(g[c]);
-        const T hi = from_f32<T>(v);
+        const TO hi = from_f32<TO>(v);
         nr[c] = hi;
-        if constexpr (SPLIT) nlo[row * d + c] = from_f32<T>(v - to_f32(hi));
+        if constexpr (SPLIT) nlo[row * d + c] = from_f32<TO>(v - to_f32(hi));
     }
 }
 
-template <typename T, int VPT, int WPR, bool SPLIT>
+template <typename T, typename TO, int VPT, int WPR, bool SPLIT>
 cudaError_t launch_reg(const void *x, const void *g, void *n, void *nlo, int64_t rows, int d,
                        float eps, cudaStream_t s) {
     const int threads = 256;
     const int rows_per_cta = (threads / 32) / WPR;
     const int64_t blocks = (rows + rows_per_cta - 1) / rows_per_cta;
     LaunchScope scope(K_RMSNORM, s);
-    rmsnorm_reg_kernel<T, VPT, WPR, SPLIT><<<static_cast<unsigned>(blocks), threads, 0, s>>>(
-        static_cast<const T *>(x), static_cast<const T *>(g), static_cast<T *>(n),
-        static_cast<T *>(nlo), rows, d, eps);
+    rmsnorm_reg_kernel<T, TO, VPT, WPR, SPLIT><<<static_cast<unsigned>(blocks), threads, 0, s>>>(
+        static_cast<const T *>(x), static_cast<const T *>(g), static_cast<TO *>(n),
+        static_cast<TO *>(nlo), rows, d, eps);
     return cudaGetLastError();
 }
 
-template <typename T, int WPR, bool SPLIT>
+template <typename T, typename TO, int WPR, bool SPLIT>
 cudaError_t dispatch_vpt(int vpt, const void *x, const void *g, void *n, void *nlo, int64_t rows,
                          int d, float eps, cudaStream_t s) {
     switch (vpt) {
-        case 1: return launch_reg<T, 1, WPR, SPLIT>(x, g, n, nlo, rows, d, eps, s);
-        case 2: return launch_reg<T, 2, WPR, SPLIT>(x, g, n, nlo, rows, d, eps, s);
-        case 4: return launch_reg<T, 4, WPR, SPLIT>(x, g, n, nlo, rows, d, eps, s);
-        default: return launch_reg<T, 8, WPR, SPLIT>(x, g, n, nlo, rows, d, eps, s);
+        case 1: return launch_reg<T, TO, 1, WPR, SPLIT>(x, g, n, nlo, rows, d, eps, s);
+        case 2: return launch_reg<T, TO, 2, WPR, SPLIT>(x, g, n, nlo, rows, d, eps, s);
+        case 4: return launch_reg<T, TO, 4, WPR, SPLIT>(x, g, n, nlo, rows, d, eps, s);
+        default: return launch_reg<T, TO, 8, WPR, SPLIT>(x, g, n, nlo, rows, d, eps, s);
     }
 }
 
-template <typename T, bool SPLIT>
+template <typename T, typename TO, bool SPLIT>
 cudaError_t launch_typed(const void *x, const void *g, void *n, void *nlo, int64_t rows,
                          int64_t d, float eps, cudaStream_t s) {
     constexpr int EPV = 16 / sizeof(T);
@@ -162,16 +164,16 @@ cudaError_t launch_typed(const void *x, const void *g, void *n, void *nlo, int64
         while (vpt < per_thread) vpt <<= 1;
         const int di = static_cast<int>(d);
         switch (wpr) {
-            case 1: return dispatch_vpt<T, 1, SPLIT>(vpt, x, g, n, nlo, rows, di, eps, s);
-            case 2: return dispatch_vpt<T, 2, SPLIT>(vpt, x, g, n, nlo, rows, di, eps, s);
-            case 4: return dispatch_vpt<T, 4, SPLIT>(vpt, x, g, n, nlo, rows, di, eps, s);
-            default: return dispatch_vpt<T, 8, SPLIT>(vpt, x, g, n, nlo, rows, di, eps, s);
+            case 1: return dispatch_vpt<T, TO, 1, SPLIT>(vpt, x, g, n, nlo, rows, di, eps, s);
+            case 2: return dispatch_vpt<T, TO, 2, SPLIT>(vpt, x, g, n, nlo, rows, di, eps, s);
+            case 4: return dispatch_vpt<T, TO, 4, SPLIT>(vpt, x, g, n, nlo, rows, di, eps, s);
+            default: return dispatch_vpt<T, TO, 8, SPLIT>(vpt, x, g, n, nlo, rows, di, eps, s);
         }
     }
     LaunchScope scope(K_RMSNORM, s);
-    rmsnorm_generic_kernel<T, SPLIT><<<static_cast<unsigned>(rows), 256, 0, s>>>(
-        static_cast<const T *>(x), static_cast<const T *>(g), static_cast<T *>(n),
-        static_cast<T *>(nlo), rows, d, eps);
+    rmsnorm_generic_kernel<T, TO, SPLIT><<<static_cast<unsigned>(rows), 256, 0, s>>>(
+        static_cast<const T *>(x), static_cast<const T *>(g), static_cast<TO *>(n),
+        static_cast<TO *>(nlo), rows, d, eps);
     return cudaGetLastError();
 }
 
@@ -181,9 +183,10 @@ cudaError_t launch_rmsnorm(const void *x, const void *g, void *n, int64_t rows, 
                            float eps, int dt, cudaStream_t s) {
     if (rows <= 0) return cudaSuccess;
     switch (dt) {
-        case DT_F32: return launch_typed<float, false>(x, g, n, nullptr, rows, d, eps, s);
-        case DT_F16: return launch_typed<__half, false>(x, g, n, nullptr, rows, d, eps, s);
-        default: return launch_typed<__nv_bfloat16, false>(x, g, n, nullptr, rows, d, eps, s);
+        case DT_F32: return launch_typed<float, float, false>(x, g, n, nullptr, rows, d, eps, s);
+        case DT_F16: return launch_typed<__half, __half, false>(x, g, n, nullptr, rows, d, eps, s);
+        default:
+            return launch_typed<__nv_bfloat16, __nv_bfloat16, false>(x, g, n, nullptr, rows, d, eps, s);
     }
 }
 
@@ -191,8 +194,19 @@ cudaError_t launch_rmsnorm_split(const void *x, const void *g, void *n_hi, void 
                                  int64_t rows, int64_t d, float eps, int dt, cudaStream_t s) {
     if (rows <= 0) return cudaSuccess;
     switch (dt) {
-        case DT_F16: return launch_typed<__half, true>(x, g, n_hi, n_lo, rows, d, eps, s);
-        case DT_BF16: return launch_typed<__nv_bfloat16, true>(x, g, n_hi, n_lo, rows, d, eps, s);
+        case DT_F16: return launch_typed<__half, __half, true>(x, g, n_hi, n_lo, rows, d, eps, s);
+        case DT_BF16:
+            return launch_typed<__nv_bfloat16, __nv_bfloat16, true>(x, g, n_hi, n_lo, rows, d, eps, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_rmsnorm_to_f16(const void *x, const void *g, void *n, int64_t rows, int64_t d,
+                                  float eps, int dt_in, cudaStream_t s) {
+    if (rows <= 0) return cudaSuccess;
+    switch (dt_in) {
+        case DT_F16: return launch_typed<__half, __half, false>(x, g, n, nullptr, rows, d, eps, s);
+        case DT_BF16: return launch_typed<__nv_bfloat16, __half, false>(x, g, n, nullptr, rows, d, eps, s);
         default: return cudaErrorInvalidValue;
     }
 }

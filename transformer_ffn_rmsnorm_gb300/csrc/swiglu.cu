@@ -63,7 +63,7 @@ __global__ void swiglu_tail_kernel(const T *gate, const T *up, T *h, int64_t beg
 // h_lo, also the residual h - round(h), rounded once.
 template <typename T>
 __global__ void __launch_bounds__(256) swiglu_f32in_kernel(const float *gate, const float *up, T *h,
-                                                           T *h_lo, int64_t count) {
+                                                           T *h_lo, int64_t count, float out_scale) {
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     const int64_t nvec = count / 8;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nvec; i += stride) {
@@ -73,6 +73,8 @@ __global__ void __launch_bounds__(256) swiglu_f32in_kernel(const float *gate, co
         float f[8] = {silu_f32(g0.x) * u0.x, silu_f32(g0.y) * u0.y, silu_f32(g0.z) * u0.z,
                       silu_f32(g0.w) * u0.w, silu_f32(g1.x) * u1.x, silu_f32(g1.y) * u1.y,
                       silu_f32(g1.z) * u1.z, silu_f32(g1.w) * u1.w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) f[e] *= out_scale;
         const uint4 hv = Vec16<T>::pack(f);
         __stcs(reinterpret_cast<uint4 *>(h) + i, hv);
         if (h_lo) {
@@ -85,7 +87,7 @@ __global__ void __launch_bounds__(256) swiglu_f32in_kernel(const float *gate, co
     }
     for (int64_t i = nvec * 8 + static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < count;
          i += stride) {
-        const float v = silu_f32(gate[i]) * up[i];
+        const float v = silu_f32(gate[i]) * up[i] * out_scale;
         const T hi = from_f32<T>(v);
         h[i] = hi;
         if (h_lo) h_lo[i] = from_f32<T>(v - to_f32(hi));
@@ -121,24 +123,24 @@ cudaError_t launch_typed(const void *gate, const void *up, void *h, int64_t coun
 
 template <typename T>
 cudaError_t launch_f32in(const float *gate, const float *up, void *h, void *h_lo, int64_t count,
-                         cudaStream_t s) {
+                         float out_scale, cudaStream_t s) {
     const int threads = 256;
     int64_t blocks = static_cast<int64_t>(sm_count()) * 8;
     const int64_t need = (count / 8 + threads - 1) / threads;
     if (blocks > need) blocks = need < 1 ? 1 : need;
     LaunchScope scope(K_SWIGLU, s);
     swiglu_f32in_kernel<T><<<static_cast<unsigned>(blocks), threads, 0, s>>>(
-        gate, up, static_cast<T *>(h), static_cast<T *>(h_lo), count);
+        gate, up, static_cast<T *>(h), static_cast<T *>(h_lo), count, out_scale);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_swiglu_f32in(const float *gate, const float *up, void *h, void *h_lo,
-                                int64_t count, int dt, cudaStream_t s) {
+                                int64_t count, int dt, float out_scale, cudaStream_t s) {
     if (count <= 0) return cudaSuccess;
-    return dt == DT_F16 ? launch_f32in<__half>(gate, up, h, h_lo, count, s)
-                        : launch_f32in<__nv_bfloat16>(gate, up, h, h_lo, count, s);
+    return dt == DT_F16 ? launch_f32in<__half>(gate, up, h, h_lo, count, out_scale, s)
+                        : launch_f32in<__nv_bfloat16>(gate, up, h, h_lo, count, out_scale, s);
 }
 
 cudaError_t launch_swiglu(const void *gate, const void *up, void *h, int64_t count, int dt,

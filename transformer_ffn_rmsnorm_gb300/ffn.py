@@ -17,7 +17,7 @@ import torch
 from . import _lib
 from ._lib import (FFN_AUTO, FFN_BF16, FFN_F16, FFN_F32, FFN_GATEUP_FUSED,  # noqa: F401
                    FFN_GATEUP_UNFUSED, FFN_ACT_SINGLE, FFN_ACT_SPLIT, FFN_PATH_GEMM,
-                   FFN_PATH_GEMV, Q4Weight)
+                   FFN_PATH_GEMV, FFN_PREPARED_WEIGHTS, Q4Weight)
 
 _DT = {torch.float32: FFN_F32, torch.float16: FFN_F16, torch.bfloat16: FFN_BF16}
 
@@ -104,6 +104,16 @@ def ffn_block_forward(x, g, w_gate, w_up, w_down, eps: float, flags: int = 0, ou
                                          _ptr(y), rows, d, ffn, float(eps), _dtype(x), flags,
                                          _ptr(ws), ws.numel(), _stream(stream)), "ffn_block_forward")
     return y
+
+
+def ffn_prepare_weights(w: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """One-time re-encoding of a bf16/fp16 weight for FFN_PREPARED_WEIGHTS
+    (fp16 values of w * 2^8)."""
+    _need_cuda(w, out)
+    dst = torch.empty(w.shape, dtype=torch.float16, device=w.device) if out is None else out
+    _check(_lib.load().ffn_prepare_weights(_ptr(w), _ptr(dst), w.numel(), _dtype(w), _stream(stream)),
+           "ffn_prepare_weights")
+    return dst
 
 
 def ffn_block_q4_workspace_bytes(rows: int, d: int, ffn: int) -> int:
