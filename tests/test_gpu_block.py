@@ -181,7 +181,7 @@ def prepared(ffn, inp):
 def test_prepare_weights_exact_and_range(ffn):
     import torch
     rng = np.random.default_rng(7)
-    v = np.concatenate([rng.standard_normal(4093) * 0.02, [255.0, -255.9, 2.0 ** -25, 3e-9, 0.0, -0.0, 1.0]])
+    v = np.concatenate([rng.standard_normal(4093) * 0.02, [255.0, -254.0, 2.0 ** -25, 3e-9, 0.0, -0.0, 1.0]])
     b = synth.round_to_storage(v, "bf16")
     w64 = oracle_widen(b)
     got = ffn.ffn_prepare_weights(to_dev(b, "bf16")).cpu().numpy().astype(np.float64)
