@@ -45,6 +45,8 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-sub", action="store_true", help="skip the secondary workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU baseline")
+    ap.add_argument("--workload", choices=["prefill", "decode", "decode_prepared", "q4"], default="prefill",
+                    help="prefill: the benchmark; others run only that workload (for profiling)")
     ap.add_argument("--only-main", action="store_true",
                     help="time the main step only (no arm comparison, e2e, sub-workloads or CPU baseline)")
     return ap.parse_args()
@@ -173,6 +175,28 @@ def timed_loop(torch, fn, steps, warmup, stream):
     return e0.elapsed_time(e1)
 
 
+def graph_time_us(torch, fn, calls, replays, stream):
+    """Per-call device time of `fn` with host submission taken out: `calls`
+    calls are captured into one CUDA graph and the graph is replayed."""
+    for i in range(3):
+        fn(i)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for i in range(calls):
+            fn(i)
+    graph.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(replays):
+        graph.replay()
+    e1.record(stream)
+    e1.synchronize()
+    return 1000.0 * e0.elapsed_time(e1) / (calls * replays)
+
+
 def kernel_table(res):
     return {k: {"launches": n, "avg_us": round(1000.0 * ms / n, 3)} for k, (n, ms) in res.items()}
 
@@ -219,54 +243,94 @@ def sub_benchmarks(torch, ffn, device, peaks, peak_src, stream):
                              "peak_source": peak_src + " hbm_gbs (copy, burst)", "algorithmic_bytes": byts}})
     del ga, up, h
 
-    # decode bf16 8 x 4096 x 14336
+    # decode bf16 8 x 4096 x 14336 (352 MB of weights > L2); whole-call time
+    # from CUDA-graph replay, per-kernel event times alongside
+    out.append(decode_bench(torch, ffn, device, hbm, peak_src, stream))
+    out.append(q4_bench(torch, ffn, device, hbm, peak_src, stream))
+    return out
+
+
+def decode_setup(torch, ffn, device, prepared=False):
     cfg = synth.C3_DECODE_BF16
     inp = synth.make_block_inputs(cfg, seed=0)
     args = [to_dev(inp[k], "bf16", torch, device) for k in ("x", "g", "w_gate", "w_up", "w_down")]
+    flags = 0
+    if prepared:
+        args[2:] = [ffn.ffn_prepare_weights(w) for w in args[2:]]
+        flags = ffn.FFN_PREPARED_WEIGHTS
     y = torch.empty_like(args[0])
-    ws = ffn.workspace(ffn.ffn_block_workspace_bytes(cfg.rows, cfg.d, cfg.ffn, torch.bfloat16), device)
-    with ffn.KernelTimer() as kt:
-        ms = timed_loop(torch, lambda i: ffn.ffn_block_forward(*args, eps=cfg.eps, out=y, ws=ws), iters, warm, stream)
-        res = kt.read()
-    wbytes = 3 * cfg.ffn * cfg.d * 2
-    gu = res["gemv_gateup"]
-    gu_us = 1000.0 * gu[1] / gu[0]
-    gu_bytes = 2 * cfg.ffn * cfg.d * 2
-    us = 1000 * ms / iters
-    out.append({"workload": cfg.name, "us_per_call": round(us, 3), "tokens_per_s": round(cfg.rows / us * 1e6, 1),
-                "block_weight_GBps": round(wbytes / us / 1e3, 1), "kernels": kernel_table(res),
-                "roofline": {"bound": "hbm", "kernel": "gemv_gateup", "achieved": round(gu_bytes / gu_us / 1e3, 1),
-                             "peak": hbm, "unit": "GB/s", "frac": round(gu_bytes / gu_us / 1e3 / hbm, 4),
-                             "peak_source": peak_src + " hbm_gbs (copy, burst)", "algorithmic_bytes": gu_bytes}})
-    del args, y, ws
+    ws = ffn.workspace(ffn.ffn_block_workspace_bytes(cfg.rows, cfg.d, cfg.ffn, torch.bfloat16, flags), device)
+    return cfg, (lambda i: ffn.ffn_block_forward(*args, eps=cfg.eps, flags=flags, out=y, ws=ws))
 
-    # Q4 decode 8 x 5120 x 17408, two weight copies rotated (2 x 150 MB > L2)
+
+def decode_bench(torch, ffn, device, hbm, peak_src, stream):
+    res_all = {}
+    for prepared in (False, True):
+        cfg, call = decode_setup(torch, ffn, device, prepared)
+        us = graph_time_us(torch, call, 20, 10, stream)
+        with ffn.KernelTimer() as kt:
+            timed_loop(torch, call, 50, 3, stream)
+            res = kt.read()
+        res_all["prepared" if prepared else "bf16_hi_lo"] = (us, res)
+    wbytes = 3 * cfg.ffn * cfg.d * 2
+    us, res = res_all["bf16_hi_lo"]
+    usp, resp = res_all["prepared"]
+    return {"workload": cfg.name, "us_per_call": round(us, 3), "tokens_per_s": round(cfg.rows / us * 1e6, 1),
+            "timing": "CUDA graph of 20 calls, 10 replays",
+            "kernels_events": kernel_table(res),
+            "prepared_weights": {"us_per_call": round(usp, 3), "tokens_per_s": round(cfg.rows / usp * 1e6, 1),
+                                 "kernels_events": kernel_table(resp)},
+            "roofline": {"bound": "hbm", "kernel": "whole block (3 launches)",
+                         "achieved": round(wbytes / us / 1e3, 1), "peak": hbm, "unit": "GB/s",
+                         "frac": round(wbytes / us / 1e3 / hbm, 4),
+                         "peak_source": peak_src + " hbm_gbs (copy, burst)", "algorithmic_bytes": wbytes}}
+
+
+def q4_setup(torch, ffn, device):
     cfg = synth.C5_DECODE_Q4
     inp = synth.make_q4_inputs(cfg, seed=0)
     xq = to_dev(inp["x"], "bf16", torch, device)
     gq = to_dev(inp["g"], "bf16", torch, device)
     wsets = []
-    for _ in range(2):
+    for _ in range(2):   # two weight copies rotated: 2 x 150 MB > L2
         wsets.append([(torch.from_numpy(inp["qs_" + n]).to(device),
                        torch.from_numpy(inp["sc_" + n].view(np.int16)).to(device)) for n in ("gate", "up", "down")])
     yq = torch.empty_like(xq)
     ws = ffn.workspace(ffn.ffn_block_q4_workspace_bytes(cfg.rows, cfg.d, cfg.ffn), device)
+    return cfg, (lambda i: ffn.ffn_block_forward_q4(xq, gq, *wsets[i % 2], ffn=cfg.ffn, eps=cfg.eps, out=yq, ws=ws))
+
+
+def q4_bench(torch, ffn, device, hbm, peak_src, stream):
+    cfg, call = q4_setup(torch, ffn, device)
+    us = graph_time_us(torch, call, 20, 10, stream)
     with ffn.KernelTimer() as kt:
-        ms = timed_loop(torch, lambda i: ffn.ffn_block_forward_q4(xq, gq, *wsets[i % 2], ffn=cfg.ffn, eps=cfg.eps,
-                                                                  out=yq, ws=ws), iters, warm, stream)
+        timed_loop(torch, call, 50, 3, stream)
         res = kt.read()
     wbytes = 3 * cfg.ffn * cfg.d * 18 // 32
-    gu = res["gemv_gateup"]
-    gu_us = 1000.0 * gu[1] / gu[0]
-    gu_bytes = 2 * cfg.ffn * cfg.d * 18 // 32
-    us = 1000 * ms / iters
-    out.append({"workload": cfg.name, "us_per_call": round(us, 3), "tokens_per_s": round(cfg.rows / us * 1e6, 1),
-                "block_weight_GBps": round(wbytes / us / 1e3, 1), "kernels": kernel_table(res),
-                "l2": "two weight copies rotated",
-                "roofline": {"bound": "hbm", "kernel": "gemv_gateup", "achieved": round(gu_bytes / gu_us / 1e3, 1),
-                             "peak": hbm, "unit": "GB/s", "frac": round(gu_bytes / gu_us / 1e3 / hbm, 4),
-                             "peak_source": peak_src + " hbm_gbs (copy, burst)", "algorithmic_bytes": gu_bytes}})
-    return out
+    return {"workload": cfg.name, "us_per_call": round(us, 3), "tokens_per_s": round(cfg.rows / us * 1e6, 1),
+            "timing": "CUDA graph of 20 calls (two weight copies alternating), 10 replays",
+            "kernels_events": kernel_table(res),
+            "roofline": {"bound": "hbm", "kernel": "whole block (3 launches)",
+                         "achieved": round(wbytes / us / 1e3, 1), "peak": hbm, "unit": "GB/s",
+                         "frac": round(wbytes / us / 1e3 / hbm, 4),
+                         "peak_source": peak_src + " hbm_gbs (copy, burst)", "algorithmic_bytes": wbytes}}
+
+
+def run_workload_only(args):
+    """--workload decode|decode_prepared|q4: run that workload for --warmup +
+    --steps calls and print a short line (used for ncu captures)."""
+    import torch
+    from transformer_ffn_rmsnorm_gb300 import ffn
+    device = torch.device("cuda", 0)
+    if args.workload == "q4":
+        cfg, call = q4_setup(torch, ffn, device)
+    else:
+        cfg, call = decode_setup(torch, ffn, device, prepared=args.workload == "decode_prepared")
+    for i in range(args.warmup + args.steps):
+        call(i)
+    torch.cuda.synchronize()
+    ffn.ffn_device_status()
+    print(json.dumps({"workload": cfg.name, "variant": args.workload, "calls": args.warmup + args.steps}))
 
 
 # ----------------------------------------------------------- CPU baseline
@@ -493,6 +557,8 @@ def main():
         raise SystemExit("--steps must be >= 1 and --warmup >= 0")
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload != "prefill":
+        run_workload_only(args)
     else:
         run_ours(args)
 

@@ -36,16 +36,18 @@
 namespace ffn {
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64, UMMA_K = 16;
+constexpr int BM = 128, BK = 64, UMMA_K = 16;
 constexpr uint32_t A_BYTES = BM * BK * 2;
-constexpr uint32_t B_BYTES = BN * BK * 2;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int NUM_THREADS = 192;
 
 // A_TERMS = 2: the A operand is given as two bf16 matrices whose sum is the
 // fp32 value (hi + lo); both are multiplied by the same B tile and accumulate
 // into the same TMEM accumulator, so A carries ~16 significant bits.
-template <int A_TERMS> struct Ring {
+// BN: accumulator columns per tile (256, or 224 for the plain GEMM when it
+// evens out the waves); the B tile is BN rows of 64 k values.
+template <int A_TERMS, int BN> struct Ring {
+    static constexpr uint32_t B_BYTES = BN * BK * 2;
     static constexpr int STAGES = A_TERMS == 1 ? 4 : 3;
     static constexpr uint32_t STAGE_BYTES = A_TERMS * A_BYTES + B_BYTES;
     static constexpr size_t SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
@@ -101,7 +103,7 @@ __device__ __forceinline__ void store_row32_f32(float *dst, int64_t col, int64_t
 
 // BF16: operand type (bf16 or fp16); OUT_BF16: type of the stored output
 // (plain mode; the fused h has the operand type, it feeds the next GEMM).
-template <int MODE, bool BF16, int A_TERMS, bool OUT_BF16>
+template <int MODE, bool BF16, int A_TERMS, bool OUT_BF16, int BN>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a,
                         const __grid_constant__ CUtensorMap map_a2,
@@ -109,8 +111,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         const __grid_constant__ CUtensorMap map_b1, const GemmParams p) {
     using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
     using TOut = typename std::conditional<OUT_BF16, __nv_bfloat16, __half>::type;
-    constexpr int STAGES = Ring<A_TERMS>::STAGES;
-    constexpr uint32_t STAGE_BYTES = Ring<A_TERMS>::STAGE_BYTES;
+    static_assert(BN % 32 == 0 && BN <= 256 && (MODE == MODE_PLAIN || BN == 256), "tile width");
+    constexpr int STAGES = Ring<A_TERMS, BN>::STAGES;
+    constexpr uint32_t STAGE_BYTES = Ring<A_TERMS, BN>::STAGE_BYTES;
+    constexpr uint32_t B_BYTES = Ring<A_TERMS, BN>::B_BYTES;
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bar_full[STAGES], bar_empty[STAGES];
     __shared__ __align__(8) uint64_t bar_tfull[2], bar_tempty[2], bar_drain;
@@ -361,18 +365,18 @@ bool make_map(CUtensorMap *m, const void *ptr, bool bf16, int64_t inner, int64_t
     return r == CUDA_SUCCESS;
 }
 
-template <int MODE, bool BF16, int A_TERMS, bool OUT_BF16 = BF16>
+template <int MODE, bool BF16, int A_TERMS, bool OUT_BF16 = BF16, int BN = 256>
 cudaError_t launch_impl(const void *A, const void *A2, const void *B0, const void *B1, void *out0,
                         void *out1, int64_t M, int64_t K, int64_t N, int kind, float acc_scale,
                         float out_scale, cudaStream_t s) {
     if (M <= 0) return cudaSuccess;
-    constexpr size_t SMEM_BYTES = Ring<A_TERMS>::SMEM_BYTES;
+    constexpr size_t SMEM_BYTES = Ring<A_TERMS, BN>::SMEM_BYTES;
     static int configured_device = -1;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (configured_device != dev) {
-        e = cudaFuncSetAttribute(gemm_tcgen05_kernel<MODE, BF16, A_TERMS, OUT_BF16>,
+        e = cudaFuncSetAttribute(gemm_tcgen05_kernel<MODE, BF16, A_TERMS, OUT_BF16, BN>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(SMEM_BYTES));
         if (e != cudaSuccess) return e;
@@ -409,7 +413,7 @@ cudaError_t launch_impl(const void *A, const void *A2, const void *B0, const voi
     int64_t grid = sm_count();
     if (grid > p.num_tiles) grid = p.num_tiles;
     LaunchScope scope(kind, s);
-    gemm_tcgen05_kernel<MODE, BF16, A_TERMS, OUT_BF16>
+    gemm_tcgen05_kernel<MODE, BF16, A_TERMS, OUT_BF16, BN>
         <<<static_cast<unsigned>(grid), NUM_THREADS, SMEM_BYTES, s>>>(ma, ma2, mb0, mb1, p);
     return cudaGetLastError();
 }
@@ -437,22 +441,50 @@ cudaError_t launch_gemm_gateup(int dt, const void *A, const void *A_lo, const vo
               : launch_impl<MODE_GATEUP_SPLIT, false, 1>(A, nullptr, Wg, Wu, G, U, M, K, F, k, a, o, s);
 }
 
+// Tile width for the plain GEMM: waves of tiles times the width of a tile
+// (time per wave scales with it); e.g. 4096 columns on 152 SMs with 32 row
+// blocks: 256 wide -> 512 tiles, 4 waves (the last 37 % full); 224 wide ->
+// 608 tiles, exactly 4 full waves.
+int plain_tile_width(int64_t M, int64_t N) {
+    const int64_t mb = (M + BM - 1) / BM;
+    const int64_t sms = sm_count();
+    int best = 256;
+    int64_t best_cost = 0;
+    for (int bn : {256, 224}) {
+        const int64_t tiles = mb * ((N + bn - 1) / bn);
+        const int64_t cost = ((tiles + sms - 1) / sms) * bn;
+        if (best_cost == 0 || cost < best_cost) {
+            best = bn;
+            best_cost = cost;
+        }
+    }
+    return best;
+}
+
+template <bool BF16, int A_TERMS, bool OUT_BF16>
+cudaError_t launch_plain_bn(const void *A, const void *A_lo, const void *B, void *C, int64_t M,
+                            int64_t K, int64_t N, float acc_scale, cudaStream_t s) {
+    if (plain_tile_width(M, N) == 224)
+        return launch_impl<MODE_PLAIN, BF16, A_TERMS, OUT_BF16, 224>(A, A_lo, B, nullptr, C, nullptr, M, K,
+                                                                     N, K_GEMM_DOWN, acc_scale, 1.f, s);
+    return launch_impl<MODE_PLAIN, BF16, A_TERMS, OUT_BF16, 256>(A, A_lo, B, nullptr, C, nullptr, M, K, N,
+                                                                 K_GEMM_DOWN, acc_scale, 1.f, s);
+}
+
 cudaError_t launch_gemm_plain(int dt, int dt_out, const void *A, const void *A_lo, const void *B,
                               void *C, int64_t M, int64_t K, int64_t N, float acc_scale,
                               cudaStream_t s) {
-    const int k = K_GEMM_DOWN;
     const float a = acc_scale;
     if (dt == DT_BF16) {
-        if (A_lo) return launch_impl<MODE_PLAIN, true, 2>(A, A_lo, B, nullptr, C, nullptr, M, K, N, k, a, 1.f, s);
-        return launch_impl<MODE_PLAIN, true, 1>(A, nullptr, B, nullptr, C, nullptr, M, K, N, k, a, 1.f, s);
+        if (A_lo) return launch_plain_bn<true, 2, true>(A, A_lo, B, C, M, K, N, a, s);
+        return launch_plain_bn<true, 1, true>(A, nullptr, B, C, M, K, N, a, s);
     }
     if (dt_out == DT_BF16) {   // fp16 operands, bf16 output (prepared-weights path)
-        if (A_lo)
-            return launch_impl<MODE_PLAIN, false, 2, true>(A, A_lo, B, nullptr, C, nullptr, M, K, N, k, a, 1.f, s);
-        return launch_impl<MODE_PLAIN, false, 1, true>(A, nullptr, B, nullptr, C, nullptr, M, K, N, k, a, 1.f, s);
+        if (A_lo) return launch_plain_bn<false, 2, true>(A, A_lo, B, C, M, K, N, a, s);
+        return launch_plain_bn<false, 1, true>(A, nullptr, B, C, M, K, N, a, s);
     }
-    if (A_lo) return launch_impl<MODE_PLAIN, false, 2>(A, A_lo, B, nullptr, C, nullptr, M, K, N, k, a, 1.f, s);
-    return launch_impl<MODE_PLAIN, false, 1>(A, nullptr, B, nullptr, C, nullptr, M, K, N, k, a, 1.f, s);
+    if (A_lo) return launch_plain_bn<false, 2, false>(A, A_lo, B, C, M, K, N, a, s);
+    return launch_plain_bn<false, 1, false>(A, nullptr, B, C, M, K, N, a, s);
 }
 
 }  // namespace ffn

@@ -97,9 +97,8 @@ def ffn_block_forward(x, g, w_gate, w_up, w_down, eps: float, flags: int = 0, ou
     rows = x.numel() // d
     ffn = w_gate.shape[0]
     y = torch.empty_like(x) if out is None else out
-    need = ffn_block_workspace_bytes(rows, d, ffn, x.dtype, flags)
-    if ws is None:
-        ws = workspace(need, x.device)
+    if ws is None:   # (a passed workspace is checked against the need by the C side)
+        ws = workspace(ffn_block_workspace_bytes(rows, d, ffn, x.dtype, flags), x.device)
     _check(_lib.load().ffn_block_forward(_ptr(x), _ptr(g), _ptr(w_gate), _ptr(w_up), _ptr(w_down),
                                          _ptr(y), rows, d, ffn, float(eps), _dtype(x), flags,
                                          _ptr(ws), ws.numel(), _stream(stream)), "ffn_block_forward")
@@ -137,9 +136,8 @@ def ffn_block_forward_q4(x, g, w_gate, w_up, w_down, ffn: int, eps: float, flags
     d = x.shape[-1]
     rows = x.numel() // d
     y = torch.empty_like(x) if out is None else out
-    need = ffn_block_q4_workspace_bytes(rows, d, ffn)
     if ws is None:
-        ws = workspace(need, x.device)
+        ws = workspace(ffn_block_q4_workspace_bytes(rows, d, ffn), x.device)
     _check(_lib.load().ffn_block_forward_q4(_ptr(x), _ptr(g), _q4(w_gate), _q4(w_up), _q4(w_down),
                                             _ptr(y), rows, d, ffn, float(eps), flags, _ptr(ws),
                                             ws.numel(), _stream(stream)), "ffn_block_forward_q4")
