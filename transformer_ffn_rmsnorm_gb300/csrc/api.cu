@@ -319,7 +319,7 @@ ffn_status ffn_block_forward(const void *x, const void *g, const void *w_gate, c
             }
             // prepared weights: fp16 operands; the weights' 2^8 is undone on
             // G and U, h is stored times 2^-8 and the two cancel in the down GEMM
-            const int op = plan.prepared ? DT_F16 : dtype;
+            const int op = plan.prepared ? static_cast<int>(DT_F16) : static_cast<int>(dtype);
             const float w_unscale = plan.prepared ? 1.f / kPreparedScale : 1.f;
             const float h_scale = plan.prepared ? 1.f / 256.f : 1.f;
             cudaError_t e;

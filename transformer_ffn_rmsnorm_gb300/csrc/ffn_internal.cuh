@@ -97,6 +97,12 @@ cudaError_t launch_gemv_block(int wfmt, const void *x, const void *g, GemvWeight
                               GemvWeights wu, GemvWeights wd, void *y, int64_t rows, int64_t d,
                               int64_t ffn, float eps, const GemvWorkspace &ws, cudaStream_t s);
 
+// A 2D tiled TMA descriptor over a row-major array of `rows` rows, `inner`
+// elements a row, rows `row_bytes` apart; boxes of box_inner x box_rows.
+bool encode_tma_2d(CUtensorMap *m, const void *ptr, CUtensorMapDataType dt, int64_t inner,
+                   int64_t rows, int64_t row_bytes, uint32_t box_inner, uint32_t box_rows,
+                   CUtensorMapSwizzle swizzle);
+
 // Prefill tensor-core GEMMs (tcgen05 + TMEM + TMA).
 //   gate/up: A = n [M x K] (plus its residual A_lo, or nullptr), B = W_gate,
 //            W_up [F x K]; G, U = accumulator * acc_scale;

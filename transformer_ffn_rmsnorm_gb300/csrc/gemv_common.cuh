@@ -1,0 +1,101 @@
+// gemv_common.cuh -- pieces shared by the decode (few-row) kernels.
+#pragma once
+
+#include "ffn_internal.cuh"
+
+namespace ffn {
+namespace gemv {
+
+constexpr int kChunk = 32;   // k values per MMA pair
+
+__host__ __device__ inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Fragment order of an activation vector of length K for one token:
+//   16-bit element index = ((nt * nch + c) * 32 + lane) * 8 + slot
+//   lane = 4 * (token % 8) + tid, nt = token / 8, c = k / 32.
+// Natural order (f16/bf16 weights): k % 32 = 8 * tid + slot.
+// Q4 order: position p = k % 32, hi = p / 16, q = p % 16, tid = q / 4,
+//   slot = 4 * hi + perm[q % 4] with perm = {0, 2, 1, 3}; this matches the
+//   nibble unpacking in dequant_word below.
+__device__ __forceinline__ int64_t frag_elem(bool q4, int64_t nch, int token, int64_t k) {
+    const int64_t c = k / kChunk;
+    const int p = static_cast<int>(k % kChunk);
+    int tid, slot;
+    if (q4) {
+        const int hi = p >> 4, q = p & 15;
+        tid = q >> 2;
+        const int e = q & 3;
+        slot = 4 * hi + ((e == 1) ? 2 : (e == 2) ? 1 : e);
+    } else {
+        tid = p >> 3;
+        slot = p & 7;
+    }
+    const int lane = 4 * (token & 7) + tid;
+    return (((token >> 3) * nch + c) * 32 + lane) * 8 + slot;
+}
+
+// Per weight format: TIn stores x, g and y; TOp is the MMA operand type of the
+// activation fragments; the weights carry a factor w_scale (undone on the
+// fp32 accumulator) and h is stored times h_scale (undone after the down
+// projection).  All factors are powers of two, so they change no bits.
+template <int WF> struct Fmt;
+template <> struct Fmt<WF_F16> {
+    using TIn = __half; using TOp = __half;
+    static constexpr bool op_bf16 = false;
+    static constexpr float w_unscale = 1.f, h_scale = 1.f;
+};
+template <> struct Fmt<WF_BF16> {
+    using TIn = __nv_bfloat16; using TOp = __nv_bfloat16;
+    static constexpr bool op_bf16 = true;
+    static constexpr float w_unscale = 1.f, h_scale = 1.f;
+};
+// Q4 codes (u - 8) are exact in fp16; activations go in as fp16 (11 bits),
+// h scaled by 2^-8 to keep fp16 clear of overflow.
+template <> struct Fmt<WF_Q4> {
+    using TIn = __nv_bfloat16; using TOp = __half;
+    static constexpr bool op_bf16 = false;
+    static constexpr float w_unscale = 1.f, h_scale = 1.f / 256.f;
+};
+// Prepared weights: fp16 values of w * 2^8.
+template <> struct Fmt<WF_F16P> {
+    using TIn = __nv_bfloat16; using TOp = __half;
+    static constexpr bool op_bf16 = false;
+    static constexpr float w_unscale = 1.f / kPreparedScale, h_scale = 1.f / 256.f;
+};
+
+// Q4: one 32-bit word = canonical bytes 4*tid .. 4*tid+3 of a block.
+// Returns (u - 8) as fp16 pairs:
+//   r[0] = (e0, e2), r[1] = (e16, e18), r[2] = (e1, e3), r[3] = (e17, e19)
+// relative to element 4*tid of the block.  0x6400 is fp16 1024.0, whose ulp
+// is 1, so 0x6400 | u is exactly 1024 + u, and subtracting 1032 gives u - 8
+// exactly.
+__device__ __forceinline__ void dequant_word(uint32_t w, uint32_t (&r)[4]) {
+    const __half2 k1032 = __floats2half2_rn(1032.f, 1032.f);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t sh = (i == 0) ? 0 : (i == 1) ? 4 : (i == 2) ? 8 : 12;
+        uint32_t v = ((w >> sh) & 0x000F000Fu) | 0x64006400u;
+        __half2 b = *reinterpret_cast<__half2 *>(&v);
+        b = __hsub2(b, k1032);
+        r[i] = *reinterpret_cast<uint32_t *>(&b);
+    }
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4 &v, int b) {
+    return b == 0 ? v.x : b == 1 ? v.y : b == 2 ? v.z : v.w;
+}
+
+// TMA-streamed decode kernels (gemv_stream.cu)
+bool stream_supported(int wfmt, int64_t d, int64_t ffn);
+int64_t stream_down_splits(int wfmt, int64_t d, int64_t ffn);
+template <int WF, int NT, bool TWO>
+cudaError_t launch_stream_gateup(GemvWeights wg, GemvWeights wu, const void *nfrag, const void *nfrag_lo,
+                                 void *hfrag, void *hfrag_lo, int64_t d, int64_t ffn, int64_t nchK,
+                                 int64_t nchF, unsigned *counters, int ncounters, cudaStream_t s);
+template <int WF, int NT, bool TWO>
+cudaError_t launch_stream_down(GemvWeights wd, const void *hfrag, const void *hfrag_lo, void *y,
+                               float *partials, unsigned *counters, int rows, int64_t d, int64_t ffn,
+                               int64_t nchF, int64_t splits, cudaStream_t s);
+
+}  // namespace gemv
+}  // namespace ffn

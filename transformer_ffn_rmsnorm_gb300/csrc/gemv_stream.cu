@@ -1,0 +1,463 @@
+// gemv_stream.cu -- decode (few-row) projections with the weight stream decoupled
+// from the math.
+//
+// The register-streaming kernels (gemv.cu) load weights straight into MMA
+// fragments: each warp issues a burst of loads, waits, computes, and only
+// then issues the next burst, so HBM idles between bursts (ncu: stalled on
+// the long scoreboard, 1.6-4.4 TB/s).  Here one producer thread per CTA keeps
+// a 6-stage shared-memory ring full with TMA bulk tensor copies of 64 weight
+// rows x one k-block (16-bit: 64 values, 128 bytes a row; Q4: 256 values,
+// 128 bytes of nibbles plus 16 bytes of fp16 scales a row), 128-byte
+// swizzled, while four MMA warps read their A fragments from shared memory
+// and the pre-arranged activation fragments from L1.  With three or four
+// CTAs per SM that keeps about 150-200 KB of weights in flight per SM.
+//
+// Roles: gate/up -- a CTA owns 32 features (32 rows of W_gate and of W_up)
+// over the whole of d and applies silu(G)*U; down -- a CTA owns 64 rows of
+// W_down over one split of ffn and hands its partial sums to the same
+// deterministic last-CTA reduction as the register kernels.
+//
+// Every mbarrier wait is bounded (1 s); a wait that gives up records
+// FFN_ERR_TIMEOUT in the device status word, stops the other roles, and the
+// producer waits (bounded) for its copies in flight before the CTA exits.
+#include <cudaTypedefs.h>
+
+#include "gemv_common.cuh"
+
+namespace ffn {
+namespace gemv {
+namespace {
+
+constexpr int kConsumers = 4;
+constexpr int kThreads = 32 * (kConsumers + 1);
+constexpr int kStages = 6;
+constexpr uint64_t kWaitNs = 1000000000ull;
+
+enum { ROLE_GATEUP = 0, ROLE_DOWN = 1 };
+
+template <int WF, int ROLE> struct Tile {
+    static constexpr bool q4 = WF == WF_Q4;
+    static constexpr int nmat = ROLE == ROLE_GATEUP ? 2 : 1;     // weight matrices per stage
+    static constexpr int box_rows = ROLE == ROLE_GATEUP ? 32 : 64;
+    static constexpr int kb = q4 ? 256 : 64;                     // k values per stage
+    static constexpr uint32_t w_bytes = box_rows * 128;          // one matrix' rows x 128 B
+    static constexpr uint32_t s_bytes = q4 ? box_rows * 16 : 0;  // its scales
+    static constexpr uint32_t tx_bytes = nmat * (w_bytes + s_bytes);
+    static constexpr uint32_t stage_bytes = (tx_bytes + 1023) & ~1023u;
+    static constexpr size_t smem_bytes = kStages * stage_bytes + 1024;
+};
+
+struct StreamParams {
+    int64_t K;              // reduction length
+    int64_t rows_w;         // rows of each weight matrix (ffn for gate/up, d for down)
+    int64_t nkb;            // k-blocks over K
+    int64_t kb_per_split;   // down: k-blocks per CTA split
+    const uint4 *bfrag, *bfrag_lo;
+    int64_t nch_b;          // fragment chunks of the activation operand
+    uint16_t *hfrag, *hfrag_lo;
+    int64_t nch_h;          // gate/up: fragment chunks of h
+    void *y;
+    float *partials;
+    unsigned *counters;
+    int ncounters;
+    int rows;               // token rows (<= 16)
+    int64_t D;              // down: output features
+    unsigned *err;
+};
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+template <int WF, int NT, bool TWO, int ROLE>
+__global__ void __launch_bounds__(kThreads) gemv_stream_kernel(
+    const __grid_constant__ CUtensorMap map_w0, const __grid_constant__ CUtensorMap map_w1,
+    const __grid_constant__ CUtensorMap map_s0, const __grid_constant__ CUtensorMap map_s1,
+    const StreamParams p) {
+    using TL = Tile<WF, ROLE>;
+    using TO = typename Fmt<WF>::TOp;
+    constexpr bool bf = Fmt<WF>::op_bf16;
+    constexpr bool q4 = TL::q4;
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t bar_full[kStages], bar_empty[kStages];
+    __shared__ float red[2][32][NT * 4];
+    __shared__ int s_abort, s_never, s_last;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t base = (ptx::smem_u32(smem_raw) + 1023u) & ~1023u;
+    auto full = [&](int s) { return ptx::smem_u32(&bar_full[s]); };
+    auto empty = [&](int s) { return ptx::smem_u32(&bar_empty[s]); };
+
+    const int64_t row0 = static_cast<int64_t>(blockIdx.x) * (ROLE == ROLE_GATEUP ? 32 : 64);
+    const int64_t kb0 = ROLE == ROLE_DOWN ? blockIdx.y * p.kb_per_split : 0;
+    const int64_t kb1 = ROLE == ROLE_DOWN ? min(p.nkb, kb0 + p.kb_per_split) : p.nkb;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            ptx::mbar_init(full(s), 1);
+            ptx::mbar_init(empty(s), kConsumers);
+        }
+        s_abort = 0;
+        s_never = 0;
+        ptx::fence_mbar_init();
+    }
+    if (ROLE == ROLE_GATEUP && blockIdx.x == 0)
+        for (int i = threadIdx.x; i < p.ncounters; i += blockDim.x) p.counters[i] = 0u;
+    __syncthreads();
+    volatile int *abort_flag = &s_abort;
+    volatile int *never = &s_never;
+    int64_t issued = 0;
+
+    if (warp == kConsumers) {
+        // ------------------------------------------------------- TMA producer
+        if (lane == 0) {
+            ptx::tma_prefetch_map(&map_w0);
+            if (TL::nmat == 2) ptx::tma_prefetch_map(&map_w1);
+            bool ok = true;
+            for (int64_t kb = kb0; kb < kb1; ++kb, ++issued) {
+                const int s = static_cast<int>(issued % kStages);
+                const uint32_t ph = static_cast<uint32_t>((issued / kStages) & 1);
+                if (!ptx::mbar_wait(empty(s), ph ^ 1u, abort_flag, kWaitNs)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t st = base + s * TL::stage_bytes;
+                ptx::mbar_arrive_expect_tx(full(s), TL::tx_bytes);
+                const int x = static_cast<int>(kb * (q4 ? 128 : 64));   // bytes of nibbles / elements
+                const int y = static_cast<int>(row0);
+                ptx::tma_load_2d(st, &map_w0, full(s), x, y);
+                if (TL::nmat == 2) ptx::tma_load_2d(st + TL::w_bytes, &map_w1, full(s), x, y);
+                if (q4) {
+                    const uint32_t sc = st + TL::nmat * TL::w_bytes;
+                    ptx::tma_load_2d(sc, &map_s0, full(s), static_cast<int>(kb * 8), y);
+                    if (TL::nmat == 2)
+                        ptx::tma_load_2d(sc + TL::s_bytes, &map_s1, full(s), static_cast<int>(kb * 8), y);
+                }
+            }
+            if (!ok) {
+                atomicOr(p.err, DEVERR_TIMEOUT);
+                *abort_flag = 1;
+            }
+        }
+    } else {
+        // ------------------------------------------------------ MMA warps
+        const int g = lane >> 2, tid = lane & 3;
+        const int mat = ROLE == ROLE_GATEUP ? (warp >> 1) : 0;
+        const int r0 = 16 * (ROLE == ROLE_GATEUP ? (warp & 1) : warp);   // row tile inside the box
+        const int ra = r0 + g, rb = r0 + g + 8;                             // (ra & 7) == (rb & 7) == g
+        float acc[NT][4];
+#pragma unroll
+        for (int n = 0; n < NT; ++n)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[n][i] = 0.f;
+        bool ok = true;
+        int64_t it = 0;
+        for (int64_t kb = kb0; kb < kb1; ++kb, ++it) {
+            const int s = static_cast<int>(it % kStages);
+            const uint32_t ph = static_cast<uint32_t>((it / kStages) & 1);
+            const bool got = ptx::mbar_wait(full(s), ph, abort_flag, kWaitNs);
+            if (!__all_sync(0xffffffffu, got)) {
+                ok = false;
+                break;
+            }
+            const uint32_t wbase = base + s * TL::stage_bytes + mat * TL::w_bytes;
+            if constexpr (!q4) {
+                // two 32-wide chunks: this lane's 16 bytes of rows ra, rb at chunk 4j + tid
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int64_t c = kb * 2 + j;
+                    uint4 b[NT], bl[TWO ? NT : 1];
+                    // a 64-wide k-block can run one chunk past the fragment
+                    // buffer when it holds an odd number of chunks; the
+                    // weights there are TMA zero fill, the operand must be 0
+                    const bool cin = c < p.nch_b;
+#pragma unroll
+                    for (int n = 0; n < NT; ++n) {
+                        b[n] = cin ? __ldg(p.bfrag + (n * p.nch_b + c) * 32 + lane) : make_uint4(0, 0, 0, 0);
+                        if constexpr (TWO)
+                            bl[n] = cin ? __ldg(p.bfrag_lo + (n * p.nch_b + c) * 32 + lane) : make_uint4(0, 0, 0, 0);
+                    }
+                    const uint32_t off = static_cast<uint32_t>(((4 * j + tid) ^ g) << 4);
+                    const uint4 a0 = lds128(wbase + ra * 128 + off);
+                    const uint4 a1 = lds128(wbase + rb * 128 + off);
+#pragma unroll
+                    for (int n = 0; n < NT; ++n) {
+                        ptx::mma_16816<bf>(acc[n], a0.x, a1.x, a0.y, a1.y, b[n].x, b[n].y);
+                        ptx::mma_16816<bf>(acc[n], a0.z, a1.z, a0.w, a1.w, b[n].z, b[n].w);
+                        if constexpr (TWO) {
+                            ptx::mma_16816<bf>(acc[n], a0.x, a1.x, a0.y, a1.y, bl[n].x, bl[n].y);
+                            ptx::mma_16816<bf>(acc[n], a0.z, a1.z, a0.w, a1.w, bl[n].z, bl[n].w);
+                        }
+                    }
+                }
+            } else {
+                // 256 k = two groups of four 32-value blocks; scales follow the nibbles
+                const uint32_t sbase = base + s * TL::stage_bytes + TL::nmat * TL::w_bytes + mat * TL::s_bytes;
+                const uint4 sa = lds128(sbase + ra * 16), sb = lds128(sbase + rb * 16);
+#pragma unroll
+                for (int grp = 0; grp < 2; ++grp) {
+                    const uint32_t off = static_cast<uint32_t>(((4 * grp + tid) ^ g) << 4);
+                    const uint4 qa = lds128(wbase + ra * 128 + off);
+                    const uint4 qb = lds128(wbase + rb * 128 + off);
+#pragma unroll
+                    for (int blk = 0; blk < 4; ++blk) {
+                        const int bi = 4 * grp + blk;            // block inside the stage, 0..7
+                        const int64_t c = kb * 8 + bi;
+                        uint4 b[NT];
+#pragma unroll
+                        for (int n = 0; n < NT; ++n) b[n] = __ldg(p.bfrag + (n * p.nch_b + c) * 32 + lane);
+                        uint32_t lo[4], hi[4];
+                        dequant_word(word_of(qa, blk), lo);
+                        dequant_word(word_of(qb, blk), hi);
+                        const uint32_t wa = word_of(sa, bi >> 1), wb = word_of(sb, bi >> 1);
+                        const float fa = __half2float(__ushort_as_half(
+                            static_cast<unsigned short>((wa >> (16 * (bi & 1))) & 0xFFFFu)));
+                        const float fb = __half2float(__ushort_as_half(
+                            static_cast<unsigned short>((wb >> (16 * (bi & 1))) & 0xFFFFu)));
+#pragma unroll
+                        for (int n = 0; n < NT; ++n) {
+                            float t[4] = {0.f, 0.f, 0.f, 0.f};
+                            ptx::mma_16816<bf>(t, lo[0], hi[0], lo[2], hi[2], b[n].x, b[n].y);
+                            ptx::mma_16816<bf>(t, lo[1], hi[1], lo[3], hi[3], b[n].z, b[n].w);
+                            acc[n][0] = fmaf(fa, t[0], acc[n][0]);
+                            acc[n][1] = fmaf(fa, t[1], acc[n][1]);
+                            acc[n][2] = fmaf(fb, t[2], acc[n][2]);
+                            acc[n][3] = fmaf(fb, t[3], acc[n][3]);
+                        }
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(empty(s));
+        }
+        if (!ok) {
+            if (lane == 0) {
+                atomicOr(p.err, DEVERR_TIMEOUT);
+                *abort_flag = 1;
+            }
+        }
+
+        // ------------------------------------------------------- epilogues
+        if constexpr (ROLE == ROLE_GATEUP) {
+            if (warp >= 2) {   // up tiles hand their fragments to the gate warps
+#pragma unroll
+                for (int n = 0; n < NT; ++n)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) red[warp - 2][lane][n * 4 + i] = acc[n][i];
+            }
+            consumer_sync();
+            if (warp < 2) {
+                constexpr float ws = Fmt<WF>::w_unscale;
+#pragma unroll
+                for (int n = 0; n < NT; ++n)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int64_t feat = row0 + r0 + g + 8 * (i >> 1);
+                        const int token = 8 * n + 2 * tid + (i & 1);
+                        const float hv = silu_f32(acc[n][i] * ws) * (red[warp][lane][n * 4 + i] * ws) *
+                                         Fmt<WF>::h_scale;
+                        const TO t = from_f32<TO>(hv);
+                        const int64_t at = frag_elem(q4, p.nch_h, token, feat);
+                        p.hfrag[at] = *reinterpret_cast<const uint16_t *>(&t);
+                        if (TWO) {
+                            const TO tl = from_f32<TO>(hv - to_f32(t));
+                            p.hfrag_lo[at] = *reinterpret_cast<const uint16_t *>(&tl);
+                        }
+                    }
+            }
+        } else {
+            using T = typename Fmt<WF>::TIn;
+            constexpr float out_scale = Fmt<WF>::w_unscale / Fmt<WF>::h_scale;
+            const int split = blockIdx.y, nsplit = gridDim.y;
+#pragma unroll
+            for (int n = 0; n < NT; ++n)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int64_t feat = row0 + r0 + g + 8 * (i >> 1);
+                    const int token = 8 * n + 2 * tid + (i & 1);
+                    if (token < p.rows && feat < p.D)
+                        p.partials[(static_cast<int64_t>(split) * p.rows + token) * p.D + feat] = acc[n][i];
+                }
+            __threadfence();
+            consumer_sync();
+            if (threadIdx.x == 0)
+                s_last = atomicAdd(&p.counters[blockIdx.x], 1u) == static_cast<unsigned>(nsplit - 1);
+            consumer_sync();
+            if (s_last) {
+                __threadfence();
+                T *y = static_cast<T *>(p.y);
+                for (int i = threadIdx.x; i < p.rows * 64; i += 32 * kConsumers) {
+                    const int token = i / 64;
+                    const int64_t feat = row0 + i % 64;
+                    if (feat >= p.D) continue;
+                    float sum = 0.f;
+                    for (int sp = 0; sp < nsplit; ++sp)
+                        sum += __ldcg(p.partials + (static_cast<int64_t>(sp) * p.rows + token) * p.D + feat);
+                    y[static_cast<int64_t>(token) * p.D + feat] = from_f32<T>(sum * out_scale);
+                }
+                if (threadIdx.x == 0) p.counters[blockIdx.x] = 0u;
+            }
+        }
+    }
+
+    __syncthreads();
+    if (warp == kConsumers && lane == 0) {
+        // copies still in flight (only after an abandoned wait) land before exit
+        for (int s = 0; s < kStages; ++s) {
+            if (issued > s) {
+                const int64_t armed = (issued - s + kStages - 1) / kStages;
+                ptx::mbar_wait(full(s), static_cast<uint32_t>((armed - 1) & 1), never, kWaitNs);
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------ host side
+bool map_rows(CUtensorMap *m, const void *ptr, CUtensorMapDataType dt, int64_t inner, int64_t rows,
+              int64_t row_bytes, uint32_t box_inner, uint32_t box_rows, bool swizzle) {
+    return encode_tma_2d(m, ptr, dt, inner, rows, row_bytes, box_inner, box_rows,
+                         swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+// Weight (and scale) maps of one matrix [rows x K] in format WF.
+template <int WF, int ROLE>
+bool weight_maps(CUtensorMap *w, CUtensorMap *sc, const GemvWeights &wt, int64_t rows, int64_t K) {
+    using TL = Tile<WF, ROLE>;
+    if (TL::q4) {
+        if (!map_rows(w, wt.qs, CU_TENSOR_MAP_DATA_TYPE_UINT8, K / 2, rows, K / 2, 128, TL::box_rows, true))
+            return false;
+        return map_rows(sc, wt.sc, CU_TENSOR_MAP_DATA_TYPE_UINT16, K / 32, rows, K / 16, 8, TL::box_rows, false);
+    }
+    *sc = CUtensorMap{};
+    return map_rows(w, wt.w, CU_TENSOR_MAP_DATA_TYPE_UINT16, K, rows, K * 2, 64, TL::box_rows, true);
+}
+
+template <typename Kern>
+cudaError_t set_smem(Kern k, size_t bytes) {
+    static int configured = -1;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (configured != dev) {
+        e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+        if (e != cudaSuccess) return e;
+        configured = dev;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace
+
+bool stream_supported(int wfmt, int64_t d, int64_t ffn) {
+    if (wfmt == WF_Q4) return d % 256 == 0 && ffn % 256 == 0;
+    return d % 8 == 0 && ffn % 8 == 0;
+}
+
+template <int WF, int NT, bool TWO>
+cudaError_t launch_stream_gateup(GemvWeights wg, GemvWeights wu, const void *nfrag, const void *nfrag_lo,
+                                 void *hfrag, void *hfrag_lo, int64_t d, int64_t ffn, int64_t nchK,
+                                 int64_t nchF, unsigned *counters, int ncounters, cudaStream_t s) {
+    using TL = Tile<WF, ROLE_GATEUP>;
+    auto kern = gemv_stream_kernel<WF, NT, TWO, ROLE_GATEUP>;
+    cudaError_t e = set_smem(kern, TL::smem_bytes);
+    if (e != cudaSuccess) return e;
+    CUtensorMap w0, w1, s0, s1;
+    if (!weight_maps<WF, ROLE_GATEUP>(&w0, &s0, wg, ffn, d) || !weight_maps<WF, ROLE_GATEUP>(&w1, &s1, wu, ffn, d))
+        return cudaErrorInvalidValue;
+    StreamParams p{};
+    p.K = d;
+    p.rows_w = ffn;
+    p.nkb = cdiv(d, TL::kb);
+    p.kb_per_split = p.nkb;
+    p.bfrag = static_cast<const uint4 *>(nfrag);
+    p.bfrag_lo = static_cast<const uint4 *>(nfrag_lo);
+    p.nch_b = nchK;
+    p.hfrag = static_cast<uint16_t *>(hfrag);
+    p.hfrag_lo = static_cast<uint16_t *>(hfrag_lo);
+    p.nch_h = nchF;
+    p.counters = counters;
+    p.ncounters = ncounters;
+    p.err = device_status_word();
+    if (!p.err) return cudaErrorUnknown;
+    // 32 features per CTA; covering nchF * 32 features writes every slot of h
+    const int64_t blocks = nchF;
+    LaunchScope scope(K_GEMV_GATEUP, s);
+    kern<<<static_cast<unsigned>(blocks), kThreads, TL::smem_bytes, s>>>(w0, w1, s0, s1, p);
+    return cudaGetLastError();
+}
+
+template <int WF, int NT, bool TWO>
+cudaError_t launch_stream_down(GemvWeights wd, const void *hfrag, const void *hfrag_lo, void *y,
+                               float *partials, unsigned *counters, int rows, int64_t d, int64_t ffn,
+                               int64_t nchF, int64_t splits, cudaStream_t s) {
+    using TL = Tile<WF, ROLE_DOWN>;
+    auto kern = gemv_stream_kernel<WF, NT, TWO, ROLE_DOWN>;
+    cudaError_t e = set_smem(kern, TL::smem_bytes);
+    if (e != cudaSuccess) return e;
+    CUtensorMap w0, s0;
+    if (!weight_maps<WF, ROLE_DOWN>(&w0, &s0, wd, d, ffn)) return cudaErrorInvalidValue;
+    StreamParams p{};
+    p.K = ffn;
+    p.rows_w = d;
+    p.nkb = cdiv(ffn, TL::kb);
+    p.kb_per_split = cdiv(p.nkb, splits);
+    (void)nchF;
+    p.bfrag = static_cast<const uint4 *>(hfrag);
+    p.bfrag_lo = static_cast<const uint4 *>(hfrag_lo);
+    p.nch_b = nchF;
+    p.y = y;
+    p.partials = partials;
+    p.counters = counters;
+    p.rows = rows;
+    p.D = d;
+    p.err = device_status_word();
+    if (!p.err) return cudaErrorUnknown;
+    const int64_t nsplit = cdiv(p.nkb, p.kb_per_split);
+    dim3 grid(static_cast<unsigned>(cdiv(d, 64)), static_cast<unsigned>(nsplit));
+    LaunchScope scope(K_GEMV_DOWN, s);
+    kern<<<grid, kThreads, TL::smem_bytes, s>>>(w0, w0, s0, s0, p);
+    return cudaGetLastError();
+}
+
+// Down-projection splits for the streaming kernel: about 640 CTAs of 64 rows
+// (four per SM on a 152-SM part, plus slack), never finer than one k-block.
+// A function of the shape alone, so workspace queries agree with launches.
+int64_t stream_down_splits(int wfmt, int64_t d, int64_t ffn) {
+    const int64_t groups = cdiv(d, 64);
+    const int64_t kb = wfmt == WF_Q4 ? 256 : 64;
+    const int64_t nkb = cdiv(ffn, kb);
+    int64_t splits = cdiv(640, groups);
+    if (splits > nkb) splits = nkb;
+    return cdiv(nkb, cdiv(nkb, splits));   // the splits the kernel will actually run
+}
+
+#define FFN_STREAM_INSTANTIATE(WF, NT, TWO)                                                            \
+    template cudaError_t launch_stream_gateup<WF, NT, TWO>(GemvWeights, GemvWeights, const void *,      \
+                                                           const void *, void *, void *, int64_t,       \
+                                                           int64_t, int64_t, int64_t, unsigned *, int,   \
+                                                           cudaStream_t);                                \
+    template cudaError_t launch_stream_down<WF, NT, TWO>(GemvWeights, const void *, const void *, void *, \
+                                                         float *, unsigned *, int, int64_t, int64_t,     \
+                                                         int64_t, int64_t, cudaStream_t);
+FFN_STREAM_INSTANTIATE(WF_F16, 1, false)
+FFN_STREAM_INSTANTIATE(WF_F16, 2, false)
+FFN_STREAM_INSTANTIATE(WF_F16, 1, true)
+FFN_STREAM_INSTANTIATE(WF_F16, 2, true)
+FFN_STREAM_INSTANTIATE(WF_BF16, 1, false)
+FFN_STREAM_INSTANTIATE(WF_BF16, 2, false)
+FFN_STREAM_INSTANTIATE(WF_BF16, 1, true)
+FFN_STREAM_INSTANTIATE(WF_BF16, 2, true)
+FFN_STREAM_INSTANTIATE(WF_Q4, 1, false)
+FFN_STREAM_INSTANTIATE(WF_Q4, 2, false)
+FFN_STREAM_INSTANTIATE(WF_F16P, 1, false)
+FFN_STREAM_INSTANTIATE(WF_F16P, 2, false)
+#undef FFN_STREAM_INSTANTIATE
+
+}  // namespace gemv
+}  // namespace ffn
