@@ -338,14 +338,16 @@ bool weight_maps(CUtensorMap *w, CUtensorMap *sc, const GemvWeights &wt, int64_t
     return map_rows(w, wt.w, CU_TENSOR_MAP_DATA_TYPE_UINT16, K, rows, K * 2, 64, TL::box_rows, true);
 }
 
-template <typename Kern>
-cudaError_t set_smem(Kern k, size_t bytes) {
+// Opt one kernel (the template argument itself, so every instantiation has
+// its own flag) into more than 48 KB of dynamic shared memory on this device.
+template <auto KERN>
+cudaError_t set_smem(size_t bytes) {
     static int configured = -1;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (configured != dev) {
-        e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+        e = cudaFuncSetAttribute(KERN, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
         if (e != cudaSuccess) return e;
         configured = dev;
     }
@@ -364,8 +366,8 @@ cudaError_t launch_stream_gateup(GemvWeights wg, GemvWeights wu, const void *nfr
                                  void *hfrag, void *hfrag_lo, int64_t d, int64_t ffn, int64_t nchK,
                                  int64_t nchF, unsigned *counters, int ncounters, cudaStream_t s) {
     using TL = Tile<WF, ROLE_GATEUP>;
-    auto kern = gemv_stream_kernel<WF, NT, TWO, ROLE_GATEUP>;
-    cudaError_t e = set_smem(kern, TL::smem_bytes);
+    constexpr auto kern = gemv_stream_kernel<WF, NT, TWO, ROLE_GATEUP>;
+    cudaError_t e = set_smem<kern>(TL::smem_bytes);
     if (e != cudaSuccess) return e;
     CUtensorMap w0, w1, s0, s1;
     if (!weight_maps<WF, ROLE_GATEUP>(&w0, &s0, wg, ffn, d) || !weight_maps<WF, ROLE_GATEUP>(&w1, &s1, wu, ffn, d))
@@ -397,8 +399,8 @@ cudaError_t launch_stream_down(GemvWeights wd, const void *hfrag, const void *hf
                                float *partials, unsigned *counters, int rows, int64_t d, int64_t ffn,
                                int64_t nchF, int64_t splits, cudaStream_t s) {
     using TL = Tile<WF, ROLE_DOWN>;
-    auto kern = gemv_stream_kernel<WF, NT, TWO, ROLE_DOWN>;
-    cudaError_t e = set_smem(kern, TL::smem_bytes);
+    constexpr auto kern = gemv_stream_kernel<WF, NT, TWO, ROLE_DOWN>;
+    cudaError_t e = set_smem<kern>(TL::smem_bytes);
     if (e != cudaSuccess) return e;
     CUtensorMap w0, s0;
     if (!weight_maps<WF, ROLE_DOWN>(&w0, &s0, wd, d, ffn)) return cudaErrorInvalidValue;
