@@ -8,9 +8,10 @@
 // a 6-stage shared-memory ring full with TMA bulk tensor copies of 64 weight
 // rows x one k-block (16-bit: 64 values, 128 bytes a row; Q4: 256 values,
 // 128 bytes of nibbles plus 16 bytes of fp16 scales a row), 128-byte
-// swizzled, while four MMA warps read their A fragments from shared memory
-// and the pre-arranged activation fragments from L1.  With three or four
-// CTAs per SM that keeps about 150-200 KB of weights in flight per SM.
+// swizzled, plus -- by 1-D bulk copies -- the pre-arranged activation
+// fragments of the same k range, while four MMA warps read everything from
+// shared memory.  (Reading the activations through L1 instead stalls: the
+// rings leave too little L1 to hold them.)
 //
 // Roles: gate/up -- a CTA owns 32 features (32 rows of W_gate and of W_up)
 // over the whole of d and applies silu(G)*U; down -- a CTA owns 64 rows of
@@ -30,21 +31,28 @@ namespace {
 
 constexpr int kConsumers = 4;
 constexpr int kThreads = 32 * (kConsumers + 1);
-constexpr int kStages = 6;
 constexpr uint64_t kWaitNs = 1000000000ull;
+constexpr uint32_t kFragBytes = 32 * 16;   // one 32-value chunk of fragments for 8 tokens
 
 enum { ROLE_GATEUP = 0, ROLE_DOWN = 1 };
 
-template <int WF, int ROLE> struct Tile {
+// Stage layout: [weights of each matrix][their scales (Q4)][activation
+// fragments: NT tiles x terms x chunks x 512 B].
+template <int WF, int ROLE, int NT, bool TWO> struct Tile {
     static constexpr bool q4 = WF == WF_Q4;
     static constexpr int nmat = ROLE == ROLE_GATEUP ? 2 : 1;     // weight matrices per stage
     static constexpr int box_rows = ROLE == ROLE_GATEUP ? 32 : 64;
     static constexpr int kb = q4 ? 256 : 64;                     // k values per stage
+    static constexpr int chunks = kb / kChunk;                   // fragment chunks per stage
+    static constexpr int terms = TWO ? 2 : 1;
     static constexpr uint32_t w_bytes = box_rows * 128;          // one matrix' rows x 128 B
     static constexpr uint32_t s_bytes = q4 ? box_rows * 16 : 0;  // its scales
-    static constexpr uint32_t tx_bytes = nmat * (w_bytes + s_bytes);
-    static constexpr uint32_t stage_bytes = (tx_bytes + 1023) & ~1023u;
-    static constexpr size_t smem_bytes = kStages * stage_bytes + 1024;
+    static constexpr uint32_t b_off = nmat * (w_bytes + s_bytes);
+    static constexpr uint32_t b_bytes = NT * terms * chunks * kFragBytes;
+    static constexpr uint32_t stage_bytes = (b_off + b_bytes + 1023) & ~1023u;
+    static constexpr int stages_fit = (52 * 1024) / stage_bytes;
+    static constexpr int stages = stages_fit < 3 ? 3 : stages_fit > 6 ? 6 : stages_fit;
+    static constexpr size_t smem_bytes = stages * stage_bytes + 1024;
 };
 
 struct StreamParams {
@@ -80,10 +88,11 @@ __global__ void __launch_bounds__(kThreads) gemv_stream_kernel(
     const __grid_constant__ CUtensorMap map_w0, const __grid_constant__ CUtensorMap map_w1,
     const __grid_constant__ CUtensorMap map_s0, const __grid_constant__ CUtensorMap map_s1,
     const StreamParams p) {
-    using TL = Tile<WF, ROLE>;
+    using TL = Tile<WF, ROLE, NT, TWO>;
     using TO = typename Fmt<WF>::TOp;
     constexpr bool bf = Fmt<WF>::op_bf16;
     constexpr bool q4 = TL::q4;
+    constexpr int kStages = TL::stages;
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bar_full[kStages], bar_empty[kStages];
     __shared__ float red[2][32][NT * 4];
@@ -128,7 +137,19 @@ __global__ void __launch_bounds__(kThreads) gemv_stream_kernel(
                     break;
                 }
                 const uint32_t st = base + s * TL::stage_bytes;
-                ptx::mbar_arrive_expect_tx(full(s), TL::tx_bytes);
+                // activation chunks of this k range that exist (the last
+                // 64-wide block can hang one chunk past the buffer)
+                const int64_t c0 = kb * TL::chunks;
+                const int64_t left = p.nch_b - c0;
+                const uint32_t nvalid = static_cast<uint32_t>(left < TL::chunks ? left : TL::chunks);
+                ptx::mbar_arrive_expect_tx(full(s), TL::b_off + NT * TL::terms * nvalid * kFragBytes);
+#pragma unroll
+                for (int n = 0; n < NT; ++n)
+#pragma unroll
+                    for (int t = 0; t < TL::terms; ++t)
+                        ptx::bulk_load(st + TL::b_off + (n * TL::terms + t) * TL::chunks * kFragBytes,
+                                       (t ? p.bfrag_lo : p.bfrag) + (n * p.nch_b + c0) * 32,
+                                       nvalid * kFragBytes, full(s));
                 const int x = static_cast<int>(kb * (q4 ? 128 : 64));   // bytes of nibbles / elements
                 const int y = static_cast<int>(row0);
                 ptx::tma_load_2d(st, &map_w0, full(s), x, y);
@@ -169,6 +190,7 @@ __global__ void __launch_bounds__(kThreads) gemv_stream_kernel(
             const uint32_t wbase = base + s * TL::stage_bytes + mat * TL::w_bytes;
             if constexpr (!q4) {
                 // two 32-wide chunks: this lane's 16 bytes of rows ra, rb at chunk 4j + tid
+                const uint32_t bbase = base + s * TL::stage_bytes + TL::b_off + lane * 16;
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
                     const int64_t c = kb * 2 + j;
@@ -179,9 +201,11 @@ __global__ void __launch_bounds__(kThreads) gemv_stream_kernel(
                     const bool cin = c < p.nch_b;
 #pragma unroll
                     for (int n = 0; n < NT; ++n) {
-                        b[n] = cin ? __ldg(p.bfrag + (n * p.nch_b + c) * 32 + lane) : make_uint4(0, 0, 0, 0);
+                        b[n] = cin ? lds128(bbase + ((n * TL::terms) * TL::chunks + j) * kFragBytes)
+                                   : make_uint4(0, 0, 0, 0);
                         if constexpr (TWO)
-                            bl[n] = cin ? __ldg(p.bfrag_lo + (n * p.nch_b + c) * 32 + lane) : make_uint4(0, 0, 0, 0);
+                            bl[n] = cin ? lds128(bbase + ((n * TL::terms + 1) * TL::chunks + j) * kFragBytes)
+                                        : make_uint4(0, 0, 0, 0);
                     }
                     const uint32_t off = static_cast<uint32_t>(((4 * j + tid) ^ g) << 4);
                     const uint4 a0 = lds128(wbase + ra * 128 + off);
@@ -199,6 +223,7 @@ __global__ void __launch_bounds__(kThreads) gemv_stream_kernel(
             } else {
                 // 256 k = two groups of four 32-value blocks; scales follow the nibbles
                 const uint32_t sbase = base + s * TL::stage_bytes + TL::nmat * TL::w_bytes + mat * TL::s_bytes;
+                const uint32_t bbase = base + s * TL::stage_bytes + TL::b_off + lane * 16;
                 const uint4 sa = lds128(sbase + ra * 16), sb = lds128(sbase + rb * 16);
 #pragma unroll
                 for (int grp = 0; grp < 2; ++grp) {
@@ -208,10 +233,9 @@ __global__ void __launch_bounds__(kThreads) gemv_stream_kernel(
 #pragma unroll
                     for (int blk = 0; blk < 4; ++blk) {
                         const int bi = 4 * grp + blk;            // block inside the stage, 0..7
-                        const int64_t c = kb * 8 + bi;
                         uint4 b[NT];
 #pragma unroll
-                        for (int n = 0; n < NT; ++n) b[n] = __ldg(p.bfrag + (n * p.nch_b + c) * 32 + lane);
+                        for (int n = 0; n < NT; ++n) b[n] = lds128(bbase + (n * TL::chunks + bi) * kFragBytes);
                         uint32_t lo[4], hi[4];
                         dequant_word(word_of(qa, blk), lo);
                         dequant_word(word_of(qb, blk), hi);
@@ -328,7 +352,7 @@ bool map_rows(CUtensorMap *m, const void *ptr, CUtensorMapDataType dt, int64_t i
 // Weight (and scale) maps of one matrix [rows x K] in format WF.
 template <int WF, int ROLE>
 bool weight_maps(CUtensorMap *w, CUtensorMap *sc, const GemvWeights &wt, int64_t rows, int64_t K) {
-    using TL = Tile<WF, ROLE>;
+    using TL = Tile<WF, ROLE, 1, false>;
     if (TL::q4) {
         if (!map_rows(w, wt.qs, CU_TENSOR_MAP_DATA_TYPE_UINT8, K / 2, rows, K / 2, 128, TL::box_rows, true))
             return false;
@@ -365,7 +389,7 @@ template <int WF, int NT, bool TWO>
 cudaError_t launch_stream_gateup(GemvWeights wg, GemvWeights wu, const void *nfrag, const void *nfrag_lo,
                                  void *hfrag, void *hfrag_lo, int64_t d, int64_t ffn, int64_t nchK,
                                  int64_t nchF, unsigned *counters, int ncounters, cudaStream_t s) {
-    using TL = Tile<WF, ROLE_GATEUP>;
+    using TL = Tile<WF, ROLE_GATEUP, NT, TWO>;
     constexpr auto kern = gemv_stream_kernel<WF, NT, TWO, ROLE_GATEUP>;
     cudaError_t e = set_smem<kern>(TL::smem_bytes);
     if (e != cudaSuccess) return e;
@@ -398,7 +422,7 @@ template <int WF, int NT, bool TWO>
 cudaError_t launch_stream_down(GemvWeights wd, const void *hfrag, const void *hfrag_lo, void *y,
                                float *partials, unsigned *counters, int rows, int64_t d, int64_t ffn,
                                int64_t nchF, int64_t splits, cudaStream_t s) {
-    using TL = Tile<WF, ROLE_DOWN>;
+    using TL = Tile<WF, ROLE_DOWN, NT, TWO>;
     constexpr auto kern = gemv_stream_kernel<WF, NT, TWO, ROLE_DOWN>;
     cudaError_t e = set_smem<kern>(TL::smem_bytes);
     if (e != cudaSuccess) return e;
