@@ -45,7 +45,8 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-sub", action="store_true", help="skip the secondary workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU baseline")
-    ap.add_argument("--workload", choices=["prefill", "decode", "decode_prepared", "q4"], default="prefill",
+    ap.add_argument("--workload", choices=["prefill", "decode", "decode_prepared", "q4", "rmsnorm", "swiglu"],
+                    default="prefill",
                     help="prefill: the benchmark; others run only that workload (for profiling)")
     ap.add_argument("--only-main", action="store_true",
                     help="time the main step only (no arm comparison, e2e, sub-workloads or CPU baseline)")
@@ -322,7 +323,19 @@ def run_workload_only(args):
     import torch
     from transformer_ffn_rmsnorm_gb300 import ffn
     device = torch.device("cuda", 0)
-    if args.workload == "q4":
+    if args.workload == "rmsnorm":
+        inp = synth.make_norm_inputs(synth.C2A_RMSNORM_F16, seed=0)
+        cfg = inp["cfg"]
+        x, gg = to_dev(inp["x"], "f16", torch, device), to_dev(inp["g"], "f16", torch, device)
+        n = torch.empty_like(x)
+        call = lambda i: ffn.ffn_rmsnorm(x, gg, cfg.eps, out=n)
+    elif args.workload == "swiglu":
+        inp = synth.make_swiglu_inputs(synth.C2B_SWIGLU_F16, seed=0)
+        cfg = inp["cfg"]
+        ga, up = to_dev(inp["gate"], "f16", torch, device), to_dev(inp["up"], "f16", torch, device)
+        h = torch.empty_like(ga)
+        call = lambda i: ffn.ffn_swiglu(ga, up, out=h)
+    elif args.workload == "q4":
         cfg, call = q4_setup(torch, ffn, device)
     else:
         cfg, call = decode_setup(torch, ffn, device, prepared=args.workload == "decode_prepared")

@@ -45,8 +45,11 @@ constexpr int kDnFeat = 16 * kDnTPC;    // features per down CTA
 
 // ---------------------------------------------------------------------------
 // 1. RMSNorm of <= 16 token rows, written in fragment order.
-//    One CTA per token slot; slots >= rows (and k >= K) are written as zeros.
-//    With TWO, nlo receives the rounding residual of every value (same order).
+//    grid = (token slots, slices): every CTA reduces its token's whole row
+//    (a few KB, cheap) and writes one slice of the fragments, so the kernel
+//    is not limited to one SM per token.  Slots >= rows (and k >= K) are
+//    written as zeros.  With TWO, nlo receives the rounding residual of every
+//    value (same order).
 template <int WF, bool TWO>
 __global__ void __launch_bounds__(256) gemv_norm_frag_kernel(const void *x_, const void *g_,
                                                              uint16_t *nfrag, uint16_t *nlo,
@@ -60,8 +63,9 @@ __global__ void __launch_bounds__(256) gemv_norm_frag_kernel(const void *x_, con
     const T *x = static_cast<const T *>(x_) + static_cast<int64_t>(token) * K;
     const T *g = static_cast<const T *>(g_);
     const int64_t ngroups = nch * 4;  // 8-element groups incl. the zero tail
+    const int64_t v0 = ngroups * blockIdx.y / gridDim.y, v1 = ngroups * (blockIdx.y + 1) / gridDim.y;
     if (token >= rows) {
-        for (int64_t v = threadIdx.x; v < ngroups; v += blockDim.x) {
+        for (int64_t v = v0 + threadIdx.x; v < v1; v += blockDim.x) {
             const int64_t k = 8 * v;
             if (q4) {
                 *reinterpret_cast<uint2 *>(nfrag + frag_elem(true, nch, token, k)) = make_uint2(0, 0);
@@ -95,7 +99,7 @@ __global__ void __launch_bounds__(256) gemv_norm_frag_kernel(const void *x_, con
     for (int w = 0; w < 8; ++w) ss += partial[w];
     const float inv = rsqrtf(ss / static_cast<float>(K) + eps);
 
-    for (int64_t v = threadIdx.x; v < ngroups; v += blockDim.x) {
+    for (int64_t v = v0 + threadIdx.x; v < v1; v += blockDim.x) {
         const int64_t k = 8 * v;
         float f[8];
         if (v < nv) {
@@ -434,7 +438,8 @@ cudaError_t launch_typed(const void *x, const void *gain, GemvWeights wg, GemvWe
     constexpr bool q4 = WF == WF_Q4;
     {
         LaunchScope scope(K_GEMV_NORM, s);
-        gemv_norm_frag_kernel<WF, TWO><<<8 * NT, 256, 0, s>>>(
+        const int64_t slices = std::min<int64_t>(16, cdiv(geo.nchK * 4, 256));
+        gemv_norm_frag_kernel<WF, TWO><<<dim3(8 * NT, static_cast<unsigned>(slices)), 256, 0, s>>>(
             x, gain, static_cast<uint16_t *>(ws.nfrag), static_cast<uint16_t *>(ws.nfrag_lo), rows, d,
             geo.nchK, eps);
         cudaError_t e = cudaGetLastError();

@@ -451,14 +451,16 @@ cudaError_t launch_stream_down(GemvWeights wd, const void *hfrag, const void *hf
     return cudaGetLastError();
 }
 
-// Down-projection splits for the streaming kernel: about 640 CTAs of 64 rows
-// (four per SM on a 152-SM part, plus slack), never finer than one k-block.
-// A function of the shape alone, so workspace queries agree with launches.
+// Down-projection splits for the streaming kernel: at most ~600 CTAs of 64
+// rows, i.e. one wave at four CTAs per SM on a 152-SM part, never finer than
+// one k-block.  A function of the shape alone, so workspace queries agree
+// with launches.
 int64_t stream_down_splits(int wfmt, int64_t d, int64_t ffn) {
     const int64_t groups = cdiv(d, 64);
     const int64_t kb = wfmt == WF_Q4 ? 256 : 64;
     const int64_t nkb = cdiv(ffn, kb);
-    int64_t splits = cdiv(640, groups);
+    int64_t splits = 600 / groups;
+    if (splits < 1) splits = 1;
     if (splits > nkb) splits = nkb;
     return cdiv(nkb, cdiv(nkb, splits));   // the splits the kernel will actually run
 }
