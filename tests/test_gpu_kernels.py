@@ -115,3 +115,23 @@ def test_swiglu_full_size_fp16(ffn, oracle_lib):
     got = to_host64(h[rows])
     assert_lowp(got, ref)              # the bf16 bound, applied to the fp16 workload
     assert_rounded(got, ref, "f16")    # and one fp16 rounding per element
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("d", [8, 520, 4096, 8192])
+def test_rmsnorm_many_rows(ffn, oracle_lib, dtype, d):
+    """Row counts that take the streaming (shared-memory ring) kernel."""
+    cfg = synth.NormConfig("t", 1000, d, 1e-5, dtype)
+    inp = synth.make_norm_inputs(cfg, seed=d + 3)
+    n = ffn.ffn_rmsnorm(to_dev(inp["x"], dtype), to_dev(inp["g"], dtype), eps=1e-5)
+    rows = np.unique(np.concatenate([[0, 303, 304, 999], np.random.default_rng(d).integers(0, 1000, 40)]))
+    ref = oracle_lib.rmsnorm(widen(inp["x"][rows], dtype), widen(inp["g"], dtype), 1e-5)
+    assert_rounded(to_host64(n[rows]), ref, dtype)
+
+
+def test_rmsnorm_many_rows_in_place(ffn, oracle_lib):
+    inp = synth.make_norm_inputs(synth.C2A_RMSNORM_F16, seed=9, rows=2000, d=1024)
+    x = to_dev(inp["x"], "f16")
+    ffn.ffn_rmsnorm(x, to_dev(inp["g"], "f16"), eps=1e-5, out=x)
+    ref = oracle_lib.rmsnorm(widen(inp["x"], "f16"), widen(inp["g"], "f16"), 1e-5)
+    assert_rounded(to_host64(x), ref, "f16")
