@@ -323,7 +323,7 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
     return __float2bfloat16_rn(v);
 }
 
-// 16 bytes <-> floats
+// 16 bytes <-> floats (paired conversions for the 16-bit types)
 template <typename T> struct Vec16 {
     static constexpr int N = 16 / sizeof(T);
     __device__ static __forceinline__ void unpack(const uint4 &v, float (&f)[16 / sizeof(T)]) {
@@ -336,6 +336,44 @@ template <typename T> struct Vec16 {
         T *e = reinterpret_cast<T *>(&v);
 #pragma unroll
         for (int i = 0; i < N; ++i) e[i] = from_f32<T>(f[i]);
+        return v;
+    }
+};
+template <> struct Vec16<__half> {
+    static constexpr int N = 8;
+    __device__ static __forceinline__ void unpack(const uint4 &v, float (&f)[8]) {
+        const __half2 *e = reinterpret_cast<const __half2 *>(&v);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 t = __half22float2(e[i]);
+            f[2 * i] = t.x;
+            f[2 * i + 1] = t.y;
+        }
+    }
+    __device__ static __forceinline__ uint4 pack(const float (&f)[8]) {
+        uint4 v;
+        __half2 *e = reinterpret_cast<__half2 *>(&v);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) e[i] = __floats2half2_rn(f[2 * i], f[2 * i + 1]);
+        return v;
+    }
+};
+template <> struct Vec16<__nv_bfloat16> {
+    static constexpr int N = 8;
+    __device__ static __forceinline__ void unpack(const uint4 &v, float (&f)[8]) {
+        const __nv_bfloat162 *e = reinterpret_cast<const __nv_bfloat162 *>(&v);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 t = __bfloat1622float2(e[i]);
+            f[2 * i] = t.x;
+            f[2 * i + 1] = t.y;
+        }
+    }
+    __device__ static __forceinline__ uint4 pack(const float (&f)[8]) {
+        uint4 v;
+        __nv_bfloat162 *e = reinterpret_cast<__nv_bfloat162 *>(&v);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) e[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
         return v;
     }
 };

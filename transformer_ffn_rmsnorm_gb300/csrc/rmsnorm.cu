@@ -126,16 +126,16 @@ __global__ void __launch_bounds__(256) rmsnorm_generic_kernel(const T *x,
 }
 
 // ---------------------------------------------------------------------------
-// Streaming variant for many rows: a persistent CTA's producer thread keeps a
-// ring of whole rows in shared memory with 1-D bulk copies (cp.async.bulk),
-// while eight warps reduce each row (fp32 squares, __shfl_xor_sync, a
-// shared-memory combine), scale it by rsqrt(ms + eps) * g (g staged in shared
-// memory once per CTA) and store it with 16-byte streaming stores.  Loads are
-// in flight continuously instead of in per-warp bursts.  Every mbarrier wait
-// is bounded (1 s) and sets the device status word when it gives up.
-constexpr int kNormConsumers = 8;
-constexpr int kNormThreads = 32 * (kNormConsumers + 1);
-constexpr int kNormMaxStages = 8;
+// Streaming variant for many rows: in a persistent CTA a producer thread
+// keeps one shared-memory slot per consumer warp filled with whole rows by
+// 1-D bulk copies (cp.async.bulk); each of the eight consumer warps owns one
+// slot and normalises its rows on its own (fp32 squares, __shfl_xor_sync, no
+// cross-warp barrier), scaling by rsqrt(ms + eps) * g with g staged in shared
+// memory once per CTA, and writes 16-byte streaming stores.  Loads stay in
+// flight continuously and sixteen rows are in process per SM.  Every mbarrier
+// wait is bounded (1 s) and sets the device status word when it gives up.
+constexpr int kNormWarps = 8;
+constexpr int kNormThreads = 32 * (kNormWarps + 1);
 constexpr uint64_t kNormWaitNs = 1000000000ull;
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
@@ -146,29 +146,24 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
     return v;
 }
 
-__device__ __forceinline__ void consumers_sync() {
-    asm volatile("bar.sync 1, %0;" ::"n"(32 * kNormConsumers) : "memory");
-}
-
 template <typename T, typename TO, bool SPLIT>
 __global__ void __launch_bounds__(kNormThreads) rmsnorm_stream_kernel(
-    const T *x, const T *__restrict__ g, TO *n, TO *nlo, int64_t rows, int d, float eps, int stages,
+    const T *x, const T *__restrict__ g, TO *n, TO *nlo, int64_t rows, int d, float eps,
     uint32_t row_bytes, unsigned *err) {
     constexpr int EPV = 16 / sizeof(T);
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t bar_full[kNormMaxStages], bar_empty[kNormMaxStages], bar_g;
-    __shared__ float partial[kNormConsumers];
+    __shared__ __align__(8) uint64_t bar_full[kNormWarps], bar_empty[kNormWarps], bar_g;
     __shared__ int s_abort, s_never;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t stride = (row_bytes + 127u) & ~127u;
     const uint32_t gsm = (ptx::smem_u32(smem_raw) + 127u) & ~127u;   // g, one row's worth
-    const uint32_t ring = gsm + stride;
+    const uint32_t ring = gsm + stride;                               // slot w: warp w's rows
     auto full = [&](int s) { return ptx::smem_u32(&bar_full[s]); };
     auto empty = [&](int s) { return ptx::smem_u32(&bar_empty[s]); };
     if (threadIdx.x == 0) {
-        for (int s = 0; s < stages; ++s) {
+        for (int s = 0; s < kNormWarps; ++s) {
             ptx::mbar_init(full(s), 1);
-            ptx::mbar_init(empty(s), kNormConsumers);
+            ptx::mbar_init(empty(s), 1);
         }
         ptx::mbar_init(ptx::smem_u32(&bar_g), 1);
         s_abort = 0;
@@ -181,14 +176,15 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_stream_kernel(
     int64_t issued = 0;
     const int nvec = d / EPV;
 
-    if (warp == kNormConsumers) {
+    if (warp == kNormWarps) {
         if (lane == 0) {
             ptx::mbar_arrive_expect_tx(ptx::smem_u32(&bar_g), row_bytes);
             ptx::bulk_load(gsm, g, row_bytes, ptx::smem_u32(&bar_g));
             bool ok = true;
+            // the i-th row of this CTA goes to slot i % kNormWarps (its k-th use)
             for (int64_t r = blockIdx.x; r < rows; r += gridDim.x, ++issued) {
-                const int s = static_cast<int>(issued % stages);
-                const uint32_t ph = static_cast<uint32_t>((issued / stages) & 1);
+                const int s = static_cast<int>(issued % kNormWarps);
+                const uint32_t ph = static_cast<uint32_t>((issued / kNormWarps) & 1);
                 if (!ptx::mbar_wait(empty(s), ph ^ 1u, abort_flag, kNormWaitNs)) {
                     ok = false;
                     break;
@@ -204,36 +200,31 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_stream_kernel(
     } else {
         const bool gok = ptx::mbar_wait(ptx::smem_u32(&bar_g), 0, abort_flag, kNormWaitNs);
         bool ok = __all_sync(0xffffffffu, gok);
-        int64_t it = 0;
-        for (int64_t r = blockIdx.x; ok && r < rows; r += gridDim.x, ++it) {
-            const int s = static_cast<int>(it % stages);
-            const uint32_t ph = static_cast<uint32_t>((it / stages) & 1);
-            const bool got = ptx::mbar_wait(full(s), ph, abort_flag, kNormWaitNs);
+        const uint32_t slot = ring + warp * stride;
+        for (int64_t k = 0; ok; ++k) {
+            const int64_t i = warp + k * kNormWarps;                      // this CTA's i-th row
+            const int64_t r = blockIdx.x + i * gridDim.x;
+            if (r >= rows) break;
+            const bool got = ptx::mbar_wait(full(warp), static_cast<uint32_t>(k & 1), abort_flag, kNormWaitNs);
             if (!__all_sync(0xffffffffu, got)) {
                 ok = false;
                 break;
             }
-            const uint32_t row = ring + s * stride;
             float ss = 0.f;
-            for (int v = threadIdx.x; v < nvec; v += 32 * kNormConsumers) {
+            for (int v = lane; v < nvec; v += 32) {
                 float f[EPV];
-                Vec16<T>::unpack(lds128(row + v * 16), f);
+                Vec16<T>::unpack(lds128(slot + v * 16), f);
 #pragma unroll
                 for (int e = 0; e < EPV; ++e) ss = fmaf(f[e], f[e], ss);
             }
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-            if (lane == 0) partial[warp] = ss;
-            consumers_sync();
-            ss = 0.f;
-#pragma unroll
-            for (int w = 0; w < kNormConsumers; ++w) ss += partial[w];
             const float inv = rsqrtf(ss / static_cast<float>(d) + eps);
             TO *nr = n + r * d;
             TO *lr = SPLIT ? nlo + r * d : nullptr;
-            for (int v = threadIdx.x; v < nvec; v += 32 * kNormConsumers) {
+            for (int v = lane; v < nvec; v += 32) {
                 float f[EPV], gf[EPV];
-                Vec16<T>::unpack(lds128(row + v * 16), f);
+                Vec16<T>::unpack(lds128(slot + v * 16), f);
                 Vec16<T>::unpack(lds128(gsm + v * 16), gf);
 #pragma unroll
                 for (int e = 0; e < EPV; ++e) f[e] = f[e] * inv * gf[e];
@@ -247,9 +238,8 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_stream_kernel(
                     __stcs(reinterpret_cast<uint4 *>(lr) + v, Vec16<TO>::pack(f));
                 }
             }
-            // every consumer has read the stage (and the partials) before either is reused
-            consumers_sync();
-            if (lane == 0) ptx::mbar_arrive(empty(s));
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(empty(warp));
         }
         if (!ok && lane == 0) {
             atomicOr(err, DEVERR_TIMEOUT);
@@ -257,42 +247,46 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_stream_kernel(
         }
     }
     __syncthreads();
-    if (warp == kNormConsumers && lane == 0) {
+    if (warp == kNormWarps && lane == 0) {
         ptx::mbar_wait(ptx::smem_u32(&bar_g), 0, never, kNormWaitNs);
-        for (int s = 0; s < stages; ++s)
+        for (int s = 0; s < kNormWarps; ++s)
             if (issued > s) {
-                const int64_t armed = (issued - s + stages - 1) / stages;
+                const int64_t armed = (issued - s + kNormWarps - 1) / kNormWarps;
                 ptx::mbar_wait(full(s), static_cast<uint32_t>((armed - 1) & 1), never, kNormWaitNs);
             }
     }
 }
+
+// Rows up to 16 KB: g plus one slot per consumer warp fit in ~144 KB.
+constexpr uint32_t kNormMaxRowBytes = 16 * 1024;
 
 template <typename T, typename TO, bool SPLIT>
 cudaError_t launch_stream(const void *x, const void *g, void *n, void *nlo, int64_t rows, int d, float eps,
                           cudaStream_t s) {
     const uint32_t row_bytes = static_cast<uint32_t>(d) * sizeof(T);
     const uint32_t stride = (row_bytes + 127u) & ~127u;
-    int stages = static_cast<int>((64u * 1024u) / stride);
-    stages = stages < 2 ? 2 : stages > kNormMaxStages ? kNormMaxStages : stages;
-    const size_t smem = static_cast<size_t>(stride) * (stages + 1) + 128;
+    const size_t smem = static_cast<size_t>(stride) * (kNormWarps + 1) + 128;
     static int configured = -1;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (configured != dev) {
         e = cudaFuncSetAttribute(rmsnorm_stream_kernel<T, TO, SPLIT>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kNormMaxRowBytes * (kNormWarps + 1) + 128));
         if (e != cudaSuccess) return e;
         configured = dev;
     }
     unsigned *err = device_status_word();
     if (!err) return cudaErrorUnknown;
-    int64_t grid = static_cast<int64_t>(sm_count()) * 2;
+    // as many CTAs as fit (two per SM at 8 KB rows), persistent over rows
+    const int per_sm = smem <= 100 * 1024 ? 2 : 1;
+    int64_t grid = static_cast<int64_t>(sm_count()) * per_sm;
     if (grid > rows) grid = rows;
     LaunchScope scope(K_RMSNORM, s);
     rmsnorm_stream_kernel<T, TO, SPLIT><<<static_cast<unsigned>(grid), kNormThreads, smem, s>>>(
         static_cast<const T *>(x), static_cast<const T *>(g), static_cast<TO *>(n), static_cast<TO *>(nlo),
-        rows, d, eps, stages, row_bytes, err);
+        rows, d, eps, row_bytes, err);
     return cudaGetLastError();
 }
 
@@ -326,8 +320,8 @@ cudaError_t launch_typed(const void *x, const void *g, void *n, void *nlo, int64
     constexpr int EPV = 16 / sizeof(T);
     const bool aligned = (d % EPV) == 0;
     const int64_t nvec = d / EPV;
-    // many rows: stream whole rows through shared memory (rows up to 32 KB)
-    if (aligned && rows >= 4 * static_cast<int64_t>(sm_count()) && d * sizeof(T) <= 32 * 1024)
+    // many rows: stream whole rows through shared memory
+    if (aligned && rows >= 4 * static_cast<int64_t>(sm_count()) && d * sizeof(T) <= kNormMaxRowBytes)
         return launch_stream<T, TO, SPLIT>(x, g, n, nlo, rows, static_cast<int>(d), eps, s);
     // registers hold the row when nvec <= 32 lanes * 8 warps * kMaxVPT
     if (aligned && nvec <= 32 * 8 * kMaxVPT) {
