@@ -16,17 +16,27 @@
 // "Packing and geometry in the unfused control"); only the epilogue differs.
 //
 // Kernel structure (one CTA per SM, persistent over output tiles):
-//   warp 0      one thread issues TMA loads of A (128 x 64) and B (256 x 64)
-//               bf16/fp16 tiles, 128-byte swizzled, into a 4-stage ring;
-//   warp 1      allocates 512 TMEM columns (two 128 x 256 fp32 accumulators);
-//               one thread issues tcgen05.mma (M=128, N=256, K=16) and
+//   warp 0      one thread issues TMA loads of A (128 x 64) and B (BN x 64)
+//               bf16/fp16 tiles, 128-byte swizzled, into a ring of as many
+//               stages as fit (4-5);
+//   warp 1      allocates 512 TMEM columns (two 128 x BN fp32 accumulators);
+//               one thread issues tcgen05.mma (M=128, N=BN, K=16) and
 //               tcgen05.commit to release ring slots and publish accumulators;
 //   warps 2-5   epilogue: tcgen05.ld rows of the finished accumulator, apply
 //               the epilogue, store 16-byte vectors, release the accumulator
 //               so the next tile's MMAs overlap this tile's epilogue.
+// CTAs run in clusters of two over row blocks 2i and 2i+1 of the same column
+// block: each loads its own A tile and one half of the common B tile with a
+// multicast TMA copy into both CTAs' rings, so every B byte leaves L2 once
+// per pair (a third less L2-to-SM traffic per flop for 256-wide tiles); a
+// ring slot is reused once the MMAs of both CTAs have released it.
+// The kernel is launched as a programmatic dependent of the kernel before it:
+// the first ring's worth of B (weights) is requested before that kernel has
+// finished, A (its output) only after.
 // Every mbarrier wait is bounded (1 s of wall time).  A wait that gives up
 // sets the device status word, tells the other roles to stop, waits (again
-// bounded) for its own TMA loads and MMAs in flight, and frees TMEM.
+// bounded) for its own TMA loads and MMAs in flight, and frees TMEM; the two
+// CTAs of a cluster leave together.
 #include <cudaTypedefs.h>
 
 #include <type_traits>
@@ -45,12 +55,24 @@ constexpr int NUM_THREADS = 192;
 // fp32 value (hi + lo); both are multiplied by the same B tile and accumulate
 // into the same TMEM accumulator, so A carries ~16 significant bits.
 // BN: accumulator columns per tile (256, or 224 for the plain GEMM when it
-// evens out the waves); the B tile is BN rows of 64 k values.
-template <int A_TERMS, int BN> struct Ring {
-    static constexpr uint32_t B_BYTES = BN * BK * 2;
-    static constexpr int STAGES = A_TERMS == 1 ? 4 : 3;
-    static constexpr uint32_t STAGE_BYTES = A_TERMS * A_BYTES + B_BYTES;
+// evens out the waves); the B tile is BN rows of 64 k values, all of them in
+// this CTA's ring, or (PAIR) BN/2 of them, the peer CTA holding the others.
+// The ring takes as many stages as fit in 225 KB; a CTA therefore always
+// holds more than half of the SM's shared memory, so two of these CTAs
+// (each allocating all of TMEM) never share an SM, not even while one kernel
+// overlaps the tail of the one before it.
+// KSUB: 64-wide k blocks per ring stage.  A pair stage holds two (one
+// barrier wait and one release per 8 MMAs instead of 4): the MMA thread's
+// per-stage overhead is not hidden by the tensor pipe's queue.
+template <int A_TERMS, int BN, bool PAIR> struct Ring {
+    static constexpr int KSUB = (PAIR && A_TERMS == 1) ? 2 : 1;
+    static constexpr uint32_t B_BYTES = (PAIR ? BN / 2 : BN) * BK * 2;   // this CTA's part of B, per k block
+    static constexpr uint32_t SUB_BYTES = A_TERMS * A_BYTES + B_BYTES;
+    static constexpr uint32_t STAGE_BYTES = KSUB * SUB_BYTES;
+    static constexpr int FIT = static_cast<int>((225u * 1024u) / STAGE_BYTES);
+    static constexpr int STAGES = FIT > 8 ? 8 : FIT;
     static constexpr size_t SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
+    static_assert(STAGES >= 3 && SMEM_BYTES > 114 * 1024, "ring");
 };
 constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;
 
@@ -60,21 +82,26 @@ struct GemmParams {
     int64_t M, N, K;          // N: output columns (ffn for gate/up, d for down)
     int64_t num_m_blocks, num_tiles;
     int num_k_blocks;
+    // CTAs per unit of work: 1, or 2 for a CTA pair (rows of row blocks 2i
+    // and 2i+1 against one column block, one M=256 MMA over both SMs)
+    int cluster;
+    int64_t num_m_pairs, num_units;
     void *out0, *out1;        // plain: C; fused: h (and its residual, or null); split: G, U
     int64_t ldo;              // output row stride in elements
     unsigned *err;
     uint64_t wait_limit_ns;
     float acc_scale;          // applied to every accumulator value (exact powers of two)
     float out_scale;          // fused: applied to h before rounding
+    int a_keep;               // keep A in L2 (evict-last): every wave of tiles re-reads it
 };
 
-// Stores 32 values rounded once; with `lo` also the rounding residual
-// v - round(v), rounded once, so that hi + lo carries ~16 significant bits.
-template <typename T>
-__device__ __forceinline__ void store_row32(T *dst, T *lo, int64_t col, int64_t ncols,
-                                            const float (&v)[32]) {
+// Stores NV (16 or 32) values rounded once; with `lo` also the rounding
+// residual v - round(v), rounded once, so that hi + lo carries ~16
+// significant bits.  Columns at or past ncols (a multiple of 8) are skipped.
+template <typename T, int NV>
+__device__ __forceinline__ void store_row(T *dst, T *lo, int64_t col, int64_t ncols, const float (&v)[NV]) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < NV / 8; ++j) {
         if (col + 8 * j < ncols) {
             float f[8];
 #pragma unroll
@@ -92,10 +119,10 @@ __device__ __forceinline__ void store_row32(T *dst, T *lo, int64_t col, int64_t 
     }
 }
 
-__device__ __forceinline__ void store_row32_f32(float *dst, int64_t col, int64_t ncols,
-                                               const float (&v)[32]) {
+template <int NV>
+__device__ __forceinline__ void store_row_f32(float *dst, int64_t col, int64_t ncols, const float (&v)[NV]) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
+    for (int j = 0; j < NV / 4; ++j)
         if (col + 4 * j < ncols)
             *reinterpret_cast<float4 *>(dst + col + 4 * j) =
                 make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
@@ -103,7 +130,17 @@ __device__ __forceinline__ void store_row32_f32(float *dst, int64_t col, int64_t
 
 // BF16: operand type (bf16 or fp16); OUT_BF16: type of the stored output
 // (plain mode; the fused h has the operand type, it feeds the next GEMM).
-template <int MODE, bool BF16, int A_TERMS, bool OUT_BF16, int BN>
+// PAIR: clusters of two CTAs on two SMs compute 256 x BN tiles with
+// tcgen05 .cta_group::2 MMAs issued by the even CTA.  Each CTA's ring holds
+// its own 128 rows of A and half of B (W_gate rows in the even CTA and W_up
+// rows in the odd one for gate/up; the two column halves for the plain
+// GEMM), so per flop an SM stores and feeds a third fewer operand bytes than
+// with one CTA per 128 x BN tile, and each B byte leaves L2 once per pair.
+// The pair's producers report their bytes to the even CTA's ring barriers;
+// the even CTA's MMA thread releases ring slots and publishes accumulators
+// to both CTAs; both epilogues (each reading its own TMEM rows) report to
+// the even CTA's accumulator barriers.
+template <int MODE, bool BF16, int A_TERMS, bool OUT_BF16, int BN, bool PAIR>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a,
                         const __grid_constant__ CUtensorMap map_a2,
@@ -111,10 +148,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         const __grid_constant__ CUtensorMap map_b1, const GemmParams p) {
     using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
     using TOut = typename std::conditional<OUT_BF16, __nv_bfloat16, __half>::type;
-    static_assert(BN % 32 == 0 && BN <= 256 && (MODE == MODE_PLAIN || BN == 256), "tile width");
-    constexpr int STAGES = Ring<A_TERMS, BN>::STAGES;
-    constexpr uint32_t STAGE_BYTES = Ring<A_TERMS, BN>::STAGE_BYTES;
-    constexpr uint32_t B_BYTES = Ring<A_TERMS, BN>::B_BYTES;
+    using RG = Ring<A_TERMS, BN, PAIR>;
+    static_assert(BN % 32 == 0 && BN <= 256 && (BN / 2) % 16 == 0, "tile width");
+    // epilogue chunk: 32 accumulator columns, or 16 when a half tile (gate
+    // or up part of a fused tile) is not a multiple of 32 wide
+    constexpr int CW = (MODE == MODE_PLAIN || (BN / 2) % 32 == 0) ? 32 : 16;
+    constexpr int STAGES = RG::STAGES, KSUB = RG::KSUB;
+    constexpr uint32_t STAGE_BYTES = RG::STAGE_BYTES, SUB_BYTES = RG::SUB_BYTES;
+    constexpr uint32_t B_BYTES = RG::B_BYTES;
+    constexpr int NCTA = PAIR ? 2 : 1;
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bar_full[STAGES], bar_empty[STAGES];
     __shared__ __align__(8) uint64_t bar_tfull[2], bar_tempty[2], bar_drain;
@@ -123,9 +165,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t base = (ptx::smem_u32(smem_raw) + 1023u) & ~1023u;
-    // stage s: A term 0 | A term 1 (if any) | B, each 1024-byte aligned
-    auto sA = [&](uint32_t s, int t) { return base + s * STAGE_BYTES + t * A_BYTES; };
-    auto sB = [&](uint32_t s) { return base + s * STAGE_BYTES + A_TERMS * A_BYTES; };
+    // stage s, k block j of it: A term 0 | A term 1 (if any) | B (or this
+    // CTA's half), each 1024-byte aligned
+    auto sA = [&](uint32_t s, int j, int t) { return base + s * STAGE_BYTES + j * SUB_BYTES + t * A_BYTES; };
+    auto sB = [&](uint32_t s, int j) { return base + s * STAGE_BYTES + j * SUB_BYTES + A_TERMS * A_BYTES; };
+    const int nst = (p.num_k_blocks + KSUB - 1) / KSUB;   // ring stages per tile
     auto full = [&](uint32_t s) { return ptx::smem_u32(&bar_full[s]); };
     auto empty = [&](uint32_t s) { return ptx::smem_u32(&bar_empty[s]); };
     auto tfull = [&](uint32_t a) { return ptx::smem_u32(&bar_tfull[a]); };
@@ -138,7 +182,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         for (int a = 0; a < 2; ++a) {
             ptx::mbar_init(tfull(a), 1);
-            ptx::mbar_init(tempty(a), 4);
+            ptx::mbar_init(tempty(a), 4 * NCTA);   // the epilogue warps of every CTA of the unit
         }
         ptx::mbar_init(ptx::smem_u32(&bar_drain), 1);
         s_abort = 0;
@@ -150,13 +194,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (MODE != MODE_PLAIN) ptx::tma_prefetch_map(&map_b1);
     }
     if (warp == 1) {
-        ptx::tmem_alloc(ptx::smem_u32(&s_tmem_base), TMEM_COLS);
-        ptx::tmem_relinquish();
+        if constexpr (PAIR) {
+            ptx::tmem_alloc_pair(ptx::smem_u32(&s_tmem_base), TMEM_COLS);
+            ptx::tmem_relinquish_pair();
+        } else {
+            ptx::tmem_alloc(ptx::smem_u32(&s_tmem_base), TMEM_COLS);
+            ptx::tmem_relinquish();
+        }
     }
     ptx::tc_fence_before();
     __syncthreads();
+    // both CTAs' barriers are initialised before either reports to the other
+    if constexpr (PAIR) ptx::cluster_sync();
     ptx::tc_fence_after();
+    // the next kernel on the stream may be scheduled once every CTA is running
+    ptx::griddep_launch_dependents();
     const uint32_t tmem_base = s_tmem_base;
+    const uint32_t rank = PAIR ? ptx::cluster_ctarank() : 0u;
+    const bool leader = rank == 0;
+    const int64_t unit0 = blockIdx.x / NCTA, unit_step = gridDim.x / NCTA;
+    auto m_blk_of = [&](int64_t u) { return (u % p.num_m_pairs) * NCTA + rank; };
+    auto n_blk_of = [&](int64_t u) { return u / p.num_m_pairs; };
+    // the barriers the pair shares live in the even CTA
+    auto lead = [&](uint32_t bar) { return PAIR ? ptx::mapa_shared(bar, 0) : bar; };
     volatile int *abort_flag = &s_abort;
     volatile int *never = &s_never;
     const uint64_t limit = p.wait_limit_ns;
@@ -164,28 +224,75 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     if (warp == 0 && lane == 0) {
         // ------------------------------------------------------ TMA producer
+        const uint64_t keep = ptx::l2_policy_evict_last();
+        auto load = [&](uint32_t dst, const CUtensorMap *map, uint32_t s, int x, int y, bool hint) {
+            if constexpr (PAIR) {
+                if (hint) ptx::tma_load_2d_pair_hint(dst, map, lead(full(s)), x, y, keep);
+                else ptx::tma_load_2d_pair(dst, map, lead(full(s)), x, y);
+            } else {
+                if (hint) ptx::tma_load_2d_hint(dst, map, full(s), x, y, keep);
+                else ptx::tma_load_2d(dst, map, full(s), x, y);
+            }
+        };
+        // stage s holds k blocks KSUB * kst .. (a block past K is TMA zero fill)
+        auto load_a = [&](uint32_t s, int kst, int m0) {
+#pragma unroll
+            for (int j = 0; j < KSUB; ++j) {
+                const int k0 = (kst * KSUB + j) * BK;
+                load(sA(s, j, 0), &map_a, s, k0, m0, p.a_keep != 0);
+                if (A_TERMS == 2) load(sA(s, j, 1), &map_a2, s, k0, m0, p.a_keep != 0);
+            }
+        };
+        auto load_b = [&](uint32_t s, int kst, int64_t n_blk) {
+#pragma unroll
+            for (int j = 0; j < KSUB; ++j) {
+                const int k0 = (kst * KSUB + j) * BK;
+                if constexpr (PAIR) {
+                    // plain: columns BN/2 * rank .. of the tile; gate/up: the
+                    // W_gate rows (even CTA) or the W_up rows (odd CTA)
+                    if (MODE == MODE_PLAIN)
+                        load(sB(s, j), &map_b0, s, k0, static_cast<int>(n_blk * BN + rank * (BN / 2)), false);
+                    else
+                        load(sB(s, j), rank ? &map_b1 : &map_b0, s, k0, static_cast<int>(n_blk * (BN / 2)), false);
+                } else if (MODE == MODE_PLAIN) {
+                    load(sB(s, j), &map_b0, s, k0, static_cast<int>(n_blk * BN), false);
+                } else {
+                    const int f0 = static_cast<int>(n_blk * (BN / 2));
+                    load(sB(s, j), &map_b0, s, k0, f0, false);
+                    load(sB(s, j) + B_BYTES / 2, &map_b1, s, k0, f0, false);
+                }
+            }
+        };
+        // the even CTA expects the bytes of the whole pair on its barrier
+        auto arm = [&](uint32_t s) {
+            if (leader) ptx::mbar_arrive_expect_tx(full(s), NCTA * STAGE_BYTES);
+        };
+        // The first ring's worth of B (weights: inputs of the call) is
+        // requested before the kernel that writes A has finished; A only
+        // after it has.  The grid never exceeds the unit count, so every CTA
+        // has a first unit.
+        const int npre = nst < STAGES ? nst : STAGES;
+        for (int kb = 0; kb < npre; ++kb) {
+            arm(kb);
+            load_b(kb, kb, n_blk_of(unit0));
+        }
+        ptx::griddep_wait();
+        for (int kb = 0; kb < npre; ++kb) load_a(kb, kb, static_cast<int>(m_blk_of(unit0) * BM));
+        produced = npre;
         bool ok = true;
-        for (int64_t t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
-            const int m0 = static_cast<int>((t % p.num_m_blocks) * BM);
-            const int64_t n_blk = t / p.num_m_blocks;
-            for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+        for (int64_t u = unit0; u < p.num_units && ok; u += unit_step) {
+            const int m0 = static_cast<int>(m_blk_of(u) * BM);
+            const int64_t n_blk = n_blk_of(u);
+            for (int kb = (u == unit0) ? npre : 0; kb < nst; ++kb) {
                 const uint32_t s = static_cast<uint32_t>(produced % STAGES);
                 const uint32_t ph = static_cast<uint32_t>((produced / STAGES) & 1);
                 if (!ptx::mbar_wait(empty(s), ph ^ 1u, abort_flag, limit)) {
                     ok = false;
                     break;
                 }
-                ptx::mbar_arrive_expect_tx(full(s), STAGE_BYTES);
-                const int k0 = kb * BK;
-                ptx::tma_load_2d(sA(s, 0), &map_a, full(s), k0, m0);
-                if (A_TERMS == 2) ptx::tma_load_2d(sA(s, 1), &map_a2, full(s), k0, m0);
-                if (MODE == MODE_PLAIN) {
-                    ptx::tma_load_2d(sB(s), &map_b0, full(s), k0, static_cast<int>(n_blk * BN));
-                } else {
-                    const int f0 = static_cast<int>(n_blk * (BN / 2));
-                    ptx::tma_load_2d(sB(s), &map_b0, full(s), k0, f0);
-                    ptx::tma_load_2d(sB(s) + B_BYTES / 2, &map_b1, full(s), k0, f0);
-                }
+                arm(s);
+                load_a(s, kb, m0);
+                load_b(s, kb, n_blk);
                 ++produced;
             }
         }
@@ -193,20 +300,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             atomicOr(p.err, DEVERR_TIMEOUT);
             *abort_flag = 1;
         }
-    } else if (warp == 1 && lane == 0) {
+    } else if (warp == 1 && lane == 0 && leader) {
         // -------------------------------------------------------- MMA issuer
-        constexpr uint32_t idesc = ptx::idesc_f16(BM, BN, BF16);
+        constexpr uint32_t idesc = ptx::idesc_f16(BM * NCTA, BN, BF16);
         bool ok = true;
         uint64_t consumed = 0;
         uint32_t acc = 0, acc_ph = 0;
-        for (int64_t t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+        for (int64_t u = unit0; u < p.num_units && ok; u += unit_step) {
             if (!ptx::mbar_wait(tempty(acc), acc_ph ^ 1u, abort_flag, limit)) {
                 ok = false;
                 break;
             }
             ptx::tc_fence_after();
             const uint32_t d_tmem = tmem_base + acc * BN;
-            for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+            for (int kb = 0; kb < nst; ++kb) {
                 const uint32_t s = static_cast<uint32_t>(consumed % STAGES);
                 const uint32_t ph = static_cast<uint32_t>((consumed / STAGES) & 1);
                 if (!ptx::mbar_wait(full(s), ph, abort_flag, limit)) {
@@ -214,21 +321,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     break;
                 }
                 ptx::tc_fence_after();
-                const uint32_t b0 = sB(s);
 #pragma unroll
-                for (int t = 0; t < A_TERMS; ++t) {
-                    const uint32_t a0 = sA(s, t);
+                for (int j = 0; j < KSUB; ++j) {
+                    const uint32_t b0 = sB(s, j);
 #pragma unroll
-                    for (int k = 0; k < BK / UMMA_K; ++k)
-                        ptx::tc_mma_f16(d_tmem, ptx::sdesc_k_sw128(a0 + k * UMMA_K * 2),
-                                        ptx::sdesc_k_sw128(b0 + k * UMMA_K * 2), idesc,
-                                        (kb | k | t) != 0 ? 1u : 0u);
+                    for (int t = 0; t < A_TERMS; ++t) {
+                        const uint32_t a0 = sA(s, j, t);
+#pragma unroll
+                        for (int k = 0; k < BK / UMMA_K; ++k) {
+                            const uint64_t ad = ptx::sdesc_k_sw128(a0 + k * UMMA_K * 2);
+                            const uint64_t bd = ptx::sdesc_k_sw128(b0 + k * UMMA_K * 2);
+                            const uint32_t accumulate = (kb | j | k | t) != 0 ? 1u : 0u;
+                            if constexpr (PAIR) ptx::tc_mma_f16_pair(d_tmem, ad, bd, idesc, accumulate);
+                            else ptx::tc_mma_f16(d_tmem, ad, bd, idesc, accumulate);
+                        }
+                    }
                 }
-                ptx::tc_commit(empty(s));
+                // the slot is free again in every CTA of the unit
+                if constexpr (PAIR) ptx::tc_commit_pair(empty(s), 0x3);
+                else ptx::tc_commit(empty(s));
                 ++consumed;
             }
             if (!ok) break;
-            ptx::tc_commit(tfull(acc));
+            if constexpr (PAIR) ptx::tc_commit_pair(tfull(acc), 0x3);
+            else ptx::tc_commit(tfull(acc));
             acc ^= 1u;
             if (acc == 0) acc_ph ^= 1u;
         }
@@ -237,17 +353,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             *abort_flag = 1;
         }
         // every MMA issued above must finish before TMEM is freed
-        ptx::tc_commit(ptx::smem_u32(&bar_drain));
+        if constexpr (PAIR) ptx::tc_commit_pair(ptx::smem_u32(&bar_drain), 0x1);
+        else ptx::tc_commit(ptx::smem_u32(&bar_drain));
         ptx::mbar_wait(ptx::smem_u32(&bar_drain), 0, never, limit);
     } else if (warp >= 2) {
         // ---------------------------------------------------------- epilogue
+        ptx::griddep_wait();   // outputs may be read by the kernel before this one
         const int q = warp & 3;   // this warp may read TMEM lanes 32q .. 32q+31
         bool ok = true;
         uint32_t acc = 0, acc_ph = 0;
         T *out0 = static_cast<T *>(p.out0);
         T *out1 = static_cast<T *>(p.out1);
-        for (int64_t t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
-            const int64_t m_blk = t % p.num_m_blocks, n_blk = t / p.num_m_blocks;
+        for (int64_t u = unit0; u < p.num_units; u += unit_step) {
+            const int64_t m_blk = m_blk_of(u), n_blk = n_blk_of(u);
             // every lane waits (each gets its own acquire); the vote keeps the
             // warp converged and in agreement before the warp-wide tcgen05.ld
             const bool got = ptx::mbar_wait(tfull(acc), acc_ph, abort_flag, limit);
@@ -261,53 +379,55 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
             if (MODE == MODE_PLAIN) {
 #pragma unroll 1
-                for (int c = 0; c < BN; c += 32) {
-                    uint32_t r[32];
-                    ptx::tmem_ld_32x32b_x32(taddr + c, r);
+                for (int c = 0; c < BN; c += CW) {
+                    uint32_t r[CW];
+                    ptx::tmem_ld_cols<CW>(taddr + c, r);
                     ptx::tmem_ld_wait();
-                    float v[32];
+                    float v[CW];
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]) * p.acc_scale;
+                    for (int j = 0; j < CW; ++j) v[j] = __uint_as_float(r[j]) * p.acc_scale;
                     if (live)
-                        store_row32<TOut>(static_cast<TOut *>(p.out0) + row * p.ldo, nullptr,
-                                          n_blk * BN + c, p.N, v);
+                        store_row<TOut, CW>(static_cast<TOut *>(p.out0) + row * p.ldo, nullptr, n_blk * BN + c,
+                                            p.N, v);
                 }
             } else {
 #pragma unroll 1
-                for (int c = 0; c < BN / 2; c += 32) {
-                    uint32_t rg[32], ru[32];
-                    ptx::tmem_ld_32x32b_x32(taddr + c, rg);
-                    ptx::tmem_ld_32x32b_x32(taddr + BN / 2 + c, ru);
+                for (int c = 0; c < BN / 2; c += CW) {
+                    uint32_t rg[CW], ru[CW];
+                    ptx::tmem_ld_cols<CW>(taddr + c, rg);
+                    ptx::tmem_ld_cols<CW>(taddr + BN / 2 + c, ru);
                     ptx::tmem_ld_wait();
                     const int64_t col = n_blk * (BN / 2) + c;
                     if (MODE == MODE_GATEUP_FUSED) {
-                        float h[32];
+                        float h[CW];
 #pragma unroll
-                        for (int j = 0; j < 32; ++j)
+                        for (int j = 0; j < CW; ++j)
                             h[j] = silu_f32(__uint_as_float(rg[j]) * p.acc_scale) *
                                    (__uint_as_float(ru[j]) * p.acc_scale) * p.out_scale;
                         if (live)
-                            store_row32<T>(out0 + row * p.ldo, out1 ? out1 + row * p.ldo : nullptr,
-                                           col, p.N, h);
+                            store_row<T, CW>(out0 + row * p.ldo, out1 ? out1 + row * p.ldo : nullptr, col, p.N, h);
                     } else {
-                        float g[32], u[32];
+                        float gv[CW], uv[CW];
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            g[j] = __uint_as_float(rg[j]) * p.acc_scale;
-                            u[j] = __uint_as_float(ru[j]) * p.acc_scale;
+                        for (int j = 0; j < CW; ++j) {
+                            gv[j] = __uint_as_float(rg[j]) * p.acc_scale;
+                            uv[j] = __uint_as_float(ru[j]) * p.acc_scale;
                         }
                         // G and U stay fp32 so that h is rounded exactly
                         // once, as in the fused arm
                         if (live) {
-                            store_row32_f32(static_cast<float *>(p.out0) + row * p.ldo, col, p.N, g);
-                            store_row32_f32(static_cast<float *>(p.out1) + row * p.ldo, col, p.N, u);
+                            store_row_f32<CW>(static_cast<float *>(p.out0) + row * p.ldo, col, p.N, gv);
+                            store_row_f32<CW>(static_cast<float *>(p.out1) + row * p.ldo, col, p.N, uv);
                         }
                     }
                 }
             }
             ptx::tc_fence_before();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(tempty(acc));
+            if (lane == 0) {
+                if (PAIR && !leader) ptx::mbar_arrive_cluster(lead(tempty(acc)));
+                else ptx::mbar_arrive(tempty(acc));
+            }
             acc ^= 1u;
             if (acc == 0) acc_ph ^= 1u;
         }
@@ -318,9 +438,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
 
     __syncthreads();
-    if (warp == 0 && lane == 0) {
+    if (warp == 0 && lane == 0 && leader) {
         // TMA loads still in flight (only after an abandoned wait) must land
-        // before this CTA's shared memory is released.
+        // before shared memory is released; the even CTA's ring barriers
+        // count the bytes of both CTAs of a pair.
         for (uint32_t s = 0; s < STAGES; ++s) {
             if (produced > s) {
                 const uint64_t armed = (produced - s + STAGES - 1) / STAGES;
@@ -328,10 +449,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
         }
     }
+    if constexpr (PAIR) {
+        // neither CTA of the pair leaves (or frees TMEM) while the other may
+        // still copy into its shared memory, arrive on its barriers or
+        // read the accumulators
+        __syncthreads();
+        ptx::cluster_sync();
+    }
     if (warp == 1) {
         __syncwarp();
         ptx::tc_fence_after();
-        ptx::tmem_dealloc(tmem_base, TMEM_COLS);
+        if constexpr (PAIR) ptx::tmem_dealloc_pair(tmem_base, TMEM_COLS);
+        else ptx::tmem_dealloc(tmem_base, TMEM_COLS);
     }
 }
 
@@ -382,29 +511,49 @@ bool make_map(CUtensorMap *m, const void *ptr, bool bf16, int64_t inner, int64_t
     return r == CUDA_SUCCESS;
 }
 
-template <int MODE, bool BF16, int A_TERMS, bool OUT_BF16 = BF16, int BN = 256>
-cudaError_t launch_impl(const void *A, const void *A2, const void *B0, const void *B1, void *out0,
-                        void *out1, int64_t M, int64_t K, int64_t N, int kind, float acc_scale,
-                        float out_scale, cudaStream_t s) {
-    if (M <= 0) return cudaSuccess;
-    constexpr size_t SMEM_BYTES = Ring<A_TERMS, BN>::SMEM_BYTES;
-    static int configured_device = -1;
+template <int MODE, bool BF16, int A_TERMS, bool OUT_BF16, int BN, bool PAIR>
+cudaError_t launch_kernel(const void *A, const void *A2, const void *B0, const void *B1, void *out0,
+                          void *out1, int64_t M, int64_t K, int64_t N, int kind, float acc_scale,
+                          float out_scale, cudaStream_t s) {
+    constexpr size_t SMEM_BYTES = Ring<A_TERMS, BN, PAIR>::SMEM_BYTES;
+    constexpr int NCTA = PAIR ? 2 : 1;
+    const auto kern = &gemm_tcgen05_kernel<MODE, BF16, A_TERMS, OUT_BF16, BN, PAIR>;
+    static int configured_device = -1, slots = 0;   // co-resident units (CTAs or pairs)
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (configured_device != dev) {
-        e = cudaFuncSetAttribute(gemm_tcgen05_kernel<MODE, BF16, A_TERMS, OUT_BF16, BN>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(SMEM_BYTES));
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(SMEM_BYTES));
         if (e != cudaSuccess) return e;
+        slots = sm_count();
+        if (PAIR) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(2 * static_cast<unsigned>(sm_count()));
+            cfg.blockDim = dim3(NUM_THREADS);
+            cfg.dynamicSmemBytes = SMEM_BYTES;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = 2;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            e = cudaOccupancyMaxActiveClusters(&slots, kern, &cfg);
+            if (e != cudaSuccess) return e;
+        }
+        if (slots < 1) return cudaErrorLaunchOutOfResources;
         configured_device = dev;
     }
+    const int64_t num_m_blocks = (M + BM - 1) / BM;
+    const int64_t ncols = MODE == MODE_PLAIN ? BN : BN / 2;
+    const int64_t num_n_blocks = (N + ncols - 1) / ncols;
     CUtensorMap ma, ma2, mb0, mb1;
     if (!make_map(&ma, A, BF16, K, M, BM)) return cudaErrorInvalidValue;
     ma2 = ma;
     if (A_TERMS == 2 && !make_map(&ma2, A2, BF16, K, M, BM)) return cudaErrorInvalidValue;
     if (MODE == MODE_PLAIN) {
-        if (!make_map(&mb0, B0, BF16, K, N, BN)) return cudaErrorInvalidValue;
+        // with a pair, each CTA loads half of the B tile
+        if (!make_map(&mb0, B0, BF16, K, N, static_cast<uint32_t>(BN / NCTA))) return cudaErrorInvalidValue;
         mb1 = mb0;
     } else {
         if (!make_map(&mb0, B0, BF16, K, N, BN / 2)) return cudaErrorInvalidValue;
@@ -414,11 +563,12 @@ cudaError_t launch_impl(const void *A, const void *A2, const void *B0, const voi
     p.M = M;
     p.N = N;
     p.K = K;
-    p.num_m_blocks = (M + BM - 1) / BM;
-    const int64_t ncols = MODE == MODE_PLAIN ? BN : BN / 2;
-    const int64_t num_n_blocks = (N + ncols - 1) / ncols;
-    p.num_tiles = p.num_m_blocks * num_n_blocks;
+    p.num_m_blocks = num_m_blocks;
+    p.num_tiles = num_m_blocks * num_n_blocks;
     p.num_k_blocks = static_cast<int>((K + BK - 1) / BK);
+    p.cluster = NCTA;
+    p.num_m_pairs = (num_m_blocks + NCTA - 1) / NCTA;
+    p.num_units = p.num_m_pairs * num_n_blocks;
     p.out0 = out0;
     p.out1 = out1;
     p.ldo = N;
@@ -426,43 +576,54 @@ cudaError_t launch_impl(const void *A, const void *A2, const void *B0, const voi
     p.wait_limit_ns = WAIT_LIMIT_NS;
     p.acc_scale = acc_scale;
     p.out_scale = out_scale;
+    // every wave of tiles re-reads all of A (tiles are ordered row block
+    // fastest); ask L2 to keep it when it fits comfortably
+    p.a_keep = (num_n_blocks > 1 && M * K * 2 * A_TERMS <= (int64_t{96} << 20)) ? 1 : 0;
     if (!p.err) return cudaErrorUnknown;
-    int64_t grid = sm_count();
-    if (grid > p.num_tiles) grid = p.num_tiles;
+    // persistent: one unit of CTAs per co-resident slot, never more units
+    // than there is work for
+    int64_t units = slots;
+    if (units > p.num_units) units = p.num_units;
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(units * NCTA));
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = static_cast<unsigned>(NCTA);
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = PAIR ? 2 : 1;
     LaunchScope scope(kind, s);
-    gemm_tcgen05_kernel<MODE, BF16, A_TERMS, OUT_BF16, BN>
-        <<<static_cast<unsigned>(grid), NUM_THREADS, SMEM_BYTES, s>>>(ma, ma2, mb0, mb1, p);
-    return cudaGetLastError();
+    e = cudaLaunchKernelEx(&cfg, kern, ma, ma2, mb0, mb1, p);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-}  // namespace
-
-cudaError_t launch_gemm_gateup(int dt, const void *A, const void *A_lo, const void *Wg,
-                               const void *Wu, void *H, void *H_lo, void *G, void *U, int64_t M,
-                               int64_t K, int64_t F, bool fused, float acc_scale, float out_scale,
-                               cudaStream_t s) {
-    const bool bf = dt == DT_BF16;
-    const int k = K_GEMM_GATEUP;
-    const float a = acc_scale, o = out_scale;
-    if (A_lo) {
-        if (fused)
-            return bf ? launch_impl<MODE_GATEUP_FUSED, true, 2>(A, A_lo, Wg, Wu, H, H_lo, M, K, F, k, a, o, s)
-                      : launch_impl<MODE_GATEUP_FUSED, false, 2>(A, A_lo, Wg, Wu, H, H_lo, M, K, F, k, a, o, s);
-        return bf ? launch_impl<MODE_GATEUP_SPLIT, true, 2>(A, A_lo, Wg, Wu, G, U, M, K, F, k, a, o, s)
-                  : launch_impl<MODE_GATEUP_SPLIT, false, 2>(A, A_lo, Wg, Wu, G, U, M, K, F, k, a, o, s);
-    }
-    if (fused)
-        return bf ? launch_impl<MODE_GATEUP_FUSED, true, 1>(A, nullptr, Wg, Wu, H, H_lo, M, K, F, k, a, o, s)
-                  : launch_impl<MODE_GATEUP_FUSED, false, 1>(A, nullptr, Wg, Wu, H, H_lo, M, K, F, k, a, o, s);
-    return bf ? launch_impl<MODE_GATEUP_SPLIT, true, 1>(A, nullptr, Wg, Wu, G, U, M, K, F, k, a, o, s)
-              : launch_impl<MODE_GATEUP_SPLIT, false, 1>(A, nullptr, Wg, Wu, G, U, M, K, F, k, a, o, s);
+// CTA pairs whenever there are at least two row blocks to pair up.
+template <int MODE, bool BF16, int A_TERMS, bool OUT_BF16 = BF16, int BN = 256>
+cudaError_t launch_impl(const void *A, const void *A2, const void *B0, const void *B1, void *out0,
+                        void *out1, int64_t M, int64_t K, int64_t N, int kind, float acc_scale,
+                        float out_scale, cudaStream_t s) {
+    if (M <= 0) return cudaSuccess;
+    if (M > BM)
+        return launch_kernel<MODE, BF16, A_TERMS, OUT_BF16, BN, true>(A, A2, B0, B1, out0, out1, M, K, N, kind,
+                                                                       acc_scale, out_scale, s);
+    return launch_kernel<MODE, BF16, A_TERMS, OUT_BF16, BN, false>(A, A2, B0, B1, out0, out1, M, K, N, kind,
+                                                                    acc_scale, out_scale, s);
 }
 
-// Tile width for the plain GEMM: waves of tiles times the width of a tile
-// (time per wave scales with it); e.g. 4096 columns on 152 SMs with 32 row
-// blocks: 256 wide -> 512 tiles, 4 waves (the last 37 % full); 224 wide ->
-// 608 tiles, exactly 4 full waves.
-int plain_tile_width(int64_t M, int64_t N) {
+// Tile width of the plain GEMM: waves of tiles times the width of a tile
+// (the time of a wave scales with it).  E.g. 4096 rows onto 4096 columns:
+// 224-wide tiles make 608 tiles, exactly 4 waves on 152 SMs (256 wide: 512
+// tiles, the 4th wave 37 % full).  The gate/up GEMM keeps 256 (128 + 128):
+// on 4096 x 11008, 112 + 112 tiles evened the waves (20.8 against 18.1) but
+// ran 6 % slower, a narrower tile moving more operand bytes from L2 per flop.
+int tile_width(int64_t M, int64_t N) {
     const int64_t mb = (M + BM - 1) / BM;
     const int64_t sms = sm_count();
     int best = 256;
@@ -478,10 +639,40 @@ int plain_tile_width(int64_t M, int64_t N) {
     return best;
 }
 
+template <int MODE, bool BF16, int A_TERMS>
+cudaError_t launch_gateup_bn(const void *A, const void *A2, const void *B0, const void *B1, void *out0,
+                             void *out1, int64_t M, int64_t K, int64_t N, float acc_scale, float out_scale,
+                             cudaStream_t s) {
+    return launch_impl<MODE, BF16, A_TERMS, BF16, 256>(A, A2, B0, B1, out0, out1, M, K, N, K_GEMM_GATEUP,
+                                                       acc_scale, out_scale, s);
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_gateup(int dt, const void *A, const void *A_lo, const void *Wg,
+                               const void *Wu, void *H, void *H_lo, void *G, void *U, int64_t M,
+                               int64_t K, int64_t F, bool fused, float acc_scale, float out_scale,
+                               cudaStream_t s) {
+    const bool bf = dt == DT_BF16;
+    const float a = acc_scale, o = out_scale;
+    if (A_lo) {
+        if (fused)
+            return bf ? launch_gateup_bn<MODE_GATEUP_FUSED, true, 2>(A, A_lo, Wg, Wu, H, H_lo, M, K, F, a, o, s)
+                      : launch_gateup_bn<MODE_GATEUP_FUSED, false, 2>(A, A_lo, Wg, Wu, H, H_lo, M, K, F, a, o, s);
+        return bf ? launch_gateup_bn<MODE_GATEUP_SPLIT, true, 2>(A, A_lo, Wg, Wu, G, U, M, K, F, a, o, s)
+                  : launch_gateup_bn<MODE_GATEUP_SPLIT, false, 2>(A, A_lo, Wg, Wu, G, U, M, K, F, a, o, s);
+    }
+    if (fused)
+        return bf ? launch_gateup_bn<MODE_GATEUP_FUSED, true, 1>(A, nullptr, Wg, Wu, H, H_lo, M, K, F, a, o, s)
+                  : launch_gateup_bn<MODE_GATEUP_FUSED, false, 1>(A, nullptr, Wg, Wu, H, H_lo, M, K, F, a, o, s);
+    return bf ? launch_gateup_bn<MODE_GATEUP_SPLIT, true, 1>(A, nullptr, Wg, Wu, G, U, M, K, F, a, o, s)
+              : launch_gateup_bn<MODE_GATEUP_SPLIT, false, 1>(A, nullptr, Wg, Wu, G, U, M, K, F, a, o, s);
+}
+
 template <bool BF16, int A_TERMS, bool OUT_BF16>
 cudaError_t launch_plain_bn(const void *A, const void *A_lo, const void *B, void *C, int64_t M,
                             int64_t K, int64_t N, float acc_scale, cudaStream_t s) {
-    if (plain_tile_width(M, N) == 224)
+    if (tile_width(M, N) == 224)
         return launch_impl<MODE_PLAIN, BF16, A_TERMS, OUT_BF16, 224>(A, A_lo, B, nullptr, C, nullptr, M, K,
                                                                      N, K_GEMM_DOWN, acc_scale, 1.f, s);
     return launch_impl<MODE_PLAIN, BF16, A_TERMS, OUT_BF16, 256>(A, A_lo, B, nullptr, C, nullptr, M, K, N,

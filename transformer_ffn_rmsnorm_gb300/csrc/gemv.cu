@@ -59,6 +59,8 @@ __global__ void __launch_bounds__(256) gemv_norm_frag_kernel(const void *x_, con
     using TO = typename Fmt<WF>::TOp;
     constexpr bool q4 = WF == WF_Q4;
     __shared__ float partial[8];
+    // the projection kernel after this one may start its weight stream now
+    ptx::griddep_launch_dependents();
     const int token = blockIdx.x;
     const T *x = static_cast<const T *>(x_) + static_cast<int64_t>(token) * K;
     const T *g = static_cast<const T *>(g_);

@@ -67,16 +67,28 @@ template <> struct Fmt<WF_F16P> {
 // Returns (u - 8) as fp16 pairs:
 //   r[0] = (e0, e2), r[1] = (e16, e18), r[2] = (e1, e3), r[3] = (e17, e19)
 // relative to element 4*tid of the block.  0x6400 is fp16 1024.0, whose ulp
-// is 1, so 0x6400 | u is exactly 1024 + u, and subtracting 1032 gives u - 8
-// exactly.
+// is 1: OR-ing a low nibble u into its mantissa gives exactly 1024 + u, and
+// subtracting 1032 gives u - 8.  A high nibble is OR-ed in where it sits
+// (mantissa bits 4-7), giving 1024 + 16u exactly; (1024 + 16u) / 16 - 72 =
+// u - 8 is one fp16 FMA whose exact result is representable.  One shift and
+// four LOP3s per word on the integer pipe, four fp16 ops on the FMA pipe.
+__device__ __forceinline__ uint32_t lop_and_or(uint32_t a, uint32_t mask, uint32_t bits) {
+    uint32_t r;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(a), "r"(mask), "r"(bits));   // (a & mask) | bits
+    return r;
+}
+
 __device__ __forceinline__ void dequant_word(uint32_t w, uint32_t (&r)[4]) {
     const __half2 k1032 = __floats2half2_rn(1032.f, 1032.f);
+    const __half2 k16th = __floats2half2_rn(0.0625f, 0.0625f);
+    const __half2 k72 = __floats2half2_rn(-72.f, -72.f);
+    const uint32_t w8 = w >> 8;
+    uint32_t v[4] = {lop_and_or(w, 0x000F000Fu, 0x64006400u), lop_and_or(w, 0x00F000F0u, 0x64006400u),
+                     lop_and_or(w8, 0x000F000Fu, 0x64006400u), lop_and_or(w8, 0x00F000F0u, 0x64006400u)};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const uint32_t sh = (i == 0) ? 0 : (i == 1) ? 4 : (i == 2) ? 8 : 12;
-        uint32_t v = ((w >> sh) & 0x000F000Fu) | 0x64006400u;
-        __half2 b = *reinterpret_cast<__half2 *>(&v);
-        b = __hsub2(b, k1032);
+        __half2 b = *reinterpret_cast<__half2 *>(&v[i]);
+        b = (i & 1) ? __hfma2(b, k16th, k72) : __hsub2(b, k1032);
         r[i] = *reinterpret_cast<uint32_t *>(&b);
     }
 }

@@ -18,6 +18,11 @@
 // W_down over one split of ffn and hands its partial sums to the same
 // deterministic last-CTA reduction as the register kernels.
 //
+// Both kernels are launched as programmatic dependents of the kernel before
+// them: a CTA starts while that kernel is still running, requests its first
+// ring's worth of weights (inputs of the call) at once, and waits for that
+// kernel to complete before it requests any activation or writes anything.
+//
 // Every mbarrier wait is bounded (1 s); a wait that gives up records
 // FFN_ERR_TIMEOUT in the device status word, stops the other roles, and the
 // producer waits (bounded) for its copies in flight before the CTA exits.
@@ -116,9 +121,9 @@ __global__ void __launch_bounds__(kThreads) gemv_stream_kernel(
         s_never = 0;
         ptx::fence_mbar_init();
     }
-    if (ROLE == ROLE_GATEUP && blockIdx.x == 0)
-        for (int i = threadIdx.x; i < p.ncounters; i += blockDim.x) p.counters[i] = 0u;
     __syncthreads();
+    // the next kernel on the stream may be scheduled once every CTA is running
+    ptx::griddep_launch_dependents();
     volatile int *abort_flag = &s_abort;
     volatile int *never = &s_never;
     int64_t issued = 0;
@@ -128,38 +133,62 @@ __global__ void __launch_bounds__(kThreads) gemv_stream_kernel(
         if (lane == 0) {
             ptx::tma_prefetch_map(&map_w0);
             if (TL::nmat == 2) ptx::tma_prefetch_map(&map_w1);
+            // activation chunks of a k range that exist (the last 64-wide
+            // block can hang one chunk past the buffer)
+            auto nvalid = [&](int64_t kb) {
+                const int64_t left = p.nch_b - kb * TL::chunks;
+                return static_cast<uint32_t>(left < TL::chunks ? left : TL::chunks);
+            };
+            auto stage_of = [&](int64_t i) { return base + static_cast<uint32_t>(i % kStages) * TL::stage_bytes; };
+            auto arm = [&](int64_t i, int64_t kb) {
+                ptx::mbar_arrive_expect_tx(full(static_cast<int>(i % kStages)),
+                                           TL::b_off + NT * TL::terms * nvalid(kb) * kFragBytes);
+            };
+            auto load_weights = [&](int64_t i, int64_t kb) {
+                const uint32_t st = stage_of(i), bar = full(static_cast<int>(i % kStages));
+                const int x = static_cast<int>(kb * (q4 ? 128 : 64));   // bytes of nibbles / elements
+                const int y = static_cast<int>(row0);
+                ptx::tma_load_2d(st, &map_w0, bar, x, y);
+                if (TL::nmat == 2) ptx::tma_load_2d(st + TL::w_bytes, &map_w1, bar, x, y);
+                if (q4) {
+                    const uint32_t sc = st + TL::nmat * TL::w_bytes;
+                    ptx::tma_load_2d(sc, &map_s0, bar, static_cast<int>(kb * 8), y);
+                    if (TL::nmat == 2) ptx::tma_load_2d(sc + TL::s_bytes, &map_s1, bar, static_cast<int>(kb * 8), y);
+                }
+            };
+            auto load_acts = [&](int64_t i, int64_t kb) {
+                const uint32_t st = stage_of(i), bar = full(static_cast<int>(i % kStages));
+                const uint32_t nv = nvalid(kb);
+#pragma unroll
+                for (int n = 0; n < NT; ++n)
+#pragma unroll
+                    for (int t = 0; t < TL::terms; ++t)
+                        ptx::bulk_load(st + TL::b_off + (n * TL::terms + t) * TL::chunks * kFragBytes,
+                                       (t ? p.bfrag_lo : p.bfrag) + (n * p.nch_b + kb * TL::chunks) * 32,
+                                       nv * kFragBytes, bar);
+            };
+            // The first ring's worth of weights is requested before the kernel
+            // that writes the activations has finished (weights are inputs of
+            // the call); the activations only after it has.
+            const int64_t npre = (kb1 - kb0) < kStages ? (kb1 - kb0) : kStages;
+            for (int64_t i = 0; i < npre; ++i) {
+                arm(i, kb0 + i);
+                load_weights(i, kb0 + i);
+            }
+            issued = npre;
+            ptx::griddep_wait();
+            for (int64_t i = 0; i < npre; ++i) load_acts(i, kb0 + i);
             bool ok = true;
-            for (int64_t kb = kb0; kb < kb1; ++kb, ++issued) {
+            for (int64_t kb = kb0 + npre; kb < kb1; ++kb, ++issued) {
                 const int s = static_cast<int>(issued % kStages);
                 const uint32_t ph = static_cast<uint32_t>((issued / kStages) & 1);
                 if (!ptx::mbar_wait(empty(s), ph ^ 1u, abort_flag, kWaitNs)) {
                     ok = false;
                     break;
                 }
-                const uint32_t st = base + s * TL::stage_bytes;
-                // activation chunks of this k range that exist (the last
-                // 64-wide block can hang one chunk past the buffer)
-                const int64_t c0 = kb * TL::chunks;
-                const int64_t left = p.nch_b - c0;
-                const uint32_t nvalid = static_cast<uint32_t>(left < TL::chunks ? left : TL::chunks);
-                ptx::mbar_arrive_expect_tx(full(s), TL::b_off + NT * TL::terms * nvalid * kFragBytes);
-#pragma unroll
-                for (int n = 0; n < NT; ++n)
-#pragma unroll
-                    for (int t = 0; t < TL::terms; ++t)
-                        ptx::bulk_load(st + TL::b_off + (n * TL::terms + t) * TL::chunks * kFragBytes,
-                                       (t ? p.bfrag_lo : p.bfrag) + (n * p.nch_b + c0) * 32,
-                                       nvalid * kFragBytes, full(s));
-                const int x = static_cast<int>(kb * (q4 ? 128 : 64));   // bytes of nibbles / elements
-                const int y = static_cast<int>(row0);
-                ptx::tma_load_2d(st, &map_w0, full(s), x, y);
-                if (TL::nmat == 2) ptx::tma_load_2d(st + TL::w_bytes, &map_w1, full(s), x, y);
-                if (q4) {
-                    const uint32_t sc = st + TL::nmat * TL::w_bytes;
-                    ptx::tma_load_2d(sc, &map_s0, full(s), static_cast<int>(kb * 8), y);
-                    if (TL::nmat == 2)
-                        ptx::tma_load_2d(sc + TL::s_bytes, &map_s1, full(s), static_cast<int>(kb * 8), y);
-                }
+                arm(issued, kb);
+                load_acts(issued, kb);
+                load_weights(issued, kb);
             }
             if (!ok) {
                 atomicOr(p.err, DEVERR_TIMEOUT);
@@ -168,6 +197,9 @@ __global__ void __launch_bounds__(kThreads) gemv_stream_kernel(
         }
     } else {
         // ------------------------------------------------------ MMA warps
+        ptx::griddep_wait();
+        if (ROLE == ROLE_GATEUP && blockIdx.x == 0)   // arrival counters of this call's down projection
+            for (int i = threadIdx.x; i < p.ncounters; i += 32 * kConsumers) p.counters[i] = 0u;
         const int g = lane >> 2, tid = lane & 3;
         const int mat = ROLE == ROLE_GATEUP ? (warp >> 1) : 0;
         const int r0 = 16 * (ROLE == ROLE_GATEUP ? (warp & 1) : warp);   // row tile inside the box
@@ -225,6 +257,14 @@ __global__ void __launch_bounds__(kThreads) gemv_stream_kernel(
                 const uint32_t sbase = base + s * TL::stage_bytes + TL::nmat * TL::w_bytes + mat * TL::s_bytes;
                 const uint32_t bbase = base + s * TL::stage_bytes + TL::b_off + lane * 16;
                 const uint4 sa = lds128(sbase + ra * 16), sb = lds128(sbase + rb * 16);
+                // the stage's eight block scales of rows ra and rb, widened in pairs
+                float2 fsa[4], fsb[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t a = word_of(sa, j), b = word_of(sb, j);
+                    fsa[j] = __half22float2(*reinterpret_cast<const __half2 *>(&a));
+                    fsb[j] = __half22float2(*reinterpret_cast<const __half2 *>(&b));
+                }
 #pragma unroll
                 for (int grp = 0; grp < 2; ++grp) {
                     const uint32_t off = static_cast<uint32_t>(((4 * grp + tid) ^ g) << 4);
@@ -239,11 +279,8 @@ __global__ void __launch_bounds__(kThreads) gemv_stream_kernel(
                         uint32_t lo[4], hi[4];
                         dequant_word(word_of(qa, blk), lo);
                         dequant_word(word_of(qb, blk), hi);
-                        const uint32_t wa = word_of(sa, bi >> 1), wb = word_of(sb, bi >> 1);
-                        const float fa = __half2float(__ushort_as_half(
-                            static_cast<unsigned short>((wa >> (16 * (bi & 1))) & 0xFFFFu)));
-                        const float fb = __half2float(__ushort_as_half(
-                            static_cast<unsigned short>((wb >> (16 * (bi & 1))) & 0xFFFFu)));
+                        const float fa = (bi & 1) ? fsa[bi >> 1].y : fsa[bi >> 1].x;
+                        const float fb = (bi & 1) ? fsb[bi >> 1].y : fsb[bi >> 1].x;
 #pragma unroll
                         for (int n = 0; n < NT; ++n) {
                             float t[4] = {0.f, 0.f, 0.f, 0.f};
@@ -414,8 +451,9 @@ cudaError_t launch_stream_gateup(GemvWeights wg, GemvWeights wu, const void *nfr
     // 32 features per CTA; covering nchF * 32 features writes every slot of h
     const int64_t blocks = nchF;
     LaunchScope scope(K_GEMV_GATEUP, s);
-    kern<<<static_cast<unsigned>(blocks), kThreads, TL::smem_bytes, s>>>(w0, w1, s0, s1, p);
-    return cudaGetLastError();
+    e = launch_dependent(kern, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), TL::smem_bytes, s, w0, w1,
+                         s0, s1, p);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <int WF, int NT, bool TWO>
@@ -447,8 +485,8 @@ cudaError_t launch_stream_down(GemvWeights wd, const void *hfrag, const void *hf
     const int64_t nsplit = cdiv(p.nkb, p.kb_per_split);
     dim3 grid(static_cast<unsigned>(cdiv(d, 64)), static_cast<unsigned>(nsplit));
     LaunchScope scope(K_GEMV_DOWN, s);
-    kern<<<grid, kThreads, TL::smem_bytes, s>>>(w0, w0, s0, s0, p);
-    return cudaGetLastError();
+    e = launch_dependent(kern, grid, dim3(kThreads), TL::smem_bytes, s, w0, w0, s0, s0, p);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 // Down-projection splits for the streaming kernel: at most ~600 CTAs of 64

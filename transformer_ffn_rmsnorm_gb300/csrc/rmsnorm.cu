@@ -42,6 +42,7 @@ __global__ void __launch_bounds__(256) rmsnorm_reg_kernel(const T *x,
     static_assert(sizeof(T) == sizeof(TO), "input and output element sizes must match");
     constexpr int EPV = 16 / sizeof(T);
     __shared__ float partial[256 / 32];
+    ptx::griddep_launch_dependents();   // the projection after this may start its weight loads
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rows_per_cta = (blockDim.x >> 5) / WPR;
     const int row_in_cta = warp / WPR, wr = warp % WPR;
@@ -101,6 +102,7 @@ __global__ void __launch_bounds__(256) rmsnorm_generic_kernel(const T *x,
                                                               TO *n, TO *nlo, int64_t rows,
                                                               int64_t d, float eps) {
     __shared__ float partial[8];
+    ptx::griddep_launch_dependents();   // the projection after this may start its weight loads
     const int64_t row = blockIdx.x;
     if (row >= rows) return;
     const T *xr = x + row * d;
@@ -154,6 +156,7 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_stream_kernel(
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bar_full[kNormWarps], bar_empty[kNormWarps], bar_g;
     __shared__ int s_abort, s_never;
+    ptx::griddep_launch_dependents();   // the projection after this may start its weight loads
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t stride = (row_bytes + 127u) & ~127u;
     const uint32_t gsm = (ptx::smem_u32(smem_raw) + 127u) & ~127u;   // g, one row's worth

@@ -64,6 +64,7 @@ __global__ void swiglu_tail_kernel(const T *gate, const T *up, T *h, int64_t beg
 template <typename T>
 __global__ void __launch_bounds__(256) swiglu_f32in_kernel(const float *gate, const float *up, T *h,
                                                            T *h_lo, int64_t count, float out_scale) {
+    ptx::griddep_launch_dependents();   // the down projection may start its weight loads
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     const int64_t nvec = count / 8;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nvec; i += stride) {
