@@ -223,6 +223,18 @@ const char *ffn_status_string(ffn_status status);
  * of range; FFN_ERR_CUDA if the synchronisation itself failed. */
 ffn_status ffn_device_status(void);
 
+/* Failure-detection self test (no counterpart on the pages; the pages ask
+ * for explicit failure behaviour -- "How Megakernels Work", section
+ * "Dependencies and synchronization").  Launches on `stream` one CTA in which
+ * one role waits on an mbarrier phase that nothing completes, with the same
+ * bounded wait every streaming kernel of this library uses, and gives up after
+ * limit_ns nanoseconds (clamped to [1 us, 1 s]); a second role, waiting with a
+ * 1000x longer limit, is released by the first one's abort flag.  The kernel
+ * records FFN_ERR_TIMEOUT in the device status word and returns normally, so
+ * the next ffn_device_status() returns FFN_ERR_TIMEOUT and the device stays
+ * usable.  Returns FFN_OK when launched, FFN_ERR_CUDA if the launch failed. */
+ffn_status ffn_selftest_bounded_wait(uint64_t limit_ns, void *stream);
+
 /* Number of kernels this library has launched since it was loaded (host count). */
 uint64_t ffn_launch_count(void);
 

@@ -42,3 +42,29 @@ def test_unsupported_dtype_tensor(env):
     x = torch.zeros((2, 8), dtype=torch.float64, device="cuda")
     with pytest.raises(TypeError):
         ffn.ffn_rmsnorm(x, x[0], eps=1e-5)
+
+
+def test_bounded_wait_gives_up_and_device_stays_usable(env):
+    """A wait that nothing completes ends after its limit with FFN_ERR_TIMEOUT
+    in the status word; a second role with a 1000x longer limit is released by
+    the abort flag; the next call on the same context computes correctly."""
+    import time
+    import numpy as np
+    torch, _lib, ffn = env
+    torch.cuda.synchronize()
+    ffn.ffn_device_status()                      # start from a clean status word
+    limit_ns = 2_000_000                         # 2 ms (the second role: 2 s)
+    t0 = time.perf_counter()
+    ffn.ffn_selftest_bounded_wait(limit_ns)
+    with pytest.raises(ffn.FFNError) as err:
+        ffn.ffn_device_status()
+    elapsed = time.perf_counter() - t0
+    assert err.value.status == _lib.FFN_ERR_TIMEOUT
+    assert elapsed < 0.5, elapsed               # far below the second role's 2 s
+    ffn.ffn_device_status()                      # the word was cleared by the read
+    x = torch.randn(4, 256, device="cuda")
+    g = torch.ones(256, device="cuda")
+    n = ffn.ffn_rmsnorm(x, g, eps=1e-6)
+    ref = x / torch.sqrt((x * x).mean(dim=1, keepdim=True) + 1e-6)
+    assert np.allclose(n.cpu().numpy(), ref.cpu().numpy(), rtol=1e-5, atol=1e-6)
+    ffn.ffn_device_status()

@@ -52,6 +52,7 @@ SIGNATURES = {
     "ffn_q4_pack_host": (c_int, [c_void_p, c_void_p, c_int64, c_int64, c_void_p, c_void_p]),
     "ffn_status_string": (ctypes.c_char_p, [c_int]),
     "ffn_device_status": (c_int, []),
+    "ffn_selftest_bounded_wait": (c_int, [ctypes.c_uint64, c_void_p]),
     "ffn_launch_count": (ctypes.c_uint64, []),
     "ffn_timing_enable": (c_int, [c_int]),
     "ffn_timing_collect": (c_int, []),

@@ -144,7 +144,7 @@ ffn_status from_cuda(cudaError_t e) { return e == cudaSuccess ? FFN_OK : FFN_ERR
 const char *kernel_name(int kind) {
     static const char *names[K_NUM_KINDS] = {
         "prepare", "rmsnorm", "swiglu", "simt_gateup", "simt_down", "gemv_norm",
-        "gemv_gateup", "gemv_down", "gemm_gateup", "gemm_down"};
+        "gemv_gateup", "gemv_down", "gemm_gateup", "gemm_down", "selftest"};
     return (kind >= 0 && kind < K_NUM_KINDS) ? names[kind] : "unknown";
 }
 
@@ -435,6 +435,12 @@ ffn_status ffn_device_status(void) {
     }
     if (word & DEVERR_TIMEOUT) return FFN_ERR_TIMEOUT;
     return (word & DEVERR_RANGE) ? FFN_ERR_RANGE : FFN_OK;
+}
+
+ffn_status ffn_selftest_bounded_wait(uint64_t limit_ns, void *stream) {
+    if (limit_ns < 1000) limit_ns = 1000;
+    if (limit_ns > 1000000000ull) limit_ns = 1000000000ull;
+    return from_cuda(launch_bounded_wait_probe(limit_ns, static_cast<cudaStream_t>(stream)));
 }
 
 ffn_status ffn_prepare_weights(const void *src, void *dst, int64_t count, ffn_dtype src_dtype,

@@ -26,6 +26,7 @@ enum KernelKind : int {
     K_GEMV_DOWN,
     K_GEMM_GATEUP,
     K_GEMM_DOWN,
+    K_SELFTEST,
     K_NUM_KINDS
 };
 const char *kernel_name(int kind);
@@ -82,6 +83,9 @@ cudaError_t launch_rmsnorm_to_f16(const void *x, const void *g, void *n, int64_t
 cudaError_t launch_prepare_weights(const void *src, void *dst, int64_t count, int dt, cudaStream_t s);
 cudaError_t launch_swiglu(const void *gate, const void *up, void *h, int64_t count, int dt,
                           cudaStream_t s);
+// One CTA whose bounded wait on a never-completed barrier gives up after
+// limit_ns and records DEVERR_TIMEOUT (selftest.cu).
+cudaError_t launch_bounded_wait_probe(uint64_t limit_ns, cudaStream_t s);
 
 // fp32 G, U -> 16-bit h = silu(G) * U * out_scale, and its residual h_lo
 // when non-null (unfused arm of the tensor-core path)

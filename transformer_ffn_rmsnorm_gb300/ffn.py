@@ -160,6 +160,12 @@ def ffn_device_status():
     _check(_lib.load().ffn_device_status(), "ffn_device_status")
 
 
+def ffn_selftest_bounded_wait(limit_ns: int = 2_000_000, stream=None):
+    """Launch the bounded-wait self test: a wait that nothing completes gives
+    up after limit_ns and the next ffn_device_status() raises FFN_ERR_TIMEOUT."""
+    _check(_lib.load().ffn_selftest_bounded_wait(int(limit_ns), _stream(stream)), "ffn_selftest_bounded_wait")
+
+
 def ffn_launch_count() -> int:
     return int(_lib.load().ffn_launch_count())
 
