@@ -133,6 +133,32 @@ ffn_status ffn_block_forward(const void *x, const void *g, const void *w_gate, c
                              size_t workspace_bytes, void *stream);
 
 /* ------------------------------------------------------------------------
+ * ffn_block_forward_host -- ffn_block_forward with x and y in HOST memory
+ * (page-locked for the copies to overlap; pageable memory works, serialised).
+ * The same block as ffn_block_forward ("Unfusing a Kernel Made It 1.63x
+ * Faster", Finding 1); the host copies have no counterpart on the pages.
+ *   x_host, y_host: [rows x d] of `dtype` in host memory, not overlapping.
+ *   g, w_gate, w_up, w_down: device pointers as in ffn_block_forward.
+ *   workspace: device scratch of ffn_block_host_workspace_bytes() bytes
+ *   (x and y are staged there, plus the block's own scratch).
+ * The rows are split into chunks (1536 rows above 2048); the input copy of
+ * every chunk is queued at once on a copy stream owned by the library, each
+ * chunk's block runs on `stream` when its rows have landed, and its output
+ * copy runs on a second library stream while the next chunk computes.
+ * `stream` waits for the last output copy: once `stream` has passed the call,
+ * y_host holds the result.  Concurrent calls on one device are serialised on
+ * the host while they are queued; the workspace must not be shared by calls
+ * that may run concurrently.  Errors as ffn_block_forward; FFN_ERR_ALIAS if
+ * x_host and y_host overlap.
+ * ---------------------------------------------------------------------- */
+ffn_status ffn_block_host_workspace_bytes(int64_t rows, int64_t d, int64_t ffn, ffn_dtype dtype,
+                                          uint32_t flags, size_t *bytes);
+ffn_status ffn_block_forward_host(const void *x_host, const void *g, const void *w_gate,
+                                  const void *w_up, const void *w_down, void *y_host, int64_t rows,
+                                  int64_t d, int64_t ffn, float eps, ffn_dtype dtype, uint32_t flags,
+                                  void *workspace, size_t workspace_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
  * Q4 weights ("Unfusing a Kernel Made It 1.63x Faster", section "The finding
  * that keeps us honest about microbenchmarks": 18-byte blocks of 32 weights,
  * 16 bytes of nibbles plus a half-precision scale, repacked so each block is

@@ -146,3 +146,27 @@ def test_prepare_weights_rejects_before_launch(lib):
     assert lib.ffn_block_workspace_bytes(8, 64, 64, _lib.FFN_F32, flags, ctypes.byref(out)) == _lib.FFN_ERR_FLAGS
     assert lib.ffn_block_workspace_bytes(8, 64, 64, _lib.FFN_BF16, flags | _lib.FFN_ACT_SPLIT,
                                          ctypes.byref(out)) == _lib.FFN_ERR_FLAGS
+
+
+def test_host_block_entry_rejects_before_launch(lib):
+    out = ctypes.c_size_t(0)
+    assert lib.ffn_block_host_workspace_bytes(0, 4096, 11008, _lib.FFN_BF16, 0, ctypes.byref(out)) == 0
+    assert out.value == 0
+    assert lib.ffn_block_host_workspace_bytes(4096, 4096, 11008, _lib.FFN_BF16, 0, ctypes.byref(out)) == 0
+    staged = 2 * 4096 * 4096 * 2
+    blk = ctypes.c_size_t(0)
+    assert lib.ffn_block_workspace_bytes(1536, 4096, 11008, _lib.FFN_BF16, 0, ctypes.byref(blk)) == 0
+    assert out.value >= staged + blk.value
+    assert lib.ffn_block_host_workspace_bytes(8, 4100, 11008, _lib.FFN_BF16, 0,
+                                              ctypes.byref(out)) == _lib.FFN_ERR_SHAPE
+    p = [ctypes.c_void_p((i + 1) << 24) for i in range(8)]
+    need = ctypes.c_size_t(0)
+    lib.ffn_block_host_workspace_bytes(8, 64, 128, _lib.FFN_BF16, 0, ctypes.byref(need))
+    # NULL host buffer, workspace too small, overlapping host buffers
+    assert lib.ffn_block_forward_host(None, *p[1:5], p[5], 8, 64, 128, 1e-5, _lib.FFN_BF16, 0, p[6],
+                                      need.value, None) == _lib.FFN_ERR_NULL
+    assert lib.ffn_block_forward_host(*p[:6], 8, 64, 128, 1e-5, _lib.FFN_BF16, 0, p[6], 16,
+                                      None) == _lib.FFN_ERR_WORKSPACE
+    x = ctypes.c_void_p(1 << 30)
+    assert lib.ffn_block_forward_host(x, *p[1:5], ctypes.c_void_p((1 << 30) + 512), 8, 64, 128, 1e-5,
+                                      _lib.FFN_BF16, 0, p[6], need.value, None) == _lib.FFN_ERR_ALIAS

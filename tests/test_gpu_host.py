@@ -1,0 +1,78 @@
+"""ffn_block_forward_host: x and y in host memory, copies overlapped with the
+compute in row chunks.  Checked against the float64 oracle and, where every
+chunk takes the same path as the whole batch, byte for byte against
+ffn_block_forward on device buffers (rows are independent: chunking changes
+no output's arithmetic)."""
+
+import numpy as np
+import pytest
+
+import synth
+from gpu_util import assert_lowp, to_dev, to_host64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ffn():
+    from transformer_ffn_rmsnorm_gb300 import ffn as m
+    return m
+
+
+def host_bf16(a):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).pin_memory()
+
+
+@pytest.mark.parametrize("rows", [8, 300, 3500])
+@pytest.mark.parametrize("prepared", [False, True])
+def test_host_block_matches_device_block(ffn, oracle_lib, rows, prepared):
+    """3500 rows: three chunks (1536, 1536, 428) through the tensor-core path."""
+    import torch
+    inp = synth.make_block_inputs(synth.C4_PREFILL_BF16, seed=rows, rows=rows, d=256, ffn=384)
+    g = to_dev(inp["g"], "bf16")
+    w = [to_dev(inp[k], "bf16") for k in ("w_gate", "w_up", "w_down")]
+    flags = 0
+    if prepared:
+        w = [ffn.ffn_prepare_weights(t) for t in w]
+        flags = ffn.FFN_PREPARED_WEIGHTS
+    y_host = ffn.ffn_block_forward_host(host_bf16(inp["x"]), g, *w, eps=inp["cfg"].eps, flags=flags)
+    torch.cuda.current_stream().synchronize()
+    y_dev = ffn.ffn_block_forward(to_dev(inp["x"], "bf16"), g, *w, eps=inp["cfg"].eps, flags=flags)
+    assert torch.equal(y_host.view(torch.int16), y_dev.cpu().view(torch.int16))
+    assert_lowp(to_host64(y_host), oracle_lib.block_from_inputs(inp))
+    ffn.ffn_device_status()
+
+
+def test_host_block_short_last_chunk(ffn, oracle_lib):
+    """3082 rows: chunks of 1536, 1536 and 10, the last on the decode path."""
+    import torch
+    inp = synth.make_block_inputs(synth.C4_PREFILL_BF16, seed=9, rows=3082, d=512, ffn=704)
+    args = [to_dev(inp[k], "bf16") for k in ("g", "w_gate", "w_up", "w_down")]
+    y = ffn.ffn_block_forward_host(host_bf16(inp["x"]), *args, eps=inp["cfg"].eps)
+    torch.cuda.current_stream().synchronize()
+    got = to_host64(y)
+    rows = np.r_[0:40, 1530:1545, 3060:3082]
+    ref = oracle_lib.block_from_inputs(inp, rows=rows)
+    assert_lowp(got[rows], ref)
+    ffn.ffn_device_status()
+
+
+def test_host_block_twice_in_a_row_and_empty(ffn):
+    """Back-to-back calls reuse the staging buffers; the second must wait for
+    the first's copies.  An empty batch is valid and queues nothing."""
+    import torch
+    inp = synth.make_block_inputs(synth.C4_PREFILL_BF16, seed=3, rows=2600, d=256, ffn=384)
+    inp2 = synth.make_block_inputs(synth.C4_PREFILL_BF16, seed=4, rows=2600, d=256, ffn=384)
+    args = [to_dev(inp[k], "bf16") for k in ("g", "w_gate", "w_up", "w_down")]
+    ws = ffn.workspace(ffn.ffn_block_host_workspace_bytes(2600, 256, 384, torch.bfloat16), torch.device("cuda"))
+    y1 = ffn.ffn_block_forward_host(host_bf16(inp["x"]), *args, eps=1e-6, ws=ws)
+    y2 = ffn.ffn_block_forward_host(host_bf16(inp2["x"]), *args, eps=1e-6, ws=ws)
+    torch.cuda.current_stream().synchronize()
+    r1 = ffn.ffn_block_forward(to_dev(inp["x"], "bf16"), *args, eps=1e-6).cpu()
+    r2 = ffn.ffn_block_forward(to_dev(inp2["x"], "bf16"), *args, eps=1e-6).cpu()
+    assert torch.equal(y1.view(torch.int16), r1.view(torch.int16))
+    assert torch.equal(y2.view(torch.int16), r2.view(torch.int16))
+    e = torch.empty((0, 256), dtype=torch.bfloat16).pin_memory()
+    assert ffn.ffn_block_forward_host(e, *args, eps=1e-6).numel() == 0
+    ffn.ffn_device_status()

@@ -105,6 +105,36 @@ def ffn_block_forward(x, g, w_gate, w_up, w_down, eps: float, flags: int = 0, ou
     return y
 
 
+def ffn_block_host_workspace_bytes(rows: int, d: int, ffn: int, dtype, flags: int = 0) -> int:
+    out = ctypes.c_size_t(0)
+    _check(_lib.load().ffn_block_host_workspace_bytes(rows, d, ffn, _DT[dtype], flags, ctypes.byref(out)),
+           "ffn_block_host_workspace_bytes")
+    return out.value
+
+
+def ffn_block_forward_host(x_host, g, w_gate, w_up, w_down, eps: float, flags: int = 0, out=None,
+                           ws: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """The block with x and y in host memory (page-locked tensors overlap their
+    copies with the compute); weights, g and the workspace on the device.
+    Returns y on the host once `stream` (default: the current one) has passed
+    the call; synchronise it before reading."""
+    _need_cuda(g, w_gate, w_up, w_down, ws)
+    if x_host.is_cuda or (out is not None and out.is_cuda):
+        raise ValueError("x_host and out must be host tensors")
+    if not x_host.is_contiguous() or (out is not None and not out.is_contiguous()):
+        raise ValueError("x_host and out must be contiguous")
+    d = x_host.shape[-1]
+    rows = x_host.numel() // d
+    ffn = w_gate.shape[0]
+    y = torch.empty(x_host.shape, dtype=x_host.dtype, pin_memory=True) if out is None else out
+    if ws is None:
+        ws = workspace(ffn_block_host_workspace_bytes(rows, d, ffn, x_host.dtype, flags), g.device)
+    _check(_lib.load().ffn_block_forward_host(_ptr(x_host), _ptr(g), _ptr(w_gate), _ptr(w_up), _ptr(w_down),
+                                              _ptr(y), rows, d, ffn, float(eps), _dtype(x_host), flags,
+                                              _ptr(ws), ws.numel(), _stream(stream)), "ffn_block_forward_host")
+    return y
+
+
 def ffn_prepare_weights(w: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """One-time re-encoding of a bf16/fp16 weight for FFN_PREPARED_WEIGHTS
     (fp16 values of w * 2^8)."""
