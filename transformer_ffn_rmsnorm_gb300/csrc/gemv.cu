@@ -59,7 +59,10 @@ __global__ void __launch_bounds__(256) gemv_norm_frag_kernel(const void *x_, con
     using TO = typename Fmt<WF>::TOp;
     constexpr bool q4 = WF == WF_Q4;
     __shared__ float partial[8];
-    // the projection kernel after this one may start its weight stream now
+    // launched as a programmatic dependent: nothing is read or written before
+    // the previous kernel has finished; only then may the projection kernel
+    // after this one start its weight stream (weights that kernel may have written)
+    ptx::griddep_wait();
     ptx::griddep_launch_dependents();
     const int token = blockIdx.x;
     const T *x = static_cast<const T *>(x_) + static_cast<int64_t>(token) * K;
@@ -243,8 +246,8 @@ __device__ __forceinline__ void warp_accumulate(const void *const (&w)[RT],
                         const float f1 = __half2float(__ushort_as_half(static_cast<unsigned short>(s1 & 0xFFFFu)));
 #pragma unroll
                         for (int n = 0; n < NT; ++n) {
-                            float t[4] = {0.f, 0.f, 0.f, 0.f};
-                            ptx::mma_16816<bf>(t, lo[0], hi[0], lo[2], hi[2], b[n].x, b[n].y);
+                            float t[4];   // this block's products alone, scaled below
+                            ptx::mma_16816_z<bf>(t, lo[0], hi[0], lo[2], hi[2], b[n].x, b[n].y);
                             ptx::mma_16816<bf>(t, lo[1], hi[1], lo[3], hi[3], b[n].z, b[n].w);
                             if constexpr (TWO) {
                                 ptx::mma_16816<bf>(t, lo[0], hi[0], lo[2], hi[2], bl[n].x, bl[n].y);
@@ -441,10 +444,10 @@ cudaError_t launch_typed(const void *x, const void *gain, GemvWeights wg, GemvWe
     {
         LaunchScope scope(K_GEMV_NORM, s);
         const int64_t slices = std::min<int64_t>(16, cdiv(geo.nchK * 4, 256));
-        gemv_norm_frag_kernel<WF, TWO><<<dim3(8 * NT, static_cast<unsigned>(slices)), 256, 0, s>>>(
-            x, gain, static_cast<uint16_t *>(ws.nfrag), static_cast<uint16_t *>(ws.nfrag_lo), rows, d,
-            geo.nchK, eps);
-        cudaError_t e = cudaGetLastError();
+        cudaError_t e = launch_dependent(gemv_norm_frag_kernel<WF, TWO>, dim3(8 * NT, static_cast<unsigned>(slices)),
+                                         dim3(256), 0, s, x, gain, static_cast<uint16_t *>(ws.nfrag),
+                                         static_cast<uint16_t *>(ws.nfrag_lo), rows, d, geo.nchK, eps);
+        if (e == cudaSuccess) e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     if (stream_supported(WF, d, ffn)) {

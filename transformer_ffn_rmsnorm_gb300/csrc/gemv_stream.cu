@@ -283,8 +283,8 @@ __global__ void __launch_bounds__(kThreads) gemv_stream_kernel(
                         const float fb = (bi & 1) ? fsb[bi >> 1].y : fsb[bi >> 1].x;
 #pragma unroll
                         for (int n = 0; n < NT; ++n) {
-                            float t[4] = {0.f, 0.f, 0.f, 0.f};
-                            ptx::mma_16816<bf>(t, lo[0], hi[0], lo[2], hi[2], b[n].x, b[n].y);
+                            float t[4];   // this block's products alone, scaled below
+                            ptx::mma_16816_z<bf>(t, lo[0], hi[0], lo[2], hi[2], b[n].x, b[n].y);
                             ptx::mma_16816<bf>(t, lo[1], hi[1], lo[3], hi[3], b[n].z, b[n].w);
                             acc[n][0] = fmaf(fa, t[0], acc[n][0]);
                             acc[n][1] = fmaf(fa, t[1], acc[n][1]);
