@@ -42,7 +42,11 @@ __global__ void __launch_bounds__(256) rmsnorm_reg_kernel(const T *x,
     static_assert(sizeof(T) == sizeof(TO), "input and output element sizes must match");
     constexpr int EPV = 16 / sizeof(T);
     __shared__ float partial[256 / 32];
-    ptx::griddep_launch_dependents();   // the projection after this may start its weight loads
+    // launched as a programmatic dependent: nothing is read before the
+    // previous kernel has finished; only then may the projection after this
+    // one start (it requests weights at once, which that kernel may have written)
+    ptx::griddep_wait();
+    ptx::griddep_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rows_per_cta = (blockDim.x >> 5) / WPR;
     const int row_in_cta = warp / WPR, wr = warp % WPR;
@@ -102,7 +106,11 @@ __global__ void __launch_bounds__(256) rmsnorm_generic_kernel(const T *x,
                                                               TO *n, TO *nlo, int64_t rows,
                                                               int64_t d, float eps) {
     __shared__ float partial[8];
-    ptx::griddep_launch_dependents();   // the projection after this may start its weight loads
+    // launched as a programmatic dependent: nothing is read before the
+    // previous kernel has finished; only then may the projection after this
+    // one start (it requests weights at once, which that kernel may have written)
+    ptx::griddep_wait();
+    ptx::griddep_launch_dependents();
     const int64_t row = blockIdx.x;
     if (row >= rows) return;
     const T *xr = x + row * d;
@@ -156,7 +164,11 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_stream_kernel(
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bar_full[kNormWarps], bar_empty[kNormWarps], bar_g;
     __shared__ int s_abort, s_never;
-    ptx::griddep_launch_dependents();   // the projection after this may start its weight loads
+    // launched as a programmatic dependent: nothing is read before the
+    // previous kernel has finished; only then may the projection after this
+    // one start (it requests weights at once, which that kernel may have written)
+    ptx::griddep_wait();
+    ptx::griddep_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t stride = (row_bytes + 127u) & ~127u;
     const uint32_t gsm = (ptx::smem_u32(smem_raw) + 127u) & ~127u;   // g, one row's worth
@@ -287,10 +299,10 @@ cudaError_t launch_stream(const void *x, const void *g, void *n, void *nlo, int6
     int64_t grid = static_cast<int64_t>(sm_count()) * per_sm;
     if (grid > rows) grid = rows;
     LaunchScope scope(K_RMSNORM, s);
-    rmsnorm_stream_kernel<T, TO, SPLIT><<<static_cast<unsigned>(grid), kNormThreads, smem, s>>>(
-        static_cast<const T *>(x), static_cast<const T *>(g), static_cast<TO *>(n), static_cast<TO *>(nlo),
-        rows, d, eps, row_bytes, err);
-    return cudaGetLastError();
+    e = launch_dependent(rmsnorm_stream_kernel<T, TO, SPLIT>, dim3(static_cast<unsigned>(grid)), dim3(kNormThreads),
+                         smem, s, static_cast<const T *>(x), static_cast<const T *>(g), static_cast<TO *>(n),
+                         static_cast<TO *>(nlo), rows, d, eps, row_bytes, err);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <typename T, typename TO, int VPT, int WPR, bool SPLIT>
@@ -300,10 +312,11 @@ cudaError_t launch_reg(const void *x, const void *g, void *n, void *nlo, int64_t
     const int rows_per_cta = (threads / 32) / WPR;
     const int64_t blocks = (rows + rows_per_cta - 1) / rows_per_cta;
     LaunchScope scope(K_RMSNORM, s);
-    rmsnorm_reg_kernel<T, TO, VPT, WPR, SPLIT><<<static_cast<unsigned>(blocks), threads, 0, s>>>(
-        static_cast<const T *>(x), static_cast<const T *>(g), static_cast<TO *>(n),
-        static_cast<TO *>(nlo), rows, d, eps);
-    return cudaGetLastError();
+    const cudaError_t e = launch_dependent(rmsnorm_reg_kernel<T, TO, VPT, WPR, SPLIT>,
+                                           dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, s,
+                                           static_cast<const T *>(x), static_cast<const T *>(g),
+                                           static_cast<TO *>(n), static_cast<TO *>(nlo), rows, d, eps);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <typename T, typename TO, int WPR, bool SPLIT>
@@ -342,10 +355,10 @@ cudaError_t launch_typed(const void *x, const void *g, void *n, void *nlo, int64
         }
     }
     LaunchScope scope(K_RMSNORM, s);
-    rmsnorm_generic_kernel<T, TO, SPLIT><<<static_cast<unsigned>(rows), 256, 0, s>>>(
-        static_cast<const T *>(x), static_cast<const T *>(g), static_cast<TO *>(n),
-        static_cast<TO *>(nlo), rows, d, eps);
-    return cudaGetLastError();
+    const cudaError_t e = launch_dependent(rmsnorm_generic_kernel<T, TO, SPLIT>, dim3(static_cast<unsigned>(rows)),
+                                           dim3(256), 0, s, static_cast<const T *>(x), static_cast<const T *>(g),
+                                           static_cast<TO *>(n), static_cast<TO *>(nlo), rows, d, eps);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace
