@@ -369,6 +369,23 @@ def dist_init():
     return world, rank, local
 
 
+def max_over_ranks(ms: float, world: int, device=None) -> float:
+    """The slowest replica's time for the timed steps (every rank processed its
+    own batch within it); the value itself with one rank."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_tokens_per_s(rows: int, steps: int, world: int, ms: float) -> float:
+    """Whole-job throughput: the tokens of every replica over the slowest time."""
+    return rows * steps * world / (ms / 1000.0)
+
+
 def run_reference(args):
     world, rank, _ = dist_init()
     if rank != 0:
@@ -450,13 +467,8 @@ def run_ours(args):
     launches = ffn.ffn_launch_count() - launches0
     ms = e0.elapsed_time(e1)
     clocks = clk.summary(t0, t1)
-    if world > 1:
-        t = torch.tensor([ms], device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
-
-    tokens = cfg.rows * args.steps * world
-    value = tokens / (ms / 1000.0)
+    ms = max_over_ranks(ms, world, device)
+    value = aggregate_tokens_per_s(cfg.rows, args.steps, world, ms)
     flops_gu = 2.0 * cfg.rows * cfg.d * (2 * cfg.ffn)
     n_gu, ms_gu = res["gemm_gateup"]
     gu_avg_s = ms_gu / n_gu / 1000.0
