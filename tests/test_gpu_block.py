@@ -232,3 +232,25 @@ def test_prepared_decode_full_size(ffn, oracle_lib):
     x, g, (wg, wu, wd) = prepared(ffn, inp)
     y = ffn.ffn_block_forward(x, g, wg, wu, wd, eps=inp["cfg"].eps, flags=ffn.FFN_PREPARED_WEIGHTS)
     assert_lowp(to_host64(y), oracle_lib.block_from_inputs(inp))
+
+
+# Several waves of CTA-pair tiles with a short last wave (76 pairs on a
+# 152-SM part): 2048 x 4096 -> 1280 (gate/up: 80 pair tiles, down: 152 tiles
+# of 224 columns) and 4096 x 1280 -> 4096 (gate/up: 512 tiles, down: 96).
+MULTIWAVE_SHAPES = [(2048, 4096, 1280), (4096, 1280, 4096)]
+
+
+@pytest.mark.parametrize("flags", [0, 2, 64])
+@pytest.mark.parametrize("rows,d,ffn_", MULTIWAVE_SHAPES)
+def test_multiwave_gemms(ffn, oracle_lib, flags, rows, d, ffn_):
+    """Fused, unfused and prepared-weights arms: sampled rows from every
+    region of the batch against the oracle."""
+    cfg = synth.BlockConfig("t", rows, d, ffn_, 1e-6, "bf16")
+    inp = synth.make_block_inputs(cfg, seed=rows + d)
+    args = [to_dev(inp[k], "bf16") for k in ("x", "g", "w_gate", "w_up", "w_down")]
+    if flags & ffn.FFN_PREPARED_WEIGHTS:
+        args[2:] = [ffn.ffn_prepare_weights(w) for w in args[2:]]
+    y = to_host64(ffn.ffn_block_forward(*args, eps=cfg.eps, flags=flags))
+    sel = np.unique(np.concatenate([np.arange(0, rows, 61), [rows - 1], np.arange(1000, 1040)]))
+    assert_lowp(y[sel], oracle_lib.block_from_inputs(inp, rows=sel))
+    ffn.ffn_device_status()
