@@ -116,7 +116,10 @@ class Oracle:
         return h
 
     def ffn_block(self, x, g, w_gate, w_up, w_down, eps: float,
-                  nthreads: int | None = None) -> np.ndarray:
+                  nthreads: int | None = None, residual: bool = False) -> np.ndarray:
+        """y = W_down (silu(W_gate n) * (W_up n)), n = RMSNorm(x); with
+        ``residual``, y = x + that (the block's skip connection, added in
+        float64)."""
         x = np.ascontiguousarray(x, dtype=np.float64)
         g = np.ascontiguousarray(g, dtype=np.float64)
         w_gate = np.ascontiguousarray(w_gate, dtype=np.float64)
@@ -132,7 +135,7 @@ class Oracle:
                                      nthreads or default_threads())
         if rc != 0:
             raise MemoryError("oracle scratch allocation failed")
-        return y
+        return x + y if residual else y
 
     def q4_dequant(self, qs, scales, out: int, inn: int) -> np.ndarray:
         qs = np.ascontiguousarray(qs, dtype=np.uint8)
@@ -145,16 +148,16 @@ class Oracle:
         return w
 
     # -- convenience: stored inputs -> float64 result --------------------
-    def block_from_inputs(self, inp: dict, rows=None, nthreads=None) -> np.ndarray:
+    def block_from_inputs(self, inp: dict, rows=None, nthreads=None, residual=False) -> np.ndarray:
         """Oracle y for a ``synth.make_block_inputs`` dict; ``rows`` selects a
         subset of token rows (rows are independent)."""
         dt = inp["cfg"].dtype
         x = inp["x"] if rows is None else inp["x"][np.asarray(rows)]
         return self.ffn_block(widen(x, dt), widen(inp["g"], dt), widen(inp["w_gate"], dt),
                               widen(inp["w_up"], dt), widen(inp["w_down"], dt),
-                              inp["cfg"].eps, nthreads)
+                              inp["cfg"].eps, nthreads, residual)
 
-    def q4_block_from_inputs(self, inp: dict, rows=None, nthreads=None) -> np.ndarray:
+    def q4_block_from_inputs(self, inp: dict, rows=None, nthreads=None, residual=False) -> np.ndarray:
         """Oracle y for a ``synth.make_q4_inputs`` dict, on weights the oracle
         dequantises itself from the packed bytes."""
         cfg = inp["cfg"]
@@ -164,7 +167,7 @@ class Oracle:
         wd = self.q4_dequant(inp["qs_down"], inp["sc_down"], D, F)
         x = inp["x"] if rows is None else inp["x"][np.asarray(rows)]
         return self.ffn_block(widen(x, "bf16"), widen(inp["g"], "bf16"), wg, wu, wd,
-                              cfg.eps, nthreads)
+                              cfg.eps, nthreads, residual)
 
 
 _default = None

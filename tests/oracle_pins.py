@@ -203,6 +203,26 @@ def pin_block_rows_independent(o):
     assert np.array_equal(sub, full[[4, 1]])
 
 
+def pin_block_residual(o):
+    """The skip connection: with W_down = 0 the block returns x itself; in
+    the closed-form block above it adds x row by row to the known output."""
+    rng = np.random.default_rng(18)
+    rows, d, F = 3, 5, 7
+    x = rng.standard_normal((rows, d))
+    g = 1.0 + 0.1 * rng.standard_normal(d)
+    wg, wu = rng.standard_normal((F, d)), rng.standard_normal((F, d))
+    assert np.array_equal(o.ffn_block(x, g, wg, wu, np.zeros((d, F)), 1e-6, residual=True), x)
+    d, F = 4, 3
+    xc = np.array([[2.5] * d, [-1.5] * d])
+    a = np.array([LN3, 0.0, -LN3])
+    b = np.array([2.0, 5.0, -4.0])
+    w_down = np.array([[1.0, 2.0, 3.0], [0.0, -1.0, 4.0], [2.0, 0.0, -2.0], [7.0, 1.0, 1.0]])
+    h = np.array([[1.5 * LN3, 0.0, LN3], [0.5 * LN3, 0.0, 3.0 * LN3]])
+    got = o.ffn_block(xc, np.ones(d), np.repeat(a[:, None] / d, d, axis=1), np.repeat(b[:, None] / d, d, axis=1),
+                      w_down, 0.0, residual=True)
+    _close(got, xc + h @ w_down.T, rtol=1e-13, atol=1e-14)
+
+
 # ---------------------------------------------------------------------- Q4
 
 def pin_half_decoder(o):
