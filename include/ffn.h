@@ -81,6 +81,11 @@ typedef enum { FFN_F32 = 0, FFN_F16 = 1, FFN_BF16 = 2 } ffn_dtype;
  * 2^-8, which keeps it clear of fp16 overflow up to |h| ~ 1.6e7), at single-
  * term speed.  Not combinable with FFN_ACT_SPLIT or FFN_F32.               */
 #define FFN_PREPARED_WEIGHTS 64u
+/* The block's skip connection: y = x + W_down (silu(W_gate n) * (W_up n)),
+ * x added in fp32 before y's one rounding (every path, ffn_block_forward and
+ * ffn_block_forward_q4).  No counterpart on the pages, whose block output
+ * stops at the down projection; the pre-norm layer adds its input back.    */
+#define FFN_RESIDUAL 128u
 
 /* ------------------------------------------------------------------------
  * ffn_rmsnorm -- n[r,c] = x[r,c] * rsqrt(ms_r + eps) * g[c],
@@ -187,8 +192,8 @@ ffn_status ffn_block_q4_workspace_bytes(int64_t rows, int64_t d, int64_t ffn, si
  *   [ffn x d], w_down is Q4 [d x ffn].  Needs d % 128 == 0, ffn % 128 == 0,
  *   Rows are processed in groups of up to 16; each group streams the weights
  *   once.  The codes (u - 8) are exact in fp16, so the MMAs run on fp16:
- *   activations enter as one fp16 rounding (h stored times 2^-8).  flags
- *   must be FFN_AUTO.
+ *   activations enter as one fp16 rounding (h stored times 2^-8).  flags:
+ *   FFN_AUTO or FFN_RESIDUAL.
  * ---------------------------------------------------------------------- */
 ffn_status ffn_block_forward_q4(const void *x, const void *g, ffn_q4_weight w_gate,
                                 ffn_q4_weight w_up, ffn_q4_weight w_down, void *y, int64_t rows,

@@ -170,3 +170,12 @@ def test_host_block_entry_rejects_before_launch(lib):
     x = ctypes.c_void_p(1 << 30)
     assert lib.ffn_block_forward_host(x, *p[1:5], ctypes.c_void_p((1 << 30) + 512), 8, 64, 128, 1e-5,
                                       _lib.FFN_BF16, 0, p[6], need.value, None) == _lib.FFN_ERR_ALIAS
+
+
+def test_residual_flag_accepted_by_the_planner(lib):
+    out = ctypes.c_size_t(0)
+    assert lib.ffn_block_workspace_bytes(4096, 4096, 11008, _lib.FFN_BF16, _lib.FFN_RESIDUAL,
+                                         ctypes.byref(out)) == 0
+    assert lib.ffn_block_workspace_bytes(8, 4096, 11008, _lib.FFN_BF16,
+                                         _lib.FFN_RESIDUAL | _lib.FFN_PREPARED_WEIGHTS, ctypes.byref(out)) == 0
+    assert lib.ffn_block_workspace_bytes(8, 64, 64, _lib.FFN_F32, _lib.FFN_RESIDUAL, ctypes.byref(out)) == 0

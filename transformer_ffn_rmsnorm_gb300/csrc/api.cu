@@ -94,7 +94,7 @@ ffn_status plan_block(int64_t rows, int64_t d, int64_t ffn, ffn_dtype dt, uint32
     ffn_status st = check_block_shape(rows, d, ffn, dt);
     if (st != FFN_OK) return st;
     const uint32_t known = FFN_GATEUP_FUSED | FFN_GATEUP_UNFUSED | FFN_PATH_GEMM | FFN_PATH_GEMV |
-                           FFN_ACT_SINGLE | FFN_ACT_SPLIT | FFN_PREPARED_WEIGHTS;
+                           FFN_ACT_SINGLE | FFN_ACT_SPLIT | FFN_PREPARED_WEIGHTS | FFN_RESIDUAL;
     if (flags & ~known) return FFN_ERR_FLAGS;
     if ((flags & FFN_GATEUP_FUSED) && (flags & FFN_GATEUP_UNFUSED)) return FFN_ERR_FLAGS;
     if ((flags & FFN_PATH_GEMM) && (flags & FFN_PATH_GEMV)) return FFN_ERR_FLAGS;
@@ -281,6 +281,7 @@ ffn_status ffn_block_forward(const void *x, const void *g, const void *w_gate, c
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     char *ws = static_cast<char *>(workspace);
+    const void *res = (flags & FFN_RESIDUAL) ? x : nullptr;   // the skip connection adds x back
     switch (plan.path) {
         case PATH_SIMT: {
             float *n = reinterpret_cast<float *>(ws);
@@ -288,7 +289,8 @@ ffn_status ffn_block_forward(const void *x, const void *g, const void *w_gate, c
             return from_cuda(launch_simt_block(
                 static_cast<const float *>(x), static_cast<const float *>(g),
                 static_cast<const float *>(w_gate), static_cast<const float *>(w_up),
-                static_cast<const float *>(w_down), static_cast<float *>(y), rows, d, ffn, eps, n, h, s));
+                static_cast<const float *>(w_down), static_cast<float *>(y), rows, d, ffn, eps, n, h, s,
+                static_cast<const float *>(res)));
         }
         case PATH_GEMV: {
             GemvWorkspace gw;
@@ -296,7 +298,7 @@ ffn_status ffn_block_forward(const void *x, const void *g, const void *w_gate, c
             GemvWeights a{w_gate, nullptr, nullptr}, b{w_up, nullptr, nullptr}, c{w_down, nullptr, nullptr};
             const int wf = plan.prepared ? (dtype == FFN_BF16 ? WF_F16P : WF_F16)
                                          : (dtype == FFN_BF16 ? WF_BF16 : WF_F16);
-            return from_cuda(launch_gemv_block(wf, x, g, a, b, c, y, rows, d, ffn, eps, gw, s));
+            return from_cuda(launch_gemv_block(wf, x, g, a, b, c, y, rows, d, ffn, eps, gw, s, res));
         }
         case PATH_GEMM: {
             const size_t nb = align256(static_cast<size_t>(rows) * d * es);
@@ -342,7 +344,7 @@ ffn_status ffn_block_forward(const void *x, const void *g, const void *w_gate, c
             }
             if (e != cudaSuccess) return FFN_ERR_CUDA;
             return from_cuda(launch_gemm_plain(op, dtype, h, h_lo, w_down, y, rows, ffn, d,
-                                               w_unscale / h_scale, s));
+                                               w_unscale / h_scale, res, s));
         }
     }
     return FFN_ERR_SHAPE;
@@ -363,7 +365,7 @@ ffn_status ffn_block_forward_q4(const void *x, const void *g, ffn_q4_weight w_ga
     if (!g || !w_gate.qs || !w_gate.scales || !w_up.qs || !w_up.scales || !w_down.qs ||
         !w_down.scales || (rows != 0 && (!x || !y)))
         return FFN_ERR_NULL;
-    if (flags != FFN_AUTO) return FFN_ERR_FLAGS;
+    if (flags & ~FFN_RESIDUAL) return FFN_ERR_FLAGS;
     size_t need = 0;
     ffn_status st = ffn_block_q4_workspace_bytes(rows, d, ffn, &need);
     if (st != FFN_OK) return st;
@@ -394,7 +396,8 @@ ffn_status ffn_block_forward_q4(const void *x, const void *g, ffn_q4_weight w_ga
         const int64_t nr = std::min<int64_t>(kGemvMaxRows, rows - r0);
         const char *xr = static_cast<const char *>(x) + r0 * d * 2;
         char *yr = static_cast<char *>(y) + r0 * d * 2;
-        cudaError_t e = launch_gemv_block(WF_Q4, xr, g, a, b, c, yr, nr, d, ffn, eps, gw, s);
+        cudaError_t e = launch_gemv_block(WF_Q4, xr, g, a, b, c, yr, nr, d, ffn, eps, gw, s,
+                                          (flags & FFN_RESIDUAL) ? xr : nullptr);
         if (e != cudaSuccess) return FFN_ERR_CUDA;
     }
     return FFN_OK;

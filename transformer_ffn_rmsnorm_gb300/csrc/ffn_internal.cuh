@@ -95,7 +95,8 @@ cudaError_t launch_swiglu_f32in(const float *gate, const float *up, void *h, voi
 // fp32 SIMT block: n (rows x d) and h (rows x ffn) are fp32 scratch.
 cudaError_t launch_simt_block(const float *x, const float *g, const float *wg, const float *wu,
                               const float *wd, float *y, int64_t rows, int64_t d, int64_t ffn,
-                              float eps, float *n, float *h, cudaStream_t s);
+                              float eps, float *n, float *h, cudaStream_t s,
+                              const float *res = nullptr);
 
 // Decode (weight-streaming) block for rows <= 16.
 struct GemvWorkspace {
@@ -118,7 +119,8 @@ struct GemvWeights {
 };
 cudaError_t launch_gemv_block(int wfmt, const void *x, const void *g, GemvWeights wg,
                               GemvWeights wu, GemvWeights wd, void *y, int64_t rows, int64_t d,
-                              int64_t ffn, float eps, const GemvWorkspace &ws, cudaStream_t s);
+                              int64_t ffn, float eps, const GemvWorkspace &ws, cudaStream_t s,
+                              const void *res = nullptr);
 
 // A 2D tiled TMA descriptor over a row-major array of `rows` rows, `inner`
 // elements a row, rows `row_bytes` apart; boxes of box_inner x box_rows.
@@ -138,9 +140,10 @@ cudaError_t launch_gemm_gateup(int dt, const void *A, const void *A_lo, const vo
                                const void *Wu, void *H, void *H_lo, void *G, void *U, int64_t M,
                                int64_t K, int64_t F, bool fused, float acc_scale, float out_scale,
                                cudaStream_t s);
+// res (optional): added to C before its one rounding (same type and layout as C)
 cudaError_t launch_gemm_plain(int dt, int dt_out, const void *A, const void *A_lo, const void *B,
                               void *C, int64_t M, int64_t K, int64_t N, float acc_scale,
-                              cudaStream_t s);
+                              const void *res, cudaStream_t s);
 
 }  // namespace ffn
 

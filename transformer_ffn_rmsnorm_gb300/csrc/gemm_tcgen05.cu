@@ -93,6 +93,7 @@ struct GemmParams {
     float acc_scale;          // applied to every accumulator value (exact powers of two)
     float out_scale;          // fused: applied to h before rounding
     int a_keep;               // keep A in L2 (evict-last): every wave of tiles re-reads it
+    const void *res;          // plain: added to C before rounding (same type and layout as C), or null
 };
 
 // Stores NV (16 or 32) values rounded once; with `lo` also the rounding
@@ -115,6 +116,21 @@ __device__ __forceinline__ void store_row(T *dst, T *lo, int64_t col, int64_t nc
                 for (int e = 0; e < 8; ++e) f[e] -= hf[e];
                 *reinterpret_cast<uint4 *>(lo + col + 8 * j) = Vec16<T>::pack(f);
             }
+        }
+    }
+}
+
+// v[e] += src[col + e] for the NV (16 or 32) columns from col that are
+// below ncols (a multiple of 8), 16-byte loads.
+template <typename T, int NV>
+__device__ __forceinline__ void add_row(const T *src, int64_t col, int64_t ncols, float (&v)[NV]) {
+#pragma unroll
+    for (int j = 0; j < NV / 8; ++j) {
+        if (col + 8 * j < ncols) {
+            float f[8];
+            Vec16<T>::unpack(*reinterpret_cast<const uint4 *>(src + col + 8 * j), f);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[8 * j + e] += f[e];
         }
     }
 }
@@ -386,9 +402,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     float v[CW];
 #pragma unroll
                     for (int j = 0; j < CW; ++j) v[j] = __uint_as_float(r[j]) * p.acc_scale;
-                    if (live)
-                        store_row<TOut, CW>(static_cast<TOut *>(p.out0) + row * p.ldo, nullptr, n_blk * BN + c,
-                                            p.N, v);
+                    if (live) {
+                        const int64_t col = n_blk * BN + c;
+                        if (p.res) add_row<TOut, CW>(static_cast<const TOut *>(p.res) + row * p.ldo, col, p.N, v);
+                        store_row<TOut, CW>(static_cast<TOut *>(p.out0) + row * p.ldo, nullptr, col, p.N, v);
+                    }
                 }
             } else {
 #pragma unroll 1
@@ -514,7 +532,7 @@ bool make_map(CUtensorMap *m, const void *ptr, bool bf16, int64_t inner, int64_t
 template <int MODE, bool BF16, int A_TERMS, bool OUT_BF16, int BN, bool PAIR>
 cudaError_t launch_kernel(const void *A, const void *A2, const void *B0, const void *B1, void *out0,
                           void *out1, int64_t M, int64_t K, int64_t N, int kind, float acc_scale,
-                          float out_scale, cudaStream_t s) {
+                          float out_scale, const void *res, cudaStream_t s) {
     constexpr size_t SMEM_BYTES = Ring<A_TERMS, BN, PAIR>::SMEM_BYTES;
     constexpr int NCTA = PAIR ? 2 : 1;
     const auto kern = &gemm_tcgen05_kernel<MODE, BF16, A_TERMS, OUT_BF16, BN, PAIR>;
@@ -579,6 +597,7 @@ cudaError_t launch_kernel(const void *A, const void *A2, const void *B0, const v
     // every wave of tiles re-reads all of A (tiles are ordered row block
     // fastest); ask L2 to keep it when it fits comfortably
     p.a_keep = (num_n_blocks > 1 && M * K * 2 * A_TERMS <= (int64_t{96} << 20)) ? 1 : 0;
+    p.res = res;
     if (!p.err) return cudaErrorUnknown;
     // persistent: one unit of CTAs per co-resident slot, never more units
     // than there is work for
@@ -608,13 +627,13 @@ cudaError_t launch_kernel(const void *A, const void *A2, const void *B0, const v
 template <int MODE, bool BF16, int A_TERMS, bool OUT_BF16 = BF16, int BN = 256>
 cudaError_t launch_impl(const void *A, const void *A2, const void *B0, const void *B1, void *out0,
                         void *out1, int64_t M, int64_t K, int64_t N, int kind, float acc_scale,
-                        float out_scale, cudaStream_t s) {
+                        float out_scale, cudaStream_t s, const void *res = nullptr) {
     if (M <= 0) return cudaSuccess;
     if (M > BM)
         return launch_kernel<MODE, BF16, A_TERMS, OUT_BF16, BN, true>(A, A2, B0, B1, out0, out1, M, K, N, kind,
-                                                                       acc_scale, out_scale, s);
+                                                                       acc_scale, out_scale, res, s);
     return launch_kernel<MODE, BF16, A_TERMS, OUT_BF16, BN, false>(A, A2, B0, B1, out0, out1, M, K, N, kind,
-                                                                    acc_scale, out_scale, s);
+                                                                    acc_scale, out_scale, res, s);
 }
 
 // Tile width of the plain GEMM: waves of tiles times the width of a tile
@@ -671,28 +690,28 @@ cudaError_t launch_gemm_gateup(int dt, const void *A, const void *A_lo, const vo
 
 template <bool BF16, int A_TERMS, bool OUT_BF16>
 cudaError_t launch_plain_bn(const void *A, const void *A_lo, const void *B, void *C, int64_t M,
-                            int64_t K, int64_t N, float acc_scale, cudaStream_t s) {
+                            int64_t K, int64_t N, float acc_scale, const void *res, cudaStream_t s) {
     if (tile_width(M, N) == 224)
         return launch_impl<MODE_PLAIN, BF16, A_TERMS, OUT_BF16, 224>(A, A_lo, B, nullptr, C, nullptr, M, K,
-                                                                     N, K_GEMM_DOWN, acc_scale, 1.f, s);
+                                                                     N, K_GEMM_DOWN, acc_scale, 1.f, s, res);
     return launch_impl<MODE_PLAIN, BF16, A_TERMS, OUT_BF16, 256>(A, A_lo, B, nullptr, C, nullptr, M, K, N,
-                                                                 K_GEMM_DOWN, acc_scale, 1.f, s);
+                                                                 K_GEMM_DOWN, acc_scale, 1.f, s, res);
 }
 
 cudaError_t launch_gemm_plain(int dt, int dt_out, const void *A, const void *A_lo, const void *B,
                               void *C, int64_t M, int64_t K, int64_t N, float acc_scale,
-                              cudaStream_t s) {
+                              const void *res, cudaStream_t s) {
     const float a = acc_scale;
     if (dt == DT_BF16) {
-        if (A_lo) return launch_plain_bn<true, 2, true>(A, A_lo, B, C, M, K, N, a, s);
-        return launch_plain_bn<true, 1, true>(A, nullptr, B, C, M, K, N, a, s);
+        if (A_lo) return launch_plain_bn<true, 2, true>(A, A_lo, B, C, M, K, N, a, res, s);
+        return launch_plain_bn<true, 1, true>(A, nullptr, B, C, M, K, N, a, res, s);
     }
     if (dt_out == DT_BF16) {   // fp16 operands, bf16 output (prepared-weights path)
-        if (A_lo) return launch_plain_bn<false, 2, true>(A, A_lo, B, C, M, K, N, a, s);
-        return launch_plain_bn<false, 1, true>(A, nullptr, B, C, M, K, N, a, s);
+        if (A_lo) return launch_plain_bn<false, 2, true>(A, A_lo, B, C, M, K, N, a, res, s);
+        return launch_plain_bn<false, 1, true>(A, nullptr, B, C, M, K, N, a, res, s);
     }
-    if (A_lo) return launch_plain_bn<false, 2, false>(A, A_lo, B, C, M, K, N, a, s);
-    return launch_plain_bn<false, 1, false>(A, nullptr, B, C, M, K, N, a, s);
+    if (A_lo) return launch_plain_bn<false, 2, false>(A, A_lo, B, C, M, K, N, a, res, s);
+    return launch_plain_bn<false, 1, false>(A, nullptr, B, C, M, K, N, a, res, s);
 }
 
 }  // namespace ffn

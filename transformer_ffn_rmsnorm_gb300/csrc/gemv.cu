@@ -353,7 +353,8 @@ template <int WF, int NT, bool TWO>
 __global__ void __launch_bounds__(128) gemv_down_kernel(
     const void *wd, const uint16_t *sd, const uint4 *__restrict__ hfrag,
     const uint4 *__restrict__ hfrag_lo, void *y_, float *partials,
-    unsigned *counters, int rows, int64_t D, int64_t F, int64_t nchF, int64_t units_per_split) {
+    unsigned *counters, int rows, int64_t D, int64_t F, int64_t nchF, int64_t units_per_split,
+    const void *res) {
     using T = typename Fmt<WF>::TIn;
     constexpr bool q4 = WF == WF_Q4;
     constexpr int U = q4 ? 2 : 8;
@@ -407,7 +408,9 @@ __global__ void __launch_bounds__(128) gemv_down_kernel(
         float sum = 0.f;
         for (int sp = 0; sp < nsplit; ++sp)
             sum += __ldcg(partials + (static_cast<int64_t>(sp) * rows + token) * D + feat);
-        y[static_cast<int64_t>(token) * D + feat] = from_f32<T>(sum * out_scale);
+        float v = sum * out_scale;
+        if (res) v += to_f32(static_cast<const T *>(res)[static_cast<int64_t>(token) * D + feat]);
+        y[static_cast<int64_t>(token) * D + feat] = from_f32<T>(v);
     }
     if (threadIdx.x == 0) counters[blockIdx.x] = 0u;
 }
@@ -439,7 +442,7 @@ size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 template <int WF, int NT, bool TWO>
 cudaError_t launch_typed(const void *x, const void *gain, GemvWeights wg, GemvWeights wu,
                          GemvWeights wd, void *y, int rows, int64_t d, int64_t ffn, float eps,
-                         const GemvWorkspace &ws, const Geometry &geo, cudaStream_t s) {
+                         const GemvWorkspace &ws, const Geometry &geo, cudaStream_t s, const void *res) {
     constexpr bool q4 = WF == WF_Q4;
     {
         LaunchScope scope(K_GEMV_NORM, s);
@@ -456,7 +459,7 @@ cudaError_t launch_typed(const void *x, const void *gain, GemvWeights wg, GemvWe
                                                           static_cast<int>(geo.groups), s);
         if (e != cudaSuccess) return e;
         return launch_stream_down<WF, NT, TWO>(wd, ws.hfrag, ws.hfrag_lo, y, ws.partials, ws.counters, rows, d,
-                                               ffn, geo.nchF, stream_down_splits(WF, d, ffn), s);
+                                               ffn, geo.nchF, stream_down_splits(WF, d, ffn), res, s);
     }
     {
         const int64_t tiles = 2 * geo.nchF;  // covers every fragment slot of h
@@ -477,7 +480,7 @@ cudaError_t launch_typed(const void *x, const void *gain, GemvWeights wg, GemvWe
         gemv_down_kernel<WF, NT, TWO><<<grid, 32 * kDnTPC, 0, s>>>(
             q4 ? static_cast<const void *>(wd.qs) : wd.w, wd.sc, static_cast<const uint4 *>(ws.hfrag),
             static_cast<const uint4 *>(ws.hfrag_lo), y, ws.partials, ws.counters, rows, d, ffn, geo.nchF,
-            geo.ups);
+            geo.ups, res);
         return cudaGetLastError();
     }
 }
@@ -485,9 +488,9 @@ cudaError_t launch_typed(const void *x, const void *gain, GemvWeights wg, GemvWe
 template <int WF, bool TWO>
 cudaError_t launch_nt(int nt, const void *x, const void *g, GemvWeights wg, GemvWeights wu,
                       GemvWeights wd, void *y, int rows, int64_t d, int64_t ffn, float eps,
-                      const GemvWorkspace &ws, const Geometry &geo, cudaStream_t s) {
-    return nt == 1 ? launch_typed<WF, 1, TWO>(x, g, wg, wu, wd, y, rows, d, ffn, eps, ws, geo, s)
-                   : launch_typed<WF, 2, TWO>(x, g, wg, wu, wd, y, rows, d, ffn, eps, ws, geo, s);
+                      const GemvWorkspace &ws, const Geometry &geo, cudaStream_t s, const void *res) {
+    return nt == 1 ? launch_typed<WF, 1, TWO>(x, g, wg, wu, wd, y, rows, d, ffn, eps, ws, geo, s, res)
+                   : launch_typed<WF, 2, TWO>(x, g, wg, wu, wd, y, rows, d, ffn, eps, ws, geo, s, res);
 }
 
 struct Layout {
@@ -540,22 +543,23 @@ void gemv_carve(void *base, int64_t rows, int64_t d, int64_t ffn, bool two_terms
 
 cudaError_t launch_gemv_block(int wfmt, const void *x, const void *g, GemvWeights wg,
                               GemvWeights wu, GemvWeights wd, void *y, int64_t rows, int64_t d,
-                              int64_t ffn, float eps, const GemvWorkspace &ws, cudaStream_t s) {
+                              int64_t ffn, float eps, const GemvWorkspace &ws, cudaStream_t s,
+                              const void *res) {
     if (rows <= 0) return cudaSuccess;
     const Geometry geo = geometry(rows, d, ffn, wfmt == WF_Q4);
     const int r = static_cast<int>(rows);
     const bool two = ws.nfrag_lo != nullptr;
     switch (wfmt) {
         case WF_F16:
-            return two ? launch_nt<WF_F16, true>(geo.nt, x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s)
-                       : launch_nt<WF_F16, false>(geo.nt, x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s);
+            return two ? launch_nt<WF_F16, true>(geo.nt, x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s, res)
+                       : launch_nt<WF_F16, false>(geo.nt, x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s, res);
         case WF_BF16:
-            return two ? launch_nt<WF_BF16, true>(geo.nt, x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s)
-                       : launch_nt<WF_BF16, false>(geo.nt, x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s);
+            return two ? launch_nt<WF_BF16, true>(geo.nt, x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s, res)
+                       : launch_nt<WF_BF16, false>(geo.nt, x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s, res);
         case WF_Q4:   // fp16 operands: one term is enough
-            return launch_nt<WF_Q4, false>(geo.nt, x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s);
+            return launch_nt<WF_Q4, false>(geo.nt, x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s, res);
         default:      // prepared fp16 weights
-            return launch_nt<WF_F16P, false>(geo.nt, x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s);
+            return launch_nt<WF_F16P, false>(geo.nt, x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s, res);
     }
 }
 

@@ -107,7 +107,7 @@ cudaError_t launch_stream_gateup(GemvWeights wg, GemvWeights wu, const void *nfr
 template <int WF, int NT, bool TWO>
 cudaError_t launch_stream_down(GemvWeights wd, const void *hfrag, const void *hfrag_lo, void *y,
                                float *partials, unsigned *counters, int rows, int64_t d, int64_t ffn,
-                               int64_t nchF, int64_t splits, cudaStream_t s);
+                               int64_t nchF, int64_t splits, const void *res, cudaStream_t s);
 
 }  // namespace gemv
 }  // namespace ffn

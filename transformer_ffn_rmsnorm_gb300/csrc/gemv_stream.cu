@@ -76,6 +76,7 @@ struct StreamParams {
     int rows;               // token rows (<= 16)
     int64_t D;              // down: output features
     unsigned *err;
+    const void *res;        // down: added to y before its rounding ([rows x D] of y's type), or null
 };
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
@@ -360,7 +361,9 @@ __global__ void __launch_bounds__(kThreads) gemv_stream_kernel(
                     float sum = 0.f;
                     for (int sp = 0; sp < nsplit; ++sp)
                         sum += __ldcg(p.partials + (static_cast<int64_t>(sp) * p.rows + token) * p.D + feat);
-                    y[static_cast<int64_t>(token) * p.D + feat] = from_f32<T>(sum * out_scale);
+                    float v = sum * out_scale;
+                    if (p.res) v += to_f32(static_cast<const T *>(p.res)[static_cast<int64_t>(token) * p.D + feat]);
+                    y[static_cast<int64_t>(token) * p.D + feat] = from_f32<T>(v);
                 }
                 if (threadIdx.x == 0) p.counters[blockIdx.x] = 0u;
             }
@@ -448,6 +451,7 @@ cudaError_t launch_stream_gateup(GemvWeights wg, GemvWeights wu, const void *nfr
     p.ncounters = ncounters;
     p.err = device_status_word();
     if (!p.err) return cudaErrorUnknown;
+    p.res = nullptr;
     // 32 features per CTA; covering nchF * 32 features writes every slot of h
     const int64_t blocks = nchF;
     LaunchScope scope(K_GEMV_GATEUP, s);
@@ -459,7 +463,7 @@ cudaError_t launch_stream_gateup(GemvWeights wg, GemvWeights wu, const void *nfr
 template <int WF, int NT, bool TWO>
 cudaError_t launch_stream_down(GemvWeights wd, const void *hfrag, const void *hfrag_lo, void *y,
                                float *partials, unsigned *counters, int rows, int64_t d, int64_t ffn,
-                               int64_t nchF, int64_t splits, cudaStream_t s) {
+                               int64_t nchF, int64_t splits, const void *res, cudaStream_t s) {
     using TL = Tile<WF, ROLE_DOWN, NT, TWO>;
     constexpr auto kern = gemv_stream_kernel<WF, NT, TWO, ROLE_DOWN>;
     cudaError_t e = set_smem<kern>(TL::smem_bytes);
@@ -480,6 +484,7 @@ cudaError_t launch_stream_down(GemvWeights wd, const void *hfrag, const void *hf
     p.counters = counters;
     p.rows = rows;
     p.D = d;
+    p.res = res;
     p.err = device_status_word();
     if (!p.err) return cudaErrorUnknown;
     const int64_t nsplit = cdiv(p.nkb, p.kb_per_split);
@@ -510,7 +515,7 @@ int64_t stream_down_splits(int wfmt, int64_t d, int64_t ffn) {
                                                            cudaStream_t);                                \
     template cudaError_t launch_stream_down<WF, NT, TWO>(GemvWeights, const void *, const void *, void *, \
                                                          float *, unsigned *, int, int64_t, int64_t,     \
-                                                         int64_t, int64_t, cudaStream_t);
+                                                         int64_t, int64_t, const void *, cudaStream_t);
 FFN_STREAM_INSTANTIATE(WF_F16, 1, false)
 FFN_STREAM_INSTANTIATE(WF_F16, 2, false)
 FFN_STREAM_INSTANTIATE(WF_F16, 1, true)

@@ -20,7 +20,8 @@ __global__ void __launch_bounds__(256) simt_gemm_nt_kernel(const float *__restri
                                                            const float *__restrict__ B0,
                                                            const float *__restrict__ B1,
                                                            float *__restrict__ C, int64_t M,
-                                                           int64_t N, int64_t K) {
+                                                           int64_t N, int64_t K,
+                                                           const float *__restrict__ R) {
     constexpr int NB = GATEUP ? 2 : 1;
     __shared__ float As[BK][BM + 4];
     __shared__ float Bs[NB][BK][BN + 4];
@@ -84,6 +85,7 @@ __global__ void __launch_bounds__(256) simt_gemm_nt_kernel(const float *__restri
             if (n >= N) continue;
             float v = acc[0][i][j];
             if constexpr (GATEUP) v = silu_f32(v) * acc[NB - 1][i][j];
+            else if (R) v += R[m * N + n];   // the block's skip connection
             C[m * N + n] = v;
         }
     }
@@ -93,20 +95,20 @@ __global__ void __launch_bounds__(256) simt_gemm_nt_kernel(const float *__restri
 
 cudaError_t launch_simt_block(const float *x, const float *g, const float *wg, const float *wu,
                               const float *wd, float *y, int64_t rows, int64_t d, int64_t ffn,
-                              float eps, float *n, float *h, cudaStream_t s) {
+                              float eps, float *n, float *h, cudaStream_t s, const float *res) {
     cudaError_t e = launch_rmsnorm(x, g, n, rows, d, eps, DT_F32, s);
     if (e != cudaSuccess) return e;
     {
         dim3 grid(static_cast<unsigned>((rows + BM - 1) / BM), static_cast<unsigned>((ffn + BN - 1) / BN));
         LaunchScope scope(K_SIMT_GATEUP, s);
-        simt_gemm_nt_kernel<true><<<grid, 256, 0, s>>>(n, wg, wu, h, rows, ffn, d);
+        simt_gemm_nt_kernel<true><<<grid, 256, 0, s>>>(n, wg, wu, h, rows, ffn, d, nullptr);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     {
         dim3 grid(static_cast<unsigned>((rows + BM - 1) / BM), static_cast<unsigned>((d + BN - 1) / BN));
         LaunchScope scope(K_SIMT_DOWN, s);
-        simt_gemm_nt_kernel<false><<<grid, 256, 0, s>>>(h, wd, nullptr, y, rows, d, ffn);
+        simt_gemm_nt_kernel<false><<<grid, 256, 0, s>>>(h, wd, nullptr, y, rows, d, ffn, res);
         e = cudaGetLastError();
     }
     return e;
