@@ -86,6 +86,11 @@ class Oracle:
         L.oracle_q4_dequant.argtypes = [ctypes.POINTER(ctypes.c_uint8),
                                         ctypes.POINTER(ctypes.c_uint16), _D,
                                         ctypes.c_int64, ctypes.c_int64]
+        L.oracle_e4m3_to_double.restype = ctypes.c_double
+        L.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+        L.oracle_fp8_dequant.restype = None
+        L.oracle_fp8_dequant.argtypes = [ctypes.POINTER(ctypes.c_uint8), ctypes.POINTER(ctypes.c_float), _D,
+                                         ctypes.c_int64, ctypes.c_int64]
         self.L = L
 
     # -- scalars ---------------------------------------------------------
@@ -94,6 +99,9 @@ class Oracle:
 
     def half_to_double(self, bits: int) -> float:
         return self.L.oracle_half_to_double(int(bits) & 0xFFFF)
+
+    def e4m3_to_double(self, code: int) -> float:
+        return self.L.oracle_e4m3_to_double(int(code) & 0xFF)
 
     # -- arrays (float64 in, float64 out) --------------------------------
     def rmsnorm(self, x, g, eps: float, nthreads: int | None = None) -> np.ndarray:
@@ -136,6 +144,26 @@ class Oracle:
         if rc != 0:
             raise MemoryError("oracle scratch allocation failed")
         return x + y if residual else y
+
+    def fp8_dequant(self, codes, scales, out: int, inn: int) -> np.ndarray:
+        codes = np.ascontiguousarray(codes, dtype=np.uint8)
+        scales = np.ascontiguousarray(scales, dtype=np.float32)
+        assert codes.size == out * inn and scales.size == out
+        w = np.empty((out, inn), dtype=np.float64)
+        self.L.oracle_fp8_dequant(codes.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8)),
+                                  scales.ctypes.data_as(ctypes.POINTER(ctypes.c_float)), _ptr(w), out, inn)
+        return w
+
+    def fp8_block_from_inputs(self, inp: dict, rows=None, nthreads=None, residual=False) -> np.ndarray:
+        """Oracle y for a ``synth.make_fp8_inputs`` dict, on weights the oracle
+        dequantises itself from the e4m3 codes and row scales."""
+        cfg = inp["cfg"]
+        D, F = cfg.d, cfg.ffn
+        wg = self.fp8_dequant(inp["c_gate"], inp["s_gate"], F, D)
+        wu = self.fp8_dequant(inp["c_up"], inp["s_up"], F, D)
+        wd = self.fp8_dequant(inp["c_down"], inp["s_down"], D, F)
+        x = inp["x"] if rows is None else inp["x"][np.asarray(rows)]
+        return self.ffn_block(widen(x, "bf16"), widen(inp["g"], "bf16"), wg, wu, wd, cfg.eps, nthreads, residual)
 
     def q4_dequant(self, qs, scales, out: int, inn: int) -> np.ndarray:
         qs = np.ascontiguousarray(qs, dtype=np.uint8)

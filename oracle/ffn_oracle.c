@@ -60,6 +60,24 @@ double oracle_half_to_double(uint16_t h) {
     return sign ? -v : v;
 }
 
+/* IEEE-style 8-bit float e4m3 (the "fn" variant: no infinities) decoded to
+ * double: sign (1 bit), exponent (4 bits, bias 7), fraction (3 bits);
+ * exponent 0 means subnormal (fraction * 2^-9); exponent 15 with fraction 7
+ * is NaN (the only non-finite code, so the largest value is 448). */
+double oracle_e4m3_to_double(uint8_t b) {
+    int sign = (b >> 7) & 1;
+    int e = (b >> 3) & 0xF;
+    int f = b & 0x7;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -9);
+    else if (e == 15 && f == 7)
+        v = NAN;
+    else
+        v = ldexp((double)(8 + f), e - 10);
+    return sign ? -v : v;
+}
+
 /* ----------------------------------------------------------- thread pool */
 
 typedef void (*range_fn)(void *ctx, int64_t lo, int64_t hi);
@@ -215,5 +233,16 @@ void oracle_q4_dequant(const uint8_t *qs, const uint16_t *scales, double *w,
                 w[o * in + blk * 32 + j] = (double)(u - 8) * s;
             }
         }
+    }
+}
+
+/* ------------------------------------------------------------------ fp8 */
+
+/* Dequantise fp8 weights: codes[o][i] is an e4m3 byte, scales[o] the row's
+ * float scale; w[o][i] = e4m3(codes[o][i]) * scales[o], exact in double. */
+void oracle_fp8_dequant(const uint8_t *codes, const float *scales, double *w, int64_t out, int64_t in) {
+    for (int64_t o = 0; o < out; ++o) {
+        const double s = (double)scales[o];
+        for (int64_t i = 0; i < in; ++i) w[o * in + i] = oracle_e4m3_to_double(codes[o * in + i]) * s;
     }
 }

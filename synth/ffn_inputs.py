@@ -30,7 +30,7 @@ __all__ = [
     "C4_PREFILL_BF16", "C5_DECODE_Q4", "CONFIGS",
     "stream", "normal", "round_to_storage", "make_block_inputs",
     "make_norm_inputs", "make_swiglu_inputs", "make_q4_inputs", "pack_q4",
-    "q4_canonical_bytes", "TENSOR_IDS",
+    "q4_canonical_bytes", "TENSOR_IDS", "Fp8Config", "C6_DECODE_FP8", "make_fp8_inputs", "to_e4m3",
 ]
 
 # Tensor ids inside one seed.  Each id owns an independent stream.
@@ -39,6 +39,7 @@ TENSOR_IDS = {
     "q_gate": 5, "q_up": 6, "q_down": 7,
     "s_gate": 8, "s_up": 9, "s_down": 10,
     "gate": 11, "up": 12,
+    "f8_gate": 13, "f8_up": 14, "f8_down": 15, "f8s_gate": 16, "f8s_up": 17, "f8s_down": 18,
 }
 
 _CHUNK = 1 << 22
@@ -142,9 +143,22 @@ C3_DECODE_BF16 = BlockConfig("decode_bf16_8x4096x14336", 8, 4096, 14336, 1e-5, "
 C4_PREFILL_BF16 = BlockConfig("prefill_bf16_4096x4096x11008", 4096, 4096, 11008, 1e-6, "bf16")
 C5_DECODE_Q4 = Q4Config("decode_q4_8x5120x17408", 8, 5120, 17408, 1e-6)
 
+
+@dataclass(frozen=True)
+class Fp8Config:
+    name: str
+    rows: int
+    d: int
+    ffn: int
+    eps: float
+
+
+# the bf16 decode shape with e4m3 weights (per-row float scales)
+C6_DECODE_FP8 = Fp8Config("decode_fp8_8x4096x14336", 8, 4096, 14336, 1e-5)
+
 CONFIGS = {
     "c1": C1_TINY_F32, "c2a": C2A_RMSNORM_F16, "c2b": C2B_SWIGLU_F16,
-    "c3": C3_DECODE_BF16, "c4": C4_PREFILL_BF16, "c5": C5_DECODE_Q4,
+    "c3": C3_DECODE_BF16, "c4": C4_PREFILL_BF16, "c5": C5_DECODE_Q4, "c6": C6_DECODE_FP8,
 }
 
 
@@ -250,4 +264,32 @@ def make_q4_inputs(cfg: Q4Config, seed: int = 0, rows: int | None = None,
         res["s_" + name] = s16
         res["qs_" + name] = qs
         res["sc_" + name] = sc
+    return res
+
+
+def to_e4m3(v: np.ndarray) -> np.ndarray:
+    """e4m3 ("fn") codes of float values, round to nearest even (a library
+    conversion; values must lie within +-448)."""
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(v, dtype=np.float32))
+    return t.to(torch.float8_e4m3fn).view(torch.uint8).numpy().copy()
+
+
+def make_fp8_inputs(cfg: Fp8Config, seed: int = 0, rows: int | None = None,
+                    d: int | None = None, ffn: int | None = None) -> dict:
+    """x~N(0,1) bf16, g=1+0.1*N(0,1) bf16, weights as e4m3 codes of
+    16*N(0,1) with float32 row scales (1 + 0.1*N(0,1)) / (16*sqrt(fan_in)),
+    i.e. weights ~N(0, 1/fan_in) as in the other block workloads."""
+    cfg = replace(cfg, rows=rows if rows is not None else cfg.rows,
+                  d=d if d is not None else cfg.d,
+                  ffn=ffn if ffn is not None else cfg.ffn)
+    M, D, F = cfg.rows, cfg.d, cfg.ffn
+    res = {"cfg": cfg,
+           "x": normal((M, D), 0.0, 1.0, seed, "x", "bf16"),
+           "g": normal((D,), 1.0, 0.1, seed, "g", "bf16")}
+    for name, (o, i) in (("gate", (F, D)), ("up", (F, D)), ("down", (D, F))):
+        v = np.clip(16.0 * stream(seed, "f8_" + name).standard_normal((o, i)), -448.0, 448.0)
+        res["c_" + name] = to_e4m3(v)
+        sc = (1.0 + 0.1 * stream(seed, "f8s_" + name).standard_normal(o)) / (16.0 * math.sqrt(i))
+        res["s_" + name] = sc.astype(np.float32)
     return res

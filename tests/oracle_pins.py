@@ -267,4 +267,37 @@ def pin_q4_single_weights(o):
             assert np.array_equal(w, ref), (o_, j)
 
 
+
+
+# --------------------------------------------------------------------- fp8
+
+def pin_e4m3_decoder(o):
+    """Every one of the 256 codes against the e4m3 ("fn") conversion of a
+    library, plus hand-checked values of the format."""
+    import torch
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = np.array([o.e4m3_to_double(c) for c in range(256)])
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(got[ok], ref[ok])
+    for code, v in ((0x38, 1.0), (0x40, 2.0), (0xB8, -1.0), (0x7E, 448.0), (0x01, 2.0 ** -9),
+                    (0x08, 2.0 ** -6), (0x07, 7 * 2.0 ** -9), (0x39, 1.125), (0x00, 0.0)):
+        assert o.e4m3_to_double(code) == v, (hex(code), v)
+    assert math.isnan(o.e4m3_to_double(0x7F)) and math.isnan(o.e4m3_to_double(0xFF))
+
+
+def pin_fp8_dequant_rows(o):
+    """Each row is its codes' values times that row's scale, nothing else."""
+    rng = np.random.default_rng(19)
+    out, inn = 5, 24
+    codes = rng.integers(0, 256, (out, inn)).astype(np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x3C      # no NaN codes
+    scales = (rng.standard_normal(out) * 0.01).astype(np.float32)
+    w = o.fp8_dequant(codes, scales, out, inn)
+    for r in range(out):
+        for i in range(inn):
+            assert w[r, i] == o.e4m3_to_double(codes[r, i]) * float(scales[r])
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -30,6 +30,10 @@ MUTANTS = [
     ("q4_group_not_interleaved", "gp[16 * t + 4 * b + e]", "gp[16 * b + 4 * t + e]"),
     ("half_bias", "e - 25", "e - 24"),
     ("half_subnormal_scale", "ldexp((double)f, -24)", "ldexp((double)f, -25)"),
+    ("e4m3_bias", "ldexp((double)(8 + f), e - 10)", "ldexp((double)(8 + f), e - 11)"),
+    ("e4m3_no_implicit_one", "ldexp((double)(8 + f), e - 10)", "ldexp((double)f, e - 7)"),
+    ("e4m3_subnormal_scale", "v = ldexp((double)f, -9);", "v = ldexp((double)f, -10);"),
+    ("fp8_scale_of_wrong_row", "const double s = (double)scales[o];", "const double s = (double)scales[(o + 1) % out];"),
 ]
 
 
