@@ -8,7 +8,7 @@ tcgen05 gate/up GEMM with the SwiGLU epilogue -> tcgen05 down GEMM), on seeded
 synthetic inputs.  The weights are re-encoded once, before timing, by
 ffn_prepare_weights (fp16 values of w * 2^8, exact), so the tensor operands are
 fp16; the unprepared bf16 path (hi + lo activation terms) is timed beside it.  Rank 0 prints one JSON line.  The standalone RMSNorm and SwiGLU
-workloads, the bf16 decode block and the Q4 decode block are timed after it
+workloads, the bf16 decode block, the Q4 and the e4m3 decode blocks are timed after it
 and reported under "sub".
 
 --impl reference times the float64 CPU oracle on the host cores on a bounded
@@ -45,7 +45,7 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-sub", action="store_true", help="skip the secondary workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU baseline")
-    ap.add_argument("--workload", choices=["prefill", "decode", "decode_prepared", "q4", "rmsnorm", "swiglu"],
+    ap.add_argument("--workload", choices=["prefill", "decode", "decode_prepared", "q4", "fp8", "rmsnorm", "swiglu"],
                     default="prefill",
                     help="prefill: the benchmark; others run only that workload (for profiling)")
     ap.add_argument("--only-main", action="store_true",
@@ -241,6 +241,7 @@ def sub_benchmarks(torch, ffn, device, peaks, peak_src, stream):
     # from CUDA-graph replay, per-kernel event times alongside
     out.append(decode_bench(torch, ffn, device, hbm, peak_src, stream))
     out.append(q4_bench(torch, ffn, device, hbm, peak_src, stream))
+    out.append(fp8_bench(torch, ffn, device, hbm, peak_src, stream))
     return out
 
 
@@ -310,8 +311,38 @@ def q4_bench(torch, ffn, device, hbm, peak_src, stream):
                          "peak_source": peak_src + " hbm_gbs (copy, burst)", "algorithmic_bytes": wbytes}}
 
 
+def fp8_setup(torch, ffn, device):
+    cfg = synth.C6_DECODE_FP8
+    inp = synth.make_fp8_inputs(cfg, seed=0)
+    x8 = to_dev(inp["x"], "bf16", torch, device)
+    g8 = to_dev(inp["g"], "bf16", torch, device)
+    wsets = []
+    for _ in range(2):   # two weight copies rotated: 2 x 176 MB > L2
+        wsets.append([(torch.from_numpy(inp["c_" + n]).to(device), torch.from_numpy(inp["s_" + n]).to(device))
+                      for n in ("gate", "up", "down")])
+    y8 = torch.empty_like(x8)
+    ws = ffn.workspace(ffn.ffn_block_fp8_workspace_bytes(cfg.rows, cfg.d, cfg.ffn), device)
+    return cfg, (lambda i: ffn.ffn_block_forward_fp8(x8, g8, *wsets[i % 2], eps=cfg.eps, out=y8, ws=ws))
+
+
+def fp8_bench(torch, ffn, device, hbm, peak_src, stream):
+    cfg, call = fp8_setup(torch, ffn, device)
+    us = graph_time_us(torch, call, 20, 10, stream)
+    with ffn.KernelTimer() as kt:
+        timed_loop(torch, call, 50, 3, stream)
+        res = kt.read()
+    wbytes = 3 * cfg.ffn * cfg.d + (2 * cfg.ffn + cfg.d) * 4   # codes and row scales
+    return {"workload": cfg.name, "us_per_call": round(us, 3), "tokens_per_s": round(cfg.rows / us * 1e6, 1),
+            "timing": "CUDA graph of 20 calls (two weight copies alternating), 10 replays",
+            "kernels_events": kernel_table(res),
+            "roofline": {"bound": "hbm", "kernel": "whole block (3 launches)",
+                         "achieved": round(wbytes / us / 1e3, 1), "peak": hbm, "unit": "GB/s",
+                         "frac": round(wbytes / us / 1e3 / hbm, 4),
+                         "peak_source": peak_src + " hbm_gbs (copy, burst)", "algorithmic_bytes": wbytes}}
+
+
 def run_workload_only(args):
-    """--workload decode|decode_prepared|q4: run that workload for --warmup +
+    """--workload decode|decode_prepared|q4|fp8|rmsnorm|swiglu: run that workload for --warmup +
     --steps calls and print a short line (used for ncu captures)."""
     import torch
     from transformer_ffn_rmsnorm_gb300 import ffn
@@ -330,6 +361,8 @@ def run_workload_only(args):
         call = lambda i: ffn.ffn_swiglu(ga, up, out=h)
     elif args.workload == "q4":
         cfg, call = q4_setup(torch, ffn, device)
+    elif args.workload == "fp8":
+        cfg, call = fp8_setup(torch, ffn, device)
     else:
         cfg, call = decode_setup(torch, ffn, device, prepared=args.workload == "decode_prepared")
     for i in range(args.warmup + args.steps):

@@ -201,6 +201,49 @@ ffn_status ffn_block_forward_q4(const void *x, const void *g, ffn_q4_weight w_ga
                                 size_t workspace_bytes, void *stream);
 
 /* ------------------------------------------------------------------------
+ * e4m3 weights with one float scale per output row.  The pages store 8-bit
+ * quantised data only for the KV cache ("Unfusing a Kernel Made It 1.63x
+ * Faster", section "Finding 2: a quantized KV cache buys nothing while
+ * you're occupancy-bound": halving the bytes pays once the kernel is bound
+ * by memory); these are the projection weights at one byte each, half the
+ * stream of bf16, which is the whole cost of a decode step.
+ *   codes: [out x in] row-major bytes, each an 8-bit float e4m3 in the "fn"
+ *   encoding (sign, 4 exponent bits with bias 7, 3 fraction bits; exponent 0
+ *   is subnormal, f * 2^-9; 0x7F and 0xFF are NaN; no infinities; largest
+ *   value 448).  scales: [out] float32.  The weight is
+ *   w[o][i] = e4m3(codes[o][i]) * scales[o].  Both arrays are device
+ *   pointers (16-byte aligned) owned by the caller.
+ * ---------------------------------------------------------------------- */
+typedef struct {
+    const uint8_t *codes;
+    const float *scales;
+} ffn_fp8_weight;
+
+ffn_status ffn_block_fp8_workspace_bytes(int64_t rows, int64_t d, int64_t ffn, size_t *bytes);
+
+/* ------------------------------------------------------------------------
+ * ffn_block_forward_fp8 -- the block with e4m3 weights ("How Megakernels
+ * Work", section "Projection shape changes the achieved rate": the decode
+ * projections are weight streams).
+ *   x [rows x d] bf16, g [d] bf16, y [rows x d] bf16; w_gate/w_up are e4m3
+ *   [ffn x d], w_down is e4m3 [d x ffn].  Needs d % 128 == 0 and
+ *   ffn % 128 == 0 (FFN_ERR_SHAPE otherwise).  Rows are processed in groups
+ *   of up to 16; each group streams the weights once.  Every code is exact in
+ *   fp16, so the MMAs multiply the codes themselves on fp16 operands
+ *   (activations as one fp16 rounding, h stored times 2^-8) and each output
+ *   is multiplied by its row scale once, in fp32.  flags: FFN_AUTO or
+ *   FFN_RESIDUAL.  Errors: FFN_ERR_NULL (a pointer missing),
+ *   FFN_ERR_FLAGS, FFN_ERR_SHAPE, FFN_ERR_WORKSPACE (workspace smaller than
+ *   ffn_block_fp8_workspace_bytes), FFN_ERR_ALIGN, FFN_ERR_ALIAS (y or the
+ *   workspace overlaps an input, or each other), FFN_ERR_CUDA (a launch
+ *   failed).  Nothing is launched on an error found on the host.
+ * ---------------------------------------------------------------------- */
+ffn_status ffn_block_forward_fp8(const void *x, const void *g, ffn_fp8_weight w_gate,
+                                 ffn_fp8_weight w_up, ffn_fp8_weight w_down, void *y, int64_t rows,
+                                 int64_t d, int64_t ffn, float eps, uint32_t flags, void *workspace,
+                                 size_t workspace_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
  * ffn_block_forward_decode_static -- the decode block (same kernels and
  * results as ffn_block_forward on its weight-streaming path) for callers that
  * cannot hand the library a workspace: runtimes that plan all device memory

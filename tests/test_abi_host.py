@@ -179,3 +179,29 @@ def test_residual_flag_accepted_by_the_planner(lib):
     assert lib.ffn_block_workspace_bytes(8, 4096, 11008, _lib.FFN_BF16,
                                          _lib.FFN_RESIDUAL | _lib.FFN_PREPARED_WEIGHTS, ctypes.byref(out)) == 0
     assert lib.ffn_block_workspace_bytes(8, 64, 64, _lib.FFN_F32, _lib.FFN_RESIDUAL, ctypes.byref(out)) == 0
+
+
+def test_fp8_entry_rejects_before_launch(lib):
+    out = ctypes.c_size_t(0)
+    assert lib.ffn_block_fp8_workspace_bytes(8, 4096, 14336, ctypes.byref(out)) == 0 and out.value > 0
+    assert lib.ffn_block_fp8_workspace_bytes(0, 4096, 14336, ctypes.byref(out)) == 0 and out.value == 0
+    for d, f in ((4160, 14336), (4096, 14400), (64, 128), (128, 64)):   # multiples of 128 only
+        assert lib.ffn_block_fp8_workspace_bytes(8, d, f, ctypes.byref(out)) == _lib.FFN_ERR_SHAPE
+    assert lib.ffn_block_fp8_workspace_bytes(-1, 128, 128, ctypes.byref(out)) == _lib.FFN_ERR_SHAPE
+    p = [ctypes.c_void_p((i + 1) << 24) for i in range(12)]
+    w = [_lib.Fp8Weight(p[2 + 2 * i].value, p[3 + 2 * i].value) for i in range(3)]
+    lib.ffn_block_fp8_workspace_bytes(8, 512, 1024, ctypes.byref(out))
+    need = out.value
+    # missing scale pointer, unknown flag, short workspace, misaligned codes, y aliasing the codes
+    bad = _lib.Fp8Weight(p[2].value, None)
+    assert lib.ffn_block_forward_fp8(p[0], p[1], bad, w[1], w[2], p[8], 8, 512, 1024, 1e-6, 0, p[9], need,
+                                     None) == _lib.FFN_ERR_NULL
+    assert lib.ffn_block_forward_fp8(p[0], p[1], *w, p[8], 8, 512, 1024, 1e-6, _lib.FFN_PATH_GEMM, p[9],
+                                     need, None) == _lib.FFN_ERR_FLAGS
+    assert lib.ffn_block_forward_fp8(p[0], p[1], *w, p[8], 8, 512, 1024, 1e-6, 0, p[9], need - 1,
+                                     None) == _lib.FFN_ERR_WORKSPACE
+    mis = _lib.Fp8Weight(p[2].value + 8, p[3].value)
+    assert lib.ffn_block_forward_fp8(p[0], p[1], mis, w[1], w[2], p[8], 8, 512, 1024, 1e-6, 0, p[9], need,
+                                     None) == _lib.FFN_ERR_ALIGN
+    assert lib.ffn_block_forward_fp8(p[0], p[1], *w, ctypes.c_void_p(p[4].value + 4096), 8, 512, 1024, 1e-6,
+                                     0, p[9], need, None) == _lib.FFN_ERR_ALIAS

@@ -33,6 +33,10 @@ class Q4Weight(ctypes.Structure):
     _fields_ = [("qs", c_void_p), ("scales", c_void_p)]
 
 
+class Fp8Weight(ctypes.Structure):
+    _fields_ = [("codes", c_void_p), ("scales", c_void_p)]
+
+
 # name -> (restype, argtypes), in the order of include/ffn.h
 SIGNATURES = {
     "ffn_rmsnorm": (c_int, [c_void_p, c_void_p, c_void_p, c_int64, c_int64, c_float, c_int, c_void_p]),
@@ -51,6 +55,10 @@ SIGNATURES = {
     "ffn_block_forward_q4": (c_int, [c_void_p, c_void_p, Q4Weight, Q4Weight, Q4Weight, c_void_p,
                                      c_int64, c_int64, c_int64, c_float, c_uint32, c_void_p,
                                      c_size_t, c_void_p]),
+    "ffn_block_fp8_workspace_bytes": (c_int, [c_int64, c_int64, c_int64, ctypes.POINTER(c_size_t)]),
+    "ffn_block_forward_fp8": (c_int, [c_void_p, c_void_p, Fp8Weight, Fp8Weight, Fp8Weight, c_void_p,
+                                      c_int64, c_int64, c_int64, c_float, c_uint32, c_void_p,
+                                      c_size_t, c_void_p]),
     "ffn_block_forward_decode_static": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                                 c_void_p, c_int64, c_int64, c_int64, c_float, c_int,
                                                 c_void_p]),

@@ -110,12 +110,14 @@ struct GemvWorkspace {
 size_t gemv_workspace_bytes(int64_t rows, int64_t d, int64_t ffn, bool two_terms);
 void gemv_carve(void *base, int64_t rows, int64_t d, int64_t ffn, bool two_terms, GemvWorkspace *ws);
 // wfmt: 0 f16, 1 bf16, 2 q4 (bf16 x/y, fp16 operands), 3 prepared fp16 weights
-// (bf16 x/y, fp16 operands)
-enum { WF_F16 = 0, WF_BF16 = 1, WF_Q4 = 2, WF_F16P = 3 };
+// (bf16 x/y, fp16 operands), 4 e4m3 weights with per-row scales (bf16 x/y,
+// fp16 operands)
+enum { WF_F16 = 0, WF_BF16 = 1, WF_Q4 = 2, WF_F16P = 3, WF_FP8 = 4 };
 struct GemvWeights {
-    const void *w;          // f16/bf16 [out x in]
+    const void *w;          // f16/bf16 [out x in]; e4m3 codes [out x in]
     const uint8_t *qs;      // q4 device layout
     const uint16_t *sc;     // q4 scales
+    const float *rs;        // e4m3: float scale of each output row [out]
 };
 cudaError_t launch_gemv_block(int wfmt, const void *x, const void *g, GemvWeights wg,
                               GemvWeights wu, GemvWeights wd, void *y, int64_t rows, int64_t d,

@@ -73,16 +73,16 @@ __global__ void __launch_bounds__(256) gemv_norm_frag_kernel(const void *x_, con
         for (int64_t v = v0 + threadIdx.x; v < v1; v += blockDim.x) {
             const int64_t k = 8 * v;
             if (q4) {
-                *reinterpret_cast<uint2 *>(nfrag + frag_elem(true, nch, token, k)) = make_uint2(0, 0);
-                *reinterpret_cast<uint2 *>(nfrag + frag_elem(true, nch, token, k + 4)) = make_uint2(0, 0);
+                *reinterpret_cast<uint2 *>(nfrag + frag_elem(FRAG_Q4, nch, token, k)) = make_uint2(0, 0);
+                *reinterpret_cast<uint2 *>(nfrag + frag_elem(FRAG_Q4, nch, token, k + 4)) = make_uint2(0, 0);
                 if (TWO) {
-                    *reinterpret_cast<uint2 *>(nlo + frag_elem(true, nch, token, k)) = make_uint2(0, 0);
-                    *reinterpret_cast<uint2 *>(nlo + frag_elem(true, nch, token, k + 4)) = make_uint2(0, 0);
+                    *reinterpret_cast<uint2 *>(nlo + frag_elem(FRAG_Q4, nch, token, k)) = make_uint2(0, 0);
+                    *reinterpret_cast<uint2 *>(nlo + frag_elem(FRAG_Q4, nch, token, k + 4)) = make_uint2(0, 0);
                 }
             } else {
-                *reinterpret_cast<uint4 *>(nfrag + frag_elem(false, nch, token, k)) = make_uint4(0, 0, 0, 0);
+                *reinterpret_cast<uint4 *>(nfrag + frag_elem(frag_order<WF>(), nch, token, k)) = make_uint4(0, 0, 0, 0);
                 if (TWO)
-                    *reinterpret_cast<uint4 *>(nlo + frag_elem(false, nch, token, k)) = make_uint4(0, 0, 0, 0);
+                    *reinterpret_cast<uint4 *>(nlo + frag_elem(frag_order<WF>(), nch, token, k)) = make_uint4(0, 0, 0, 0);
             }
         }
         return;
@@ -132,12 +132,12 @@ __global__ void __launch_bounds__(256) gemv_norm_frag_kernel(const void *x_, con
                     o[e] = from_f32<TO>(f[4 * run + src[e]]);
                     ol[e] = from_f32<TO>(r[4 * run + src[e]]);
                 }
-                const int64_t base = frag_elem(true, nch, token, k + 4 * run);
+                const int64_t base = frag_elem(FRAG_Q4, nch, token, k + 4 * run);
                 *reinterpret_cast<uint2 *>(nfrag + base) = *reinterpret_cast<const uint2 *>(o);
                 if (TWO) *reinterpret_cast<uint2 *>(nlo + base) = *reinterpret_cast<const uint2 *>(ol);
             }
         } else {
-            const int64_t base = frag_elem(false, nch, token, k);
+            const int64_t base = frag_elem(frag_order<WF>(), nch, token, k);
             *reinterpret_cast<uint4 *>(nfrag + base) = Vec16<TO>::pack(f);
             if (TWO) *reinterpret_cast<uint4 *>(nlo + base) = Vec16<TO>::pack(r);
         }
@@ -338,7 +338,7 @@ __global__ void __launch_bounds__(256) gemv_gateup_kernel(
             constexpr float ws = Fmt<WF>::w_unscale;
             const float hv = silu_f32(acc[0][n][i] * ws) * (acc[1][n][i] * ws) * Fmt<WF>::h_scale;
             const TO t = from_f32<TO>(hv);
-            const int64_t at = frag_elem(q4, nchF, token, feat);
+            const int64_t at = frag_elem(frag_order<WF>(), nchF, token, feat);
             hfrag[at] = *reinterpret_cast<const uint16_t *>(&t);
             if (TWO) {
                 const TO tl = from_f32<TO>(hv - to_f32(t));
@@ -461,20 +461,22 @@ cudaError_t launch_typed(const void *x, const void *gain, GemvWeights wg, GemvWe
         return launch_stream_down<WF, NT, TWO>(wd, ws.hfrag, ws.hfrag_lo, y, ws.partials, ws.counters, rows, d,
                                                ffn, geo.nchF, stream_down_splits(WF, d, ffn), res, s);
     }
-    {
-        const int64_t tiles = 2 * geo.nchF;  // covers every fragment slot of h
-        const int64_t blocks = cdiv(tiles, kGuTPC);
-        const int64_t units = q4 ? d / 128 : geo.nchK;
-        LaunchScope scope(K_GEMV_GATEUP, s);
-        gemv_gateup_kernel<WF, NT, TWO><<<static_cast<unsigned>(blocks), 32 * kGuTPC * kGuKS, 0, s>>>(
-            q4 ? static_cast<const void *>(wg.qs) : wg.w, q4 ? static_cast<const void *>(wu.qs) : wu.w,
-            wg.sc, wu.sc, static_cast<const uint4 *>(ws.nfrag), static_cast<const uint4 *>(ws.nfrag_lo),
-            static_cast<uint16_t *>(ws.hfrag), static_cast<uint16_t *>(ws.hfrag_lo), d, ffn, geo.nchK,
-            geo.nchF, units, ws.counters, static_cast<int>(geo.groups));
-        cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-    }
-    {
+    if constexpr (WF == WF_FP8) {
+        return cudaErrorInvalidValue;   // e4m3 weights stream through the TMA kernels only
+    } else {
+        {
+            const int64_t tiles = 2 * geo.nchF;  // covers every fragment slot of h
+            const int64_t blocks = cdiv(tiles, kGuTPC);
+            const int64_t units = q4 ? d / 128 : geo.nchK;
+            LaunchScope scope(K_GEMV_GATEUP, s);
+            gemv_gateup_kernel<WF, NT, TWO><<<static_cast<unsigned>(blocks), 32 * kGuTPC * kGuKS, 0, s>>>(
+                q4 ? static_cast<const void *>(wg.qs) : wg.w, q4 ? static_cast<const void *>(wu.qs) : wu.w,
+                wg.sc, wu.sc, static_cast<const uint4 *>(ws.nfrag), static_cast<const uint4 *>(ws.nfrag_lo),
+                static_cast<uint16_t *>(ws.hfrag), static_cast<uint16_t *>(ws.hfrag_lo), d, ffn, geo.nchK,
+                geo.nchF, units, ws.counters, static_cast<int>(geo.groups));
+            cudaError_t e = cudaGetLastError();
+            if (e != cudaSuccess) return e;
+        }
         dim3 grid(static_cast<unsigned>(geo.groups), static_cast<unsigned>(geo.splits));
         LaunchScope scope(K_GEMV_DOWN, s);
         gemv_down_kernel<WF, NT, TWO><<<grid, 32 * kDnTPC, 0, s>>>(
@@ -503,7 +505,7 @@ Layout layout(int64_t rows, int64_t d, int64_t ffn) {
     const Geometry a = geometry(rows, d, ffn, false);
     const Geometry b = geometry(rows, d, ffn, (d % 128 == 0) && (ffn % 128 == 0));
     int64_t splits = a.splits > b.splits ? a.splits : b.splits;
-    for (int wf : {WF_BF16, WF_Q4})
+    for (int wf : {WF_BF16, WF_Q4, WF_FP8})
         if (stream_supported(wf, d, ffn)) splits = std::max(splits, stream_down_splits(wf, d, ffn));
     Layout l;
     l.frag_n = align256(static_cast<size_t>(a.nt) * a.nchK * 32 * 16);
@@ -558,6 +560,8 @@ cudaError_t launch_gemv_block(int wfmt, const void *x, const void *g, GemvWeight
                        : launch_nt<WF_BF16, false>(geo.nt, x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s, res);
         case WF_Q4:   // fp16 operands: one term is enough
             return launch_nt<WF_Q4, false>(geo.nt, x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s, res);
+        case WF_FP8:  // fp16 operands, as for Q4
+            return launch_nt<WF_FP8, false>(geo.nt, x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s, res);
         default:      // prepared fp16 weights
             return launch_nt<WF_F16P, false>(geo.nt, x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s, res);
     }

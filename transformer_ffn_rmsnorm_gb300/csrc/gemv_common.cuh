@@ -12,23 +12,41 @@ __host__ __device__ inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 
 
 // Fragment order of an activation vector of length K for one token:
 //   16-bit element index = ((nt * nch + c) * 32 + lane) * 8 + slot
-//   lane = 4 * (token % 8) + tid, nt = token / 8, c = k / 32.
-// Natural order (f16/bf16 weights): k % 32 = 8 * tid + slot.
-// Q4 order: position p = k % 32, hi = p / 16, q = p % 16, tid = q / 4,
-//   slot = 4 * hi + perm[q % 4] with perm = {0, 2, 1, 3}; this matches the
-//   nibble unpacking in dequant_word below.
-__device__ __forceinline__ int64_t frag_elem(bool q4, int64_t nch, int token, int64_t k) {
-    const int64_t c = k / kChunk;
-    const int p = static_cast<int>(k % kChunk);
+//   lane = 4 * (token % 8) + tid, nt = token / 8.
+// Natural order (f16/bf16 weights): c = k / 32, k % 32 = 8 * tid + slot.
+// Q4 order: c = k / 32; position p = k % 32, hi = p / 16, q = p % 16,
+//   tid = q / 4, slot = 4 * hi + perm[q % 4] with perm = {0, 2, 1, 3}; this
+//   matches the nibble unpacking in dequant_word below.
+// e4m3 order: groups of 64 k, one group = two chunks; position p = k % 64,
+//   tid = p / 16, j = p % 16, c = 2 * (k / 64) + j / 8, slot = j % 8.  A
+//   lane reads 16 consecutive weight bytes of a row (k = 16 tid .. 16 tid +
+//   15 of the group) and feeds four MMAs with them, four k each; its B
+//   values for those MMAs are these 16 k in order, split over the group's
+//   two chunks.
+enum { FRAG_NATURAL = 0, FRAG_Q4 = 1, FRAG_FP8 = 2 };
+template <int WF> __host__ __device__ constexpr int frag_order() {
+    return WF == WF_Q4 ? FRAG_Q4 : WF == WF_FP8 ? FRAG_FP8 : FRAG_NATURAL;
+}
+__device__ __forceinline__ int64_t frag_elem(int order, int64_t nch, int token, int64_t k) {
+    int64_t c;
     int tid, slot;
-    if (q4) {
-        const int hi = p >> 4, q = p & 15;
-        tid = q >> 2;
-        const int e = q & 3;
-        slot = 4 * hi + ((e == 1) ? 2 : (e == 2) ? 1 : e);
+    if (order == FRAG_FP8) {
+        const int p = static_cast<int>(k & 63), j = p & 15;
+        tid = p >> 4;
+        c = 2 * (k >> 6) + (j >> 3);
+        slot = j & 7;
     } else {
-        tid = p >> 3;
-        slot = p & 7;
+        c = k / kChunk;
+        const int p = static_cast<int>(k % kChunk);
+        if (order == FRAG_Q4) {
+            const int hi = p >> 4, q = p & 15;
+            tid = q >> 2;
+            const int e = q & 3;
+            slot = 4 * hi + ((e == 1) ? 2 : (e == 2) ? 1 : e);
+        } else {
+            tid = p >> 3;
+            slot = p & 7;
+        }
     }
     const int lane = 4 * (token & 7) + tid;
     return (((token >> 3) * nch + c) * 32 + lane) * 8 + slot;
@@ -62,6 +80,14 @@ template <> struct Fmt<WF_F16P> {
     static constexpr bool op_bf16 = false;
     static constexpr float w_unscale = 1.f / kPreparedScale, h_scale = 1.f / 256.f;
 };
+// e4m3 weights: every code is exact in fp16 (3 fraction bits, exponents
+// 2^-9 .. 2^8), so the MMA multiplies the codes themselves and the row scale
+// multiplies each output once; activations as for Q4.
+template <> struct Fmt<WF_FP8> {
+    using TIn = __nv_bfloat16; using TOp = __half;
+    static constexpr bool op_bf16 = false;
+    static constexpr float w_unscale = 1.f, h_scale = 1.f / 256.f;
+};
 
 // Q4: one 32-bit word = canonical bytes 4*tid .. 4*tid+3 of a block.
 // Returns (u - 8) as fp16 pairs:
@@ -91,6 +117,14 @@ __device__ __forceinline__ void dequant_word(uint32_t w, uint32_t (&r)[4]) {
         b = (i & 1) ? __hfma2(b, k16th, k72) : __hsub2(b, k1032);
         r[i] = *reinterpret_cast<uint32_t *>(&b);
     }
+}
+
+// Two e4m3 codes (the low byte is the first) as an fp16 pair, exactly.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
+    uint32_t r;
+    const uint16_t v = static_cast<uint16_t>(two_codes);
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
+    return r;
 }
 
 __device__ __forceinline__ uint32_t word_of(const uint4 &v, int b) {

@@ -7,8 +7,8 @@
 // the long scoreboard, 1.6-4.4 TB/s).  Here one producer thread per CTA keeps
 // a 6-stage shared-memory ring full with TMA bulk tensor copies of 64 weight
 // rows x one k-block (16-bit: 64 values, 128 bytes a row; Q4: 256 values,
-// 128 bytes of nibbles plus 16 bytes of fp16 scales a row), 128-byte
-// swizzled, plus -- by 1-D bulk copies -- the pre-arranged activation
+// 128 bytes of nibbles plus 16 bytes of fp16 scales a row; e4m3: 128 codes,
+// 128 bytes a row), 128-byte swizzled, plus -- by 1-D bulk copies -- the pre-arranged activation
 // fragments of the same k range, while four MMA warps read everything from
 // shared memory.  (Reading the activations through L1 instead stalls: the
 // rings leave too little L1 to hold them.)
@@ -42,12 +42,15 @@ constexpr uint32_t kFragBytes = 32 * 16;   // one 32-value chunk of fragments fo
 enum { ROLE_GATEUP = 0, ROLE_DOWN = 1 };
 
 // Stage layout: [weights of each matrix][their scales (Q4)][activation
-// fragments: NT tiles x terms x chunks x 512 B].
+// fragments: NT tiles x terms x chunks x 512 B].  Every format moves 128
+// bytes of each weight row per stage.
 template <int WF, int ROLE, int NT, bool TWO> struct Tile {
     static constexpr bool q4 = WF == WF_Q4;
+    static constexpr bool fp8 = WF == WF_FP8;
     static constexpr int nmat = ROLE == ROLE_GATEUP ? 2 : 1;     // weight matrices per stage
     static constexpr int box_rows = ROLE == ROLE_GATEUP ? 32 : 64;
-    static constexpr int kb = q4 ? 256 : 64;                     // k values per stage
+    static constexpr int kb = q4 ? 256 : fp8 ? 128 : 64;         // k values per stage
+    static constexpr int x_per_kb = (q4 || fp8) ? 128 : 64;      // TMA inner coordinate per stage
     static constexpr int chunks = kb / kChunk;                   // fragment chunks per stage
     static constexpr int terms = TWO ? 2 : 1;
     static constexpr uint32_t w_bytes = box_rows * 128;          // one matrix' rows x 128 B
@@ -77,6 +80,7 @@ struct StreamParams {
     int64_t D;              // down: output features
     unsigned *err;
     const void *res;        // down: added to y before its rounding ([rows x D] of y's type), or null
+    const float *rs0, *rs1; // e4m3: row scales of the weight matrices (gate and up, or down)
 };
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
@@ -98,6 +102,7 @@ __global__ void __launch_bounds__(kThreads) gemv_stream_kernel(
     using TO = typename Fmt<WF>::TOp;
     constexpr bool bf = Fmt<WF>::op_bf16;
     constexpr bool q4 = TL::q4;
+    constexpr bool fp8 = TL::fp8;
     constexpr int kStages = TL::stages;
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bar_full[kStages], bar_empty[kStages];
@@ -147,7 +152,7 @@ __global__ void __launch_bounds__(kThreads) gemv_stream_kernel(
             };
             auto load_weights = [&](int64_t i, int64_t kb) {
                 const uint32_t st = stage_of(i), bar = full(static_cast<int>(i % kStages));
-                const int x = static_cast<int>(kb * (q4 ? 128 : 64));   // bytes of nibbles / elements
+                const int x = static_cast<int>(kb * TL::x_per_kb);   // bytes of nibbles or codes / elements
                 const int y = static_cast<int>(row0);
                 ptx::tma_load_2d(st, &map_w0, bar, x, y);
                 if (TL::nmat == 2) ptx::tma_load_2d(st + TL::w_bytes, &map_w1, bar, x, y);
@@ -221,7 +226,36 @@ __global__ void __launch_bounds__(kThreads) gemv_stream_kernel(
                 break;
             }
             const uint32_t wbase = base + s * TL::stage_bytes + mat * TL::w_bytes;
-            if constexpr (!q4) {
+            if constexpr (fp8) {
+                // 128 k = two groups of 64; in each, this lane's 16 codes of
+                // rows ra and rb (k = 16 tid .. 16 tid + 15) feed four MMAs,
+                // four k each, against the group's two fragment chunks
+                const uint32_t bbase = base + s * TL::stage_bytes + TL::b_off + lane * 16;
+#pragma unroll
+                for (int grp = 0; grp < 2; ++grp) {
+                    uint4 b0[NT], b1[NT];
+#pragma unroll
+                    for (int n = 0; n < NT; ++n) {
+                        b0[n] = lds128(bbase + (n * TL::chunks + 2 * grp) * kFragBytes);
+                        b1[n] = lds128(bbase + (n * TL::chunks + 2 * grp + 1) * kFragBytes);
+                    }
+                    const uint32_t off = static_cast<uint32_t>(((4 * grp + tid) ^ g) << 4);
+                    const uint4 qa = lds128(wbase + ra * 128 + off);
+                    const uint4 qb = lds128(wbase + rb * 128 + off);
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) {
+                        const uint32_t wa = word_of(qa, m), wb = word_of(qb, m);
+                        const uint32_t a0 = e4m3x2_to_f16x2(wa), a2 = e4m3x2_to_f16x2(wa >> 16);
+                        const uint32_t a1 = e4m3x2_to_f16x2(wb), a3 = e4m3x2_to_f16x2(wb >> 16);
+#pragma unroll
+                        for (int n = 0; n < NT; ++n) {
+                            const uint4 &bv = m < 2 ? b0[n] : b1[n];
+                            const uint32_t x0 = (m & 1) ? bv.z : bv.x, x1 = (m & 1) ? bv.w : bv.y;
+                            ptx::mma_16816<bf>(acc[n], a0, a1, a2, a3, x0, x1);
+                        }
+                    }
+                }
+            } else if constexpr (!q4) {
                 // two 32-wide chunks: this lane's 16 bytes of rows ra, rb at chunk 4j + tid
                 const uint32_t bbase = base + s * TL::stage_bytes + TL::b_off + lane * 16;
 #pragma unroll
@@ -316,16 +350,25 @@ __global__ void __launch_bounds__(kThreads) gemv_stream_kernel(
             consumer_sync();
             if (warp < 2) {
                 constexpr float ws = Fmt<WF>::w_unscale;
+                float rsg[2] = {ws, ws}, rsu[2] = {ws, ws};   // weight scales of rows ra and rb
+                if constexpr (fp8) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int64_t feat = row0 + r0 + g + 8 * h;
+                        rsg[h] = feat < p.rows_w ? p.rs0[feat] : 0.f;
+                        rsu[h] = feat < p.rows_w ? p.rs1[feat] : 0.f;
+                    }
+                }
 #pragma unroll
                 for (int n = 0; n < NT; ++n)
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         const int64_t feat = row0 + r0 + g + 8 * (i >> 1);
                         const int token = 8 * n + 2 * tid + (i & 1);
-                        const float hv = silu_f32(acc[n][i] * ws) * (red[warp][lane][n * 4 + i] * ws) *
-                                         Fmt<WF>::h_scale;
+                        const float hv = silu_f32(acc[n][i] * rsg[i >> 1]) *
+                                         (red[warp][lane][n * 4 + i] * rsu[i >> 1]) * Fmt<WF>::h_scale;
                         const TO t = from_f32<TO>(hv);
-                        const int64_t at = frag_elem(q4, p.nch_h, token, feat);
+                        const int64_t at = frag_elem(frag_order<WF>(), p.nch_h, token, feat);
                         p.hfrag[at] = *reinterpret_cast<const uint16_t *>(&t);
                         if (TWO) {
                             const TO tl = from_f32<TO>(hv - to_f32(t));
@@ -361,7 +404,7 @@ __global__ void __launch_bounds__(kThreads) gemv_stream_kernel(
                     float sum = 0.f;
                     for (int sp = 0; sp < nsplit; ++sp)
                         sum += __ldcg(p.partials + (static_cast<int64_t>(sp) * p.rows + token) * p.D + feat);
-                    float v = sum * out_scale;
+                    float v = fp8 ? (sum * p.rs0[feat]) * out_scale : sum * out_scale;
                     if (p.res) v += to_f32(static_cast<const T *>(p.res)[static_cast<int64_t>(token) * p.D + feat]);
                     y[static_cast<int64_t>(token) * p.D + feat] = from_f32<T>(v);
                 }
@@ -393,6 +436,10 @@ bool map_rows(CUtensorMap *m, const void *ptr, CUtensorMapDataType dt, int64_t i
 template <int WF, int ROLE>
 bool weight_maps(CUtensorMap *w, CUtensorMap *sc, const GemvWeights &wt, int64_t rows, int64_t K) {
     using TL = Tile<WF, ROLE, 1, false>;
+    if (TL::fp8) {
+        *sc = CUtensorMap{};
+        return map_rows(w, wt.w, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, rows, K, 128, TL::box_rows, true);
+    }
     if (TL::q4) {
         if (!map_rows(w, wt.qs, CU_TENSOR_MAP_DATA_TYPE_UINT8, K / 2, rows, K / 2, 128, TL::box_rows, true))
             return false;
@@ -422,6 +469,7 @@ cudaError_t set_smem(size_t bytes) {
 
 bool stream_supported(int wfmt, int64_t d, int64_t ffn) {
     if (wfmt == WF_Q4) return d % 256 == 0 && ffn % 256 == 0;
+    if (wfmt == WF_FP8) return d % 128 == 0 && ffn % 128 == 0;
     return d % 8 == 0 && ffn % 8 == 0;
 }
 
@@ -452,6 +500,8 @@ cudaError_t launch_stream_gateup(GemvWeights wg, GemvWeights wu, const void *nfr
     p.err = device_status_word();
     if (!p.err) return cudaErrorUnknown;
     p.res = nullptr;
+    p.rs0 = wg.rs;
+    p.rs1 = wu.rs;
     // 32 features per CTA; covering nchF * 32 features writes every slot of h
     const int64_t blocks = nchF;
     LaunchScope scope(K_GEMV_GATEUP, s);
@@ -485,6 +535,8 @@ cudaError_t launch_stream_down(GemvWeights wd, const void *hfrag, const void *hf
     p.rows = rows;
     p.D = d;
     p.res = res;
+    p.rs0 = wd.rs;
+    p.rs1 = nullptr;
     p.err = device_status_word();
     if (!p.err) return cudaErrorUnknown;
     const int64_t nsplit = cdiv(p.nkb, p.kb_per_split);
@@ -500,7 +552,7 @@ cudaError_t launch_stream_down(GemvWeights wd, const void *hfrag, const void *hf
 // with launches.
 int64_t stream_down_splits(int wfmt, int64_t d, int64_t ffn) {
     const int64_t groups = cdiv(d, 64);
-    const int64_t kb = wfmt == WF_Q4 ? 256 : 64;
+    const int64_t kb = wfmt == WF_Q4 ? 256 : wfmt == WF_FP8 ? 128 : 64;
     const int64_t nkb = cdiv(ffn, kb);
     int64_t splits = 600 / groups;
     if (splits < 1) splits = 1;
@@ -528,6 +580,8 @@ FFN_STREAM_INSTANTIATE(WF_Q4, 1, false)
 FFN_STREAM_INSTANTIATE(WF_Q4, 2, false)
 FFN_STREAM_INSTANTIATE(WF_F16P, 1, false)
 FFN_STREAM_INSTANTIATE(WF_F16P, 2, false)
+FFN_STREAM_INSTANTIATE(WF_FP8, 1, false)
+FFN_STREAM_INSTANTIATE(WF_FP8, 2, false)
 #undef FFN_STREAM_INSTANTIATE
 
 }  // namespace gemv

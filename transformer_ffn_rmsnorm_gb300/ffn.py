@@ -17,7 +17,7 @@ import torch
 from . import _lib
 from ._lib import (FFN_AUTO, FFN_BF16, FFN_F16, FFN_F32, FFN_GATEUP_FUSED,  # noqa: F401
                    FFN_GATEUP_UNFUSED, FFN_ACT_SINGLE, FFN_ACT_SPLIT, FFN_PATH_GEMM,
-                   FFN_PATH_GEMV, FFN_PREPARED_WEIGHTS, FFN_RESIDUAL, Q4Weight)
+                   FFN_PATH_GEMV, FFN_PREPARED_WEIGHTS, FFN_RESIDUAL, Fp8Weight, Q4Weight)
 
 _DT = {torch.float32: FFN_F32, torch.float16: FFN_F16, torch.bfloat16: FFN_BF16}
 
@@ -171,6 +171,38 @@ def ffn_block_forward_q4(x, g, w_gate, w_up, w_down, ffn: int, eps: float, flags
     _check(_lib.load().ffn_block_forward_q4(_ptr(x), _ptr(g), _q4(w_gate), _q4(w_up), _q4(w_down),
                                             _ptr(y), rows, d, ffn, float(eps), flags, _ptr(ws),
                                             ws.numel(), _stream(stream)), "ffn_block_forward_q4")
+    return y
+
+
+def ffn_block_fp8_workspace_bytes(rows: int, d: int, ffn: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check(_lib.load().ffn_block_fp8_workspace_bytes(rows, d, ffn, ctypes.byref(out)),
+           "ffn_block_fp8_workspace_bytes")
+    return out.value
+
+
+def _fp8(w):
+    codes, sc = w
+    _need_cuda(codes, sc)
+    if codes.element_size() != 1 or sc.dtype != torch.float32:
+        raise TypeError("e4m3 weights are (1-byte codes, float32 row scales)")
+    return Fp8Weight(codes.data_ptr(), sc.data_ptr())
+
+
+def ffn_block_forward_fp8(x, g, w_gate, w_up, w_down, eps: float, flags: int = 0,
+                          out=None, ws: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """``w_*`` are (codes, scales) CUDA tensor pairs: e4m3 codes [out, in]
+    (uint8 or torch.float8_e4m3fn) and float32 row scales [out]."""
+    _need_cuda(x, g, out, ws)
+    d = x.shape[-1]
+    rows = x.numel() // d
+    ffn = w_gate[0].shape[0]
+    y = torch.empty_like(x) if out is None else out
+    if ws is None:
+        ws = workspace(ffn_block_fp8_workspace_bytes(rows, d, ffn), x.device)
+    _check(_lib.load().ffn_block_forward_fp8(_ptr(x), _ptr(g), _fp8(w_gate), _fp8(w_up), _fp8(w_down),
+                                             _ptr(y), rows, d, ffn, float(eps), flags, _ptr(ws),
+                                             ws.numel(), _stream(stream)), "ffn_block_forward_fp8")
     return y
 
 
