@@ -397,16 +397,45 @@ __global__ void __launch_bounds__(kThreads) gemv_stream_kernel(
             if (s_last) {
                 __threadfence();
                 T *y = static_cast<T *>(p.y);
-                for (int i = threadIdx.x; i < p.rows * 64; i += 32 * kConsumers) {
-                    const int token = i / 64;
-                    const int64_t feat = row0 + i % 64;
-                    if (feat >= p.D) continue;
-                    float sum = 0.f;
-                    for (int sp = 0; sp < nsplit; ++sp)
-                        sum += __ldcg(p.partials + (static_cast<int64_t>(sp) * p.rows + token) * p.D + feat);
-                    float v = fp8 ? (sum * p.rs0[feat]) * out_scale : sum * out_scale;
-                    if (p.res) v += to_f32(static_cast<const T *>(p.res)[static_cast<int64_t>(token) * p.D + feat]);
-                    y[static_cast<int64_t>(token) * p.D + feat] = from_f32<T>(v);
+                // four outputs a thread at a time, their partials four splits at a
+                // time (16 loads in flight), each output summed in split order
+                constexpr int kStep = 32 * kConsumers;
+                const int nout = p.rows * 64;
+                const int64_t stride = static_cast<int64_t>(p.rows) * p.D;
+                for (int i0 = threadIdx.x; i0 < nout; i0 += 4 * kStep) {
+                    bool live[4];
+                    const float *src[4];
+                    float sum[4];
+#pragma unroll
+                    for (int o = 0; o < 4; ++o) {
+                        const int i = i0 + o * kStep;
+                        const int64_t feat = row0 + i % 64;
+                        live[o] = i < nout && feat < p.D;
+                        src[o] = p.partials + static_cast<int64_t>(i / 64) * p.D + feat;
+                        sum[o] = 0.f;
+                    }
+                    for (int sp0 = 0; sp0 < nsplit; sp0 += 4) {
+                        float v[4][4];
+#pragma unroll
+                        for (int o = 0; o < 4; ++o)
+#pragma unroll
+                            for (int q = 0; q < 4; ++q)
+                                v[o][q] = (live[o] && sp0 + q < nsplit) ? __ldcg(src[o] + (sp0 + q) * stride) : 0.f;
+#pragma unroll
+                        for (int o = 0; o < 4; ++o)
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) sum[o] += v[o][q];
+                    }
+#pragma unroll
+                    for (int o = 0; o < 4; ++o) {
+                        if (!live[o]) continue;
+                        const int i = i0 + o * kStep;
+                        const int token = i / 64;
+                        const int64_t feat = row0 + i % 64;
+                        float v = fp8 ? (sum[o] * p.rs0[feat]) * out_scale : sum[o] * out_scale;
+                        if (p.res) v += to_f32(static_cast<const T *>(p.res)[static_cast<int64_t>(token) * p.D + feat]);
+                        y[static_cast<int64_t>(token) * p.D + feat] = from_f32<T>(v);
+                    }
                 }
                 if (threadIdx.x == 0) p.counters[blockIdx.x] = 0u;
             }
