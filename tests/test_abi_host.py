@@ -155,7 +155,7 @@ def test_host_block_entry_rejects_before_launch(lib):
     assert lib.ffn_block_host_workspace_bytes(4096, 4096, 11008, _lib.FFN_BF16, 0, ctypes.byref(out)) == 0
     staged = 2 * 4096 * 4096 * 2
     blk = ctypes.c_size_t(0)
-    assert lib.ffn_block_workspace_bytes(1536, 4096, 11008, _lib.FFN_BF16, 0, ctypes.byref(blk)) == 0
+    assert lib.ffn_block_workspace_bytes(1024, 4096, 11008, _lib.FFN_BF16, 0, ctypes.byref(blk)) == 0
     assert out.value >= staged + blk.value
     assert lib.ffn_block_host_workspace_bytes(8, 4100, 11008, _lib.FFN_BF16, 0,
                                               ctypes.byref(out)) == _lib.FFN_ERR_SHAPE

@@ -27,7 +27,7 @@ def host_bf16(a):
 @pytest.mark.parametrize("rows", [8, 300, 3500])
 @pytest.mark.parametrize("prepared", [False, True])
 def test_host_block_matches_device_block(ffn, oracle_lib, rows, prepared):
-    """3500 rows: three chunks (1536, 1536, 428) through the tensor-core path."""
+    """3500 rows: four chunks (1024, 1024, 1024, 428) through the tensor-core path."""
     import torch
     inp = synth.make_block_inputs(synth.C4_PREFILL_BF16, seed=rows, rows=rows, d=256, ffn=384)
     g = to_dev(inp["g"], "bf16")
@@ -45,14 +45,14 @@ def test_host_block_matches_device_block(ffn, oracle_lib, rows, prepared):
 
 
 def test_host_block_short_last_chunk(ffn, oracle_lib):
-    """3082 rows: chunks of 1536, 1536 and 10, the last on the decode path."""
+    """3082 rows: chunks of 1024, 1024, 1024 and 10, the last on the decode path."""
     import torch
     inp = synth.make_block_inputs(synth.C4_PREFILL_BF16, seed=9, rows=3082, d=512, ffn=704)
     args = [to_dev(inp[k], "bf16") for k in ("g", "w_gate", "w_up", "w_down")]
     y = ffn.ffn_block_forward_host(host_bf16(inp["x"]), *args, eps=inp["cfg"].eps)
     torch.cuda.current_stream().synchronize()
     got = to_host64(y)
-    rows = np.r_[0:40, 1530:1545, 3060:3082]
+    rows = np.r_[0:40, 1015:1035, 2040:2055, 3060:3082]
     ref = oracle_lib.block_from_inputs(inp, rows=rows)
     assert_lowp(got[rows], ref)
     ffn.ffn_device_status()

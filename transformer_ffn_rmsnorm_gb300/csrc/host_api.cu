@@ -9,9 +9,15 @@
 // last copy, so synchronising that stream means y is in host memory.  Only
 // the first chunk's input copy and the last chunk's output copy are exposed.
 //
-// Chunks are 1536 rows for batches above 2048 rows: 6 pairs of 128-row
-// blocks, whose 516 gate/up tile pairs (ffn 11008) fill 6.8 of 7 waves on 76
-// CTA pairs (97 %), against 90 % for 1024 or 2048 rows.
+// Chunks are 1024 rows for batches above 1024 rows.  On the host link of a
+// GB300 (about 200 GB/s each way for page-locked memory) the exposed copies
+// are the first chunk's input and the last chunk's output, so chunks should
+// be short; but each chunk's GEMMs run in whole waves of 76 CTA pairs.  At
+// 1024 rows (4 pairs of 128-row blocks) the down projection of d = 4096 is
+// exactly one wave (4 x 19 tiles of 224 columns) and gate/up (ffn 11008, 4 x
+// 86 tile pairs) fills 4.5 of 5 waves; 1536-row chunks fill gate/up better
+// (6.8 of 7) but leave the down projection's second wave half empty, and
+// cost 50 % more exposed copy time.
 #include <cstring>
 #include <mutex>
 
@@ -31,12 +37,12 @@ struct Chunks {
 
 Chunks plan_chunks(int64_t rows) {
     Chunks c;
-    if (rows <= 2048) {
+    if (rows <= 1024) {
         c.rows = rows;
         c.count = rows > 0 ? 1 : 0;
         return c;
     }
-    c.rows = 1536;
+    c.rows = 1024;
     if ((rows + c.rows - 1) / c.rows > kMaxChunks) c.rows = ((rows + kMaxChunks - 1) / kMaxChunks + 255) / 256 * 256;
     c.count = static_cast<int>((rows + c.rows - 1) / c.rows);
     return c;
