@@ -282,6 +282,27 @@ ffn_status ffn_block_forward_decode_static(const void *x, const void *g, const v
 ffn_status ffn_prepare_weights(const void *src, void *dst, int64_t count, ffn_dtype src_dtype,
                                void *stream);
 
+/* ------------------------------------------------------------------------
+ * ffn_prepare_weights_fp8 / ffn_prepare_weights_q4 -- the same prepared form
+ * (fp16 values of w * 2^8, [out x in] row-major) from quantised weights, for
+ * many-row batches: ffn_block_forward_fp8 and ffn_block_forward_q4 stream the
+ * whole quantised weight set once per group of 16 rows, the fast path for a
+ * prefill batch is to prepare once and call ffn_block_forward with
+ * FFN_PREPARED_WEIGHTS (tensor-core GEMMs).  No page describes the step.
+ *   fp8: w = e4m3(codes[o][i]) * scales[o]; in % 16 == 0.  The product times
+ *   2^8 is rounded to fp16 once (round to nearest even), i.e. to 11
+ *   significant bits of the exact w.
+ *   Q4: w = (u - 8) * s in the device layout above; in % 128 == 0.  Exact
+ *   before the one rounding to fp16 as well.
+ *   dst: out * in device fp16 values, 16-byte aligned, overlapping neither
+ *   input (FFN_ERR_ALIAS).  Values whose |w| * 2^8 exceeds fp16's range
+ *   become infinite and record FFN_ERR_RANGE in the device status word.
+ *   FFN_ERR_NULL, FFN_ERR_SHAPE, FFN_ERR_ALIGN are found before any launch;
+ *   out == 0 or in == 0 launches nothing.
+ * ---------------------------------------------------------------------- */
+ffn_status ffn_prepare_weights_fp8(ffn_fp8_weight w, void *dst, int64_t out, int64_t in, void *stream);
+ffn_status ffn_prepare_weights_q4(ffn_q4_weight w, void *dst, int64_t out, int64_t in, void *stream);
+
 /* Host helper (not on the hot path): pack int8 q [out x in] (values -8..7) and
  * fp16 scale bits [out x in/32] into the device layout above.  Host pointers;
  * qs_out holds out*in/2 bytes, scales_out out*in/32 entries.  in % 128 == 0. */

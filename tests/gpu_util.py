@@ -59,3 +59,9 @@ def q4_dev(inp: dict, name: str):
     import torch
     return (torch.from_numpy(inp["qs_" + name]).cuda(),
             torch.from_numpy(inp["sc_" + name].view(np.int16)).cuda())
+
+
+def fp8_dev(inp: dict, name: str):
+    import torch
+    return (torch.from_numpy(np.ascontiguousarray(inp["c_" + name])).cuda(),
+            torch.from_numpy(np.ascontiguousarray(inp["s_" + name])).cuda())

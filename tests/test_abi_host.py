@@ -205,3 +205,16 @@ def test_fp8_entry_rejects_before_launch(lib):
                                      None) == _lib.FFN_ERR_ALIGN
     assert lib.ffn_block_forward_fp8(p[0], p[1], *w, ctypes.c_void_p(p[4].value + 4096), 8, 512, 1024, 1e-6,
                                      0, p[9], need, None) == _lib.FFN_ERR_ALIAS
+
+
+def test_quantised_prepare_rejects_before_launch(lib):
+    p = [ctypes.c_void_p((i + 1) << 24) for i in range(6)]
+    f = _lib.Fp8Weight(p[0].value, p[1].value)
+    q = _lib.Q4Weight(p[0].value, p[1].value)
+    assert lib.ffn_prepare_weights_fp8(f, p[2], 4, 24, None) == _lib.FFN_ERR_SHAPE       # in % 16
+    assert lib.ffn_prepare_weights_q4(q, p[2], 4, 64, None) == _lib.FFN_ERR_SHAPE        # in % 128
+    assert lib.ffn_prepare_weights_fp8(_lib.Fp8Weight(p[0].value, None), p[2], 4, 32, None) == _lib.FFN_ERR_NULL
+    assert lib.ffn_prepare_weights_fp8(f, ctypes.c_void_p(p[2].value + 8), 4, 32, None) == _lib.FFN_ERR_ALIGN
+    assert lib.ffn_prepare_weights_fp8(f, ctypes.c_void_p(p[0].value + 64), 4, 32, None) == _lib.FFN_ERR_ALIAS
+    assert lib.ffn_prepare_weights_q4(q, ctypes.c_void_p(p[1].value), 4, 128, None) == _lib.FFN_ERR_ALIAS
+    assert lib.ffn_prepare_weights_fp8(f, p[2], 0, 32, None) == _lib.FFN_OK

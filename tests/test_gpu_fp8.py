@@ -5,7 +5,7 @@ import numpy as np
 import pytest
 
 import synth
-from gpu_util import assert_lowp, to_dev, to_host64
+from gpu_util import assert_lowp, fp8_dev, to_dev, to_host64
 
 pytestmark = pytest.mark.gpu
 
@@ -14,12 +14,6 @@ pytestmark = pytest.mark.gpu
 def ffn():
     from transformer_ffn_rmsnorm_gb300 import ffn as m
     return m
-
-
-def fp8_dev(inp: dict, name: str):
-    import torch
-    return (torch.from_numpy(np.ascontiguousarray(inp["c_" + name])).cuda(),
-            torch.from_numpy(np.ascontiguousarray(inp["s_" + name])).cuda())
 
 
 def run_fp8(ffn, inp, flags=0):

@@ -63,6 +63,8 @@ SIGNATURES = {
                                                 c_void_p, c_int64, c_int64, c_int64, c_float, c_int,
                                                 c_void_p]),
     "ffn_prepare_weights": (c_int, [c_void_p, c_void_p, c_int64, c_int, c_void_p]),
+    "ffn_prepare_weights_fp8": (c_int, [Fp8Weight, c_void_p, c_int64, c_int64, c_void_p]),
+    "ffn_prepare_weights_q4": (c_int, [Q4Weight, c_void_p, c_int64, c_int64, c_void_p]),
     "ffn_q4_pack_host": (c_int, [c_void_p, c_void_p, c_int64, c_int64, c_void_p, c_void_p]),
     "ffn_status_string": (ctypes.c_char_p, [c_int]),
     "ffn_device_status": (c_int, []),

@@ -512,6 +512,28 @@ ffn_status ffn_prepare_weights(const void *src, void *dst, int64_t count, ffn_dt
     return from_cuda(launch_prepare_weights(src, dst, count, src_dtype, static_cast<cudaStream_t>(stream)));
 }
 
+ffn_status ffn_prepare_weights_fp8(ffn_fp8_weight w, void *dst, int64_t out, int64_t in, void *stream) {
+    if (out < 0 || in < 0 || in % 16) return FFN_ERR_SHAPE;
+    if (out == 0 || in == 0) return FFN_OK;
+    if (!w.codes || !w.scales || !dst) return FFN_ERR_NULL;
+    if (!aligned16(w.codes) || !aligned16(w.scales) || !aligned16(dst)) return FFN_ERR_ALIGN;
+    const size_t n = static_cast<size_t>(out) * in;
+    const Range rd{dst, 2 * n};
+    if (overlaps(rd, {w.codes, n}) || overlaps(rd, {w.scales, static_cast<size_t>(out) * 4})) return FFN_ERR_ALIAS;
+    return from_cuda(launch_prepare_fp8(w.codes, w.scales, dst, out, in, static_cast<cudaStream_t>(stream)));
+}
+
+ffn_status ffn_prepare_weights_q4(ffn_q4_weight w, void *dst, int64_t out, int64_t in, void *stream) {
+    if (out < 0 || in < 0 || in % 128) return FFN_ERR_SHAPE;
+    if (out == 0 || in == 0) return FFN_OK;
+    if (!w.qs || !w.scales || !dst) return FFN_ERR_NULL;
+    if (!aligned16(w.qs) || !aligned16(w.scales) || !aligned16(dst)) return FFN_ERR_ALIGN;
+    const size_t n = static_cast<size_t>(out) * in;
+    const Range rd{dst, 2 * n};
+    if (overlaps(rd, {w.qs, n / 2}) || overlaps(rd, {w.scales, n / 16})) return FFN_ERR_ALIAS;
+    return from_cuda(launch_prepare_q4(w.qs, w.scales, dst, out, in, static_cast<cudaStream_t>(stream)));
+}
+
 ffn_status ffn_timing_enable(int on) {
     g_timing.store(on != 0);
     return FFN_OK;

@@ -81,6 +81,11 @@ cudaError_t launch_rmsnorm_to_f16(const void *x, const void *g, void *n, int64_t
 // dst[i] = fp16(src[i] * 2^8) for 16-bit src of type dt; out-of-range values
 // set DEVERR_RANGE in the device status word.
 cudaError_t launch_prepare_weights(const void *src, void *dst, int64_t count, int dt, cudaStream_t s);
+// fp16(w * 2^8) from e4m3 codes with row scales / from Q4 in the device layout
+cudaError_t launch_prepare_fp8(const uint8_t *codes, const float *scales, void *dst, int64_t rows, int64_t cols,
+                               cudaStream_t s);
+cudaError_t launch_prepare_q4(const uint8_t *qs, const uint16_t *scales, void *dst, int64_t rows, int64_t cols,
+                              cudaStream_t s);
 cudaError_t launch_swiglu(const void *gate, const void *up, void *h, int64_t count, int dt,
                           cudaStream_t s);
 // One CTA whose bounded wait on a never-completed barrier gives up after

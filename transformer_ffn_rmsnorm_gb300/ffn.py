@@ -145,6 +145,28 @@ def ffn_prepare_weights(w: torch.Tensor, out: torch.Tensor | None = None, stream
     return dst
 
 
+def ffn_prepare_weights_fp8(w, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Prepared fp16 weights (values of e4m3 * row scale * 2^8) from a
+    (codes [out, in], scales [out]) pair, for FFN_PREPARED_WEIGHTS."""
+    codes, _ = w
+    o, i = codes.shape
+    dst = torch.empty((o, i), dtype=torch.float16, device=codes.device) if out is None else out
+    _need_cuda(dst)
+    _check(_lib.load().ffn_prepare_weights_fp8(_fp8(w), _ptr(dst), o, i, _stream(stream)), "ffn_prepare_weights_fp8")
+    return dst
+
+
+def ffn_prepare_weights_q4(w, inn: int, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Prepared fp16 weights (values of (u - 8) * s * 2^8) from a Q4 (qs,
+    scales) pair in the device layout; `inn` is the input dimension."""
+    qs, _ = w
+    o = qs.shape[0]
+    dst = torch.empty((o, inn), dtype=torch.float16, device=qs.device) if out is None else out
+    _need_cuda(dst)
+    _check(_lib.load().ffn_prepare_weights_q4(_q4(w), _ptr(dst), o, inn, _stream(stream)), "ffn_prepare_weights_q4")
+    return dst
+
+
 def ffn_block_q4_workspace_bytes(rows: int, d: int, ffn: int) -> int:
     out = ctypes.c_size_t(0)
     _check(_lib.load().ffn_block_q4_workspace_bytes(rows, d, ffn, ctypes.byref(out)),
