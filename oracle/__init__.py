@@ -88,6 +88,9 @@ class Oracle:
                                         ctypes.c_int64, ctypes.c_int64]
         L.oracle_e4m3_to_double.restype = ctypes.c_double
         L.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+        L.oracle_q8_dequant.restype = None
+        L.oracle_q8_dequant.argtypes = [ctypes.POINTER(ctypes.c_int8), ctypes.POINTER(ctypes.c_uint16), _D,
+                                        ctypes.c_int64, ctypes.c_int64]
         L.oracle_fp8_dequant.restype = None
         L.oracle_fp8_dequant.argtypes = [ctypes.POINTER(ctypes.c_uint8), ctypes.POINTER(ctypes.c_float), _D,
                                          ctypes.c_int64, ctypes.c_int64]
@@ -174,6 +177,26 @@ class Oracle:
                                  scales.ctypes.data_as(ctypes.POINTER(ctypes.c_uint16)),
                                  _ptr(w), out, inn)
         return w
+
+    def q8_dequant(self, q, scales, out: int, inn: int) -> np.ndarray:
+        q = np.ascontiguousarray(q, dtype=np.int8)
+        scales = np.ascontiguousarray(scales).view(np.uint16)
+        assert q.size == out * inn and scales.size == out * (inn // 32)
+        w = np.empty((out, inn), dtype=np.float64)
+        self.L.oracle_q8_dequant(q.ctypes.data_as(ctypes.POINTER(ctypes.c_int8)),
+                                 scales.ctypes.data_as(ctypes.POINTER(ctypes.c_uint16)), _ptr(w), out, inn)
+        return w
+
+    def q8_block_from_inputs(self, inp: dict, rows=None, nthreads=None, residual=False) -> np.ndarray:
+        """Oracle y for a ``synth.make_q8_inputs`` dict, on weights the oracle
+        dequantises itself from the codes and scale bits."""
+        cfg = inp["cfg"]
+        D, F = cfg.d, cfg.ffn
+        wg = self.q8_dequant(inp["q8_gate"], inp["q8s_gate"], F, D)
+        wu = self.q8_dequant(inp["q8_up"], inp["q8s_up"], F, D)
+        wd = self.q8_dequant(inp["q8_down"], inp["q8s_down"], D, F)
+        x = inp["x"] if rows is None else inp["x"][np.asarray(rows)]
+        return self.ffn_block(widen(x, "bf16"), widen(inp["g"], "bf16"), wg, wu, wd, cfg.eps, nthreads, residual)
 
     # -- convenience: stored inputs -> float64 result --------------------
     def block_from_inputs(self, inp: dict, rows=None, nthreads=None, residual=False) -> np.ndarray:

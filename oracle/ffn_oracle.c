@@ -29,6 +29,11 @@
  *               a half-precision scale).  w = (u - 8) * s with u the 4-bit
  *               offset-binary value; the layout is documented at
  *               oracle_q4_dequant below.
+ *   Q8_0     -- "Unfusing a Kernel Made It 1.63x Faster", "Finding 2: a
+ *               quantized KV cache buys nothing while you're
+ *               occupancy-bound" (Q8_0, there for the KV cache): blocks of
+ *               32 signed 8-bit values with one half-precision scale,
+ *               w = q * s; oracle_q8_dequant below.
  *
  * Build: cc -O2 -ffp-contract=off -fPIC -shared ffn_oracle.c -lm -lpthread
  * (no -ffast-math; -ffp-contract=off keeps x86 and Arm results identical).
@@ -234,6 +239,20 @@ void oracle_q4_dequant(const uint8_t *qs, const uint16_t *scales, double *w,
             }
         }
     }
+}
+
+/* ----------------------------------------------------------------- Q8_0 */
+
+/* Dequantise Q8_0 weights into double w[out x in].  Blocks of 32 weights run
+ * along the input dimension, each with one fp16 scale; q[o][i] is a signed
+ * byte (two's complement, -128..127) and w[o][i] = q[o][i] * s[o][i / 32].
+ * The layout keeps the bytes in natural order, [out x in], and the scales in
+ * their own array [out x in/32] (a block's 34 bytes, split in two). */
+void oracle_q8_dequant(const int8_t *q, const uint16_t *scales, double *w, int64_t out, int64_t in) {
+    int64_t nblk = in / 32;
+    for (int64_t o = 0; o < out; ++o)
+        for (int64_t i = 0; i < in; ++i)
+            w[o * in + i] = (double)q[o * in + i] * oracle_half_to_double(scales[o * nblk + i / 32]);
 }
 
 /* ------------------------------------------------------------------ fp8 */

@@ -31,6 +31,7 @@ __all__ = [
     "stream", "normal", "round_to_storage", "make_block_inputs",
     "make_norm_inputs", "make_swiglu_inputs", "make_q4_inputs", "pack_q4",
     "q4_canonical_bytes", "TENSOR_IDS", "Fp8Config", "C6_DECODE_FP8", "make_fp8_inputs", "to_e4m3",
+    "Q8Config", "C7_DECODE_Q8", "make_q8_inputs",
 ]
 
 # Tensor ids inside one seed.  Each id owns an independent stream.
@@ -40,6 +41,7 @@ TENSOR_IDS = {
     "s_gate": 8, "s_up": 9, "s_down": 10,
     "gate": 11, "up": 12,
     "f8_gate": 13, "f8_up": 14, "f8_down": 15, "f8s_gate": 16, "f8s_up": 17, "f8s_down": 18,
+    "q8_gate": 19, "q8_up": 20, "q8_down": 21, "q8s_gate": 22, "q8s_up": 23, "q8s_down": 24,
 }
 
 _CHUNK = 1 << 22
@@ -292,4 +294,39 @@ def make_fp8_inputs(cfg: Fp8Config, seed: int = 0, rows: int | None = None,
         res["c_" + name] = to_e4m3(v)
         sc = (1.0 + 0.1 * stream(seed, "f8s_" + name).standard_normal(o)) / (16.0 * math.sqrt(i))
         res["s_" + name] = sc.astype(np.float32)
+    return res
+
+
+# ------------------------------------------------------------------ Q8_0
+@dataclass(frozen=True)
+class Q8Config:
+    name: str
+    rows: int
+    d: int
+    ffn: int
+    eps: float
+
+
+# the bf16 decode shape with Q8_0 weights (int8 codes, an fp16 scale per 32)
+C7_DECODE_Q8 = Q8Config("decode_q8_8x4096x14336", 8, 4096, 14336, 1e-5)
+
+
+def make_q8_inputs(cfg: Q8Config, seed: int = 0, rows: int | None = None,
+                   d: int | None = None, ffn: int | None = None) -> dict:
+    """x~N(0,1) bf16, g=1+0.1*N(0,1) bf16, weights as int8 codes
+    clip(round(32*N(0,1)), -128, 127) with fp16 block scales
+    (1 + 0.1*N(0,1)) / (32*sqrt(fan_in)), i.e. weights ~N(0, 1/fan_in) as in
+    the other block workloads.  Scales are returned as uint16 bit patterns."""
+    cfg = replace(cfg, rows=rows if rows is not None else cfg.rows,
+                  d=d if d is not None else cfg.d,
+                  ffn=ffn if ffn is not None else cfg.ffn)
+    M, D, F = cfg.rows, cfg.d, cfg.ffn
+    res = {"cfg": cfg,
+           "x": normal((M, D), 0.0, 1.0, seed, "x", "bf16"),
+           "g": normal((D,), 1.0, 0.1, seed, "g", "bf16")}
+    for name, (o, i) in (("gate", (F, D)), ("up", (F, D)), ("down", (D, F))):
+        q = np.clip(np.rint(32.0 * stream(seed, "q8_" + name).standard_normal((o, i))), -128, 127)
+        res["q8_" + name] = q.astype(np.int8)
+        sc = (1.0 + 0.1 * stream(seed, "q8s_" + name).standard_normal((o, i // 32))) / (32.0 * math.sqrt(i))
+        res["q8s_" + name] = sc.astype(np.float16).view(np.uint16)
     return res

@@ -300,4 +300,22 @@ def pin_fp8_dequant_rows(o):
             assert w[r, i] == o.e4m3_to_double(codes[r, i]) * float(scales[r])
 
 
+def pin_q8_dequant_values(o):
+    """Q8_0: every weight is its signed code times its own block's scale,
+    checked against numpy's fp16 decoding of the scale bits and the codes'
+    integers, with the extreme codes, zero, negative scales and a different
+    scale in every block."""
+    rng = np.random.default_rng(23)
+    out, inn = 3, 128
+    q = rng.integers(-128, 128, (out, inn)).astype(np.int8)
+    q[0, :4] = [-128, 127, 0, -1]
+    scales = (rng.standard_normal((out, inn // 32)) * 0.01).astype(np.float16)
+    scales[1, 2] = -0.5
+    w = o.q8_dequant(q, scales.view(np.uint16), out, inn)
+    ref = q.astype(np.float64) * np.repeat(scales.astype(np.float64), 32, axis=1)
+    assert np.array_equal(w, ref)
+    assert w[0, 0] == -128.0 * float(scales[0, 0]) and w[0, 1] == 127.0 * float(scales[0, 0])
+    assert w[1, 64] == q[1, 64] * -0.5 and w[1, 95] == q[1, 95] * -0.5
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

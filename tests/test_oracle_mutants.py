@@ -34,6 +34,10 @@ MUTANTS = [
     ("e4m3_no_implicit_one", "ldexp((double)(8 + f), e - 10)", "ldexp((double)f, e - 7)"),
     ("e4m3_subnormal_scale", "v = ldexp((double)f, -9);", "v = ldexp((double)f, -10);"),
     ("fp8_scale_of_wrong_row", "const double s = (double)scales[o];", "const double s = (double)scales[(o + 1) % out];"),
+    ("q8_block_of_16", "scales[o * nblk + i / 32]", "scales[o * nblk + i / 16 % nblk]"),
+    ("q8_codes_unsigned", "(double)q[o * in + i] * oracle_half_to_double",
+     "(double)(uint8_t)q[o * in + i] * oracle_half_to_double"),
+    ("q8_scale_of_next_row", "scales[o * nblk + i / 32]", "scales[((o + 1) % out) * nblk + i / 32]"),
 ]
 
 
