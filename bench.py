@@ -8,7 +8,7 @@ tcgen05 gate/up GEMM with the SwiGLU epilogue -> tcgen05 down GEMM), on seeded
 synthetic inputs.  The weights are re-encoded once, before timing, by
 ffn_prepare_weights (fp16 values of w * 2^8, exact), so the tensor operands are
 fp16; the unprepared bf16 path (hi + lo activation terms) is timed beside it.  Rank 0 prints one JSON line.  The standalone RMSNorm and SwiGLU
-workloads, the bf16 decode block, the Q4 and the e4m3 decode blocks are timed after it
+workloads, the bf16 decode block, the Q4, e4m3 and Q8_0 decode blocks are timed after it
 and reported under "sub".
 
 --impl reference times the float64 CPU oracle on the host cores on a bounded
@@ -45,7 +45,7 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-sub", action="store_true", help="skip the secondary workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU baseline")
-    ap.add_argument("--workload", choices=["prefill", "decode", "decode_prepared", "q4", "fp8", "rmsnorm", "swiglu"],
+    ap.add_argument("--workload", choices=["prefill", "decode", "decode_prepared", "q4", "fp8", "q8", "rmsnorm", "swiglu"],
                     default="prefill",
                     help="prefill: the benchmark; others run only that workload (for profiling)")
     ap.add_argument("--only-main", action="store_true",
@@ -242,6 +242,7 @@ def sub_benchmarks(torch, ffn, device, peaks, peak_src, stream):
     out.append(decode_bench(torch, ffn, device, hbm, peak_src, stream))
     out.append(q4_bench(torch, ffn, device, hbm, peak_src, stream))
     out.append(fp8_bench(torch, ffn, device, hbm, peak_src, stream))
+    out.append(q8_bench(torch, ffn, device, hbm, peak_src, stream))
     return out
 
 
@@ -341,8 +342,38 @@ def fp8_bench(torch, ffn, device, hbm, peak_src, stream):
                          "peak_source": peak_src + " hbm_gbs (copy, burst)", "algorithmic_bytes": wbytes}}
 
 
+def q8_setup(torch, ffn, device):
+    cfg = synth.C7_DECODE_Q8
+    inp = synth.make_q8_inputs(cfg, seed=0)
+    xq = to_dev(inp["x"], "bf16", torch, device)
+    gq = to_dev(inp["g"], "bf16", torch, device)
+    wsets = []
+    for _ in range(2):   # two weight copies rotated: 2 x 187 MB > L2
+        wsets.append([(torch.from_numpy(inp["q8_" + n]).to(device),
+                       torch.from_numpy(inp["q8s_" + n].view(np.int16)).to(device)) for n in ("gate", "up", "down")])
+    yq = torch.empty_like(xq)
+    ws = ffn.workspace(ffn.ffn_block_q8_workspace_bytes(cfg.rows, cfg.d, cfg.ffn), device)
+    return cfg, (lambda i: ffn.ffn_block_forward_q8(xq, gq, *wsets[i % 2], eps=cfg.eps, out=yq, ws=ws))
+
+
+def q8_bench(torch, ffn, device, hbm, peak_src, stream):
+    cfg, call = q8_setup(torch, ffn, device)
+    us = graph_time_us(torch, call, 20, 10, stream)
+    with ffn.KernelTimer() as kt:
+        timed_loop(torch, call, 50, 3, stream)
+        res = kt.read()
+    wbytes = 3 * cfg.ffn * cfg.d * 34 // 32   # codes and fp16 block scales
+    return {"workload": cfg.name, "us_per_call": round(us, 3), "tokens_per_s": round(cfg.rows / us * 1e6, 1),
+            "timing": "CUDA graph of 20 calls (two weight copies alternating), 10 replays",
+            "kernels_events": kernel_table(res),
+            "roofline": {"bound": "hbm", "kernel": "whole block (3 launches)",
+                         "achieved": round(wbytes / us / 1e3, 1), "peak": hbm, "unit": "GB/s",
+                         "frac": round(wbytes / us / 1e3 / hbm, 4),
+                         "peak_source": peak_src + " hbm_gbs (copy, burst)", "algorithmic_bytes": wbytes}}
+
+
 def run_workload_only(args):
-    """--workload decode|decode_prepared|q4|fp8|rmsnorm|swiglu: run that workload for --warmup +
+    """--workload decode|decode_prepared|q4|fp8|q8|rmsnorm|swiglu: run that workload for --warmup +
     --steps calls and print a short line (used for ncu captures)."""
     import torch
     from transformer_ffn_rmsnorm_gb300 import ffn
@@ -363,6 +394,8 @@ def run_workload_only(args):
         cfg, call = q4_setup(torch, ffn, device)
     elif args.workload == "fp8":
         cfg, call = fp8_setup(torch, ffn, device)
+    elif args.workload == "q8":
+        cfg, call = q8_setup(torch, ffn, device)
     else:
         cfg, call = decode_setup(torch, ffn, device, prepared=args.workload == "decode_prepared")
     for i in range(args.warmup + args.steps):

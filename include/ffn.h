@@ -283,7 +283,41 @@ ffn_status ffn_prepare_weights(const void *src, void *dst, int64_t count, ffn_dt
                                void *stream);
 
 /* ------------------------------------------------------------------------
- * ffn_prepare_weights_fp8 / ffn_prepare_weights_q4 -- the same prepared form
+ * Q8_0 weights: blocks of 32 signed 8-bit codes along the input dimension,
+ * one IEEE fp16 scale per block ("Unfusing a Kernel Made It 1.63x Faster",
+ * section "Finding 2: a quantized KV cache buys nothing while you're
+ * occupancy-bound" names the format, there for the KV cache; here the
+ * projection weights, at 34 bytes per 32 weights).
+ *   codes: [out x in] int8, row-major (natural order); scales: [out x in/32]
+ *   fp16 bit patterns; w[o][i] = codes[o][i] * scales[o][i / 32].  Both are
+ *   device pointers (16-byte aligned) owned by the caller.
+ * ---------------------------------------------------------------------- */
+typedef struct {
+    const int8_t *codes;
+    const uint16_t *scales;
+} ffn_q8_weight;
+
+ffn_status ffn_block_q8_workspace_bytes(int64_t rows, int64_t d, int64_t ffn, size_t *bytes);
+
+/* ------------------------------------------------------------------------
+ * ffn_block_forward_q8 -- the block with Q8_0 weights (decode: the weights
+ * are streamed; "How Megakernels Work", section "Projection shape changes
+ * the achieved rate").
+ *   x [rows x d] bf16, g [d] bf16, y [rows x d] bf16; w_gate/w_up are Q8_0
+ *   [ffn x d], w_down is Q8_0 [d x ffn].  Needs d % 256 == 0 and
+ *   ffn % 256 == 0 (FFN_ERR_SHAPE otherwise).  Rows are processed in groups
+ *   of up to 16; each group streams the weights once.  The codes are exact in
+ *   fp16; each 32-weight block's MMA result is multiplied by its scale in
+ *   fp32; activations enter as one fp16 rounding (h stored times 2^-8).
+ *   flags: FFN_AUTO or FFN_RESIDUAL.  Errors as ffn_block_forward_fp8.
+ * ---------------------------------------------------------------------- */
+ffn_status ffn_block_forward_q8(const void *x, const void *g, ffn_q8_weight w_gate, ffn_q8_weight w_up,
+                                ffn_q8_weight w_down, void *y, int64_t rows, int64_t d, int64_t ffn, float eps,
+                                uint32_t flags, void *workspace, size_t workspace_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
+ * ffn_prepare_weights_fp8 / ffn_prepare_weights_q4 / ffn_prepare_weights_q8
+ * -- the same prepared form
  * (fp16 values of w * 2^8, [out x in] row-major) from quantised weights, for
  * many-row batches: ffn_block_forward_fp8 and ffn_block_forward_q4 stream the
  * whole quantised weight set once per group of 16 rows, the fast path for a
@@ -302,6 +336,8 @@ ffn_status ffn_prepare_weights(const void *src, void *dst, int64_t count, ffn_dt
  * ---------------------------------------------------------------------- */
 ffn_status ffn_prepare_weights_fp8(ffn_fp8_weight w, void *dst, int64_t out, int64_t in, void *stream);
 ffn_status ffn_prepare_weights_q4(ffn_q4_weight w, void *dst, int64_t out, int64_t in, void *stream);
+/* Q8_0: w = q * s; in % 32 == 0; exact before the one rounding to fp16. */
+ffn_status ffn_prepare_weights_q8(ffn_q8_weight w, void *dst, int64_t out, int64_t in, void *stream);
 
 /* Host helper (not on the hot path): pack int8 q [out x in] (values -8..7) and
  * fp16 scale bits [out x in/32] into the device layout above.  Host pointers;

@@ -65,3 +65,9 @@ def fp8_dev(inp: dict, name: str):
     import torch
     return (torch.from_numpy(np.ascontiguousarray(inp["c_" + name])).cuda(),
             torch.from_numpy(np.ascontiguousarray(inp["s_" + name])).cuda())
+
+
+def q8_dev(inp: dict, name: str):
+    import torch
+    return (torch.from_numpy(np.ascontiguousarray(inp["q8_" + name])).cuda(),
+            torch.from_numpy(np.ascontiguousarray(inp["q8s_" + name]).view(np.int16)).cuda())

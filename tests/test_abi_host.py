@@ -218,3 +218,25 @@ def test_quantised_prepare_rejects_before_launch(lib):
     assert lib.ffn_prepare_weights_fp8(f, ctypes.c_void_p(p[0].value + 64), 4, 32, None) == _lib.FFN_ERR_ALIAS
     assert lib.ffn_prepare_weights_q4(q, ctypes.c_void_p(p[1].value), 4, 128, None) == _lib.FFN_ERR_ALIAS
     assert lib.ffn_prepare_weights_fp8(f, p[2], 0, 32, None) == _lib.FFN_OK
+
+
+def test_q8_entry_rejects_before_launch(lib):
+    out = ctypes.c_size_t(0)
+    assert lib.ffn_block_q8_workspace_bytes(8, 4096, 14336, ctypes.byref(out)) == 0 and out.value > 0
+    for d, f in ((4096 + 128, 14336), (4096, 14336 + 128)):   # multiples of 256 only
+        assert lib.ffn_block_q8_workspace_bytes(8, d, f, ctypes.byref(out)) == _lib.FFN_ERR_SHAPE
+    p = [ctypes.c_void_p((i + 1) << 24) for i in range(12)]
+    w = [_lib.Q8Weight(p[2 + 2 * i].value, p[3 + 2 * i].value) for i in range(3)]
+    lib.ffn_block_q8_workspace_bytes(8, 512, 1024, ctypes.byref(out))
+    need = out.value
+    assert lib.ffn_block_forward_q8(p[0], p[1], _lib.Q8Weight(p[2].value, None), w[1], w[2], p[8], 8, 512, 1024,
+                                    1e-6, 0, p[9], need, None) == _lib.FFN_ERR_NULL
+    assert lib.ffn_block_forward_q8(p[0], p[1], *w, p[8], 8, 512, 1024, 1e-6, _lib.FFN_GATEUP_FUSED, p[9], need,
+                                    None) == _lib.FFN_ERR_FLAGS
+    assert lib.ffn_block_forward_q8(p[0], p[1], *w, p[8], 8, 512, 1024, 1e-6, 0, p[9], need - 1,
+                                    None) == _lib.FFN_ERR_WORKSPACE
+    assert lib.ffn_block_forward_q8(p[0], p[1], *w, ctypes.c_void_p(p[3].value + 256), 8, 512, 1024, 1e-6, 0, p[9],
+                                    need, None) == _lib.FFN_ERR_ALIAS
+    q = _lib.Q8Weight(p[0].value, p[1].value)
+    assert lib.ffn_prepare_weights_q8(q, p[2], 4, 48, None) == _lib.FFN_ERR_SHAPE        # in % 32
+    assert lib.ffn_prepare_weights_q8(q, ctypes.c_void_p(p[1].value + 32), 64, 64, None) == _lib.FFN_ERR_ALIAS

@@ -37,6 +37,10 @@ class Fp8Weight(ctypes.Structure):
     _fields_ = [("codes", c_void_p), ("scales", c_void_p)]
 
 
+class Q8Weight(ctypes.Structure):
+    _fields_ = [("codes", c_void_p), ("scales", c_void_p)]
+
+
 # name -> (restype, argtypes), in the order of include/ffn.h
 SIGNATURES = {
     "ffn_rmsnorm": (c_int, [c_void_p, c_void_p, c_void_p, c_int64, c_int64, c_float, c_int, c_void_p]),
@@ -59,12 +63,17 @@ SIGNATURES = {
     "ffn_block_forward_fp8": (c_int, [c_void_p, c_void_p, Fp8Weight, Fp8Weight, Fp8Weight, c_void_p,
                                       c_int64, c_int64, c_int64, c_float, c_uint32, c_void_p,
                                       c_size_t, c_void_p]),
+    "ffn_block_q8_workspace_bytes": (c_int, [c_int64, c_int64, c_int64, ctypes.POINTER(c_size_t)]),
+    "ffn_block_forward_q8": (c_int, [c_void_p, c_void_p, Q8Weight, Q8Weight, Q8Weight, c_void_p,
+                                     c_int64, c_int64, c_int64, c_float, c_uint32, c_void_p,
+                                     c_size_t, c_void_p]),
     "ffn_block_forward_decode_static": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                                 c_void_p, c_int64, c_int64, c_int64, c_float, c_int,
                                                 c_void_p]),
     "ffn_prepare_weights": (c_int, [c_void_p, c_void_p, c_int64, c_int, c_void_p]),
     "ffn_prepare_weights_fp8": (c_int, [Fp8Weight, c_void_p, c_int64, c_int64, c_void_p]),
     "ffn_prepare_weights_q4": (c_int, [Q4Weight, c_void_p, c_int64, c_int64, c_void_p]),
+    "ffn_prepare_weights_q8": (c_int, [Q8Weight, c_void_p, c_int64, c_int64, c_void_p]),
     "ffn_q4_pack_host": (c_int, [c_void_p, c_void_p, c_int64, c_int64, c_void_p, c_void_p]),
     "ffn_status_string": (ctypes.c_char_p, [c_int]),
     "ffn_device_status": (c_int, []),

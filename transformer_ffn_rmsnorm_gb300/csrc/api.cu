@@ -457,6 +457,59 @@ ffn_status ffn_block_forward_fp8(const void *x, const void *g, ffn_fp8_weight w_
     return FFN_OK;
 }
 
+ffn_status ffn_block_q8_workspace_bytes(int64_t rows, int64_t d, int64_t ffn, size_t *bytes) {
+    if (!bytes) return FFN_ERR_NULL;
+    if (rows < 0 || d < 256 || ffn < 256 || d % 256 || ffn % 256) return FFN_ERR_SHAPE;
+    if (rows > INT32_MAX || d > INT32_MAX || ffn > INT32_MAX) return FFN_ERR_SHAPE;
+    *bytes = rows == 0 ? 0 : gemv_workspace_bytes(std::min<int64_t>(rows, kGemvMaxRows), d, ffn, false);
+    return FFN_OK;
+}
+
+ffn_status ffn_block_forward_q8(const void *x, const void *g, ffn_q8_weight w_gate,
+                                 ffn_q8_weight w_up, ffn_q8_weight w_down, void *y, int64_t rows,
+                                 int64_t d, int64_t ffn, float eps, uint32_t flags, void *workspace,
+                                 size_t workspace_bytes, void *stream) {
+    if (!g || !w_gate.codes || !w_gate.scales || !w_up.codes || !w_up.scales || !w_down.codes ||
+        !w_down.scales || (rows != 0 && (!x || !y)))
+        return FFN_ERR_NULL;
+    if (flags & ~FFN_RESIDUAL) return FFN_ERR_FLAGS;
+    size_t need = 0;
+    ffn_status st = ffn_block_q8_workspace_bytes(rows, d, ffn, &need);
+    if (st != FFN_OK) return st;
+    if (need > 0 && !workspace) return FFN_ERR_WORKSPACE;
+    if (workspace_bytes < need) return FFN_ERR_WORKSPACE;
+    const void *ptrs[] = {x, g, y, w_gate.codes, w_gate.scales, w_up.codes, w_up.scales, w_down.codes,
+                          w_down.scales};
+    for (const void *p : ptrs)
+        if (!aligned16(p)) return FFN_ERR_ALIGN;
+    if (workspace && !aligned16(workspace)) return FFN_ERR_ALIGN;
+    const size_t cb = static_cast<size_t>(ffn) * d, sb = cb / 16;
+    const Range ry{y, static_cast<size_t>(rows) * d * 2}, rws{workspace, need};
+    const Range ins[] = {{x, static_cast<size_t>(rows) * d * 2}, {g, static_cast<size_t>(d) * 2},
+                         {w_gate.codes, cb}, {w_gate.scales, sb}, {w_up.codes, cb}, {w_up.scales, sb},
+                         {w_down.codes, cb}, {w_down.scales, sb}};
+    for (const Range &in : ins)
+        if (overlaps(ry, in) || overlaps(rws, in)) return FFN_ERR_ALIAS;
+    if (overlaps(ry, rws)) return FFN_ERR_ALIAS;
+    if (rows == 0) return FFN_OK;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t grp = std::min<int64_t>(rows, kGemvMaxRows);
+    GemvWorkspace gw;
+    gemv_carve(workspace, grp, d, ffn, false, &gw);
+    GemvWeights a{w_gate.codes, nullptr, w_gate.scales}, b{w_up.codes, nullptr, w_up.scales},
+        c{w_down.codes, nullptr, w_down.scales};
+    for (int64_t r0 = 0; r0 < rows; r0 += kGemvMaxRows) {
+        const int64_t nr = std::min<int64_t>(kGemvMaxRows, rows - r0);
+        const char *xr = static_cast<const char *>(x) + r0 * d * 2;
+        char *yr = static_cast<char *>(y) + r0 * d * 2;
+        cudaError_t e = launch_gemv_block(WF_Q8, xr, g, a, b, c, yr, nr, d, ffn, eps, gw, s,
+                                          (flags & FFN_RESIDUAL) ? xr : nullptr);
+        if (e != cudaSuccess) return FFN_ERR_CUDA;
+    }
+    return FFN_OK;
+}
+
 ffn_status ffn_q4_pack_host(const int8_t *q, const uint16_t *scales, int64_t out, int64_t in,
                             uint8_t *qs_out, uint16_t *scales_out) {
     if (!q || !scales || !qs_out || !scales_out) return FFN_ERR_NULL;
@@ -532,6 +585,17 @@ ffn_status ffn_prepare_weights_q4(ffn_q4_weight w, void *dst, int64_t out, int64
     const Range rd{dst, 2 * n};
     if (overlaps(rd, {w.qs, n / 2}) || overlaps(rd, {w.scales, n / 16})) return FFN_ERR_ALIAS;
     return from_cuda(launch_prepare_q4(w.qs, w.scales, dst, out, in, static_cast<cudaStream_t>(stream)));
+}
+
+ffn_status ffn_prepare_weights_q8(ffn_q8_weight w, void *dst, int64_t out, int64_t in, void *stream) {
+    if (out < 0 || in < 0 || in % 32) return FFN_ERR_SHAPE;
+    if (out == 0 || in == 0) return FFN_OK;
+    if (!w.codes || !w.scales || !dst) return FFN_ERR_NULL;
+    if (!aligned16(w.codes) || !aligned16(w.scales) || !aligned16(dst)) return FFN_ERR_ALIGN;
+    const size_t n = static_cast<size_t>(out) * in;
+    const Range rd{dst, 2 * n};
+    if (overlaps(rd, {w.codes, n}) || overlaps(rd, {w.scales, n / 16})) return FFN_ERR_ALIAS;
+    return from_cuda(launch_prepare_q8(w.codes, w.scales, dst, out, in, static_cast<cudaStream_t>(stream)));
 }
 
 ffn_status ffn_timing_enable(int on) {

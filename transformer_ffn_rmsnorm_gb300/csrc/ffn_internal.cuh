@@ -86,6 +86,8 @@ cudaError_t launch_prepare_fp8(const uint8_t *codes, const float *scales, void *
                                cudaStream_t s);
 cudaError_t launch_prepare_q4(const uint8_t *qs, const uint16_t *scales, void *dst, int64_t rows, int64_t cols,
                               cudaStream_t s);
+cudaError_t launch_prepare_q8(const int8_t *codes, const uint16_t *scales, void *dst, int64_t rows, int64_t cols,
+                              cudaStream_t s);
 cudaError_t launch_swiglu(const void *gate, const void *up, void *h, int64_t count, int dt,
                           cudaStream_t s);
 // One CTA whose bounded wait on a never-completed barrier gives up after
@@ -116,12 +118,13 @@ size_t gemv_workspace_bytes(int64_t rows, int64_t d, int64_t ffn, bool two_terms
 void gemv_carve(void *base, int64_t rows, int64_t d, int64_t ffn, bool two_terms, GemvWorkspace *ws);
 // wfmt: 0 f16, 1 bf16, 2 q4 (bf16 x/y, fp16 operands), 3 prepared fp16 weights
 // (bf16 x/y, fp16 operands), 4 e4m3 weights with per-row scales (bf16 x/y,
-// fp16 operands)
-enum { WF_F16 = 0, WF_BF16 = 1, WF_Q4 = 2, WF_F16P = 3, WF_FP8 = 4 };
+// fp16 operands), 5 Q8_0 (int8 codes, fp16 scale per 32; bf16 x/y, fp16
+// operands)
+enum { WF_F16 = 0, WF_BF16 = 1, WF_Q4 = 2, WF_F16P = 3, WF_FP8 = 4, WF_Q8 = 5 };
 struct GemvWeights {
-    const void *w;          // f16/bf16 [out x in]; e4m3 codes [out x in]
+    const void *w;          // f16/bf16 [out x in]; e4m3 or int8 codes [out x in]
     const uint8_t *qs;      // q4 device layout
-    const uint16_t *sc;     // q4 scales
+    const uint16_t *sc;     // q4 / Q8_0 block scales [out x in/32]
     const float *rs;        // e4m3: float scale of each output row [out]
 };
 cudaError_t launch_gemv_block(int wfmt, const void *x, const void *g, GemvWeights wg,

@@ -461,8 +461,8 @@ cudaError_t launch_typed(const void *x, const void *gain, GemvWeights wg, GemvWe
         return launch_stream_down<WF, NT, TWO>(wd, ws.hfrag, ws.hfrag_lo, y, ws.partials, ws.counters, rows, d,
                                                ffn, geo.nchF, stream_down_splits(WF, d, ffn), res, s);
     }
-    if constexpr (WF == WF_FP8) {
-        return cudaErrorInvalidValue;   // e4m3 weights stream through the TMA kernels only
+    if constexpr (WF == WF_FP8 || WF == WF_Q8) {
+        return cudaErrorInvalidValue;   // e4m3 and Q8_0 weights stream through the TMA kernels only
     } else {
         {
             const int64_t tiles = 2 * geo.nchF;  // covers every fragment slot of h
@@ -505,7 +505,7 @@ Layout layout(int64_t rows, int64_t d, int64_t ffn) {
     const Geometry a = geometry(rows, d, ffn, false);
     const Geometry b = geometry(rows, d, ffn, (d % 128 == 0) && (ffn % 128 == 0));
     int64_t splits = a.splits > b.splits ? a.splits : b.splits;
-    for (int wf : {WF_BF16, WF_Q4, WF_FP8})
+    for (int wf : {WF_BF16, WF_Q4, WF_FP8, WF_Q8})
         if (stream_supported(wf, d, ffn)) splits = std::max(splits, stream_down_splits(wf, d, ffn));
     Layout l;
     l.frag_n = align256(static_cast<size_t>(a.nt) * a.nchK * 32 * 16);
@@ -562,6 +562,8 @@ cudaError_t launch_gemv_block(int wfmt, const void *x, const void *g, GemvWeight
             return launch_nt<WF_Q4, false>(geo.nt, x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s, res);
         case WF_FP8:  // fp16 operands, as for Q4
             return launch_nt<WF_FP8, false>(geo.nt, x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s, res);
+        case WF_Q8:
+            return launch_nt<WF_Q8, false>(geo.nt, x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s, res);
         default:      // prepared fp16 weights
             return launch_nt<WF_F16P, false>(geo.nt, x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s, res);
     }

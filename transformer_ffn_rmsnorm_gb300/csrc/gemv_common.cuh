@@ -80,6 +80,14 @@ template <> struct Fmt<WF_F16P> {
     static constexpr bool op_bf16 = false;
     static constexpr float w_unscale = 1.f / kPreparedScale, h_scale = 1.f / 256.f;
 };
+// Q8_0: the codes (-128..127) are exact in fp16 and times an fp16 block scale
+// exact in fp32; activations as for Q4.
+template <> struct Fmt<WF_Q8> {
+    using TIn = __nv_bfloat16; using TOp = __half;
+    static constexpr bool op_bf16 = false;
+    static constexpr float w_unscale = 1.f, h_scale = 1.f / 256.f;
+};
+
 // e4m3 weights: every code is exact in fp16 (3 fraction bits, exponents
 // 2^-9 .. 2^8), so the MMA multiplies the codes themselves and the row scale
 // multiplies each output once; activations as for Q4.
@@ -117,6 +125,22 @@ __device__ __forceinline__ void dequant_word(uint32_t w, uint32_t (&r)[4]) {
         b = (i & 1) ? __hfma2(b, k16th, k72) : __hsub2(b, k1032);
         r[i] = *reinterpret_cast<uint32_t *>(&b);
     }
+}
+
+// Four signed bytes (the low byte first) as two fp16 pairs, exactly: each
+// byte q + 128 (the sign bit flipped) goes into the low mantissa byte of
+// fp16 1024 (ulp 1), giving 1024 + 128 + q; one fp16 subtraction of 1152
+// leaves q.  One LOP3, two PRMT and two HSUB2.
+__device__ __forceinline__ void s8x4_to_f16x2(uint32_t w, uint32_t &h01, uint32_t &h23) {
+    const uint32_t u = w ^ 0x80808080u;
+    uint32_t a, b;
+    asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(a) : "r"(u), "r"(0x64646464u));   // [u0, 0x64, u1, 0x64]
+    asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(b) : "r"(u), "r"(0x64646464u));   // [u2, 0x64, u3, 0x64]
+    const __half2 k1152 = __floats2half2_rn(1152.f, 1152.f);
+    const __half2 ha = __hsub2(*reinterpret_cast<const __half2 *>(&a), k1152);
+    const __half2 hb = __hsub2(*reinterpret_cast<const __half2 *>(&b), k1152);
+    h01 = *reinterpret_cast<const uint32_t *>(&ha);
+    h23 = *reinterpret_cast<const uint32_t *>(&hb);
 }
 
 // Two e4m3 codes (the low byte is the first) as an fp16 pair, exactly.

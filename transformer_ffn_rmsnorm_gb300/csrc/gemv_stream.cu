@@ -8,7 +8,8 @@
 // a 6-stage shared-memory ring full with TMA bulk tensor copies of 64 weight
 // rows x one k-block (16-bit: 64 values, 128 bytes a row; Q4: 256 values,
 // 128 bytes of nibbles plus 16 bytes of fp16 scales a row; e4m3: 128 codes,
-// 128 bytes a row), 128-byte swizzled, plus -- by 1-D bulk copies -- the pre-arranged activation
+// 128 bytes a row; Q8_0: 256 codes in two 128-byte boxes plus 16 bytes of
+// scales a row), 128-byte swizzled, plus -- by 1-D bulk copies -- the pre-arranged activation
 // fragments of the same k range, while four MMA warps read everything from
 // shared memory.  (Reading the activations through L1 instead stalls: the
 // rings leave too little L1 to hold them.)
@@ -42,19 +43,22 @@ constexpr uint32_t kFragBytes = 32 * 16;   // one 32-value chunk of fragments fo
 enum { ROLE_GATEUP = 0, ROLE_DOWN = 1 };
 
 // Stage layout: [weights of each matrix][their scales (Q4)][activation
-// fragments: NT tiles x terms x chunks x 512 B].  Every format moves 128
-// bytes of each weight row per stage.
+// fragments: NT tiles x terms x chunks x 512 B].  Every format but Q8_0
+// moves 128 bytes of each weight row per stage (Q8_0: 256).
 template <int WF, int ROLE, int NT, bool TWO> struct Tile {
     static constexpr bool q4 = WF == WF_Q4;
     static constexpr bool fp8 = WF == WF_FP8;
+    static constexpr bool q8 = WF == WF_Q8;
+    static constexpr bool blocks = q4 || q8;                     // fp16 scales per 32 weights
     static constexpr int nmat = ROLE == ROLE_GATEUP ? 2 : 1;     // weight matrices per stage
     static constexpr int box_rows = ROLE == ROLE_GATEUP ? 32 : 64;
-    static constexpr int kb = q4 ? 256 : fp8 ? 128 : 64;         // k values per stage
-    static constexpr int x_per_kb = (q4 || fp8) ? 128 : 64;      // TMA inner coordinate per stage
+    static constexpr int kb = (q4 || q8) ? 256 : fp8 ? 128 : 64; // k values per stage
+    static constexpr int x_per_kb = q8 ? 256 : (q4 || fp8) ? 128 : 64;   // TMA inner coordinate per stage
     static constexpr int chunks = kb / kChunk;                   // fragment chunks per stage
     static constexpr int terms = TWO ? 2 : 1;
-    static constexpr uint32_t w_bytes = box_rows * 128;          // one matrix' rows x 128 B
-    static constexpr uint32_t s_bytes = q4 ? box_rows * 16 : 0;  // its scales
+    static constexpr uint32_t box_bytes = box_rows * 128;        // one 128-byte-wide TMA box
+    static constexpr uint32_t w_bytes = (q8 ? 2 : 1) * box_bytes;   // one matrix' rows of a stage
+    static constexpr uint32_t s_bytes = blocks ? box_rows * 16 : 0; // its scales
     static constexpr uint32_t b_off = nmat * (w_bytes + s_bytes);
     static constexpr uint32_t b_bytes = NT * terms * chunks * kFragBytes;
     static constexpr uint32_t stage_bytes = (b_off + b_bytes + 1023) & ~1023u;
@@ -88,6 +92,12 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
     asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                  : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
     return v;
 }
 
@@ -156,7 +166,11 @@ __global__ void __launch_bounds__(kThreads) gemv_stream_kernel(
                 const int y = static_cast<int>(row0);
                 ptx::tma_load_2d(st, &map_w0, bar, x, y);
                 if (TL::nmat == 2) ptx::tma_load_2d(st + TL::w_bytes, &map_w1, bar, x, y);
-                if (q4) {
+                if (TL::q8) {   // the second 128 codes of each row
+                    ptx::tma_load_2d(st + TL::box_bytes, &map_w0, bar, x + 128, y);
+                    if (TL::nmat == 2) ptx::tma_load_2d(st + TL::w_bytes + TL::box_bytes, &map_w1, bar, x + 128, y);
+                }
+                if (TL::blocks) {
                     const uint32_t sc = st + TL::nmat * TL::w_bytes;
                     ptx::tma_load_2d(sc, &map_s0, bar, static_cast<int>(kb * 8), y);
                     if (TL::nmat == 2) ptx::tma_load_2d(sc + TL::s_bytes, &map_s1, bar, static_cast<int>(kb * 8), y);
@@ -253,6 +267,48 @@ __global__ void __launch_bounds__(kThreads) gemv_stream_kernel(
                             const uint32_t x0 = (m & 1) ? bv.z : bv.x, x1 = (m & 1) ? bv.w : bv.y;
                             ptx::mma_16816<bf>(acc[n], a0, a1, a2, a3, x0, x1);
                         }
+                    }
+                }
+            } else if constexpr (TL::q8) {
+                // 256 k = eight 32-value blocks, 0-3 in the first 128-byte box of a
+                // row, 4-7 in the second; in block b this lane owns k = 8 tid .. 8
+                // tid + 7 (natural fragment order) of rows ra and rb
+                const uint32_t sbase = base + s * TL::stage_bytes + TL::nmat * TL::w_bytes + mat * TL::s_bytes;
+                const uint32_t bbase = base + s * TL::stage_bytes + TL::b_off + lane * 16;
+                const uint4 sa = lds128(sbase + ra * 16), sb = lds128(sbase + rb * 16);
+                float2 fsa[4], fsb[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t a = word_of(sa, j), b = word_of(sb, j);
+                    fsa[j] = __half22float2(*reinterpret_cast<const __half2 *>(&a));
+                    fsb[j] = __half22float2(*reinterpret_cast<const __half2 *>(&b));
+                }
+#pragma unroll
+                for (int bi = 0; bi < 8; ++bi) {
+                    const uint32_t box = wbase + static_cast<uint32_t>(bi >> 2) * TL::box_bytes;
+                    const int bl = bi & 3;
+                    // bytes 32 bl + 8 tid .. + 7 of the row: 16-byte granule 2 bl + tid / 2
+                    const uint32_t off = static_cast<uint32_t>((((2 * bl + (tid >> 1)) ^ g) << 4) + ((tid & 1) << 3));
+                    const uint2 qa = lds64(box + ra * 128 + off), qb = lds64(box + rb * 128 + off);
+                    uint4 b[NT];
+#pragma unroll
+                    for (int n = 0; n < NT; ++n) b[n] = lds128(bbase + (n * TL::chunks + bi) * kFragBytes);
+                    uint32_t a01x, a23x, a01y, a23y, c01x, c23x, c01y, c23y;
+                    s8x4_to_f16x2(qa.x, a01x, a23x);
+                    s8x4_to_f16x2(qa.y, a01y, a23y);
+                    s8x4_to_f16x2(qb.x, c01x, c23x);
+                    s8x4_to_f16x2(qb.y, c01y, c23y);
+                    const float fa = (bi & 1) ? fsa[bi >> 1].y : fsa[bi >> 1].x;
+                    const float fb = (bi & 1) ? fsb[bi >> 1].y : fsb[bi >> 1].x;
+#pragma unroll
+                    for (int n = 0; n < NT; ++n) {
+                        float t[4];   // this block's products alone, scaled below
+                        ptx::mma_16816_z<bf>(t, a01x, c01x, a23x, c23x, b[n].x, b[n].y);
+                        ptx::mma_16816<bf>(t, a01y, c01y, a23y, c23y, b[n].z, b[n].w);
+                        acc[n][0] = fmaf(fa, t[0], acc[n][0]);
+                        acc[n][1] = fmaf(fa, t[1], acc[n][1]);
+                        acc[n][2] = fmaf(fb, t[2], acc[n][2]);
+                        acc[n][3] = fmaf(fb, t[3], acc[n][3]);
                     }
                 }
             } else if constexpr (!q4) {
@@ -465,6 +521,10 @@ bool map_rows(CUtensorMap *m, const void *ptr, CUtensorMapDataType dt, int64_t i
 template <int WF, int ROLE>
 bool weight_maps(CUtensorMap *w, CUtensorMap *sc, const GemvWeights &wt, int64_t rows, int64_t K) {
     using TL = Tile<WF, ROLE, 1, false>;
+    if (TL::q8) {
+        if (!map_rows(w, wt.w, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, rows, K, 128, TL::box_rows, true)) return false;
+        return map_rows(sc, wt.sc, CU_TENSOR_MAP_DATA_TYPE_UINT16, K / 32, rows, K / 16, 8, TL::box_rows, false);
+    }
     if (TL::fp8) {
         *sc = CUtensorMap{};
         return map_rows(w, wt.w, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, rows, K, 128, TL::box_rows, true);
@@ -499,6 +559,7 @@ cudaError_t set_smem(size_t bytes) {
 bool stream_supported(int wfmt, int64_t d, int64_t ffn) {
     if (wfmt == WF_Q4) return d % 256 == 0 && ffn % 256 == 0;
     if (wfmt == WF_FP8) return d % 128 == 0 && ffn % 128 == 0;
+    if (wfmt == WF_Q8) return d % 256 == 0 && ffn % 256 == 0;
     return d % 8 == 0 && ffn % 8 == 0;
 }
 
@@ -575,15 +636,26 @@ cudaError_t launch_stream_down(GemvWeights wd, const void *hfrag, const void *hf
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-// Down-projection splits for the streaming kernel: at most ~600 CTAs of 64
-// rows, i.e. one wave at four CTAs per SM on a 152-SM part, never finer than
-// one k-block.  A function of the shape alone, so workspace queries agree
-// with launches.
+// Down-projection CTAs that fit in one wave: the CTAs per SM that the
+// format's ring allows (its shared memory plus ~3 KB of static and reserved
+// shared memory, out of 228 KB) times 152 SMs, less a small margin.
+template <int WF>
+constexpr int64_t down_cta_budget() {
+    constexpr size_t per_cta = Tile<WF, ROLE_DOWN, 1, false>::smem_bytes + 3 * 1024;
+    return 152 * static_cast<int64_t>((228 * 1024) / per_cta) - 8;
+}
+
+// Down-projection splits for the streaming kernel: at most one wave of CTAs
+// of 64 rows (600 with the four CTAs per SM of most formats, 448 for Q8_0's
+// larger ring), never finer than one k-block.  A function of the shape
+// alone, so workspace queries agree with launches.
 int64_t stream_down_splits(int wfmt, int64_t d, int64_t ffn) {
     const int64_t groups = cdiv(d, 64);
-    const int64_t kb = wfmt == WF_Q4 ? 256 : wfmt == WF_FP8 ? 128 : 64;
+    const int64_t kb = (wfmt == WF_Q4 || wfmt == WF_Q8) ? 256 : wfmt == WF_FP8 ? 128 : 64;
     const int64_t nkb = cdiv(ffn, kb);
-    int64_t splits = 600 / groups;
+    const int64_t budget = wfmt == WF_Q8 ? down_cta_budget<WF_Q8>() : wfmt == WF_Q4 ? down_cta_budget<WF_Q4>()
+                         : wfmt == WF_FP8 ? down_cta_budget<WF_FP8>() : down_cta_budget<WF_BF16>();
+    int64_t splits = budget / groups;
     if (splits < 1) splits = 1;
     if (splits > nkb) splits = nkb;
     return cdiv(nkb, cdiv(nkb, splits));   // the splits the kernel will actually run
@@ -611,6 +683,8 @@ FFN_STREAM_INSTANTIATE(WF_F16P, 1, false)
 FFN_STREAM_INSTANTIATE(WF_F16P, 2, false)
 FFN_STREAM_INSTANTIATE(WF_FP8, 1, false)
 FFN_STREAM_INSTANTIATE(WF_FP8, 2, false)
+FFN_STREAM_INSTANTIATE(WF_Q8, 1, false)
+FFN_STREAM_INSTANTIATE(WF_Q8, 2, false)
 #undef FFN_STREAM_INSTANTIATE
 
 }  // namespace gemv

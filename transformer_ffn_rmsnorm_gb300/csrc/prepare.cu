@@ -119,6 +119,34 @@ __global__ void __launch_bounds__(256) prepare_q4_kernel(const uint8_t *__restri
     if (bad) atomicOr(status, DEVERR_RANGE);
 }
 
+// Q8_0 codes [rows x cols] with fp16 scales per 32: w = q * s.  q * s * 2^8
+// (8 + 11 significant bits) is exact in fp32, so each output is one rounding.
+// One thread per 16 codes (cols % 32 == 0).
+__global__ void __launch_bounds__(256) prepare_q8_kernel(const int8_t *__restrict__ codes,
+                                                         const uint16_t *__restrict__ sc, __half *__restrict__ dst,
+                                                         int64_t rows, int64_t cols, unsigned *status) {
+    const int64_t nvec = rows * (cols / 16);
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    bool bad = false;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nvec; i += stride) {
+        // 16 codes of one block: element 16 i is column (16 i) % cols of row (16 i) / cols
+        const float s = __half2float(__ushort_as_half(sc[(16 * i) / 32])) * kPreparedScale;
+        const uint4 c = __ldcs(reinterpret_cast<const uint4 *>(codes) + i);
+        const int8_t *q = reinterpret_cast<const int8_t *>(&c);
+        uint32_t out[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const __half2 o = __floats2half2_rn(static_cast<float>(q[2 * k]) * s, static_cast<float>(q[2 * k + 1]) * s);
+            bad |= isfinite(s) && (!isfinite(__low2float(o)) || !isfinite(__high2float(o)));
+            out[k] = *reinterpret_cast<const uint32_t *>(&o);
+        }
+        uint4 *d = reinterpret_cast<uint4 *>(dst) + 2 * i;
+        __stcs(d, make_uint4(out[0], out[1], out[2], out[3]));
+        __stcs(d + 1, make_uint4(out[4], out[5], out[6], out[7]));
+    }
+    if (bad) atomicOr(status, DEVERR_RANGE);
+}
+
 int64_t prepare_grid(int64_t units) {
     int64_t blocks = static_cast<int64_t>(sm_count()) * 8;
     const int64_t need = (units + 255) / 256;
@@ -146,6 +174,17 @@ cudaError_t launch_prepare_q4(const uint8_t *qs, const uint16_t *scales, void *d
     LaunchScope scope(K_PREPARE, s);
     prepare_q4_kernel<<<static_cast<unsigned>(prepare_grid(rows * (cols / 128))), 256, 0, s>>>(
         qs, scales, static_cast<__half *>(dst), rows, cols, status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_prepare_q8(const int8_t *codes, const uint16_t *scales, void *dst, int64_t rows, int64_t cols,
+                              cudaStream_t s) {
+    if (rows <= 0 || cols <= 0) return cudaSuccess;
+    unsigned *status = device_status_word();
+    if (!status) return cudaErrorUnknown;
+    LaunchScope scope(K_PREPARE, s);
+    prepare_q8_kernel<<<static_cast<unsigned>(prepare_grid(rows * (cols / 16))), 256, 0, s>>>(
+        codes, scales, static_cast<__half *>(dst), rows, cols, status);
     return cudaGetLastError();
 }
 

@@ -17,7 +17,8 @@ import torch
 from . import _lib
 from ._lib import (FFN_AUTO, FFN_BF16, FFN_F16, FFN_F32, FFN_GATEUP_FUSED,  # noqa: F401
                    FFN_GATEUP_UNFUSED, FFN_ACT_SINGLE, FFN_ACT_SPLIT, FFN_PATH_GEMM,
-                   FFN_PATH_GEMV, FFN_PREPARED_WEIGHTS, FFN_RESIDUAL, Fp8Weight, Q4Weight)
+                   FFN_PATH_GEMV, FFN_PREPARED_WEIGHTS, FFN_RESIDUAL, Fp8Weight, Q4Weight,
+                   Q8Weight)
 
 _DT = {torch.float32: FFN_F32, torch.float16: FFN_F16, torch.bfloat16: FFN_BF16}
 
@@ -226,6 +227,49 @@ def ffn_block_forward_fp8(x, g, w_gate, w_up, w_down, eps: float, flags: int = 0
                                              _ptr(y), rows, d, ffn, float(eps), flags, _ptr(ws),
                                              ws.numel(), _stream(stream)), "ffn_block_forward_fp8")
     return y
+
+
+def ffn_block_q8_workspace_bytes(rows: int, d: int, ffn: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check(_lib.load().ffn_block_q8_workspace_bytes(rows, d, ffn, ctypes.byref(out)),
+           "ffn_block_q8_workspace_bytes")
+    return out.value
+
+
+def _q8(w):
+    codes, sc = w
+    _need_cuda(codes, sc)
+    if codes.element_size() != 1 or sc.element_size() != 2:
+        raise TypeError("Q8_0 weights are (1-byte codes, 2-byte fp16 scale bits)")
+    return Q8Weight(codes.data_ptr(), sc.data_ptr())
+
+
+def ffn_block_forward_q8(x, g, w_gate, w_up, w_down, eps: float, flags: int = 0,
+                         out=None, ws: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """``w_*`` are (codes int8 [out, in], scales [out, in/32] fp16 or their
+    int16 bits) CUDA tensor pairs."""
+    _need_cuda(x, g, out, ws)
+    d = x.shape[-1]
+    rows = x.numel() // d
+    ffn = w_gate[0].shape[0]
+    y = torch.empty_like(x) if out is None else out
+    if ws is None:
+        ws = workspace(ffn_block_q8_workspace_bytes(rows, d, ffn), x.device)
+    _check(_lib.load().ffn_block_forward_q8(_ptr(x), _ptr(g), _q8(w_gate), _q8(w_up), _q8(w_down),
+                                            _ptr(y), rows, d, ffn, float(eps), flags, _ptr(ws),
+                                            ws.numel(), _stream(stream)), "ffn_block_forward_q8")
+    return y
+
+
+def ffn_prepare_weights_q8(w, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Prepared fp16 weights (values of q * s * 2^8) from a Q8_0 (codes,
+    scales) pair, for FFN_PREPARED_WEIGHTS."""
+    codes, _ = w
+    o, i = codes.shape
+    dst = torch.empty((o, i), dtype=torch.float16, device=codes.device) if out is None else out
+    _need_cuda(dst)
+    _check(_lib.load().ffn_prepare_weights_q8(_q8(w), _ptr(dst), o, i, _stream(stream)), "ffn_prepare_weights_q8")
+    return dst
 
 
 def ffn_q4_pack_host(q: np.ndarray, scales_bits: np.ndarray):
