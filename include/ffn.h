@@ -226,8 +226,8 @@ ffn_status ffn_block_fp8_workspace_bytes(int64_t rows, int64_t d, int64_t ffn, s
  * Work", section "Projection shape changes the achieved rate": the decode
  * projections are weight streams).
  *   x [rows x d] bf16, g [d] bf16, y [rows x d] bf16; w_gate/w_up are e4m3
- *   [ffn x d], w_down is e4m3 [d x ffn].  Needs d % 128 == 0 and
- *   ffn % 128 == 0 (FFN_ERR_SHAPE otherwise).  Rows are processed in groups
+ *   [ffn x d], w_down is e4m3 [d x ffn].  Needs d % 256 == 0 and
+ *   ffn % 256 == 0 (FFN_ERR_SHAPE otherwise).  Rows are processed in groups
  *   of up to 16; each group streams the weights once.  Every code is exact in
  *   fp16, so the MMAs multiply the codes themselves on fp16 operands
  *   (activations as one fp16 rounding, h stored times 2^-8) and each output

@@ -185,9 +185,9 @@ def test_fp8_entry_rejects_before_launch(lib):
     out = ctypes.c_size_t(0)
     assert lib.ffn_block_fp8_workspace_bytes(8, 4096, 14336, ctypes.byref(out)) == 0 and out.value > 0
     assert lib.ffn_block_fp8_workspace_bytes(0, 4096, 14336, ctypes.byref(out)) == 0 and out.value == 0
-    for d, f in ((4160, 14336), (4096, 14400), (64, 128), (128, 64)):   # multiples of 128 only
+    for d, f in ((4160, 14336), (4096, 14400), (4096 + 128, 14336), (128, 256), (256, 128)):   # multiples of 256
         assert lib.ffn_block_fp8_workspace_bytes(8, d, f, ctypes.byref(out)) == _lib.FFN_ERR_SHAPE
-    assert lib.ffn_block_fp8_workspace_bytes(-1, 128, 128, ctypes.byref(out)) == _lib.FFN_ERR_SHAPE
+    assert lib.ffn_block_fp8_workspace_bytes(-1, 256, 256, ctypes.byref(out)) == _lib.FFN_ERR_SHAPE
     p = [ctypes.c_void_p((i + 1) << 24) for i in range(12)]
     w = [_lib.Fp8Weight(p[2 + 2 * i].value, p[3 + 2 * i].value) for i in range(3)]
     lib.ffn_block_fp8_workspace_bytes(8, 512, 1024, ctypes.byref(out))

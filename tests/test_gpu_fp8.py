@@ -36,7 +36,7 @@ def test_fp8_rows(ffn, oracle_lib, rows):
     assert_lowp(to_host64(run_fp8(ffn, inp)), oracle_lib.fp8_block_from_inputs(inp))
 
 
-@pytest.mark.parametrize("d,ffn_", [(128, 128), (384, 640), (4096, 2176), (1152, 11008)])
+@pytest.mark.parametrize("d,ffn_", [(256, 256), (768, 1280), (4096, 2304), (1280, 11008)])
 def test_fp8_shapes(ffn, oracle_lib, d, ffn_):
     """One k-block, odd numbers of k-blocks and of 64-row groups, one split."""
     inp = synth.make_fp8_inputs(synth.C6_DECODE_FP8, seed=d, rows=4, d=d, ffn=ffn_)
@@ -110,7 +110,7 @@ def test_fp8_deterministic(ffn):
 
 def test_fp8_rejects_float8_dtype_mismatch(ffn):
     import torch
-    inp = synth.make_fp8_inputs(synth.C6_DECODE_FP8, seed=3, rows=2, d=128, ffn=128)
+    inp = synth.make_fp8_inputs(synth.C6_DECODE_FP8, seed=3, rows=2, d=256, ffn=256)
     c, s = fp8_dev(inp, "gate")
     with pytest.raises(TypeError):
         ffn.ffn_block_forward_fp8(to_dev(inp["x"], "bf16"), to_dev(inp["g"], "bf16"), (c, s.double()),

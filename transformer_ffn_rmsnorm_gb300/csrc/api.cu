@@ -405,7 +405,7 @@ ffn_status ffn_block_forward_q4(const void *x, const void *g, ffn_q4_weight w_ga
 
 ffn_status ffn_block_fp8_workspace_bytes(int64_t rows, int64_t d, int64_t ffn, size_t *bytes) {
     if (!bytes) return FFN_ERR_NULL;
-    if (rows < 0 || d < 128 || ffn < 128 || d % 128 || ffn % 128) return FFN_ERR_SHAPE;
+    if (rows < 0 || d < 256 || ffn < 256 || d % 256 || ffn % 256) return FFN_ERR_SHAPE;
     if (rows > INT32_MAX || d > INT32_MAX || ffn > INT32_MAX) return FFN_ERR_SHAPE;
     *bytes = rows == 0 ? 0 : gemv_workspace_bytes(std::min<int64_t>(rows, kGemvMaxRows), d, ffn, false);
     return FFN_OK;

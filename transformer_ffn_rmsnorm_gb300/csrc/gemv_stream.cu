@@ -6,10 +6,10 @@
 // then issues the next burst, so HBM idles between bursts (ncu: stalled on
 // the long scoreboard, 1.6-4.4 TB/s).  Here one producer thread per CTA keeps
 // a 6-stage shared-memory ring full with TMA bulk tensor copies of 64 weight
-// rows x one k-block (16-bit: 64 values, 128 bytes a row; Q4: 256 values,
-// 128 bytes of nibbles plus 16 bytes of fp16 scales a row; e4m3: 128 codes,
-// 128 bytes a row; Q8_0: 256 codes in two 128-byte boxes plus 16 bytes of
-// scales a row), 128-byte swizzled, plus -- by 1-D bulk copies -- the pre-arranged activation
+// rows x one k-block (16-bit: 128 values in two 128-byte boxes a row; Q4: 256 values,
+// 128 bytes of nibbles plus 16 bytes of fp16 scales a row; e4m3: 256 codes
+// in two 128-byte boxes a row; Q8_0: the same plus 16 bytes of scales a
+// row), 128-byte swizzled, plus -- by 1-D bulk copies -- the pre-arranged activation
 // fragments of the same k range, while four MMA warps read everything from
 // shared memory.  (Reading the activations through L1 instead stalls: the
 // rings leave too little L1 to hold them.)
@@ -52,12 +52,14 @@ template <int WF, int ROLE, int NT, bool TWO> struct Tile {
     static constexpr bool blocks = q4 || q8;                     // fp16 scales per 32 weights
     static constexpr int nmat = ROLE == ROLE_GATEUP ? 2 : 1;     // weight matrices per stage
     static constexpr int box_rows = ROLE == ROLE_GATEUP ? 32 : 64;
-    static constexpr int kb = (q4 || q8) ? 256 : fp8 ? 128 : 64; // k values per stage
-    static constexpr int x_per_kb = q8 ? 256 : (q4 || fp8) ? 128 : 64;   // TMA inner coordinate per stage
+    static constexpr int boxes = q4 ? 1 : 2;                     // 128-byte boxes per row and stage
+    static constexpr int box_x = (q8 || fp8) ? 128 : 64;         // TMA inner coordinate per box (bytes / elements)
+    static constexpr int kb = (q4 || q8 || fp8) ? 256 : 128;    // k values per stage
+    static constexpr int x_per_kb = q4 ? 128 : boxes * box_x;   // TMA inner coordinate per stage
     static constexpr int chunks = kb / kChunk;                   // fragment chunks per stage
     static constexpr int terms = TWO ? 2 : 1;
     static constexpr uint32_t box_bytes = box_rows * 128;        // one 128-byte-wide TMA box
-    static constexpr uint32_t w_bytes = (q8 ? 2 : 1) * box_bytes;   // one matrix' rows of a stage
+    static constexpr uint32_t w_bytes = boxes * box_bytes;       // one matrix' rows of a stage
     static constexpr uint32_t s_bytes = blocks ? box_rows * 16 : 0; // its scales
     static constexpr uint32_t b_off = nmat * (w_bytes + s_bytes);
     static constexpr uint32_t b_bytes = NT * terms * chunks * kFragBytes;
@@ -166,9 +168,10 @@ __global__ void __launch_bounds__(kThreads) gemv_stream_kernel(
                 const int y = static_cast<int>(row0);
                 ptx::tma_load_2d(st, &map_w0, bar, x, y);
                 if (TL::nmat == 2) ptx::tma_load_2d(st + TL::w_bytes, &map_w1, bar, x, y);
-                if (TL::q8) {   // the second 128 codes of each row
-                    ptx::tma_load_2d(st + TL::box_bytes, &map_w0, bar, x + 128, y);
-                    if (TL::nmat == 2) ptx::tma_load_2d(st + TL::w_bytes + TL::box_bytes, &map_w1, bar, x + 128, y);
+                if (TL::boxes == 2) {   // the second 128 bytes of each row
+                    ptx::tma_load_2d(st + TL::box_bytes, &map_w0, bar, x + TL::box_x, y);
+                    if (TL::nmat == 2)
+                        ptx::tma_load_2d(st + TL::w_bytes + TL::box_bytes, &map_w1, bar, x + TL::box_x, y);
                 }
                 if (TL::blocks) {
                     const uint32_t sc = st + TL::nmat * TL::w_bytes;
@@ -241,21 +244,23 @@ __global__ void __launch_bounds__(kThreads) gemv_stream_kernel(
             }
             const uint32_t wbase = base + s * TL::stage_bytes + mat * TL::w_bytes;
             if constexpr (fp8) {
-                // 128 k = two groups of 64; in each, this lane's 16 codes of
-                // rows ra and rb (k = 16 tid .. 16 tid + 15) feed four MMAs,
-                // four k each, against the group's two fragment chunks
+                // 256 k = four groups of 64, two in each 128-byte box of a row; in
+                // each, this lane's 16 codes of rows ra and rb (k = 16 tid .. 16
+                // tid + 15) feed four MMAs, four k each, against the group's two
+                // fragment chunks
                 const uint32_t bbase = base + s * TL::stage_bytes + TL::b_off + lane * 16;
 #pragma unroll
-                for (int grp = 0; grp < 2; ++grp) {
+                for (int grp = 0; grp < 4; ++grp) {
                     uint4 b0[NT], b1[NT];
 #pragma unroll
                     for (int n = 0; n < NT; ++n) {
                         b0[n] = lds128(bbase + (n * TL::chunks + 2 * grp) * kFragBytes);
                         b1[n] = lds128(bbase + (n * TL::chunks + 2 * grp + 1) * kFragBytes);
                     }
-                    const uint32_t off = static_cast<uint32_t>(((4 * grp + tid) ^ g) << 4);
-                    const uint4 qa = lds128(wbase + ra * 128 + off);
-                    const uint4 qb = lds128(wbase + rb * 128 + off);
+                    const uint32_t box = wbase + static_cast<uint32_t>(grp >> 1) * TL::box_bytes;
+                    const uint32_t off = static_cast<uint32_t>(((4 * (grp & 1) + tid) ^ g) << 4);
+                    const uint4 qa = lds128(box + ra * 128 + off);
+                    const uint4 qb = lds128(box + rb * 128 + off);
 #pragma unroll
                     for (int m = 0; m < 4; ++m) {
                         const uint32_t wa = word_of(qa, m), wb = word_of(qb, m);
@@ -312,15 +317,16 @@ __global__ void __launch_bounds__(kThreads) gemv_stream_kernel(
                     }
                 }
             } else if constexpr (!q4) {
-                // two 32-wide chunks: this lane's 16 bytes of rows ra, rb at chunk 4j + tid
+                // 32-wide chunks, two in each 128-byte box of a row: this lane's 16
+                // bytes of rows ra, rb at granule 4 (j % 2) + tid of box j / 2
                 const uint32_t bbase = base + s * TL::stage_bytes + TL::b_off + lane * 16;
 #pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    const int64_t c = kb * 2 + j;
+                for (int j = 0; j < TL::chunks; ++j) {
+                    const int64_t c = kb * TL::chunks + j;
                     uint4 b[NT], bl[TWO ? NT : 1];
-                    // a 64-wide k-block can run one chunk past the fragment
-                    // buffer when it holds an odd number of chunks; the
-                    // weights there are TMA zero fill, the operand must be 0
+                    // the last k-block can run past the fragment buffer (K a
+                    // multiple of 8 only); the weights there are TMA zero fill,
+                    // the operand must be 0
                     const bool cin = c < p.nch_b;
 #pragma unroll
                     for (int n = 0; n < NT; ++n) {
@@ -330,9 +336,10 @@ __global__ void __launch_bounds__(kThreads) gemv_stream_kernel(
                             bl[n] = cin ? lds128(bbase + ((n * TL::terms + 1) * TL::chunks + j) * kFragBytes)
                                         : make_uint4(0, 0, 0, 0);
                     }
-                    const uint32_t off = static_cast<uint32_t>(((4 * j + tid) ^ g) << 4);
-                    const uint4 a0 = lds128(wbase + ra * 128 + off);
-                    const uint4 a1 = lds128(wbase + rb * 128 + off);
+                    const uint32_t box = wbase + static_cast<uint32_t>(j >> 1) * TL::box_bytes;
+                    const uint32_t off = static_cast<uint32_t>(((4 * (j & 1) + tid) ^ g) << 4);
+                    const uint4 a0 = lds128(box + ra * 128 + off);
+                    const uint4 a1 = lds128(box + rb * 128 + off);
 #pragma unroll
                     for (int n = 0; n < NT; ++n) {
                         ptx::mma_16816<bf>(acc[n], a0.x, a1.x, a0.y, a1.y, b[n].x, b[n].y);
@@ -558,7 +565,7 @@ cudaError_t set_smem(size_t bytes) {
 
 bool stream_supported(int wfmt, int64_t d, int64_t ffn) {
     if (wfmt == WF_Q4) return d % 256 == 0 && ffn % 256 == 0;
-    if (wfmt == WF_FP8) return d % 128 == 0 && ffn % 128 == 0;
+    if (wfmt == WF_FP8) return d % 256 == 0 && ffn % 256 == 0;
     if (wfmt == WF_Q8) return d % 256 == 0 && ffn % 256 == 0;
     return d % 8 == 0 && ffn % 8 == 0;
 }
@@ -651,7 +658,7 @@ constexpr int64_t down_cta_budget() {
 // alone, so workspace queries agree with launches.
 int64_t stream_down_splits(int wfmt, int64_t d, int64_t ffn) {
     const int64_t groups = cdiv(d, 64);
-    const int64_t kb = (wfmt == WF_Q4 || wfmt == WF_Q8) ? 256 : wfmt == WF_FP8 ? 128 : 64;
+    const int64_t kb = (wfmt == WF_Q4 || wfmt == WF_Q8 || wfmt == WF_FP8) ? 256 : 128;
     const int64_t nkb = cdiv(ffn, kb);
     const int64_t budget = wfmt == WF_Q8 ? down_cta_budget<WF_Q8>() : wfmt == WF_Q4 ? down_cta_budget<WF_Q4>()
                          : wfmt == WF_FP8 ? down_cta_budget<WF_FP8>() : down_cta_budget<WF_BF16>();
