@@ -427,6 +427,23 @@ def cpu_oracle_rate(inp, rows_per_step: int, steps: int, warmup: int = 0, seed: 
     return rows_per_step * steps / dt_s, dt_s, threads
 
 
+def sampled_parity(torch, ffn, inp, step, y, rows: int = 32, seed: int = 1):
+    """The timed path's y on sampled token rows against the oracle (rows are
+    independent): max and mean |y - y_oracle| over rms(y_oracle)."""
+    import oracle
+    step(0)
+    torch.cuda.synchronize()
+    ffn.ffn_device_status()
+    M = inp["cfg"].rows
+    r = np.sort(np.random.default_rng(seed).choice(M, rows, replace=False))
+    got = oracle.widen(y[torch.from_numpy(r).to(y.device)].view(torch.int16).cpu().numpy().view(np.uint16), "bf16")
+    ref = oracle.get().block_from_inputs(inp, rows=r)
+    rms = float(np.sqrt(np.mean(ref * ref)))
+    diff = np.abs(got - ref)
+    return {"rows": rows, "max_abs_over_rms": float(diff.max() / rms), "mean_abs_over_rms": float(diff.mean() / rms),
+            "bound": {"max": 2e-2, "mean": 4e-3}, "against": "float64 oracle on the same sampled rows"}
+
+
 # ------------------------------------------------------------------- main
 def dist_init():
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -605,11 +622,13 @@ def run_ours(args):
         sub = sub_benchmarks(torch, ffn, device, peaks, peak_src, stream)
 
     cpu = None
+    parity = None
     if not args.no_cpu and not args.only_main and rank == 0:
         rows_sample = 32
         rate, secs, threads = cpu_oracle_rate(inp, rows_sample, 2, 0)
         cpu = {"value": round(rate, 3), "unit": "tokens/s", "cores": threads, "kind": "oracle",
                "sample": f"2 x {rows_sample} random token rows of the {cfg.rows}-row batch ({secs:.1f} s wall)"}
+        parity = sampled_parity(torch, ffn, inp, step, y)
 
     if rank == 0:
         line = {
@@ -631,7 +650,7 @@ def run_ours(args):
                     "h2d_bytes_per_step": cfg.rows * cfg.d * 2, "d2h_bytes_per_step": cfg.rows * cfg.d * 2,
                     "path": "ffn_block_forward_host (C ABI; pinned host x and y; copies overlapped with the "
                             "compute in 1024-row chunks)"},
-            "cpu_baseline": cpu, "sub": sub,
+            "cpu_baseline": cpu, "parity": parity, "sub": sub,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
