@@ -84,7 +84,8 @@ def test_workspace_query(lib):
     assert _ws(lib, 4, 4096, 11008, _lib.FFN_F32, _lib.FFN_PATH_GEMM)[0] == _lib.FFN_ERR_FLAGS
     assert _ws(lib, 4, 4096, 11008, _lib.FFN_BF16, 3)[0] == _lib.FFN_ERR_FLAGS      # fused+unfused
     assert _ws(lib, 4, 4096, 11008, _lib.FFN_BF16, 1 << 20)[0] == _lib.FFN_ERR_FLAGS
-    assert _ws(lib, 17, 4096, 11008, _lib.FFN_BF16, _lib.FFN_PATH_GEMV)[0] == _lib.FFN_ERR_SHAPE
+    assert _ws(lib, 65, 4096, 11008, _lib.FFN_BF16, _lib.FFN_PATH_GEMV)[0] == _lib.FFN_ERR_SHAPE
+    assert _ws(lib, 64, 4096, 11008, _lib.FFN_BF16, _lib.FFN_PATH_GEMV)[0] == 0
     out = ctypes.c_size_t(0)
     assert lib.ffn_block_q4_workspace_bytes(8, 5120, 17408, ctypes.byref(out)) == 0 and out.value > 0
     assert lib.ffn_block_q4_workspace_bytes(8, 5000, 17408, ctypes.byref(out)) == _lib.FFN_ERR_SHAPE

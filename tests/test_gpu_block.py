@@ -54,6 +54,31 @@ def test_decode_rows(ffn, oracle_lib, rows, dtype):
     assert_lowp(to_host64(y), oracle_lib.block_from_inputs(inp))
 
 
+@pytest.mark.parametrize("rows", [17, 24, 32, 33, 47, 64])
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_decode_batched_rows(ffn, oracle_lib, rows, dtype):
+    """17 to 64 rows: four and eight token tiles on the weight-streaming
+    kernels (ragged last tiles included)."""
+    cfg = synth.BlockConfig("t", rows, 1024, 2816, 1e-5, dtype)
+    inp = synth.make_block_inputs(cfg, seed=200 + rows)
+    assert_lowp(to_host64(run_block(ffn, inp)), oracle_lib.block_from_inputs(inp))
+
+
+@pytest.mark.parametrize("rows", [24, 64])
+def test_decode_batched_prepared_and_residual(ffn, oracle_lib, rows):
+    cfg = synth.BlockConfig("t", rows, 2048, 5632, 1e-5, "bf16")
+    inp = synth.make_block_inputs(cfg, seed=300 + rows)
+    x, g = to_dev(inp["x"], "bf16"), to_dev(inp["g"], "bf16")
+    w = [ffn.ffn_prepare_weights(to_dev(inp[k], "bf16")) for k in ("w_gate", "w_up", "w_down")]
+    P, R = ffn.FFN_PREPARED_WEIGHTS, ffn.FFN_RESIDUAL
+    assert_lowp(to_host64(ffn.ffn_block_forward(x, g, *w, eps=cfg.eps, flags=P)), oracle_lib.block_from_inputs(inp))
+    y = ffn.ffn_block_forward(x, g, *w, eps=cfg.eps, flags=P | R)
+    assert_lowp(to_host64(y), oracle_lib.block_from_inputs(inp, residual=True))
+    # the same rows forced through the tensor-core GEMMs agree within the bound
+    yg = ffn.ffn_block_forward(x, g, *w, eps=cfg.eps, flags=P | ffn.FFN_PATH_GEMM)
+    assert_lowp(to_host64(yg), oracle_lib.block_from_inputs(inp))
+
+
 @pytest.mark.parametrize("d,ffn_", [(264, 200), (8, 8), (520, 4104), (2048, 2056)])
 def test_decode_ragged_k(ffn, oracle_lib, d, ffn_):
     """Reduction lengths that are not multiples of 32, feature counts that are

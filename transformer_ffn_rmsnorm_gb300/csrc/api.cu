@@ -22,7 +22,10 @@ __device__ unsigned g_ffn_status_word;
 namespace ffn {
 namespace {
 
-constexpr int64_t kGemvMaxRows = 16;
+// rows up to which the block runs on the weight-streaming (decode) kernels;
+// the quantised entries run their rows in groups of kQuantGroupRows
+constexpr int64_t kGemvMaxRows = 64;
+constexpr int64_t kQuantGroupRows = 16;
 constexpr int kMaxDevices = 64;
 
 std::atomic<uint64_t> g_launch_count{0};
@@ -354,7 +357,7 @@ ffn_status ffn_block_q4_workspace_bytes(int64_t rows, int64_t d, int64_t ffn, si
     if (!bytes) return FFN_ERR_NULL;
     if (rows < 0 || d < 128 || ffn < 128 || d % 128 || ffn % 128) return FFN_ERR_SHAPE;
     if (rows > INT32_MAX || d > INT32_MAX || ffn > INT32_MAX) return FFN_ERR_SHAPE;
-    *bytes = rows == 0 ? 0 : gemv_workspace_bytes(std::min<int64_t>(rows, kGemvMaxRows), d, ffn, false);
+    *bytes = rows == 0 ? 0 : gemv_workspace_bytes(std::min<int64_t>(rows, kQuantGroupRows), d, ffn, false);
     return FFN_OK;
 }
 
@@ -387,13 +390,13 @@ ffn_status ffn_block_forward_q4(const void *x, const void *g, ffn_q4_weight w_ga
     if (rows == 0) return FFN_OK;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const int64_t grp = std::min<int64_t>(rows, kGemvMaxRows);
+    const int64_t grp = std::min<int64_t>(rows, kQuantGroupRows);
     GemvWorkspace gw;
     gemv_carve(workspace, grp, d, ffn, false, &gw);
     GemvWeights a{nullptr, w_gate.qs, w_gate.scales}, b{nullptr, w_up.qs, w_up.scales},
         c{nullptr, w_down.qs, w_down.scales};
-    for (int64_t r0 = 0; r0 < rows; r0 += kGemvMaxRows) {
-        const int64_t nr = std::min<int64_t>(kGemvMaxRows, rows - r0);
+    for (int64_t r0 = 0; r0 < rows; r0 += kQuantGroupRows) {
+        const int64_t nr = std::min<int64_t>(kQuantGroupRows, rows - r0);
         const char *xr = static_cast<const char *>(x) + r0 * d * 2;
         char *yr = static_cast<char *>(y) + r0 * d * 2;
         cudaError_t e = launch_gemv_block(WF_Q4, xr, g, a, b, c, yr, nr, d, ffn, eps, gw, s,
@@ -407,7 +410,7 @@ ffn_status ffn_block_fp8_workspace_bytes(int64_t rows, int64_t d, int64_t ffn, s
     if (!bytes) return FFN_ERR_NULL;
     if (rows < 0 || d < 256 || ffn < 256 || d % 256 || ffn % 256) return FFN_ERR_SHAPE;
     if (rows > INT32_MAX || d > INT32_MAX || ffn > INT32_MAX) return FFN_ERR_SHAPE;
-    *bytes = rows == 0 ? 0 : gemv_workspace_bytes(std::min<int64_t>(rows, kGemvMaxRows), d, ffn, false);
+    *bytes = rows == 0 ? 0 : gemv_workspace_bytes(std::min<int64_t>(rows, kQuantGroupRows), d, ffn, false);
     return FFN_OK;
 }
 
@@ -441,13 +444,13 @@ ffn_status ffn_block_forward_fp8(const void *x, const void *g, ffn_fp8_weight w_
     if (rows == 0) return FFN_OK;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const int64_t grp = std::min<int64_t>(rows, kGemvMaxRows);
+    const int64_t grp = std::min<int64_t>(rows, kQuantGroupRows);
     GemvWorkspace gw;
     gemv_carve(workspace, grp, d, ffn, false, &gw);
     GemvWeights a{w_gate.codes, nullptr, nullptr, w_gate.scales}, b{w_up.codes, nullptr, nullptr, w_up.scales},
         c{w_down.codes, nullptr, nullptr, w_down.scales};
-    for (int64_t r0 = 0; r0 < rows; r0 += kGemvMaxRows) {
-        const int64_t nr = std::min<int64_t>(kGemvMaxRows, rows - r0);
+    for (int64_t r0 = 0; r0 < rows; r0 += kQuantGroupRows) {
+        const int64_t nr = std::min<int64_t>(kQuantGroupRows, rows - r0);
         const char *xr = static_cast<const char *>(x) + r0 * d * 2;
         char *yr = static_cast<char *>(y) + r0 * d * 2;
         cudaError_t e = launch_gemv_block(WF_FP8, xr, g, a, b, c, yr, nr, d, ffn, eps, gw, s,
@@ -461,7 +464,7 @@ ffn_status ffn_block_q8_workspace_bytes(int64_t rows, int64_t d, int64_t ffn, si
     if (!bytes) return FFN_ERR_NULL;
     if (rows < 0 || d < 256 || ffn < 256 || d % 256 || ffn % 256) return FFN_ERR_SHAPE;
     if (rows > INT32_MAX || d > INT32_MAX || ffn > INT32_MAX) return FFN_ERR_SHAPE;
-    *bytes = rows == 0 ? 0 : gemv_workspace_bytes(std::min<int64_t>(rows, kGemvMaxRows), d, ffn, false);
+    *bytes = rows == 0 ? 0 : gemv_workspace_bytes(std::min<int64_t>(rows, kQuantGroupRows), d, ffn, false);
     return FFN_OK;
 }
 
@@ -494,13 +497,13 @@ ffn_status ffn_block_forward_q8(const void *x, const void *g, ffn_q8_weight w_ga
     if (rows == 0) return FFN_OK;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const int64_t grp = std::min<int64_t>(rows, kGemvMaxRows);
+    const int64_t grp = std::min<int64_t>(rows, kQuantGroupRows);
     GemvWorkspace gw;
     gemv_carve(workspace, grp, d, ffn, false, &gw);
     GemvWeights a{w_gate.codes, nullptr, w_gate.scales}, b{w_up.codes, nullptr, w_up.scales},
         c{w_down.codes, nullptr, w_down.scales};
-    for (int64_t r0 = 0; r0 < rows; r0 += kGemvMaxRows) {
-        const int64_t nr = std::min<int64_t>(kGemvMaxRows, rows - r0);
+    for (int64_t r0 = 0; r0 < rows; r0 += kQuantGroupRows) {
+        const int64_t nr = std::min<int64_t>(kQuantGroupRows, rows - r0);
         const char *xr = static_cast<const char *>(x) + r0 * d * 2;
         char *yr = static_cast<char *>(y) + r0 * d * 2;
         cudaError_t e = launch_gemv_block(WF_Q8, xr, g, a, b, c, yr, nr, d, ffn, eps, gw, s,

@@ -427,7 +427,7 @@ struct Geometry {
 
 Geometry geometry(int64_t rows, int64_t d, int64_t ffn, bool q4) {
     Geometry g;
-    g.nt = rows > 8 ? 2 : 1;
+    g.nt = rows <= 8 ? 1 : rows <= 16 ? 2 : rows <= 32 ? 4 : 8;   // token tiles of 8 (16-bit weights: up to 8)
     g.nchK = cdiv(d, kChunk);
     g.nchF = cdiv(ffn, kChunk);
     g.ups = q4 ? kSplitK / 128 : kSplitK / kChunk;
@@ -461,8 +461,10 @@ cudaError_t launch_typed(const void *x, const void *gain, GemvWeights wg, GemvWe
         return launch_stream_down<WF, NT, TWO>(wd, ws.hfrag, ws.hfrag_lo, y, ws.partials, ws.counters, rows, d,
                                                ffn, geo.nchF, stream_down_splits(WF, d, ffn), res, s);
     }
-    if constexpr (WF == WF_FP8 || WF == WF_Q8) {
-        return cudaErrorInvalidValue;   // e4m3 and Q8_0 weights stream through the TMA kernels only
+    if constexpr (WF == WF_FP8 || WF == WF_Q8 || NT > 2) {
+        // e4m3 and Q8_0 weights, and more than two token tiles, stream through
+        // the TMA kernels only
+        return cudaErrorInvalidValue;
     } else {
         {
             const int64_t tiles = 2 * geo.nchF;  // covers every fragment slot of h
@@ -491,8 +493,14 @@ template <int WF, bool TWO>
 cudaError_t launch_nt(int nt, const void *x, const void *g, GemvWeights wg, GemvWeights wu,
                       GemvWeights wd, void *y, int rows, int64_t d, int64_t ffn, float eps,
                       const GemvWorkspace &ws, const Geometry &geo, cudaStream_t s, const void *res) {
-    return nt == 1 ? launch_typed<WF, 1, TWO>(x, g, wg, wu, wd, y, rows, d, ffn, eps, ws, geo, s, res)
-                   : launch_typed<WF, 2, TWO>(x, g, wg, wu, wd, y, rows, d, ffn, eps, ws, geo, s, res);
+    if (nt == 1) return launch_typed<WF, 1, TWO>(x, g, wg, wu, wd, y, rows, d, ffn, eps, ws, geo, s, res);
+    if (nt == 2) return launch_typed<WF, 2, TWO>(x, g, wg, wu, wd, y, rows, d, ffn, eps, ws, geo, s, res);
+    // 17 to 64 rows: 16-bit weights only (the quantised entries go in groups of 16)
+    if constexpr (WF == WF_F16 || WF == WF_BF16 || WF == WF_F16P) {
+        if (nt == 4) return launch_typed<WF, 4, TWO>(x, g, wg, wu, wd, y, rows, d, ffn, eps, ws, geo, s, res);
+        return launch_typed<WF, 8, TWO>(x, g, wg, wu, wd, y, rows, d, ffn, eps, ws, geo, s, res);
+    }
+    return cudaErrorInvalidValue;
 }
 
 struct Layout {
@@ -510,7 +518,7 @@ Layout layout(int64_t rows, int64_t d, int64_t ffn) {
     Layout l;
     l.frag_n = align256(static_cast<size_t>(a.nt) * a.nchK * 32 * 16);
     l.frag_h = align256(static_cast<size_t>(a.nt) * a.nchF * 32 * 16);
-    l.partials = align256(static_cast<size_t>(splits) * (rows > 16 ? 16 : rows) * d * 4);
+    l.partials = align256(static_cast<size_t>(splits) * (rows > 64 ? 64 : rows) * d * 4);
     l.counters = align256(static_cast<size_t>(a.groups) * 4);
     return l;
 }

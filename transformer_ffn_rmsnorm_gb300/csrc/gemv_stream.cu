@@ -52,9 +52,12 @@ template <int WF, int ROLE, int NT, bool TWO> struct Tile {
     static constexpr bool blocks = q4 || q8;                     // fp16 scales per 32 weights
     static constexpr int nmat = ROLE == ROLE_GATEUP ? 2 : 1;     // weight matrices per stage
     static constexpr int box_rows = ROLE == ROLE_GATEUP ? 32 : 64;
-    static constexpr int boxes = q4 ? 1 : 2;                     // 128-byte boxes per row and stage
+    // 128-byte boxes per row and stage: two, but one for Q4 (its 128 bytes
+    // hold 256 weights) and for four or more token tiles, whose activation
+    // fragments would otherwise outgrow the weights in the stage
+    static constexpr int boxes = (q4 || (NT >= 4 && !q8)) ? 1 : 2;
     static constexpr int box_x = (q8 || fp8) ? 128 : 64;         // TMA inner coordinate per box (bytes / elements)
-    static constexpr int kb = (q4 || q8 || fp8) ? 256 : 128;    // k values per stage
+    static constexpr int kb = (q4 || q8) ? 256 : boxes * box_x;  // k values per stage
     static constexpr int x_per_kb = q4 ? 128 : boxes * box_x;   // TMA inner coordinate per stage
     static constexpr int chunks = kb / kChunk;                   // fragment chunks per stage
     static constexpr int terms = TWO ? 2 : 1;
@@ -65,7 +68,9 @@ template <int WF, int ROLE, int NT, bool TWO> struct Tile {
     static constexpr uint32_t b_bytes = NT * terms * chunks * kFragBytes;
     static constexpr uint32_t stage_bytes = (b_off + b_bytes + 1023) & ~1023u;
     static constexpr int stages_fit = (52 * 1024) / stage_bytes;
-    static constexpr int stages = stages_fit < 3 ? 3 : stages_fit > 6 ? 6 : stages_fit;
+    // (large stages of many token tiles run with two, keeping three CTAs a SM)
+    static constexpr int min_stages = (NT >= 4 && stage_bytes > 20 * 1024) ? 2 : 3;
+    static constexpr int stages = stages_fit < min_stages ? min_stages : stages_fit > 6 ? 6 : stages_fit;
     static constexpr size_t smem_bytes = stages * stage_bytes + 1024;
 };
 
@@ -250,7 +255,7 @@ __global__ void __launch_bounds__(kThreads) gemv_stream_kernel(
                 // fragment chunks
                 const uint32_t bbase = base + s * TL::stage_bytes + TL::b_off + lane * 16;
 #pragma unroll
-                for (int grp = 0; grp < 4; ++grp) {
+                for (int grp = 0; grp < 2 * TL::boxes; ++grp) {
                     uint4 b0[NT], b1[NT];
 #pragma unroll
                     for (int n = 0; n < NT; ++n) {
@@ -323,30 +328,27 @@ __global__ void __launch_bounds__(kThreads) gemv_stream_kernel(
 #pragma unroll
                 for (int j = 0; j < TL::chunks; ++j) {
                     const int64_t c = kb * TL::chunks + j;
-                    uint4 b[NT], bl[TWO ? NT : 1];
                     // the last k-block can run past the fragment buffer (K a
                     // multiple of 8 only); the weights there are TMA zero fill,
                     // the operand must be 0
                     const bool cin = c < p.nch_b;
-#pragma unroll
-                    for (int n = 0; n < NT; ++n) {
-                        b[n] = cin ? lds128(bbase + ((n * TL::terms) * TL::chunks + j) * kFragBytes)
-                                   : make_uint4(0, 0, 0, 0);
-                        if constexpr (TWO)
-                            bl[n] = cin ? lds128(bbase + ((n * TL::terms + 1) * TL::chunks + j) * kFragBytes)
-                                        : make_uint4(0, 0, 0, 0);
-                    }
                     const uint32_t box = wbase + static_cast<uint32_t>(j >> 1) * TL::box_bytes;
                     const uint32_t off = static_cast<uint32_t>(((4 * (j & 1) + tid) ^ g) << 4);
                     const uint4 a0 = lds128(box + ra * 128 + off);
                     const uint4 a1 = lds128(box + rb * 128 + off);
+                    // one token tile's operand at a time (eight tiles' would
+                    // cost 64 registers)
 #pragma unroll
                     for (int n = 0; n < NT; ++n) {
-                        ptx::mma_16816<bf>(acc[n], a0.x, a1.x, a0.y, a1.y, b[n].x, b[n].y);
-                        ptx::mma_16816<bf>(acc[n], a0.z, a1.z, a0.w, a1.w, b[n].z, b[n].w);
+                        const uint4 b = cin ? lds128(bbase + ((n * TL::terms) * TL::chunks + j) * kFragBytes)
+                                            : make_uint4(0, 0, 0, 0);
+                        ptx::mma_16816<bf>(acc[n], a0.x, a1.x, a0.y, a1.y, b.x, b.y);
+                        ptx::mma_16816<bf>(acc[n], a0.z, a1.z, a0.w, a1.w, b.z, b.w);
                         if constexpr (TWO) {
-                            ptx::mma_16816<bf>(acc[n], a0.x, a1.x, a0.y, a1.y, bl[n].x, bl[n].y);
-                            ptx::mma_16816<bf>(acc[n], a0.z, a1.z, a0.w, a1.w, bl[n].z, bl[n].w);
+                            const uint4 bl = cin ? lds128(bbase + ((n * TL::terms + 1) * TL::chunks + j) * kFragBytes)
+                                                 : make_uint4(0, 0, 0, 0);
+                            ptx::mma_16816<bf>(acc[n], a0.x, a1.x, a0.y, a1.y, bl.x, bl.y);
+                            ptx::mma_16816<bf>(acc[n], a0.z, a1.z, a0.w, a1.w, bl.z, bl.w);
                         }
                     }
                 }
@@ -688,6 +690,17 @@ FFN_STREAM_INSTANTIATE(WF_Q4, 1, false)
 FFN_STREAM_INSTANTIATE(WF_Q4, 2, false)
 FFN_STREAM_INSTANTIATE(WF_F16P, 1, false)
 FFN_STREAM_INSTANTIATE(WF_F16P, 2, false)
+// four and eight token tiles (17 to 64 rows): 16-bit weights only
+FFN_STREAM_INSTANTIATE(WF_F16, 4, false)
+FFN_STREAM_INSTANTIATE(WF_F16, 8, false)
+FFN_STREAM_INSTANTIATE(WF_F16, 4, true)
+FFN_STREAM_INSTANTIATE(WF_F16, 8, true)
+FFN_STREAM_INSTANTIATE(WF_BF16, 4, false)
+FFN_STREAM_INSTANTIATE(WF_BF16, 8, false)
+FFN_STREAM_INSTANTIATE(WF_BF16, 4, true)
+FFN_STREAM_INSTANTIATE(WF_BF16, 8, true)
+FFN_STREAM_INSTANTIATE(WF_F16P, 4, false)
+FFN_STREAM_INSTANTIATE(WF_F16P, 8, false)
 FFN_STREAM_INSTANTIATE(WF_FP8, 1, false)
 FFN_STREAM_INSTANTIATE(WF_FP8, 2, false)
 FFN_STREAM_INSTANTIATE(WF_Q8, 1, false)
