@@ -56,12 +56,15 @@ def test_decode_rows(ffn, oracle_lib, rows, dtype):
 
 @pytest.mark.parametrize("rows", [17, 24, 32, 33, 47, 64])
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
-def test_decode_batched_rows(ffn, oracle_lib, rows, dtype):
+@pytest.mark.parametrize("path", ["auto", "gemv"])
+def test_decode_batched_rows(ffn, oracle_lib, rows, dtype, path):
     """17 to 64 rows: four and eight token tiles on the weight-streaming
-    kernels (ragged last tiles included)."""
+    kernels (ragged last tiles included), forced there and as routed (bf16
+    hi + lo above 32 rows goes to the one-row-block GEMMs)."""
     cfg = synth.BlockConfig("t", rows, 1024, 2816, 1e-5, dtype)
     inp = synth.make_block_inputs(cfg, seed=200 + rows)
-    assert_lowp(to_host64(run_block(ffn, inp)), oracle_lib.block_from_inputs(inp))
+    flags = ffn.FFN_PATH_GEMV if path == "gemv" else 0
+    assert_lowp(to_host64(run_block(ffn, inp, flags)), oracle_lib.block_from_inputs(inp))
 
 
 @pytest.mark.parametrize("rows", [24, 64])
@@ -126,6 +129,29 @@ def test_single_term_activations_are_opt_in(ffn, oracle_lib, rows):
     ys = to_host64(run_block(ffn, inp))
     _, mx2, mean2 = errors(ys, ref)
     assert mx2 < mx and mean2 < mean
+
+
+@pytest.mark.parametrize("mode", ["fused", "unfused", "prepared", "prepared_residual"])
+@pytest.mark.parametrize("rows,d,ffn_", [(40, 456, 1000), (100, 1032, 2056), (128, 2048, 5632)])
+def test_one_row_block_gemm_tiles(ffn, oracle_lib, mode, rows, d, ffn_):
+    """At most 128 rows the GEMMs take 96 + 96-feature gate/up tiles and
+    64-wide down tiles: ffn and d not multiples of those widths (ragged last
+    tiles), every epilogue (fused SwiGLU, unfused, prepared weights, skip
+    connection)."""
+    cfg = synth.BlockConfig("t", rows, d, ffn_, 1e-5, "bf16")
+    inp = synth.make_block_inputs(cfg, seed=rows * 7 + d)
+    args = [to_dev(inp[k], "bf16") for k in ("x", "g", "w_gate", "w_up", "w_down")]
+    flags = ffn.FFN_PATH_GEMM
+    if mode == "unfused":
+        flags |= ffn.FFN_GATEUP_UNFUSED
+    if mode.startswith("prepared"):
+        args[2:] = [ffn.ffn_prepare_weights(w) for w in args[2:]]
+        flags |= ffn.FFN_PREPARED_WEIGHTS
+    residual = mode == "prepared_residual"
+    if residual:
+        flags |= ffn.FFN_RESIDUAL
+    y = ffn.ffn_block_forward(*args, eps=cfg.eps, flags=flags)
+    assert_lowp(to_host64(y), oracle_lib.block_from_inputs(inp, residual=residual))
 
 
 @pytest.mark.parametrize("rows", [1, 8, 16])

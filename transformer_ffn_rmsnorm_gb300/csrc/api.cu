@@ -119,7 +119,10 @@ ffn_status plan_block(int64_t rows, int64_t d, int64_t ffn, ffn_dtype dt, uint32
     } else if (flags & FFN_PATH_GEMM) {
         plan->path = PATH_GEMM;
     } else {
-        plan->path = rows <= kGemvMaxRows ? PATH_GEMV : PATH_GEMM;
+        // two-term operands (bf16 hi + lo) double the weight-streaming kernels'
+        // MMAs, which bind them from eight token tiles on: there the GEMMs win
+        const int64_t gemv_rows = plan->split_act ? kGemvMaxRows / 2 : kGemvMaxRows;
+        plan->path = rows <= gemv_rows ? PATH_GEMV : PATH_GEMM;
     }
     const size_t es = dtype_size(dt);
     const size_t r = static_cast<size_t>(rows);
