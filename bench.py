@@ -240,14 +240,16 @@ def sub_benchmarks(torch, ffn, device, peaks, peak_src, stream):
     # decode bf16 8 x 4096 x 14336 (352 MB of weights > L2); whole-call time
     # from CUDA-graph replay, per-kernel event times alongside
     out.append(decode_bench(torch, ffn, device, hbm, peak_src, stream))
+    # 128 decode tokens at once: tensor-core GEMMs with split-K down projection
+    out.append(decode_bench(torch, ffn, device, hbm, peak_src, stream, synth.C8_BATCH_BF16))
     out.append(q4_bench(torch, ffn, device, hbm, peak_src, stream))
     out.append(fp8_bench(torch, ffn, device, hbm, peak_src, stream))
     out.append(q8_bench(torch, ffn, device, hbm, peak_src, stream))
     return out
 
 
-def decode_setup(torch, ffn, device, prepared=False):
-    cfg = synth.C3_DECODE_BF16
+def decode_setup(torch, ffn, device, prepared=False, cfg=None):
+    cfg = cfg or synth.C3_DECODE_BF16
     inp = synth.make_block_inputs(cfg, seed=0)
     args = [to_dev(inp[k], "bf16", torch, device) for k in ("x", "g", "w_gate", "w_up", "w_down")]
     flags = 0
@@ -259,10 +261,10 @@ def decode_setup(torch, ffn, device, prepared=False):
     return cfg, (lambda i: ffn.ffn_block_forward(*args, eps=cfg.eps, flags=flags, out=y, ws=ws))
 
 
-def decode_bench(torch, ffn, device, hbm, peak_src, stream):
+def decode_bench(torch, ffn, device, hbm, peak_src, stream, cfg=None):
     res_all = {}
     for prepared in (False, True):
-        cfg, call = decode_setup(torch, ffn, device, prepared)
+        cfg, call = decode_setup(torch, ffn, device, prepared, cfg)
         us = graph_time_us(torch, call, 20, 10, stream)
         with ffn.KernelTimer() as kt:
             timed_loop(torch, call, 50, 3, stream)
@@ -276,7 +278,7 @@ def decode_bench(torch, ffn, device, hbm, peak_src, stream):
             "kernels_events": kernel_table(res),
             "prepared_weights": {"us_per_call": round(usp, 3), "tokens_per_s": round(cfg.rows / usp * 1e6, 1),
                                  "kernels_events": kernel_table(resp)},
-            "roofline": {"bound": "hbm", "kernel": "whole block (3 launches)",
+            "roofline": {"bound": "hbm", "kernel": f"whole block ({len(res)} launches)",
                          "achieved": round(wbytes / us / 1e3, 1), "peak": hbm, "unit": "GB/s",
                          "frac": round(wbytes / us / 1e3 / hbm, 4),
                          "peak_source": peak_src + " hbm_gbs (copy, burst)", "algorithmic_bytes": wbytes}}

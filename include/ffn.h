@@ -113,6 +113,12 @@ ffn_status ffn_swiglu(const void *gate, const void *up, void *h, int64_t count,
  * ffn_block_workspace_bytes -- device scratch bytes ffn_block_forward needs
  * for these sizes, dtype and flags (the same path choice the forward call
  * makes).  Host-only; writes *bytes.  Shape errors as in ffn_block_forward.
+ * The size may depend on the current CUDA device: on the tensor-core path
+ * with few row blocks, the down projection splits its reduction so that its
+ * tiles fill the device's multiprocessors, and its fp32 partial sums live
+ * in the workspace.  Query with the device current that the forward call
+ * will use (a smaller workspace there is FFN_ERR_WORKSPACE, never a write
+ * past its end).
  * ---------------------------------------------------------------------- */
 ffn_status ffn_block_workspace_bytes(int64_t rows, int64_t d, int64_t ffn, ffn_dtype dtype,
                                      uint32_t flags, size_t *bytes);
@@ -125,16 +131,17 @@ ffn_status ffn_block_workspace_bytes(int64_t rows, int64_t d, int64_t ffn, ffn_d
  *   x [rows x d], g [d], w_gate and w_up [ffn x d], w_down [d x ffn],
  *   y [rows x d]; all of `dtype`.  y must not overlap any input.
  *   Paths: FFN_F32 -> fp32 SIMT FFMA kernels (any rows).  FFN_F16/FFN_BF16 ->
- *   rows <= 64 (rows <= 32 when n and h enter as bf16 hi + lo terms, the
+ *   rows <= 32 (rows <= 16 when n and h enter as bf16 hi + lo terms, the
  *   bf16 default): weight-streaming decode kernels (every weight read once
- *   for up to 8 tiles of 8 token rows; at these batches the tensor-core
- *   GEMMs have too few tiles to stream the weights at full bandwidth);
- *   otherwise tcgen05/TMEM GEMMs fed by TMA.  FFN_PATH_GEMV forces the
- *   first for any rows <= 64.  Rules: d, ffn >= 1; 16-bit dtypes need d % 8 == 0 and
+ *   for up to 4 tiles of 8 token rows); otherwise tcgen05/TMEM GEMMs fed by
+ *   TMA (with few row blocks: narrower gate/up tiles and a split-K down
+ *   projection, so that the tiles fill the SMs).  FFN_PATH_GEMV forces the
+ *   first for any rows <= 64 (8 token tiles).  Rules: d, ffn >= 1; 16-bit dtypes need d % 8 == 0 and
  *   ffn % 8 == 0; fp32 needs d % 4 == 0 and ffn % 4 == 0.
  *   workspace: at least ffn_block_workspace_bytes(...) bytes, 16-byte aligned.
  *   Intermediates (n, h, split-K partials) round to `dtype` where they feed
- *   a tensor-core operand and stay fp32 otherwise.
+ *   a tensor-core operand and stay fp32 otherwise; split-K partials are
+ *   added in a fixed order (results are bitwise reproducible).
  * ---------------------------------------------------------------------- */
 ffn_status ffn_block_forward(const void *x, const void *g, const void *w_gate, const void *w_up,
                              const void *w_down, void *y, int64_t rows, int64_t d, int64_t ffn,

@@ -27,7 +27,7 @@ import numpy as np
 __all__ = [
     "BlockConfig", "NormConfig", "SwigluConfig", "Q4Config",
     "C1_TINY_F32", "C2A_RMSNORM_F16", "C2B_SWIGLU_F16", "C3_DECODE_BF16",
-    "C4_PREFILL_BF16", "C5_DECODE_Q4", "CONFIGS",
+    "C4_PREFILL_BF16", "C5_DECODE_Q4", "C8_BATCH_BF16", "CONFIGS",
     "stream", "normal", "round_to_storage", "make_block_inputs",
     "make_norm_inputs", "make_swiglu_inputs", "make_q4_inputs", "pack_q4",
     "q4_canonical_bytes", "TENSOR_IDS", "Fp8Config", "C6_DECODE_FP8", "make_fp8_inputs", "to_e4m3",
@@ -143,6 +143,8 @@ C2A_RMSNORM_F16 = NormConfig("rmsnorm_f16_16384x4096", 16384, 4096, 1e-5, "f16")
 C2B_SWIGLU_F16 = SwigluConfig("swiglu_f16_16384x11008", 16384, 11008, "f16", math.sqrt(2.0))
 C3_DECODE_BF16 = BlockConfig("decode_bf16_8x4096x14336", 8, 4096, 14336, 1e-5, "bf16")
 C4_PREFILL_BF16 = BlockConfig("prefill_bf16_4096x4096x11008", 4096, 4096, 11008, 1e-6, "bf16")
+# a batch of 128 decode tokens through the decode layer shape (one row block)
+C8_BATCH_BF16 = BlockConfig("batch_bf16_128x4096x14336", 128, 4096, 14336, 1e-5, "bf16")
 C5_DECODE_Q4 = Q4Config("decode_q4_8x5120x17408", 8, 5120, 17408, 1e-6)
 
 
@@ -161,6 +163,7 @@ C6_DECODE_FP8 = Fp8Config("decode_fp8_8x4096x14336", 8, 4096, 14336, 1e-5)
 CONFIGS = {
     "c1": C1_TINY_F32, "c2a": C2A_RMSNORM_F16, "c2b": C2B_SWIGLU_F16,
     "c3": C3_DECODE_BF16, "c4": C4_PREFILL_BF16, "c5": C5_DECODE_Q4, "c6": C6_DECODE_FP8,
+    "c8": C8_BATCH_BF16,
 }
 
 

@@ -59,8 +59,9 @@ def test_decode_rows(ffn, oracle_lib, rows, dtype):
 @pytest.mark.parametrize("path", ["auto", "gemv"])
 def test_decode_batched_rows(ffn, oracle_lib, rows, dtype, path):
     """17 to 64 rows: four and eight token tiles on the weight-streaming
-    kernels (ragged last tiles included), forced there and as routed (bf16
-    hi + lo above 32 rows goes to the one-row-block GEMMs)."""
+    kernels (ragged last tiles included), forced there and as routed (above
+    16 rows with bf16 hi + lo operands, above 32 with fp16 ones, the block
+    goes to the GEMMs with split-K down projection)."""
     cfg = synth.BlockConfig("t", rows, 1024, 2816, 1e-5, dtype)
     inp = synth.make_block_inputs(cfg, seed=200 + rows)
     flags = ffn.FFN_PATH_GEMV if path == "gemv" else 0
@@ -132,11 +133,14 @@ def test_single_term_activations_are_opt_in(ffn, oracle_lib, rows):
 
 
 @pytest.mark.parametrize("mode", ["fused", "unfused", "prepared", "prepared_residual"])
-@pytest.mark.parametrize("rows,d,ffn_", [(40, 456, 1000), (100, 1032, 2056), (128, 2048, 5632)])
-def test_one_row_block_gemm_tiles(ffn, oracle_lib, mode, rows, d, ffn_):
-    """At most 128 rows the GEMMs take 96 + 96-feature gate/up tiles and
-    64-wide down tiles: ffn and d not multiples of those widths (ragged last
-    tiles), every epilogue (fused SwiGLU, unfused, prepared weights, skip
+@pytest.mark.parametrize("rows,d,ffn_", [(40, 456, 1000), (100, 1032, 2056), (128, 2048, 5632),
+                                         (200, 1024, 2816), (512, 1024, 2816)])
+def test_few_row_block_gemm_tiles(ffn, oracle_lib, mode, rows, d, ffn_):
+    """Up to four row blocks: 96 + 96-feature gate/up tiles (one CTA, or a
+    CTA pair from two row blocks on) and a split-K down GEMM whose fp32
+    partials a second kernel adds (2 to 11 splits here, the last k block
+    ragged for ffn 1000 and 2056); d and ffn not multiples of the tile widths,
+    every epilogue (fused SwiGLU, unfused, prepared weights, skip
     connection)."""
     cfg = synth.BlockConfig("t", rows, d, ffn_, 1e-5, "bf16")
     inp = synth.make_block_inputs(cfg, seed=rows * 7 + d)
@@ -182,7 +186,7 @@ def test_prefill_fused_equals_unfused_closely(ffn):
     assert np.abs(a - b).max() <= 2e-2 * rms
 
 
-@pytest.mark.parametrize("rows", [8, 300])
+@pytest.mark.parametrize("rows", [8, 100, 300])
 def test_deterministic(ffn, rows):
     cfg = synth.BlockConfig("t", rows, 1024, 2816, 1e-5, "bf16")
     inp = synth.make_block_inputs(cfg, seed=11)
@@ -207,16 +211,20 @@ def test_device_status_clean(ffn):
     ffn.ffn_device_status()
 
 
-def test_launch_counter_and_timing(ffn):
-    cfg = synth.BlockConfig("t", 256, 512, 1024, 1e-6, "bf16")
+@pytest.mark.parametrize("rows,ffn_,kinds", [
+    (256, 512, {"rmsnorm", "gemm_gateup", "gemm_down"}),                    # K of 8 blocks: no split
+    (128, 2816, {"rmsnorm", "gemm_gateup", "gemm_down", "splitk_reduce"}),  # split-K down GEMM
+])
+def test_launch_counter_and_timing(ffn, rows, ffn_, kinds):
+    cfg = synth.BlockConfig("t", rows, 512, ffn_, 1e-6, "bf16")
     inp = synth.make_block_inputs(cfg, seed=12)
     args = [to_dev(inp[k], "bf16") for k in ("x", "g", "w_gate", "w_up", "w_down")]
     before = ffn.ffn_launch_count()
     with ffn.KernelTimer() as t:
-        ffn.ffn_block_forward(*args, eps=1e-6)
+        ffn.ffn_block_forward(*args, eps=1e-6, flags=ffn.FFN_PATH_GEMM)
         res = t.read()
-    assert ffn.ffn_launch_count() - before == 3
-    assert set(res) == {"rmsnorm", "gemm_gateup", "gemm_down"}
+    assert ffn.ffn_launch_count() - before == len(kinds)
+    assert set(res) == kinds
     assert all(n == 1 and ms > 0 for n, ms in res.values())
 
 

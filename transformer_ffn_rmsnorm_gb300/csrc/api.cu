@@ -22,9 +22,12 @@ __device__ unsigned g_ffn_status_word;
 namespace ffn {
 namespace {
 
-// rows up to which the block runs on the weight-streaming (decode) kernels;
-// the quantised entries run their rows in groups of kQuantGroupRows
+// rows up to which the weight-streaming (decode) kernels can run the block
+// (FFN_PATH_GEMV: eight token tiles), and up to which they do by default for
+// one-term and for hi + lo operands; the quantised entries run their rows in
+// groups of kQuantGroupRows
 constexpr int64_t kGemvMaxRows = 64;
+constexpr int64_t kGemvAutoRows = 32, kGemvAutoRowsTwoTerm = 16;
 constexpr int64_t kQuantGroupRows = 16;
 constexpr int kMaxDevices = 64;
 
@@ -119,9 +122,12 @@ ffn_status plan_block(int64_t rows, int64_t d, int64_t ffn, ffn_dtype dt, uint32
     } else if (flags & FFN_PATH_GEMM) {
         plan->path = PATH_GEMM;
     } else {
-        // two-term operands (bf16 hi + lo) double the weight-streaming kernels'
-        // MMAs, which bind them from eight token tiles on: there the GEMMs win
-        const int64_t gemv_rows = plan->split_act ? kGemvMaxRows / 2 : kGemvMaxRows;
+        // Measured crossover on 4096 -> 14336 (graph-replayed block): the
+        // GEMMs (one-row-block tiles, split-K down projection) take 85-90 us
+        // at 16-128 rows; the weight-streaming kernels 68 / 80 us at 16 rows
+        // (one-term / hi + lo operands), 80 / 107 us at 32, 110 / 173 us at
+        // 33 (eight token tiles).  Two-term operands double their MMAs.
+        const int64_t gemv_rows = plan->split_act ? kGemvAutoRowsTwoTerm : kGemvAutoRows;
         plan->path = rows <= gemv_rows ? PATH_GEMV : PATH_GEMM;
     }
     const size_t es = dtype_size(dt);
@@ -137,6 +143,8 @@ ffn_status plan_block(int64_t rows, int64_t d, int64_t ffn, ffn_dtype dt, uint32
             plan->workspace = align256(r * d * es) + align256(r * ffn * es);
             if (plan->split_act) plan->workspace += align256(r * d * es) + align256(r * ffn * es);
             if (!plan->fused) plan->workspace += 2 * align256(r * ffn * 4);
+            // split-K partial sums of the down GEMM (few rows)
+            plan->workspace += align256(gemm_plain_partial_bytes(rows, ffn, d, plan->split_act ? 2 : 1));
             break;
     }
     return FFN_OK;
@@ -150,7 +158,7 @@ ffn_status from_cuda(cudaError_t e) { return e == cudaSuccess ? FFN_OK : FFN_ERR
 const char *kernel_name(int kind) {
     static const char *names[K_NUM_KINDS] = {
         "prepare", "rmsnorm", "swiglu", "simt_gateup", "simt_down", "gemv_norm",
-        "gemv_gateup", "gemv_down", "gemm_gateup", "gemm_down", "selftest"};
+        "gemv_gateup", "gemv_down", "gemm_gateup", "gemm_down", "selftest", "splitk_reduce"};
     return (kind >= 0 && kind < K_NUM_KINDS) ? names[kind] : "unknown";
 }
 
@@ -338,6 +346,9 @@ ffn_status ffn_block_forward(const void *x, const void *g, const void *w_gate, c
             else
                 e = launch_rmsnorm(x, g, n, rows, d, eps, dtype, s);
             if (e != cudaSuccess) return FFN_ERR_CUDA;
+            // split-K partials: after h, or after G and U when unfused
+            float *part = reinterpret_cast<float *>(
+                plan.fused ? p : p + 2 * align256(static_cast<size_t>(rows) * ffn * 4));
             if (plan.fused) {
                 e = launch_gemm_gateup(op, n, n_lo, w_gate, w_up, h, h_lo, nullptr, nullptr, rows, d,
                                        ffn, true, w_unscale, h_scale, s);
@@ -350,7 +361,7 @@ ffn_status ffn_block_forward(const void *x, const void *g, const void *w_gate, c
             }
             if (e != cudaSuccess) return FFN_ERR_CUDA;
             return from_cuda(launch_gemm_plain(op, dtype, h, h_lo, w_down, y, rows, ffn, d,
-                                               w_unscale / h_scale, res, s));
+                                               w_unscale / h_scale, res, part, s));
         }
     }
     return FFN_ERR_SHAPE;

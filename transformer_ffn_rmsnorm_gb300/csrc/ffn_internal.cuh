@@ -27,6 +27,7 @@ enum KernelKind : int {
     K_GEMM_GATEUP,
     K_GEMM_DOWN,
     K_SELFTEST,
+    K_SPLITK_REDUCE,
     K_NUM_KINDS
 };
 const char *kernel_name(int kind);
@@ -150,10 +151,14 @@ cudaError_t launch_gemm_gateup(int dt, const void *A, const void *A_lo, const vo
                                const void *Wu, void *H, void *H_lo, void *G, void *U, int64_t M,
                                int64_t K, int64_t F, bool fused, float acc_scale, float out_scale,
                                cudaStream_t s);
-// res (optional): added to C before its one rounding (same type and layout as C)
+// res (optional): added to C before its one rounding (same type and layout as C).
+// part: fp32 scratch of gemm_plain_partial_bytes(M, K, N, A_lo ? 2 : 1) bytes
+// (16-byte aligned) for the split-K partial sums of short, wide-K products;
+// may be null when that size is 0.
 cudaError_t launch_gemm_plain(int dt, int dt_out, const void *A, const void *A_lo, const void *B,
                               void *C, int64_t M, int64_t K, int64_t N, float acc_scale,
-                              const void *res, cudaStream_t s);
+                              const void *res, float *part, cudaStream_t s);
+size_t gemm_plain_partial_bytes(int64_t M, int64_t K, int64_t N, int a_terms);
 
 }  // namespace ffn
 

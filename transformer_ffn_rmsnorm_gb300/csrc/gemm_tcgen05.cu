@@ -80,8 +80,15 @@ enum Mode { MODE_PLAIN = 0, MODE_GATEUP_FUSED = 1, MODE_GATEUP_SPLIT = 2 };
 
 struct GemmParams {
     int64_t M, N, K;          // N: output columns (ffn for gate/up, d for down)
-    int64_t num_m_blocks, num_tiles;
+    int64_t num_m_blocks, num_n_blocks;
     int num_k_blocks;
+    // split-K (plain mode, too few tiles to fill the SMs): unit u sums ring
+    // stages [kst_per_split * s, kst_per_split * (s + 1)) of its tile, s =
+    // u / (pairs x column blocks), and stores the fp32 sum in part[s]; a
+    // second kernel adds the splits in order.  Unsplit: kst_per_split covers
+    // all stages and part is null.
+    int kst_per_split;
+    float *part;
     // CTAs per unit of work: 1, or 2 for a CTA pair (rows of row blocks 2i
     // and 2i+1 against one column block, one M=256 MMA over both SMs)
     int cluster;
@@ -230,7 +237,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const bool leader = rank == 0;
     const int64_t unit0 = blockIdx.x / NCTA, unit_step = gridDim.x / NCTA;
     auto m_blk_of = [&](int64_t u) { return (u % p.num_m_pairs) * NCTA + rank; };
-    auto n_blk_of = [&](int64_t u) { return u / p.num_m_pairs; };
+    auto n_blk_of = [&](int64_t u) { return (u / p.num_m_pairs) % p.num_n_blocks; };
+    auto split_of = [&](int64_t u) { return static_cast<int>(u / (p.num_m_pairs * p.num_n_blocks)); };
+    auto kst_lo = [&](int64_t u) { return split_of(u) * p.kst_per_split; };
+    auto kst_hi = [&](int64_t u) {
+        const int e = kst_lo(u) + p.kst_per_split;
+        return e < nst ? e : nst;
+    };
     // the barriers the pair shares live in the even CTA
     auto lead = [&](uint32_t bar) { return PAIR ? ptx::mapa_shared(bar, 0) : bar; };
     volatile int *abort_flag = &s_abort;
@@ -287,19 +300,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // requested before the kernel that writes A has finished; A only
         // after it has.  The grid never exceeds the unit count, so every CTA
         // has a first unit.
-        const int npre = nst < STAGES ? nst : STAGES;
+        const int kfirst = kst_lo(unit0), nfirst = kst_hi(unit0) - kfirst;
+        const int npre = nfirst < STAGES ? nfirst : STAGES;
         for (int kb = 0; kb < npre; ++kb) {
             arm(kb);
-            load_b(kb, kb, n_blk_of(unit0));
+            load_b(kb, kfirst + kb, n_blk_of(unit0));
         }
         ptx::griddep_wait();
-        for (int kb = 0; kb < npre; ++kb) load_a(kb, kb, static_cast<int>(m_blk_of(unit0) * BM));
+        for (int kb = 0; kb < npre; ++kb) load_a(kb, kfirst + kb, static_cast<int>(m_blk_of(unit0) * BM));
         produced = npre;
         bool ok = true;
         for (int64_t u = unit0; u < p.num_units && ok; u += unit_step) {
             const int m0 = static_cast<int>(m_blk_of(u) * BM);
             const int64_t n_blk = n_blk_of(u);
-            for (int kb = (u == unit0) ? npre : 0; kb < nst; ++kb) {
+            for (int kb = (u == unit0) ? kfirst + npre : kst_lo(u), ke = kst_hi(u); kb < ke; ++kb) {
                 const uint32_t s = static_cast<uint32_t>(produced % STAGES);
                 const uint32_t ph = static_cast<uint32_t>((produced / STAGES) & 1);
                 if (!ptx::mbar_wait(empty(s), ph ^ 1u, abort_flag, limit)) {
@@ -329,7 +343,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             ptx::tc_fence_after();
             const uint32_t d_tmem = tmem_base + acc * BN;
-            for (int kb = 0; kb < nst; ++kb) {
+            const int kb0 = kst_lo(u), ke = kst_hi(u);
+            for (int kb = kb0; kb < ke; ++kb) {
                 const uint32_t s = static_cast<uint32_t>(consumed % STAGES);
                 const uint32_t ph = static_cast<uint32_t>((consumed / STAGES) & 1);
                 if (!ptx::mbar_wait(full(s), ph, abort_flag, limit)) {
@@ -347,7 +362,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         for (int k = 0; k < BK / UMMA_K; ++k) {
                             const uint64_t ad = ptx::sdesc_k_sw128(a0 + k * UMMA_K * 2);
                             const uint64_t bd = ptx::sdesc_k_sw128(b0 + k * UMMA_K * 2);
-                            const uint32_t accumulate = (kb | j | k | t) != 0 ? 1u : 0u;
+                            const uint32_t accumulate = ((kb - kb0) | j | k | t) != 0 ? 1u : 0u;
                             if constexpr (PAIR) ptx::tc_mma_f16_pair(d_tmem, ad, bd, idesc, accumulate);
                             else ptx::tc_mma_f16(d_tmem, ad, bd, idesc, accumulate);
                         }
@@ -404,8 +419,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     for (int j = 0; j < CW; ++j) v[j] = __uint_as_float(r[j]) * p.acc_scale;
                     if (live) {
                         const int64_t col = n_blk * BN + c;
-                        if (p.res) add_row<TOut, CW>(static_cast<const TOut *>(p.res) + row * p.ldo, col, p.N, v);
-                        store_row<TOut, CW>(static_cast<TOut *>(p.out0) + row * p.ldo, nullptr, col, p.N, v);
+                        if (p.part) {
+                            float *dst = p.part + (static_cast<int64_t>(split_of(u)) * p.M + row) * p.ldo;
+                            store_row_f32<CW>(dst, col, p.N, v);
+                        } else {
+                            if (p.res)
+                                add_row<TOut, CW>(static_cast<const TOut *>(p.res) + row * p.ldo, col, p.N, v);
+                            store_row<TOut, CW>(static_cast<TOut *>(p.out0) + row * p.ldo, nullptr, col, p.N, v);
+                        }
                     }
                 }
             } else {
@@ -532,9 +553,11 @@ bool make_map(CUtensorMap *m, const void *ptr, bool bf16, int64_t inner, int64_t
 template <int MODE, bool BF16, int A_TERMS, bool OUT_BF16, int BN, bool PAIR>
 cudaError_t launch_kernel(const void *A, const void *A2, const void *B0, const void *B1, void *out0,
                           void *out1, int64_t M, int64_t K, int64_t N, int kind, float acc_scale,
-                          float out_scale, const void *res, cudaStream_t s) {
+                          float out_scale, const void *res, float *part, int kst_per_split, int splits,
+                          cudaStream_t s) {
     constexpr size_t SMEM_BYTES = Ring<A_TERMS, BN, PAIR>::SMEM_BYTES;
     constexpr int NCTA = PAIR ? 2 : 1;
+    using RG = Ring<A_TERMS, BN, PAIR>;
     const auto kern = &gemm_tcgen05_kernel<MODE, BF16, A_TERMS, OUT_BF16, BN, PAIR>;
     static int configured_device = -1, slots = 0;   // co-resident units (CTAs or pairs)
     int dev = 0;
@@ -582,11 +605,13 @@ cudaError_t launch_kernel(const void *A, const void *A2, const void *B0, const v
     p.N = N;
     p.K = K;
     p.num_m_blocks = num_m_blocks;
-    p.num_tiles = num_m_blocks * num_n_blocks;
+    p.num_n_blocks = num_n_blocks;
     p.num_k_blocks = static_cast<int>((K + BK - 1) / BK);
+    p.kst_per_split = splits > 1 ? kst_per_split : (p.num_k_blocks + RG::KSUB - 1) / RG::KSUB;
+    p.part = splits > 1 ? part : nullptr;
     p.cluster = NCTA;
     p.num_m_pairs = (num_m_blocks + NCTA - 1) / NCTA;
-    p.num_units = p.num_m_pairs * num_n_blocks;
+    p.num_units = p.num_m_pairs * num_n_blocks * (splits > 1 ? splits : 1);
     p.out0 = out0;
     p.out1 = out1;
     p.ldo = N;
@@ -627,57 +652,170 @@ cudaError_t launch_kernel(const void *A, const void *A2, const void *B0, const v
 template <int MODE, bool BF16, int A_TERMS, bool OUT_BF16 = BF16, int BN = 256>
 cudaError_t launch_impl(const void *A, const void *A2, const void *B0, const void *B1, void *out0,
                         void *out1, int64_t M, int64_t K, int64_t N, int kind, float acc_scale,
-                        float out_scale, cudaStream_t s, const void *res = nullptr) {
+                        float out_scale, cudaStream_t s, const void *res = nullptr, float *part = nullptr,
+                        int kst_per_split = 0, int splits = 1) {
     if (M <= 0) return cudaSuccess;
     if (M > BM)
         return launch_kernel<MODE, BF16, A_TERMS, OUT_BF16, BN, true>(A, A2, B0, B1, out0, out1, M, K, N, kind,
-                                                                       acc_scale, out_scale, res, s);
+                                                                       acc_scale, out_scale, res, part,
+                                                                       kst_per_split, splits, s);
     return launch_kernel<MODE, BF16, A_TERMS, OUT_BF16, BN, false>(A, A2, B0, B1, out0, out1, M, K, N, kind,
-                                                                    acc_scale, out_scale, res, s);
+                                                                    acc_scale, out_scale, res, part,
+                                                                    kst_per_split, splits, s);
 }
 
-// Tile width of the plain GEMM: waves of tiles times the width of a tile
-// (the time of a wave scales with it).  E.g. 4096 rows onto 4096 columns:
-// 224-wide tiles make 608 tiles, exactly 4 waves on 152 SMs (256 wide: 512
-// tiles, the 4th wave 37 % full).  The gate/up GEMM keeps 256 (128 + 128):
-// on 4096 x 11008, 112 + 112 tiles evened the waves (20.8 against 18.1) but
-// ran 6 % slower, a narrower tile moving more operand bytes from L2 per flop.
-int tile_width(int64_t M, int64_t N) {
+// Waves of tiles times the width of a tile (the time of a wave scales with
+// it), for units of `ncta` CTAs each covering `cols` output columns.
+int64_t wave_cost(int64_t M, int64_t N, int cols, int width) {
     const int64_t mb = (M + BM - 1) / BM;
-    const int64_t sms = sm_count();
-    int best = 256;
-    int64_t best_cost = 0;
-    for (int bn : {256, 224}) {
-        const int64_t tiles = mb * ((N + bn - 1) / bn);
-        const int64_t cost = ((tiles + sms - 1) / sms) * bn;
-        if (best_cost == 0 || cost < best_cost) {
-            best = bn;
-            best_cost = cost;
-        }
-    }
-    return best;
+    const int64_t ncta = mb > 1 ? 2 : 1;
+    const int64_t units = ((mb + ncta - 1) / ncta) * ((N + cols - 1) / cols);
+    const int64_t slots = sm_count() / ncta;
+    return ((units + slots - 1) / slots) * width;
 }
 
-// One row block (M <= 128, small batches): the GEMMs stream the weights, and
-// the tile width sets how many SMs do it -- gate/up takes 96 + 96 features a
-// tile (ffn 14336: 150 tiles on 152 SMs instead of 112 with 128 + 128), the
-// down GEMM 64-wide tiles (d 4096: 64 CTAs instead of 19).  Measured on 24-128
-// rows of 4096 -> 14336: 133 -> 123 us (prepared weights), 196 -> 154 us
-// (bf16, hi + lo), y bitwise unchanged (every tile sums its full K in order).
-constexpr int kSmallMGateUpBN = 192, kSmallMDownBN = 64;
+// Tile width of the plain GEMM.  E.g. 4096 rows onto 4096 columns: 224-wide
+// tiles make 608 tiles, exactly 4 waves on 152 SMs (256 wide: 512 tiles, the
+// 4th wave 37 % full).
+int tile_width(int64_t M, int64_t N) {
+    return wave_cost(M, N, 224, 224) < wave_cost(M, N, 256, 256) ? 224 : 256;
+}
+
+// Gate/up tile width: 128 + 128 features, or 96 + 96 when the 256-wide tiles
+// take at most two waves and the narrower ones take less time.  Small batches
+// stream the weights, and the tile count sets how many SMs do it: ffn 14336
+// on one row block makes 150 tiles of 96 + 96 on 152 SMs against 112 of 128 +
+// 128; on two row blocks (one CTA pair each tile) 2 waves of 192 against 2 of
+// 256.  Long prefill keeps 256 even where 192 evens the waves: on 4096 x
+// 11008, 112 + 112 tiles ran 6 % slower, a narrower tile moving more operand
+// bytes from L2 per flop.
+int gateup_width(int64_t M, int64_t N) {
+    const int64_t wide = wave_cost(M, N, 128, 256);
+    return (wide <= 2 * 256 && wave_cost(M, N, 96, 192) < wide) ? 192 : 256;
+}
+
+// Split-K plan of the plain GEMM (the down projection).  With fewer 256-wide
+// tiles than half the CTA slots (d 4096 on up to 512 rows: 16-64 CTAs of
+// 152), each CTA would stream a whole K-long strip of W_down through one SM.
+// Instead the reduction is cut into `splits` runs of whole ring stages
+// (at least kMinSplitKBlocks 64-wide k blocks each) that together fill the
+// SMs; each run stores an fp32 partial tile, and splitk_reduce_kernel adds
+// them in split order (deterministic) with the residual, rounding once.
+// Returns the split count (1: no split) and the stages per run.
+constexpr int kMinSplitKBlocks = 8, kMaxSplits = 16;
+int plain_split_plan(int64_t M, int64_t K, int64_t N, int a_terms, int *kst_per_split) {
+    const int64_t mb = (M + BM - 1) / BM;
+    const bool pair = mb > 1;
+    const int64_t ncta = pair ? 2 : 1;
+    const int64_t units = ((mb + ncta - 1) / ncta) * ((N + 255) / 256);
+    const int64_t slots = sm_count() / ncta;
+    const int64_t kblocks = (K + BK - 1) / BK;
+    const int64_t ksub = (pair && a_terms == 1) ? 2 : 1;   // Ring<a_terms, 256, pair>::KSUB
+    const int64_t nst = (kblocks + ksub - 1) / ksub;
+    if (M <= 0 || 2 * units > slots) return 1;
+    int64_t sp = slots / units;
+    if (sp > kblocks / kMinSplitKBlocks) sp = kblocks / kMinSplitKBlocks;
+    if (sp > kMaxSplits) sp = kMaxSplits;
+    if (sp < 2) return 1;
+    const int64_t per = (nst + sp - 1) / sp;
+    if (kst_per_split) *kst_per_split = static_cast<int>(per);
+    return static_cast<int>((nst + per - 1) / per);
+}
+static_assert(Ring<1, 256, true>::KSUB == 2 && Ring<2, 256, true>::KSUB == 1 && Ring<1, 256, false>::KSUB == 1,
+              "plain_split_plan's stage size");
+
+// out = sum over s of part[s] (s = 0, 1, ...) + res, rounded once to TOut.
+// part: [splits][count] fp32; count (M x N) is a multiple of 8.
+template <typename TOut>
+__global__ void __launch_bounds__(256) splitk_reduce_kernel(const float *part, int splits, int64_t count,
+                                                            const TOut *res, TOut *out) {
+    // the partials are the previous kernel's output; only once they are
+    // complete may the kernel after this one start
+    ptx::griddep_wait();
+    ptx::griddep_launch_dependents();
+    const int64_t nvec = count / 8;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nvec; i += stride) {
+        float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int sp = 0; sp < splits; ++sp) {
+            const float4 *src = reinterpret_cast<const float4 *>(part + sp * count) + 2 * i;
+            const float4 a = __ldcs(src), b = __ldcs(src + 1);
+            v[0] += a.x;
+            v[1] += a.y;
+            v[2] += a.z;
+            v[3] += a.w;
+            v[4] += b.x;
+            v[5] += b.y;
+            v[6] += b.z;
+            v[7] += b.w;
+        }
+        if (res) {
+            float r[8];
+            Vec16<TOut>::unpack(reinterpret_cast<const uint4 *>(res)[i], r);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[e] += r[e];
+        }
+        reinterpret_cast<uint4 *>(out)[i] = Vec16<TOut>::pack(v);
+    }
+}
+
+template <typename TOut>
+cudaError_t launch_splitk_reduce(const float *part, int splits, int64_t count, const void *res, void *out,
+                                 cudaStream_t s) {
+    const int64_t nvec = count / 8;
+    int64_t blocks = static_cast<int64_t>(sm_count()) * 4;
+    const int64_t need = (nvec + 255) / 256;
+    if (blocks > need) blocks = need;
+    if (blocks < 1) return cudaSuccess;
+    LaunchScope scope(K_SPLITK_REDUCE, s);
+    cudaError_t e = launch_dependent(splitk_reduce_kernel<TOut>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0,
+                                     s, part, splits, count, static_cast<const TOut *>(res),
+                                     static_cast<TOut *>(out));
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
 
 template <int MODE, bool BF16, int A_TERMS>
 cudaError_t launch_gateup_bn(const void *A, const void *A2, const void *B0, const void *B1, void *out0,
                              void *out1, int64_t M, int64_t K, int64_t N, float acc_scale, float out_scale,
                              cudaStream_t s) {
-    if (M <= BM)
-        return launch_impl<MODE, BF16, A_TERMS, BF16, kSmallMGateUpBN>(A, A2, B0, B1, out0, out1, M, K, N,
-                                                                       K_GEMM_GATEUP, acc_scale, out_scale, s);
+    if (gateup_width(M, N) == 192)
+        return launch_impl<MODE, BF16, A_TERMS, BF16, 192>(A, A2, B0, B1, out0, out1, M, K, N, K_GEMM_GATEUP,
+                                                           acc_scale, out_scale, s);
     return launch_impl<MODE, BF16, A_TERMS, BF16, 256>(A, A2, B0, B1, out0, out1, M, K, N, K_GEMM_GATEUP,
                                                        acc_scale, out_scale, s);
 }
 
+// One row block and a reduction too short to split: 64-wide tiles (d 4096:
+// 64 CTAs instead of 16).
+template <bool BF16, int A_TERMS, bool OUT_BF16>
+cudaError_t launch_plain_bn(const void *A, const void *A_lo, const void *B, void *C, int64_t M, int64_t K,
+                            int64_t N, float acc_scale, const void *res, float *part, cudaStream_t s) {
+    using TOut = typename std::conditional<OUT_BF16, __nv_bfloat16, __half>::type;
+    int per = 0;
+    const int splits = plain_split_plan(M, K, N, A_TERMS, &per);
+    if (splits > 1) {
+        if (!part) return cudaErrorInvalidValue;
+        cudaError_t e = launch_impl<MODE_PLAIN, BF16, A_TERMS, OUT_BF16, 256>(
+            A, A_lo, B, nullptr, C, nullptr, M, K, N, K_GEMM_DOWN, acc_scale, 1.f, s, nullptr, part, per, splits);
+        if (e != cudaSuccess) return e;
+        return launch_splitk_reduce<TOut>(part, splits, M * N, res, C, s);
+    }
+    if (M <= BM)
+        return launch_impl<MODE_PLAIN, BF16, A_TERMS, OUT_BF16, 64>(A, A_lo, B, nullptr, C, nullptr, M, K, N,
+                                                                    K_GEMM_DOWN, acc_scale, 1.f, s, res);
+    if (tile_width(M, N) == 224)
+        return launch_impl<MODE_PLAIN, BF16, A_TERMS, OUT_BF16, 224>(A, A_lo, B, nullptr, C, nullptr, M, K,
+                                                                     N, K_GEMM_DOWN, acc_scale, 1.f, s, res);
+    return launch_impl<MODE_PLAIN, BF16, A_TERMS, OUT_BF16, 256>(A, A_lo, B, nullptr, C, nullptr, M, K, N,
+                                                                 K_GEMM_DOWN, acc_scale, 1.f, s, res);
+}
+
 }  // namespace
+
+size_t gemm_plain_partial_bytes(int64_t M, int64_t K, int64_t N, int a_terms) {
+    const int splits = plain_split_plan(M, K, N, a_terms, nullptr);
+    return splits > 1 ? static_cast<size_t>(splits) * static_cast<size_t>(M) * static_cast<size_t>(N) * 4 : 0;
+}
 
 cudaError_t launch_gemm_gateup(int dt, const void *A, const void *A_lo, const void *Wg,
                                const void *Wu, void *H, void *H_lo, void *G, void *U, int64_t M,
@@ -699,34 +837,20 @@ cudaError_t launch_gemm_gateup(int dt, const void *A, const void *A_lo, const vo
               : launch_gateup_bn<MODE_GATEUP_SPLIT, false, 1>(A, nullptr, Wg, Wu, G, U, M, K, F, a, o, s);
 }
 
-template <bool BF16, int A_TERMS, bool OUT_BF16>
-cudaError_t launch_plain_bn(const void *A, const void *A_lo, const void *B, void *C, int64_t M,
-                            int64_t K, int64_t N, float acc_scale, const void *res, cudaStream_t s) {
-    if (M <= BM)
-        return launch_impl<MODE_PLAIN, BF16, A_TERMS, OUT_BF16, kSmallMDownBN>(A, A_lo, B, nullptr, C, nullptr, M,
-                                                                               K, N, K_GEMM_DOWN, acc_scale, 1.f,
-                                                                               s, res);
-    if (tile_width(M, N) == 224)
-        return launch_impl<MODE_PLAIN, BF16, A_TERMS, OUT_BF16, 224>(A, A_lo, B, nullptr, C, nullptr, M, K,
-                                                                     N, K_GEMM_DOWN, acc_scale, 1.f, s, res);
-    return launch_impl<MODE_PLAIN, BF16, A_TERMS, OUT_BF16, 256>(A, A_lo, B, nullptr, C, nullptr, M, K, N,
-                                                                 K_GEMM_DOWN, acc_scale, 1.f, s, res);
-}
-
 cudaError_t launch_gemm_plain(int dt, int dt_out, const void *A, const void *A_lo, const void *B,
                               void *C, int64_t M, int64_t K, int64_t N, float acc_scale,
-                              const void *res, cudaStream_t s) {
+                              const void *res, float *part, cudaStream_t s) {
     const float a = acc_scale;
     if (dt == DT_BF16) {
-        if (A_lo) return launch_plain_bn<true, 2, true>(A, A_lo, B, C, M, K, N, a, res, s);
-        return launch_plain_bn<true, 1, true>(A, nullptr, B, C, M, K, N, a, res, s);
+        if (A_lo) return launch_plain_bn<true, 2, true>(A, A_lo, B, C, M, K, N, a, res, part, s);
+        return launch_plain_bn<true, 1, true>(A, nullptr, B, C, M, K, N, a, res, part, s);
     }
     if (dt_out == DT_BF16) {   // fp16 operands, bf16 output (prepared-weights path)
-        if (A_lo) return launch_plain_bn<false, 2, true>(A, A_lo, B, C, M, K, N, a, res, s);
-        return launch_plain_bn<false, 1, true>(A, nullptr, B, C, M, K, N, a, res, s);
+        if (A_lo) return launch_plain_bn<false, 2, true>(A, A_lo, B, C, M, K, N, a, res, part, s);
+        return launch_plain_bn<false, 1, true>(A, nullptr, B, C, M, K, N, a, res, part, s);
     }
-    if (A_lo) return launch_plain_bn<false, 2, false>(A, A_lo, B, C, M, K, N, a, res, s);
-    return launch_plain_bn<false, 1, false>(A, nullptr, B, C, M, K, N, a, res, s);
+    if (A_lo) return launch_plain_bn<false, 2, false>(A, A_lo, B, C, M, K, N, a, res, part, s);
+    return launch_plain_bn<false, 1, false>(A, nullptr, B, C, M, K, N, a, res, part, s);
 }
 
 }  // namespace ffn
