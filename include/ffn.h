@@ -157,7 +157,8 @@ ffn_status ffn_block_forward(const void *x, const void *g, const void *w_gate, c
  *   g, w_gate, w_up, w_down: device pointers as in ffn_block_forward.
  *   workspace: device scratch of ffn_block_host_workspace_bytes() bytes
  *   (x and y are staged there, plus the block's own scratch).
- * The rows are split into chunks (1024 rows above 1024); the input copy of
+ * The rows are split into chunks (above 1024 rows: first and last chunks of
+ * 1024 rows, the rows between in chunks of at most 2048); the input copy of
  * every chunk is queued at once on a copy stream owned by the library, each
  * chunk's block runs on `stream` when its rows have landed, and its output
  * copy runs on a second library stream while the next chunk computes.

@@ -158,6 +158,18 @@ def test_few_row_block_gemm_tiles(ffn, oracle_lib, mode, rows, d, ffn_):
     assert_lowp(to_host64(y), oracle_lib.block_from_inputs(inp, residual=residual))
 
 
+@pytest.mark.parametrize("d,ffn_", [(4096, 11008), (4096, 14336), (1024, 2816), (8192, 28672)])
+def test_workspace_never_shrinks_with_rows(ffn, d, ffn_):
+    """A workspace sized for a batch serves every smaller batch: the split-K
+    partial sums of small batches (sized by the device's SM count) are
+    covered at every larger row count."""
+    import torch
+    for flags in (0, ffn.FFN_PREPARED_WEIGHTS, ffn.FFN_GATEUP_UNFUSED, ffn.FFN_PATH_GEMM):
+        sizes = [ffn.ffn_block_workspace_bytes(r, d, ffn_, torch.bfloat16, flags)
+                 for r in list(range(1, 1100, 5)) + [1536, 2048, 4096]]
+        assert all(b >= a for a, b in zip(sizes, sizes[1:])), flags
+
+
 @pytest.mark.parametrize("rows", [1, 8, 16])
 def test_forced_gemm_path_for_few_rows(ffn, oracle_lib, rows):
     cfg = synth.BlockConfig("t", rows, 1024, 2816, 1e-5, "bf16")

@@ -113,23 +113,22 @@ ffn_status plan_block(int64_t rows, int64_t d, int64_t ffn, ffn_dtype dt, uint32
     if (plan->prepared && (dt == FFN_F32 || (flags & FFN_ACT_SPLIT))) return FFN_ERR_FLAGS;
     plan->split_act = !plan->prepared &&
                       ((flags & FFN_ACT_SPLIT) || (dt == FFN_BF16 && !(flags & FFN_ACT_SINGLE)));
-    if (dt == FFN_F32) {
-        if (flags & (FFN_PATH_GEMM | FFN_PATH_GEMV)) return FFN_ERR_FLAGS;
+    if (dt == FFN_F32 && (flags & (FFN_PATH_GEMM | FFN_PATH_GEMV))) return FFN_ERR_FLAGS;
+    if ((flags & FFN_PATH_GEMV) && rows > kGemvMaxRows) return FFN_ERR_SHAPE;
+    // rows up to which these flags take the decode kernels.  Measured
+    // crossover on 4096 -> 14336 (graph-replayed block): the GEMMs
+    // (one-row-block tiles, split-K down projection) take 85-90 us at 16-128
+    // rows; the weight-streaming kernels 68 / 80 us at 16 rows (one-term /
+    // hi + lo operands), 80 / 107 us at 32, 110 / 173 us at 33 (eight token
+    // tiles).  Two-term operands double their MMAs.
+    int64_t gemv_rows = 0;
+    if (dt != FFN_F32 && !(flags & FFN_PATH_GEMM))
+        gemv_rows = (flags & FFN_PATH_GEMV) ? kGemvMaxRows
+                                            : (plan->split_act ? kGemvAutoRowsTwoTerm : kGemvAutoRows);
+    if (dt == FFN_F32)
         plan->path = PATH_SIMT;
-    } else if (flags & FFN_PATH_GEMV) {
-        if (rows > kGemvMaxRows) return FFN_ERR_SHAPE;
-        plan->path = PATH_GEMV;
-    } else if (flags & FFN_PATH_GEMM) {
-        plan->path = PATH_GEMM;
-    } else {
-        // Measured crossover on 4096 -> 14336 (graph-replayed block): the
-        // GEMMs (one-row-block tiles, split-K down projection) take 85-90 us
-        // at 16-128 rows; the weight-streaming kernels 68 / 80 us at 16 rows
-        // (one-term / hi + lo operands), 80 / 107 us at 32, 110 / 173 us at
-        // 33 (eight token tiles).  Two-term operands double their MMAs.
-        const int64_t gemv_rows = plan->split_act ? kGemvAutoRowsTwoTerm : kGemvAutoRows;
+    else
         plan->path = rows <= gemv_rows ? PATH_GEMV : PATH_GEMM;
-    }
     const size_t es = dtype_size(dt);
     const size_t r = static_cast<size_t>(rows);
     switch (plan->path) {
@@ -145,6 +144,11 @@ ffn_status plan_block(int64_t rows, int64_t d, int64_t ffn, ffn_dtype dt, uint32
             if (!plan->fused) plan->workspace += 2 * align256(r * ffn * 4);
             // split-K partial sums of the down GEMM (few rows)
             plan->workspace += align256(gemm_plain_partial_bytes(rows, ffn, d, plan->split_act ? 2 : 1));
+            // a workspace sized for these rows also serves every smaller
+            // batch, those that take the decode kernels included
+            if (gemv_rows > 0)
+                plan->workspace = std::max(plan->workspace, gemv_workspace_bytes(std::min(rows, gemv_rows), d, ffn,
+                                                                                  plan->split_act));
             break;
     }
     return FFN_OK;

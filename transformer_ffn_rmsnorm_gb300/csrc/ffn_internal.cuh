@@ -154,7 +154,7 @@ cudaError_t launch_gemm_gateup(int dt, const void *A, const void *A_lo, const vo
 // res (optional): added to C before its one rounding (same type and layout as C).
 // part: fp32 scratch of gemm_plain_partial_bytes(M, K, N, A_lo ? 2 : 1) bytes
 // (16-byte aligned) for the split-K partial sums of short, wide-K products;
-// may be null when that size is 0.
+// may be null when that size is 0.  That size never decreases with M.
 cudaError_t launch_gemm_plain(int dt, int dt_out, const void *A, const void *A_lo, const void *B,
                               void *C, int64_t M, int64_t K, int64_t N, float acc_scale,
                               const void *res, float *part, cudaStream_t s);

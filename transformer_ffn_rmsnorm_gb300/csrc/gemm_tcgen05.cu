@@ -812,9 +812,23 @@ cudaError_t launch_plain_bn(const void *A, const void *A_lo, const void *B, void
 
 }  // namespace
 
+// The largest partial-sum buffer any M' <= M needs, so that a workspace sized
+// for a batch also serves every smaller one.  Splits only occur while the
+// tiles fill less than half the SMs, and they are fixed per row-block count,
+// so the maximum is over the first few row-block counts at their full rows.
 size_t gemm_plain_partial_bytes(int64_t M, int64_t K, int64_t N, int a_terms) {
-    const int splits = plain_split_plan(M, K, N, a_terms, nullptr);
-    return splits > 1 ? static_cast<size_t>(splits) * static_cast<size_t>(M) * static_cast<size_t>(N) * 4 : 0;
+    size_t most = 0;
+    for (int64_t mb = 1; mb <= (M + BM - 1) / BM; ++mb) {
+        const int64_t rows = mb * BM < M ? mb * BM : M;
+        const int splits = plain_split_plan(rows, K, N, a_terms, nullptr);
+        if (splits <= 1) {
+            if (mb > 1) break;   // more row blocks, more tiles: no split from here on
+            continue;
+        }
+        const size_t bytes = static_cast<size_t>(splits) * static_cast<size_t>(rows) * static_cast<size_t>(N) * 4;
+        if (bytes > most) most = bytes;
+    }
+    return most;
 }
 
 cudaError_t launch_gemm_gateup(int dt, const void *A, const void *A_lo, const void *Wg,

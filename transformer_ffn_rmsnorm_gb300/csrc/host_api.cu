@@ -6,18 +6,21 @@
 // library's own, each chunk's block runs on the caller's stream as soon as its
 // rows have landed, and its device-to-host copy runs on a second copy stream
 // while the next chunk computes.  The caller's stream finally waits for the
-// last copy, so synchronising that stream means y is in host memory.  Only
-// the first chunk's input copy and the last chunk's output copy are exposed.
+// last copy, so synchronising that stream means y is in host memory.
 //
-// Chunks are 1024 rows for batches above 1024 rows.  On the host link of a
-// GB300 (about 200 GB/s each way for page-locked memory) the exposed copies
-// are the first chunk's input and the last chunk's output, so chunks should
-// be short; but each chunk's GEMMs run in whole waves of 76 CTA pairs.  At
-// 1024 rows (4 pairs of 128-row blocks) the down projection of d = 4096 is
-// exactly one wave (4 x 19 tiles of 224 columns) and gate/up (ffn 11008, 4 x
-// 86 tile pairs) fills 4.5 of 5 waves; 1536-row chunks fill gate/up better
-// (6.8 of 7) but leave the down projection's second wave half empty, and
-// cost 50 % more exposed copy time.
+// Only the first chunk's input copy and the last chunk's output copy are
+// exposed (the host link of a GB300 moves about 200 GB/s each way for
+// page-locked memory, 160 GB/s each way when both directions run), so the
+// edge chunks are short; but each chunk's GEMMs run in whole waves and pay
+// their ramp and drain, so the chunks between are long.  Measured on 4096 x
+// 4096 -> 11008 (prepared weights, burst clocks), x and y on the host:
+//   chunks 1024 x 4            836 us (compute alone 723 us)
+//   1024, 2048, 1024           797 us (691 us)
+//   512, 3072, 512             791 us (719 us)
+//   768, 2560, 768             827 us;  256, 3584, 256  868 us (the middle
+//                              chunk's copies outlast the edge chunks)
+//   one chunk of 4096          989 us (635 us)
+// The plan: edge chunks of 1024 rows, the middle in chunks of at most 2048.
 #include <cstring>
 #include <mutex>
 
@@ -31,20 +34,39 @@ constexpr int kMaxChunks = 16;
 constexpr int kMaxDevices = 64;
 
 struct Chunks {
-    int64_t rows;    // rows per chunk (the last may be fewer)
+    int64_t start[kMaxChunks + 1];   // chunk i holds rows start[i] .. start[i+1]-1
     int count;
+    int64_t rows(int i) const { return start[i + 1] - start[i]; }
 };
 
+// First and last chunks of kEdgeRows, the rows between in near-equal chunks
+// of at most kMidRows (multiples of 256), at most kMaxChunks in all.
+constexpr int64_t kEdgeRows = 1024, kMidRows = 2048;
 Chunks plan_chunks(int64_t rows) {
     Chunks c;
-    if (rows <= 1024) {
-        c.rows = rows;
-        c.count = rows > 0 ? 1 : 0;
+    c.count = 0;
+    c.start[0] = 0;
+    if (rows <= 0) return c;
+    auto push = [&](int64_t n) {
+        c.start[c.count + 1] = c.start[c.count] + n;
+        ++c.count;
+    };
+    if (rows <= kEdgeRows) {
+        push(rows);
         return c;
     }
-    c.rows = 1024;
-    if ((rows + c.rows - 1) / c.rows > kMaxChunks) c.rows = ((rows + kMaxChunks - 1) / kMaxChunks + 255) / 256 * 256;
-    c.count = static_cast<int>((rows + c.rows - 1) / c.rows);
+    if (rows <= 2 * kEdgeRows) {
+        push(kEdgeRows);
+        push(rows - kEdgeRows);
+        return c;
+    }
+    const int64_t mid = rows - 2 * kEdgeRows;
+    int64_t pieces = (mid + kMidRows - 1) / kMidRows;
+    if (pieces > kMaxChunks - 2) pieces = kMaxChunks - 2;
+    const int64_t each = ((mid + pieces - 1) / pieces + 255) / 256 * 256;
+    push(kEdgeRows);
+    for (int64_t left = mid; left > 0; left -= each) push(left < each ? left : each);
+    push(kEdgeRows);
     return c;
 }
 
@@ -59,13 +81,12 @@ ffn_status layout(int64_t rows, int64_t d, int64_t ffn, ffn_dtype dt, uint32_t f
     const Chunks c = plan_chunks(rows);
     size_t block = 0;
     if (c.count > 0) {
-        size_t a = 0, b = 0;
-        ffn_status st = ffn_block_workspace_bytes(c.rows, d, ffn, dt, flags, &a);
-        if (st != FFN_OK) return st;
-        const int64_t last = rows - c.rows * (c.count - 1);
-        st = ffn_block_workspace_bytes(last, d, ffn, dt, flags, &b);
-        if (st != FFN_OK) return st;
-        block = a > b ? a : b;
+        for (int i = 0; i < c.count; ++i) {
+            size_t a = 0;
+            ffn_status st = ffn_block_workspace_bytes(c.rows(i), d, ffn, dt, flags, &a);
+            if (st != FFN_OK) return st;
+            if (a > block) block = a;
+        }
     } else {
         size_t a = 0;
         ffn_status st = ffn_block_workspace_bytes(0, d, ffn, dt, flags, &a);
@@ -154,14 +175,14 @@ ffn_status ffn_block_forward_host(const void *x_host, const void *g, const void 
     if (cudaStreamWaitEvent(p.h2d, p.start, 0) != cudaSuccess) return FFN_ERR_CUDA;
     if (cudaStreamWaitEvent(p.d2h, p.start, 0) != cudaSuccess) return FFN_ERR_CUDA;
     for (int i = 0; i < c.count; ++i) {
-        const int64_t r0 = c.rows * i, nr = (i + 1 < c.count) ? c.rows : rows - r0;
+        const int64_t r0 = c.start[i], nr = c.rows(i);
         if (cudaMemcpyAsync(x_dev + r0 * row_bytes, xh + r0 * row_bytes, nr * row_bytes, cudaMemcpyHostToDevice,
                             p.h2d) != cudaSuccess)
             return FFN_ERR_CUDA;
         if (cudaEventRecord(p.landed[i], p.h2d) != cudaSuccess) return FFN_ERR_CUDA;
     }
     for (int i = 0; i < c.count; ++i) {
-        const int64_t r0 = c.rows * i, nr = (i + 1 < c.count) ? c.rows : rows - r0;
+        const int64_t r0 = c.start[i], nr = c.rows(i);
         if (cudaStreamWaitEvent(s, p.landed[i], 0) != cudaSuccess) return FFN_ERR_CUDA;
         st = ffn_block_forward(x_dev + r0 * row_bytes, g, w_gate, w_up, w_down, y_dev + r0 * row_bytes, nr, d, ffn,
                                eps, dtype, flags, block_ws, l.block, stream);
