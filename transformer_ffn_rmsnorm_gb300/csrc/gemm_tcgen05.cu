@@ -670,7 +670,7 @@ int64_t wave_cost(int64_t M, int64_t N, int cols, int width) {
     const int64_t mb = (M + BM - 1) / BM;
     const int64_t ncta = mb > 1 ? 2 : 1;
     const int64_t units = ((mb + ncta - 1) / ncta) * ((N + cols - 1) / cols);
-    const int64_t slots = sm_count() / ncta;
+    const int64_t slots = sm_count() / ncta > 0 ? sm_count() / ncta : 1;
     return ((units + slots - 1) / slots) * width;
 }
 
