@@ -45,7 +45,8 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-sub", action="store_true", help="skip the secondary workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU baseline")
-    ap.add_argument("--workload", choices=["prefill", "decode", "decode_prepared", "q4", "fp8", "q8", "rmsnorm", "swiglu"],
+    ap.add_argument("--workload", choices=["prefill", "decode", "decode_prepared", "batch", "batch_prepared", "q4", "fp8",
+                                           "q8", "rmsnorm", "swiglu"],
                     default="prefill",
                     help="prefill: the benchmark; others run only that workload (for profiling)")
     ap.add_argument("--only-main", action="store_true",
@@ -375,7 +376,7 @@ def q8_bench(torch, ffn, device, hbm, peak_src, stream):
 
 
 def run_workload_only(args):
-    """--workload decode|decode_prepared|q4|fp8|q8|rmsnorm|swiglu: run that workload for --warmup +
+    """--workload decode|decode_prepared|batch|batch_prepared|q4|fp8|q8|rmsnorm|swiglu: run that workload for --warmup +
     --steps calls and print a short line (used for ncu captures)."""
     import torch
     from transformer_ffn_rmsnorm_gb300 import ffn
@@ -398,6 +399,8 @@ def run_workload_only(args):
         cfg, call = fp8_setup(torch, ffn, device)
     elif args.workload == "q8":
         cfg, call = q8_setup(torch, ffn, device)
+    elif args.workload.startswith("batch"):
+        cfg, call = decode_setup(torch, ffn, device, args.workload == "batch_prepared", synth.C8_BATCH_BF16)
     else:
         cfg, call = decode_setup(torch, ffn, device, prepared=args.workload == "decode_prepared")
     for i in range(args.warmup + args.steps):
