@@ -725,7 +725,35 @@ static_assert(Ring<1, 256, true>::KSUB == 2 && Ring<2, 256, true>::KSUB == 1 && 
               "plain_split_plan's stage size");
 
 // out = sum over s of part[s] (s = 0, 1, ...) + res, rounded once to TOut.
-// part: [splits][count] fp32; count (M x N) is a multiple of 8.
+// part: [splits][count] fp32; count (M x N) is a multiple of 8.  One float4
+// a thread; the loads of up to four splits are in flight at once (the
+// partials sit in L2: the kernel is bound by their latency, not bandwidth).
+template <typename TOut>
+__device__ __forceinline__ uint2 pack4(float a, float b, float c, float d) {
+    uint2 v;
+    if constexpr (std::is_same<TOut, __nv_bfloat16>::value) {
+        *reinterpret_cast<__nv_bfloat162 *>(&v.x) = __floats2bfloat162_rn(a, b);
+        *reinterpret_cast<__nv_bfloat162 *>(&v.y) = __floats2bfloat162_rn(c, d);
+    } else {
+        *reinterpret_cast<__half2 *>(&v.x) = __floats2half2_rn(a, b);
+        *reinterpret_cast<__half2 *>(&v.y) = __floats2half2_rn(c, d);
+    }
+    return v;
+}
+
+template <typename TOut>
+__device__ __forceinline__ float4 unpack4(uint2 v) {
+    float2 lo, hi;
+    if constexpr (std::is_same<TOut, __nv_bfloat16>::value) {
+        lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&v.x));
+        hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&v.y));
+    } else {
+        lo = __half22float2(*reinterpret_cast<const __half2 *>(&v.x));
+        hi = __half22float2(*reinterpret_cast<const __half2 *>(&v.y));
+    }
+    return make_float4(lo.x, lo.y, hi.x, hi.y);
+}
+
 template <typename TOut>
 __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float *part, int splits, int64_t count,
                                                             const TOut *res, TOut *out) {
@@ -733,38 +761,48 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float *part, i
     // complete may the kernel after this one start
     ptx::griddep_wait();
     ptx::griddep_launch_dependents();
-    const int64_t nvec = count / 8;
+    const int64_t n4 = count / 4;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nvec; i += stride) {
-        float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        for (int sp = 0; sp < splits; ++sp) {
-            const float4 *src = reinterpret_cast<const float4 *>(part + sp * count) + 2 * i;
-            const float4 a = __ldcs(src), b = __ldcs(src + 1);
-            v[0] += a.x;
-            v[1] += a.y;
-            v[2] += a.z;
-            v[3] += a.w;
-            v[4] += b.x;
-            v[5] += b.y;
-            v[6] += b.z;
-            v[7] += b.w;
+    const float4 *p4 = reinterpret_cast<const float4 *>(part);
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += stride) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        int sp = 0;
+        for (; sp + 4 <= splits; sp += 4) {
+            float4 v[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) v[k] = __ldcs(p4 + (sp + k) * n4 + i);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                acc.x += v[k].x;
+                acc.y += v[k].y;
+                acc.z += v[k].z;
+                acc.w += v[k].w;
+            }
+        }
+        for (; sp < splits; ++sp) {
+            const float4 v = __ldcs(p4 + sp * n4 + i);
+            acc.x += v.x;
+            acc.y += v.y;
+            acc.z += v.z;
+            acc.w += v.w;
         }
         if (res) {
-            float r[8];
-            Vec16<TOut>::unpack(reinterpret_cast<const uint4 *>(res)[i], r);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) v[e] += r[e];
+            const float4 r = unpack4<TOut>(reinterpret_cast<const uint2 *>(res)[i]);
+            acc.x += r.x;
+            acc.y += r.y;
+            acc.z += r.z;
+            acc.w += r.w;
         }
-        reinterpret_cast<uint4 *>(out)[i] = Vec16<TOut>::pack(v);
+        reinterpret_cast<uint2 *>(out)[i] = pack4<TOut>(acc.x, acc.y, acc.z, acc.w);
     }
 }
 
 template <typename TOut>
 cudaError_t launch_splitk_reduce(const float *part, int splits, int64_t count, const void *res, void *out,
                                  cudaStream_t s) {
-    const int64_t nvec = count / 8;
-    int64_t blocks = static_cast<int64_t>(sm_count()) * 4;
-    const int64_t need = (nvec + 255) / 256;
+    const int64_t n4 = count / 4;
+    int64_t blocks = static_cast<int64_t>(sm_count()) * 8;
+    const int64_t need = (n4 + 255) / 256;
     if (blocks > need) blocks = need;
     if (blocks < 1) return cudaSuccess;
     LaunchScope scope(K_SPLITK_REDUCE, s);
