@@ -27,7 +27,9 @@ def host_bf16(a):
 @pytest.mark.parametrize("rows", [8, 300, 3500])
 @pytest.mark.parametrize("prepared", [False, True])
 def test_host_block_matches_device_block(ffn, oracle_lib, rows, prepared):
-    """3500 rows: four chunks (1024, 1024, 1024, 428) through the tensor-core path."""
+    """3500 rows: chunks of 1024, 1452 and 1024 rows through the tensor-core
+    path (every tile sums its whole K in the same order, so the chunked
+    result is bitwise the one-call result)."""
     import torch
     inp = synth.make_block_inputs(synth.C4_PREFILL_BF16, seed=rows, rows=rows, d=256, ffn=384)
     g = to_dev(inp["g"], "bf16")
@@ -44,15 +46,17 @@ def test_host_block_matches_device_block(ffn, oracle_lib, rows, prepared):
     ffn.ffn_device_status()
 
 
-def test_host_block_short_last_chunk(ffn, oracle_lib):
-    """3082 rows: chunks of 1024, 1024, 1024 and 10, the last on the decode path."""
+@pytest.mark.parametrize("total", [1034, 2058])
+def test_host_block_short_chunk(ffn, oracle_lib, total):
+    """1034 rows: chunks of 1024 and 10, the last on the decode path; 2058
+    rows: 1024, 10 and 1024, the middle one on the decode path."""
     import torch
-    inp = synth.make_block_inputs(synth.C4_PREFILL_BF16, seed=9, rows=3082, d=512, ffn=704)
+    inp = synth.make_block_inputs(synth.C4_PREFILL_BF16, seed=9, rows=total, d=512, ffn=704)
     args = [to_dev(inp[k], "bf16") for k in ("g", "w_gate", "w_up", "w_down")]
     y = ffn.ffn_block_forward_host(host_bf16(inp["x"]), *args, eps=inp["cfg"].eps)
     torch.cuda.current_stream().synchronize()
     got = to_host64(y)
-    rows = np.r_[0:40, 1015:1035, 2040:2055, 3060:3082]
+    rows = np.unique(np.r_[0:40, 1015:1040, total - 30:total])
     ref = oracle_lib.block_from_inputs(inp, rows=rows)
     assert_lowp(got[rows], ref)
     ffn.ffn_device_status()
