@@ -57,6 +57,7 @@ def test_host_block_short_chunk(ffn, oracle_lib, total):
     torch.cuda.current_stream().synchronize()
     got = to_host64(y)
     rows = np.unique(np.r_[0:40, 1015:1040, total - 30:total])
+    rows = rows[rows < total]
     ref = oracle_lib.block_from_inputs(inp, rows=rows)
     assert_lowp(got[rows], ref)
     ffn.ffn_device_status()
