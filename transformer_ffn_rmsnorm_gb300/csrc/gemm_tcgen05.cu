@@ -54,8 +54,9 @@ constexpr int NUM_THREADS = 192;
 // A_TERMS = 2: the A operand is given as two bf16 matrices whose sum is the
 // fp32 value (hi + lo); both are multiplied by the same B tile and accumulate
 // into the same TMEM accumulator, so A carries ~16 significant bits.
-// BN: accumulator columns per tile (256, or 224 for the plain GEMM when it
-// evens out the waves); the B tile is BN rows of 64 k values, all of them in
+// BN: accumulator columns per tile (256; 224 for the plain GEMM when it
+// evens out the waves; with few row blocks 192, or 64 for a down GEMM whose
+// reduction is too short to split); the B tile is BN rows of 64 k values, all of them in
 // this CTA's ring, or (PAIR) BN/2 of them, the peer CTA holding the others.
 // The ring takes as many stages as fit in 225 KB; a CTA therefore always
 // holds more than half of the SM's shared memory, so two of these CTAs
@@ -701,27 +702,35 @@ int gateup_width(int64_t M, int64_t N) {
 // (at least kMinSplitKBlocks 64-wide k blocks each) that together fill the
 // SMs; each run stores an fp32 partial tile, and splitk_reduce_kernel adds
 // them in split order (deterministic) with the residual, rounding once.
-// Returns the split count (1: no split) and the stages per run.
+// Tiles are 192 wide when those can be split (fewer splits, so less partial
+// traffic: 4096 columns at 64-256 rows 1-3 % faster than 256 wide), else 256.
+// Returns the split count (1: no split), the stages per run and the width.
 constexpr int kMinSplitKBlocks = 8, kMaxSplits = 16;
-int plain_split_plan(int64_t M, int64_t K, int64_t N, int a_terms, int *kst_per_split) {
+int plain_split_plan(int64_t M, int64_t K, int64_t N, int a_terms, int *kst_per_split, int *width) {
     const int64_t mb = (M + BM - 1) / BM;
     const bool pair = mb > 1;
     const int64_t ncta = pair ? 2 : 1;
-    const int64_t units = ((mb + ncta - 1) / ncta) * ((N + 255) / 256);
     const int64_t slots = sm_count() / ncta;
     const int64_t kblocks = (K + BK - 1) / BK;
-    const int64_t ksub = (pair && a_terms == 1) ? 2 : 1;   // Ring<a_terms, 256, pair>::KSUB
+    const int64_t ksub = (pair && a_terms == 1) ? 2 : 1;   // Ring<a_terms, BN, pair>::KSUB
     const int64_t nst = (kblocks + ksub - 1) / ksub;
-    if (M <= 0 || 2 * units > slots) return 1;
-    int64_t sp = slots / units;
-    if (sp > kblocks / kMinSplitKBlocks) sp = kblocks / kMinSplitKBlocks;
-    if (sp > kMaxSplits) sp = kMaxSplits;
-    if (sp < 2) return 1;
-    const int64_t per = (nst + sp - 1) / sp;
-    if (kst_per_split) *kst_per_split = static_cast<int>(per);
-    return static_cast<int>((nst + per - 1) / per);
+    if (M <= 0) return 1;
+    for (int bn : {192, 256}) {
+        const int64_t units = ((mb + ncta - 1) / ncta) * ((N + bn - 1) / bn);
+        if (2 * units > slots) continue;
+        int64_t sp = slots / units;
+        if (sp > kblocks / kMinSplitKBlocks) sp = kblocks / kMinSplitKBlocks;
+        if (sp > kMaxSplits) sp = kMaxSplits;
+        if (sp < 2) return 1;
+        const int64_t per = (nst + sp - 1) / sp;
+        if (kst_per_split) *kst_per_split = static_cast<int>(per);
+        if (width) *width = bn;
+        return static_cast<int>((nst + per - 1) / per);
+    }
+    return 1;
 }
-static_assert(Ring<1, 256, true>::KSUB == 2 && Ring<2, 256, true>::KSUB == 1 && Ring<1, 256, false>::KSUB == 1,
+static_assert(Ring<1, 256, true>::KSUB == 2 && Ring<2, 256, true>::KSUB == 1 && Ring<1, 256, false>::KSUB == 1 &&
+                  Ring<1, 192, true>::KSUB == 2 && Ring<1, 192, false>::KSUB == 1,
               "plain_split_plan's stage size");
 
 // out = sum over s of part[s] (s = 0, 1, ...) + res, rounded once to TOut.
@@ -829,12 +838,17 @@ template <bool BF16, int A_TERMS, bool OUT_BF16>
 cudaError_t launch_plain_bn(const void *A, const void *A_lo, const void *B, void *C, int64_t M, int64_t K,
                             int64_t N, float acc_scale, const void *res, float *part, cudaStream_t s) {
     using TOut = typename std::conditional<OUT_BF16, __nv_bfloat16, __half>::type;
-    int per = 0;
-    const int splits = plain_split_plan(M, K, N, A_TERMS, &per);
+    int per = 0, bn = 256;
+    const int splits = plain_split_plan(M, K, N, A_TERMS, &per, &bn);
     if (splits > 1) {
         if (!part) return cudaErrorInvalidValue;
-        cudaError_t e = launch_impl<MODE_PLAIN, BF16, A_TERMS, OUT_BF16, 256>(
-            A, A_lo, B, nullptr, C, nullptr, M, K, N, K_GEMM_DOWN, acc_scale, 1.f, s, nullptr, part, per, splits);
+        cudaError_t e =
+            bn == 192 ? launch_impl<MODE_PLAIN, BF16, A_TERMS, OUT_BF16, 192>(A, A_lo, B, nullptr, C, nullptr, M, K, N,
+                                                                              K_GEMM_DOWN, acc_scale, 1.f, s, nullptr,
+                                                                              part, per, splits)
+                      : launch_impl<MODE_PLAIN, BF16, A_TERMS, OUT_BF16, 256>(A, A_lo, B, nullptr, C, nullptr, M, K, N,
+                                                                              K_GEMM_DOWN, acc_scale, 1.f, s, nullptr,
+                                                                              part, per, splits);
         if (e != cudaSuccess) return e;
         return launch_splitk_reduce<TOut>(part, splits, M * N, res, C, s);
     }
@@ -858,7 +872,7 @@ size_t gemm_plain_partial_bytes(int64_t M, int64_t K, int64_t N, int a_terms) {
     size_t most = 0;
     for (int64_t mb = 1; mb <= (M + BM - 1) / BM; ++mb) {
         const int64_t rows = mb * BM < M ? mb * BM : M;
-        const int splits = plain_split_plan(rows, K, N, a_terms, nullptr);
+        const int splits = plain_split_plan(rows, K, N, a_terms, nullptr, nullptr);
         if (splits <= 1) {
             if (mb > 1) break;   // more row blocks, more tiles: no split from here on
             continue;
