@@ -156,7 +156,9 @@ ffn_status ffn_block_forward(const void *x, const void *g, const void *w_gate, c
  *   x_host, y_host: [rows x d] of `dtype` in host memory, not overlapping.
  *   g, w_gate, w_up, w_down: device pointers as in ffn_block_forward.
  *   workspace: device scratch of ffn_block_host_workspace_bytes() bytes
- *   (x and y are staged there, plus the block's own scratch).
+ *   (two sets of x and y staging buffers, used by consecutive calls in
+ *   turn so that a call's input copies overlap the compute of the call
+ *   before it, plus the block's own scratch).
  * The rows are split into chunks (above 1024 rows: first and last chunks of
  * 1024 rows, the rows between in chunks of at most 2048); the input copy of
  * every chunk is queued at once on a copy stream owned by the library, each

@@ -38,7 +38,8 @@ def test_host_block_matches_device_block(ffn, oracle_lib, rows, prepared):
     if prepared:
         w = [ffn.ffn_prepare_weights(t) for t in w]
         flags = ffn.FFN_PREPARED_WEIGHTS
-    y_host = ffn.ffn_block_forward_host(host_bf16(inp["x"]), g, *w, eps=inp["cfg"].eps, flags=flags)
+    xh = host_bf16(inp["x"])   # alive until the stream has passed the call
+    y_host = ffn.ffn_block_forward_host(xh, g, *w, eps=inp["cfg"].eps, flags=flags)
     torch.cuda.current_stream().synchronize()
     y_dev = ffn.ffn_block_forward(to_dev(inp["x"], "bf16"), g, *w, eps=inp["cfg"].eps, flags=flags)
     assert torch.equal(y_host.view(torch.int16), y_dev.cpu().view(torch.int16))
@@ -53,7 +54,8 @@ def test_host_block_short_chunk(ffn, oracle_lib, total):
     import torch
     inp = synth.make_block_inputs(synth.C4_PREFILL_BF16, seed=9, rows=total, d=512, ffn=704)
     args = [to_dev(inp[k], "bf16") for k in ("g", "w_gate", "w_up", "w_down")]
-    y = ffn.ffn_block_forward_host(host_bf16(inp["x"]), *args, eps=inp["cfg"].eps)
+    xh = host_bf16(inp["x"])   # alive until the stream has passed the call
+    y = ffn.ffn_block_forward_host(xh, *args, eps=inp["cfg"].eps)
     torch.cuda.current_stream().synchronize()
     got = to_host64(y)
     rows = np.unique(np.r_[0:40, 1015:1040, total - 30:total])
@@ -63,21 +65,22 @@ def test_host_block_short_chunk(ffn, oracle_lib, total):
     ffn.ffn_device_status()
 
 
-def test_host_block_twice_in_a_row_and_empty(ffn):
-    """Back-to-back calls reuse the staging buffers; the second must wait for
-    the first's copies.  An empty batch is valid and queues nothing."""
+def test_host_block_calls_in_a_row_and_empty(ffn):
+    """Back-to-back calls on one workspace use its two staging sets in turn:
+    the third call's input copies must wait until the first call has
+    computed from that set, and its compute until the first call's output
+    copies have drained it.  An empty batch is valid and queues nothing."""
     import torch
-    inp = synth.make_block_inputs(synth.C4_PREFILL_BF16, seed=3, rows=2600, d=256, ffn=384)
-    inp2 = synth.make_block_inputs(synth.C4_PREFILL_BF16, seed=4, rows=2600, d=256, ffn=384)
-    args = [to_dev(inp[k], "bf16") for k in ("g", "w_gate", "w_up", "w_down")]
+    inps = [synth.make_block_inputs(synth.C4_PREFILL_BF16, seed=3 + k, rows=2600, d=256, ffn=384)
+            for k in range(4)]
+    args = [to_dev(inps[0][k], "bf16") for k in ("g", "w_gate", "w_up", "w_down")]
     ws = ffn.workspace(ffn.ffn_block_host_workspace_bytes(2600, 256, 384, torch.bfloat16), torch.device("cuda"))
-    y1 = ffn.ffn_block_forward_host(host_bf16(inp["x"]), *args, eps=1e-6, ws=ws)
-    y2 = ffn.ffn_block_forward_host(host_bf16(inp2["x"]), *args, eps=1e-6, ws=ws)
+    xs = [host_bf16(inp["x"]) for inp in inps]   # kept alive until the copies have run
+    ys = [ffn.ffn_block_forward_host(x, *args, eps=1e-6, ws=ws) for x in xs]
     torch.cuda.current_stream().synchronize()
-    r1 = ffn.ffn_block_forward(to_dev(inp["x"], "bf16"), *args, eps=1e-6).cpu()
-    r2 = ffn.ffn_block_forward(to_dev(inp2["x"], "bf16"), *args, eps=1e-6).cpu()
-    assert torch.equal(y1.view(torch.int16), r1.view(torch.int16))
-    assert torch.equal(y2.view(torch.int16), r2.view(torch.int16))
+    for inp, y in zip(inps, ys):
+        r = ffn.ffn_block_forward(to_dev(inp["x"], "bf16"), *args, eps=1e-6).cpu()
+        assert torch.equal(y.view(torch.int16), r.view(torch.int16))
     e = torch.empty((0, 256), dtype=torch.bfloat16).pin_memory()
     assert ffn.ffn_block_forward_host(e, *args, eps=1e-6).numel() == 0
     ffn.ffn_device_status()

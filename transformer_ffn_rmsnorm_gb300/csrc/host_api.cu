@@ -6,7 +6,9 @@
 // library's own, each chunk's block runs on the caller's stream as soon as its
 // rows have landed, and its device-to-host copy runs on a second copy stream
 // while the next chunk computes.  The caller's stream finally waits for the
-// last copy, so synchronising that stream means y is in host memory.
+// last copy, so synchronising that stream means y is in host memory.  The
+// staging buffers come in two sets used by consecutive calls in turn, so one
+// call's input copies run while the call before it still computes.
 //
 // Only the first chunk's input copy and the last chunk's output copy are
 // exposed (the host link of a GB300 moves about 200 GB/s each way for
@@ -73,8 +75,10 @@ Chunks plan_chunks(int64_t rows) {
 int64_t elem_bytes(ffn_dtype dt) { return dt == FFN_F32 ? 4 : 2; }
 size_t align256(size_t v) { return (v + 255) & ~size_t{255}; }
 
+// The workspace holds two sets of x and y staging buffers, used by calls in
+// turn, and the block's scratch (sized for the largest chunk).
 struct Layout {
-    size_t x_stage, y_stage, block, total;   // byte sizes; block = scratch of the largest chunk
+    size_t x_stage, y_stage, block, total;   // byte sizes of one x and one y staging buffer, scratch, all
 };
 
 ffn_status layout(int64_t rows, int64_t d, int64_t ffn, ffn_dtype dt, uint32_t flags, Layout *l) {
@@ -95,15 +99,22 @@ ffn_status layout(int64_t rows, int64_t d, int64_t ffn, ffn_dtype dt, uint32_t f
     l->x_stage = align256(static_cast<size_t>(rows) * d * elem_bytes(dt));
     l->y_stage = l->x_stage;
     l->block = align256(block);
-    l->total = l->x_stage + l->y_stage + l->block;
+    l->total = 2 * (l->x_stage + l->y_stage) + l->block;
     return FFN_OK;
 }
 
 // Copy streams and events of one device, created on first use and kept for
 // the life of the process.
+// Calls alternate between the two staging sets: a call's input copies wait
+// only until the call before the previous one has finished computing from
+// that set's x (x_free), and its compute until that call's output copies
+// have drained that set's y (y_free), so the input copies of a call overlap
+// the compute of the call before it.
 struct Pipe {
     cudaStream_t h2d = nullptr, d2h = nullptr;
-    cudaEvent_t start = nullptr, end = nullptr, landed[kMaxChunks] = {}, computed[kMaxChunks] = {};
+    cudaEvent_t landed[kMaxChunks] = {}, computed[kMaxChunks] = {};
+    cudaEvent_t x_free[2] = {}, y_free[2] = {};
+    int next = 0;   // staging set of the next call
     bool ready = false;
 };
 std::mutex g_pipe_mu;
@@ -114,8 +125,10 @@ bool make_pipe(Pipe &p) {
     const unsigned ev = cudaEventDisableTiming;
     if (cudaStreamCreateWithFlags(&p.h2d, cudaStreamNonBlocking) != cudaSuccess) return false;
     if (cudaStreamCreateWithFlags(&p.d2h, cudaStreamNonBlocking) != cudaSuccess) return false;
-    if (cudaEventCreateWithFlags(&p.start, ev) != cudaSuccess) return false;
-    if (cudaEventCreateWithFlags(&p.end, ev) != cudaSuccess) return false;
+    for (int b = 0; b < 2; ++b) {
+        if (cudaEventCreateWithFlags(&p.x_free[b], ev) != cudaSuccess) return false;
+        if (cudaEventCreateWithFlags(&p.y_free[b], ev) != cudaSuccess) return false;
+    }
     for (int i = 0; i < kMaxChunks; ++i) {
         if (cudaEventCreateWithFlags(&p.landed[i], ev) != cudaSuccess) return false;
         if (cudaEventCreateWithFlags(&p.computed[i], ev) != cudaSuccess) return false;
@@ -163,17 +176,20 @@ ffn_status ffn_block_forward_host(const void *x_host, const void *g, const void 
     Pipe &p = g_pipes[dev];
     if (!make_pipe(p)) return FFN_ERR_CUDA;
 
+    const int b = p.next;
+    p.next ^= 1;
     char *ws = static_cast<char *>(workspace);
-    char *x_dev = ws, *y_dev = ws + l.x_stage, *block_ws = ws + l.x_stage + l.y_stage;
+    char *x_dev = ws + b * (l.x_stage + l.y_stage), *y_dev = x_dev + l.x_stage;
+    char *block_ws = ws + 2 * (l.x_stage + l.y_stage);
     const char *xh = static_cast<const char *>(x_host);
     char *yh = static_cast<char *>(y_host);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const Chunks c = plan_chunks(rows);
 
-    // the staging buffers may still be in use by work queued before this call
-    if (cudaEventRecord(p.start, s) != cudaSuccess) return FFN_ERR_CUDA;
-    if (cudaStreamWaitEvent(p.h2d, p.start, 0) != cudaSuccess) return FFN_ERR_CUDA;
-    if (cudaStreamWaitEvent(p.d2h, p.start, 0) != cudaSuccess) return FFN_ERR_CUDA;
+    // this staging set's x may still be read, and its y still be copied out,
+    // by the call before the previous one
+    if (cudaStreamWaitEvent(p.h2d, p.x_free[b], 0) != cudaSuccess) return FFN_ERR_CUDA;
+    if (cudaStreamWaitEvent(s, p.y_free[b], 0) != cudaSuccess) return FFN_ERR_CUDA;
     for (int i = 0; i < c.count; ++i) {
         const int64_t r0 = c.start[i], nr = c.rows(i);
         if (cudaMemcpyAsync(x_dev + r0 * row_bytes, xh + r0 * row_bytes, nr * row_bytes, cudaMemcpyHostToDevice,
@@ -193,8 +209,9 @@ ffn_status ffn_block_forward_host(const void *x_host, const void *g, const void 
                             p.d2h) != cudaSuccess)
             return FFN_ERR_CUDA;
     }
-    if (cudaEventRecord(p.end, p.d2h) != cudaSuccess) return FFN_ERR_CUDA;
-    if (cudaStreamWaitEvent(s, p.end, 0) != cudaSuccess) return FFN_ERR_CUDA;
+    if (cudaEventRecord(p.x_free[b], s) != cudaSuccess) return FFN_ERR_CUDA;
+    if (cudaEventRecord(p.y_free[b], p.d2h) != cudaSuccess) return FFN_ERR_CUDA;
+    if (cudaStreamWaitEvent(s, p.y_free[b], 0) != cudaSuccess) return FFN_ERR_CUDA;
     return FFN_OK;
 }
 
