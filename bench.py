@@ -654,7 +654,8 @@ def run_ours(args):
             "e2e": {"value": e2e_val, "unit": "tokens/s",
                     "h2d_bytes_per_step": cfg.rows * cfg.d * 2, "d2h_bytes_per_step": cfg.rows * cfg.d * 2,
                     "path": "ffn_block_forward_host (C ABI; pinned host x and y; copies overlapped with the "
-                            "compute in chunks: 1024, 2048, 1024 rows)"},
+                            "compute in chunks of 3072 and 1024 rows; two staging sets, so each call's input copy overlaps the "
+                            "previous call's compute)"},
             "cpu_baseline": cpu, "parity": parity, "sub": sub,
         }
         print(json.dumps(line), flush=True)

@@ -159,8 +159,8 @@ ffn_status ffn_block_forward(const void *x, const void *g, const void *w_gate, c
  *   (two sets of x and y staging buffers, used by consecutive calls in
  *   turn so that a call's input copies overlap the compute of the call
  *   before it, plus the block's own scratch).
- * The rows are split into chunks (above 1024 rows: first and last chunks of
- * 1024 rows, the rows between in chunks of at most 2048); the input copy of
+ * The rows are split into chunks (above 1024 rows: a last chunk of 1024
+ * rows, the rows before it in chunks of at most 4096); the input copy of
  * every chunk is queued at once on a copy stream owned by the library, each
  * chunk's block runs on `stream` when its rows have landed, and its output
  * copy runs on a second library stream while the next chunk computes.

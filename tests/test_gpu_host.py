@@ -27,9 +27,9 @@ def host_bf16(a):
 @pytest.mark.parametrize("rows", [8, 300, 3500])
 @pytest.mark.parametrize("prepared", [False, True])
 def test_host_block_matches_device_block(ffn, oracle_lib, rows, prepared):
-    """3500 rows: chunks of 1024, 1452 and 1024 rows through the tensor-core
-    path (every tile sums its whole K in the same order, so the chunked
-    result is bitwise the one-call result)."""
+    """3500 rows: chunks of 2476 and 1024 rows through the tensor-core path
+    (every tile sums its whole K in the same order, so the chunked result is
+    bitwise the one-call result)."""
     import torch
     inp = synth.make_block_inputs(synth.C4_PREFILL_BF16, seed=rows, rows=rows, d=256, ffn=384)
     g = to_dev(inp["g"], "bf16")
@@ -49,8 +49,8 @@ def test_host_block_matches_device_block(ffn, oracle_lib, rows, prepared):
 
 @pytest.mark.parametrize("total", [1034, 2058])
 def test_host_block_short_chunk(ffn, oracle_lib, total):
-    """1034 rows: chunks of 1024 and 10, the last on the decode path; 2058
-    rows: 1024, 10 and 1024, the middle one on the decode path."""
+    """1034 rows: chunks of 10 and 1024, the first on the decode path; 2058
+    rows: 1034 and 1024."""
     import torch
     inp = synth.make_block_inputs(synth.C4_PREFILL_BF16, seed=9, rows=total, d=512, ffn=704)
     args = [to_dev(inp[k], "bf16") for k in ("g", "w_gate", "w_up", "w_down")]

@@ -10,19 +10,21 @@
 // staging buffers come in two sets used by consecutive calls in turn, so one
 // call's input copies run while the call before it still computes.
 //
-// Only the first chunk's input copy and the last chunk's output copy are
-// exposed (the host link of a GB300 moves about 200 GB/s each way for
-// page-locked memory, 160 GB/s each way when both directions run), so the
-// edge chunks are short; but each chunk's GEMMs run in whole waves and pay
-// their ramp and drain, so the chunks between are long.  Measured on 4096 x
-// 4096 -> 11008 (prepared weights, burst clocks), x and y on the host:
-//   chunks 1024 x 4            836 us (compute alone 723 us)
-//   1024, 2048, 1024           797 us (691 us)
-//   512, 3072, 512             791 us (719 us)
-//   768, 2560, 768             827 us;  256, 3584, 256  868 us (the middle
-//                              chunk's copies outlast the edge chunks)
-//   one chunk of 4096          989 us (635 us)
-// The plan: edge chunks of 1024 rows, the middle in chunks of at most 2048.
+// With calls back to back, every input copy runs while the call before
+// computes, and only the last chunk's output copy is exposed (the host link
+// of a GB300 moves about 200 GB/s each way for page-locked memory, 160 GB/s
+// each way when both directions run).  Each chunk's GEMMs pay a ramp, a
+// drain and a partly filled last wave, so few, long chunks compute fastest;
+// the last one is short because its output copy is exposed.  Measured on
+// 4096 x 4096 -> 11008 (prepared weights, burst clocks), calls back to back,
+// x and y on the host (in brackets the same chunks computed from device
+// memory):
+//   3072, 1024                 722 us (646-654 us)
+//   1024, 2048, 1024           766 us (689 us)
+//   3584, 512                  753-765 us;  2048, 2048  793-805 us
+//   2048, 1024, 1024           781-819 us;  3072, 512, 512  787-838 us
+// A single call, with nothing before it to overlap, also pays the first
+// chunk's input copy (3072 rows: ~125 us).
 #include <cstring>
 #include <mutex>
 
@@ -41,9 +43,10 @@ struct Chunks {
     int64_t rows(int i) const { return start[i + 1] - start[i]; }
 };
 
-// First and last chunks of kEdgeRows, the rows between in near-equal chunks
-// of at most kMidRows (multiples of 256), at most kMaxChunks in all.
-constexpr int64_t kEdgeRows = 1024, kMidRows = 2048;
+// A last chunk of kLastRows (its output copy is the one exposed), the rows
+// before it in near-equal chunks of at most kFrontRows (multiples of 256),
+// at most kMaxChunks in all.
+constexpr int64_t kLastRows = 1024, kFrontRows = 4096;
 Chunks plan_chunks(int64_t rows) {
     Chunks c;
     c.count = 0;
@@ -53,22 +56,16 @@ Chunks plan_chunks(int64_t rows) {
         c.start[c.count + 1] = c.start[c.count] + n;
         ++c.count;
     };
-    if (rows <= kEdgeRows) {
+    if (rows <= kLastRows) {
         push(rows);
         return c;
     }
-    if (rows <= 2 * kEdgeRows) {
-        push(kEdgeRows);
-        push(rows - kEdgeRows);
-        return c;
-    }
-    const int64_t mid = rows - 2 * kEdgeRows;
-    int64_t pieces = (mid + kMidRows - 1) / kMidRows;
-    if (pieces > kMaxChunks - 2) pieces = kMaxChunks - 2;
-    const int64_t each = ((mid + pieces - 1) / pieces + 255) / 256 * 256;
-    push(kEdgeRows);
-    for (int64_t left = mid; left > 0; left -= each) push(left < each ? left : each);
-    push(kEdgeRows);
+    const int64_t front = rows - kLastRows;
+    int64_t pieces = (front + kFrontRows - 1) / kFrontRows;
+    if (pieces > kMaxChunks - 1) pieces = kMaxChunks - 1;
+    const int64_t each = ((front + pieces - 1) / pieces + 255) / 256 * 256;
+    for (int64_t left = front; left > 0; left -= each) push(left < each ? left : each);
+    push(kLastRows);
     return c;
 }
 
