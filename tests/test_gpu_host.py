@@ -24,12 +24,12 @@ def host_bf16(a):
     return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).pin_memory()
 
 
-@pytest.mark.parametrize("rows", [8, 300, 3500])
+@pytest.mark.parametrize("rows", [8, 300, 3500, 9000])
 @pytest.mark.parametrize("prepared", [False, True])
 def test_host_block_matches_device_block(ffn, oracle_lib, rows, prepared):
-    """3500 rows: chunks of 2476 and 1024 rows through the tensor-core path
-    (every tile sums its whole K in the same order, so the chunked result is
-    bitwise the one-call result)."""
+    """3500 rows: chunks of 2476 and 1024 rows; 9000 rows: 4096, 3880 and
+    1024; all through the tensor-core path (every tile sums its whole K in
+    the same order, so the chunked result is bitwise the one-call result)."""
     import torch
     inp = synth.make_block_inputs(synth.C4_PREFILL_BF16, seed=rows, rows=rows, d=256, ffn=384)
     g = to_dev(inp["g"], "bf16")
