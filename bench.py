@@ -24,6 +24,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -100,7 +101,7 @@ class ClockSampler:
     def __init__(self, device_uuid: str | None):
         self.uuid = device_uuid
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        self.path = os.path.join(tempfile.gettempdir(), f"ffn_bench_clocks_{os.getpid()}.csv")
 
     def __enter__(self):
         try:
