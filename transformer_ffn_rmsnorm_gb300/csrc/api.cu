@@ -128,11 +128,12 @@ ffn_status plan_block(int64_t rows, int64_t d, int64_t ffn, ffn_dtype dt, uint32
     if (dt == FFN_F32 && (flags & (FFN_PATH_GEMM | FFN_PATH_GEMV))) return FFN_ERR_FLAGS;
     if ((flags & FFN_PATH_GEMV) && rows > kGemvMaxRows) return FFN_ERR_SHAPE;
     // rows up to which these flags take the decode kernels.  Measured
-    // crossover on 4096 -> 14336 (graph-replayed block): the GEMMs
-    // (one-row-block tiles, split-K down projection) take 85-90 us at 16-128
-    // rows; the weight-streaming kernels 68 / 80 us at 16 rows (one-term /
-    // hi + lo operands), 80 / 107 us at 32, 110 / 173 us at 33 (eight token
-    // tiles).  Two-term operands double their MMAs.
+    // crossover on 4096 -> 14336 (graph-replayed block, one-term / hi + lo
+    // operands): the GEMMs (one-row-block tiles, split-K down projection)
+    // take 81 / 89 us at 16 rows, 79 / 84 us at 32, 78-81 / 83-86 us at
+    // 64-128; the weight-streaming kernels 66 / 80 us at 16, 76 / 87 us at
+    // 17, 79 / 84 us at 32, 110 / 173 us at 33 (eight token tiles).
+    // Two-term operands double their MMAs.
     int64_t gemv_rows = 0;
     if (dt != FFN_F32 && !(flags & FFN_PATH_GEMM))
         gemv_rows = (flags & FFN_PATH_GEMV) ? kGemvMaxRows
