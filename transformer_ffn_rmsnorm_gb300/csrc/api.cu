@@ -95,18 +95,6 @@ ffn_status check_block_shape(int64_t rows, int64_t d, int64_t ffn, ffn_dtype dt)
     return FFN_OK;
 }
 
-// Rows of n and h on the tensor-core path: the batch rounded up to whole
-// tiles of the projections' operand (128 rows for one row block, else whole
-// CTA pairs of 256).  The rmsnorm fills the rows past the batch with a
-// constant: operand tiles whose rows past the batch were zero (the copy
-// engine's fill for rows past a buffer) ran the gate/up GEMM 15-20 % slower
-// (4096 -> 14336, prepared weights: 320-448 rows 143-145 us against 131 us
-// at 512).  Those rows' results are never stored.
-int64_t gemm_rows(int64_t rows) {
-    if (rows <= 128) return 128;
-    return (rows + 255) / 256 * 256;
-}
-
 ffn_status plan_block(int64_t rows, int64_t d, int64_t ffn, ffn_dtype dt, uint32_t flags,
                       Plan *plan) {
     ffn_status st = check_block_shape(rows, d, ffn, dt);
@@ -151,10 +139,9 @@ ffn_status plan_block(int64_t rows, int64_t d, int64_t ffn, ffn_dtype dt, uint32
         case PATH_GEMV:
             plan->workspace = rows == 0 ? 0 : gemv_workspace_bytes(rows, d, ffn, plan->split_act);
             break;
-        case PATH_GEMM: {   // n and h (and their residuals); both 2 bytes when prepared
-            const size_t rp = static_cast<size_t>(gemm_rows(rows));
-            plan->workspace = align256(rp * d * es) + align256(rp * ffn * es);
-            if (plan->split_act) plan->workspace += align256(rp * d * es) + align256(rp * ffn * es);
+        case PATH_GEMM:   // n and h (and their residuals); both 2 bytes when prepared
+            plan->workspace = align256(r * d * es) + align256(r * ffn * es);
+            if (plan->split_act) plan->workspace += align256(r * d * es) + align256(r * ffn * es);
             if (!plan->fused) plan->workspace += 2 * align256(r * ffn * 4);
             // split-K partial sums of the down GEMM (few rows)
             plan->workspace += align256(gemm_plain_partial_bytes(rows, ffn, d, plan->split_act ? 2 : 1));
@@ -164,7 +151,6 @@ ffn_status plan_block(int64_t rows, int64_t d, int64_t ffn, ffn_dtype dt, uint32
                 plan->workspace = std::max(plan->workspace, gemv_workspace_bytes(std::min(rows, gemv_rows), d, ffn,
                                                                                   plan->split_act));
             break;
-        }
     }
     return FFN_OK;
 }
@@ -334,9 +320,8 @@ ffn_status ffn_block_forward(const void *x, const void *g, const void *w_gate, c
             return from_cuda(launch_gemv_block(wf, x, g, a, b, c, y, rows, d, ffn, eps, gw, s, res));
         }
         case PATH_GEMM: {
-            const int64_t rp = gemm_rows(rows);   // rows of n and h, the padding filled by the rmsnorm
-            const size_t nb = align256(static_cast<size_t>(rp) * d * es);
-            const size_t hb = align256(static_cast<size_t>(rp) * ffn * es);
+            const size_t nb = align256(static_cast<size_t>(rows) * d * es);
+            const size_t hb = align256(static_cast<size_t>(rows) * ffn * es);
             char *p = ws;
             void *n = p;
             p += nb;
@@ -360,27 +345,27 @@ ffn_status ffn_block_forward(const void *x, const void *g, const void *w_gate, c
             const float h_scale = plan.prepared ? 1.f / 256.f : 1.f;
             cudaError_t e;
             if (plan.prepared)
-                e = launch_rmsnorm_to_f16(x, g, n, rows, d, eps, dtype, s, rp);
+                e = launch_rmsnorm_to_f16(x, g, n, rows, d, eps, dtype, s);
             else if (plan.split_act)
-                e = launch_rmsnorm_split(x, g, n, n_lo, rows, d, eps, dtype, s, rp);
+                e = launch_rmsnorm_split(x, g, n, n_lo, rows, d, eps, dtype, s);
             else
-                e = launch_rmsnorm(x, g, n, rows, d, eps, dtype, s, rp);
+                e = launch_rmsnorm(x, g, n, rows, d, eps, dtype, s);
             if (e != cudaSuccess) return FFN_ERR_CUDA;
             // split-K partials: after h, or after G and U when unfused
             float *part = reinterpret_cast<float *>(
                 plan.fused ? p : p + 2 * align256(static_cast<size_t>(rows) * ffn * 4));
             if (plan.fused) {
-                e = launch_gemm_gateup(op, n, n_lo, w_gate, w_up, h, h_lo, nullptr, nullptr, rows, rp, d,
+                e = launch_gemm_gateup(op, n, n_lo, w_gate, w_up, h, h_lo, nullptr, nullptr, rows, d,
                                        ffn, true, w_unscale, h_scale, s);
             } else {
                 float *G = reinterpret_cast<float *>(p);
                 float *U = reinterpret_cast<float *>(p + align256(static_cast<size_t>(rows) * ffn * 4));
-                e = launch_gemm_gateup(op, n, n_lo, w_gate, w_up, nullptr, nullptr, G, U, rows, rp, d, ffn,
+                e = launch_gemm_gateup(op, n, n_lo, w_gate, w_up, nullptr, nullptr, G, U, rows, d, ffn,
                                        false, w_unscale, 1.f, s);
                 if (e == cudaSuccess) e = launch_swiglu_f32in(G, U, h, h_lo, rows * ffn, op, h_scale, s);
             }
             if (e != cudaSuccess) return FFN_ERR_CUDA;
-            return from_cuda(launch_gemm_plain(op, dtype, h, h_lo, w_down, y, rows, rp, ffn, d,
+            return from_cuda(launch_gemm_plain(op, dtype, h, h_lo, w_down, y, rows, ffn, d,
                                                w_unscale / h_scale, res, part, s));
         }
     }

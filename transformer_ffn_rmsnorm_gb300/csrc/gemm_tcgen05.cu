@@ -553,7 +553,7 @@ bool make_map(CUtensorMap *m, const void *ptr, bool bf16, int64_t inner, int64_t
 
 template <int MODE, bool BF16, int A_TERMS, bool OUT_BF16, int BN, bool PAIR>
 cudaError_t launch_kernel(const void *A, const void *A2, const void *B0, const void *B1, void *out0,
-                          void *out1, int64_t M, int64_t a_rows, int64_t K, int64_t N, int kind, float acc_scale,
+                          void *out1, int64_t M, int64_t K, int64_t N, int kind, float acc_scale,
                           float out_scale, const void *res, float *part, int kst_per_split, int splits,
                           cudaStream_t s) {
     constexpr size_t SMEM_BYTES = Ring<A_TERMS, BN, PAIR>::SMEM_BYTES;
@@ -590,10 +590,9 @@ cudaError_t launch_kernel(const void *A, const void *A2, const void *B0, const v
     const int64_t ncols = MODE == MODE_PLAIN ? BN : BN / 2;
     const int64_t num_n_blocks = (N + ncols - 1) / ncols;
     CUtensorMap ma, ma2, mb0, mb1;
-    // A's tensor map spans its a_rows (>= M) allocated rows
-    if (!make_map(&ma, A, BF16, K, a_rows, BM)) return cudaErrorInvalidValue;
+    if (!make_map(&ma, A, BF16, K, M, BM)) return cudaErrorInvalidValue;
     ma2 = ma;
-    if (A_TERMS == 2 && !make_map(&ma2, A2, BF16, K, a_rows, BM)) return cudaErrorInvalidValue;
+    if (A_TERMS == 2 && !make_map(&ma2, A2, BF16, K, M, BM)) return cudaErrorInvalidValue;
     if (MODE == MODE_PLAIN) {
         // with a pair, each CTA loads half of the B tile
         if (!make_map(&mb0, B0, BF16, K, N, static_cast<uint32_t>(BN / NCTA))) return cudaErrorInvalidValue;
@@ -653,15 +652,15 @@ cudaError_t launch_kernel(const void *A, const void *A2, const void *B0, const v
 // CTA pairs whenever there are at least two row blocks to pair up.
 template <int MODE, bool BF16, int A_TERMS, bool OUT_BF16 = BF16, int BN = 256>
 cudaError_t launch_impl(const void *A, const void *A2, const void *B0, const void *B1, void *out0,
-                        void *out1, int64_t M, int64_t a_rows, int64_t K, int64_t N, int kind, float acc_scale,
+                        void *out1, int64_t M, int64_t K, int64_t N, int kind, float acc_scale,
                         float out_scale, cudaStream_t s, const void *res = nullptr, float *part = nullptr,
                         int kst_per_split = 0, int splits = 1) {
     if (M <= 0) return cudaSuccess;
     if (M > BM)
-        return launch_kernel<MODE, BF16, A_TERMS, OUT_BF16, BN, true>(A, A2, B0, B1, out0, out1, M, a_rows, K, N, kind,
+        return launch_kernel<MODE, BF16, A_TERMS, OUT_BF16, BN, true>(A, A2, B0, B1, out0, out1, M, K, N, kind,
                                                                        acc_scale, out_scale, res, part,
                                                                        kst_per_split, splits, s);
-    return launch_kernel<MODE, BF16, A_TERMS, OUT_BF16, BN, false>(A, A2, B0, B1, out0, out1, M, a_rows, K, N, kind,
+    return launch_kernel<MODE, BF16, A_TERMS, OUT_BF16, BN, false>(A, A2, B0, B1, out0, out1, M, K, N, kind,
                                                                     acc_scale, out_scale, res, part,
                                                                     kst_per_split, splits, s);
 }
@@ -824,42 +823,42 @@ cudaError_t launch_splitk_reduce(const float *part, int splits, int64_t count, c
 
 template <int MODE, bool BF16, int A_TERMS>
 cudaError_t launch_gateup_bn(const void *A, const void *A2, const void *B0, const void *B1, void *out0,
-                             void *out1, int64_t M, int64_t a_rows, int64_t K, int64_t N, float acc_scale,
-                             float out_scale, cudaStream_t s) {
+                             void *out1, int64_t M, int64_t K, int64_t N, float acc_scale, float out_scale,
+                             cudaStream_t s) {
     if (gateup_width(M, N) == 192)
-        return launch_impl<MODE, BF16, A_TERMS, BF16, 192>(A, A2, B0, B1, out0, out1, M, a_rows, K, N, K_GEMM_GATEUP,
+        return launch_impl<MODE, BF16, A_TERMS, BF16, 192>(A, A2, B0, B1, out0, out1, M, K, N, K_GEMM_GATEUP,
                                                            acc_scale, out_scale, s);
-    return launch_impl<MODE, BF16, A_TERMS, BF16, 256>(A, A2, B0, B1, out0, out1, M, a_rows, K, N, K_GEMM_GATEUP,
+    return launch_impl<MODE, BF16, A_TERMS, BF16, 256>(A, A2, B0, B1, out0, out1, M, K, N, K_GEMM_GATEUP,
                                                        acc_scale, out_scale, s);
 }
 
 // One row block and a reduction too short to split: 64-wide tiles (d 4096:
 // 64 CTAs instead of 16).
 template <bool BF16, int A_TERMS, bool OUT_BF16>
-cudaError_t launch_plain_bn(const void *A, const void *A_lo, const void *B, void *C, int64_t M, int64_t a_rows,
-                            int64_t K, int64_t N, float acc_scale, const void *res, float *part, cudaStream_t s) {
+cudaError_t launch_plain_bn(const void *A, const void *A_lo, const void *B, void *C, int64_t M, int64_t K,
+                            int64_t N, float acc_scale, const void *res, float *part, cudaStream_t s) {
     using TOut = typename std::conditional<OUT_BF16, __nv_bfloat16, __half>::type;
     int per = 0, bn = 256;
     const int splits = plain_split_plan(M, K, N, A_TERMS, &per, &bn);
     if (splits > 1) {
         if (!part) return cudaErrorInvalidValue;
         cudaError_t e =
-            bn == 192 ? launch_impl<MODE_PLAIN, BF16, A_TERMS, OUT_BF16, 192>(A, A_lo, B, nullptr, C, nullptr, M, a_rows, K, N,
+            bn == 192 ? launch_impl<MODE_PLAIN, BF16, A_TERMS, OUT_BF16, 192>(A, A_lo, B, nullptr, C, nullptr, M, K, N,
                                                                               K_GEMM_DOWN, acc_scale, 1.f, s, nullptr,
                                                                               part, per, splits)
-                      : launch_impl<MODE_PLAIN, BF16, A_TERMS, OUT_BF16, 256>(A, A_lo, B, nullptr, C, nullptr, M, a_rows, K, N,
+                      : launch_impl<MODE_PLAIN, BF16, A_TERMS, OUT_BF16, 256>(A, A_lo, B, nullptr, C, nullptr, M, K, N,
                                                                               K_GEMM_DOWN, acc_scale, 1.f, s, nullptr,
                                                                               part, per, splits);
         if (e != cudaSuccess) return e;
         return launch_splitk_reduce<TOut>(part, splits, M * N, res, C, s);
     }
     if (M <= BM)
-        return launch_impl<MODE_PLAIN, BF16, A_TERMS, OUT_BF16, 64>(A, A_lo, B, nullptr, C, nullptr, M, a_rows, K, N,
+        return launch_impl<MODE_PLAIN, BF16, A_TERMS, OUT_BF16, 64>(A, A_lo, B, nullptr, C, nullptr, M, K, N,
                                                                     K_GEMM_DOWN, acc_scale, 1.f, s, res);
     if (tile_width(M, N) == 224)
-        return launch_impl<MODE_PLAIN, BF16, A_TERMS, OUT_BF16, 224>(A, A_lo, B, nullptr, C, nullptr, M, a_rows, K,
+        return launch_impl<MODE_PLAIN, BF16, A_TERMS, OUT_BF16, 224>(A, A_lo, B, nullptr, C, nullptr, M, K,
                                                                      N, K_GEMM_DOWN, acc_scale, 1.f, s, res);
-    return launch_impl<MODE_PLAIN, BF16, A_TERMS, OUT_BF16, 256>(A, A_lo, B, nullptr, C, nullptr, M, a_rows, K, N,
+    return launch_impl<MODE_PLAIN, BF16, A_TERMS, OUT_BF16, 256>(A, A_lo, B, nullptr, C, nullptr, M, K, N,
                                                                  K_GEMM_DOWN, acc_scale, 1.f, s, res);
 }
 
@@ -886,38 +885,38 @@ size_t gemm_plain_partial_bytes(int64_t M, int64_t K, int64_t N, int a_terms) {
 
 cudaError_t launch_gemm_gateup(int dt, const void *A, const void *A_lo, const void *Wg,
                                const void *Wu, void *H, void *H_lo, void *G, void *U, int64_t M,
-                               int64_t a_rows, int64_t K, int64_t F, bool fused, float acc_scale,
-                               float out_scale, cudaStream_t s) {
+                               int64_t K, int64_t F, bool fused, float acc_scale, float out_scale,
+                               cudaStream_t s) {
     const bool bf = dt == DT_BF16;
     const float a = acc_scale, o = out_scale;
     if (A_lo) {
         if (fused)
-            return bf ? launch_gateup_bn<MODE_GATEUP_FUSED, true, 2>(A, A_lo, Wg, Wu, H, H_lo, M, a_rows, K, F, a, o, s)
-                      : launch_gateup_bn<MODE_GATEUP_FUSED, false, 2>(A, A_lo, Wg, Wu, H, H_lo, M, a_rows, K, F, a, o, s);
-        return bf ? launch_gateup_bn<MODE_GATEUP_SPLIT, true, 2>(A, A_lo, Wg, Wu, G, U, M, a_rows, K, F, a, o, s)
-                  : launch_gateup_bn<MODE_GATEUP_SPLIT, false, 2>(A, A_lo, Wg, Wu, G, U, M, a_rows, K, F, a, o, s);
+            return bf ? launch_gateup_bn<MODE_GATEUP_FUSED, true, 2>(A, A_lo, Wg, Wu, H, H_lo, M, K, F, a, o, s)
+                      : launch_gateup_bn<MODE_GATEUP_FUSED, false, 2>(A, A_lo, Wg, Wu, H, H_lo, M, K, F, a, o, s);
+        return bf ? launch_gateup_bn<MODE_GATEUP_SPLIT, true, 2>(A, A_lo, Wg, Wu, G, U, M, K, F, a, o, s)
+                  : launch_gateup_bn<MODE_GATEUP_SPLIT, false, 2>(A, A_lo, Wg, Wu, G, U, M, K, F, a, o, s);
     }
     if (fused)
-        return bf ? launch_gateup_bn<MODE_GATEUP_FUSED, true, 1>(A, nullptr, Wg, Wu, H, H_lo, M, a_rows, K, F, a, o, s)
-                  : launch_gateup_bn<MODE_GATEUP_FUSED, false, 1>(A, nullptr, Wg, Wu, H, H_lo, M, a_rows, K, F, a, o, s);
-    return bf ? launch_gateup_bn<MODE_GATEUP_SPLIT, true, 1>(A, nullptr, Wg, Wu, G, U, M, a_rows, K, F, a, o, s)
-              : launch_gateup_bn<MODE_GATEUP_SPLIT, false, 1>(A, nullptr, Wg, Wu, G, U, M, a_rows, K, F, a, o, s);
+        return bf ? launch_gateup_bn<MODE_GATEUP_FUSED, true, 1>(A, nullptr, Wg, Wu, H, H_lo, M, K, F, a, o, s)
+                  : launch_gateup_bn<MODE_GATEUP_FUSED, false, 1>(A, nullptr, Wg, Wu, H, H_lo, M, K, F, a, o, s);
+    return bf ? launch_gateup_bn<MODE_GATEUP_SPLIT, true, 1>(A, nullptr, Wg, Wu, G, U, M, K, F, a, o, s)
+              : launch_gateup_bn<MODE_GATEUP_SPLIT, false, 1>(A, nullptr, Wg, Wu, G, U, M, K, F, a, o, s);
 }
 
 cudaError_t launch_gemm_plain(int dt, int dt_out, const void *A, const void *A_lo, const void *B,
-                              void *C, int64_t M, int64_t a_rows, int64_t K, int64_t N, float acc_scale,
+                              void *C, int64_t M, int64_t K, int64_t N, float acc_scale,
                               const void *res, float *part, cudaStream_t s) {
     const float a = acc_scale;
     if (dt == DT_BF16) {
-        if (A_lo) return launch_plain_bn<true, 2, true>(A, A_lo, B, C, M, a_rows, K, N, a, res, part, s);
-        return launch_plain_bn<true, 1, true>(A, nullptr, B, C, M, a_rows, K, N, a, res, part, s);
+        if (A_lo) return launch_plain_bn<true, 2, true>(A, A_lo, B, C, M, K, N, a, res, part, s);
+        return launch_plain_bn<true, 1, true>(A, nullptr, B, C, M, K, N, a, res, part, s);
     }
     if (dt_out == DT_BF16) {   // fp16 operands, bf16 output (prepared-weights path)
-        if (A_lo) return launch_plain_bn<false, 2, true>(A, A_lo, B, C, M, a_rows, K, N, a, res, part, s);
-        return launch_plain_bn<false, 1, true>(A, nullptr, B, C, M, a_rows, K, N, a, res, part, s);
+        if (A_lo) return launch_plain_bn<false, 2, true>(A, A_lo, B, C, M, K, N, a, res, part, s);
+        return launch_plain_bn<false, 1, true>(A, nullptr, B, C, M, K, N, a, res, part, s);
     }
-    if (A_lo) return launch_plain_bn<false, 2, false>(A, A_lo, B, C, M, a_rows, K, N, a, res, part, s);
-    return launch_plain_bn<false, 1, false>(A, nullptr, B, C, M, a_rows, K, N, a, res, part, s);
+    if (A_lo) return launch_plain_bn<false, 2, false>(A, A_lo, B, C, M, K, N, a, res, part, s);
+    return launch_plain_bn<false, 1, false>(A, nullptr, B, C, M, K, N, a, res, part, s);
 }
 
 }  // namespace ffn

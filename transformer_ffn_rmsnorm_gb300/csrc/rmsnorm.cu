@@ -32,28 +32,13 @@ __device__ __forceinline__ void store_vec(T *hi, T *lo, int64_t i, const float (
     }
 }
 
-// Rows fill_rows > r >= rows of n (and n_lo): a constant.  The projections
-// read their operand in tiles of whole CTA pairs of rows, and tiles whose
-// rows past the batch held zeros (the copy engine's fill, or zeroed memory)
-// measured 15-20 % slower in the gate/up GEMM than tiles of non-zero rows;
-// those rows' results are never stored.  Spread over the CTAs of the grid.
-template <typename TO, bool SPLIT>
-__device__ __forceinline__ void fill_pad_rows(TO *n, TO *nlo, int64_t rows, int64_t fill_rows, int64_t d) {
-    const TO one = from_f32<TO>(1.f), lo = from_f32<TO>(1.f / 512.f);
-    for (int64_t k = rows + blockIdx.x; k < fill_rows; k += gridDim.x)
-        for (int64_t c = threadIdx.x; c < d; c += blockDim.x) {
-            n[k * d + c] = one;
-            if constexpr (SPLIT) nlo[k * d + c] = lo;
-        }
-}
-
 // One row per group of WPR warps; each thread holds VPT 16-byte vectors.
 // T: storage of x and g; TO: storage of n (same element size).
 template <typename T, typename TO, int VPT, int WPR, bool SPLIT>
 __global__ void __launch_bounds__(256) rmsnorm_reg_kernel(const T *x,
                                                           const T *__restrict__ g,
                                                           TO *n, TO *nlo, int64_t rows,
-                                                          int d, float eps, int64_t fill_rows) {
+                                                          int d, float eps) {
     static_assert(sizeof(T) == sizeof(TO), "input and output element sizes must match");
     constexpr int EPV = 16 / sizeof(T);
     __shared__ float partial[256 / 32];
@@ -62,7 +47,6 @@ __global__ void __launch_bounds__(256) rmsnorm_reg_kernel(const T *x,
     // one start (it requests weights at once, which that kernel may have written)
     ptx::griddep_wait();
     ptx::griddep_launch_dependents();
-    fill_pad_rows<TO, SPLIT>(n, nlo, rows, fill_rows, d);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rows_per_cta = (blockDim.x >> 5) / WPR;
     const int row_in_cta = warp / WPR, wr = warp % WPR;
@@ -120,14 +104,13 @@ template <typename T, typename TO, bool SPLIT>
 __global__ void __launch_bounds__(256) rmsnorm_generic_kernel(const T *x,
                                                               const T *__restrict__ g,
                                                               TO *n, TO *nlo, int64_t rows,
-                                                              int64_t d, float eps, int64_t fill_rows) {
+                                                              int64_t d, float eps) {
     __shared__ float partial[8];
     // launched as a programmatic dependent: nothing is read before the
     // previous kernel has finished; only then may the projection after this
     // one start (it requests weights at once, which that kernel may have written)
     ptx::griddep_wait();
     ptx::griddep_launch_dependents();
-    fill_pad_rows<TO, SPLIT>(n, nlo, rows, fill_rows, d);
     const int64_t row = blockIdx.x;
     if (row >= rows) return;
     const T *xr = x + row * d;
@@ -176,7 +159,7 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
 template <typename T, typename TO, bool SPLIT>
 __global__ void __launch_bounds__(kNormThreads) rmsnorm_stream_kernel(
     const T *x, const T *__restrict__ g, TO *n, TO *nlo, int64_t rows, int d, float eps,
-    uint32_t row_bytes, unsigned *err, int64_t fill_rows) {
+    uint32_t row_bytes, unsigned *err) {
     constexpr int EPV = 16 / sizeof(T);
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bar_full[kNormWarps], bar_empty[kNormWarps], bar_g;
@@ -186,7 +169,6 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_stream_kernel(
     // one start (it requests weights at once, which that kernel may have written)
     ptx::griddep_wait();
     ptx::griddep_launch_dependents();
-    fill_pad_rows<TO, SPLIT>(n, nlo, rows, fill_rows, d);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t stride = (row_bytes + 127u) & ~127u;
     const uint32_t gsm = (ptx::smem_u32(smem_raw) + 127u) & ~127u;   // g, one row's worth
@@ -295,7 +277,7 @@ constexpr uint32_t kNormMaxRowBytes = 16 * 1024;
 
 template <typename T, typename TO, bool SPLIT>
 cudaError_t launch_stream(const void *x, const void *g, void *n, void *nlo, int64_t rows, int d, float eps,
-                          int64_t fill_rows, cudaStream_t s) {
+                          cudaStream_t s) {
     const uint32_t row_bytes = static_cast<uint32_t>(d) * sizeof(T);
     const uint32_t stride = (row_bytes + 127u) & ~127u;
     const size_t smem = static_cast<size_t>(stride) * (kNormWarps + 1) + 128;
@@ -323,13 +305,13 @@ cudaError_t launch_stream(const void *x, const void *g, void *n, void *nlo, int6
     LaunchScope scope(K_RMSNORM, s);
     e = launch_dependent(rmsnorm_stream_kernel<T, TO, SPLIT>, dim3(static_cast<unsigned>(grid)), dim3(kNormThreads),
                          smem, s, static_cast<const T *>(x), static_cast<const T *>(g), static_cast<TO *>(n),
-                         static_cast<TO *>(nlo), rows, d, eps, row_bytes, err, fill_rows);
+                         static_cast<TO *>(nlo), rows, d, eps, row_bytes, err);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <typename T, typename TO, int VPT, int WPR, bool SPLIT>
 cudaError_t launch_reg(const void *x, const void *g, void *n, void *nlo, int64_t rows, int d,
-                       float eps, int64_t fill_rows, cudaStream_t s) {
+                       float eps, cudaStream_t s) {
     const int threads = 256;
     const int rows_per_cta = (threads / 32) / WPR;
     const int64_t blocks = (rows + rows_per_cta - 1) / rows_per_cta;
@@ -337,30 +319,30 @@ cudaError_t launch_reg(const void *x, const void *g, void *n, void *nlo, int64_t
     const cudaError_t e = launch_dependent(rmsnorm_reg_kernel<T, TO, VPT, WPR, SPLIT>,
                                            dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, s,
                                            static_cast<const T *>(x), static_cast<const T *>(g),
-                                           static_cast<TO *>(n), static_cast<TO *>(nlo), rows, d, eps, fill_rows);
+                                           static_cast<TO *>(n), static_cast<TO *>(nlo), rows, d, eps);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <typename T, typename TO, int WPR, bool SPLIT>
 cudaError_t dispatch_vpt(int vpt, const void *x, const void *g, void *n, void *nlo, int64_t rows,
-                         int d, float eps, int64_t fill_rows, cudaStream_t s) {
+                         int d, float eps, cudaStream_t s) {
     switch (vpt) {
-        case 1: return launch_reg<T, TO, 1, WPR, SPLIT>(x, g, n, nlo, rows, d, eps, fill_rows, s);
-        case 2: return launch_reg<T, TO, 2, WPR, SPLIT>(x, g, n, nlo, rows, d, eps, fill_rows, s);
-        case 4: return launch_reg<T, TO, 4, WPR, SPLIT>(x, g, n, nlo, rows, d, eps, fill_rows, s);
-        default: return launch_reg<T, TO, 8, WPR, SPLIT>(x, g, n, nlo, rows, d, eps, fill_rows, s);
+        case 1: return launch_reg<T, TO, 1, WPR, SPLIT>(x, g, n, nlo, rows, d, eps, s);
+        case 2: return launch_reg<T, TO, 2, WPR, SPLIT>(x, g, n, nlo, rows, d, eps, s);
+        case 4: return launch_reg<T, TO, 4, WPR, SPLIT>(x, g, n, nlo, rows, d, eps, s);
+        default: return launch_reg<T, TO, 8, WPR, SPLIT>(x, g, n, nlo, rows, d, eps, s);
     }
 }
 
 template <typename T, typename TO, bool SPLIT>
 cudaError_t launch_typed(const void *x, const void *g, void *n, void *nlo, int64_t rows,
-                         int64_t d, float eps, int64_t fill_rows, cudaStream_t s) {
+                         int64_t d, float eps, cudaStream_t s) {
     constexpr int EPV = 16 / sizeof(T);
     const bool aligned = (d % EPV) == 0;
     const int64_t nvec = d / EPV;
     // many rows: stream whole rows through shared memory
     if (aligned && rows >= 4 * static_cast<int64_t>(sm_count()) && d * sizeof(T) <= kNormMaxRowBytes)
-        return launch_stream<T, TO, SPLIT>(x, g, n, nlo, rows, static_cast<int>(d), eps, fill_rows, s);
+        return launch_stream<T, TO, SPLIT>(x, g, n, nlo, rows, static_cast<int>(d), eps, s);
     // registers hold the row when nvec <= 32 lanes * 8 warps * kMaxVPT
     if (aligned && nvec <= 32 * 8 * kMaxVPT) {
         int wpr = 1;
@@ -370,49 +352,49 @@ cudaError_t launch_typed(const void *x, const void *g, void *n, void *nlo, int64
         while (vpt < per_thread) vpt <<= 1;
         const int di = static_cast<int>(d);
         switch (wpr) {
-            case 1: return dispatch_vpt<T, TO, 1, SPLIT>(vpt, x, g, n, nlo, rows, di, eps, fill_rows, s);
-            case 2: return dispatch_vpt<T, TO, 2, SPLIT>(vpt, x, g, n, nlo, rows, di, eps, fill_rows, s);
-            case 4: return dispatch_vpt<T, TO, 4, SPLIT>(vpt, x, g, n, nlo, rows, di, eps, fill_rows, s);
-            default: return dispatch_vpt<T, TO, 8, SPLIT>(vpt, x, g, n, nlo, rows, di, eps, fill_rows, s);
+            case 1: return dispatch_vpt<T, TO, 1, SPLIT>(vpt, x, g, n, nlo, rows, di, eps, s);
+            case 2: return dispatch_vpt<T, TO, 2, SPLIT>(vpt, x, g, n, nlo, rows, di, eps, s);
+            case 4: return dispatch_vpt<T, TO, 4, SPLIT>(vpt, x, g, n, nlo, rows, di, eps, s);
+            default: return dispatch_vpt<T, TO, 8, SPLIT>(vpt, x, g, n, nlo, rows, di, eps, s);
         }
     }
     LaunchScope scope(K_RMSNORM, s);
     const cudaError_t e = launch_dependent(rmsnorm_generic_kernel<T, TO, SPLIT>, dim3(static_cast<unsigned>(rows)),
                                            dim3(256), 0, s, static_cast<const T *>(x), static_cast<const T *>(g),
-                                           static_cast<TO *>(n), static_cast<TO *>(nlo), rows, d, eps, fill_rows);
+                                           static_cast<TO *>(n), static_cast<TO *>(nlo), rows, d, eps);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_rmsnorm(const void *x, const void *g, void *n, int64_t rows, int64_t d,
-                           float eps, int dt, cudaStream_t s, int64_t fill_rows) {
+                           float eps, int dt, cudaStream_t s) {
     if (rows <= 0) return cudaSuccess;
     switch (dt) {
-        case DT_F32: return launch_typed<float, float, false>(x, g, n, nullptr, rows, d, eps, fill_rows, s);
-        case DT_F16: return launch_typed<__half, __half, false>(x, g, n, nullptr, rows, d, eps, fill_rows, s);
+        case DT_F32: return launch_typed<float, float, false>(x, g, n, nullptr, rows, d, eps, s);
+        case DT_F16: return launch_typed<__half, __half, false>(x, g, n, nullptr, rows, d, eps, s);
         default:
-            return launch_typed<__nv_bfloat16, __nv_bfloat16, false>(x, g, n, nullptr, rows, d, eps, fill_rows, s);
+            return launch_typed<__nv_bfloat16, __nv_bfloat16, false>(x, g, n, nullptr, rows, d, eps, s);
     }
 }
 
 cudaError_t launch_rmsnorm_split(const void *x, const void *g, void *n_hi, void *n_lo,
-                                 int64_t rows, int64_t d, float eps, int dt, cudaStream_t s, int64_t fill_rows) {
+                                 int64_t rows, int64_t d, float eps, int dt, cudaStream_t s) {
     if (rows <= 0) return cudaSuccess;
     switch (dt) {
-        case DT_F16: return launch_typed<__half, __half, true>(x, g, n_hi, n_lo, rows, d, eps, fill_rows, s);
+        case DT_F16: return launch_typed<__half, __half, true>(x, g, n_hi, n_lo, rows, d, eps, s);
         case DT_BF16:
-            return launch_typed<__nv_bfloat16, __nv_bfloat16, true>(x, g, n_hi, n_lo, rows, d, eps, fill_rows, s);
+            return launch_typed<__nv_bfloat16, __nv_bfloat16, true>(x, g, n_hi, n_lo, rows, d, eps, s);
         default: return cudaErrorInvalidValue;
     }
 }
 
 cudaError_t launch_rmsnorm_to_f16(const void *x, const void *g, void *n, int64_t rows, int64_t d,
-                                  float eps, int dt_in, cudaStream_t s, int64_t fill_rows) {
+                                  float eps, int dt_in, cudaStream_t s) {
     if (rows <= 0) return cudaSuccess;
     switch (dt_in) {
-        case DT_F16: return launch_typed<__half, __half, false>(x, g, n, nullptr, rows, d, eps, fill_rows, s);
-        case DT_BF16: return launch_typed<__nv_bfloat16, __half, false>(x, g, n, nullptr, rows, d, eps, fill_rows, s);
+        case DT_F16: return launch_typed<__half, __half, false>(x, g, n, nullptr, rows, d, eps, s);
+        case DT_BF16: return launch_typed<__nv_bfloat16, __half, false>(x, g, n, nullptr, rows, d, eps, s);
         default: return cudaErrorInvalidValue;
     }
 }
