@@ -131,12 +131,11 @@ ffn_status ffn_block_workspace_bytes(int64_t rows, int64_t d, int64_t ffn, ffn_d
  *   x [rows x d], g [d], w_gate and w_up [ffn x d], w_down [d x ffn],
  *   y [rows x d]; all of `dtype`.  y must not overlap any input.
  *   Paths: FFN_F32 -> fp32 SIMT FFMA kernels (any rows).  FFN_F16/FFN_BF16 ->
- *   rows <= 32 (rows <= 16 when n and h enter as bf16 hi + lo terms, the
- *   bf16 default): weight-streaming decode kernels (every weight read once
- *   for up to 4 tiles of 8 token rows); otherwise tcgen05/TMEM GEMMs fed by
- *   TMA (with few row blocks: narrower gate/up tiles and a split-K down
+ *   rows <= 16: weight-streaming decode kernels (every weight read once for
+ *   up to 2 tiles of 8 token rows); otherwise tcgen05/TMEM GEMMs fed by TMA
+ *   (with few row blocks: narrower gate/up tiles and a split-K down
  *   projection, so that the tiles fill the SMs).  FFN_PATH_GEMV forces the
- *   first for any rows <= 64 (8 token tiles).  Rules: d, ffn >= 1; 16-bit dtypes need d % 8 == 0 and
+ *   first for any rows <= 64 (up to 8 token tiles).  Rules: d, ffn >= 1; 16-bit dtypes need d % 8 == 0 and
  *   ffn % 8 == 0; fp32 needs d % 4 == 0 and ffn % 4 == 0.
  *   workspace: at least ffn_block_workspace_bytes(...) bytes, 16-byte aligned.
  *   Intermediates (n, h, split-K partials) round to `dtype` where they feed

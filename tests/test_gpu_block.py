@@ -60,8 +60,7 @@ def test_decode_rows(ffn, oracle_lib, rows, dtype):
 def test_decode_batched_rows(ffn, oracle_lib, rows, dtype, path):
     """17 to 64 rows: four and eight token tiles on the weight-streaming
     kernels (ragged last tiles included), forced there and as routed (above
-    16 rows with bf16 hi + lo operands, above 32 with fp16 ones, the block
-    goes to the GEMMs with split-K down projection)."""
+    16 rows the block goes to the GEMMs with split-K down projection)."""
     cfg = synth.BlockConfig("t", rows, 1024, 2816, 1e-5, dtype)
     inp = synth.make_block_inputs(cfg, seed=200 + rows)
     flags = ffn.FFN_PATH_GEMV if path == "gemv" else 0

@@ -23,11 +23,10 @@ namespace ffn {
 namespace {
 
 // rows up to which the weight-streaming (decode) kernels can run the block
-// (FFN_PATH_GEMV: eight token tiles), and up to which they do by default for
-// one-term and for hi + lo operands; the quantised entries run their rows in
-// groups of kQuantGroupRows
+// (FFN_PATH_GEMV: eight token tiles), and up to which they do by default;
+// the quantised entries run their rows in groups of kQuantGroupRows
 constexpr int64_t kGemvMaxRows = 64;
-constexpr int64_t kGemvAutoRows = 32, kGemvAutoRowsTwoTerm = 16;
+constexpr int64_t kGemvAutoRows = 16;
 constexpr int64_t kQuantGroupRows = 16;
 constexpr int kMaxDevices = 64;
 
@@ -118,14 +117,13 @@ ffn_status plan_block(int64_t rows, int64_t d, int64_t ffn, ffn_dtype dt, uint32
     // rows up to which these flags take the decode kernels.  Measured
     // crossover on 4096 -> 14336 (graph-replayed block, one-term / hi + lo
     // operands): the GEMMs (one-row-block tiles, split-K down projection)
-    // take 81 / 89 us at 16 rows, 79 / 84 us at 32, 78-81 / 83-86 us at
-    // 64-128; the weight-streaming kernels 66 / 80 us at 16, 76 / 87 us at
-    // 17, 79 / 84 us at 32, 110 / 173 us at 33 (eight token tiles).
+    // take 84 / 97 us at 12 rows, 73 / 78 us at 16-32, 75-79 / 81-86 us at
+    // 64-128; the weight-streaming kernels 65 / 79 us at 12, 66 / 80 us at
+    // 16, 75 / 104 us at 17, 79 / 107 us at 32 (four token tiles).
     // Two-term operands double their MMAs.
     int64_t gemv_rows = 0;
     if (dt != FFN_F32 && !(flags & FFN_PATH_GEMM))
-        gemv_rows = (flags & FFN_PATH_GEMV) ? kGemvMaxRows
-                                            : (plan->split_act ? kGemvAutoRowsTwoTerm : kGemvAutoRows);
+        gemv_rows = (flags & FFN_PATH_GEMV) ? kGemvMaxRows : kGemvAutoRows;
     if (dt == FFN_F32)
         plan->path = PATH_SIMT;
     else
