@@ -269,8 +269,11 @@ ffn_status ffn_block_forward_fp8(const void *x, const void *g, ffn_fp8_weight w_
  *   allocation, no free, no allocating library call is made.  Limits (checked,
  *   FFN_ERR_SHAPE beyond them): rows <= 16, d <= 8192, ffn <= 32768, plus
  *   d % 8 == 0 and ffn % 8 == 0; dtype FFN_F16 or FFN_BF16.
- *   The first call on a device looks up the array's device address (with that
- *   device current) -- make that first call before any stream capture.
+ *   Every call looks up the array's device address in the current device's
+ *   context (a host-side query that allocates nothing), so the address stays
+ *   right after cudaDeviceReset; the first call in a context also loads the
+ *   library's device code there -- make that first call before any stream
+ *   capture.
  *   Every call reuses the same array: calls that may run at the same time on
  *   the GPU (other streams, other host threads) race and must be serialised
  *   by the caller.  Other arguments, layouts and errors as ffn_block_forward.

@@ -84,3 +84,29 @@ def test_host_block_calls_in_a_row_and_empty(ffn):
     e = torch.empty((0, 256), dtype=torch.bfloat16).pin_memory()
     assert ffn.ffn_block_forward_host(e, *args, eps=1e-6).numel() == 0
     ffn.ffn_device_status()
+
+
+def test_host_block_at_the_benchmark_shape(ffn, oracle_lib):
+    """The timed end-to-end call itself: 4096 tokens, d 4096 -> ffn 11008,
+    prepared weights, chunks of 3072 and 1024 rows, three calls in a row on
+    one workspace (both staging sets, the first one twice).  Bitwise against
+    one ffn_block_forward of the whole batch on device buffers; sampled rows
+    (both ends of each chunk and its middle) against the float64 oracle."""
+    import torch
+    inp = synth.make_block_inputs(synth.C4_PREFILL_BF16, seed=0)
+    cfg = inp["cfg"]
+    assert (cfg.rows, cfg.d, cfg.ffn) == (4096, 4096, 11008)
+    g = to_dev(inp["g"], "bf16")
+    w = [ffn.ffn_prepare_weights(to_dev(inp[k], "bf16")) for k in ("w_gate", "w_up", "w_down")]
+    flags = ffn.FFN_PREPARED_WEIGHTS
+    ws = ffn.workspace(ffn.ffn_block_host_workspace_bytes(cfg.rows, cfg.d, cfg.ffn, torch.bfloat16, flags),
+                       torch.device("cuda"))
+    xh = host_bf16(inp["x"])   # alive until the stream has passed the calls
+    ys = [ffn.ffn_block_forward_host(xh, g, *w, eps=cfg.eps, flags=flags, ws=ws) for _ in range(3)]
+    torch.cuda.current_stream().synchronize()
+    y_dev = ffn.ffn_block_forward(to_dev(inp["x"], "bf16"), g, *w, eps=cfg.eps, flags=flags).cpu()
+    for y in ys:
+        assert torch.equal(y.view(torch.int16), y_dev.view(torch.int16))
+    rows = np.r_[0:4, 1534:1538, 3068:3076, 3582:3586, 4092:4096]
+    assert_lowp(to_host64(ys[-1])[rows], oracle_lib.block_from_inputs(inp, rows=rows))
+    ffn.ffn_device_status()

@@ -26,10 +26,14 @@
 //               the epilogue, store 16-byte vectors, release the accumulator
 //               so the next tile's MMAs overlap this tile's epilogue.
 // CTAs run in clusters of two over row blocks 2i and 2i+1 of the same column
-// block: each loads its own A tile and one half of the common B tile with a
-// multicast TMA copy into both CTAs' rings, so every B byte leaves L2 once
-// per pair (a third less L2-to-SM traffic per flop for 256-wide tiles); a
-// ring slot is reused once the MMAs of both CTAs have released it.
+// block, and the even CTA issues tcgen05.mma.cta_group::2 over both: each
+// CTA loads its own 128-row A tile and one half of the B tile
+// (cp.async.bulk.tensor ... .cta_group::2) into its OWN ring, the two copies'
+// byte counts completing on the even CTA's ring barrier; the pair MMA reads
+// the A rows and the B half from each CTA's shared memory.  No copy is
+// multicast: every B byte leaves L2 once per pair because each CTA fetches a
+// different half.  A ring slot is reused once the pair's MMAs have released
+// it (the commit arrives on the barriers of both CTAs).
 // The kernel is launched as a programmatic dependent of the kernel before it:
 // the first ring's worth of B (weights) is requested before that kernel has
 // finished, A (its output) only after.

@@ -174,7 +174,6 @@ ffn_status ffn_block_forward_host(const void *x_host, const void *g, const void 
     if (!make_pipe(p)) return FFN_ERR_CUDA;
 
     const int b = p.next;
-    p.next ^= 1;
     char *ws = static_cast<char *>(workspace);
     char *x_dev = ws + b * (l.x_stage + l.y_stage), *y_dev = x_dev + l.x_stage;
     char *block_ws = ws + 2 * (l.x_stage + l.y_stage);
@@ -182,6 +181,19 @@ ffn_status ffn_block_forward_host(const void *x_host, const void *g, const void 
     char *yh = static_cast<char *>(y_host);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const Chunks c = plan_chunks(rows);
+
+    // A call that fails part way has queued some copies and blocks on this
+    // staging set.  Its free events are then re-recorded behind everything
+    // queued so far (s after h2d, d2h after s), and the set is not handed on,
+    // so the next call on it waits for this one's work before overwriting
+    // the buffers.  Best effort: the error being reported comes first.
+    auto fail = [&](ffn_status why) {
+        if (cudaEventRecord(p.landed[0], p.h2d) == cudaSuccess) cudaStreamWaitEvent(s, p.landed[0], 0);
+        cudaEventRecord(p.x_free[b], s);
+        if (cudaEventRecord(p.computed[0], s) == cudaSuccess) cudaStreamWaitEvent(p.d2h, p.computed[0], 0);
+        cudaEventRecord(p.y_free[b], p.d2h);
+        return why;
+    };
 
     // this staging set's x may still be read, and its y still be copied out,
     // by the call before the previous one
@@ -191,24 +203,25 @@ ffn_status ffn_block_forward_host(const void *x_host, const void *g, const void 
         const int64_t r0 = c.start[i], nr = c.rows(i);
         if (cudaMemcpyAsync(x_dev + r0 * row_bytes, xh + r0 * row_bytes, nr * row_bytes, cudaMemcpyHostToDevice,
                             p.h2d) != cudaSuccess)
-            return FFN_ERR_CUDA;
-        if (cudaEventRecord(p.landed[i], p.h2d) != cudaSuccess) return FFN_ERR_CUDA;
+            return fail(FFN_ERR_CUDA);
+        if (cudaEventRecord(p.landed[i], p.h2d) != cudaSuccess) return fail(FFN_ERR_CUDA);
     }
     for (int i = 0; i < c.count; ++i) {
         const int64_t r0 = c.start[i], nr = c.rows(i);
-        if (cudaStreamWaitEvent(s, p.landed[i], 0) != cudaSuccess) return FFN_ERR_CUDA;
+        if (cudaStreamWaitEvent(s, p.landed[i], 0) != cudaSuccess) return fail(FFN_ERR_CUDA);
         st = ffn_block_forward(x_dev + r0 * row_bytes, g, w_gate, w_up, w_down, y_dev + r0 * row_bytes, nr, d, ffn,
                                eps, dtype, flags, block_ws, l.block, stream);
-        if (st != FFN_OK) return st;
-        if (cudaEventRecord(p.computed[i], s) != cudaSuccess) return FFN_ERR_CUDA;
-        if (cudaStreamWaitEvent(p.d2h, p.computed[i], 0) != cudaSuccess) return FFN_ERR_CUDA;
+        if (st != FFN_OK) return fail(st);
+        if (cudaEventRecord(p.computed[i], s) != cudaSuccess) return fail(FFN_ERR_CUDA);
+        if (cudaStreamWaitEvent(p.d2h, p.computed[i], 0) != cudaSuccess) return fail(FFN_ERR_CUDA);
         if (cudaMemcpyAsync(yh + r0 * row_bytes, y_dev + r0 * row_bytes, nr * row_bytes, cudaMemcpyDeviceToHost,
                             p.d2h) != cudaSuccess)
-            return FFN_ERR_CUDA;
+            return fail(FFN_ERR_CUDA);
     }
-    if (cudaEventRecord(p.x_free[b], s) != cudaSuccess) return FFN_ERR_CUDA;
-    if (cudaEventRecord(p.y_free[b], p.d2h) != cudaSuccess) return FFN_ERR_CUDA;
-    if (cudaStreamWaitEvent(s, p.y_free[b], 0) != cudaSuccess) return FFN_ERR_CUDA;
+    if (cudaEventRecord(p.x_free[b], s) != cudaSuccess) return fail(FFN_ERR_CUDA);
+    if (cudaEventRecord(p.y_free[b], p.d2h) != cudaSuccess) return fail(FFN_ERR_CUDA);
+    if (cudaStreamWaitEvent(s, p.y_free[b], 0) != cudaSuccess) return fail(FFN_ERR_CUDA);
+    p.next = b ^ 1;   // the next call uses the other staging set
     return FFN_OK;
 }
 

@@ -24,7 +24,6 @@ constexpr int64_t kStaticMaxRows = 16;
 constexpr int64_t kStaticMaxD = 8192;
 constexpr int64_t kStaticMaxFfn = 32768;
 constexpr size_t kStaticScratchBytes = size_t(12) << 20;   // 12 MiB
-constexpr int kMaxDevices = 64;
 
 }  // namespace
 
@@ -35,24 +34,17 @@ static __device__ __align__(256) unsigned char g_decode_scratch[kStaticScratchBy
 
 namespace {
 
-// Device address of g_decode_scratch for the current device, looked up once
-// per device (with that device current) on its first call.
+// Device address of g_decode_scratch in the current device's context, looked
+// up on every call.  The lookup allocates nothing and, once the module is
+// loaded in a context, is a host-side table query; not caching it keeps the
+// address right after cudaDeviceReset or a context rebuilt in the same
+// process (the module is then loaded again, perhaps elsewhere) and needs no
+// lock between host threads.  The first call in a context loads the module,
+// so make it before any stream capture.
 void *static_scratch(cudaError_t *err) {
-    static void *addr[kMaxDevices] = {};
-    int dev = 0;
-    *err = cudaGetDevice(&dev);
-    if (*err != cudaSuccess) return nullptr;
-    if (dev < 0 || dev >= kMaxDevices) {
-        *err = cudaErrorInvalidDevice;
-        return nullptr;
-    }
-    if (!addr[dev]) {
-        void *p = nullptr;
-        *err = cudaGetSymbolAddress(&p, g_decode_scratch);
-        if (*err != cudaSuccess) return nullptr;
-        addr[dev] = p;
-    }
-    return addr[dev];
+    void *p = nullptr;
+    *err = cudaGetSymbolAddress(&p, g_decode_scratch);
+    return *err == cudaSuccess ? p : nullptr;
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
