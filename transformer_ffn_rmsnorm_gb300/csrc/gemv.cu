@@ -45,19 +45,111 @@ constexpr int kDnFeat = 16 * kDnTPC;    // features per down CTA
 
 // ---------------------------------------------------------------------------
 // 1. RMSNorm of <= 16 token rows, written in fragment order.
-//    grid = (token slots, slices): every CTA reduces its token's whole row
-//    (a few KB, cheap) and writes one slice of the fragments, so the kernel
-//    is not limited to one SM per token.  Slots >= rows (and k >= K) are
-//    written as zeros.  With TWO, nlo receives the rounding residual of every
-//    value (same order).
+//
+// Eight normalised values n[k .. k+7] of one token (k a multiple of 8) into
+// their fragment slots; with TWO, nlo receives the rounding residual of every
+// value (same order).
+template <int WF, bool TWO>
+__device__ __forceinline__ void store_group(uint16_t *nfrag, uint16_t *nlo, int64_t nch, int token, int64_t k,
+                                            const float (&f)[8]) {
+    using TO = typename Fmt<WF>::TOp;
+    float r[8];   // residuals v - round(v)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) r[e] = f[e] - to_f32(from_f32<TO>(f[e]));
+    if constexpr (WF == WF_Q4) {
+        // two runs of 4 consecutive k; each lands in one 8-byte half of a
+        // lane's fragment with its elements in order {0, 2, 1, 3}
+#pragma unroll
+        for (int run = 0; run < 2; ++run) {
+            TO o[4], ol[4];
+            const int src[4] = {0, 2, 1, 3};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                o[e] = from_f32<TO>(f[4 * run + src[e]]);
+                ol[e] = from_f32<TO>(r[4 * run + src[e]]);
+            }
+            const int64_t base = frag_elem(FRAG_Q4, nch, token, k + 4 * run);
+            *reinterpret_cast<uint2 *>(nfrag + base) = *reinterpret_cast<const uint2 *>(o);
+            if (TWO) *reinterpret_cast<uint2 *>(nlo + base) = *reinterpret_cast<const uint2 *>(ol);
+        }
+    } else {
+        const int64_t base = frag_elem(frag_order<WF>(), nch, token, k);
+        *reinterpret_cast<uint4 *>(nfrag + base) = Vec16<TO>::pack(f);
+        if (TWO) *reinterpret_cast<uint4 *>(nlo + base) = Vec16<TO>::pack(r);
+    }
+}
+
+// Sum over the CTA (256 threads) of every thread's v, returned to all.
+__device__ __forceinline__ float cta_sum256(float v, float (&partial)[8]) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if ((threadIdx.x & 31) == 0) partial[threadIdx.x >> 5] = v;
+    __syncthreads();
+    v = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) v += partial[w];
+    return v;
+}
+
+// One CTA per token slot, the row held in registers (VPT 16-byte vectors of
+// x and of g per thread, read together in one round trip): sum of squares,
+// reciprocal root, the fragments.  Slots >= rows (and k >= K) are written as
+// zeros.  The call's first kernel: it waits for the kernel before it, then
+// lets the projection kernel after it start its weight stream, at once
+// (release_early) or when it has finished (its reads then do not queue
+// behind that stream).
+template <int WF, bool TWO, int VPT>
+__global__ void __launch_bounds__(256) gemv_norm_frag_reg_kernel(const void *x_, const void *g_,
+                                                                 uint16_t *nfrag, uint16_t *nlo, int rows,
+                                                                 int64_t K, int64_t nch, float eps,
+                                                                 int release_early) {
+    using T = typename Fmt<WF>::TIn;
+    __shared__ float partial[8];
+    ptx::griddep_wait();
+    if (release_early) ptx::griddep_launch_dependents();
+    const int token = blockIdx.x;
+    const int64_t nv = K / 8, ngroups = nch * 4;   // 8-element groups incl. the zero tail
+    const uint4 *x = reinterpret_cast<const uint4 *>(static_cast<const T *>(x_) + static_cast<int64_t>(token) * K);
+    const uint4 *g = static_cast<const uint4 *>(g_);
+    uint4 xv[VPT], gv[VPT];
+    const bool live = token < rows;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+        const int64_t v = threadIdx.x + 256 * i;
+        const bool in = live && v < nv;
+        xv[i] = in ? x[v] : make_uint4(0, 0, 0, 0);
+        gv[i] = in ? g[v] : make_uint4(0, 0, 0, 0);
+    }
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+        float f[8];
+        Vec16<T>::unpack(xv[i], f);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
+    }
+    const float inv = rsqrtf(cta_sum256(ss, partial) / static_cast<float>(K) + eps);
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+        const int64_t v = threadIdx.x + 256 * i;
+        if (v >= ngroups) break;
+        float f[8], gf[8];
+        Vec16<T>::unpack(xv[i], f);
+        Vec16<T>::unpack(gv[i], gf);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) f[e] = f[e] * inv * gf[e];
+        store_group<WF, TWO>(nfrag, nlo, nch, token, 8 * v, f);
+    }
+}
+
+// The same for rows too long for registers (d > 16384): grid = (token slots,
+// slices); every CTA reduces its token's whole row and writes one slice.
 template <int WF, bool TWO>
 __global__ void __launch_bounds__(256) gemv_norm_frag_kernel(const void *x_, const void *g_,
                                                              uint16_t *nfrag, uint16_t *nlo,
                                                              int rows, int64_t K, int64_t nch,
                                                              float eps) {
     using T = typename Fmt<WF>::TIn;
-    using TO = typename Fmt<WF>::TOp;
-    constexpr bool q4 = WF == WF_Q4;
     __shared__ float partial[8];
     // launched as a programmatic dependent: nothing is read or written before
     // the previous kernel has finished; only then may the projection kernel
@@ -69,45 +161,20 @@ __global__ void __launch_bounds__(256) gemv_norm_frag_kernel(const void *x_, con
     const T *g = static_cast<const T *>(g_);
     const int64_t ngroups = nch * 4;  // 8-element groups incl. the zero tail
     const int64_t v0 = ngroups * blockIdx.y / gridDim.y, v1 = ngroups * (blockIdx.y + 1) / gridDim.y;
-    if (token >= rows) {
-        for (int64_t v = v0 + threadIdx.x; v < v1; v += blockDim.x) {
-            const int64_t k = 8 * v;
-            if (q4) {
-                *reinterpret_cast<uint2 *>(nfrag + frag_elem(FRAG_Q4, nch, token, k)) = make_uint2(0, 0);
-                *reinterpret_cast<uint2 *>(nfrag + frag_elem(FRAG_Q4, nch, token, k + 4)) = make_uint2(0, 0);
-                if (TWO) {
-                    *reinterpret_cast<uint2 *>(nlo + frag_elem(FRAG_Q4, nch, token, k)) = make_uint2(0, 0);
-                    *reinterpret_cast<uint2 *>(nlo + frag_elem(FRAG_Q4, nch, token, k + 4)) = make_uint2(0, 0);
-                }
-            } else {
-                *reinterpret_cast<uint4 *>(nfrag + frag_elem(frag_order<WF>(), nch, token, k)) = make_uint4(0, 0, 0, 0);
-                if (TWO)
-                    *reinterpret_cast<uint4 *>(nlo + frag_elem(frag_order<WF>(), nch, token, k)) = make_uint4(0, 0, 0, 0);
-            }
-        }
-        return;
-    }
     const int64_t nv = K / 8;
     float ss = 0.f;
-    for (int64_t v = threadIdx.x; v < nv; v += blockDim.x) {
-        float f[8];
-        Vec16<T>::unpack(reinterpret_cast<const uint4 *>(x)[v], f);
+    if (token < rows) {
+        for (int64_t v = threadIdx.x; v < nv; v += blockDim.x) {
+            float f[8];
+            Vec16<T>::unpack(reinterpret_cast<const uint4 *>(x)[v], f);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
+            for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
+        }
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    if ((threadIdx.x & 31) == 0) partial[threadIdx.x >> 5] = ss;
-    __syncthreads();
-    ss = 0.f;
-#pragma unroll
-    for (int w = 0; w < 8; ++w) ss += partial[w];
-    const float inv = rsqrtf(ss / static_cast<float>(K) + eps);
-
+    const float inv = rsqrtf(cta_sum256(ss, partial) / static_cast<float>(K) + eps);
     for (int64_t v = v0 + threadIdx.x; v < v1; v += blockDim.x) {
-        const int64_t k = 8 * v;
         float f[8];
-        if (v < nv) {
+        if (token < rows && v < nv) {
             float gf[8];
             Vec16<T>::unpack(reinterpret_cast<const uint4 *>(x)[v], f);
             Vec16<T>::unpack(reinterpret_cast<const uint4 *>(g)[v], gf);
@@ -117,30 +184,7 @@ __global__ void __launch_bounds__(256) gemv_norm_frag_kernel(const void *x_, con
 #pragma unroll
             for (int e = 0; e < 8; ++e) f[e] = 0.f;
         }
-        float r[8];   // residuals v - round(v)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) r[e] = f[e] - to_f32(from_f32<TO>(f[e]));
-        if (q4) {
-            // two runs of 4 consecutive k; each lands in one 8-byte half of a
-            // lane's fragment with its elements in order {0, 2, 1, 3}
-#pragma unroll
-            for (int run = 0; run < 2; ++run) {
-                TO o[4], ol[4];
-                const int src[4] = {0, 2, 1, 3};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    o[e] = from_f32<TO>(f[4 * run + src[e]]);
-                    ol[e] = from_f32<TO>(r[4 * run + src[e]]);
-                }
-                const int64_t base = frag_elem(FRAG_Q4, nch, token, k + 4 * run);
-                *reinterpret_cast<uint2 *>(nfrag + base) = *reinterpret_cast<const uint2 *>(o);
-                if (TWO) *reinterpret_cast<uint2 *>(nlo + base) = *reinterpret_cast<const uint2 *>(ol);
-            }
-        } else {
-            const int64_t base = frag_elem(frag_order<WF>(), nch, token, k);
-            *reinterpret_cast<uint4 *>(nfrag + base) = Vec16<TO>::pack(f);
-            if (TWO) *reinterpret_cast<uint4 *>(nlo + base) = Vec16<TO>::pack(r);
-        }
+        store_group<WF, TWO>(nfrag, nlo, nch, token, 8 * v, f);
     }
 }
 
@@ -446,10 +490,27 @@ cudaError_t launch_typed(const void *x, const void *gain, GemvWeights wg, GemvWe
     constexpr bool q4 = WF == WF_Q4;
     {
         LaunchScope scope(K_GEMV_NORM, s);
-        const int64_t slices = std::min<int64_t>(16, cdiv(geo.nchK * 4, 256));
-        cudaError_t e = launch_dependent(gemv_norm_frag_kernel<WF, TWO>, dim3(8 * NT, static_cast<unsigned>(slices)),
-                                         dim3(256), 0, s, x, gain, static_cast<uint16_t *>(ws.nfrag),
-                                         static_cast<uint16_t *>(ws.nfrag_lo), rows, d, geo.nchK, eps);
+        uint16_t *nf = static_cast<uint16_t *>(ws.nfrag), *nl = static_cast<uint16_t *>(ws.nfrag_lo);
+        const int64_t vpt = cdiv(geo.nchK * 4, 256);   // 16-byte groups per thread, one CTA per token slot
+        const dim3 grid(8 * NT);
+        const int early = decode_tuning(TUNE_NORM_RELEASE_EARLY);
+        cudaError_t e;
+        if (vpt <= 1)
+            e = launch_dependent(gemv_norm_frag_reg_kernel<WF, TWO, 1>, grid, dim3(256), 0, s, x, gain, nf, nl, rows,
+                                 d, geo.nchK, eps, early);
+        else if (vpt <= 2)
+            e = launch_dependent(gemv_norm_frag_reg_kernel<WF, TWO, 2>, grid, dim3(256), 0, s, x, gain, nf, nl, rows,
+                                 d, geo.nchK, eps, early);
+        else if (vpt <= 4)
+            e = launch_dependent(gemv_norm_frag_reg_kernel<WF, TWO, 4>, grid, dim3(256), 0, s, x, gain, nf, nl, rows,
+                                 d, geo.nchK, eps, early);
+        else if (vpt <= 8)
+            e = launch_dependent(gemv_norm_frag_reg_kernel<WF, TWO, 8>, grid, dim3(256), 0, s, x, gain, nf, nl, rows,
+                                 d, geo.nchK, eps, early);
+        else
+            e = launch_dependent(gemv_norm_frag_kernel<WF, TWO>,
+                                 dim3(8 * NT, static_cast<unsigned>(std::min<int64_t>(16, cdiv(vpt, 4)))), dim3(256),
+                                 0, s, x, gain, nf, nl, rows, d, geo.nchK, eps);
         if (e == cudaSuccess) e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }

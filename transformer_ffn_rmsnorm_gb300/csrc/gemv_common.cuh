@@ -155,6 +155,10 @@ __device__ __forceinline__ uint32_t word_of(const uint4 &v, int b) {
     return b == 0 ? v.x : b == 1 ? v.y : b == 2 ? v.z : v.w;
 }
 
+// Launch-shape knobs of the decode kernels.
+enum { TUNE_NORM_RELEASE_EARLY = 0, TUNE_PRE_STAGES_GATEUP = 1, TUNE_PRE_STAGES_DOWN = 2, TUNE_COUNT = 3 };
+int decode_tuning(int knob);
+
 // TMA-streamed decode kernels (gemv_stream.cu)
 bool stream_supported(int wfmt, int64_t d, int64_t ffn);
 int64_t stream_down_splits(int wfmt, int64_t d, int64_t ffn);

@@ -29,6 +29,8 @@
 // producer waits (bounded) for its copies in flight before the CTA exits.
 #include <cudaTypedefs.h>
 
+#include <cstdlib>
+
 #include "gemv_common.cuh"
 
 namespace ffn {
@@ -92,6 +94,7 @@ struct StreamParams {
     unsigned *err;
     const void *res;        // down: added to y before its rounding ([rows x D] of y's type), or null
     const float *rs0, *rs1; // e4m3: row scales of the weight matrices (gate and up, or down)
+    int pre_stages;         // weight stages requested before the wait (at most the ring)
 };
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
@@ -198,7 +201,8 @@ __global__ void __launch_bounds__(kThreads) gemv_stream_kernel(
             // The first ring's worth of weights is requested before the kernel
             // that writes the activations has finished (weights are inputs of
             // the call); the activations only after it has.
-            const int64_t npre = (kb1 - kb0) < kStages ? (kb1 - kb0) : kStages;
+            int64_t npre = (kb1 - kb0) < kStages ? (kb1 - kb0) : kStages;
+            if (npre > p.pre_stages) npre = p.pre_stages;
             for (int64_t i = 0; i < npre; ++i) {
                 arm(i, kb0 + i);
                 load_weights(i, kb0 + i);
@@ -565,6 +569,32 @@ cudaError_t set_smem(size_t bytes) {
 
 }  // namespace
 
+// Launch-shape choices of the decode kernels, measured on GB300 (per-CTA
+// globaltimer traces of graph-replayed 8 x 4096 -> 14336 bf16 and 8 x 5120 ->
+// 17408 Q4 calls):
+//  - the norm kernel releases the gate/up kernel right after its own wait,
+//    so the gate/up kernel is resident and requesting weights while the norm
+//    runs (Q4 call 38.2 us against 39.3 us when released at its end);
+//  - gate/up requests ONE stage of weights before its wait, not its whole
+//    ring: the wait returns once the norm kernel has completed, and that
+//    completion takes longer while megabytes of loads are in flight (3.1 us
+//    against 4.7 us after the call starts; Q4 call 38.2 against 38.9 us);
+//  - down requests its whole ring before its wait (the gate/up tail it
+//    overlaps has few loads left in flight).
+// FFN_NORM_RELEASE_EARLY, FFN_PRE_STAGES_GATEUP and FFN_PRE_STAGES_DOWN in the
+// environment override them (read once per process, for measurement).
+int decode_tuning(int knob) {
+    static int v[TUNE_COUNT] = {-1, -1, -1};
+    static const char *names[TUNE_COUNT] = {"FFN_NORM_RELEASE_EARLY", "FFN_PRE_STAGES_GATEUP", "FFN_PRE_STAGES_DOWN"};
+    static const int defaults[TUNE_COUNT] = {1, 1, 64};
+    if (v[knob] < 0) {
+        const char *e = getenv(names[knob]);
+        v[knob] = e ? atoi(e) : defaults[knob];
+        if (v[knob] < 0) v[knob] = 0;
+    }
+    return v[knob];
+}
+
 bool stream_supported(int wfmt, int64_t d, int64_t ffn) {
     if (wfmt == WF_Q4) return d % 256 == 0 && ffn % 256 == 0;
     if (wfmt == WF_FP8) return d % 256 == 0 && ffn % 256 == 0;
@@ -601,6 +631,7 @@ cudaError_t launch_stream_gateup(GemvWeights wg, GemvWeights wu, const void *nfr
     p.res = nullptr;
     p.rs0 = wg.rs;
     p.rs1 = wu.rs;
+    p.pre_stages = decode_tuning(TUNE_PRE_STAGES_GATEUP);
     // 32 features per CTA; covering nchF * 32 features writes every slot of h
     const int64_t blocks = nchF;
     LaunchScope scope(K_GEMV_GATEUP, s);
@@ -636,6 +667,7 @@ cudaError_t launch_stream_down(GemvWeights wd, const void *hfrag, const void *hf
     p.res = res;
     p.rs0 = wd.rs;
     p.rs1 = nullptr;
+    p.pre_stages = decode_tuning(TUNE_PRE_STAGES_DOWN);
     p.err = device_status_word();
     if (!p.err) return cudaErrorUnknown;
     const int64_t nsplit = cdiv(p.nkb, p.kb_per_split);
