@@ -76,6 +76,8 @@ class Oracle:
         L.oracle_rmsnorm.restype = None
         L.oracle_rmsnorm.argtypes = [_D, _D, _D, ctypes.c_int64, ctypes.c_int64,
                                      ctypes.c_double, ctypes.c_int]
+        L.oracle_row_sumsq.restype = None
+        L.oracle_row_sumsq.argtypes = [_D, _D, ctypes.c_int64, ctypes.c_int64]
         L.oracle_swiglu.restype = None
         L.oracle_swiglu.argtypes = [_D, _D, _D, ctypes.c_int64, ctypes.c_int]
         L.oracle_ffn_block.restype = ctypes.c_int
@@ -116,6 +118,14 @@ class Oracle:
         self.L.oracle_rmsnorm(_ptr(x), _ptr(g), _ptr(n), rows, d, float(eps),
                               nthreads or default_threads())
         return n
+
+    def row_sumsq(self, y) -> np.ndarray:
+        """Sum of squares of every row of y (the next RMSNorm's reduction)."""
+        y = np.ascontiguousarray(y, dtype=np.float64)
+        rows, d = y.shape
+        ss = np.empty(rows, dtype=np.float64)
+        self.L.oracle_row_sumsq(_ptr(y), _ptr(ss), rows, d)
+        return ss
 
     def swiglu(self, gate, up, nthreads: int | None = None) -> np.ndarray:
         gate = np.ascontiguousarray(gate, dtype=np.float64)

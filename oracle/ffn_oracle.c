@@ -29,6 +29,13 @@
  *               a half-precision scale).  w = (u - 8) * s with u the 4-bit
  *               offset-binary value; the layout is documented at
  *               oracle_q4_dequant below.
+ *   Row sum of squares -- "How Megakernels Work", section "Dependencies and
+ *               synchronization": after the down projection produces a hidden
+ *               vector, the next RMSNorm needs the sum of squares of all its
+ *               elements:
+ *                   ss[r] = sum_c y[r,c]^2
+ *               (oracle_row_sumsq; with the skip connection, y is the next
+ *               layer's input).
  *   Q8_0     -- "Unfusing a Kernel Made It 1.63x Faster", "Finding 2: a
  *               quantized KV cache buys nothing while you're
  *               occupancy-bound" (Q8_0, there for the KV cache): blocks of
@@ -137,6 +144,16 @@ void oracle_rmsnorm(const double *x, const double *g, double *n, int64_t rows,
                     int64_t d, double eps, int nthreads) {
     norm_ctx c = {x, g, n, d, eps};
     parallel_range(rows, nthreads, norm_rows, &c);
+}
+
+/* ss[r] = sum over c of y[r,c]^2, a left-to-right sum per row. */
+void oracle_row_sumsq(const double *y, double *ss, int64_t rows, int64_t d) {
+    for (int64_t r = 0; r < rows; ++r) {
+        const double *yr = y + r * d;
+        double acc = 0.0;
+        for (int64_t c = 0; c < d; ++c) acc += yr[c] * yr[c];
+        ss[r] = acc;
+    }
 }
 
 /* ---------------------------------------------------------------- SwiGLU */

@@ -223,6 +223,35 @@ def pin_block_residual(o):
     _close(got, xc + h @ w_down.T, rtol=1e-13, atol=1e-14)
 
 
+# ------------------------------------------------------- row sum of squares
+
+def pin_row_sumsq_values(o):
+    """Closed forms ([3, 4] -> 25, [1, 2, 2] -> 9, a zero row -> 0), exact
+    scaling by powers of two (ss(2^k y) = 4^k ss(y)), and brute force with an
+    exactly rounded sum (math.fsum) on random rows of several lengths."""
+    _close(o.row_sumsq(np.array([[3.0, 4.0], [0.0, 0.0]])), [25.0, 0.0], rtol=0, atol=0)
+    _close(o.row_sumsq(np.array([[1.0, 2.0, 2.0], [-1.0, -2.0, 2.0]])), [9.0, 9.0], rtol=0, atol=0)
+    rng = np.random.default_rng(30)
+    for d in (1, 7, 64, 333):
+        y = rng.standard_normal((5, d))
+        ss = o.row_sumsq(y)
+        _close(ss, [math.fsum(v * v for v in row) for row in y], rtol=1e-13, atol=0)
+        _close(o.row_sumsq(8.0 * y), 64.0 * ss, rtol=0, atol=0)
+
+
+def pin_row_sumsq_feeds_rmsnorm(o):
+    """The statistic is the reduction RMSNorm needs: x / sqrt(ss / d + eps) * g
+    is the oracle's own RMSNorm of x, and a row whose every element is c
+    gives d * c^2."""
+    rng = np.random.default_rng(31)
+    rows, d, eps = 4, 48, 1e-5
+    x = rng.standard_normal((rows, d))
+    g = 1.0 + 0.1 * rng.standard_normal(d)
+    ss = o.row_sumsq(x)
+    _close(x / np.sqrt(ss / d + eps)[:, None] * g, o.rmsnorm(x, g, eps), rtol=1e-13, atol=1e-15)
+    _close(o.row_sumsq(np.full((2, 10), -1.5)), [22.5, 22.5], rtol=0, atol=0)
+
+
 # ---------------------------------------------------------------------- Q4
 
 def pin_half_decoder(o):

@@ -38,6 +38,11 @@ MUTANTS = [
     ("q8_codes_unsigned", "(double)q[o * in + i] * oracle_half_to_double",
      "(double)(uint8_t)q[o * in + i] * oracle_half_to_double"),
     ("q8_scale_of_next_row", "scales[o * nblk + i / 32]", "scales[((o + 1) % out) * nblk + i / 32]"),
+    ("sumsq_abs", "for (int64_t c = 0; c < d; ++c) acc += yr[c] * yr[c];",
+     "for (int64_t c = 0; c < d; ++c) acc += fabs(yr[c]);"),
+    ("sumsq_mean", "        ss[r] = acc;\n", "        ss[r] = acc / (double)d;\n"),
+    ("sumsq_skips_first", "for (int64_t c = 0; c < d; ++c) acc += yr[c] * yr[c];",
+     "for (int64_t c = 1; c < d; ++c) acc += yr[c] * yr[c];"),
 ]
 
 
