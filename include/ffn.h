@@ -199,7 +199,7 @@ ffn_status ffn_block_q4_workspace_bytes(int64_t rows, int64_t d, int64_t ffn, si
 
 /* ------------------------------------------------------------------------
  * ffn_block_forward_q4 -- the block with Q4 weights, dequantised in registers.
- * "How Megakernels Work", section "Threadgroup staging" (stream Q4 weights
+ * "Megakernels on Mac: What Fusion Saves and What It Costs", section "Threadgroup staging" (stream Q4 weights
  * to registers; staging through shared memory lost).
  *   x [rows x d] bf16, g [d] bf16, y [rows x d] bf16; w_gate/w_up are Q4
  *   [ffn x d], w_down is Q4 [d x ffn].  Needs d % 128 == 0, ffn % 128 == 0,
@@ -317,7 +317,7 @@ ffn_status ffn_block_q8_workspace_bytes(int64_t rows, int64_t d, int64_t ffn, si
 
 /* ------------------------------------------------------------------------
  * ffn_block_forward_q8 -- the block with Q8_0 weights (decode: the weights
- * are streamed; "How Megakernels Work", section "Projection shape changes
+ * are streamed; "Megakernels on Mac: What Fusion Saves and What It Costs", section "Projection shape changes
  * the achieved rate").
  *   x [rows x d] bf16, g [d] bf16, y [rows x d] bf16; w_gate/w_up are Q8_0
  *   [ffn x d], w_down is Q8_0 [d x ffn].  Needs d % 256 == 0 and
@@ -371,7 +371,7 @@ const char *ffn_status_string(ffn_status status);
 ffn_status ffn_device_status(void);
 
 /* Failure-detection self test (no counterpart on the pages; the pages ask
- * for explicit failure behaviour -- "How Megakernels Work", section
+ * for explicit failure behaviour -- "Megakernels on Mac: What Fusion Saves and What It Costs", section
  * "Dependencies and synchronization").  Launches on `stream` one CTA in which
  * one role waits on an mbarrier phase that nothing completes, with the same
  * bounded wait every streaming kernel of this library uses, and gives up after

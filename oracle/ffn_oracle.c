@@ -29,7 +29,7 @@
  *               a half-precision scale).  w = (u - 8) * s with u the 4-bit
  *               offset-binary value; the layout is documented at
  *               oracle_q4_dequant below.
- *   Row sum of squares -- "How Megakernels Work", section "Dependencies and
+ *   Row sum of squares -- "Megakernels on Mac: What Fusion Saves and What It Costs", section "Dependencies and
  *               synchronization": after the down projection produces a hidden
  *               vector, the next RMSNorm needs the sum of squares of all its
  *               elements:

@@ -12,7 +12,7 @@
 // 128 gate columns and the 128 up columns of the same features side by side
 // (the B tile is 128 rows of W_gate stacked on 128 rows of W_up), so the
 // fused epilogue costs no extra accumulator space.  Both arms share this
-// kernel's main loop, tiles and schedule ("How Megakernels Work", section
+// kernel's main loop, tiles and schedule ("Megakernels on Mac: What Fusion Saves and What It Costs", section
 // "Packing and geometry in the unfused control"); only the epilogue differs.
 //
 // Kernel structure (one CTA per SM, persistent over output tiles):

@@ -2,7 +2,7 @@
 //
 // With at most 16 token rows every weight byte is used for at most 16
 // multiply-adds, far below the GB300's ridge point, so the time is the HBM
-// stream of W_gate, W_up and W_down ("How Megakernels Work", section
+// stream of W_gate, W_up and W_down ("Megakernels on Mac: What Fusion Saves and What It Costs", section
 // "Projection shape changes the achieved rate": eight-row projections, and
 // a deeper K split for the long-K down projection).  Design:
 //
@@ -17,7 +17,7 @@
 //   as long as the weight stream itself; the MMA needs one per 256 weights.
 // * Q4 weights ("Unfusing a Kernel Made It 1.63x Faster", section "The
 //   finding that keeps us honest about microbenchmarks": repacked so every
-//   block is read once, coalesced; "How Megakernels Work", section
+//   block is read once, coalesced; "Megakernels on Mac: What Fusion Saves and What It Costs", section
 //   "Threadgroup staging": no shared-memory staging) are dequantised in
 //   registers: nibbles become (u - 8) exactly in bf16, one block's two MMAs
 //   accumulate into a fresh fp32 fragment, and the block scale multiplies
