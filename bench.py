@@ -344,6 +344,7 @@ def sub_benchmarks(torch, ffn, device, peaks, peak_src, stream, with_oracle=True
     out.append(decode_bench(torch, ffn, device, hbm, peak_src, stream, None, with_oracle))
     # 128 decode tokens at once: tensor-core GEMMs with split-K down projection
     out.append(decode_bench(torch, ffn, device, hbm, peak_src, stream, synth.C8_BATCH_BF16, with_oracle))
+    out.append(chain_bench(torch, ffn, device, hbm, peak_src, stream))
     out.append(q4_bench(torch, ffn, device, hbm, peak_src, stream, with_oracle))
     out.append(fp8_bench(torch, ffn, device, hbm, peak_src, stream, with_oracle))
     out.append(q8_bench(torch, ffn, device, hbm, peak_src, stream, with_oracle))
@@ -402,6 +403,42 @@ def decode_bench(torch, ffn, device, hbm, peak_src, stream, cfg=None, with_oracl
         e["prepared_weights"]["parity"] = {"max_abs_over_rms": float(np.abs(gotp[sel] - ref).max() / rms),
                                            "mean_abs_over_rms": float(np.abs(gotp[sel] - ref).mean() / rms)}
     return e
+
+
+def chain_bench(torch, ffn, device, hbm, peak_src, stream):
+    """Two decode blocks in sequence (8 x 4096 -> 14336 bf16, two weight sets,
+    skip connection): each block's RMSNorm reducing its row itself, against
+    the first block handing its output rows' sums of squares to the second
+    (ffn_block_forward_chained)."""
+    cfg = synth.C3_DECODE_BF16
+    sets = []
+    for seed in (0, 1):
+        inp = synth.make_block_inputs(cfg, seed=seed)
+        sets.append([to_dev(inp[k], "bf16", torch, device) for k in ("x", "g", "w_gate", "w_up", "w_down")])
+    R = ffn.FFN_RESIDUAL
+    y1, y2 = torch.empty_like(sets[0][0]), torch.empty_like(sets[0][0])
+    ss1, ss2 = (torch.empty(cfg.rows, dtype=torch.float32, device=device) for _ in range(2))
+    ws = ffn.workspace(ffn.ffn_block_workspace_bytes(cfg.rows, cfg.d, cfg.ffn, torch.bfloat16, R), device)
+    x = sets[0][0]
+
+    def plain(_i):
+        ffn.ffn_block_forward(x, *sets[0][1:], eps=cfg.eps, flags=R, out=y1, ws=ws)
+        ffn.ffn_block_forward(y1, *sets[1][1:], eps=cfg.eps, flags=R, out=y2, ws=ws)
+
+    def chained(_i):
+        ffn.ffn_block_forward_chained(x, *sets[0][1:], eps=cfg.eps, flags=R, out=y1, ss_out=ss1, ws=ws)
+        ffn.ffn_block_forward_chained(y1, *sets[1][1:], eps=cfg.eps, flags=R, x_sumsq=ss1, out=y2, ss_out=ss2,
+                                      ws=ws)
+
+    us_plain = graph_time_us(torch, plain, 10, 10, stream)
+    us_chain = graph_time_us(torch, chained, 10, 10, stream)
+    wbytes = 2 * 3 * cfg.ffn * cfg.d * 2
+    return {"workload": "decode_chain_2x_bf16_8x4096x14336", "us_per_call": round(us_chain, 3),
+            "tokens_per_s": round(cfg.rows / us_chain * 1e6, 1),
+            "timing": "CUDA graph of 10 two-block sequences, 10 replays (us per two-block sequence)",
+            "plain_us": round(us_plain, 3),
+            "note": "chained: block 1 hands its output rows' sums of squares to block 2's RMSNorm",
+            "roofline": hbm_roof(wbytes, us_chain, hbm, peak_src, "two blocks")}
 
 
 def q4_setup(torch, ffn, device, inp=None):

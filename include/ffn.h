@@ -148,6 +148,33 @@ ffn_status ffn_block_forward(const void *x, const void *g, const void *w_gate, c
                              size_t workspace_bytes, void *stream);
 
 /* ------------------------------------------------------------------------
+ * ffn_block_forward_chained -- ffn_block_forward that hands the RMSNorm
+ * reduction from one block to the next.  "Megakernels on Mac: What Fusion
+ * Saves and What It Costs", section "Dependencies and synchronization": after
+ * a down projection produces a hidden vector, the next RMSNorm needs the sum
+ * of squares of all its elements, and a worker that finishes one part of the
+ * row must leave its partial sum until the last part is done.
+ *   x_sumsq (optional, NULL = reduce the row as usual): [rows] fp32 device,
+ *     sum over c of x[r,c]^2; the RMSNorm uses it instead of reducing x
+ *     (e.g. the previous call's y_sumsq, with x that call's y).
+ *   y_sumsq (optional): [rows] fp32 device, receives sum over c of y[r,c]^2
+ *     of the y this call stores.  Where the down projection finishes a part
+ *     of a row (a 64-column group on the decode kernels, an output tile on
+ *     the tensor-core path), it adds the squares of the values it stored;
+ *     the last part of a row to finish adds the parts in column order
+ *     (fp32, the same bits every run).  Where that projection splits its
+ *     reduction, the kernel that adds the splits sums each row; on the fp32
+ *     path one pass over y sums each row.  With FFN_RESIDUAL, y is the next
+ *     block's x and y_sumsq its x_sumsq.
+ *   Both 16-byte aligned; y_sumsq overlaps no other argument or the
+ *   workspace.  Everything else as ffn_block_forward (same workspace size).
+ * ---------------------------------------------------------------------- */
+ffn_status ffn_block_forward_chained(const void *x, const float *x_sumsq, const void *g, const void *w_gate,
+                                     const void *w_up, const void *w_down, void *y, float *y_sumsq, int64_t rows,
+                                     int64_t d, int64_t ffn, float eps, ffn_dtype dtype, uint32_t flags,
+                                     void *workspace, size_t workspace_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
  * ffn_block_forward_host -- ffn_block_forward with x and y in HOST memory
  * (page-locked for the copies to overlap; pageable memory works, serialised).
  * The same block as ffn_block_forward ("Unfusing a Kernel Made It 1.63x

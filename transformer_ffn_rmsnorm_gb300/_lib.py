@@ -50,6 +50,9 @@ SIGNATURES = {
     "ffn_block_forward": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                   c_int64, c_int64, c_int64, c_float, c_int, c_uint32, c_void_p,
                                   c_size_t, c_void_p]),
+    "ffn_block_forward_chained": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                          c_void_p, c_int64, c_int64, c_int64, c_float, c_int, c_uint32,
+                                          c_void_p, c_size_t, c_void_p]),
     "ffn_block_host_workspace_bytes": (c_int, [c_int64, c_int64, c_int64, c_int, c_uint32,
                                                ctypes.POINTER(c_size_t)]),
     "ffn_block_forward_host": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,

@@ -143,6 +143,10 @@ ffn_status plan_block(int64_t rows, int64_t d, int64_t ffn, ffn_dtype dt, uint32
             if (!plan->fused) plan->workspace += 2 * align256(r * ffn * 4);
             // split-K partial sums of the down GEMM (few rows)
             plan->workspace += align256(gemm_plain_partial_bytes(rows, ffn, d, plan->split_act ? 2 : 1));
+            // the rows' sums of squares of y (ffn_block_forward_chained): parts per
+            // 64-column block (the narrowest down tile) and counters per 128 rows
+            plan->workspace += align256(static_cast<size_t>((d + 63) / 64) * r * 4) +
+                               align256(static_cast<size_t>((rows + 127) / 128) * 4);
             // a workspace sized for these rows also serves every smaller
             // batch, those that take the decode kernels included
             if (gemv_rows > 0)
@@ -272,10 +276,10 @@ ffn_status ffn_block_workspace_bytes(int64_t rows, int64_t d, int64_t ffn, ffn_d
     return FFN_OK;
 }
 
-ffn_status ffn_block_forward(const void *x, const void *g, const void *w_gate, const void *w_up,
-                             const void *w_down, void *y, int64_t rows, int64_t d, int64_t ffn,
-                             float eps, ffn_dtype dtype, uint32_t flags, void *workspace,
-                             size_t workspace_bytes, void *stream) {
+static ffn_status block_forward(const void *x, const float *x_sumsq, const void *g, const void *w_gate,
+                                const void *w_up, const void *w_down, void *y, float *y_sumsq, int64_t rows,
+                                int64_t d, int64_t ffn, float eps, ffn_dtype dtype, uint32_t flags,
+                                void *workspace, size_t workspace_bytes, void *stream) {
     if (!g || !w_gate || !w_up || !w_down || (rows != 0 && (!x || !y))) return FFN_ERR_NULL;
     Plan plan;
     ffn_status st = plan_block(rows, d, ffn, dtype, flags, &plan);
@@ -294,6 +298,12 @@ ffn_status ffn_block_forward(const void *x, const void *g, const void *w_gate, c
     for (const Range &in : {rx, rg, rwg, rwu, rwd})
         if (overlaps(ry, in) || overlaps(rws, in)) return FFN_ERR_ALIAS;
     if (overlaps(ry, rws)) return FFN_ERR_ALIAS;
+    if ((x_sumsq && !aligned16(x_sumsq)) || (y_sumsq && !aligned16(y_sumsq))) return FFN_ERR_ALIGN;
+    if (y_sumsq) {   // written last: may overlap nothing the call reads or writes
+        const Range rso{y_sumsq, static_cast<size_t>(rows) * 4}, rsi{x_sumsq, static_cast<size_t>(rows) * 4};
+        for (const Range &o : {rx, rg, rwg, rwu, rwd, ry, rws, rsi})
+            if (overlaps(rso, o)) return FFN_ERR_ALIAS;
+    }
     if (rows == 0) return FFN_OK;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -307,7 +317,7 @@ ffn_status ffn_block_forward(const void *x, const void *g, const void *w_gate, c
                 static_cast<const float *>(x), static_cast<const float *>(g),
                 static_cast<const float *>(w_gate), static_cast<const float *>(w_up),
                 static_cast<const float *>(w_down), static_cast<float *>(y), rows, d, ffn, eps, n, h, s,
-                static_cast<const float *>(res)));
+                static_cast<const float *>(res), x_sumsq, y_sumsq));
         }
         case PATH_GEMV: {
             GemvWorkspace gw;
@@ -315,7 +325,10 @@ ffn_status ffn_block_forward(const void *x, const void *g, const void *w_gate, c
             GemvWeights a{w_gate, nullptr, nullptr}, b{w_up, nullptr, nullptr}, c{w_down, nullptr, nullptr};
             const int wf = plan.prepared ? (dtype == FFN_BF16 ? WF_F16P : WF_F16)
                                          : (dtype == FFN_BF16 ? WF_BF16 : WF_F16);
-            return from_cuda(launch_gemv_block(wf, x, g, a, b, c, y, rows, d, ffn, eps, gw, s, res));
+            RowStats rs;
+            rs.ss_in = x_sumsq;
+            rs.ss_out = y_sumsq;
+            return from_cuda(launch_gemv_block(wf, x, g, a, b, c, y, rows, d, ffn, eps, gw, s, res, rs));
         }
         case PATH_GEMM: {
             const size_t nb = align256(static_cast<size_t>(rows) * d * es);
@@ -343,31 +356,53 @@ ffn_status ffn_block_forward(const void *x, const void *g, const void *w_gate, c
             const float h_scale = plan.prepared ? 1.f / 256.f : 1.f;
             cudaError_t e;
             if (plan.prepared)
-                e = launch_rmsnorm_to_f16(x, g, n, rows, d, eps, dtype, s);
+                e = launch_rmsnorm_to_f16(x, g, n, rows, d, eps, dtype, s, x_sumsq);
             else if (plan.split_act)
-                e = launch_rmsnorm_split(x, g, n, n_lo, rows, d, eps, dtype, s);
+                e = launch_rmsnorm_split(x, g, n, n_lo, rows, d, eps, dtype, s, x_sumsq);
             else
-                e = launch_rmsnorm(x, g, n, rows, d, eps, dtype, s);
+                e = launch_rmsnorm(x, g, n, rows, d, eps, dtype, s, x_sumsq);
             if (e != cudaSuccess) return FFN_ERR_CUDA;
-            // split-K partials: after h, or after G and U when unfused
-            float *part = reinterpret_cast<float *>(
-                plan.fused ? p : p + 2 * align256(static_cast<size_t>(rows) * ffn * 4));
+            // split-K partials: after h, or after G and U when unfused; then
+            // the parts and counters of the rows' sums of squares of y
+            char *pp = plan.fused ? p : p + 2 * align256(static_cast<size_t>(rows) * ffn * 4);
+            float *part = reinterpret_cast<float *>(pp);
+            pp += align256(gemm_plain_partial_bytes(rows, ffn, d, plan.split_act ? 2 : 1));
+            float *ss_part = reinterpret_cast<float *>(pp);
+            pp += align256(static_cast<size_t>((d + 63) / 64) * rows * 4);
+            unsigned *ss_ctr = reinterpret_cast<unsigned *>(pp);
+            const int nctr = y_sumsq ? static_cast<int>((rows + 127) / 128) : 0;
             if (plan.fused) {
                 e = launch_gemm_gateup(op, n, n_lo, w_gate, w_up, h, h_lo, nullptr, nullptr, rows, d,
-                                       ffn, true, w_unscale, h_scale, s);
+                                       ffn, true, w_unscale, h_scale, s, ss_ctr, nctr);
             } else {
                 float *G = reinterpret_cast<float *>(p);
                 float *U = reinterpret_cast<float *>(p + align256(static_cast<size_t>(rows) * ffn * 4));
                 e = launch_gemm_gateup(op, n, n_lo, w_gate, w_up, nullptr, nullptr, G, U, rows, d, ffn,
-                                       false, w_unscale, 1.f, s);
+                                       false, w_unscale, 1.f, s, ss_ctr, nctr);
                 if (e == cudaSuccess) e = launch_swiglu_f32in(G, U, h, h_lo, rows * ffn, op, h_scale, s);
             }
             if (e != cudaSuccess) return FFN_ERR_CUDA;
             return from_cuda(launch_gemm_plain(op, dtype, h, h_lo, w_down, y, rows, ffn, d,
-                                               w_unscale / h_scale, res, part, s));
+                                               w_unscale / h_scale, res, part, s, ss_part, ss_ctr, y_sumsq));
         }
     }
     return FFN_ERR_SHAPE;
+}
+
+ffn_status ffn_block_forward(const void *x, const void *g, const void *w_gate, const void *w_up,
+                             const void *w_down, void *y, int64_t rows, int64_t d, int64_t ffn,
+                             float eps, ffn_dtype dtype, uint32_t flags, void *workspace,
+                             size_t workspace_bytes, void *stream) {
+    return block_forward(x, nullptr, g, w_gate, w_up, w_down, y, nullptr, rows, d, ffn, eps, dtype, flags,
+                         workspace, workspace_bytes, stream);
+}
+
+ffn_status ffn_block_forward_chained(const void *x, const float *x_sumsq, const void *g, const void *w_gate,
+                                     const void *w_up, const void *w_down, void *y, float *y_sumsq, int64_t rows,
+                                     int64_t d, int64_t ffn, float eps, ffn_dtype dtype, uint32_t flags,
+                                     void *workspace, size_t workspace_bytes, void *stream) {
+    return block_forward(x, x_sumsq, g, w_gate, w_up, w_down, y, y_sumsq, rows, d, ffn, eps, dtype, flags,
+                         workspace, workspace_bytes, stream);
 }
 
 ffn_status ffn_block_q4_workspace_bytes(int64_t rows, int64_t d, int64_t ffn, size_t *bytes) {

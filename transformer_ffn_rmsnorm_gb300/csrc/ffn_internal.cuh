@@ -70,15 +70,18 @@ unsigned *device_status_word();   // device address, for the current device
 int sm_count();                   // multiprocessors on the current device
 
 // ---------------------------------------------------------------- launchers
+// ss_in (optional): each row's sum of squares of x, used instead of reducing
+// the row (the block before handed it on).
 cudaError_t launch_rmsnorm(const void *x, const void *g, void *n, int64_t rows, int64_t d,
-                           float eps, int dt, cudaStream_t s);
+                           float eps, int dt, cudaStream_t s, const float *ss_in = nullptr);
 // As launch_rmsnorm, for 16-bit storage, also writing the rounding residual:
 // n_hi = round(v), n_lo = round(v - n_hi), so n_hi + n_lo carries ~16 bits.
 cudaError_t launch_rmsnorm_split(const void *x, const void *g, void *n_hi, void *n_lo,
-                                 int64_t rows, int64_t d, float eps, int dt, cudaStream_t s);
+                                 int64_t rows, int64_t d, float eps, int dt, cudaStream_t s,
+                                 const float *ss_in = nullptr);
 // 16-bit x and g of type dt_in, n written as fp16 (operand of fp16 tensor ops).
 cudaError_t launch_rmsnorm_to_f16(const void *x, const void *g, void *n, int64_t rows, int64_t d,
-                                  float eps, int dt_in, cudaStream_t s);
+                                  float eps, int dt_in, cudaStream_t s, const float *ss_in = nullptr);
 // dst[i] = fp16(src[i] * 2^8) for 16-bit src of type dt; out-of-range values
 // set DEVERR_RANGE in the device status word.
 cudaError_t launch_prepare_weights(const void *src, void *dst, int64_t count, int dt, cudaStream_t s);
@@ -104,7 +107,7 @@ cudaError_t launch_swiglu_f32in(const float *gate, const float *up, void *h, voi
 cudaError_t launch_simt_block(const float *x, const float *g, const float *wg, const float *wu,
                               const float *wd, float *y, int64_t rows, int64_t d, int64_t ffn,
                               float eps, float *n, float *h, cudaStream_t s,
-                              const float *res = nullptr);
+                              const float *res = nullptr, const float *ss_in = nullptr, float *ss_out = nullptr);
 
 // Decode (weight-streaming) block for rows <= 16.
 struct GemvWorkspace {
@@ -113,7 +116,15 @@ struct GemvWorkspace {
     void *nfrag_lo;     // their rounding residuals (two-term operands), or null
     void *hfrag_lo;
     float *partials;    // [splits][rows][d] fp32
-    unsigned *counters; // [d / 64] arrival counters
+    unsigned *counters; // [d / 64] arrival counters, then one for the rows' sums of squares
+    float *ss_part;     // [d / 64][rows] parts of the rows' sums of squares of y
+};
+// The block's RMSNorm reduction handed from one block to the next: ss_in (or
+// null) holds each row's sum of squares of x, used instead of reducing the
+// row; ss_out (or null) receives each row's sum of squares of the stored y.
+struct RowStats {
+    const float *ss_in = nullptr;
+    float *ss_out = nullptr;
 };
 size_t gemv_workspace_bytes(int64_t rows, int64_t d, int64_t ffn, bool two_terms);
 void gemv_carve(void *base, int64_t rows, int64_t d, int64_t ffn, bool two_terms, GemvWorkspace *ws);
@@ -131,7 +142,7 @@ struct GemvWeights {
 cudaError_t launch_gemv_block(int wfmt, const void *x, const void *g, GemvWeights wg,
                               GemvWeights wu, GemvWeights wd, void *y, int64_t rows, int64_t d,
                               int64_t ffn, float eps, const GemvWorkspace &ws, cudaStream_t s,
-                              const void *res = nullptr);
+                              const void *res = nullptr, RowStats rs = {});
 
 // A 2D tiled TMA descriptor over a row-major array of `rows` rows, `inner`
 // elements a row, rows `row_bytes` apart; boxes of box_inner x box_rows.
@@ -147,17 +158,24 @@ bool encode_tma_2d(CUtensorMap *m, const void *ptr, CUtensorMapDataType dt, int6
 //   down:    A = h [M x F] (plus residual A_lo, or nullptr), B = W_down [N x F]
 //            -> C = accumulator * acc_scale [M x N] stored as dt_out
 // dt: the operand type (bf16 or fp16); h has the operand type.
+// zero, nzero: counters the down projection of the same call uses, zeroed
+// once the kernel before this one has completed.
 cudaError_t launch_gemm_gateup(int dt, const void *A, const void *A_lo, const void *Wg,
                                const void *Wu, void *H, void *H_lo, void *G, void *U, int64_t M,
                                int64_t K, int64_t F, bool fused, float acc_scale, float out_scale,
-                               cudaStream_t s);
+                               cudaStream_t s, unsigned *zero = nullptr, int nzero = 0);
 // res (optional): added to C before its one rounding (same type and layout as C).
 // part: fp32 scratch of gemm_plain_partial_bytes(M, K, N, A_lo ? 2 : 1) bytes
 // (16-byte aligned) for the split-K partial sums of short, wide-K products;
 // may be null when that size is 0.  That size never decreases with M.
+// ss_out (optional): each row's sum of squares of the stored C, through
+// ss_part [ceil(N / 64)][M] fp32 and ss_ctr [ceil(M / 128)] counters (zero
+// when the GEMM starts) -- or, when the reduction is split, by the kernel
+// that adds the splits.
 cudaError_t launch_gemm_plain(int dt, int dt_out, const void *A, const void *A_lo, const void *B,
                               void *C, int64_t M, int64_t K, int64_t N, float acc_scale,
-                              const void *res, float *part, cudaStream_t s);
+                              const void *res, float *part, cudaStream_t s, float *ss_part = nullptr,
+                              unsigned *ss_ctr = nullptr, float *ss_out = nullptr);
 size_t gemm_plain_partial_bytes(int64_t M, int64_t K, int64_t N, int a_terms);
 
 }  // namespace ffn

@@ -106,6 +106,25 @@ struct GemmParams {
     float out_scale;          // fused: applied to h before rounding
     int a_keep;               // keep A in L2 (evict-last): every wave of tiles re-reads it
     const void *res;          // plain: added to C before rounding (same type and layout as C), or null
+    // plain, unsplit, with ss_out: each row's sum of squares of the stored C,
+    // through per-column-block parts ss_part[n_blk][M] and per-row-block
+    // arrival counters ss_ctr[m_blk] (zero at the start; the last arrival
+    // adds the parts in column-block order)
+    float *ss_part;
+    unsigned *ss_ctr;
+    float *ss_out;
+    unsigned *zero;           // counters of a later kernel of the call, zeroed once the wait returns
+    int nzero;
+};
+
+// What a launch adds to the plain GEMM's output, and what it clears for a
+// later kernel (see GemmParams).
+struct GemmRowSS {
+    float *part = nullptr;
+    unsigned *ctr = nullptr;
+    float *out = nullptr;
+    unsigned *zero = nullptr;
+    int nzero = 0;
 };
 
 // Stores NV (16 or 32) values rounded once; with `lo` also the rounding
@@ -130,6 +149,22 @@ __device__ __forceinline__ void store_row(T *dst, T *lo, int64_t col, int64_t nc
             }
         }
     }
+}
+
+// Sum of the squares of v rounded to T (the values store_row writes), over
+// the columns below ncols, in column order.
+template <typename T, int NV>
+__device__ __forceinline__ float stored_sumsq(int64_t col, int64_t ncols, const float (&v)[NV]) {
+    float s = 0.f;
+#pragma unroll
+    for (int j = 0; j < NV / 8; ++j)
+        if (col + 8 * j < ncols)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float r = to_f32(from_f32<T>(v[8 * j + e]));
+                s = fmaf(r, r, s);
+            }
+    return s;
 }
 
 // v[e] += src[col + e] for the NV (16 or 32) columns from col that are
@@ -395,6 +430,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     } else if (warp >= 2) {
         // ---------------------------------------------------------- epilogue
         ptx::griddep_wait();   // outputs may be read by the kernel before this one
+        if (blockIdx.x == 0 && warp == 2)
+            for (int i = lane; i < p.nzero; i += 32) p.zero[i] = 0u;
         const int q = warp & 3;   // this warp may read TMEM lanes 32q .. 32q+31
         bool ok = true;
         uint32_t acc = 0, acc_ph = 0;
@@ -413,6 +450,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int64_t row = m_blk * BM + q * 32 + lane;
             const bool live = row < p.M;
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+            float ss = 0.f;   // this row's stored values squared, over the tile's columns
             if (MODE == MODE_PLAIN) {
 #pragma unroll 1
                 for (int c = 0; c < BN; c += CW) {
@@ -431,6 +469,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             if (p.res)
                                 add_row<TOut, CW>(static_cast<const TOut *>(p.res) + row * p.ldo, col, p.N, v);
                             store_row<TOut, CW>(static_cast<TOut *>(p.out0) + row * p.ldo, nullptr, col, p.N, v);
+                            if (p.ss_out) ss += stored_sumsq<TOut, CW>(col, p.N, v);
                         }
                     }
                 }
@@ -474,6 +513,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             acc ^= 1u;
             if (acc == 0) acc_ph ^= 1u;
+            if (MODE == MODE_PLAIN && p.ss_out && !p.part) {
+                // "Megakernels on Mac: What Fusion Saves and What It Costs",
+                // "Dependencies and synchronization": the next RMSNorm needs
+                // the whole row's sum of squares; each warp leaves its rows'
+                // part for this column block, and the last of the row block's
+                // arrivals (4 warps per column block) adds them in order
+                if (live) p.ss_part[n_blk * p.M + row] = ss;
+                __syncwarp();
+                unsigned last = 0;
+                if (lane == 0) {
+                    __threadfence();
+                    last = atomicAdd(&p.ss_ctr[m_blk], 1u) == static_cast<unsigned>(4 * p.num_n_blocks - 1);
+                }
+                if (__shfl_sync(0xffffffffu, last, 0)) {
+                    __threadfence();
+                    for (int r = lane; r < BM; r += 32) {
+                        const int64_t rr = m_blk * BM + r;
+                        if (rr >= p.M) continue;
+                        float t = 0.f;
+                        for (int64_t nb = 0; nb < p.num_n_blocks; ++nb) t += __ldcg(p.ss_part + nb * p.M + rr);
+                        p.ss_out[rr] = t;
+                    }
+                    if (lane == 0) p.ss_ctr[m_blk] = 0u;
+                }
+            }
         }
         if (!ok && lane == 0) {
             atomicOr(p.err, DEVERR_TIMEOUT);
@@ -559,7 +623,7 @@ template <int MODE, bool BF16, int A_TERMS, bool OUT_BF16, int BN, bool PAIR>
 cudaError_t launch_kernel(const void *A, const void *A2, const void *B0, const void *B1, void *out0,
                           void *out1, int64_t M, int64_t K, int64_t N, int kind, float acc_scale,
                           float out_scale, const void *res, float *part, int kst_per_split, int splits,
-                          cudaStream_t s) {
+                          GemmRowSS ex, cudaStream_t s) {
     constexpr size_t SMEM_BYTES = Ring<A_TERMS, BN, PAIR>::SMEM_BYTES;
     constexpr int NCTA = PAIR ? 2 : 1;
     using RG = Ring<A_TERMS, BN, PAIR>;
@@ -628,6 +692,11 @@ cudaError_t launch_kernel(const void *A, const void *A2, const void *B0, const v
     // fastest); ask L2 to keep it when it fits comfortably
     p.a_keep = (num_n_blocks > 1 && M * K * 2 * A_TERMS <= (int64_t{96} << 20)) ? 1 : 0;
     p.res = res;
+    p.ss_part = ex.part;
+    p.ss_ctr = ex.ctr;
+    p.ss_out = ex.out;
+    p.zero = ex.zero;
+    p.nzero = ex.nzero;
     if (!p.err) return cudaErrorUnknown;
     // persistent: one unit of CTAs per co-resident slot, never more units
     // than there is work for
@@ -658,15 +727,15 @@ template <int MODE, bool BF16, int A_TERMS, bool OUT_BF16 = BF16, int BN = 256>
 cudaError_t launch_impl(const void *A, const void *A2, const void *B0, const void *B1, void *out0,
                         void *out1, int64_t M, int64_t K, int64_t N, int kind, float acc_scale,
                         float out_scale, cudaStream_t s, const void *res = nullptr, float *part = nullptr,
-                        int kst_per_split = 0, int splits = 1) {
+                        int kst_per_split = 0, int splits = 1, GemmRowSS ex = {}) {
     if (M <= 0) return cudaSuccess;
     if (M > BM)
         return launch_kernel<MODE, BF16, A_TERMS, OUT_BF16, BN, true>(A, A2, B0, B1, out0, out1, M, K, N, kind,
                                                                        acc_scale, out_scale, res, part,
-                                                                       kst_per_split, splits, s);
+                                                                       kst_per_split, splits, ex, s);
     return launch_kernel<MODE, BF16, A_TERMS, OUT_BF16, BN, false>(A, A2, B0, B1, out0, out1, M, K, N, kind,
                                                                     acc_scale, out_scale, res, part,
-                                                                    kst_per_split, splits, s);
+                                                                    kst_per_split, splits, ex, s);
 }
 
 // Waves of tiles times the width of a tile (the time of a wave scales with
@@ -810,9 +879,64 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float *part, i
     }
 }
 
+// The same sums a row per CTA, also writing the row's sum of squares of the
+// stored values (fixed thread-to-column map and reduction tree: the same bits
+// every run).  N is a multiple of 8.
+template <typename TOut>
+__global__ void __launch_bounds__(256) splitk_reduce_rows_kernel(const float *part, int splits, int64_t M, int64_t N,
+                                                                 const TOut *res, TOut *out, float *ss_out) {
+    ptx::griddep_wait();
+    ptx::griddep_launch_dependents();
+    __shared__ float red[8];
+    const int64_t row = blockIdx.x, n4 = N / 4, count4 = M * n4;
+    const float4 *p4 = reinterpret_cast<const float4 *>(part);
+    float ss = 0.f;
+    for (int64_t c = threadIdx.x; c < n4; c += 256) {
+        const int64_t i = row * n4 + c;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int sp = 0; sp < splits; ++sp) {
+            const float4 v = __ldcs(p4 + sp * count4 + i);
+            acc.x += v.x;
+            acc.y += v.y;
+            acc.z += v.z;
+            acc.w += v.w;
+        }
+        if (res) {
+            const float4 r = unpack4<TOut>(reinterpret_cast<const uint2 *>(res)[i]);
+            acc.x += r.x;
+            acc.y += r.y;
+            acc.z += r.z;
+            acc.w += r.w;
+        }
+        const uint2 pk = pack4<TOut>(acc.x, acc.y, acc.z, acc.w);
+        reinterpret_cast<uint2 *>(out)[i] = pk;
+        const float4 r = unpack4<TOut>(pk);
+        ss = fmaf(r.x, r.x, ss);
+        ss = fmaf(r.y, r.y, ss);
+        ss = fmaf(r.z, r.z, ss);
+        ss = fmaf(r.w, r.w, ss);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float t = 0.f;
+        for (int w = 0; w < 8; ++w) t += red[w];
+        ss_out[row] = t;
+    }
+}
+
 template <typename TOut>
 cudaError_t launch_splitk_reduce(const float *part, int splits, int64_t count, const void *res, void *out,
-                                 cudaStream_t s) {
+                                 cudaStream_t s, int64_t M = 0, float *ss_out = nullptr) {
+    if (ss_out) {
+        LaunchScope scope(K_SPLITK_REDUCE, s);
+        cudaError_t e = launch_dependent(splitk_reduce_rows_kernel<TOut>, dim3(static_cast<unsigned>(M)), dim3(256),
+                                         0, s, part, splits, M, count / M, static_cast<const TOut *>(res),
+                                         static_cast<TOut *>(out), ss_out);
+        return e != cudaSuccess ? e : cudaGetLastError();
+    }
     const int64_t n4 = count / 4;
     int64_t blocks = static_cast<int64_t>(sm_count()) * 8;
     const int64_t need = (n4 + 255) / 256;
@@ -828,19 +952,19 @@ cudaError_t launch_splitk_reduce(const float *part, int splits, int64_t count, c
 template <int MODE, bool BF16, int A_TERMS>
 cudaError_t launch_gateup_bn(const void *A, const void *A2, const void *B0, const void *B1, void *out0,
                              void *out1, int64_t M, int64_t K, int64_t N, float acc_scale, float out_scale,
-                             cudaStream_t s) {
+                             GemmRowSS ex, cudaStream_t s) {
     if (gateup_width(M, N) == 192)
         return launch_impl<MODE, BF16, A_TERMS, BF16, 192>(A, A2, B0, B1, out0, out1, M, K, N, K_GEMM_GATEUP,
-                                                           acc_scale, out_scale, s);
+                                                           acc_scale, out_scale, s, nullptr, nullptr, 0, 1, ex);
     return launch_impl<MODE, BF16, A_TERMS, BF16, 256>(A, A2, B0, B1, out0, out1, M, K, N, K_GEMM_GATEUP,
-                                                       acc_scale, out_scale, s);
+                                                       acc_scale, out_scale, s, nullptr, nullptr, 0, 1, ex);
 }
 
 // One row block and a reduction too short to split: 64-wide tiles (d 4096:
 // 64 CTAs instead of 16).
 template <bool BF16, int A_TERMS, bool OUT_BF16>
 cudaError_t launch_plain_bn(const void *A, const void *A_lo, const void *B, void *C, int64_t M, int64_t K,
-                            int64_t N, float acc_scale, const void *res, float *part, cudaStream_t s) {
+                            int64_t N, float acc_scale, const void *res, float *part, GemmRowSS ex, cudaStream_t s) {
     using TOut = typename std::conditional<OUT_BF16, __nv_bfloat16, __half>::type;
     int per = 0, bn = 256;
     const int splits = plain_split_plan(M, K, N, A_TERMS, &per, &bn);
@@ -854,16 +978,19 @@ cudaError_t launch_plain_bn(const void *A, const void *A_lo, const void *B, void
                                                                               K_GEMM_DOWN, acc_scale, 1.f, s, nullptr,
                                                                               part, per, splits);
         if (e != cudaSuccess) return e;
-        return launch_splitk_reduce<TOut>(part, splits, M * N, res, C, s);
+        return launch_splitk_reduce<TOut>(part, splits, M * N, res, C, s, M, ex.out);
     }
     if (M <= BM)
         return launch_impl<MODE_PLAIN, BF16, A_TERMS, OUT_BF16, 64>(A, A_lo, B, nullptr, C, nullptr, M, K, N,
-                                                                    K_GEMM_DOWN, acc_scale, 1.f, s, res);
+                                                                    K_GEMM_DOWN, acc_scale, 1.f, s, res, nullptr, 0,
+                                                                    1, ex);
     if (tile_width(M, N) == 224)
         return launch_impl<MODE_PLAIN, BF16, A_TERMS, OUT_BF16, 224>(A, A_lo, B, nullptr, C, nullptr, M, K,
-                                                                     N, K_GEMM_DOWN, acc_scale, 1.f, s, res);
+                                                                     N, K_GEMM_DOWN, acc_scale, 1.f, s, res, nullptr,
+                                                                     0, 1, ex);
     return launch_impl<MODE_PLAIN, BF16, A_TERMS, OUT_BF16, 256>(A, A_lo, B, nullptr, C, nullptr, M, K, N,
-                                                                 K_GEMM_DOWN, acc_scale, 1.f, s, res);
+                                                                 K_GEMM_DOWN, acc_scale, 1.f, s, res, nullptr, 0, 1,
+                                                                 ex);
 }
 
 }  // namespace
@@ -890,37 +1017,45 @@ size_t gemm_plain_partial_bytes(int64_t M, int64_t K, int64_t N, int a_terms) {
 cudaError_t launch_gemm_gateup(int dt, const void *A, const void *A_lo, const void *Wg,
                                const void *Wu, void *H, void *H_lo, void *G, void *U, int64_t M,
                                int64_t K, int64_t F, bool fused, float acc_scale, float out_scale,
-                               cudaStream_t s) {
+                               cudaStream_t s, unsigned *zero, int nzero) {
     const bool bf = dt == DT_BF16;
     const float a = acc_scale, o = out_scale;
+    GemmRowSS ex;
+    ex.zero = zero;
+    ex.nzero = nzero;
     if (A_lo) {
         if (fused)
-            return bf ? launch_gateup_bn<MODE_GATEUP_FUSED, true, 2>(A, A_lo, Wg, Wu, H, H_lo, M, K, F, a, o, s)
-                      : launch_gateup_bn<MODE_GATEUP_FUSED, false, 2>(A, A_lo, Wg, Wu, H, H_lo, M, K, F, a, o, s);
-        return bf ? launch_gateup_bn<MODE_GATEUP_SPLIT, true, 2>(A, A_lo, Wg, Wu, G, U, M, K, F, a, o, s)
-                  : launch_gateup_bn<MODE_GATEUP_SPLIT, false, 2>(A, A_lo, Wg, Wu, G, U, M, K, F, a, o, s);
+            return bf ? launch_gateup_bn<MODE_GATEUP_FUSED, true, 2>(A, A_lo, Wg, Wu, H, H_lo, M, K, F, a, o, ex, s)
+                      : launch_gateup_bn<MODE_GATEUP_FUSED, false, 2>(A, A_lo, Wg, Wu, H, H_lo, M, K, F, a, o, ex, s);
+        return bf ? launch_gateup_bn<MODE_GATEUP_SPLIT, true, 2>(A, A_lo, Wg, Wu, G, U, M, K, F, a, o, ex, s)
+                  : launch_gateup_bn<MODE_GATEUP_SPLIT, false, 2>(A, A_lo, Wg, Wu, G, U, M, K, F, a, o, ex, s);
     }
     if (fused)
-        return bf ? launch_gateup_bn<MODE_GATEUP_FUSED, true, 1>(A, nullptr, Wg, Wu, H, H_lo, M, K, F, a, o, s)
-                  : launch_gateup_bn<MODE_GATEUP_FUSED, false, 1>(A, nullptr, Wg, Wu, H, H_lo, M, K, F, a, o, s);
-    return bf ? launch_gateup_bn<MODE_GATEUP_SPLIT, true, 1>(A, nullptr, Wg, Wu, G, U, M, K, F, a, o, s)
-              : launch_gateup_bn<MODE_GATEUP_SPLIT, false, 1>(A, nullptr, Wg, Wu, G, U, M, K, F, a, o, s);
+        return bf ? launch_gateup_bn<MODE_GATEUP_FUSED, true, 1>(A, nullptr, Wg, Wu, H, H_lo, M, K, F, a, o, ex, s)
+                  : launch_gateup_bn<MODE_GATEUP_FUSED, false, 1>(A, nullptr, Wg, Wu, H, H_lo, M, K, F, a, o, ex, s);
+    return bf ? launch_gateup_bn<MODE_GATEUP_SPLIT, true, 1>(A, nullptr, Wg, Wu, G, U, M, K, F, a, o, ex, s)
+              : launch_gateup_bn<MODE_GATEUP_SPLIT, false, 1>(A, nullptr, Wg, Wu, G, U, M, K, F, a, o, ex, s);
 }
 
 cudaError_t launch_gemm_plain(int dt, int dt_out, const void *A, const void *A_lo, const void *B,
                               void *C, int64_t M, int64_t K, int64_t N, float acc_scale,
-                              const void *res, float *part, cudaStream_t s) {
+                              const void *res, float *part, cudaStream_t s, float *ss_part,
+                              unsigned *ss_ctr, float *ss_out) {
     const float a = acc_scale;
+    GemmRowSS ex;
+    ex.part = ss_part;
+    ex.ctr = ss_ctr;
+    ex.out = ss_out;
     if (dt == DT_BF16) {
-        if (A_lo) return launch_plain_bn<true, 2, true>(A, A_lo, B, C, M, K, N, a, res, part, s);
-        return launch_plain_bn<true, 1, true>(A, nullptr, B, C, M, K, N, a, res, part, s);
+        if (A_lo) return launch_plain_bn<true, 2, true>(A, A_lo, B, C, M, K, N, a, res, part, ex, s);
+        return launch_plain_bn<true, 1, true>(A, nullptr, B, C, M, K, N, a, res, part, ex, s);
     }
     if (dt_out == DT_BF16) {   // fp16 operands, bf16 output (prepared-weights path)
-        if (A_lo) return launch_plain_bn<false, 2, true>(A, A_lo, B, C, M, K, N, a, res, part, s);
-        return launch_plain_bn<false, 1, true>(A, nullptr, B, C, M, K, N, a, res, part, s);
+        if (A_lo) return launch_plain_bn<false, 2, true>(A, A_lo, B, C, M, K, N, a, res, part, ex, s);
+        return launch_plain_bn<false, 1, true>(A, nullptr, B, C, M, K, N, a, res, part, ex, s);
     }
-    if (A_lo) return launch_plain_bn<false, 2, false>(A, A_lo, B, C, M, K, N, a, res, part, s);
-    return launch_plain_bn<false, 1, false>(A, nullptr, B, C, M, K, N, a, res, part, s);
+    if (A_lo) return launch_plain_bn<false, 2, false>(A, A_lo, B, C, M, K, N, a, res, part, ex, s);
+    return launch_plain_bn<false, 1, false>(A, nullptr, B, C, M, K, N, a, res, part, ex, s);
 }
 
 }  // namespace ffn

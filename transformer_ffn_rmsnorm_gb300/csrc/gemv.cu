@@ -102,7 +102,7 @@ template <int WF, bool TWO, int VPT>
 __global__ void __launch_bounds__(256) gemv_norm_frag_reg_kernel(const void *x_, const void *g_,
                                                                  uint16_t *nfrag, uint16_t *nlo, int rows,
                                                                  int64_t K, int64_t nch, float eps,
-                                                                 int release_early) {
+                                                                 int release_early, const float *ss_in) {
     using T = typename Fmt<WF>::TIn;
     __shared__ float partial[8];
     ptx::griddep_wait();
@@ -121,14 +121,19 @@ __global__ void __launch_bounds__(256) gemv_norm_frag_reg_kernel(const void *x_,
         gv[i] = in ? g[v] : make_uint4(0, 0, 0, 0);
     }
     float ss = 0.f;
+    if (ss_in) {   // the row's sum of squares, handed on by the block before
+        ss = live ? ss_in[token] : 0.f;
+    } else {
 #pragma unroll
-    for (int i = 0; i < VPT; ++i) {
-        float f[8];
-        Vec16<T>::unpack(xv[i], f);
+        for (int i = 0; i < VPT; ++i) {
+            float f[8];
+            Vec16<T>::unpack(xv[i], f);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
+            for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
+        }
+        ss = cta_sum256(ss, partial);
     }
-    const float inv = rsqrtf(cta_sum256(ss, partial) / static_cast<float>(K) + eps);
+    const float inv = rsqrtf(ss / static_cast<float>(K) + eps);
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
         const int64_t v = threadIdx.x + 256 * i;
@@ -148,7 +153,7 @@ template <int WF, bool TWO>
 __global__ void __launch_bounds__(256) gemv_norm_frag_kernel(const void *x_, const void *g_,
                                                              uint16_t *nfrag, uint16_t *nlo,
                                                              int rows, int64_t K, int64_t nch,
-                                                             float eps) {
+                                                             float eps, const float *ss_in) {
     using T = typename Fmt<WF>::TIn;
     __shared__ float partial[8];
     // launched as a programmatic dependent: nothing is read or written before
@@ -171,7 +176,9 @@ __global__ void __launch_bounds__(256) gemv_norm_frag_kernel(const void *x_, con
             for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
         }
     }
-    const float inv = rsqrtf(cta_sum256(ss, partial) / static_cast<float>(K) + eps);
+    ss = cta_sum256(ss, partial);
+    if (ss_in) ss = token < rows ? ss_in[token] : 0.f;
+    const float inv = rsqrtf(ss / static_cast<float>(K) + eps);
     for (int64_t v = v0 + threadIdx.x; v < v1; v += blockDim.x) {
         float f[8];
         if (token < rows && v < nv) {
@@ -398,12 +405,13 @@ __global__ void __launch_bounds__(128) gemv_down_kernel(
     const void *wd, const uint16_t *sd, const uint4 *__restrict__ hfrag,
     const uint4 *__restrict__ hfrag_lo, void *y_, float *partials,
     unsigned *counters, int rows, int64_t D, int64_t F, int64_t nchF, int64_t units_per_split,
-    const void *res) {
+    const void *res, float *ss_part, float *y_sumsq) {
     using T = typename Fmt<WF>::TIn;
     constexpr bool q4 = WF == WF_Q4;
     constexpr int U = q4 ? 2 : 8;
     constexpr float out_scale = Fmt<WF>::w_unscale / Fmt<WF>::h_scale;
-    __shared__ int s_last;
+    __shared__ int s_last, s_last_row;
+    __shared__ float sq[16 * kDnFeat];   // stored y squared (rows <= 16 on this path)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int gq = lane >> 2, tid = lane & 3;
     const int64_t f0 = (static_cast<int64_t>(blockIdx.x) * kDnTPC + warp) * 16;
@@ -454,9 +462,37 @@ __global__ void __launch_bounds__(128) gemv_down_kernel(
             sum += __ldcg(partials + (static_cast<int64_t>(sp) * rows + token) * D + feat);
         float v = sum * out_scale;
         if (res) v += to_f32(static_cast<const T *>(res)[static_cast<int64_t>(token) * D + feat]);
-        y[static_cast<int64_t>(token) * D + feat] = from_f32<T>(v);
+        const T yv = from_f32<T>(v);
+        y[static_cast<int64_t>(token) * D + feat] = yv;
+        const float r = to_f32(yv);
+        sq[i] = r * r;
     }
     if (threadIdx.x == 0) counters[blockIdx.x] = 0u;
+    if (!y_sumsq) return;
+    // the row's sum of squares of the stored y ("Megakernels on Mac: What
+    // Fusion Saves and What It Costs", "Dependencies and synchronization"):
+    // this group's part, then the last group adds the parts in group order
+    __syncthreads();
+    const int64_t nf = D - fbase < kDnFeat ? D - fbase : kDnFeat;
+    if (threadIdx.x < rows) {
+        float ss = 0.f;
+        for (int j = 0; j < nf; ++j) ss += sq[threadIdx.x * kDnFeat + j];
+        ss_part[static_cast<int64_t>(blockIdx.x) * rows + threadIdx.x] = ss;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        s_last_row = atomicAdd(&counters[gridDim.x], 1u) == gridDim.x - 1;
+    }
+    __syncthreads();
+    if (!s_last_row) return;
+    __threadfence();
+    if (threadIdx.x < rows) {
+        float ss = 0.f;
+        for (unsigned gi = 0; gi < gridDim.x; ++gi) ss += __ldcg(ss_part + static_cast<int64_t>(gi) * rows + threadIdx.x);
+        y_sumsq[threadIdx.x] = ss;
+    }
+    if (threadIdx.x == 0) counters[gridDim.x] = 0u;
 }
 
 // ---------------------------------------------------------------------------
@@ -486,7 +522,8 @@ size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 template <int WF, int NT, bool TWO>
 cudaError_t launch_typed(const void *x, const void *gain, GemvWeights wg, GemvWeights wu,
                          GemvWeights wd, void *y, int rows, int64_t d, int64_t ffn, float eps,
-                         const GemvWorkspace &ws, const Geometry &geo, cudaStream_t s, const void *res) {
+                         const GemvWorkspace &ws, const Geometry &geo, cudaStream_t s, const void *res,
+                         RowStats rs) {
     constexpr bool q4 = WF == WF_Q4;
     {
         LaunchScope scope(K_GEMV_NORM, s);
@@ -497,30 +534,31 @@ cudaError_t launch_typed(const void *x, const void *gain, GemvWeights wg, GemvWe
         cudaError_t e;
         if (vpt <= 1)
             e = launch_dependent(gemv_norm_frag_reg_kernel<WF, TWO, 1>, grid, dim3(256), 0, s, x, gain, nf, nl, rows,
-                                 d, geo.nchK, eps, early);
+                                 d, geo.nchK, eps, early, rs.ss_in);
         else if (vpt <= 2)
             e = launch_dependent(gemv_norm_frag_reg_kernel<WF, TWO, 2>, grid, dim3(256), 0, s, x, gain, nf, nl, rows,
-                                 d, geo.nchK, eps, early);
+                                 d, geo.nchK, eps, early, rs.ss_in);
         else if (vpt <= 4)
             e = launch_dependent(gemv_norm_frag_reg_kernel<WF, TWO, 4>, grid, dim3(256), 0, s, x, gain, nf, nl, rows,
-                                 d, geo.nchK, eps, early);
+                                 d, geo.nchK, eps, early, rs.ss_in);
         else if (vpt <= 8)
             e = launch_dependent(gemv_norm_frag_reg_kernel<WF, TWO, 8>, grid, dim3(256), 0, s, x, gain, nf, nl, rows,
-                                 d, geo.nchK, eps, early);
+                                 d, geo.nchK, eps, early, rs.ss_in);
         else
             e = launch_dependent(gemv_norm_frag_kernel<WF, TWO>,
                                  dim3(8 * NT, static_cast<unsigned>(std::min<int64_t>(16, cdiv(vpt, 4)))), dim3(256),
-                                 0, s, x, gain, nf, nl, rows, d, geo.nchK, eps);
+                                 0, s, x, gain, nf, nl, rows, d, geo.nchK, eps, rs.ss_in);
         if (e == cudaSuccess) e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     if (stream_supported(WF, d, ffn)) {
         cudaError_t e = launch_stream_gateup<WF, NT, TWO>(wg, wu, ws.nfrag, ws.nfrag_lo, ws.hfrag, ws.hfrag_lo, d,
                                                           ffn, geo.nchK, geo.nchF, ws.counters,
-                                                          static_cast<int>(geo.groups), s);
+                                                          static_cast<int>(geo.groups + 1), s);
         if (e != cudaSuccess) return e;
         return launch_stream_down<WF, NT, TWO>(wd, ws.hfrag, ws.hfrag_lo, y, ws.partials, ws.counters, rows, d,
-                                               ffn, geo.nchF, stream_down_splits(WF, d, ffn), res, s);
+                                               ffn, geo.nchF, stream_down_splits(WF, d, ffn), res, ws.ss_part,
+                                               rs.ss_out, s);
     }
     if constexpr (WF == WF_FP8 || WF == WF_Q8 || NT > 2) {
         // e4m3 and Q8_0 weights, and more than two token tiles, stream through
@@ -536,7 +574,7 @@ cudaError_t launch_typed(const void *x, const void *gain, GemvWeights wg, GemvWe
                 q4 ? static_cast<const void *>(wg.qs) : wg.w, q4 ? static_cast<const void *>(wu.qs) : wu.w,
                 wg.sc, wu.sc, static_cast<const uint4 *>(ws.nfrag), static_cast<const uint4 *>(ws.nfrag_lo),
                 static_cast<uint16_t *>(ws.hfrag), static_cast<uint16_t *>(ws.hfrag_lo), d, ffn, geo.nchK,
-                geo.nchF, units, ws.counters, static_cast<int>(geo.groups));
+                geo.nchF, units, ws.counters, static_cast<int>(geo.groups + 1));
             cudaError_t e = cudaGetLastError();
             if (e != cudaSuccess) return e;
         }
@@ -545,7 +583,7 @@ cudaError_t launch_typed(const void *x, const void *gain, GemvWeights wg, GemvWe
         gemv_down_kernel<WF, NT, TWO><<<grid, 32 * kDnTPC, 0, s>>>(
             q4 ? static_cast<const void *>(wd.qs) : wd.w, wd.sc, static_cast<const uint4 *>(ws.hfrag),
             static_cast<const uint4 *>(ws.hfrag_lo), y, ws.partials, ws.counters, rows, d, ffn, geo.nchF,
-            geo.ups, res);
+            geo.ups, res, ws.ss_part, rs.ss_out);
         return cudaGetLastError();
     }
 }
@@ -553,19 +591,20 @@ cudaError_t launch_typed(const void *x, const void *gain, GemvWeights wg, GemvWe
 template <int WF, bool TWO>
 cudaError_t launch_nt(int nt, const void *x, const void *g, GemvWeights wg, GemvWeights wu,
                       GemvWeights wd, void *y, int rows, int64_t d, int64_t ffn, float eps,
-                      const GemvWorkspace &ws, const Geometry &geo, cudaStream_t s, const void *res) {
-    if (nt == 1) return launch_typed<WF, 1, TWO>(x, g, wg, wu, wd, y, rows, d, ffn, eps, ws, geo, s, res);
-    if (nt == 2) return launch_typed<WF, 2, TWO>(x, g, wg, wu, wd, y, rows, d, ffn, eps, ws, geo, s, res);
+                      const GemvWorkspace &ws, const Geometry &geo, cudaStream_t s, const void *res,
+                      RowStats rs) {
+    if (nt == 1) return launch_typed<WF, 1, TWO>(x, g, wg, wu, wd, y, rows, d, ffn, eps, ws, geo, s, res, rs);
+    if (nt == 2) return launch_typed<WF, 2, TWO>(x, g, wg, wu, wd, y, rows, d, ffn, eps, ws, geo, s, res, rs);
     // 17 to 64 rows: 16-bit weights only (the quantised entries go in groups of 16)
     if constexpr (WF == WF_F16 || WF == WF_BF16 || WF == WF_F16P) {
-        if (nt == 4) return launch_typed<WF, 4, TWO>(x, g, wg, wu, wd, y, rows, d, ffn, eps, ws, geo, s, res);
-        return launch_typed<WF, 8, TWO>(x, g, wg, wu, wd, y, rows, d, ffn, eps, ws, geo, s, res);
+        if (nt == 4) return launch_typed<WF, 4, TWO>(x, g, wg, wu, wd, y, rows, d, ffn, eps, ws, geo, s, res, rs);
+        return launch_typed<WF, 8, TWO>(x, g, wg, wu, wd, y, rows, d, ffn, eps, ws, geo, s, res, rs);
     }
     return cudaErrorInvalidValue;
 }
 
 struct Layout {
-    size_t frag_n, frag_h, partials, counters;
+    size_t frag_n, frag_h, partials, counters, ss_part;
 };
 
 Layout layout(int64_t rows, int64_t d, int64_t ffn) {
@@ -580,7 +619,8 @@ Layout layout(int64_t rows, int64_t d, int64_t ffn) {
     l.frag_n = align256(static_cast<size_t>(a.nt) * a.nchK * 32 * 16);
     l.frag_h = align256(static_cast<size_t>(a.nt) * a.nchF * 32 * 16);
     l.partials = align256(static_cast<size_t>(splits) * (rows > 64 ? 64 : rows) * d * 4);
-    l.counters = align256(static_cast<size_t>(a.groups) * 4);
+    l.counters = align256(static_cast<size_t>(a.groups + 1) * 4);   // arrivals per group, then for the row sums
+    l.ss_part = align256(static_cast<size_t>(a.groups) * (rows > 64 ? 64 : rows) * 4);
     return l;
 }
 
@@ -589,7 +629,7 @@ Layout layout(int64_t rows, int64_t d, int64_t ffn) {
 size_t gemv_workspace_bytes(int64_t rows, int64_t d, int64_t ffn, bool two_terms) {
     const Layout l = layout(rows, d, ffn);
     const size_t frags = l.frag_n + l.frag_h;
-    return (two_terms ? 2 * frags : frags) + l.partials + l.counters;
+    return (two_terms ? 2 * frags : frags) + l.partials + l.counters + l.ss_part;
 }
 
 void gemv_carve(void *base, int64_t rows, int64_t d, int64_t ffn, bool two_terms, GemvWorkspace *ws) {
@@ -610,31 +650,33 @@ void gemv_carve(void *base, int64_t rows, int64_t d, int64_t ffn, bool two_terms
     ws->partials = reinterpret_cast<float *>(p);
     p += l.partials;
     ws->counters = reinterpret_cast<unsigned *>(p);
+    p += l.counters;
+    ws->ss_part = reinterpret_cast<float *>(p);
 }
 
 cudaError_t launch_gemv_block(int wfmt, const void *x, const void *g, GemvWeights wg,
                               GemvWeights wu, GemvWeights wd, void *y, int64_t rows, int64_t d,
                               int64_t ffn, float eps, const GemvWorkspace &ws, cudaStream_t s,
-                              const void *res) {
+                              const void *res, RowStats rs) {
     if (rows <= 0) return cudaSuccess;
     const Geometry geo = geometry(rows, d, ffn, wfmt == WF_Q4);
     const int r = static_cast<int>(rows);
     const bool two = ws.nfrag_lo != nullptr;
     switch (wfmt) {
         case WF_F16:
-            return two ? launch_nt<WF_F16, true>(geo.nt, x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s, res)
-                       : launch_nt<WF_F16, false>(geo.nt, x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s, res);
+            return two ? launch_nt<WF_F16, true>(geo.nt, x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s, res, rs)
+                       : launch_nt<WF_F16, false>(geo.nt, x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s, res, rs);
         case WF_BF16:
-            return two ? launch_nt<WF_BF16, true>(geo.nt, x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s, res)
-                       : launch_nt<WF_BF16, false>(geo.nt, x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s, res);
+            return two ? launch_nt<WF_BF16, true>(geo.nt, x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s, res, rs)
+                       : launch_nt<WF_BF16, false>(geo.nt, x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s, res, rs);
         case WF_Q4:   // fp16 operands: one term is enough
-            return launch_nt<WF_Q4, false>(geo.nt, x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s, res);
+            return launch_nt<WF_Q4, false>(geo.nt, x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s, res, rs);
         case WF_FP8:  // fp16 operands, as for Q4
-            return launch_nt<WF_FP8, false>(geo.nt, x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s, res);
+            return launch_nt<WF_FP8, false>(geo.nt, x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s, res, rs);
         case WF_Q8:
-            return launch_nt<WF_Q8, false>(geo.nt, x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s, res);
+            return launch_nt<WF_Q8, false>(geo.nt, x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s, res, rs);
         default:      // prepared fp16 weights
-            return launch_nt<WF_F16P, false>(geo.nt, x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s, res);
+            return launch_nt<WF_F16P, false>(geo.nt, x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s, res, rs);
     }
 }
 

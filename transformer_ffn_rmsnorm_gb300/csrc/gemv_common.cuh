@@ -167,9 +167,12 @@ cudaError_t launch_stream_gateup(GemvWeights wg, GemvWeights wu, const void *nfr
                                  void *hfrag, void *hfrag_lo, int64_t d, int64_t ffn, int64_t nchK,
                                  int64_t nchF, unsigned *counters, int ncounters, cudaStream_t s);
 template <int WF, int NT, bool TWO>
+// ss_part, y_sumsq (y_sumsq may be null): the rows' sums of squares of the
+// stored y, through [ceil(d/64)][rows] partial sums and counters[ceil(d/64)]
 cudaError_t launch_stream_down(GemvWeights wd, const void *hfrag, const void *hfrag_lo, void *y,
                                float *partials, unsigned *counters, int rows, int64_t d, int64_t ffn,
-                               int64_t nchF, int64_t splits, const void *res, cudaStream_t s);
+                               int64_t nchF, int64_t splits, const void *res, float *ss_part, float *y_sumsq,
+                               cudaStream_t s);
 
 }  // namespace gemv
 }  // namespace ffn

@@ -95,6 +95,8 @@ struct StreamParams {
     const void *res;        // down: added to y before its rounding ([rows x D] of y's type), or null
     const float *rs0, *rs1; // e4m3: row scales of the weight matrices (gate and up, or down)
     int pre_stages;         // weight stages requested before the wait (at most the ring)
+    float *ss_part;         // down, with y_sumsq: [feature groups][rows] sums of squares of stored y
+    float *y_sumsq;         // down: [rows] sum over the row of the stored y squared, or null
 };
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
@@ -127,7 +129,7 @@ __global__ void __launch_bounds__(kThreads) gemv_stream_kernel(
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bar_full[kStages], bar_empty[kStages];
     __shared__ float red[2][32][NT * 4];
-    __shared__ int s_abort, s_never, s_last;
+    __shared__ int s_abort, s_never, s_last, s_last_row;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t base = (ptx::smem_u32(smem_raw) + 1023u) & ~1023u;
@@ -503,10 +505,46 @@ __global__ void __launch_bounds__(kThreads) gemv_stream_kernel(
                         const int64_t feat = row0 + i % 64;
                         float v = fp8 ? (sum[o] * p.rs0[feat]) * out_scale : sum[o] * out_scale;
                         if (p.res) v += to_f32(static_cast<const T *>(p.res)[static_cast<int64_t>(token) * p.D + feat]);
-                        y[static_cast<int64_t>(token) * p.D + feat] = from_f32<T>(v);
+                        const T yv = from_f32<T>(v);
+                        y[static_cast<int64_t>(token) * p.D + feat] = yv;
+                        if (p.y_sumsq) {   // the stored value squared, for the row's sum (ring memory is free now)
+                            const float r = to_f32(yv);
+                            reinterpret_cast<float *>(smem_raw + (base - ptx::smem_u32(smem_raw)))[i] = r * r;
+                        }
                     }
                 }
                 if (threadIdx.x == 0) p.counters[blockIdx.x] = 0u;
+                if (p.y_sumsq) {
+                    // "Megakernels on Mac: What Fusion Saves and What It Costs",
+                    // "Dependencies and synchronization": the next RMSNorm needs
+                    // the sum of squares of every element of the row, so each
+                    // feature group's closing CTA leaves its part of it, and the
+                    // last group to finish adds the parts in group order
+                    const float *sq = reinterpret_cast<const float *>(smem_raw + (base - ptx::smem_u32(smem_raw)));
+                    consumer_sync();
+                    const int64_t nf = p.D - row0 < 64 ? p.D - row0 : 64;
+                    if (threadIdx.x < p.rows) {
+                        float ss = 0.f;
+                        for (int j = 0; j < nf; ++j) ss += sq[threadIdx.x * 64 + j];
+                        p.ss_part[static_cast<int64_t>(blockIdx.x) * p.rows + threadIdx.x] = ss;
+                    }
+                    consumer_sync();
+                    if (threadIdx.x == 0) {
+                        __threadfence();
+                        s_last_row = atomicAdd(&p.counters[gridDim.x], 1u) == gridDim.x - 1;
+                    }
+                    consumer_sync();
+                    if (s_last_row) {
+                        __threadfence();
+                        if (threadIdx.x < p.rows) {
+                            float ss = 0.f;
+                            for (unsigned gi = 0; gi < gridDim.x; ++gi)
+                                ss += __ldcg(p.ss_part + static_cast<int64_t>(gi) * p.rows + threadIdx.x);
+                            p.y_sumsq[threadIdx.x] = ss;
+                        }
+                        if (threadIdx.x == 0) p.counters[gridDim.x] = 0u;
+                    }
+                }
             }
         }
     }
@@ -643,7 +681,8 @@ cudaError_t launch_stream_gateup(GemvWeights wg, GemvWeights wu, const void *nfr
 template <int WF, int NT, bool TWO>
 cudaError_t launch_stream_down(GemvWeights wd, const void *hfrag, const void *hfrag_lo, void *y,
                                float *partials, unsigned *counters, int rows, int64_t d, int64_t ffn,
-                               int64_t nchF, int64_t splits, const void *res, cudaStream_t s) {
+                               int64_t nchF, int64_t splits, const void *res, float *ss_part, float *y_sumsq,
+                               cudaStream_t s) {
     using TL = Tile<WF, ROLE_DOWN, NT, TWO>;
     constexpr auto kern = gemv_stream_kernel<WF, NT, TWO, ROLE_DOWN>;
     cudaError_t e = set_smem<kern>(TL::smem_bytes);
@@ -668,6 +707,8 @@ cudaError_t launch_stream_down(GemvWeights wd, const void *hfrag, const void *hf
     p.rs0 = wd.rs;
     p.rs1 = nullptr;
     p.pre_stages = decode_tuning(TUNE_PRE_STAGES_DOWN);
+    p.ss_part = ss_part;
+    p.y_sumsq = y_sumsq;
     p.err = device_status_word();
     if (!p.err) return cudaErrorUnknown;
     const int64_t nsplit = cdiv(p.nkb, p.kb_per_split);
@@ -709,7 +750,8 @@ int64_t stream_down_splits(int wfmt, int64_t d, int64_t ffn) {
                                                            cudaStream_t);                                \
     template cudaError_t launch_stream_down<WF, NT, TWO>(GemvWeights, const void *, const void *, void *, \
                                                          float *, unsigned *, int, int64_t, int64_t,     \
-                                                         int64_t, int64_t, const void *, cudaStream_t);
+                                                         int64_t, int64_t, const void *, float *, float *, \
+                                                         cudaStream_t);
 FFN_STREAM_INSTANTIATE(WF_F16, 1, false)
 FFN_STREAM_INSTANTIATE(WF_F16, 2, false)
 FFN_STREAM_INSTANTIATE(WF_F16, 1, true)

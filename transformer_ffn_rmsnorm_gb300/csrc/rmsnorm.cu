@@ -38,7 +38,7 @@ template <typename T, typename TO, int VPT, int WPR, bool SPLIT>
 __global__ void __launch_bounds__(256) rmsnorm_reg_kernel(const T *x,
                                                           const T *__restrict__ g,
                                                           TO *n, TO *nlo, int64_t rows,
-                                                          int d, float eps) {
+                                                          int d, float eps, const float *ss_in) {
     static_assert(sizeof(T) == sizeof(TO), "input and output element sizes must match");
     constexpr int EPV = 16 / sizeof(T);
     __shared__ float partial[256 / 32];
@@ -80,6 +80,7 @@ __global__ void __launch_bounds__(256) rmsnorm_reg_kernel(const T *x,
         for (int w = 0; w < WPR; ++w) ss += partial[row_in_cta * WPR + w];
     }
     if (!valid) return;
+    if (ss_in) ss = ss_in[row];   // the row's sum of squares, handed on by the block before
     const float inv = rsqrtf(ss / static_cast<float>(d) + eps);
     const uint4 *gv = reinterpret_cast<const uint4 *>(g);
     TO *nr = n + row * d;
@@ -104,7 +105,7 @@ template <typename T, typename TO, bool SPLIT>
 __global__ void __launch_bounds__(256) rmsnorm_generic_kernel(const T *x,
                                                               const T *__restrict__ g,
                                                               TO *n, TO *nlo, int64_t rows,
-                                                              int64_t d, float eps) {
+                                                              int64_t d, float eps, const float *ss_in) {
     __shared__ float partial[8];
     // launched as a programmatic dependent: nothing is read before the
     // previous kernel has finished; only then may the projection after this
@@ -125,6 +126,7 @@ __global__ void __launch_bounds__(256) rmsnorm_generic_kernel(const T *x,
     __syncthreads();
     ss = 0.f;
     for (int w = 0; w < (int)(blockDim.x >> 5); ++w) ss += partial[w];
+    if (ss_in) ss = ss_in[row];
     const float inv = rsqrtf(ss / static_cast<float>(d) + eps);
     TO *nr = n + row * d;
     for (int64_t c = threadIdx.x; c < d; c += blockDim.x) {
@@ -159,7 +161,7 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
 template <typename T, typename TO, bool SPLIT>
 __global__ void __launch_bounds__(kNormThreads) rmsnorm_stream_kernel(
     const T *x, const T *__restrict__ g, TO *n, TO *nlo, int64_t rows, int d, float eps,
-    uint32_t row_bytes, unsigned *err) {
+    uint32_t row_bytes, unsigned *err, const float *ss_in) {
     constexpr int EPV = 16 / sizeof(T);
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bar_full[kNormWarps], bar_empty[kNormWarps], bar_g;
@@ -226,14 +228,18 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_stream_kernel(
                 break;
             }
             float ss = 0.f;
-            for (int v = lane; v < nvec; v += 32) {
-                float f[EPV];
-                Vec16<T>::unpack(lds128(slot + v * 16), f);
+            if (ss_in) {
+                ss = ss_in[r];   // the row's sum of squares, handed on by the block before
+            } else {
+                for (int v = lane; v < nvec; v += 32) {
+                    float f[EPV];
+                    Vec16<T>::unpack(lds128(slot + v * 16), f);
 #pragma unroll
-                for (int e = 0; e < EPV; ++e) ss = fmaf(f[e], f[e], ss);
+                    for (int e = 0; e < EPV; ++e) ss = fmaf(f[e], f[e], ss);
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
             }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
             const float inv = rsqrtf(ss / static_cast<float>(d) + eps);
             TO *nr = n + r * d;
             TO *lr = SPLIT ? nlo + r * d : nullptr;
@@ -277,7 +283,7 @@ constexpr uint32_t kNormMaxRowBytes = 16 * 1024;
 
 template <typename T, typename TO, bool SPLIT>
 cudaError_t launch_stream(const void *x, const void *g, void *n, void *nlo, int64_t rows, int d, float eps,
-                          cudaStream_t s) {
+                          const float *ss_in, cudaStream_t s) {
     const uint32_t row_bytes = static_cast<uint32_t>(d) * sizeof(T);
     const uint32_t stride = (row_bytes + 127u) & ~127u;
     const size_t smem = static_cast<size_t>(stride) * (kNormWarps + 1) + 128;
@@ -305,13 +311,13 @@ cudaError_t launch_stream(const void *x, const void *g, void *n, void *nlo, int6
     LaunchScope scope(K_RMSNORM, s);
     e = launch_dependent(rmsnorm_stream_kernel<T, TO, SPLIT>, dim3(static_cast<unsigned>(grid)), dim3(kNormThreads),
                          smem, s, static_cast<const T *>(x), static_cast<const T *>(g), static_cast<TO *>(n),
-                         static_cast<TO *>(nlo), rows, d, eps, row_bytes, err);
+                         static_cast<TO *>(nlo), rows, d, eps, row_bytes, err, ss_in);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <typename T, typename TO, int VPT, int WPR, bool SPLIT>
 cudaError_t launch_reg(const void *x, const void *g, void *n, void *nlo, int64_t rows, int d,
-                       float eps, cudaStream_t s) {
+                       float eps, const float *ss_in, cudaStream_t s) {
     const int threads = 256;
     const int rows_per_cta = (threads / 32) / WPR;
     const int64_t blocks = (rows + rows_per_cta - 1) / rows_per_cta;
@@ -319,30 +325,30 @@ cudaError_t launch_reg(const void *x, const void *g, void *n, void *nlo, int64_t
     const cudaError_t e = launch_dependent(rmsnorm_reg_kernel<T, TO, VPT, WPR, SPLIT>,
                                            dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, s,
                                            static_cast<const T *>(x), static_cast<const T *>(g),
-                                           static_cast<TO *>(n), static_cast<TO *>(nlo), rows, d, eps);
+                                           static_cast<TO *>(n), static_cast<TO *>(nlo), rows, d, eps, ss_in);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <typename T, typename TO, int WPR, bool SPLIT>
 cudaError_t dispatch_vpt(int vpt, const void *x, const void *g, void *n, void *nlo, int64_t rows,
-                         int d, float eps, cudaStream_t s) {
+                         int d, float eps, const float *ss_in, cudaStream_t s) {
     switch (vpt) {
-        case 1: return launch_reg<T, TO, 1, WPR, SPLIT>(x, g, n, nlo, rows, d, eps, s);
-        case 2: return launch_reg<T, TO, 2, WPR, SPLIT>(x, g, n, nlo, rows, d, eps, s);
-        case 4: return launch_reg<T, TO, 4, WPR, SPLIT>(x, g, n, nlo, rows, d, eps, s);
-        default: return launch_reg<T, TO, 8, WPR, SPLIT>(x, g, n, nlo, rows, d, eps, s);
+        case 1: return launch_reg<T, TO, 1, WPR, SPLIT>(x, g, n, nlo, rows, d, eps, ss_in, s);
+        case 2: return launch_reg<T, TO, 2, WPR, SPLIT>(x, g, n, nlo, rows, d, eps, ss_in, s);
+        case 4: return launch_reg<T, TO, 4, WPR, SPLIT>(x, g, n, nlo, rows, d, eps, ss_in, s);
+        default: return launch_reg<T, TO, 8, WPR, SPLIT>(x, g, n, nlo, rows, d, eps, ss_in, s);
     }
 }
 
 template <typename T, typename TO, bool SPLIT>
 cudaError_t launch_typed(const void *x, const void *g, void *n, void *nlo, int64_t rows,
-                         int64_t d, float eps, cudaStream_t s) {
+                         int64_t d, float eps, const float *ss_in, cudaStream_t s) {
     constexpr int EPV = 16 / sizeof(T);
     const bool aligned = (d % EPV) == 0;
     const int64_t nvec = d / EPV;
     // many rows: stream whole rows through shared memory
     if (aligned && rows >= 4 * static_cast<int64_t>(sm_count()) && d * sizeof(T) <= kNormMaxRowBytes)
-        return launch_stream<T, TO, SPLIT>(x, g, n, nlo, rows, static_cast<int>(d), eps, s);
+        return launch_stream<T, TO, SPLIT>(x, g, n, nlo, rows, static_cast<int>(d), eps, ss_in, s);
     // registers hold the row when nvec <= 32 lanes * 8 warps * kMaxVPT
     if (aligned && nvec <= 32 * 8 * kMaxVPT) {
         int wpr = 1;
@@ -352,49 +358,49 @@ cudaError_t launch_typed(const void *x, const void *g, void *n, void *nlo, int64
         while (vpt < per_thread) vpt <<= 1;
         const int di = static_cast<int>(d);
         switch (wpr) {
-            case 1: return dispatch_vpt<T, TO, 1, SPLIT>(vpt, x, g, n, nlo, rows, di, eps, s);
-            case 2: return dispatch_vpt<T, TO, 2, SPLIT>(vpt, x, g, n, nlo, rows, di, eps, s);
-            case 4: return dispatch_vpt<T, TO, 4, SPLIT>(vpt, x, g, n, nlo, rows, di, eps, s);
-            default: return dispatch_vpt<T, TO, 8, SPLIT>(vpt, x, g, n, nlo, rows, di, eps, s);
+            case 1: return dispatch_vpt<T, TO, 1, SPLIT>(vpt, x, g, n, nlo, rows, di, eps, ss_in, s);
+            case 2: return dispatch_vpt<T, TO, 2, SPLIT>(vpt, x, g, n, nlo, rows, di, eps, ss_in, s);
+            case 4: return dispatch_vpt<T, TO, 4, SPLIT>(vpt, x, g, n, nlo, rows, di, eps, ss_in, s);
+            default: return dispatch_vpt<T, TO, 8, SPLIT>(vpt, x, g, n, nlo, rows, di, eps, ss_in, s);
         }
     }
     LaunchScope scope(K_RMSNORM, s);
     const cudaError_t e = launch_dependent(rmsnorm_generic_kernel<T, TO, SPLIT>, dim3(static_cast<unsigned>(rows)),
                                            dim3(256), 0, s, static_cast<const T *>(x), static_cast<const T *>(g),
-                                           static_cast<TO *>(n), static_cast<TO *>(nlo), rows, d, eps);
+                                           static_cast<TO *>(n), static_cast<TO *>(nlo), rows, d, eps, ss_in);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_rmsnorm(const void *x, const void *g, void *n, int64_t rows, int64_t d,
-                           float eps, int dt, cudaStream_t s) {
+                           float eps, int dt, cudaStream_t s, const float *ss_in) {
     if (rows <= 0) return cudaSuccess;
     switch (dt) {
-        case DT_F32: return launch_typed<float, float, false>(x, g, n, nullptr, rows, d, eps, s);
-        case DT_F16: return launch_typed<__half, __half, false>(x, g, n, nullptr, rows, d, eps, s);
+        case DT_F32: return launch_typed<float, float, false>(x, g, n, nullptr, rows, d, eps, ss_in, s);
+        case DT_F16: return launch_typed<__half, __half, false>(x, g, n, nullptr, rows, d, eps, ss_in, s);
         default:
-            return launch_typed<__nv_bfloat16, __nv_bfloat16, false>(x, g, n, nullptr, rows, d, eps, s);
+            return launch_typed<__nv_bfloat16, __nv_bfloat16, false>(x, g, n, nullptr, rows, d, eps, ss_in, s);
     }
 }
 
 cudaError_t launch_rmsnorm_split(const void *x, const void *g, void *n_hi, void *n_lo,
-                                 int64_t rows, int64_t d, float eps, int dt, cudaStream_t s) {
+                                 int64_t rows, int64_t d, float eps, int dt, cudaStream_t s, const float *ss_in) {
     if (rows <= 0) return cudaSuccess;
     switch (dt) {
-        case DT_F16: return launch_typed<__half, __half, true>(x, g, n_hi, n_lo, rows, d, eps, s);
+        case DT_F16: return launch_typed<__half, __half, true>(x, g, n_hi, n_lo, rows, d, eps, ss_in, s);
         case DT_BF16:
-            return launch_typed<__nv_bfloat16, __nv_bfloat16, true>(x, g, n_hi, n_lo, rows, d, eps, s);
+            return launch_typed<__nv_bfloat16, __nv_bfloat16, true>(x, g, n_hi, n_lo, rows, d, eps, ss_in, s);
         default: return cudaErrorInvalidValue;
     }
 }
 
 cudaError_t launch_rmsnorm_to_f16(const void *x, const void *g, void *n, int64_t rows, int64_t d,
-                                  float eps, int dt_in, cudaStream_t s) {
+                                  float eps, int dt_in, cudaStream_t s, const float *ss_in) {
     if (rows <= 0) return cudaSuccess;
     switch (dt_in) {
-        case DT_F16: return launch_typed<__half, __half, false>(x, g, n, nullptr, rows, d, eps, s);
-        case DT_BF16: return launch_typed<__nv_bfloat16, __half, false>(x, g, n, nullptr, rows, d, eps, s);
+        case DT_F16: return launch_typed<__half, __half, false>(x, g, n, nullptr, rows, d, eps, ss_in, s);
+        case DT_BF16: return launch_typed<__nv_bfloat16, __half, false>(x, g, n, nullptr, rows, d, eps, ss_in, s);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -209,6 +209,29 @@ using WideDown = Simt<64, 64, 4, 4, 1, 32, false>;
 using SmallGateUp = Simt<16, 32, 2, 2, 2, 128, true>;
 using SmallDown = Simt<16, 32, 2, 2, 4, 256, false>;
 
+// ss[r] = sum over the row of y[r,c]^2: one CTA a row, a fixed reduction
+// tree (the same bits every run).  The fp32 path's rows' sums of squares for
+// the next block's RMSNorm: a pass over y after the down projection (on this
+// path, whose outputs carry no rounding, the tile epilogues would have to
+// combine across CTAs for the same sums).
+__global__ void __launch_bounds__(256) row_sumsq_kernel(const float *y, int64_t d, float *ss) {
+    ptx::griddep_wait();
+    ptx::griddep_launch_dependents();
+    __shared__ float red[8];
+    const float *yr = y + static_cast<int64_t>(blockIdx.x) * d;
+    float acc = 0.f;
+    for (int64_t c = threadIdx.x; c < d; c += 256) acc = fmaf(yr[c], yr[c], acc);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = acc;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float t = 0.f;
+        for (int w = 0; w < 8; ++w) t += red[w];
+        ss[blockIdx.x] = t;
+    }
+}
+
 // The wide tiles once their grid covers every SM; the small ones before.
 bool wide_tiles(int64_t M, int64_t N) { return ((M + 63) / 64) * ((N + 63) / 64) >= sm_count(); }
 
@@ -216,8 +239,9 @@ bool wide_tiles(int64_t M, int64_t N) { return ((M + 63) / 64) * ((N + 63) / 64)
 
 cudaError_t launch_simt_block(const float *x, const float *g, const float *wg, const float *wu,
                               const float *wd, float *y, int64_t rows, int64_t d, int64_t ffn,
-                              float eps, float *n, float *h, cudaStream_t s, const float *res) {
-    cudaError_t e = launch_rmsnorm(x, g, n, rows, d, eps, DT_F32, s);
+                              float eps, float *n, float *h, cudaStream_t s, const float *res,
+                              const float *ss_in, float *ss_out) {
+    cudaError_t e = launch_rmsnorm(x, g, n, rows, d, eps, DT_F32, s, ss_in);
     if (e != cudaSuccess) return e;
     {
         LaunchScope scope(K_SIMT_GATEUP, s);
@@ -225,9 +249,16 @@ cudaError_t launch_simt_block(const float *x, const float *g, const float *wg, c
                                   : launch_simt<SmallGateUp, true>(n, wg, wu, h, rows, ffn, d, nullptr, s);
         if (e != cudaSuccess) return e;
     }
+    {
+        LaunchScope scope(K_SIMT_DOWN, s);
+        e = wide_tiles(rows, d) ? launch_simt<WideDown, false>(h, wd, nullptr, y, rows, d, ffn, res, s)
+                                : launch_simt<SmallDown, false>(h, wd, nullptr, y, rows, d, ffn, res, s);
+        if (e != cudaSuccess || !ss_out) return e;
+    }
     LaunchScope scope(K_SIMT_DOWN, s);
-    return wide_tiles(rows, d) ? launch_simt<WideDown, false>(h, wd, nullptr, y, rows, d, ffn, res, s)
-                               : launch_simt<SmallDown, false>(h, wd, nullptr, y, rows, d, ffn, res, s);
+    e = launch_dependent(row_sumsq_kernel, dim3(static_cast<unsigned>(rows)), dim3(256), 0, s,
+                         static_cast<const float *>(y), d, ss_out);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace ffn

@@ -106,6 +106,29 @@ def ffn_block_forward(x, g, w_gate, w_up, w_down, eps: float, flags: int = 0, ou
     return y
 
 
+def ffn_block_forward_chained(x, g, w_gate, w_up, w_down, eps: float, flags: int = 0, x_sumsq=None,
+                              y_sumsq: bool = True, out=None, ss_out=None, ws: torch.Tensor | None = None,
+                              stream=None):
+    """ffn_block_forward that takes each row's sum of squares of x (x_sumsq,
+    fp32 [rows], or None) and returns (y, y_sumsq): the rows' sums of squares
+    of the stored y (None unless y_sumsq)."""
+    _need_cuda(x, g, w_gate, w_up, w_down, out, ws, x_sumsq, ss_out)
+    d = x.shape[-1]
+    rows = x.numel() // d
+    ffn = w_gate.shape[0]
+    y = torch.empty_like(x) if out is None else out
+    ss = None
+    if y_sumsq:
+        ss = torch.empty(rows, dtype=torch.float32, device=x.device) if ss_out is None else ss_out
+    if ws is None:
+        ws = workspace(ffn_block_workspace_bytes(rows, d, ffn, x.dtype, flags), x.device)
+    _check(_lib.load().ffn_block_forward_chained(_ptr(x), _ptr(x_sumsq), _ptr(g), _ptr(w_gate), _ptr(w_up),
+                                                 _ptr(w_down), _ptr(y), _ptr(ss), rows, d, ffn, float(eps),
+                                                 _dtype(x), flags, _ptr(ws), ws.numel(), _stream(stream)),
+           "ffn_block_forward_chained")
+    return y, ss
+
+
 def ffn_block_host_workspace_bytes(rows: int, d: int, ffn: int, dtype, flags: int = 0) -> int:
     out = ctypes.c_size_t(0)
     _check(_lib.load().ffn_block_host_workspace_bytes(rows, d, ffn, _DT[dtype], flags, ctypes.byref(out)),
