@@ -186,16 +186,14 @@ LaunchScope::~LaunchScope() {
     g_pending.push_back({kind, static_cast<cudaEvent_t>(ev0), e1});
 }
 
+// Looked up on every call, not cached: after a cudaDeviceReset (or a context
+// rebuilt in the same process) the module loads again and the word may sit
+// elsewhere; once the module is loaded the lookup is a host-side query that
+// allocates nothing, and it needs no lock between host threads.
 unsigned *device_status_word() {
-    static unsigned *addr[kMaxDevices] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-    if (!addr[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_ffn_status_word) != cudaSuccess) return nullptr;
-        addr[dev] = static_cast<unsigned *>(p);
-    }
-    return addr[dev];
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_ffn_status_word) != cudaSuccess) return nullptr;
+    return static_cast<unsigned *>(p);
 }
 
 int sm_count() {
