@@ -253,6 +253,8 @@ def brief(entry):
     if p:
         parts.append(f"max {p['max_abs_over_rms']:.1e} mean {p['mean_abs_over_rms']:.1e} rms "
                      f"({'ok' if p['ok'] else 'FAIL'})")
+    if entry.get("one_kernel"):
+        parts.append(f"one-kernel form {entry['one_kernel']['us_per_call']:.1f} us")
     return ", ".join(parts)
 
 
@@ -351,14 +353,13 @@ def sub_benchmarks(torch, ffn, device, peaks, peak_src, stream, with_oracle=True
     return out
 
 
-def decode_setup(torch, ffn, device, prepared=False, cfg=None, inp=None):
+def decode_setup(torch, ffn, device, prepared=False, cfg=None, inp=None, flags=0):
     cfg = cfg or synth.C3_DECODE_BF16
     inp = inp or synth.make_block_inputs(cfg, seed=0)
     args = [to_dev(inp[k], "bf16", torch, device) for k in ("x", "g", "w_gate", "w_up", "w_down")]
-    flags = 0
     if prepared:
         args[2:] = [ffn.ffn_prepare_weights(w) for w in args[2:]]
-        flags = ffn.FFN_PREPARED_WEIGHTS
+        flags |= ffn.FFN_PREPARED_WEIGHTS
     y = torch.empty_like(args[0])
     ws = ffn.workspace(ffn.ffn_block_workspace_bytes(cfg.rows, cfg.d, cfg.ffn, torch.bfloat16, flags), device)
     call = lambda i: ffn.ffn_block_forward(*args, eps=cfg.eps, flags=flags, out=y, ws=ws)
@@ -377,6 +378,10 @@ def decode_bench(torch, ffn, device, hbm, peak_src, stream, cfg=None, with_oracl
             timed_loop(torch, call, 50, 3, stream)
             res = kt.read()
         res_all["prepared" if prepared else "bf16_hi_lo"] = (us, res, host64(call.y))
+    if cfg.rows <= 16:
+        # the same block as one persistent kernel (FFN_DECODE_ONE_KERNEL), for comparison
+        _, call = decode_setup(torch, ffn, device, False, cfg, inp, ffn.FFN_DECODE_ONE_KERNEL)
+        res_all["one_kernel"] = graph_time_us(torch, call, 20, 10, stream)
     wbytes = 3 * cfg.ffn * cfg.d * 2
     us, res, got = res_all["bf16_hi_lo"]
     usp, resp, gotp = res_all["prepared"]
@@ -387,6 +392,10 @@ def decode_bench(torch, ffn, device, hbm, peak_src, stream, cfg=None, with_oracl
                               "kernels_events": kernel_table(resp),
                               "roofline": hbm_roof(wbytes, usp, hbm, peak_src)},
          "roofline": hbm_roof(wbytes, us, hbm, peak_src, f"whole block ({len(res)} launches)")}
+    if "one_kernel" in res_all:
+        uo = res_all["one_kernel"]
+        e["one_kernel"] = {"us_per_call": round(uo, 3), "tokens_per_s": round(cfg.rows / uo * 1e6, 1),
+                           "roofline": hbm_roof(wbytes, uo, hbm, peak_src, "whole block (1 launch)")}
     if with_oracle:
         import oracle
         o = oracle.get()
@@ -441,7 +450,7 @@ def chain_bench(torch, ffn, device, hbm, peak_src, stream):
             "roofline": hbm_roof(wbytes, us_chain, hbm, peak_src, "two blocks")}
 
 
-def q4_setup(torch, ffn, device, inp=None):
+def q4_setup(torch, ffn, device, inp=None, flags=0):
     cfg = synth.C5_DECODE_Q4
     inp = inp or synth.make_q4_inputs(cfg, seed=0)
     xq = to_dev(inp["x"], "bf16", torch, device)
@@ -452,7 +461,8 @@ def q4_setup(torch, ffn, device, inp=None):
                        torch.from_numpy(inp["sc_" + n].view(np.int16)).to(device)) for n in ("gate", "up", "down")])
     yq = torch.empty_like(xq)
     ws = ffn.workspace(ffn.ffn_block_q4_workspace_bytes(cfg.rows, cfg.d, cfg.ffn), device)
-    call = lambda i: ffn.ffn_block_forward_q4(xq, gq, *wsets[i % 2], ffn=cfg.ffn, eps=cfg.eps, out=yq, ws=ws)
+    call = lambda i: ffn.ffn_block_forward_q4(xq, gq, *wsets[i % 2], ffn=cfg.ffn, eps=cfg.eps, flags=flags,
+                                              out=yq, ws=ws)
     call.y = yq
     return cfg, call
 
@@ -481,7 +491,13 @@ def q4_bench(torch, ffn, device, hbm, peak_src, stream, with_oracle=False):
     if with_oracle:
         import oracle
         fn = lambda: oracle.get().q4_block_from_inputs(inp)
-    return quant_bench(torch, ffn, stream, cfg, call, wbytes, hbm, peak_src, fn)
+    e = quant_bench(torch, ffn, stream, cfg, call, wbytes, hbm, peak_src, fn)
+    # the same block as one persistent kernel (FFN_DECODE_ONE_KERNEL), for comparison
+    _, call1 = q4_setup(torch, ffn, device, inp, ffn.FFN_DECODE_ONE_KERNEL)
+    uo = graph_time_us(torch, call1, 20, 10, stream)
+    e["one_kernel"] = {"us_per_call": round(uo, 3), "tokens_per_s": round(cfg.rows / uo * 1e6, 1),
+                       "roofline": hbm_roof(wbytes, uo, hbm, peak_src, "whole block (1 launch)")}
+    return e
 
 
 def fp8_setup(torch, ffn, device, inp=None):

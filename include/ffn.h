@@ -86,6 +86,17 @@ typedef enum { FFN_F32 = 0, FFN_F16 = 1, FFN_BF16 = 2 } ffn_dtype;
  * ffn_block_forward_q4).  No counterpart on the pages, whose block output
  * stops at the down projection; the pre-norm layer adds its input back.    */
 #define FFN_RESIDUAL 128u
+/* Decode (weight-streaming) path, where its TMA-streamed kernels run: the
+ * whole block as ONE persistent kernel -- a cooperative launch in which the
+ * RMSNorm, gate/up and down stages hand over through counters and flags in
+ * memory, and a CTA done with gate/up streams its down weights at once
+ * ("Megakernels on Mac: What Fusion Saves and What It Costs", sections
+ * "Dependencies and synchronization" and "Small gaps between dispatches").
+ * Same results within the bounds; on GB300 slower than the default chain of
+ * three programmatically dependent kernels (e.g. 8 x 4096 -> 14336 bf16: 69
+ * against 62 us), so opt-in.  Also accepted by ffn_block_forward_q4 / _fp8 /
+ * _q8 and ffn_block_forward_chained; ignored where the block runs otherwise. */
+#define FFN_DECODE_ONE_KERNEL 256u
 
 /* ------------------------------------------------------------------------
  * ffn_rmsnorm -- n[r,c] = x[r,c] * rsqrt(ms_r + eps) * g[c],

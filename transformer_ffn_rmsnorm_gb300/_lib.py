@@ -26,7 +26,7 @@ FFN_ERR_RANGE = 10
 FFN_F32, FFN_F16, FFN_BF16 = 0, 1, 2
 FFN_AUTO, FFN_GATEUP_FUSED, FFN_GATEUP_UNFUSED, FFN_PATH_GEMM, FFN_PATH_GEMV = 0, 1, 2, 4, 8
 FFN_ACT_SINGLE, FFN_ACT_SPLIT, FFN_PREPARED_WEIGHTS = 16, 32, 64
-FFN_RESIDUAL = 128
+FFN_RESIDUAL, FFN_DECODE_ONE_KERNEL = 128, 256
 
 
 class Q4Weight(ctypes.Structure):

@@ -99,7 +99,8 @@ ffn_status plan_block(int64_t rows, int64_t d, int64_t ffn, ffn_dtype dt, uint32
     ffn_status st = check_block_shape(rows, d, ffn, dt);
     if (st != FFN_OK) return st;
     const uint32_t known = FFN_GATEUP_FUSED | FFN_GATEUP_UNFUSED | FFN_PATH_GEMM | FFN_PATH_GEMV |
-                           FFN_ACT_SINGLE | FFN_ACT_SPLIT | FFN_PREPARED_WEIGHTS | FFN_RESIDUAL;
+                           FFN_ACT_SINGLE | FFN_ACT_SPLIT | FFN_PREPARED_WEIGHTS | FFN_RESIDUAL |
+                           FFN_DECODE_ONE_KERNEL;
     if (flags & ~known) return FFN_ERR_FLAGS;
     if ((flags & FFN_GATEUP_FUSED) && (flags & FFN_GATEUP_UNFUSED)) return FFN_ERR_FLAGS;
     if ((flags & FFN_PATH_GEMM) && (flags & FFN_PATH_GEMV)) return FFN_ERR_FLAGS;
@@ -165,7 +166,8 @@ ffn_status from_cuda(cudaError_t e) { return e == cudaSuccess ? FFN_OK : FFN_ERR
 const char *kernel_name(int kind) {
     static const char *names[K_NUM_KINDS] = {
         "prepare", "rmsnorm", "swiglu", "simt_gateup", "simt_down", "gemv_norm",
-        "gemv_gateup", "gemv_down", "gemm_gateup", "gemm_down", "selftest", "splitk_reduce"};
+        "gemv_gateup", "gemv_down", "gemm_gateup", "gemm_down", "selftest", "splitk_reduce",
+        "gemv_fused"};
     return (kind >= 0 && kind < K_NUM_KINDS) ? names[kind] : "unknown";
 }
 
@@ -326,7 +328,8 @@ static ffn_status block_forward(const void *x, const float *x_sumsq, const void 
             RowStats rs;
             rs.ss_in = x_sumsq;
             rs.ss_out = y_sumsq;
-            return from_cuda(launch_gemv_block(wf, x, g, a, b, c, y, rows, d, ffn, eps, gw, s, res, rs));
+            return from_cuda(launch_gemv_block(wf, x, g, a, b, c, y, rows, d, ffn, eps, gw, s, res, rs,
+                                               (flags & FFN_DECODE_ONE_KERNEL) != 0));
         }
         case PATH_GEMM: {
             const size_t nb = align256(static_cast<size_t>(rows) * d * es);
@@ -418,7 +421,7 @@ ffn_status ffn_block_forward_q4(const void *x, const void *g, ffn_q4_weight w_ga
     if (!g || !w_gate.qs || !w_gate.scales || !w_up.qs || !w_up.scales || !w_down.qs ||
         !w_down.scales || (rows != 0 && (!x || !y)))
         return FFN_ERR_NULL;
-    if (flags & ~FFN_RESIDUAL) return FFN_ERR_FLAGS;
+    if (flags & ~(FFN_RESIDUAL | FFN_DECODE_ONE_KERNEL)) return FFN_ERR_FLAGS;
     size_t need = 0;
     ffn_status st = ffn_block_q4_workspace_bytes(rows, d, ffn, &need);
     if (st != FFN_OK) return st;
@@ -450,7 +453,8 @@ ffn_status ffn_block_forward_q4(const void *x, const void *g, ffn_q4_weight w_ga
         const char *xr = static_cast<const char *>(x) + r0 * d * 2;
         char *yr = static_cast<char *>(y) + r0 * d * 2;
         cudaError_t e = launch_gemv_block(WF_Q4, xr, g, a, b, c, yr, nr, d, ffn, eps, gw, s,
-                                          (flags & FFN_RESIDUAL) ? xr : nullptr);
+                                          (flags & FFN_RESIDUAL) ? xr : nullptr, RowStats{},
+                                          (flags & FFN_DECODE_ONE_KERNEL) != 0);
         if (e != cudaSuccess) return FFN_ERR_CUDA;
     }
     return FFN_OK;
@@ -471,7 +475,7 @@ ffn_status ffn_block_forward_fp8(const void *x, const void *g, ffn_fp8_weight w_
     if (!g || !w_gate.codes || !w_gate.scales || !w_up.codes || !w_up.scales || !w_down.codes ||
         !w_down.scales || (rows != 0 && (!x || !y)))
         return FFN_ERR_NULL;
-    if (flags & ~FFN_RESIDUAL) return FFN_ERR_FLAGS;
+    if (flags & ~(FFN_RESIDUAL | FFN_DECODE_ONE_KERNEL)) return FFN_ERR_FLAGS;
     size_t need = 0;
     ffn_status st = ffn_block_fp8_workspace_bytes(rows, d, ffn, &need);
     if (st != FFN_OK) return st;
@@ -504,7 +508,8 @@ ffn_status ffn_block_forward_fp8(const void *x, const void *g, ffn_fp8_weight w_
         const char *xr = static_cast<const char *>(x) + r0 * d * 2;
         char *yr = static_cast<char *>(y) + r0 * d * 2;
         cudaError_t e = launch_gemv_block(WF_FP8, xr, g, a, b, c, yr, nr, d, ffn, eps, gw, s,
-                                          (flags & FFN_RESIDUAL) ? xr : nullptr);
+                                          (flags & FFN_RESIDUAL) ? xr : nullptr, RowStats{},
+                                          (flags & FFN_DECODE_ONE_KERNEL) != 0);
         if (e != cudaSuccess) return FFN_ERR_CUDA;
     }
     return FFN_OK;
@@ -525,7 +530,7 @@ ffn_status ffn_block_forward_q8(const void *x, const void *g, ffn_q8_weight w_ga
     if (!g || !w_gate.codes || !w_gate.scales || !w_up.codes || !w_up.scales || !w_down.codes ||
         !w_down.scales || (rows != 0 && (!x || !y)))
         return FFN_ERR_NULL;
-    if (flags & ~FFN_RESIDUAL) return FFN_ERR_FLAGS;
+    if (flags & ~(FFN_RESIDUAL | FFN_DECODE_ONE_KERNEL)) return FFN_ERR_FLAGS;
     size_t need = 0;
     ffn_status st = ffn_block_q8_workspace_bytes(rows, d, ffn, &need);
     if (st != FFN_OK) return st;
@@ -557,7 +562,8 @@ ffn_status ffn_block_forward_q8(const void *x, const void *g, ffn_q8_weight w_ga
         const char *xr = static_cast<const char *>(x) + r0 * d * 2;
         char *yr = static_cast<char *>(y) + r0 * d * 2;
         cudaError_t e = launch_gemv_block(WF_Q8, xr, g, a, b, c, yr, nr, d, ffn, eps, gw, s,
-                                          (flags & FFN_RESIDUAL) ? xr : nullptr);
+                                          (flags & FFN_RESIDUAL) ? xr : nullptr, RowStats{},
+                                          (flags & FFN_DECODE_ONE_KERNEL) != 0);
         if (e != cudaSuccess) return FFN_ERR_CUDA;
     }
     return FFN_OK;

@@ -28,6 +28,7 @@ enum KernelKind : int {
     K_GEMM_DOWN,
     K_SELFTEST,
     K_SPLITK_REDUCE,
+    K_GEMV_FUSED,
     K_NUM_KINDS
 };
 const char *kernel_name(int kind);
@@ -139,10 +140,12 @@ struct GemvWeights {
     const uint16_t *sc;     // q4 / Q8_0 block scales [out x in/32]
     const float *rs;        // e4m3: float scale of each output row [out]
 };
+// one_kernel: the whole block as one persistent kernel where the streaming
+// kernels run (FFN_DECODE_ONE_KERNEL), else the norm, gate/up and down kernels.
 cudaError_t launch_gemv_block(int wfmt, const void *x, const void *g, GemvWeights wg,
                               GemvWeights wu, GemvWeights wd, void *y, int64_t rows, int64_t d,
                               int64_t ffn, float eps, const GemvWorkspace &ws, cudaStream_t s,
-                              const void *res = nullptr, RowStats rs = {});
+                              const void *res = nullptr, RowStats rs = {}, bool one_kernel = false);
 
 // A 2D tiled TMA descriptor over a row-major array of `rows` rows, `inner`
 // elements a row, rows `row_bytes` apart; boxes of box_inner x box_rows.

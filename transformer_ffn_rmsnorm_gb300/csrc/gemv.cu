@@ -46,39 +46,6 @@ constexpr int kDnFeat = 16 * kDnTPC;    // features per down CTA
 // ---------------------------------------------------------------------------
 // 1. RMSNorm of <= 16 token rows, written in fragment order.
 //
-// Eight normalised values n[k .. k+7] of one token (k a multiple of 8) into
-// their fragment slots; with TWO, nlo receives the rounding residual of every
-// value (same order).
-template <int WF, bool TWO>
-__device__ __forceinline__ void store_group(uint16_t *nfrag, uint16_t *nlo, int64_t nch, int token, int64_t k,
-                                            const float (&f)[8]) {
-    using TO = typename Fmt<WF>::TOp;
-    float r[8];   // residuals v - round(v)
-#pragma unroll
-    for (int e = 0; e < 8; ++e) r[e] = f[e] - to_f32(from_f32<TO>(f[e]));
-    if constexpr (WF == WF_Q4) {
-        // two runs of 4 consecutive k; each lands in one 8-byte half of a
-        // lane's fragment with its elements in order {0, 2, 1, 3}
-#pragma unroll
-        for (int run = 0; run < 2; ++run) {
-            TO o[4], ol[4];
-            const int src[4] = {0, 2, 1, 3};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                o[e] = from_f32<TO>(f[4 * run + src[e]]);
-                ol[e] = from_f32<TO>(r[4 * run + src[e]]);
-            }
-            const int64_t base = frag_elem(FRAG_Q4, nch, token, k + 4 * run);
-            *reinterpret_cast<uint2 *>(nfrag + base) = *reinterpret_cast<const uint2 *>(o);
-            if (TWO) *reinterpret_cast<uint2 *>(nlo + base) = *reinterpret_cast<const uint2 *>(ol);
-        }
-    } else {
-        const int64_t base = frag_elem(frag_order<WF>(), nch, token, k);
-        *reinterpret_cast<uint4 *>(nfrag + base) = Vec16<TO>::pack(f);
-        if (TWO) *reinterpret_cast<uint4 *>(nlo + base) = Vec16<TO>::pack(r);
-    }
-}
-
 // Sum over the CTA (256 threads) of every thread's v, returned to all.
 __device__ __forceinline__ float cta_sum256(float v, float (&partial)[8]) {
 #pragma unroll
@@ -523,8 +490,12 @@ template <int WF, int NT, bool TWO>
 cudaError_t launch_typed(const void *x, const void *gain, GemvWeights wg, GemvWeights wu,
                          GemvWeights wd, void *y, int rows, int64_t d, int64_t ffn, float eps,
                          const GemvWorkspace &ws, const Geometry &geo, cudaStream_t s, const void *res,
-                         RowStats rs) {
+                         RowStats rs, bool one_kernel) {
     constexpr bool q4 = WF == WF_Q4;
+    if (one_kernel && stream_supported(WF, d, ffn))
+        if (unsigned long long *ctl = fused_control(d, s))
+            return launch_fused<WF, NT, TWO>(wg, wu, wd, x, gain, y, rows, d, ffn, eps, ws, res, rs.ss_in, rs.ss_out,
+                                             ctl, s);
     {
         LaunchScope scope(K_GEMV_NORM, s);
         uint16_t *nf = static_cast<uint16_t *>(ws.nfrag), *nl = static_cast<uint16_t *>(ws.nfrag_lo);
@@ -592,14 +563,16 @@ template <int WF, bool TWO>
 cudaError_t launch_nt(int nt, const void *x, const void *g, GemvWeights wg, GemvWeights wu,
                       GemvWeights wd, void *y, int rows, int64_t d, int64_t ffn, float eps,
                       const GemvWorkspace &ws, const Geometry &geo, cudaStream_t s, const void *res,
-                      RowStats rs) {
-    if (nt == 1) return launch_typed<WF, 1, TWO>(x, g, wg, wu, wd, y, rows, d, ffn, eps, ws, geo, s, res, rs);
-    if (nt == 2) return launch_typed<WF, 2, TWO>(x, g, wg, wu, wd, y, rows, d, ffn, eps, ws, geo, s, res, rs);
+                      RowStats rs, bool one_kernel) {
+#define FFN_TYPED_ARGS x, g, wg, wu, wd, y, rows, d, ffn, eps, ws, geo, s, res, rs, one_kernel
+    if (nt == 1) return launch_typed<WF, 1, TWO>(FFN_TYPED_ARGS);
+    if (nt == 2) return launch_typed<WF, 2, TWO>(FFN_TYPED_ARGS);
     // 17 to 64 rows: 16-bit weights only (the quantised entries go in groups of 16)
     if constexpr (WF == WF_F16 || WF == WF_BF16 || WF == WF_F16P) {
-        if (nt == 4) return launch_typed<WF, 4, TWO>(x, g, wg, wu, wd, y, rows, d, ffn, eps, ws, geo, s, res, rs);
-        return launch_typed<WF, 8, TWO>(x, g, wg, wu, wd, y, rows, d, ffn, eps, ws, geo, s, res, rs);
+        if (nt == 4) return launch_typed<WF, 4, TWO>(FFN_TYPED_ARGS);
+        return launch_typed<WF, 8, TWO>(FFN_TYPED_ARGS);
     }
+#undef FFN_TYPED_ARGS
     return cudaErrorInvalidValue;
 }
 
@@ -615,10 +588,16 @@ Layout layout(int64_t rows, int64_t d, int64_t ffn) {
     int64_t splits = a.splits > b.splits ? a.splits : b.splits;
     for (int wf : {WF_BF16, WF_Q4, WF_FP8, WF_Q8})
         if (stream_supported(wf, d, ffn)) splits = std::max(splits, stream_down_splits(wf, d, ffn));
+    // (and the one-kernel decode's split partials)
+    const int64_t r = rows > 64 ? 64 : rows;
+    int64_t floats = splits * r * d;
+    for (int wf : {WF_BF16, WF_Q4, WF_FP8, WF_Q8})
+        if (stream_supported(wf, d, ffn))
+            for (bool two : {false, true}) floats = std::max(floats, fused_partial_floats(wf, r, d, ffn, a.nt, two));
     Layout l;
     l.frag_n = align256(static_cast<size_t>(a.nt) * a.nchK * 32 * 16);
     l.frag_h = align256(static_cast<size_t>(a.nt) * a.nchF * 32 * 16);
-    l.partials = align256(static_cast<size_t>(splits) * (rows > 64 ? 64 : rows) * d * 4);
+    l.partials = align256(static_cast<size_t>(floats) * 4);
     l.counters = align256(static_cast<size_t>(a.groups + 1) * 4);   // arrivals per group, then for the row sums
     l.ss_part = align256(static_cast<size_t>(a.groups) * (rows > 64 ? 64 : rows) * 4);
     return l;
@@ -657,27 +636,27 @@ void gemv_carve(void *base, int64_t rows, int64_t d, int64_t ffn, bool two_terms
 cudaError_t launch_gemv_block(int wfmt, const void *x, const void *g, GemvWeights wg,
                               GemvWeights wu, GemvWeights wd, void *y, int64_t rows, int64_t d,
                               int64_t ffn, float eps, const GemvWorkspace &ws, cudaStream_t s,
-                              const void *res, RowStats rs) {
+                              const void *res, RowStats rs, bool one_kernel) {
     if (rows <= 0) return cudaSuccess;
     const Geometry geo = geometry(rows, d, ffn, wfmt == WF_Q4);
     const int r = static_cast<int>(rows);
     const bool two = ws.nfrag_lo != nullptr;
+#define FFN_GEMV_ARGS geo.nt, x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s, res, rs, one_kernel
     switch (wfmt) {
         case WF_F16:
-            return two ? launch_nt<WF_F16, true>(geo.nt, x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s, res, rs)
-                       : launch_nt<WF_F16, false>(geo.nt, x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s, res, rs);
+            return two ? launch_nt<WF_F16, true>(FFN_GEMV_ARGS) : launch_nt<WF_F16, false>(FFN_GEMV_ARGS);
         case WF_BF16:
-            return two ? launch_nt<WF_BF16, true>(geo.nt, x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s, res, rs)
-                       : launch_nt<WF_BF16, false>(geo.nt, x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s, res, rs);
+            return two ? launch_nt<WF_BF16, true>(FFN_GEMV_ARGS) : launch_nt<WF_BF16, false>(FFN_GEMV_ARGS);
         case WF_Q4:   // fp16 operands: one term is enough
-            return launch_nt<WF_Q4, false>(geo.nt, x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s, res, rs);
+            return launch_nt<WF_Q4, false>(FFN_GEMV_ARGS);
         case WF_FP8:  // fp16 operands, as for Q4
-            return launch_nt<WF_FP8, false>(geo.nt, x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s, res, rs);
+            return launch_nt<WF_FP8, false>(FFN_GEMV_ARGS);
         case WF_Q8:
-            return launch_nt<WF_Q8, false>(geo.nt, x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s, res, rs);
+            return launch_nt<WF_Q8, false>(FFN_GEMV_ARGS);
         default:      // prepared fp16 weights
-            return launch_nt<WF_F16P, false>(geo.nt, x, g, wg, wu, wd, y, r, d, ffn, eps, ws, geo, s, res, rs);
+            return launch_nt<WF_F16P, false>(FFN_GEMV_ARGS);
     }
+#undef FFN_GEMV_ARGS
 }
 
 }  // namespace ffn

@@ -155,6 +155,39 @@ __device__ __forceinline__ uint32_t word_of(const uint4 &v, int b) {
     return b == 0 ? v.x : b == 1 ? v.y : b == 2 ? v.z : v.w;
 }
 
+// Eight normalised values n[k .. k+7] of one token (k a multiple of 8) into
+// their fragment slots; with TWO, nlo receives the rounding residual of every
+// value (same order).
+template <int WF, bool TWO>
+__device__ __forceinline__ void store_group(uint16_t *nfrag, uint16_t *nlo, int64_t nch, int token, int64_t k,
+                                            const float (&f)[8]) {
+    using TO = typename Fmt<WF>::TOp;
+    float r[8];   // residuals v - round(v)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) r[e] = f[e] - to_f32(from_f32<TO>(f[e]));
+    if constexpr (WF == WF_Q4) {
+        // two runs of 4 consecutive k; each lands in one 8-byte half of a
+        // lane's fragment with its elements in order {0, 2, 1, 3}
+#pragma unroll
+        for (int run = 0; run < 2; ++run) {
+            TO o[4], ol[4];
+            const int src[4] = {0, 2, 1, 3};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                o[e] = from_f32<TO>(f[4 * run + src[e]]);
+                ol[e] = from_f32<TO>(r[4 * run + src[e]]);
+            }
+            const int64_t base = frag_elem(FRAG_Q4, nch, token, k + 4 * run);
+            *reinterpret_cast<uint2 *>(nfrag + base) = *reinterpret_cast<const uint2 *>(o);
+            if (TWO) *reinterpret_cast<uint2 *>(nlo + base) = *reinterpret_cast<const uint2 *>(ol);
+        }
+    } else {
+        const int64_t base = frag_elem(frag_order<WF>(), nch, token, k);
+        *reinterpret_cast<uint4 *>(nfrag + base) = Vec16<TO>::pack(f);
+        if (TWO) *reinterpret_cast<uint4 *>(nlo + base) = Vec16<TO>::pack(r);
+    }
+}
+
 // Launch-shape knobs of the decode kernels.
 enum { TUNE_NORM_RELEASE_EARLY = 0, TUNE_PRE_STAGES_GATEUP = 1, TUNE_PRE_STAGES_DOWN = 2, TUNE_COUNT = 3 };
 int decode_tuning(int knob);
@@ -173,6 +206,20 @@ cudaError_t launch_stream_down(GemvWeights wd, const void *hfrag, const void *hf
                                float *partials, unsigned *counters, int rows, int64_t d, int64_t ffn,
                                int64_t nchF, int64_t splits, const void *res, float *ss_part, float *y_sumsq,
                                cudaStream_t s);
+
+// The decode block as one cooperative persistent kernel (gemv_fused.cu,
+// FFN_DECODE_ONE_KERNEL): norm, gate/up and down handing over through the
+// stream's control block; ws.partials holds fused_partial_floats(...) fp32
+// split partials.  The shapes of stream_supported().
+int64_t fused_partial_floats(int wfmt, int64_t rows, int64_t d, int64_t ffn, int nt, bool two);
+// The control block of stream s on the current device, or null (d above
+// 65536, or 64 streams of this device already hold one): then the three
+// kernels run instead.
+unsigned long long *fused_control(int64_t d, cudaStream_t s);
+template <int WF, int NT, bool TWO>
+cudaError_t launch_fused(GemvWeights wg, GemvWeights wu, GemvWeights wd, const void *x, const void *gain, void *y,
+                         int rows, int64_t d, int64_t ffn, float eps, const GemvWorkspace &ws, const void *res,
+                         const float *ss_in, float *y_sumsq, unsigned long long *ctl, cudaStream_t s);
 
 }  // namespace gemv
 }  // namespace ffn

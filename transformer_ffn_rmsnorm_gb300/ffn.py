@@ -17,8 +17,8 @@ import torch
 from . import _lib
 from ._lib import (FFN_AUTO, FFN_BF16, FFN_F16, FFN_F32, FFN_GATEUP_FUSED,  # noqa: F401
                    FFN_GATEUP_UNFUSED, FFN_ACT_SINGLE, FFN_ACT_SPLIT, FFN_PATH_GEMM,
-                   FFN_PATH_GEMV, FFN_PREPARED_WEIGHTS, FFN_RESIDUAL, Fp8Weight, Q4Weight,
-                   Q8Weight)
+                   FFN_PATH_GEMV, FFN_PREPARED_WEIGHTS, FFN_RESIDUAL, FFN_DECODE_ONE_KERNEL,
+                   Fp8Weight, Q4Weight, Q8Weight)
 
 _DT = {torch.float32: FFN_F32, torch.float16: FFN_F16, torch.bfloat16: FFN_BF16}
 
