@@ -131,8 +131,8 @@ __device__ __forceinline__ void cursor_next(Cursor &c, const FusedParams &p) {
     }
 }
 
-// Control blocks: library-owned device memory, zeroed when created, one
-// block a stream (calls on one stream run one after another; calls on
+// Control blocks: library-owned device memory (a module array, zero when
+// the module loads), one block a stream (calls on one stream run one after another; calls on
 // different streams may overlap).  Arrival counters are plain atomicAdd
 // counters that their last arrival sets back to zero, so every call finds
 // them at zero.  Go flags carry the call's epoch (one more than the last
@@ -158,6 +158,7 @@ enum : int {
     kCtlWords = W_SPLIT0 + kMaxGroups
 };
 static_assert(kCtlWords % 16 == 0, "blocks of whole 128-byte lines");
+__device__ __align__(128) unsigned long long g_fused_ctl[kCtlSlots * kCtlWords];
 enum { GO_NORM = 0, GO_GATEUP = 1 };
 
 // Polls read relaxed (an acquire load on every poll held up the SM's other
@@ -736,28 +737,21 @@ unsigned long long *fused_control(int64_t d, cudaStream_t s) {
     static std::map<std::pair<int, cudaStream_t>, int> slot_of;
     constexpr int kDevices = 64;
     static int used[kDevices] = {};
-    static unsigned long long *pool[kDevices] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDevices) return nullptr;
+    // the blocks' address in the current context, looked up every call (a
+    // host-side query once the module is loaded): right after a
+    // cudaDeviceReset too, when the module loads again with its blocks zero
+    void *base = nullptr;
+    if (cudaGetSymbolAddress(&base, g_fused_ctl) != cudaSuccess) return nullptr;
     std::lock_guard<std::mutex> lock(mu);
-    if (!pool[dev]) {
-        void *ptr = nullptr;
-        if (cudaMalloc(&ptr, sizeof(unsigned long long) * kCtlSlots * kCtlWords) != cudaSuccess) {
-            (void)cudaGetLastError();
-            return nullptr;
-        }
-        pool[dev] = static_cast<unsigned long long *>(ptr);
-    }
     const auto key = std::make_pair(dev, s);
     auto it = slot_of.find(key);
     if (it == slot_of.end()) {
         if (used[dev] == kCtlSlots) return nullptr;
-        unsigned long long *blk = pool[dev] + static_cast<size_t>(used[dev]) * kCtlWords;
-        // zero before the first call that uses it, in that call's stream order
-        if (cudaMemsetAsync(blk, 0, sizeof(unsigned long long) * kCtlWords, s) != cudaSuccess) return nullptr;
         it = slot_of.emplace(key, used[dev]++).first;
     }
-    return pool[dev] + static_cast<size_t>(it->second) * kCtlWords;
+    return static_cast<unsigned long long *>(base) + static_cast<size_t>(it->second) * kCtlWords;
 }
 
 int64_t fused_partial_floats(int wfmt, int64_t rows, int64_t d, int64_t ffn, int nt, bool two) {
