@@ -46,8 +46,8 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-sub", action="store_true", help="skip the secondary workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU baseline")
-    ap.add_argument("--workload", choices=["prefill", "tiny", "decode", "decode_prepared", "batch", "batch_prepared", "q4", "fp8",
-                                           "q8", "rmsnorm", "swiglu"],
+    ap.add_argument("--workload", choices=["prefill", "tiny", "decode", "decode_prepared", "decode_one_kernel", "batch",
+                                           "batch_prepared", "q4", "q4_one_kernel", "fp8", "q8", "rmsnorm", "swiglu"],
                     default="prefill",
                     help="prefill: the benchmark; others run only that workload (for profiling)")
     ap.add_argument("--only-main", action="store_true",
@@ -555,8 +555,8 @@ def q8_bench(torch, ffn, device, hbm, peak_src, stream, with_oracle=False):
 
 
 def run_workload_only(args):
-    """--workload tiny|decode|decode_prepared|batch|batch_prepared|q4|fp8|q8|rmsnorm|swiglu: run that workload for --warmup +
-    --steps calls and print a short line (used for ncu captures)."""
+    """--workload tiny|decode|decode_prepared|decode_one_kernel|batch|batch_prepared|q4|q4_one_kernel|fp8|q8|rmsnorm|
+    swiglu: run that workload for --warmup + --steps calls and print a short line (used for ncu captures)."""
     import torch
     from transformer_ffn_rmsnorm_gb300 import ffn
     device = torch.device("cuda", 0)
@@ -577,8 +577,9 @@ def run_workload_only(args):
         inp = synth.make_block_inputs(cfg, seed=0)
         targs = [torch.from_numpy(inp[k]).to(device) for k in ("x", "g", "w_gate", "w_up", "w_down")]
         call = lambda i: ffn.ffn_block_forward(*targs, eps=cfg.eps)
-    elif args.workload == "q4":
-        cfg, call = q4_setup(torch, ffn, device)
+    elif args.workload in ("q4", "q4_one_kernel"):
+        cfg, call = q4_setup(torch, ffn, device, None,
+                             ffn.FFN_DECODE_ONE_KERNEL if args.workload == "q4_one_kernel" else 0)
     elif args.workload == "fp8":
         cfg, call = fp8_setup(torch, ffn, device)
     elif args.workload == "q8":
@@ -586,7 +587,8 @@ def run_workload_only(args):
     elif args.workload.startswith("batch"):
         cfg, call = decode_setup(torch, ffn, device, args.workload == "batch_prepared", synth.C8_BATCH_BF16)
     else:
-        cfg, call = decode_setup(torch, ffn, device, prepared=args.workload == "decode_prepared")
+        cfg, call = decode_setup(torch, ffn, device, prepared=args.workload == "decode_prepared",
+                                 flags=ffn.FFN_DECODE_ONE_KERNEL if args.workload == "decode_one_kernel" else 0)
     for i in range(args.warmup + args.steps):
         call(i)
     torch.cuda.synchronize()
