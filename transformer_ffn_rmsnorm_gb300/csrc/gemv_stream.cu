@@ -102,21 +102,33 @@ __global__ void __launch_bounds__(kThreads) gemv_stream_kernel(
         if (lane == 0) {
             ptx::tma_prefetch_map(&map_w0);
             if (TL::nmat == 2) ptx::tma_prefetch_map(&map_w1);
-            // activation chunks of a k range that exist (the last 64-wide
+            // Stage slots and phases are running 32-bit counters, and every
+            // address below is one multiply-add from a per-CTA base: the
+            // producer shares its SM's issue slots with the MMA warps of up to
+            // four CTAs (64-bit stage arithmetic here had cost ~120
+            // instructions per stage, 9 % of the Q4 gate/up kernel's).
+            const int nkb = static_cast<int>(kb1 - kb0);
+            const int nch_b = static_cast<int>(p.nch_b);
+            const int y = static_cast<int>(row0);
+            const uint4 *act[NT * TL::terms];
+#pragma unroll
+            for (int n = 0; n < NT; ++n)
+#pragma unroll
+                for (int t = 0; t < TL::terms; ++t)
+                    act[n * TL::terms + t] = (t ? p.bfrag_lo : p.bfrag) + (n * p.nch_b + kb0 * TL::chunks) * 32;
+            // activation chunks of k-block j that exist (the last 64-wide
             // block can hang one chunk past the buffer)
-            auto nvalid = [&](int64_t kb) {
-                const int64_t left = p.nch_b - kb * TL::chunks;
+            auto nvalid = [&](int j) {
+                const int left = nch_b - static_cast<int>(kb0 + j) * TL::chunks;
                 return static_cast<uint32_t>(left < TL::chunks ? left : TL::chunks);
             };
-            auto stage_of = [&](int64_t i) { return base + static_cast<uint32_t>(i % kStages) * TL::stage_bytes; };
-            auto arm = [&](int64_t i, int64_t kb) {
-                ptx::mbar_arrive_expect_tx(full(static_cast<int>(i % kStages)),
-                                           TL::b_off + NT * TL::terms * nvalid(kb) * kFragBytes);
+            auto arm = [&](int s, int j) {
+                ptx::mbar_arrive_expect_tx(full(s), TL::b_off + NT * TL::terms * nvalid(j) * kFragBytes);
             };
-            auto load_weights = [&](int64_t i, int64_t kb) {
-                const uint32_t st = stage_of(i), bar = full(static_cast<int>(i % kStages));
-                const int x = static_cast<int>(kb * TL::x_per_kb);   // bytes of nibbles or codes / elements
-                const int y = static_cast<int>(row0);
+            auto load_weights = [&](int s, int j) {
+                const uint32_t st = base + s * TL::stage_bytes, bar = full(s);
+                const int kb = static_cast<int>(kb0) + j;
+                const int x = kb * TL::x_per_kb;   // bytes of nibbles or codes / elements
                 ptx::tma_load_2d(st, &map_w0, bar, x, y);
                 if (TL::nmat == 2) ptx::tma_load_2d(st + TL::w_bytes, &map_w1, bar, x, y);
                 if (TL::boxes == 2) {   // the second 128 bytes of each row
@@ -126,44 +138,48 @@ __global__ void __launch_bounds__(kThreads) gemv_stream_kernel(
                 }
                 if (TL::blocks) {
                     const uint32_t sc = st + TL::nmat * TL::w_bytes;
-                    ptx::tma_load_2d(sc, &map_s0, bar, static_cast<int>(kb * 8), y);
-                    if (TL::nmat == 2) ptx::tma_load_2d(sc + TL::s_bytes, &map_s1, bar, static_cast<int>(kb * 8), y);
+                    ptx::tma_load_2d(sc, &map_s0, bar, kb * 8, y);
+                    if (TL::nmat == 2) ptx::tma_load_2d(sc + TL::s_bytes, &map_s1, bar, kb * 8, y);
                 }
             };
-            auto load_acts = [&](int64_t i, int64_t kb) {
-                const uint32_t st = stage_of(i), bar = full(static_cast<int>(i % kStages));
-                const uint32_t nv = nvalid(kb);
+            auto load_acts = [&](int s, int j) {
+                const uint32_t st = base + s * TL::stage_bytes, bar = full(s);
+                const uint32_t nv = nvalid(j);
 #pragma unroll
                 for (int n = 0; n < NT; ++n)
 #pragma unroll
                     for (int t = 0; t < TL::terms; ++t)
                         ptx::bulk_load(st + TL::b_off + (n * TL::terms + t) * TL::chunks * kFragBytes,
-                                       (t ? p.bfrag_lo : p.bfrag) + (n * p.nch_b + kb * TL::chunks) * 32,
-                                       nv * kFragBytes, bar);
+                                       act[n * TL::terms + t] + j * (TL::chunks * 32), nv * kFragBytes, bar);
             };
             // The first ring's worth of weights is requested before the kernel
             // that writes the activations has finished (weights are inputs of
             // the call); the activations only after it has.
-            int64_t npre = (kb1 - kb0) < kStages ? (kb1 - kb0) : kStages;
+            int npre = nkb < kStages ? nkb : kStages;
             if (npre > p.pre_stages) npre = p.pre_stages;
-            for (int64_t i = 0; i < npre; ++i) {
-                arm(i, kb0 + i);
-                load_weights(i, kb0 + i);
+            for (int j = 0; j < npre; ++j) {
+                arm(j, j);
+                load_weights(j, j);
             }
             issued = npre;
             ptx::griddep_wait();
-            for (int64_t i = 0; i < npre; ++i) load_acts(i, kb0 + i);
+            for (int j = 0; j < npre; ++j) load_acts(j, j);
             bool ok = true;
-            for (int64_t kb = kb0 + npre; kb < kb1; ++kb, ++issued) {
-                const int s = static_cast<int>(issued % kStages);
-                const uint32_t ph = static_cast<uint32_t>((issued / kStages) & 1);
+            int s = npre == kStages ? 0 : npre;
+            uint32_t ph = npre == kStages ? 1u : 0u;   // parity of the slot's current use
+            for (int j = npre; j < nkb; ++j) {
                 if (!ptx::mbar_wait(empty(s), ph ^ 1u, abort_flag, kWaitNs)) {
                     ok = false;
                     break;
                 }
-                arm(issued, kb);
-                load_acts(issued, kb);
-                load_weights(issued, kb);
+                arm(s, j);
+                load_acts(s, j);
+                load_weights(s, j);
+                issued = j + 1;
+                if (++s == kStages) {
+                    s = 0;
+                    ph ^= 1u;
+                }
             }
             if (!ok) {
                 atomicOr(p.err, DEVERR_TIMEOUT);
@@ -183,10 +199,9 @@ __global__ void __launch_bounds__(kThreads) gemv_stream_kernel(
 #pragma unroll
             for (int i = 0; i < 4; ++i) acc[n][i] = 0.f;
         bool ok = true;
-        int64_t it = 0;
-        for (int64_t kb = kb0; kb < kb1; ++kb, ++it) {
-            const int s = static_cast<int>(it % kStages);
-            const uint32_t ph = static_cast<uint32_t>((it / kStages) & 1);
+        int s = 0;
+        uint32_t ph = 0;   // slot and parity of the stage consumed next
+        for (int64_t kb = kb0; kb < kb1; ++kb) {
             const bool got = ptx::mbar_wait(full(s), ph, abort_flag, kWaitNs);
             if (!__all_sync(0xffffffffu, got)) {
                 ok = false;
@@ -195,6 +210,10 @@ __global__ void __launch_bounds__(kThreads) gemv_stream_kernel(
             stage_mma<WF, NT, TWO, ROLE>(acc, base + s * TL::stage_bytes, kb, p.nch_b, warp, lane);
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(empty(s));
+            if (++s == kStages) {
+                s = 0;
+                ph ^= 1u;
+            }
         }
         if (!ok) {
             if (lane == 0) {
