@@ -119,6 +119,8 @@ struct GemvWorkspace {
     float *partials;    // [splits][rows][d] fp32
     unsigned *counters; // [d / 64] arrival counters, then one for the rows' sums of squares
     float *ss_part;     // [d / 64][rows] parts of the rows' sums of squares of y
+    float *ncorr;       // Q4 streaming kernels: block offsets of n and of h
+    float *hcorr;
 };
 // The block's RMSNorm reduction handed from one block to the next: ss_in (or
 // null) holds each row's sum of squares of x, used instead of reducing the
@@ -468,6 +470,24 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
             : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
             : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
     }
+}
+
+// d += a * b on tf32 operands, m16n8k8: a0 (row g, k t), a1 (row g + 8, k t),
+// a2 (row g, k t + 4), a3 (row g + 8, k t + 4); b0 (k t, column g), b1 (k t
+// + 4, column g); d as for m16n8k16 (g = lane / 4, t = lane % 4).
+__device__ __forceinline__ void mma_1688_tf32(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// fp32 rounded to tf32 (10 fraction bits, nearest, ties away), as fp32 bits
+__device__ __forceinline__ float round_tf32(float v) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(v));
+    return __uint_as_float(r);
 }
 
 // d = a * b (a zero accumulator that the compiler need not materialise in

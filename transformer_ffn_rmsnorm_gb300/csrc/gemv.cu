@@ -58,35 +58,45 @@ __device__ __forceinline__ float cta_sum256(float v, float (&partial)[8]) {
     return v;
 }
 
-// One CTA per token slot, the row held in registers (VPT 16-byte vectors of
-// x and of g per thread, read together in one round trip): sum of squares,
-// reciprocal root, the fragments.  Slots >= rows (and k >= K) are written as
-// zeros.  The call's first kernel: it waits for the kernel before it, then
-// lets the projection kernel after it start its weight stream, at once
+// grid = (token slots, slices): every CTA reads its token's row (VPT
+// 16-byte vectors of x per thread) for the sum of squares, and with it, in
+// the same round trip, x and g of its slice of whole 32-value blocks (at
+// most one 8-value group per thread); then the reciprocal root and the
+// slice's fragments.  Slots >= rows (and k >= K) are written as zeros.  The
+// call's first kernel: it waits for the kernel before it, then lets the
+// projection kernel after it start its weight stream, at once
 // (release_early) or when it has finished (its reads then do not queue
-// behind that stream).
-template <int WF, bool TWO, int VPT>
+// behind that stream).  Slices: as few as give every thread one group at
+// most (FFN_NORM_SLICES asks for more; 2 to 8 a token measured the same
+// per call for bf16, e4m3, Q8_0 and Q4 blocks).
+// With BIAS (Q4 for the streaming kernels) the fragments take the biased
+// form (store_group_q4_biased) and each block's offset goes to corr: a
+// block's four 8-value groups sit on four adjacent lanes.
+template <int WF, bool TWO, int VPT, bool BIAS>
 __global__ void __launch_bounds__(256) gemv_norm_frag_reg_kernel(const void *x_, const void *g_,
                                                                  uint16_t *nfrag, uint16_t *nlo, int rows,
                                                                  int64_t K, int64_t nch, float eps,
-                                                                 int release_early, const float *ss_in) {
+                                                                 int release_early, const float *ss_in,
+                                                                 float *corr) {
     using T = typename Fmt<WF>::TIn;
     __shared__ float partial[8];
     ptx::griddep_wait();
     if (release_early) ptx::griddep_launch_dependents();
     const int token = blockIdx.x;
-    const int64_t nv = K / 8, ngroups = nch * 4;   // 8-element groups incl. the zero tail
+    const int64_t nv = K / 8;
+    const int64_t v0 = 4 * (nch * blockIdx.y / gridDim.y), v1 = 4 * (nch * (blockIdx.y + 1) / gridDim.y);
     const uint4 *x = reinterpret_cast<const uint4 *>(static_cast<const T *>(x_) + static_cast<int64_t>(token) * K);
     const uint4 *g = static_cast<const uint4 *>(g_);
-    uint4 xv[VPT], gv[VPT];
     const bool live = token < rows;
+    uint4 xv[VPT];
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
         const int64_t v = threadIdx.x + 256 * i;
-        const bool in = live && v < nv;
-        xv[i] = in ? x[v] : make_uint4(0, 0, 0, 0);
-        gv[i] = in ? g[v] : make_uint4(0, 0, 0, 0);
+        xv[i] = (live && !ss_in && v < nv) ? x[v] : make_uint4(0, 0, 0, 0);
     }
+    const int64_t vs = v0 + threadIdx.x;   // this thread's group of the slice
+    const bool in = vs < v1, ld = live && in && vs < nv;
+    const uint4 xs = ld ? x[vs] : make_uint4(0, 0, 0, 0), gs = ld ? g[vs] : make_uint4(0, 0, 0, 0);
     float ss = 0.f;
     if (ss_in) {   // the row's sum of squares, handed on by the block before
         ss = live ? ss_in[token] : 0.f;
@@ -101,26 +111,29 @@ __global__ void __launch_bounds__(256) gemv_norm_frag_reg_kernel(const void *x_,
         ss = cta_sum256(ss, partial);
     }
     const float inv = rsqrtf(ss / static_cast<float>(K) + eps);
+    float f[8], gf[8];
+    Vec16<T>::unpack(xs, f);
+    Vec16<T>::unpack(gs, gf);
 #pragma unroll
-    for (int i = 0; i < VPT; ++i) {
-        const int64_t v = threadIdx.x + 256 * i;
-        if (v >= ngroups) break;
-        float f[8], gf[8];
-        Vec16<T>::unpack(xv[i], f);
-        Vec16<T>::unpack(gv[i], gf);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) f[e] = f[e] * inv * gf[e];
-        store_group<WF, TWO>(nfrag, nlo, nch, token, 8 * v, f);
+    for (int e = 0; e < 8; ++e) f[e] = f[e] * inv * gf[e];
+    if constexpr (BIAS) {
+        // (v0 and v1 are multiples of 4: a lane quad is in or out as a whole)
+        float part = in ? store_group_q4_biased(nfrag, nch, token, 8 * vs, f) : 0.f;
+        part += __shfl_xor_sync(0xffffffffu, part, 1);
+        part += __shfl_xor_sync(0xffffffffu, part, 2);
+        if (in && (vs & 3) == 0) store_q4_corr(corr, gridDim.x / 8, token, vs >> 2, part);
+    } else if (in) {
+        store_group<WF, TWO>(nfrag, nlo, nch, token, 8 * vs, f);
     }
 }
 
 // The same for rows too long for registers (d > 16384): grid = (token slots,
 // slices); every CTA reduces its token's whole row and writes one slice.
-template <int WF, bool TWO>
+template <int WF, bool TWO, bool BIAS>
 __global__ void __launch_bounds__(256) gemv_norm_frag_kernel(const void *x_, const void *g_,
                                                              uint16_t *nfrag, uint16_t *nlo,
                                                              int rows, int64_t K, int64_t nch,
-                                                             float eps, const float *ss_in) {
+                                                             float eps, const float *ss_in, float *corr) {
     using T = typename Fmt<WF>::TIn;
     __shared__ float partial[8];
     // launched as a programmatic dependent: nothing is read or written before
@@ -131,8 +144,8 @@ __global__ void __launch_bounds__(256) gemv_norm_frag_kernel(const void *x_, con
     const int token = blockIdx.x;
     const T *x = static_cast<const T *>(x_) + static_cast<int64_t>(token) * K;
     const T *g = static_cast<const T *>(g_);
-    const int64_t ngroups = nch * 4;  // 8-element groups incl. the zero tail
-    const int64_t v0 = ngroups * blockIdx.y / gridDim.y, v1 = ngroups * (blockIdx.y + 1) / gridDim.y;
+    // slices of whole 32-value blocks (four 8-element groups), the zero tail included
+    const int64_t v0 = 4 * (nch * blockIdx.y / gridDim.y), v1 = 4 * (nch * (blockIdx.y + 1) / gridDim.y);
     const int64_t nv = K / 8;
     float ss = 0.f;
     if (token < rows) {
@@ -146,9 +159,12 @@ __global__ void __launch_bounds__(256) gemv_norm_frag_kernel(const void *x_, con
     ss = cta_sum256(ss, partial);
     if (ss_in) ss = token < rows ? ss_in[token] : 0.f;
     const float inv = rsqrtf(ss / static_cast<float>(K) + eps);
-    for (int64_t v = v0 + threadIdx.x; v < v1; v += blockDim.x) {
+    // every thread takes the same number of turns (the biased form reduces
+    // over lane quads)
+    for (int64_t vb = v0; vb < v1; vb += blockDim.x) {
+        const int64_t v = vb + threadIdx.x;
         float f[8];
-        if (token < rows && v < nv) {
+        if (token < rows && v < nv && v < v1) {
             float gf[8];
             Vec16<T>::unpack(reinterpret_cast<const uint4 *>(x)[v], f);
             Vec16<T>::unpack(reinterpret_cast<const uint4 *>(g)[v], gf);
@@ -158,7 +174,14 @@ __global__ void __launch_bounds__(256) gemv_norm_frag_kernel(const void *x_, con
 #pragma unroll
             for (int e = 0; e < 8; ++e) f[e] = 0.f;
         }
-        store_group<WF, TWO>(nfrag, nlo, nch, token, 8 * v, f);
+        if constexpr (BIAS) {
+            float part = v < v1 ? store_group_q4_biased(nfrag, nch, token, 8 * v, f) : 0.f;
+            part += __shfl_xor_sync(0xffffffffu, part, 1);
+            part += __shfl_xor_sync(0xffffffffu, part, 2);
+            if (v < v1 && (v & 3) == 0) store_q4_corr(corr, gridDim.x / 8, token, v >> 2, part);
+        } else if (v < v1) {
+            store_group<WF, TWO>(nfrag, nlo, nch, token, 8 * v, f);
+        }
     }
 }
 
@@ -486,6 +509,35 @@ Geometry geometry(int64_t rows, int64_t d, int64_t ffn, bool q4) {
 
 size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 
+// The call's norm kernel: one CTA per token slot holding its row in
+// registers, or (rows past 16384 values) slices of the row per CTA.
+template <int WF, bool TWO, bool BIAS, int NT>
+cudaError_t launch_norm(const void *x, const void *gain, int rows, int64_t d, float eps, const GemvWorkspace &ws,
+                        const Geometry &geo, cudaStream_t s, RowStats rs) {
+    uint16_t *nf = static_cast<uint16_t *>(ws.nfrag), *nl = static_cast<uint16_t *>(ws.nfrag_lo);
+    const int64_t vpt = cdiv(geo.nchK * 4, 256);   // 16-byte vectors of the row per thread
+    // slices a token: at least one 8-value group a thread, at most one block a slice
+    int64_t slices = std::max<int64_t>(decode_tuning(TUNE_NORM_SLICES), vpt);
+    slices = std::max<int64_t>(1, std::min<int64_t>(slices, geo.nchK));
+    const dim3 grid(8 * NT, static_cast<unsigned>(slices));
+    const int early = decode_tuning(TUNE_NORM_RELEASE_EARLY);
+    if (vpt <= 1)
+        return launch_dependent(gemv_norm_frag_reg_kernel<WF, TWO, 1, BIAS>, grid, dim3(256), 0, s, x, gain, nf, nl,
+                                rows, d, geo.nchK, eps, early, rs.ss_in, ws.ncorr);
+    if (vpt <= 2)
+        return launch_dependent(gemv_norm_frag_reg_kernel<WF, TWO, 2, BIAS>, grid, dim3(256), 0, s, x, gain, nf, nl,
+                                rows, d, geo.nchK, eps, early, rs.ss_in, ws.ncorr);
+    if (vpt <= 4)
+        return launch_dependent(gemv_norm_frag_reg_kernel<WF, TWO, 4, BIAS>, grid, dim3(256), 0, s, x, gain, nf, nl,
+                                rows, d, geo.nchK, eps, early, rs.ss_in, ws.ncorr);
+    if (vpt <= 8)
+        return launch_dependent(gemv_norm_frag_reg_kernel<WF, TWO, 8, BIAS>, grid, dim3(256), 0, s, x, gain, nf, nl,
+                                rows, d, geo.nchK, eps, early, rs.ss_in, ws.ncorr);
+    return launch_dependent(gemv_norm_frag_kernel<WF, TWO, BIAS>,
+                            dim3(8 * NT, static_cast<unsigned>(std::min<int64_t>(16, cdiv(vpt, 4)))), dim3(256), 0, s,
+                            x, gain, nf, nl, rows, d, geo.nchK, eps, rs.ss_in, ws.ncorr);
+}
+
 template <int WF, int NT, bool TWO>
 cudaError_t launch_typed(const void *x, const void *gain, GemvWeights wg, GemvWeights wu,
                          GemvWeights wd, void *y, int rows, int64_t d, int64_t ffn, float eps,
@@ -498,38 +550,24 @@ cudaError_t launch_typed(const void *x, const void *gain, GemvWeights wg, GemvWe
                                              ctl, s);
     {
         LaunchScope scope(K_GEMV_NORM, s);
-        uint16_t *nf = static_cast<uint16_t *>(ws.nfrag), *nl = static_cast<uint16_t *>(ws.nfrag_lo);
-        const int64_t vpt = cdiv(geo.nchK * 4, 256);   // 16-byte groups per thread, one CTA per token slot
-        const dim3 grid(8 * NT);
-        const int early = decode_tuning(TUNE_NORM_RELEASE_EARLY);
         cudaError_t e;
-        if (vpt <= 1)
-            e = launch_dependent(gemv_norm_frag_reg_kernel<WF, TWO, 1>, grid, dim3(256), 0, s, x, gain, nf, nl, rows,
-                                 d, geo.nchK, eps, early, rs.ss_in);
-        else if (vpt <= 2)
-            e = launch_dependent(gemv_norm_frag_reg_kernel<WF, TWO, 2>, grid, dim3(256), 0, s, x, gain, nf, nl, rows,
-                                 d, geo.nchK, eps, early, rs.ss_in);
-        else if (vpt <= 4)
-            e = launch_dependent(gemv_norm_frag_reg_kernel<WF, TWO, 4>, grid, dim3(256), 0, s, x, gain, nf, nl, rows,
-                                 d, geo.nchK, eps, early, rs.ss_in);
-        else if (vpt <= 8)
-            e = launch_dependent(gemv_norm_frag_reg_kernel<WF, TWO, 8>, grid, dim3(256), 0, s, x, gain, nf, nl, rows,
-                                 d, geo.nchK, eps, early, rs.ss_in);
+        // Q4 activations for the streaming kernels take the biased form
+        if constexpr (q4)
+            e = stream_supported(WF, d, ffn) ? launch_norm<WF, TWO, true, NT>(x, gain, rows, d, eps, ws, geo, s, rs)
+                                             : launch_norm<WF, TWO, false, NT>(x, gain, rows, d, eps, ws, geo, s, rs);
         else
-            e = launch_dependent(gemv_norm_frag_kernel<WF, TWO>,
-                                 dim3(8 * NT, static_cast<unsigned>(std::min<int64_t>(16, cdiv(vpt, 4)))), dim3(256),
-                                 0, s, x, gain, nf, nl, rows, d, geo.nchK, eps, rs.ss_in);
+            e = launch_norm<WF, TWO, false, NT>(x, gain, rows, d, eps, ws, geo, s, rs);
         if (e == cudaSuccess) e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     if (stream_supported(WF, d, ffn)) {
         cudaError_t e = launch_stream_gateup<WF, NT, TWO>(wg, wu, ws.nfrag, ws.nfrag_lo, ws.hfrag, ws.hfrag_lo, d,
                                                           ffn, geo.nchK, geo.nchF, ws.counters,
-                                                          static_cast<int>(geo.groups + 1), s);
+                                                          static_cast<int>(geo.groups + 1), ws.ncorr, ws.hcorr, s);
         if (e != cudaSuccess) return e;
         return launch_stream_down<WF, NT, TWO>(wd, ws.hfrag, ws.hfrag_lo, y, ws.partials, ws.counters, rows, d,
                                                ffn, geo.nchF, stream_down_splits(WF, d, ffn), res, ws.ss_part,
-                                               rs.ss_out, s);
+                                               rs.ss_out, ws.hcorr, s);
     }
     if constexpr (WF == WF_FP8 || WF == WF_Q8 || NT > 2) {
         // e4m3 and Q8_0 weights, and more than two token tiles, stream through
@@ -577,7 +615,7 @@ cudaError_t launch_nt(int nt, const void *x, const void *g, GemvWeights wg, Gemv
 }
 
 struct Layout {
-    size_t frag_n, frag_h, partials, counters, ss_part;
+    size_t frag_n, frag_h, partials, counters, ss_part, corr_n, corr_h;
 };
 
 Layout layout(int64_t rows, int64_t d, int64_t ffn) {
@@ -600,6 +638,8 @@ Layout layout(int64_t rows, int64_t d, int64_t ffn) {
     l.partials = align256(static_cast<size_t>(floats) * 4);
     l.counters = align256(static_cast<size_t>(a.groups + 1) * 4);   // arrivals per group, then for the row sums
     l.ss_part = align256(static_cast<size_t>(a.groups) * (rows > 64 ? 64 : rows) * 4);
+    l.corr_n = align256(static_cast<size_t>(q4_corr_floats(a.nt, a.nchK)) * 4);
+    l.corr_h = align256(static_cast<size_t>(q4_corr_floats(a.nt, a.nchF)) * 4);
     return l;
 }
 
@@ -608,7 +648,7 @@ Layout layout(int64_t rows, int64_t d, int64_t ffn) {
 size_t gemv_workspace_bytes(int64_t rows, int64_t d, int64_t ffn, bool two_terms) {
     const Layout l = layout(rows, d, ffn);
     const size_t frags = l.frag_n + l.frag_h;
-    return (two_terms ? 2 * frags : frags) + l.partials + l.counters + l.ss_part;
+    return (two_terms ? 2 * frags : frags) + l.partials + l.counters + l.ss_part + l.corr_n + l.corr_h;
 }
 
 void gemv_carve(void *base, int64_t rows, int64_t d, int64_t ffn, bool two_terms, GemvWorkspace *ws) {
@@ -631,6 +671,10 @@ void gemv_carve(void *base, int64_t rows, int64_t d, int64_t ffn, bool two_terms
     ws->counters = reinterpret_cast<unsigned *>(p);
     p += l.counters;
     ws->ss_part = reinterpret_cast<float *>(p);
+    p += l.ss_part;
+    ws->ncorr = reinterpret_cast<float *>(p);
+    p += l.corr_n;
+    ws->hcorr = reinterpret_cast<float *>(p);
 }
 
 cudaError_t launch_gemv_block(int wfmt, const void *x, const void *g, GemvWeights wg,

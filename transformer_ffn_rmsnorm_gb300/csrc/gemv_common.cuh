@@ -127,6 +127,40 @@ __device__ __forceinline__ void dequant_word(uint32_t w, uint32_t (&r)[4]) {
     }
 }
 
+// The same unpacking with the offsets left in (the streaming kernels): r[0]
+// and r[2] hold 1024 + u, r[1] and r[3] hold 1024 + 16u, exactly, from one
+// shift and four LOP3s.  The high-nibble activations are stored divided by
+// 16, so a weight meets its stored activation a as ((u - 8) + 1032) a in a
+// low position and as ((u - 8) + 72) (16 a) in a high one: every block's
+// products carry 1032 * (sum of its low stored values) + 1152 * (sum of its
+// high ones), a per-(block, token) constant that the activation writer
+// stores beside the fragments (store_q4_corr) and one tf32 MMA a stage
+// takes off again, weighted by the block scales.
+__device__ __forceinline__ void unpack_word_biased(uint32_t w, uint32_t (&r)[4]) {
+    const uint32_t w8 = w >> 8;
+    r[0] = lop_and_or(w, 0x000F000Fu, 0x64006400u);
+    r[1] = lop_and_or(w, 0x00F000F0u, 0x64006400u);
+    r[2] = lop_and_or(w8, 0x000F000Fu, 0x64006400u);
+    r[3] = lop_and_or(w8, 0x00F000F0u, 0x64006400u);
+}
+
+// Offsets of the biased Q4 operands (unpack_word_biased), per block of 32
+// and token: C = 1032 * sum(low stored values) + 1152 * sum(high stored
+// values), stored negated as two tf32 terms (hi + lo = -C to ~2^-22) in the
+// order of the stage's correction MMA: per stage of 8 blocks and token tile
+// (nt tiles), lane 4 * (token % 8) + t holds {hi(2t), hi(2t + 1), lo(2t),
+// lo(2t + 1)} for blocks 2t and 2t + 1 of the stage (16 bytes a lane, 512 a
+// tile, nt x 512 contiguous bytes a stage).
+__host__ __device__ constexpr int64_t q4_corr_floats(int nt, int64_t nch) { return static_cast<int64_t>(nt) * nch * 16; }
+__device__ __forceinline__ void store_q4_corr(float *corr, int nt, int token, int64_t blk, float c) {
+    const float hi = ptx::round_tf32(-c);
+    const float lo = ptx::round_tf32(-c - hi);
+    float *p = corr + ((((blk >> 3) * nt + (token >> 3)) * 32 + 4 * (token & 7) + ((blk & 7) >> 1)) * 4 +
+                       (blk & 1));
+    p[0] = hi;
+    p[2] = lo;
+}
+
 // Four signed bytes (the low byte first) as two fp16 pairs, exactly: each
 // byte q + 128 (the sign bit flipped) goes into the low mantissa byte of
 // fp16 1024 (ulp 1), giving 1024 + 128 + q; one fp16 subtraction of 1152
@@ -188,8 +222,38 @@ __device__ __forceinline__ void store_group(uint16_t *nfrag, uint16_t *nlo, int6
     }
 }
 
+// Q4 for the streaming kernels: eight values n[k .. k+7] (k a multiple of 8)
+// into their fragment slots as store_group does, the high-nibble positions
+// of a block (k % 32 >= 16) divided by 16; returns those stored values
+// summed and weighted by their offset (1032 low, 1152 high).
+__device__ __forceinline__ float store_group_q4_biased(uint16_t *nfrag, int64_t nch, int token, int64_t k,
+                                                       const float (&f)[8]) {
+    const bool hi = (k & 31) >= 16;
+    const float scale = hi ? 0.0625f : 1.f;
+    float sum = 0.f;
+#pragma unroll
+    for (int run = 0; run < 2; ++run) {
+        __half o[4];
+        const int src[4] = {0, 2, 1, 3};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            o[e] = __float2half_rn(f[4 * run + src[e]] * scale);
+            sum += __half2float(o[e]);
+        }
+        const int64_t base = frag_elem(FRAG_Q4, nch, token, k + 4 * run);
+        *reinterpret_cast<uint2 *>(nfrag + base) = *reinterpret_cast<const uint2 *>(o);
+    }
+    return sum * (hi ? 1152.f : 1032.f);
+}
+
 // Launch-shape knobs of the decode kernels.
-enum { TUNE_NORM_RELEASE_EARLY = 0, TUNE_PRE_STAGES_GATEUP = 1, TUNE_PRE_STAGES_DOWN = 2, TUNE_COUNT = 3 };
+enum {
+    TUNE_NORM_RELEASE_EARLY = 0,
+    TUNE_PRE_STAGES_GATEUP = 1,
+    TUNE_PRE_STAGES_DOWN = 2,
+    TUNE_NORM_SLICES = 3,
+    TUNE_COUNT = 4
+};
 int decode_tuning(int knob);
 
 // TMA-streamed decode kernels (gemv_stream.cu)
@@ -198,14 +262,16 @@ int64_t stream_down_splits(int wfmt, int64_t d, int64_t ffn);
 template <int WF, int NT, bool TWO>
 cudaError_t launch_stream_gateup(GemvWeights wg, GemvWeights wu, const void *nfrag, const void *nfrag_lo,
                                  void *hfrag, void *hfrag_lo, int64_t d, int64_t ffn, int64_t nchK,
-                                 int64_t nchF, unsigned *counters, int ncounters, cudaStream_t s);
+                                 int64_t nchF, unsigned *counters, int ncounters, const float *ncorr,
+                                 float *hcorr, cudaStream_t s);
 template <int WF, int NT, bool TWO>
 // ss_part, y_sumsq (y_sumsq may be null): the rows' sums of squares of the
-// stored y, through [ceil(d/64)][rows] partial sums and counters[ceil(d/64)]
+// stored y, through [ceil(d/64)][rows] partial sums and counters[ceil(d/64)];
+// Q4: ncorr / hcorr the block offsets of n (read) and h (written, then read)
 cudaError_t launch_stream_down(GemvWeights wd, const void *hfrag, const void *hfrag_lo, void *y,
                                float *partials, unsigned *counters, int rows, int64_t d, int64_t ffn,
                                int64_t nchF, int64_t splits, const void *res, float *ss_part, float *y_sumsq,
-                               cudaStream_t s);
+                               const float *hcorr, cudaStream_t s);
 
 // The decode block as one cooperative persistent kernel (gemv_fused.cu,
 // FFN_DECODE_ONE_KERNEL): norm, gate/up and down handing over through the

@@ -20,8 +20,11 @@ enum { ROLE_GATEUP = 0, ROLE_DOWN = 1 };
 
 // Stage layout: [weights of each matrix][their scales (Q4)][activation
 // fragments: NT tiles x terms x chunks x 512 B].  Every format but Q8_0
-// moves 128 bytes of each weight row per stage (Q8_0: 256).
-template <int WF, int ROLE, int NT, bool TWO> struct Tile {
+// moves 128 bytes of each weight row per stage (Q8_0: 256).  With BIAS (Q4
+// on the streaming kernels) each stage also has NT x 512 bytes of block
+// offsets (store_q4_corr), kept in a ring of their own after the stages so
+// that the stages keep their 1 KB multiple.
+template <int WF, int ROLE, int NT, bool TWO, bool BIAS = false> struct Tile {
     static constexpr bool q4 = WF == WF_Q4;
     static constexpr bool fp8 = WF == WF_FP8;
     static constexpr bool q8 = WF == WF_Q8;
@@ -47,7 +50,8 @@ template <int WF, int ROLE, int NT, bool TWO> struct Tile {
     // (large stages of many token tiles run with two, keeping three CTAs a SM)
     static constexpr int min_stages = (NT >= 4 && stage_bytes > 20 * 1024) ? 2 : 3;
     static constexpr int stages = stages_fit < min_stages ? min_stages : stages_fit > 6 ? 6 : stages_fit;
-    static constexpr size_t smem_bytes = stages * stage_bytes + 1024;
+    static constexpr uint32_t corr_bytes = (q4 && BIAS) ? NT * 512 : 0;
+    static constexpr size_t smem_bytes = stages * (stage_bytes + corr_bytes) + 1024;
 };
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
@@ -70,11 +74,11 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, 128;
 // st holds k-block kb of the warp's weight rows (gate/up: warp / 2 picks the
 // matrix, warp % 2 the 16-row tile of the box's 32 rows; down: warp picks the
 // 16-row tile of 64) and of the activation fragments; acc gathers the
-// products for NT token tiles.
-template <int WF, int NT, bool TWO, int ROLE>
+// products for NT token tiles.  With BIAS, cst is the stage's block offsets.
+template <int WF, int NT, bool TWO, int ROLE, bool BIAS = false>
 __device__ __forceinline__ void stage_mma(float (&acc)[NT][4], uint32_t st, int64_t kb, int64_t nch_b, int warp,
-                                          int lane) {
-    using TL = Tile<WF, ROLE, NT, TWO>;
+                                          int lane, uint32_t cst = 0) {
+    using TL = Tile<WF, ROLE, NT, TWO, BIAS>;
     constexpr bool bf = Fmt<WF>::op_bf16;
     constexpr bool q4 = TL::q4;
     constexpr bool fp8 = TL::fp8;
@@ -212,8 +216,13 @@ __device__ __forceinline__ void stage_mma(float (&acc)[NT][4], uint32_t st, int6
 #pragma unroll
                 for (int n = 0; n < NT; ++n) b[n] = lds128(bbase + (n * TL::chunks + bi) * kFragBytes);
                 uint32_t lo[4], hi[4];
-                dequant_word(word_of(qa, blk), lo);
-                dequant_word(word_of(qb, blk), hi);
+                if constexpr (BIAS) {
+                    unpack_word_biased(word_of(qa, blk), lo);
+                    unpack_word_biased(word_of(qb, blk), hi);
+                } else {
+                    dequant_word(word_of(qa, blk), lo);
+                    dequant_word(word_of(qb, blk), hi);
+                }
                 const float fa = (bi & 1) ? fsa[bi >> 1].y : fsa[bi >> 1].x;
                 const float fb = (bi & 1) ? fsb[bi >> 1].y : fsb[bi >> 1].x;
 #pragma unroll
@@ -226,6 +235,25 @@ __device__ __forceinline__ void stage_mma(float (&acc)[NT][4], uint32_t st, int6
                     acc[n][2] = fmaf(fb, t[2], acc[n][2]);
                     acc[n][3] = fmaf(fb, t[3], acc[n][3]);
                 }
+            }
+        }
+        if constexpr (BIAS) {
+            // the offsets of the stage's 8 blocks: acc += s(row, block) x
+            // (-C(block, token)) summed over the blocks, one tf32 MMA per term
+            // of -C (k = block: this lane's k t and t + 4 are blocks 2t and
+            // 2t + 1, whose scales are one 4-byte load a row)
+            uint32_t s2a, s2b;
+            asm volatile("ld.shared.u32 %0, [%1];" : "=r"(s2a) : "r"(sbase + ra * 16 + 4 * tid));
+            asm volatile("ld.shared.u32 %0, [%1];" : "=r"(s2b) : "r"(sbase + rb * 16 + 4 * tid));
+            const float2 ca = __half22float2(*reinterpret_cast<const __half2 *>(&s2a));
+            const float2 cb = __half22float2(*reinterpret_cast<const __half2 *>(&s2b));
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+                const uint4 c = lds128(cst + n * 512 + lane * 16);
+                ptx::mma_1688_tf32(acc[n], __float_as_uint(ca.x), __float_as_uint(cb.x), __float_as_uint(ca.y),
+                                   __float_as_uint(cb.y), c.x, c.y);
+                ptx::mma_1688_tf32(acc[n], __float_as_uint(ca.x), __float_as_uint(cb.x), __float_as_uint(ca.y),
+                                   __float_as_uint(cb.y), c.z, c.w);
             }
         }
     }

@@ -56,6 +56,8 @@ struct StreamParams {
     int pre_stages;         // weight stages requested before the wait (at most the ring)
     float *ss_part;         // down, with y_sumsq: [feature groups][rows] sums of squares of stored y
     float *y_sumsq;         // down: [rows] sum over the row of the stored y squared, or null
+    const float *bcorr;     // Q4: block offsets of the activation operand (store_q4_corr)
+    float *hcorr;           // Q4 gate/up: block offsets of h, written here
 };
 
 template <int WF, int NT, bool TWO, int ROLE>
@@ -63,17 +65,26 @@ __global__ void __launch_bounds__(kThreads) gemv_stream_kernel(
     const __grid_constant__ CUtensorMap map_w0, const __grid_constant__ CUtensorMap map_w1,
     const __grid_constant__ CUtensorMap map_s0, const __grid_constant__ CUtensorMap map_s1,
     const StreamParams p) {
-    using TL = Tile<WF, ROLE, NT, TWO>;
+    // Q4 operands take the biased form (unpack_word_biased) here
+    constexpr bool BIAS = WF == WF_Q4;
+    using TL = Tile<WF, ROLE, NT, TWO, BIAS>;
     using TO = typename Fmt<WF>::TOp;
     constexpr bool fp8 = TL::fp8;
     constexpr int kStages = TL::stages;
+    // h is stored times hs (the biased Q4 form: low positions 2^-4, high
+    // ones a further 2^-4, so both keep the precision of the plain form's
+    // 2^-8 where it matters and |h| up to 2^20 stays finite)
+    constexpr float hs = BIAS ? 0.0625f : Fmt<WF>::h_scale;
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bar_full[kStages], bar_empty[kStages];
-    __shared__ float red[2][32][NT * 4];
+    __shared__ float s_bias[2][BIAS ? 8 * NT : 1];
     __shared__ int s_abort, s_never, s_last, s_last_row;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t base = (ptx::smem_u32(smem_raw) + 1023u) & ~1023u;
+    const uint32_t cbase = base + kStages * TL::stage_bytes;   // the ring of block offsets (BIAS)
+    // generic address of the ring, for epilogue scratch once every stage is consumed
+    uint8_t *const ring = smem_raw + (base - ptx::smem_u32(smem_raw));
     auto full = [&](int s) { return ptx::smem_u32(&bar_full[s]); };
     auto empty = [&](int s) { return ptx::smem_u32(&bar_empty[s]); };
 
@@ -123,7 +134,8 @@ __global__ void __launch_bounds__(kThreads) gemv_stream_kernel(
                 return static_cast<uint32_t>(left < TL::chunks ? left : TL::chunks);
             };
             auto arm = [&](int s, int j) {
-                ptx::mbar_arrive_expect_tx(full(s), TL::b_off + NT * TL::terms * nvalid(j) * kFragBytes);
+                ptx::mbar_arrive_expect_tx(full(s), TL::b_off + NT * TL::terms * nvalid(j) * kFragBytes +
+                                                        TL::corr_bytes);
             };
             auto load_weights = [&](int s, int j) {
                 const uint32_t st = base + s * TL::stage_bytes, bar = full(s);
@@ -151,6 +163,9 @@ __global__ void __launch_bounds__(kThreads) gemv_stream_kernel(
                     for (int t = 0; t < TL::terms; ++t)
                         ptx::bulk_load(st + TL::b_off + (n * TL::terms + t) * TL::chunks * kFragBytes,
                                        act[n * TL::terms + t] + j * (TL::chunks * 32), nv * kFragBytes, bar);
+                if constexpr (TL::corr_bytes != 0)   // the stage's block offsets: NT x 512 contiguous bytes
+                    ptx::bulk_load(cbase + s * TL::corr_bytes, p.bcorr + (kb0 + j) * (TL::corr_bytes / 4),
+                                   TL::corr_bytes, bar);
             };
             // The first ring's worth of weights is requested before the kernel
             // that writes the activations has finished (weights are inputs of
@@ -207,7 +222,8 @@ __global__ void __launch_bounds__(kThreads) gemv_stream_kernel(
                 ok = false;
                 break;
             }
-            stage_mma<WF, NT, TWO, ROLE>(acc, base + s * TL::stage_bytes, kb, p.nch_b, warp, lane);
+            stage_mma<WF, NT, TWO, ROLE, BIAS>(acc, base + s * TL::stage_bytes, kb, p.nch_b, warp, lane,
+                                               cbase + s * TL::corr_bytes);
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(empty(s));
             if (++s == kStages) {
@@ -224,6 +240,9 @@ __global__ void __launch_bounds__(kThreads) gemv_stream_kernel(
 
         // ------------------------------------------------------- epilogues
         if constexpr (ROLE == ROLE_GATEUP) {
+            // scratch in the ring, once every MMA warp is past its last stage
+            float (*red)[32][NT * 4] = reinterpret_cast<float (*)[32][NT * 4]>(ring);
+            consumer_sync();
             if (warp >= 2) {   // up tiles hand their fragments to the gate warps
 #pragma unroll
                 for (int n = 0; n < NT; ++n)
@@ -242,14 +261,17 @@ __global__ void __launch_bounds__(kThreads) gemv_stream_kernel(
                         rsu[h] = feat < p.rows_w ? p.rs1[feat] : 0.f;
                     }
                 }
+                // (BIAS: this CTA's 32 features are one Q4 block of the down
+                // projection's K, warp 0's its low half, warp 1's its high half)
+                float bsum[NT][2];
 #pragma unroll
                 for (int n = 0; n < NT; ++n)
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         const int64_t feat = row0 + r0 + g + 8 * (i >> 1);
                         const int token = 8 * n + 2 * tid + (i & 1);
-                        const float hv = silu_f32(acc[n][i] * rsg[i >> 1]) *
-                                         (red[warp][lane][n * 4 + i] * rsu[i >> 1]) * Fmt<WF>::h_scale;
+                        float hv = silu_f32(acc[n][i] * rsg[i >> 1]) * (red[warp][lane][n * 4 + i] * rsu[i >> 1]) * hs;
+                        if (BIAS && warp == 1) hv *= 0.0625f;
                         const TO t = from_f32<TO>(hv);
                         const int64_t at = frag_elem(frag_order<WF>(), p.nch_h, token, feat);
                         p.hfrag[at] = *reinterpret_cast<const uint16_t *>(&t);
@@ -257,11 +279,32 @@ __global__ void __launch_bounds__(kThreads) gemv_stream_kernel(
                             const TO tl = from_f32<TO>(hv - to_f32(t));
                             p.hfrag_lo[at] = *reinterpret_cast<const uint16_t *>(&tl);
                         }
+                        if (BIAS) bsum[n][i & 1] = (i < 2 ? 0.f : bsum[n][i & 1]) + to_f32(t);
                     }
+                if constexpr (BIAS) {
+                    // per token, the sum of the stored h over the warp's 16
+                    // features (lanes of one t share the tokens), weighted by
+                    // the half's offset
+#pragma unroll
+                    for (int n = 0; n < NT; ++n)
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            float v = bsum[n][e];
+                            v += __shfl_xor_sync(0xffffffffu, v, 4);
+                            v += __shfl_xor_sync(0xffffffffu, v, 8);
+                            v += __shfl_xor_sync(0xffffffffu, v, 16);
+                            if (g == 0) s_bias[warp][8 * n + 2 * tid + e] = v * (warp ? 1152.f : 1032.f);
+                        }
+                }
+            }
+            if constexpr (BIAS) {
+                consumer_sync();
+                if (threadIdx.x < 8 * NT)
+                    store_q4_corr(p.hcorr, NT, threadIdx.x, blockIdx.x, s_bias[0][threadIdx.x] + s_bias[1][threadIdx.x]);
             }
         } else {
             using T = typename Fmt<WF>::TIn;
-            constexpr float out_scale = Fmt<WF>::w_unscale / Fmt<WF>::h_scale;
+            constexpr float out_scale = Fmt<WF>::w_unscale / hs;
             const int split = blockIdx.y, nsplit = gridDim.y;
 #pragma unroll
             for (int n = 0; n < NT; ++n)
@@ -321,7 +364,7 @@ __global__ void __launch_bounds__(kThreads) gemv_stream_kernel(
                         y[static_cast<int64_t>(token) * p.D + feat] = yv;
                         if (p.y_sumsq) {   // the stored value squared, for the row's sum (ring memory is free now)
                             const float r = to_f32(yv);
-                            reinterpret_cast<float *>(smem_raw + (base - ptx::smem_u32(smem_raw)))[i] = r * r;
+                            reinterpret_cast<float *>(ring)[i] = r * r;
                         }
                     }
                 }
@@ -332,7 +375,7 @@ __global__ void __launch_bounds__(kThreads) gemv_stream_kernel(
                     // the sum of squares of every element of the row, so each
                     // feature group's closing CTA leaves its part of it, and the
                     // last group to finish adds the parts in group order
-                    const float *sq = reinterpret_cast<const float *>(smem_raw + (base - ptx::smem_u32(smem_raw)));
+                    const float *sq = reinterpret_cast<const float *>(ring);
                     consumer_sync();
                     const int64_t nf = p.D - row0 < 64 ? p.D - row0 : 64;
                     if (threadIdx.x < p.rows) {
@@ -390,9 +433,10 @@ __global__ void __launch_bounds__(kThreads) gemv_stream_kernel(
 // FFN_NORM_RELEASE_EARLY, FFN_PRE_STAGES_GATEUP and FFN_PRE_STAGES_DOWN in the
 // environment override them (read once per process, for measurement).
 int decode_tuning(int knob) {
-    static int v[TUNE_COUNT] = {-1, -1, -1};
-    static const char *names[TUNE_COUNT] = {"FFN_NORM_RELEASE_EARLY", "FFN_PRE_STAGES_GATEUP", "FFN_PRE_STAGES_DOWN"};
-    static const int defaults[TUNE_COUNT] = {1, 1, 64};
+    static int v[TUNE_COUNT] = {-1, -1, -1, -1};
+    static const char *names[TUNE_COUNT] = {"FFN_NORM_RELEASE_EARLY", "FFN_PRE_STAGES_GATEUP", "FFN_PRE_STAGES_DOWN",
+                                            "FFN_NORM_SLICES"};
+    static const int defaults[TUNE_COUNT] = {1, 1, 64, 1};
     if (v[knob] < 0) {
         const char *e = getenv(names[knob]);
         v[knob] = e ? atoi(e) : defaults[knob];
@@ -411,8 +455,9 @@ bool stream_supported(int wfmt, int64_t d, int64_t ffn) {
 template <int WF, int NT, bool TWO>
 cudaError_t launch_stream_gateup(GemvWeights wg, GemvWeights wu, const void *nfrag, const void *nfrag_lo,
                                  void *hfrag, void *hfrag_lo, int64_t d, int64_t ffn, int64_t nchK,
-                                 int64_t nchF, unsigned *counters, int ncounters, cudaStream_t s) {
-    using TL = Tile<WF, ROLE_GATEUP, NT, TWO>;
+                                 int64_t nchF, unsigned *counters, int ncounters, const float *ncorr, float *hcorr,
+                                 cudaStream_t s) {
+    using TL = Tile<WF, ROLE_GATEUP, NT, TWO, WF == WF_Q4>;
     constexpr auto kern = gemv_stream_kernel<WF, NT, TWO, ROLE_GATEUP>;
     cudaError_t e = set_smem<kern>(TL::smem_bytes);
     if (e != cudaSuccess) return e;
@@ -437,6 +482,8 @@ cudaError_t launch_stream_gateup(GemvWeights wg, GemvWeights wu, const void *nfr
     p.res = nullptr;
     p.rs0 = wg.rs;
     p.rs1 = wu.rs;
+    p.bcorr = ncorr;
+    p.hcorr = hcorr;
     p.pre_stages = decode_tuning(TUNE_PRE_STAGES_GATEUP);
     // 32 features per CTA; covering nchF * 32 features writes every slot of h
     const int64_t blocks = nchF;
@@ -450,8 +497,8 @@ template <int WF, int NT, bool TWO>
 cudaError_t launch_stream_down(GemvWeights wd, const void *hfrag, const void *hfrag_lo, void *y,
                                float *partials, unsigned *counters, int rows, int64_t d, int64_t ffn,
                                int64_t nchF, int64_t splits, const void *res, float *ss_part, float *y_sumsq,
-                               cudaStream_t s) {
-    using TL = Tile<WF, ROLE_DOWN, NT, TWO>;
+                               const float *hcorr, cudaStream_t s) {
+    using TL = Tile<WF, ROLE_DOWN, NT, TWO, WF == WF_Q4>;
     constexpr auto kern = gemv_stream_kernel<WF, NT, TWO, ROLE_DOWN>;
     cudaError_t e = set_smem<kern>(TL::smem_bytes);
     if (e != cudaSuccess) return e;
@@ -477,6 +524,7 @@ cudaError_t launch_stream_down(GemvWeights wd, const void *hfrag, const void *hf
     p.pre_stages = decode_tuning(TUNE_PRE_STAGES_DOWN);
     p.ss_part = ss_part;
     p.y_sumsq = y_sumsq;
+    p.bcorr = hcorr;
     p.err = device_status_word();
     if (!p.err) return cudaErrorUnknown;
     const int64_t nsplit = cdiv(p.nkb, p.kb_per_split);
@@ -488,10 +536,13 @@ cudaError_t launch_stream_down(GemvWeights wd, const void *hfrag, const void *hf
 
 // Down-projection CTAs that fit in one wave: the CTAs per SM that the
 // format's ring allows (its shared memory plus ~3 KB of static and reserved
-// shared memory, out of 228 KB) times 152 SMs, less a small margin.
+// shared memory, out of 228 KB; Q4: its ring of block offsets, and 1.5 KB,
+// its epilogue scratch living in the ring) times 152 SMs, less a small
+// margin.
 template <int WF>
 constexpr int64_t down_cta_budget() {
-    constexpr size_t per_cta = Tile<WF, ROLE_DOWN, 1, false>::smem_bytes + 3 * 1024;
+    constexpr size_t per_cta = WF == WF_Q4 ? Tile<WF, ROLE_DOWN, 1, false, true>::smem_bytes + 1536
+                                           : Tile<WF, ROLE_DOWN, 1, false>::smem_bytes + 3 * 1024;
     return 152 * static_cast<int64_t>((228 * 1024) / per_cta) - 8;
 }
 
@@ -515,11 +566,11 @@ int64_t stream_down_splits(int wfmt, int64_t d, int64_t ffn) {
     template cudaError_t launch_stream_gateup<WF, NT, TWO>(GemvWeights, GemvWeights, const void *,      \
                                                            const void *, void *, void *, int64_t,       \
                                                            int64_t, int64_t, int64_t, unsigned *, int,   \
-                                                           cudaStream_t);                                \
+                                                           const float *, float *, cudaStream_t);        \
     template cudaError_t launch_stream_down<WF, NT, TWO>(GemvWeights, const void *, const void *, void *, \
                                                          float *, unsigned *, int, int64_t, int64_t,     \
                                                          int64_t, int64_t, const void *, float *, float *, \
-                                                         cudaStream_t);
+                                                         const float *, cudaStream_t);
 FFN_STREAM_INSTANTIATE(WF_F16, 1, false)
 FFN_STREAM_INSTANTIATE(WF_F16, 2, false)
 FFN_STREAM_INSTANTIATE(WF_F16, 1, true)
