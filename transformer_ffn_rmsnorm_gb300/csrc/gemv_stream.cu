@@ -19,6 +19,14 @@
 // W_down over one split of ffn and hands its partial sums to the same
 // deterministic last-CTA reduction as the register kernels.
 //
+// Q4 ("Unfusing a Kernel Made It 1.63x Faster", "The finding that keeps us
+// honest about microbenchmarks": the unpacking must hide under the stream):
+// the nibbles enter the MMAs as the LOP3s leave them (unpack_word_biased),
+// and each stage's per-block offsets, written beside the activations by the
+// kernel that wrote them (store_block_corr), come off through two tf32 MMAs
+// on the block scales; the gate/up epilogue writes h and its offsets in the
+// same form for the down kernel.
+//
 // Both kernels are launched as programmatic dependents of the kernel before
 // them: a CTA starts while that kernel is still running, requests its first
 // ring's worth of weights (inputs of the call) at once, and waits for that
