@@ -76,3 +76,20 @@ def test_q4_flags_rejected(ffn):
         ffn.ffn_block_forward_q4(to_dev(inp["x"], "bf16"), to_dev(inp["g"], "bf16"), q4_dev(inp, "gate"),
                                  q4_dev(inp, "up"), q4_dev(inp, "down"), ffn=cfg.ffn, eps=cfg.eps,
                                  flags=ffn.FFN_ACT_SPLIT)
+
+
+def test_q4_large_activations(ffn, oracle_lib):
+    """Gain x 64 and gate/up block scales x 4 (powers of two, exact): h of
+    order 10^4 (up to ~10^5), so the block offsets of n and of h reach ~10^8.
+    The streaming kernels carry them as two tf32 terms and take them off
+    after the products; the result stays within the bound of the oracle."""
+    inp = synth.make_q4_inputs(synth.C5_DECODE_Q4, seed=71, rows=8, d=1024, ffn=2816)
+    gb = inp["g"].astype(np.int32)            # bf16 bit patterns
+    exp = (gb >> 7) & 0xFF
+    assert np.all((exp > 0) & (exp < 200))    # normal values: x 64 is +6 in the exponent field
+    inp["g"] = (gb + (6 << 7)).astype(np.uint16)
+    for name in ("gate", "up"):
+        inp["s_" + name] = (inp["s_" + name] * np.float16(4)).astype(np.float16)
+        inp["qs_" + name], inp["sc_" + name] = synth.pack_q4(inp["q_" + name], inp["s_" + name])
+    ref = oracle_lib.q4_block_from_inputs(inp)
+    assert_lowp(to_host64(run_q4(ffn, inp)), ref)

@@ -35,6 +35,7 @@
 // Every mbarrier wait is bounded (1 s); a wait that gives up records
 // FFN_ERR_TIMEOUT in the device status word, stops the other roles, and the
 // producer waits (bounded) for its copies in flight before the CTA exits.
+#include <algorithm>
 #include <cstdlib>
 
 #include "gemv_stage.cuh"
@@ -436,19 +437,24 @@ __global__ void __launch_bounds__(kThreads) gemv_stream_kernel(
 //    ring: the wait returns once the norm kernel has completed, and that
 //    completion takes longer while megabytes of loads are in flight (3.1 us
 //    against 4.7 us after the call starts; Q4 call 38.2 against 38.9 us);
-//  - down requests its whole ring before its wait (the gate/up tail it
-//    overlaps has few loads left in flight).
+//  - down requests all of its ring but one stage before its wait (-1 below):
+//    the whole ring competes with the gate/up tail it overlaps for HBM, none
+//    leaves the ring to fill after the wait.  Calls, us (Q4 / bf16 / e4m3 /
+//    Q8_0): whole ring 36.9 / 62.2 / 36.3 / 37.7; ring less one 37.0 / 61.4
+//    / 36.0 / 37.0 (Q4's ring has four stages, the others three); one stage
+//    37.5 / 62.0 / 36.7 / 37.6; none 39.3 / 62.9 / 37.3 / 38.9.
 // FFN_NORM_RELEASE_EARLY, FFN_PRE_STAGES_GATEUP and FFN_PRE_STAGES_DOWN in the
 // environment override them (read once per process, for measurement).
 int decode_tuning(int knob) {
-    static int v[TUNE_COUNT] = {-1, -1, -1, -1};
+    static int v[TUNE_COUNT];
+    static bool read[TUNE_COUNT];
     static const char *names[TUNE_COUNT] = {"FFN_NORM_RELEASE_EARLY", "FFN_PRE_STAGES_GATEUP", "FFN_PRE_STAGES_DOWN",
                                             "FFN_NORM_SLICES"};
-    static const int defaults[TUNE_COUNT] = {1, 1, 64, 1};
-    if (v[knob] < 0) {
+    static const int defaults[TUNE_COUNT] = {1, 1, -1, 1};
+    if (!read[knob]) {
         const char *e = getenv(names[knob]);
-        v[knob] = e ? atoi(e) : defaults[knob];
-        if (v[knob] < 0) v[knob] = 0;
+        v[knob] = e ? std::max(0, atoi(e)) : defaults[knob];
+        read[knob] = true;
     }
     return v[knob];
 }
@@ -529,7 +535,8 @@ cudaError_t launch_stream_down(GemvWeights wd, const void *hfrag, const void *hf
     p.res = res;
     p.rs0 = wd.rs;
     p.rs1 = nullptr;
-    p.pre_stages = decode_tuning(TUNE_PRE_STAGES_DOWN);
+    const int pre = decode_tuning(TUNE_PRE_STAGES_DOWN);
+    p.pre_stages = pre < 0 ? TL::stages - 1 : pre;   // (default: the ring less one stage)
     p.ss_part = ss_part;
     p.y_sumsq = y_sumsq;
     p.bcorr = hcorr;
