@@ -324,3 +324,13 @@ def test_multiwave_gemms(ffn, oracle_lib, flags, rows, d, ffn_):
     sel = np.unique(np.concatenate([np.arange(0, rows, 61), [rows - 1], np.arange(1000, 1040)]))
     assert_lowp(y[sel], oracle_lib.block_from_inputs(inp, rows=sel))
     ffn.ffn_device_status()
+
+
+@pytest.mark.parametrize("rows", [3, 12])
+def test_decode_long_rows(ffn, oracle_lib, rows):
+    """d = 16392 (more than 16384 values a row, not a multiple of 32): the
+    decode norm kernel that reduces each row in every slice CTA; one and two
+    token tiles."""
+    cfg = synth.BlockConfig("t", rows, 16392, 264, 1e-5, "bf16")
+    inp = synth.make_block_inputs(cfg, seed=16392 + rows)
+    assert_lowp(to_host64(run_block(ffn, inp)), oracle_lib.block_from_inputs(inp))

@@ -93,3 +93,12 @@ def test_q4_large_activations(ffn, oracle_lib):
         inp["qs_" + name], inp["sc_" + name] = synth.pack_q4(inp["q_" + name], inp["s_" + name])
     ref = oracle_lib.q4_block_from_inputs(inp)
     assert_lowp(to_host64(run_q4(ffn, inp)), ref)
+
+
+@pytest.mark.parametrize("rows", [3, 12])
+def test_q4_long_rows(ffn, oracle_lib, rows):
+    """d = 16640 (65 stages of 256): the sliced norm kernel writing the
+    offset form of the streaming kernels (slices of whole blocks, offsets
+    reduced over lane quads); one and two token tiles."""
+    inp = synth.make_q4_inputs(synth.C5_DECODE_Q4, seed=90 + rows, rows=rows, d=16640, ffn=512)
+    assert_lowp(to_host64(run_q4(ffn, inp)), oracle_lib.q4_block_from_inputs(inp))
