@@ -181,7 +181,8 @@ class Oracle:
     def q4_dequant(self, qs, scales, out: int, inn: int) -> np.ndarray:
         qs = np.ascontiguousarray(qs, dtype=np.uint8)
         scales = np.ascontiguousarray(scales, dtype=np.uint16)
-        assert qs.size == out * inn // 2 and scales.size == out * (inn // 32)
+        ngrp = -(-inn // 128)   # groups of four blocks a row, the last one padded
+        assert qs.size == out * ngrp * 64 and scales.size == out * ngrp * 4
         w = np.empty((out, inn), dtype=np.float64)
         self.L.oracle_q4_dequant(qs.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8)),
                                  scales.ctypes.data_as(ctypes.POINTER(ctypes.c_uint16)),

@@ -233,17 +233,21 @@ int oracle_ffn_block(const double *x, const double *g, const double *w_gate,
  * offset-binary nibble u_j = q_j + 8; canonical byte i (0..15) holds u_i in
  * its low nibble and u_(i+16) in its high nibble; w_j = (u_j - 8) * s.
  *
- * Device layout: a weight row has in/2 bytes.  Blocks are taken four at a
- * time along the input dimension (a group of 128 weights, 64 bytes); byte
- * 16*t + 4*b + e of a group is canonical byte 4*t + e of block b of that
- * group.  scales[o][blk] holds the fp16 bits of block blk's scale. */
+ * Device layout: blocks are taken four at a time along the input dimension
+ * (a group of 128 weights, 64 bytes); byte 16*t + 4*b + e of a group is
+ * canonical byte 4*t + e of block b of that group.  A weight row holds
+ * ceil(in/128) groups (in/2 bytes when in is a multiple of 128); blocks of
+ * a last, partial group past in/32 are padding and are not read.  Scales
+ * [out][4*ceil(in/128)]: scales[o][blk] holds the fp16 bits of block blk's
+ * scale. */
 void oracle_q4_dequant(const uint8_t *qs, const uint16_t *scales, double *w,
                        int64_t out, int64_t in) {
     int64_t nblk = in / 32;
+    int64_t ngrp = (in + 127) / 128;
     for (int64_t o = 0; o < out; ++o) {
-        const uint8_t *row = qs + o * (in / 2);
+        const uint8_t *row = qs + o * ngrp * 64;
         for (int64_t blk = 0; blk < nblk; ++blk) {
-            double s = oracle_half_to_double(scales[o * nblk + blk]);
+            double s = oracle_half_to_double(scales[o * ngrp * 4 + blk]);
             int64_t group = blk / 4;
             int b = (int)(blk % 4);
             const uint8_t *gp = row + group * 64;

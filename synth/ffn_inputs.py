@@ -232,20 +232,26 @@ def q4_canonical_bytes(q: np.ndarray) -> np.ndarray:
 def pack_q4(q: np.ndarray, scales_f16: np.ndarray):
     """Pack int8 Q4 values and fp16 block scales into the device layout.
 
-    Device layout of ``qs`` (uint8, in/2 bytes per weight row): blocks are
-    grouped four at a time along the input dimension; inside a group of 64
-    bytes, offset 16*t + 4*b + e holds canonical byte 4*t + e of block b of
-    the group (t, b, e in 0..3).  ``scales`` stays [out, in/32] fp16 bits.
-    Requires ``in % 128 == 0``."""
+    Device layout of ``qs`` (uint8): blocks are grouped four at a time along
+    the input dimension; inside a group of 64 bytes, offset 16*t + 4*b + e
+    holds canonical byte 4*t + e of block b of the group (t, b, e in 0..3).
+    A row holds ceil(in/128) groups (in/2 bytes when in % 128 == 0); the
+    blocks of a last, partial group past in/32 are zero bytes.  ``scales``:
+    [out, 4*ceil(in/128)] fp16 bits, zero past in/32.  Requires
+    ``in % 32 == 0``."""
     out, inn = q.shape
-    if inn % 128:
-        raise ValueError("the Q4 device layout needs in % 128 == 0")
-    cb = q4_canonical_bytes(q)                            # [out, nb, 16]
-    g = cb.reshape(out, inn // 128, 4, 4, 4)              # [o, G, b, t, e]
-    qs = np.ascontiguousarray(g.transpose(0, 1, 3, 2, 4)).reshape(out, inn // 2)
-    sc = np.ascontiguousarray(np.asarray(scales_f16, dtype=np.float16)).view(np.uint16)
-    if sc.shape != (out, inn // 32):
+    if inn % 32:
+        raise ValueError("the Q4 device layout needs in % 32 == 0")
+    nb, ngrp = inn // 32, -(-inn // 128)
+    cb = np.zeros((out, 4 * ngrp, 16), dtype=np.uint8)
+    cb[:, :nb] = q4_canonical_bytes(q)                    # [out, 4G, 16]
+    g = cb.reshape(out, ngrp, 4, 4, 4)                    # [o, G, b, t, e]
+    qs = np.ascontiguousarray(g.transpose(0, 1, 3, 2, 4)).reshape(out, 64 * ngrp)
+    sc16 = np.ascontiguousarray(np.asarray(scales_f16, dtype=np.float16)).view(np.uint16)
+    if sc16.shape != (out, nb):
         raise ValueError("scales must be [out, in/32]")
+    sc = np.zeros((out, 4 * ngrp), dtype=np.uint16)
+    sc[:, :nb] = sc16
     return qs, sc
 
 

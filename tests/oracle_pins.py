@@ -281,6 +281,30 @@ def pin_q4_dequant_matches_integers(o):
     assert np.array_equal(w, ref)
 
 
+def pin_q4_dequant_partial_groups(o):
+    """Rows whose length is not a multiple of 128 (one, two and three
+    blocks in the last group): every weight at its own index, the padding
+    of the last group never read (it is filled with 0xFF bytes and NaN
+    scales here, which would show)."""
+    rng = np.random.default_rng(19)
+    for inn in (32, 96, 160, 224):
+        out = 3
+        q = rng.integers(-8, 8, size=(out, inn), dtype=np.int8)
+        s = (np.abs(rng.standard_normal((out, inn // 32))) / 40.0).astype(np.float16)
+        qs, sc = synth.pack_q4(q, s)
+        nb, ngrp = inn // 32, -(-inn // 128)
+        assert qs.shape == (out, 64 * ngrp) and sc.shape == (out, 4 * ngrp)
+        qs = qs.copy()
+        sc = sc.copy()
+        g = qs.reshape(out, ngrp, 4, 4, 4)          # [o, G, t, b, e]
+        for b in range(nb % 4 or 4, 4):
+            g[:, -1, :, b, :] = 0xFF
+        sc[:, nb:] = 0x7E00                         # fp16 NaN
+        w = o.q4_dequant(qs, sc, out, inn)
+        ref = q.astype(np.float64) * np.repeat(s.astype(np.float64), 32, axis=1)
+        assert np.array_equal(w, ref), inn
+
+
 def pin_q4_single_weights(o):
     """One non-zero weight at a time: its value must land at its own index."""
     out, inn = 2, 128
