@@ -222,10 +222,12 @@ ffn_status ffn_block_forward_host(const void *x_host, const void *g, const void 
  *   Canonical block: weight j (0..31) is q_j in [-8, 7] stored offset-binary
  *   u_j = q_j + 8; canonical byte i (0..15) holds u_i in the low nibble and
  *   u_(i+16) in the high nibble; the weight is w_j = (u_j - 8) * s.
- *   Device layout of qs: each weight row holds in/2 bytes; blocks go four at a
- *   time along the input dimension (128 weights, 64 bytes per group); byte
- *   16*t + 4*b + e of a group is canonical byte 4*t + e of block b of the group
- *   (t, b, e in 0..3).  scales: [out][in/32] IEEE fp16 bit patterns.
+ *   Device layout of qs: blocks go four at a time along the input dimension
+ *   (128 weights, 64 bytes per group); byte 16*t + 4*b + e of a group is
+ *   canonical byte 4*t + e of block b of the group (t, b, e in 0..3).  Each
+ *   weight row holds ceil(in/128) groups (in/2 bytes when in % 128 == 0); the
+ *   blocks of a last, partial group past in/32 are padding: zero bytes.
+ *   scales: [out][4*ceil(in/128)] IEEE fp16 bit patterns, zero past in/32.
  *   Both arrays are device pointers (16-byte aligned) owned by the caller.
  * ---------------------------------------------------------------------- */
 typedef struct {
@@ -240,11 +242,17 @@ ffn_status ffn_block_q4_workspace_bytes(int64_t rows, int64_t d, int64_t ffn, si
  * "Megakernels on Mac: What Fusion Saves and What It Costs", section "Threadgroup staging" (stream Q4 weights
  * to registers; staging through shared memory lost).
  *   x [rows x d] bf16, g [d] bf16, y [rows x d] bf16; w_gate/w_up are Q4
- *   [ffn x d], w_down is Q4 [d x ffn].  Needs d % 128 == 0, ffn % 128 == 0,
- *   Rows are processed in groups of up to 16; each group streams the weights
- *   once.  The codes (u - 8) are exact in fp16, so the MMAs run on fp16:
- *   activations enter as one fp16 rounding (h stored times 2^-8).  flags:
- *   FFN_AUTO or FFN_RESIDUAL.
+ *   [ffn x d], w_down is Q4 [d x ffn].  Needs d % 32 == 0, ffn % 32 == 0
+ *   (multiples of 256 stream through the TMA kernels, the rest through the
+ *   register kernels).  Rows are processed in groups of up to 16; each group
+ *   streams the weights once.  The codes (u - 8) are exact in fp16, so the
+ *   MMAs run on fp16: activations enter as one fp16 rounding (h stored times
+ *   2^-8).  On the TMA kernels the nibbles enter the MMAs as 1024 + u (low)
+ *   and 1024 + 16u (high nibble, against activations stored divided by 16),
+ *   each block's offset removed in fp32 (to ~2^-22 of it) after the
+ *   products; h is stored times 2^-4 in the low-nibble positions of a block
+ *   and 2^-8 in the high ones, so |h| must stay below 2^20 there.  flags:
+ *   FFN_AUTO, FFN_RESIDUAL, FFN_DECODE_ONE_KERNEL.
  * ---------------------------------------------------------------------- */
 ffn_status ffn_block_forward_q4(const void *x, const void *g, ffn_q4_weight w_gate,
                                 ffn_q4_weight w_up, ffn_q4_weight w_down, void *y, int64_t rows,
@@ -380,7 +388,7 @@ ffn_status ffn_block_forward_q8(const void *x, const void *g, ffn_q8_weight w_ga
  *   fp8: w = e4m3(codes[o][i]) * scales[o]; in % 16 == 0.  The product times
  *   2^8 is rounded to fp16 once (round to nearest even), i.e. to 11
  *   significant bits of the exact w.
- *   Q4: w = (u - 8) * s in the device layout above; in % 128 == 0.  Exact
+ *   Q4: w = (u - 8) * s in the device layout above; in % 32 == 0.  Exact
  *   before the one rounding to fp16 as well.
  *   dst: out * in device fp16 values, 16-byte aligned, overlapping neither
  *   input (FFN_ERR_ALIAS).  Values whose |w| * 2^8 exceeds fp16's range
@@ -395,7 +403,8 @@ ffn_status ffn_prepare_weights_q8(ffn_q8_weight w, void *dst, int64_t out, int64
 
 /* Host helper (not on the hot path): pack int8 q [out x in] (values -8..7) and
  * fp16 scale bits [out x in/32] into the device layout above.  Host pointers;
- * qs_out holds out*in/2 bytes, scales_out out*in/32 entries.  in % 128 == 0. */
+ * qs_out holds out * 64 * ceil(in/128) bytes, scales_out out * 4 *
+ * ceil(in/128) entries (the padding written as zeros).  in % 32 == 0. */
 ffn_status ffn_q4_pack_host(const int8_t *q, const uint16_t *scales, int64_t out, int64_t in,
                             uint8_t *qs_out, uint16_t *scales_out);
 

@@ -88,7 +88,9 @@ def test_workspace_query(lib):
     assert _ws(lib, 64, 4096, 11008, _lib.FFN_BF16, _lib.FFN_PATH_GEMV)[0] == 0
     out = ctypes.c_size_t(0)
     assert lib.ffn_block_q4_workspace_bytes(8, 5120, 17408, ctypes.byref(out)) == 0 and out.value > 0
-    assert lib.ffn_block_q4_workspace_bytes(8, 5000, 17408, ctypes.byref(out)) == _lib.FFN_ERR_SHAPE
+    assert lib.ffn_block_q4_workspace_bytes(8, 5000, 17408, ctypes.byref(out)) == _lib.FFN_ERR_SHAPE   # in % 32
+    assert lib.ffn_block_q4_workspace_bytes(8, 5024, 17408, ctypes.byref(out)) == 0            # whole blocks
+    assert lib.ffn_block_q4_workspace_bytes(8, 5120, 17400, ctypes.byref(out)) == _lib.FFN_ERR_SHAPE
 
 
 def test_block_forward_rejects_before_launch(lib):
@@ -108,12 +110,16 @@ def test_block_forward_rejects_before_launch(lib):
                                     None) == _lib.FFN_ERR_FLAGS
 
 
-def test_q4_pack_host_matches_layout(lib):
+@pytest.mark.parametrize("d,ffn_", [(256, 384), (96, 160), (416, 224)])
+def test_q4_pack_host_matches_layout(lib, d, ffn_):
+    """The library's packer writes the bytes of the documented layout, the
+    padding of a last, partial group included (zero bytes, zero scales)."""
     from transformer_ffn_rmsnorm_gb300 import ffn
-    inp = synth.make_q4_inputs(synth.C5_DECODE_Q4, seed=4, rows=1, d=256, ffn=384)
-    qs, sc = ffn.ffn_q4_pack_host(inp["q_gate"], inp["s_gate"].view(np.uint16))
-    assert np.array_equal(qs, inp["qs_gate"])
-    assert np.array_equal(sc, inp["sc_gate"])
+    inp = synth.make_q4_inputs(synth.C5_DECODE_Q4, seed=4, rows=1, d=d, ffn=ffn_)
+    for name in ("gate", "down"):
+        qs, sc = ffn.ffn_q4_pack_host(inp["q_" + name], inp["s_" + name].view(np.uint16))
+        assert np.array_equal(qs, inp["qs_" + name])
+        assert np.array_equal(sc, inp["sc_" + name])
     bad = inp["q_gate"].copy()
     bad[0, 0] = 8
     with pytest.raises(Exception):
@@ -213,7 +219,7 @@ def test_quantised_prepare_rejects_before_launch(lib):
     f = _lib.Fp8Weight(p[0].value, p[1].value)
     q = _lib.Q4Weight(p[0].value, p[1].value)
     assert lib.ffn_prepare_weights_fp8(f, p[2], 4, 24, None) == _lib.FFN_ERR_SHAPE       # in % 16
-    assert lib.ffn_prepare_weights_q4(q, p[2], 4, 64, None) == _lib.FFN_ERR_SHAPE        # in % 128
+    assert lib.ffn_prepare_weights_q4(q, p[2], 4, 48, None) == _lib.FFN_ERR_SHAPE        # in % 32
     assert lib.ffn_prepare_weights_fp8(_lib.Fp8Weight(p[0].value, None), p[2], 4, 32, None) == _lib.FFN_ERR_NULL
     assert lib.ffn_prepare_weights_fp8(f, ctypes.c_void_p(p[2].value + 8), 4, 32, None) == _lib.FFN_ERR_ALIGN
     assert lib.ffn_prepare_weights_fp8(f, ctypes.c_void_p(p[0].value + 64), 4, 32, None) == _lib.FFN_ERR_ALIAS

@@ -37,12 +37,16 @@ def test_prepare_fp8_bit_exact(ffn, oracle_lib):
     ffn.ffn_device_status()
 
 
-def test_prepare_q4_bit_exact(ffn, oracle_lib):
-    inp = synth.make_q4_inputs(synth.C5_DECODE_Q4, seed=4, rows=2, d=1024, ffn=640)
+@pytest.mark.parametrize("d,ffn_", [(1024, 640), (96, 160), (416, 224)])
+def test_prepare_q4_bit_exact(ffn, oracle_lib, d, ffn_):
+    """Whole 128-weight groups and rows ending in a partial group (1 and 3
+    blocks): every weight written once, nothing past the row."""
+    inp = synth.make_q4_inputs(synth.C5_DECODE_Q4, seed=4, rows=2, d=d, ffn=ffn_)
     qs, sc = q4_dev(inp, "gate")
-    got = ffn.ffn_prepare_weights_q4((qs, sc), 1024)
-    w = oracle_lib.q4_dequant(inp["qs_gate"], inp["sc_gate"], 640, 1024)
+    got = ffn.ffn_prepare_weights_q4((qs, sc), d)
+    w = oracle_lib.q4_dequant(inp["qs_gate"], inp["sc_gate"], ffn_, d)
     import torch
+    assert got.shape == (ffn_, d)
     assert np.array_equal(got.view(torch.int16).cpu().numpy().view(np.uint16), f16_bits(w * 256.0))
     ffn.ffn_device_status()
 

@@ -102,3 +102,18 @@ def test_q4_long_rows(ffn, oracle_lib, rows):
     reduced over lane quads); one and two token tiles."""
     inp = synth.make_q4_inputs(synth.C5_DECODE_Q4, seed=90 + rows, rows=rows, d=16640, ffn=512)
     assert_lowp(to_host64(run_q4(ffn, inp)), oracle_lib.q4_block_from_inputs(inp))
+
+
+@pytest.mark.parametrize("rows,d,ffn_,residual", [(1, 96, 160, False), (5, 416, 224, True), (12, 32, 96, False),
+                                                  (16, 1056, 2080, True)])
+def test_q4_partial_groups(ffn, oracle_lib, rows, d, ffn_, residual):
+    """d and ffn multiples of 32 but not of 128: rows ending in a padded
+    group of 1-3 blocks (the register kernels), one and two token tiles,
+    with and without the skip connection."""
+    inp = synth.make_q4_inputs(synth.C5_DECODE_Q4, seed=rows + d, rows=rows, d=d, ffn=ffn_)
+    cfg = inp["cfg"]
+    y = ffn.ffn_block_forward_q4(to_dev(inp["x"], "bf16"), to_dev(inp["g"], "bf16"), q4_dev(inp, "gate"),
+                                 q4_dev(inp, "up"), q4_dev(inp, "down"), ffn=cfg.ffn, eps=cfg.eps,
+                                 flags=ffn.FFN_RESIDUAL if residual else 0)
+    assert_lowp(to_host64(y), oracle_lib.q4_block_from_inputs(inp, residual=residual))
+    ffn.ffn_device_status()

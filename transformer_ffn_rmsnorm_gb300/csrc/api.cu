@@ -65,6 +65,9 @@ bool valid_dtype(ffn_dtype dt) { return dt == FFN_F32 || dt == FFN_F16 || dt == 
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// 64-byte groups of four Q4 blocks in a device-layout row of `in` weights
+int64_t q4_groups(int64_t in) { return (in + 127) / 128; }
+
 struct Range {
     const void *p;
     size_t bytes;
@@ -408,7 +411,7 @@ ffn_status ffn_block_forward_chained(const void *x, const float *x_sumsq, const 
 
 ffn_status ffn_block_q4_workspace_bytes(int64_t rows, int64_t d, int64_t ffn, size_t *bytes) {
     if (!bytes) return FFN_ERR_NULL;
-    if (rows < 0 || d < 128 || ffn < 128 || d % 128 || ffn % 128) return FFN_ERR_SHAPE;
+    if (rows < 0 || d < 32 || ffn < 32 || d % 32 || ffn % 32) return FFN_ERR_SHAPE;
     if (rows > INT32_MAX || d > INT32_MAX || ffn > INT32_MAX) return FFN_ERR_SHAPE;
     *bytes = rows == 0 ? 0 : gemv_workspace_bytes(std::min<int64_t>(rows, kQuantGroupRows), d, ffn, false);
     return FFN_OK;
@@ -432,11 +435,13 @@ ffn_status ffn_block_forward_q4(const void *x, const void *g, ffn_q4_weight w_ga
     for (const void *p : ptrs)
         if (!aligned16(p)) return FFN_ERR_ALIGN;
     if (workspace && !aligned16(workspace)) return FFN_ERR_ALIGN;
-    const size_t qb = static_cast<size_t>(ffn) * d / 2, sb = static_cast<size_t>(ffn) * (d / 32) * 2;
+    // device-layout bytes: rows of ceil(in/128) 64-byte groups, 4 scales a group
+    const size_t qb = static_cast<size_t>(ffn) * q4_groups(d) * 64, sb = static_cast<size_t>(ffn) * q4_groups(d) * 8;
+    const size_t qbd = static_cast<size_t>(d) * q4_groups(ffn) * 64, sbd = static_cast<size_t>(d) * q4_groups(ffn) * 8;
     const Range ry{y, static_cast<size_t>(rows) * d * 2}, rws{workspace, need};
     const Range ins[] = {{x, static_cast<size_t>(rows) * d * 2}, {g, static_cast<size_t>(d) * 2},
                          {w_gate.qs, qb}, {w_gate.scales, sb}, {w_up.qs, qb}, {w_up.scales, sb},
-                         {w_down.qs, qb}, {w_down.scales, sb}};
+                         {w_down.qs, qbd}, {w_down.scales, sbd}};
     for (const Range &in : ins)
         if (overlaps(ry, in) || overlaps(rws, in)) return FFN_ERR_ALIAS;
     if (overlaps(ry, rws)) return FFN_ERR_ALIAS;
@@ -572,13 +577,16 @@ ffn_status ffn_block_forward_q8(const void *x, const void *g, ffn_q8_weight w_ga
 ffn_status ffn_q4_pack_host(const int8_t *q, const uint16_t *scales, int64_t out, int64_t in,
                             uint8_t *qs_out, uint16_t *scales_out) {
     if (!q || !scales || !qs_out || !scales_out) return FFN_ERR_NULL;
-    if (out < 0 || in < 0 || in % 128) return FFN_ERR_SHAPE;
-    const int64_t nblk = in / 32;
+    if (out < 0 || in < 0 || in % 32) return FFN_ERR_SHAPE;
+    const int64_t nblk = in / 32, ngrp = q4_groups(in);
     for (int64_t o = 0; o < out; ++o) {
         const int8_t *qr = q + o * in;
         for (int64_t i = 0; i < in; ++i)
             if (qr[i] < -8 || qr[i] > 7) return FFN_ERR_SHAPE;
-        uint8_t *dst = qs_out + o * (in / 2);
+        uint8_t *dst = qs_out + o * ngrp * 64;
+        // a last, partial group's padding: zero bytes, zero scales
+        std::memset(dst, 0, static_cast<size_t>(ngrp) * 64);
+        std::memset(scales_out + o * ngrp * 4, 0, static_cast<size_t>(ngrp) * 8);
         for (int64_t blk = 0; blk < nblk; ++blk) {
             const int64_t grp = blk / 4;
             const int b = static_cast<int>(blk % 4);
@@ -589,7 +597,7 @@ ffn_status ffn_q4_pack_host(const int8_t *q, const uint16_t *scales, int64_t out
                 dst[grp * 64 + 16 * t + 4 * b + e] = static_cast<uint8_t>(lo | (hi << 4));
             }
         }
-        std::memcpy(scales_out + o * nblk, scales + o * nblk, static_cast<size_t>(nblk) * 2);
+        std::memcpy(scales_out + o * ngrp * 4, scales + o * nblk, static_cast<size_t>(nblk) * 2);
     }
     return FFN_OK;
 }
@@ -636,13 +644,13 @@ ffn_status ffn_prepare_weights_fp8(ffn_fp8_weight w, void *dst, int64_t out, int
 }
 
 ffn_status ffn_prepare_weights_q4(ffn_q4_weight w, void *dst, int64_t out, int64_t in, void *stream) {
-    if (out < 0 || in < 0 || in % 128) return FFN_ERR_SHAPE;
+    if (out < 0 || in < 0 || in % 32) return FFN_ERR_SHAPE;
     if (out == 0 || in == 0) return FFN_OK;
     if (!w.qs || !w.scales || !dst) return FFN_ERR_NULL;
     if (!aligned16(w.qs) || !aligned16(w.scales) || !aligned16(dst)) return FFN_ERR_ALIGN;
-    const size_t n = static_cast<size_t>(out) * in;
+    const size_t n = static_cast<size_t>(out) * in, grp = static_cast<size_t>(out) * q4_groups(in);
     const Range rd{dst, 2 * n};
-    if (overlaps(rd, {w.qs, n / 2}) || overlaps(rd, {w.scales, n / 16})) return FFN_ERR_ALIAS;
+    if (overlaps(rd, {w.qs, grp * 64}) || overlaps(rd, {w.scales, grp * 8})) return FFN_ERR_ALIAS;
     return from_cuda(launch_prepare_q4(w.qs, w.scales, dst, out, in, static_cast<cudaStream_t>(stream)));
 }
 

@@ -188,7 +188,9 @@ __global__ void __launch_bounds__(256) gemv_norm_frag_kernel(const void *x_, con
 // ---------------------------------------------------------------------------
 // Accumulate RT row tiles (16 weight rows each) x NT token tiles over a
 // range of K for one warp.  For f16/bf16, [c0, c1) are 32-wide chunks; for
-// Q4, [c0, c1) are 128-wide groups (four blocks).
+// Q4, [c0, c1) are 128-wide groups (four blocks; a row holds ceil(K / 128),
+// the padding of a last, partial group being zero bytes and zero scales that
+// meet zero activations).
 // With TWO, the activation operand is given as two fragments (value and
 // rounding residual) and every weight fragment is multiplied by both.
 template <int WF, int RT, int NT, int U, bool TWO>
@@ -245,8 +247,8 @@ __device__ __forceinline__ void warp_accumulate(const void *const (&w)[RT],
                     }
         }
     } else {
-        const int64_t qrow = K / 2;    // bytes per weight row
-        const int64_t srow = K / 32;   // scales per weight row
+        const int64_t qrow = cdiv(K, 128) * 64;   // bytes per weight row
+        const int64_t srow = cdiv(K, 128) * 4;    // scales per weight row
         for (int64_t gi = c0; gi < c1; gi += U) {
             uint4 q[U][RT][2];
             uint2 s[U][RT][2];
@@ -406,7 +408,7 @@ __global__ void __launch_bounds__(128) gemv_down_kernel(
     const int gq = lane >> 2, tid = lane & 3;
     const int64_t f0 = (static_cast<int64_t>(blockIdx.x) * kDnTPC + warp) * 16;
     const int split = blockIdx.y, nsplit = gridDim.y;
-    const int64_t nunits = q4 ? (F / 128) : nchF;
+    const int64_t nunits = q4 ? cdiv(F, 128) : nchF;
     const int64_t c0 = split * units_per_split;
     const int64_t c1 = (c0 + units_per_split < nunits) ? c0 + units_per_split : nunits;
 
@@ -498,10 +500,12 @@ struct Geometry {
 Geometry geometry(int64_t rows, int64_t d, int64_t ffn, bool q4) {
     Geometry g;
     g.nt = rows <= 8 ? 1 : rows <= 16 ? 2 : rows <= 32 ? 4 : 8;   // token tiles of 8 (16-bit weights: up to 8)
-    g.nchK = cdiv(d, kChunk);
-    g.nchF = cdiv(ffn, kChunk);
+    // (Q4 rows hold whole 128-wide groups: the chunk counts round up to them,
+    // the chunks past K being zeros)
+    g.nchK = q4 ? 4 * cdiv(d, 128) : cdiv(d, kChunk);
+    g.nchF = q4 ? 4 * cdiv(ffn, 128) : cdiv(ffn, kChunk);
     g.ups = q4 ? kSplitK / 128 : kSplitK / kChunk;
-    const int64_t units = q4 ? ffn / 128 : g.nchF;
+    const int64_t units = q4 ? cdiv(ffn, 128) : g.nchF;
     g.splits = cdiv(units, g.ups);
     g.groups = cdiv(d, kDnFeat);
     return g;
@@ -577,7 +581,7 @@ cudaError_t launch_typed(const void *x, const void *gain, GemvWeights wg, GemvWe
         {
             const int64_t tiles = 2 * geo.nchF;  // covers every fragment slot of h
             const int64_t blocks = cdiv(tiles, kGuTPC);
-            const int64_t units = q4 ? d / 128 : geo.nchK;
+            const int64_t units = q4 ? cdiv(d, 128) : geo.nchK;
             LaunchScope scope(K_GEMV_GATEUP, s);
             gemv_gateup_kernel<WF, NT, TWO><<<static_cast<unsigned>(blocks), 32 * kGuTPC * kGuKS, 0, s>>>(
                 q4 ? static_cast<const void *>(wg.qs) : wg.w, q4 ? static_cast<const void *>(wu.qs) : wu.w,
@@ -622,7 +626,7 @@ Layout layout(int64_t rows, int64_t d, int64_t ffn) {
     // sized for the Q4 or 16-bit geometry and for the register or streaming
     // down kernel, whichever needs most split-K partials
     const Geometry a = geometry(rows, d, ffn, false);
-    const Geometry b = geometry(rows, d, ffn, (d % 128 == 0) && (ffn % 128 == 0));
+    const Geometry b = geometry(rows, d, ffn, (d % 32 == 0) && (ffn % 32 == 0));
     int64_t splits = a.splits > b.splits ? a.splits : b.splits;
     for (int wf : {WF_BF16, WF_Q4, WF_FP8, WF_Q8})
         if (stream_supported(wf, d, ffn)) splits = std::max(splits, stream_down_splits(wf, d, ffn));
@@ -633,8 +637,9 @@ Layout layout(int64_t rows, int64_t d, int64_t ffn) {
         if (stream_supported(wf, d, ffn))
             for (bool two : {false, true}) floats = std::max(floats, fused_partial_floats(wf, r, d, ffn, a.nt, two));
     Layout l;
-    l.frag_n = align256(static_cast<size_t>(a.nt) * a.nchK * 32 * 16);
-    l.frag_h = align256(static_cast<size_t>(a.nt) * a.nchF * 32 * 16);
+    // (Q4 fragments cover whole 128-wide groups)
+    l.frag_n = align256(static_cast<size_t>(a.nt) * std::max(a.nchK, b.nchK) * 32 * 16);
+    l.frag_h = align256(static_cast<size_t>(a.nt) * std::max(a.nchF, b.nchF) * 32 * 16);
     l.partials = align256(static_cast<size_t>(floats) * 4);
     l.counters = align256(static_cast<size_t>(a.groups + 1) * 4);   // arrivals per group, then for the row sums
     l.ss_part = align256(static_cast<size_t>(a.groups) * (rows > 64 ? 64 : rows) * 4);

@@ -77,11 +77,12 @@ __global__ void __launch_bounds__(256) prepare_fp8_kernel(const uint8_t *__restr
 // each output is one rounding.  One thread per 64-byte group of four blocks
 // (128 weights); byte 16 t + 4 b + e of the group is canonical byte 4 t + e of
 // block b, whose low nibble is weight 4 t + e of the block and whose high
-// nibble is weight 4 t + e + 16.
+// nibble is weight 4 t + e + 16.  A row holds ceil(cols / 128) groups; the
+// blocks of a last, partial group past cols are padding and write nothing.
 __global__ void __launch_bounds__(256) prepare_q4_kernel(const uint8_t *__restrict__ qs,
                                                          const uint16_t *__restrict__ sc, __half *__restrict__ dst,
                                                          int64_t rows, int64_t cols, unsigned *status) {
-    const int64_t per_row = cols / 128, ngroups = rows * per_row;
+    const int64_t per_row = (cols + 127) / 128, ngroups = rows * per_row;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     bool bad = false;
     for (int64_t gi = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; gi < ngroups; gi += stride) {
@@ -92,9 +93,11 @@ __global__ void __launch_bounds__(256) prepare_q4_kernel(const uint8_t *__restri
         const uint2 sraw = *reinterpret_cast<const uint2 *>(sc + 4 * gi);
         const uint16_t sbits[4] = {static_cast<uint16_t>(sraw.x), static_cast<uint16_t>(sraw.x >> 16),
                                    static_cast<uint16_t>(sraw.y), static_cast<uint16_t>(sraw.y >> 16)};
-        __half *out = dst + 128 * gi;
+        const int64_t col0 = 128 * (gi % per_row);
+        __half *out = dst + (gi / per_row) * cols + col0;
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
+            if (col0 + 32 * b >= cols) break;
             const float s = __half2float(__ushort_as_half(sbits[b])) * kPreparedScale;
             uint32_t w[16];
 #pragma unroll
@@ -172,7 +175,7 @@ cudaError_t launch_prepare_q4(const uint8_t *qs, const uint16_t *scales, void *d
     unsigned *status = device_status_word();
     if (!status) return cudaErrorUnknown;
     LaunchScope scope(K_PREPARE, s);
-    prepare_q4_kernel<<<static_cast<unsigned>(prepare_grid(rows * (cols / 128))), 256, 0, s>>>(
+    prepare_q4_kernel<<<static_cast<unsigned>(prepare_grid(rows * ((cols + 127) / 128))), 256, 0, s>>>(
         qs, scales, static_cast<__half *>(dst), rows, cols, status);
     return cudaGetLastError();
 }

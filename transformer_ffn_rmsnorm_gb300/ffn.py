@@ -296,12 +296,15 @@ def ffn_prepare_weights_q8(w, out: torch.Tensor | None = None, stream=None) -> t
 
 
 def ffn_q4_pack_host(q: np.ndarray, scales_bits: np.ndarray):
-    """Host packer: int8 q [out, in] in [-8, 7] and fp16 scale bits [out, in/32]."""
+    """Host packer: int8 q [out, in] in [-8, 7] and fp16 scale bits [out, in/32]
+    into the device layout (rows of ceil(in/128) 64-byte groups, 4 scales a
+    group)."""
     q = np.ascontiguousarray(q, dtype=np.int8)
     s = np.ascontiguousarray(scales_bits).view(np.uint16)
     out, inn = q.shape
-    qs = np.empty((out, inn // 2), dtype=np.uint8)
-    so = np.empty((out, inn // 32), dtype=np.uint16)
+    ngrp = -(-inn // 128)
+    qs = np.empty((out, 64 * ngrp), dtype=np.uint8)
+    so = np.empty((out, 4 * ngrp), dtype=np.uint16)
     _check(_lib.load().ffn_q4_pack_host(q.ctypes.data, s.ctypes.data, out, inn, qs.ctypes.data,
                                         so.ctypes.data), "ffn_q4_pack_host")
     return qs, so
