@@ -28,6 +28,9 @@ MUTANTS = [
     ("q4_nibbles_swapped", "(j < 16) ? (byte & 0x0F) : (byte >> 4)", "(j < 16) ? (byte >> 4) : (byte & 0x0F)"),
     ("q4_offset_7", "(double)(u - 8) * s", "(double)(u - 7) * s"),
     ("q4_group_not_interleaved", "gp[16 * t + 4 * b + e]", "gp[16 * b + 4 * t + e]"),
+    ("q4_row_pitch_unpadded", "const uint8_t *row = qs + o * ngrp * 64;", "const uint8_t *row = qs + o * (in / 2);"),
+    ("q4_scale_pitch_unpadded", "scales[o * ngrp * 4 + blk]", "scales[o * nblk + blk]"),
+    ("q4_groups_rounded_down", "int64_t ngrp = (in + 127) / 128;", "int64_t ngrp = in / 128;"),
     ("half_bias", "e - 25", "e - 24"),
     ("half_subnormal_scale", "ldexp((double)f, -24)", "ldexp((double)f, -25)"),
     ("e4m3_bias", "ldexp((double)(8 + f), e - 10)", "ldexp((double)(8 + f), e - 11)"),
